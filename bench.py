@@ -1,0 +1,412 @@
+#!/usr/bin/env python
+"""Benchmark of the verify-round MoE layer on one GB300 (or N independent replicas).
+
+Metric: µs per MoE decode layer and HBM GB/s (fraction of peak) vs verify rows
+1/4/16.  A step is one round over the 40-layer 35B-A3B-shaped stack
+(H 2048, 128 experts, top-8, intermediate 768, int4 blocks of 32 + fp16 scales);
+the headline row count is 1, the 4- and 16-row rounds (1 + 3 MTP drafts; 16
+near-duplicate lookup-copy rows) run on the same weights and are reported under
+"rows".  `value` is achieved HBM GB/s on algorithmic bytes (unique routed-expert
+bytes + router + activations in/out), whole job; `us_per_layer` is the same time.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With --impl reference the CPU oracle is timed instead (the reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "µs per MoE decode layer and HBM GB/s (fraction of peak) vs verify rows 1/4/16"
+UNIT = "GB/s"
+L2_NOTE = ("no L2 flush: a 1-row round streams ~0.9 GB of distinct layer weights, "
+           "far above the 129 MB L2, so each layer's experts are evicted before reuse")
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--layers", type=int, default=0, help="override the stack depth (0 = 40)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peak_hbm():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def layer_bytes(cfg, U, rows):
+    return U * cfg.expert_bytes + cfg.router_bytes + rows * cfg.hidden * (2 + 4)
+
+
+def workload_config(cfg, rows, L):
+    return {"workload": f"{cfg.name}: MoE decode layer H{cfg.hidden} E{cfg.experts} top-{cfg.top_k} "
+                        f"I{cfg.inter}, int4 blocks of 32 + fp16 scales, {rows} row(s), {L}-layer round",
+            "hidden": cfg.hidden, "experts": cfg.experts, "top_k": cfg.top_k, "inter": cfg.inter,
+            "rows": rows, "layers": L, "row_sigma": cfg.row_sigma, "seed": cfg.seed, "l2": L2_NOTE}
+
+
+# ---- clocks during the timed region ---------------------------------------------------
+
+REASON_BITS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+               0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x100: "display_clock_setting"}
+
+
+class ClockSampler:
+    def __init__(self, index: int):
+        self.index = index
+        self.samples = []  # (t, sm_mhz, max_mhz, reasons_mask)
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        cmd = ["nvidia-smi", "-i", str(self.index),
+               "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+               "--format=csv,noheader,nounits", "-lms", "100"]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            try:
+                sm, mx, rs = [v.strip() for v in line.split(",")]
+                self.samples.append((time.time(), float(sm), float(mx), int(rs, 16)))
+            except Exception:
+                pass
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        win = [s for s in self.samples if t0 <= s[0] <= t1]
+        if not win and self.samples:
+            mid = (t0 + t1) / 2
+            win = [min(self.samples, key=lambda s: abs(s[0] - mid))]
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        mask = 0
+        for s in win:
+            mask |= s[3]
+        reasons = [n for b, n in REASON_BITS.items() if mask & b and n != "gpu_idle"]
+        return {"sm_mhz": statistics.median(s[1] for s in win), "sm_max_mhz": max(s[2] for s in win),
+                "reasons": reasons, "samples": len(win)}
+
+
+# ---- CPU baseline / reference arm: the oracle --------------------------------------------
+
+def oracle_sample(cfg, layers, budget_s, rows=None, sigma=None, warm=0):
+    """Times oracle.route + oracle.layer (single-threaded) over `layers` in turn until the
+    budget is spent; input generation is outside the timed region."""
+    import oracle
+    import syngen
+    t_total, bytes_total, n = 0.0, 0, 0
+    per_layer = []
+    i = 0
+    while True:
+        l = layers[i % len(layers)]
+        router = syngen.router(cfg, l)
+        xb = syngen.rows(cfg, l, rows, sigma)
+        rt0 = oracle.route(router, xb, cfg.top_k)
+        ew = syngen.experts_stacked(cfg, l, rt0.union)
+        t0 = time.perf_counter()
+        rt = oracle.route(router, xb, cfg.top_k)
+        oracle.layer(router, xb, cfg.top_k, rt.union, ew)
+        dt = time.perf_counter() - t0
+        if i >= warm:
+            t_total += dt
+            bytes_total += layer_bytes(cfg, rt.union.size, xb.shape[0])
+            per_layer.append(dt)
+            n += 1
+        i += 1
+        if (t_total >= budget_s and n >= 1) or (budget_s <= 0 and n >= len(layers)):
+            break
+    return t_total, bytes_total, n
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import syngen
+    cfg = syngen.CONFIGS["a3b_r1"]
+    L = args.layers or cfg.layers
+    import oracle
+    times, byts = [], 0
+    for step in range(args.warmup + args.steps):
+        l = step % L
+        router = syngen.router(cfg, l)
+        xb = syngen.rows(cfg, l)
+        rt0 = oracle.route(router, xb, cfg.top_k)
+        ew = syngen.experts_stacked(cfg, l, rt0.union)
+        t0 = time.perf_counter()
+        rt = oracle.route(router, xb, cfg.top_k)
+        oracle.layer(router, xb, cfg.top_k, rt.union, ew)
+        dt = time.perf_counter() - t0
+        if step >= args.warmup:
+            times.append(dt)
+            byts += layer_bytes(cfg, rt.union.size, 1)
+    t = sum(times)
+    gbs = byts / t / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded counter-based generator)",
+            "config": workload_config(cfg, 1, L),
+            "us_per_layer": 1e6 * t / len(times),
+            "cpu_baseline": {"value": gbs, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"{len(times)} single-row layers of the 40-layer stack "
+                                       f"(one layer per step), oracle route + layer only"},
+            "e2e": {"value": gbs, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---- our arm ---------------------------------------------------------------------------------
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import spec_verify_layer_gb300 as mv  # fails loudly when the library is missing
+    import syngen
+    from spec_verify_layer_gb300.weights import Packer, workspace
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    cfg = syngen.CONFIGS["a3b_r1"]
+    L = args.layers or cfg.layers
+    H = cfg.hidden
+    max_rows = 16
+    dims = mv.make_dims(H, cfg.experts, cfg.top_k, cfg.inter, max_rows)
+    packer = Packer(dims)
+    layers = []
+    for l in range(L):
+        packer.pack_all(lambda e, l=l: syngen.expert(cfg, l, e))
+        layers.append(packer.upload(syngen.router(cfg, l), dev))
+    wl = [ly.w for ly in layers]
+    handle = mv.moe_create(dims, local)
+    ws = workspace(dims, max_rows, dev)
+    stream = torch.cuda.Stream(dev)
+    st = stream.cuda_stream
+
+    def buffers(rows, sigma):
+        xs = np.stack([syngen.rows(cfg, l, rows, sigma) for l in range(L)])
+        x = torch.from_numpy(xs.view(np.int16)).to(dev)
+        out = torch.empty((L, rows, H), dtype=torch.float32, device=dev)
+        stats = torch.zeros(L, dtype=torch.int32, device=dev)
+        return xs, x, out, stats
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def max_over_ranks(v):
+        if world == 1:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def time_rounds(rows, sigma, steps, warmup, sampler=None):
+        xs, x, out, stats = buffers(rows, sigma)
+        with torch.cuda.stream(stream):
+            for _ in range(warmup):
+                mv.moe_round(handle, wl, x.data_ptr(), rows, out.data_ptr(), stats.data_ptr(),
+                             ws.data_ptr(), ws.numel(), True, st)
+        launches_per_round = mv.moe_last_launch_count(handle)
+        torch.cuda.synchronize(dev)
+        barrier()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t_wall0 = time.time()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(steps):
+                mv.moe_round(handle, wl, x.data_ptr(), rows, out.data_ptr(), stats.data_ptr(),
+                             ws.data_ptr(), ws.numel(), True, st)
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        t_wall1 = time.time()
+        barrier()
+        ms = max_over_ranks(e0.elapsed_time(e1))
+        assert mv.moe_last_device_status(handle, st) == mv.MOE_OK
+        U = stats.cpu().numpy()
+        per_round_bytes = sum(layer_bytes(cfg, int(u), rows) for u in U)
+        return {"ms_total": ms, "steps": steps, "U": U, "bytes_per_round": per_round_bytes,
+                "launches_per_round": launches_per_round, "t_wall": (t_wall0, t_wall1),
+                "x": x, "out": out, "xs": xs}
+
+    peak, peak_src = peak_hbm()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    head = time_rounds(1, 0.0, args.steps, max(args.warmup, 3))
+    sampler.stop()
+    clocks = sampler.summary(*head["t_wall"])
+
+    ms_round = head["ms_total"] / head["steps"]
+    us_layer = 1e3 * ms_round / L
+    value = world * head["bytes_per_round"] / (ms_round * 1e-3) / 1e9   # whole job
+
+    # rows sweep on the same weights
+    sweep = {}
+    for rows, sigma, name in ((4, 0.5, "a3b_r4"), (16, 0.1, "a3b_r16")):
+        r = time_rounds(rows, sigma, max(20, args.steps // 4), max(args.warmup, 3))
+        msr = r["ms_total"] / r["steps"]
+        gbs = r["bytes_per_round"] / (msr * 1e-3) / 1e9
+        sweep[f"r{rows}"] = {"workload": name, "us_per_layer": 1e3 * msr / L, "us_per_round": 1e3 * msr,
+                             "hbm_gbs": gbs, "frac_of_peak": gbs / peak,
+                             "unique_experts_per_layer": float(np.mean(r["U"])),
+                             "picks_per_layer": rows * cfg.top_k,
+                             "tokens_per_round_equiv_per_s": rows / (msr * 1e-3)}
+
+    # per-kernel device time (eager launches, CUDA events on the launching stream)
+    prof_rounds = max(5, min(50, args.steps // 10))
+    xs1, x1, out1, stats1 = head["xs"], head["x"], head["out"], torch.zeros(L, dtype=torch.int32, device=dev)
+    mv.moe_profile(handle, True)
+    with torch.cuda.stream(stream):
+        for _ in range(prof_rounds):
+            mv.moe_round(handle, wl, x1.data_ptr(), 1, out1.data_ptr(), stats1.data_ptr(), ws.data_ptr(),
+                         ws.numel(), False, st)
+    kinds = {}
+    for kind, name in ((mv.KIND_ROUTE, "k_route"), (mv.KIND_EXPERT, "k_expert"), (mv.KIND_REDUCE, "k_reduce")):
+        tot, n = mv.moe_profile_read(handle, kind)
+        kinds[name] = {"launches": n, "total_ms": tot, "avg_us": 1e3 * tot / max(n, 1)}
+    mv.moe_profile(handle, False)
+    tot_all = sum(k["total_ms"] for k in kinds.values())
+    for k in kinds.values():
+        k["share"] = k["total_ms"] / tot_all if tot_all else None
+    dom = max(kinds, key=lambda n: kinds[n]["total_ms"])
+    U1 = head["U"]
+    if dom == "k_expert":
+        alg_per_launch = float(np.mean([int(u) * cfg.expert_bytes for u in U1]))
+    elif dom == "k_route":
+        alg_per_launch = float(cfg.router_bytes + H * 2)
+    else:  # reduction: the row's fp32 output
+        alg_per_launch = float(H * 4)
+    achieved = alg_per_launch / (kinds[dom]["avg_us"] * 1e-6) / 1e9
+    traffic = read_traffic(dom)
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src,
+                "alg_bytes_per_launch": alg_per_launch, "avg_launch_us": kinds[dom]["avg_us"],
+                "kernels": kinds, "timing": f"eager profiled pass, {prof_rounds} rounds, CUDA events on the launch stream"}
+
+    # end to end through the C ABI with host buffers (pinned), copies inside the timed region
+    xh = torch.from_numpy(head["xs"].view(np.int16)).pin_memory()
+    oh = torch.empty((L, 1, H), dtype=torch.float32).pin_memory()
+    e2e_steps = max(10, min(args.steps, 500))
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            x1.copy_(xh, non_blocking=True)
+            mv.moe_round(handle, wl, x1.data_ptr(), 1, out1.data_ptr(), stats1.data_ptr(), ws.data_ptr(),
+                         ws.numel(), True, st)
+            oh.copy_(out1, non_blocking=True)
+            stream.synchronize()
+    barrier()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for _ in range(e2e_steps):
+            x1.copy_(xh, non_blocking=True)
+            mv.moe_round(handle, wl, x1.data_ptr(), 1, out1.data_ptr(), stats1.data_ptr(), ws.data_ptr(),
+                         ws.numel(), True, st)
+            oh.copy_(out1, non_blocking=True)
+            stream.synchronize()
+    t_e2e = max_over_ranks(time.perf_counter() - t0) / e2e_steps
+    e2e = {"value": world * head["bytes_per_round"] / t_e2e / 1e9, "unit": UNIT,
+           "h2d_bytes_per_step": int(xh.numel() * 2), "d2h_bytes_per_step": int(oh.numel() * 4),
+           "us_per_layer": 1e6 * t_e2e / L, "steps": e2e_steps}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        t, b, n = oracle_sample(cfg, list(range(L)), budget_s=10.0)
+        cpu = {"value": b / t / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "us_per_layer": 1e6 * t / n,
+               "sample": f"{n} single-row layers of the same stack, oracle route + layer only, "
+                         f"one host core, ~10 s of CPU work"}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": max(args.warmup, 3), "ms_per_step": ms_round, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+                "data": "synthetic (seeded counter-based generator; random int4 weights, bf16 rows)",
+                "config": workload_config(cfg, 1, L),
+                "us_per_layer": us_layer, "us_per_round": 1e3 * ms_round,
+                "hbm_gbs_per_gpu": value / world, "frac_of_peak": value / world / peak,
+                "tokens_per_round_equiv_per_s": 1.0 / (ms_round * 1e-3),
+                "unique_experts_per_layer": float(np.mean(U1)),
+                "rows": {"r1": {"us_per_layer": us_layer, "hbm_gbs": value / world,
+                                "frac_of_peak": value / world / peak,
+                                "unique_experts_per_layer": float(np.mean(U1))}, **sweep},
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+                "gpu_launches": int(head["launches_per_round"] * args.steps)}
+        print(json.dumps(line), flush=True)
+    mv.moe_destroy(handle)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def read_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current kernel source (its recorded source digest matches); else None."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    src = os.path.join(ROOT, "spec_verify_layer_gb300", "csrc", "moe_verify.cu")
+    try:
+        kv = dict(l.split(":", 1) for l in open(path) if ":" in l and not l.startswith("#"))
+        kv = {k.strip(): v.strip() for k, v in kv.items()}
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        if kv.get("kernel") == kernel and kv.get("source_sha256_16") == digest:
+            return float(kv["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

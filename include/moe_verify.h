@@ -1,0 +1,168 @@
+/*
+ * moe_verify.h -- C ABI of the MoE layer of a speculative-decoding verify round,
+ * on one NVIDIA GB300 (sm_103a).
+ *
+ * The layer (sources: "How AlphaInfer makes local decoding fast", sections 2 and 3.1:
+ * a decode round over 1..16 token rows replayed as one captured graph with
+ * per-request data as ingress buffers, where every extra verified row can route to
+ * experts the other rows did not need and so adds weight bytes; "infero", the
+ * decoder-block diagram and Design notes: a SwiGLU expert FFN silu(W_g x) * (W_u x)
+ * -> W_d, weights consumed in 32-element block encoding, block scales folded in in
+ * float; a dedicated top-k routing kernel at decode):
+ *
+ *   1. logits[r][e] = Wr[e] . x[r]                  fp32, fixed summation order (*)
+ *   2. per row: the k largest logits, ordered by (logit desc, id asc);
+ *      w_j = exp(l_j - l_1) / sum_i exp(l_i - l_1)   (softmax renormalised over the k)
+ *   3. U = ascending distinct ids over all rows (each routed expert's weights are
+ *      streamed once per call, however many rows picked it)
+ *   4. per (row, routed expert): h = silu(Wg x) * (Wu x), silu(t) = t / (1 + e^-t)
+ *   5. out[r] = sum_j w_j * (Wd h_{r,j})            (j in rank order)
+ * Expert weights are int4 codes q in [-8, 7] with one fp16 scale per 32 codes;
+ * weight = scale * q.  Activations in are bf16; everything after is fp32.
+ *
+ * (*) The router summation order is part of the definition so that the top-k
+ * decision is reproducible bit for bit: 32 lane partials, lane l takes elements
+ * 128c + 4l + j (c ascending, j = 0..3), each with one correctly rounded fma; the
+ * partials are combined by p_l <- p_l + p_{l^o} for o = 16, 8, 4, 2, 1; logit = p_0.
+ *
+ * Conventions for every call below:
+ *   - Device pointers are caller-owned device memory, 16-byte aligned (256 recommended).
+ *     The library never frees caller memory.  Host pointers are plain host memory.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Compute calls are
+ *     asynchronous on that stream and return only argument/launch status; errors a
+ *     kernel finds (a bounded wait that gave up) are read with moe_last_device_status.
+ *   - Return codes: MOE_OK, or a negative MOE_E* code; moe_strerror names it.
+ *   - Rows are independent: a row's outputs do not depend on which other rows share
+ *     the call or on its position among them (bitwise).
+ *   - Activations must be finite with |x| < 2^40 (and so must the SwiGLU output h);
+ *     beyond that range results are undefined.
+ */
+#ifndef MOE_VERIFY_H
+#define MOE_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  MOE_OK = 0,
+  MOE_EINVAL = -1,       /* bad dimensions, NULL or misaligned pointer, rows out of range */
+  MOE_ECUDA = -2,        /* a CUDA runtime call failed (no device, launch failure, ...) */
+  MOE_EWORKSPACE = -3,   /* workspace smaller than moe_workspace_bytes() */
+  MOE_ETIMEOUT = -4,     /* a device-side bounded wait gave up (moe_last_device_status) */
+  MOE_EUNSUPPORTED = -5  /* valid dimensions this build does not handle (see moe_create) */
+};
+
+/* which matrix set a packing call refers to */
+enum { MOE_GATEUP = 0, MOE_DOWN = 1 };
+
+/* Layer dimensions.  hidden H, n_experts E, top_k k, inter I (expert intermediate),
+ * max_rows = the largest row count any call on this handle will pass. */
+typedef struct moe_dims {
+  int32_t hidden, n_experts, top_k, inter, max_rows;
+} moe_dims;
+
+/* One layer's weights, all DEVICE pointers in the packed layout of moe_pack_q4:
+ *   router        fp32 [E][H] row-major
+ *   gateup_nib    E * moe_packed_bytes(MOE_GATEUP, 0) bytes
+ *   gateup_scale  E * moe_packed_bytes(MOE_GATEUP, 1) bytes of fp16 bits
+ *   down_nib      E * moe_packed_bytes(MOE_DOWN, 0) bytes
+ *   down_scale    E * moe_packed_bytes(MOE_DOWN, 1) bytes of fp16 bits          */
+typedef struct moe_layer_w {
+  const float* router;
+  const uint8_t* gateup_nib;
+  const uint16_t* gateup_scale;
+  const uint8_t* down_nib;
+  const uint16_t* down_scale;
+} moe_layer_w;
+
+typedef struct moe_handle moe_handle;
+
+/* Validates dims and binds a handle to `device` (queries its SM count, allocates a
+ * 4-byte device status word -- the only device allocation the library makes).
+ * Supported: hidden a multiple of 256 in [256, 2048], inter a multiple of 32 in
+ * [32, 4096], 1 <= top_k <= min(n_experts, 32), n_experts <= 1024, 1 <= max_rows <= 32.
+ * MOE_EINVAL for dims that make no sense, MOE_EUNSUPPORTED for sizes outside those
+ * ranges, MOE_ECUDA if the device cannot be used.  *out is NULL on failure. */
+int moe_create(const moe_dims* dims, int device, moe_handle** out);
+void moe_destroy(moe_handle* h);
+
+/* Device workspace (bytes) a call with `rows` rows needs: routing tables and the
+ * fp32 split-K partials of the expert stage.  0 for invalid dims/rows. */
+size_t moe_workspace_bytes(const moe_dims* dims, int32_t rows);
+
+/* Packed size of ONE expert: part 0 = code bytes, part 1 = scale bytes.  0 if invalid. */
+size_t moe_packed_bytes(const moe_dims* dims, int which, int part);
+
+/* Host-side packer (HOST buffers).  Packs n_experts consecutive experts:
+ *   MOE_GATEUP: q_a = gate codes [n][I][H], s_a = gate scales [n][I][H/32],
+ *               q_b = up codes [n][I][H],   s_b = up scales [n][I][H/32]
+ *   MOE_DOWN:   q_a = down codes [n][H][I], s_a = down scales [n][H][I/32]; q_b, s_b unused
+ * into nib_out / scale_out (n * moe_packed_bytes(which, 0 / 1) bytes).  Codes outside
+ * [-8, 7] give MOE_EINVAL.  Layout (GB300 kernel order, 32-element blocks, code q
+ * stored as the nibble q + 8, element 2t in the low nibble of byte t of its block):
+ *   gate/up codes  [E][I/32 slices][2: gate, up][32 rows][H/32 blocks][16 B]
+ *   gate/up scales [E][I/32][2][32][H/32]
+ *   down codes     [E][I/32 blocks][H rows][16 B]
+ *   down scales    [E][I/32][H]                                                  */
+int moe_pack_q4(const moe_dims* dims, int which, int32_t n_experts, const int8_t* q_a,
+                const uint16_t* s_a, const int8_t* q_b, const uint16_t* s_b, uint8_t* nib_out,
+                uint16_t* scale_out);
+
+/* Steps 1-3 only (router GEMV, top-k + renormalised weights, union).
+ * x_bf16 [rows][H] device; topk_ids [rows][k] int32 (rank order), topk_w [rows][k]
+ * fp32, union_ids [E] int32 (first *n_union valid, ascending), n_union: device int32.
+ * Any of the four outputs may be NULL.  ws: device workspace of ws_bytes. */
+int moe_route(moe_handle* h, const moe_layer_w* w, const uint16_t* x_bf16, int32_t rows,
+              int32_t* topk_ids, float* topk_w, int32_t* union_ids, int32_t* n_union, void* ws,
+              size_t ws_bytes, void* stream);
+
+/* Steps 1-5 for one layer.  x_bf16 [rows][H] device, out [rows][H] fp32 device. */
+int moe_decode_layer(moe_handle* h, const moe_layer_w* w, const uint16_t* x_bf16, int32_t rows,
+                     float* out, void* ws, size_t ws_bytes, void* stream);
+
+/* A round over an L-layer stack, layer after layer in stream order (layer l+1's
+ * routing starts only after layer l's output is complete).  layers: HOST array [L] of
+ * device weight sets; x_bf16 [L][rows][H] device (layer l reads its own rows);
+ * out [L][rows][H] fp32 device; stats: device int32 [L] receiving |U| per layer, or
+ * NULL.  use_graph != 0 captures the round once per (handle, argument set) into a
+ * CUDA graph and replays it on later calls with the same arguments; the buffers
+ * are ingress: write new rows into the same x buffer and call again.  use_graph
+ * needs a non-default stream. */
+int moe_round(moe_handle* h, const moe_layer_w* layers, int32_t L, const uint16_t* x_bf16,
+              int32_t rows, float* out, int32_t* stats, void* ws, size_t ws_bytes, int use_graph,
+              void* stream);
+
+/* Synchronizes `stream`, reads and clears the handle's device status word.
+ * MOE_OK, MOE_ETIMEOUT (a bounded device wait gave up), or MOE_ECUDA. */
+int moe_last_device_status(moe_handle* h, void* stream);
+
+/* Number of kernel launches the most recent moe_route / moe_decode_layer /
+ * moe_round call enqueued (a graph replay counts the kernels inside it). */
+int32_t moe_last_launch_count(const moe_handle* h);
+
+/* Bound on every device-side wait of this handle's kernels (default 2 s; 0 restores
+ * the default).  A tiny bound makes the waits give up at once: the kernels then set
+ * the timeout bit, drain their copies in flight under the default bound, and return,
+ * so tests can exercise the MOE_ETIMEOUT path without any hang. */
+int moe_set_wait_limit_ns(moe_handle* h, uint64_t ns);
+
+/* Per-kernel timing of eager (non-graph) calls.  moe_profile(h, 1) starts recording a
+ * CUDA event pair around every kernel the handle launches on the caller's stream
+ * (and discards earlier records); moe_profile(h, 0) stops.  moe_profile_read
+ * synchronizes the recorded events and returns, for one kernel kind (0 = router and
+ * top-k, 1 = expert stage, 2 = reduction), the summed device time in ms and the
+ * number of launches.  Graph replays are not recorded. */
+int moe_profile(moe_handle* h, int enable);
+int moe_profile_read(moe_handle* h, int kind, double* total_ms, int32_t* launches);
+
+const char* moe_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_VERIFY_H */

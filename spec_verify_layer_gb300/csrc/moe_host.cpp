@@ -1,0 +1,127 @@
+// Host-side parts of the verify-round MoE library that need no GPU: dimension
+// checks, workspace and packed sizes, the int4 block packer, error strings.
+#include <cstring>
+
+#include "moe_internal.h"
+
+namespace moe {
+
+int check_dims(const moe_dims* d) {
+  if (!d) return MOE_EINVAL;
+  if (d->hidden <= 0 || d->n_experts <= 0 || d->top_k <= 0 || d->inter <= 0 || d->max_rows <= 0)
+    return MOE_EINVAL;
+  if (d->top_k > d->n_experts) return MOE_EINVAL;
+  if (d->hidden % 128 || d->inter % 32) return MOE_EINVAL;  // block and router-order structure
+  if (d->hidden % 256 || d->hidden < kMinHidden || d->hidden > kMaxHidden) return MOE_EUNSUPPORTED;
+  if (d->inter > kMaxInter || d->n_experts > kMaxExperts || d->top_k > kMaxTopK ||
+      d->max_rows > kMaxRows)
+    return MOE_EUNSUPPORTED;
+  return MOE_OK;
+}
+
+static size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+WsLayout ws_layout(const moe_dims& d, int rows) {
+  WsLayout L{};
+  size_t R = (size_t)rows, E = (size_t)d.n_experts, k = (size_t)d.top_k;
+  size_t off = 0;
+  L.ctrl = off;     off += 256;
+  L.logits = off;   off += up256(R * E * 4);
+  L.ids = off;      off += up256(R * k * 4);
+  L.w = off;        off += up256(R * k * 4);
+  L.uni = off;      off += up256(E * 4);
+  L.csr_off = off;  off += up256((E + 1) * 4);
+  L.csr_pair = off; off += up256(R * k * 4);
+  L.partial = off;  off += up256(R * k * (size_t)(d.inter / kSlice) * (size_t)d.hidden * 4);
+  L.total = off;
+  return L;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+size_t moe_workspace_bytes(const moe_dims* dims, int32_t rows) {
+  if (check_dims(dims) != MOE_OK || rows < 1 || rows > dims->max_rows) return 0;
+  return ws_layout(*dims, rows).total;
+}
+
+size_t moe_packed_bytes(const moe_dims* dims, int which, int part) {
+  if (check_dims(dims) != MOE_OK || (part != 0 && part != 1)) return 0;
+  if (which == MOE_GATEUP) return part == 0 ? gu_nib_bytes(*dims) : gu_sc_bytes(*dims);
+  if (which == MOE_DOWN) return part == 0 ? dn_nib_bytes(*dims) : dn_sc_bytes(*dims);
+  return 0;
+}
+
+// One 32-element block of codes -> 16 bytes: element 2t in the low nibble of byte t,
+// element 2t+1 in the high nibble, each stored as q + 8.
+static bool pack_block(const int8_t* q, uint8_t* dst) {
+  for (int t = 0; t < 16; ++t) {
+    int lo = q[2 * t], hi = q[2 * t + 1];
+    if (lo < -8 || lo > 7 || hi < -8 || hi > 7) return false;
+    dst[t] = (uint8_t)((lo + 8) | ((hi + 8) << 4));
+  }
+  return true;
+}
+
+int moe_pack_q4(const moe_dims* dims, int which, int32_t n_experts, const int8_t* q_a,
+                const uint16_t* s_a, const int8_t* q_b, const uint16_t* s_b, uint8_t* nib_out,
+                uint16_t* scale_out) {
+  int rc = check_dims(dims);
+  if (rc != MOE_OK) return rc;
+  if (n_experts < 1 || !q_a || !s_a || !nib_out || !scale_out) return MOE_EINVAL;
+  const size_t H = (size_t)dims->hidden, I = (size_t)dims->inter;
+  const size_t NB = H / 32, NS = I / kSlice;
+  if (which == MOE_GATEUP) {
+    if (!q_b || !s_b) return MOE_EINVAL;
+    for (size_t e = 0; e < (size_t)n_experts; ++e) {
+      uint8_t* nib = nib_out + e * gu_nib_bytes(*dims);
+      uint16_t* sc = scale_out + e * (gu_sc_bytes(*dims) / 2);
+      for (size_t s = 0; s < NS; ++s)
+        for (size_t m = 0; m < 2; ++m) {
+          const int8_t* q = (m == 0 ? q_a : q_b) + e * I * H;
+          const uint16_t* sv = (m == 0 ? s_a : s_b) + e * I * NB;
+          for (size_t ii = 0; ii < (size_t)kSlice; ++ii) {
+            size_t i = s * kSlice + ii;
+            size_t base = ((s * 2 + m) * kSlice + ii) * NB;
+            for (size_t b = 0; b < NB; ++b) {
+              if (!pack_block(q + i * H + b * 32, nib + (base + b) * 16)) return MOE_EINVAL;
+              sc[base + b] = sv[i * NB + b];
+            }
+          }
+        }
+    }
+    return MOE_OK;
+  }
+  if (which == MOE_DOWN) {
+    for (size_t e = 0; e < (size_t)n_experts; ++e) {
+      uint8_t* nib = nib_out + e * dn_nib_bytes(*dims);
+      uint16_t* sc = scale_out + e * (dn_sc_bytes(*dims) / 2);
+      const int8_t* q = q_a + e * H * I;
+      const uint16_t* sv = s_a + e * H * NS;
+      for (size_t s = 0; s < NS; ++s)
+        for (size_t o = 0; o < H; ++o) {
+          if (!pack_block(q + o * I + s * 32, nib + (s * H + o) * 16)) return MOE_EINVAL;
+          sc[s * H + o] = sv[o * NS + s];
+        }
+    }
+    return MOE_OK;
+  }
+  return MOE_EINVAL;
+}
+
+const char* moe_strerror(int code) {
+  switch (code) {
+    case MOE_OK: return "ok";
+    case MOE_EINVAL: return "invalid argument (dimensions, NULL or misaligned pointer, rows)";
+    case MOE_ECUDA: return "CUDA runtime error";
+    case MOE_EWORKSPACE: return "workspace smaller than moe_workspace_bytes()";
+    case MOE_ETIMEOUT: return "a bounded device-side wait gave up";
+    case MOE_EUNSUPPORTED: return "dimensions outside what this build supports";
+    default: return "unknown error code";
+  }
+}
+
+}  // extern "C"

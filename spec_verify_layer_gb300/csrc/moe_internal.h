@@ -1,0 +1,34 @@
+// Internal declarations shared by the host code and the CUDA launchers of the
+// verify-round MoE library.  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/moe_verify.h"
+
+namespace moe {
+
+constexpr int kSlice = 32;     // intermediate rows per expert work item (one down K-block)
+constexpr int kMaxRows = 32;   // rows are tracked in 32-bit masks
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxTopK = 32;
+constexpr int kMinHidden = 256, kMaxHidden = 2048;
+constexpr int kMaxInter = 4096;
+
+// 0 = valid and supported, MOE_EINVAL, or MOE_EUNSUPPORTED.
+int check_dims(const moe_dims* d);
+
+// Byte offsets of the workspace regions for `rows` rows (each region 256-aligned).
+struct WsLayout {
+  size_t ctrl, logits, ids, w, uni, csr_off, csr_pair, partial, total;
+};
+WsLayout ws_layout(const moe_dims& d, int rows);
+
+// Per-expert packed sizes (bytes).
+inline size_t gu_nib_bytes(const moe_dims& d) { return (size_t)d.inter * d.hidden; }
+inline size_t gu_sc_bytes(const moe_dims& d) { return (size_t)d.inter * d.hidden / 8; }
+inline size_t dn_nib_bytes(const moe_dims& d) { return (size_t)d.inter * d.hidden / 2; }
+inline size_t dn_sc_bytes(const moe_dims& d) { return (size_t)d.inter * d.hidden / 16; }
+
+}  // namespace moe

@@ -12,6 +12,12 @@ def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA device (GB300) and the built library")
 
 
+def pytest_sessionstart(session):
+    # compile the library, generator and oracle if a source is newer than its .so
+    import __graft_entry__
+    __graft_entry__.build()
+
+
 def pytest_collection_modifyitems(config, items):
     # GPU tests need a device; on a CPU-only host they are skipped, never faked.
     try:
