@@ -155,38 +155,44 @@ def oracle_sample(cfg, layers, budget_s, rows=None, sigma=None, warm=0):
 
 
 def run_reference(args):
+    """The reference arm: the CPU oracle as it stands, on one host core.
+
+    A step is a bounded sample of the 1-row round: one layer's routing (router GEMV,
+    top-k, weights, union) plus the SwiGLU FFN of one of its routed experts, layers and
+    ranks cycling; GB/s counts the bytes that sample touches (router + one expert +
+    row in/out).  Input generation is outside the timed region."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
+    import oracle
     import syngen
     cfg = syngen.CONFIGS["a3b_r1"]
     L = args.layers or cfg.layers
-    import oracle
     times, byts = [], 0
     for step in range(args.warmup + args.steps):
-        l = step % L
+        l = (step // cfg.top_k) % L
+        j = step % cfg.top_k
         router = syngen.router(cfg, l)
         xb = syngen.rows(cfg, l)
         rt0 = oracle.route(router, xb, cfg.top_k)
-        ew = syngen.experts_stacked(cfg, l, rt0.union)
+        ew = syngen.experts_stacked(cfg, l, [int(rt0.ids[0, j])], threads=1)
         t0 = time.perf_counter()
         rt = oracle.route(router, xb, cfg.top_k)
-        oracle.layer(router, xb, cfg.top_k, rt.union, ew)
+        oracle.expert_ffn(xb[0], ew, 0)
         dt = time.perf_counter() - t0
         if step >= args.warmup:
             times.append(dt)
-            byts += layer_bytes(cfg, rt.union.size, 1)
+            byts += cfg.expert_bytes + cfg.router_bytes + cfg.hidden * 6
     t = sum(times)
     gbs = byts / t / 1e9
+    sample = (f"{len(times)} steps; each = routing of one 1-row layer + the FFN of one of its "
+              f"routed experts (layers 0..{L - 1} cycling), oracle only, one host core")
     line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / len(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded counter-based generator)",
             "config": workload_config(cfg, 1, L),
-            "us_per_layer": 1e6 * t / len(times),
-            "cpu_baseline": {"value": gbs, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": f"{len(times)} single-row layers of the 40-layer stack "
-                                       f"(one layer per step), oracle route + layer only"},
+            "cpu_baseline": {"value": gbs, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": gbs, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0

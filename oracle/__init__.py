@@ -57,6 +57,8 @@ def lib():
         L.oracle_layer.restype = i32
         L.oracle_layer_dense.argtypes = [i32] * 5 + [vp] * 9
         L.oracle_layer_dense.restype = i32
+        L.oracle_expert_ffn.argtypes = [i32, i32] + [vp] * 8
+        L.oracle_expert_ffn.restype = i32
         L.oracle_unique_expert_bytes.argtypes = [i32, i32, i32]
         L.oracle_unique_expert_bytes.restype = ctypes.c_int64
         _lib = L
@@ -143,6 +145,18 @@ def layer_dense(router, x_bf16, k: int, ew) -> np.ndarray:
     if rc != 0:
         raise ValueError(f"oracle_layer_dense rejected the dimensions (rc={rc})")
     return out
+
+
+def expert_ffn(x_row_bf16: np.ndarray, ew, p: int = 0) -> np.ndarray:
+    """y[H] (fp64) of one expert (index p of the stacked weights ``ew``) for one row."""
+    x = np.ascontiguousarray(x_row_bf16, np.uint16)
+    I, H = ew.qg.shape[1], ew.qg.shape[2]
+    y = np.empty(H, np.float64)
+    sl = [np.ascontiguousarray(getattr(ew, f)[p]) for f in ("qg", "sg", "qu", "su", "qd", "sd")]
+    rc = lib().oracle_expert_ffn(H, I, _p(x), *(_p(a) for a in sl), _p(y))
+    if rc != 0:
+        raise ValueError(f"oracle_expert_ffn rejected the dimensions (rc={rc})")
+    return y
 
 
 def unique_expert_bytes(H: int, I: int, n_union: int) -> int:

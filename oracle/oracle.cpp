@@ -295,6 +295,18 @@ int oracle_layer_dense(int H, int E, int k, int I, int R, const float* router,
   return 0;
 }
 
+// a4 + a5 for one (row, expert) pair: y[H] = Wd (silu(Wg x) * (Wu x)) in fp64, with
+// x the row's bf16 activations; qg/qu [I][H], sg/su [I][H/32], qd [H][I], sd [H][I/32].
+int oracle_expert_ffn(int H, int I, const uint16_t* x_bf16, const int8_t* qg, const uint16_t* sg,
+                      const int8_t* qu, const uint16_t* su, const int8_t* qd, const uint16_t* sd,
+                      double* y) {
+  if (H <= 0 || H % 32 || I <= 0 || I % 32) return -1;
+  std::vector<float> x(H);
+  for (int h = 0; h < H; ++h) x[h] = bf16_bits_to_float(x_bf16[h]);
+  expert_ffn(H, I, x.data(), qg, sg, qu, su, qd, sd, y);
+  return 0;
+}
+
 // Unique expert bytes of a round: |U| experts, each 3 matrices of H*I int4 codes
 // stored as 16 B of codes + 2 B fp16 scale per 32 codes.
 int64_t oracle_unique_expert_bytes(int H, int I, int n_union) {

@@ -182,6 +182,16 @@ def test_single_expert_is_plain_swiglu_mlp():
     np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
 
 
+def test_expert_ffn_matches_single_expert_layer():
+    rng = np.random.default_rng(21)
+    H, I = 128, 64
+    ew = _rand_experts(rng, 1, H, I)
+    router = np.zeros((1, H), np.float32)
+    xb = np.array([[bf16(float(v)) for v in rng.standard_normal(H)]], np.uint16)
+    y = oracle.expert_ffn(xb[0], ew, 0)
+    np.testing.assert_array_equal(y, oracle.layer(router, xb, 1, [0], ew)[0])
+
+
 def test_k_equals_e_is_full_softmax():
     rng = np.random.default_rng(12)
     E, H = 8, 512
