@@ -304,36 +304,29 @@ def run_ours(args):
                              "picks_per_layer": rows * cfg.top_k,
                              "tokens_per_round_equiv_per_s": rows / (msr * 1e-3)}
 
-    # per-kernel device time (eager launches, CUDA events on the launching stream)
-    prof_rounds = max(5, min(50, args.steps // 10))
-    xs1, x1, out1, stats1 = head["xs"], head["x"], head["out"], torch.zeros(L, dtype=torch.int32, device=dev)
+    # The round is one kernel launch (k_round): its average launch duration is the timed
+    # region's per-step time, from CUDA events on the launching stream.  A separate
+    # eager pass records where the time goes inside it (device timestamps per phase).
+    alg_per_launch = float(head["bytes_per_round"])
+    avg_launch_us = 1e3 * ms_round
+    achieved = alg_per_launch / (avg_launch_us * 1e-6) / 1e9
+    prof_rounds = max(3, min(20, args.steps // 50))
+    x1, out1 = head["x"], head["out"]
+    stats1 = torch.zeros(L, dtype=torch.int32, device=dev)
     mv.moe_profile(handle, True)
     with torch.cuda.stream(stream):
         for _ in range(prof_rounds):
             mv.moe_round(handle, wl, x1.data_ptr(), 1, out1.data_ptr(), stats1.data_ptr(), ws.data_ptr(),
                          ws.numel(), False, st)
-    kinds = {}
-    for kind, name in ((mv.KIND_ROUTE, "k_route"), (mv.KIND_EXPERT, "k_expert"), (mv.KIND_REDUCE, "k_reduce")):
-        tot, n = mv.moe_profile_read(handle, kind)
-        kinds[name] = {"launches": n, "total_ms": tot, "avg_us": 1e3 * tot / max(n, 1)}
+    eager_ms, eager_n = mv.moe_profile_read(handle, mv.KIND_ROUND)
+    phases = {k: {"mean_us": v[0], "max_us": v[1]} for k, v in mv.moe_profile_phases(handle).items()}
     mv.moe_profile(handle, False)
-    tot_all = sum(k["total_ms"] for k in kinds.values())
-    for k in kinds.values():
-        k["share"] = k["total_ms"] / tot_all if tot_all else None
-    dom = max(kinds, key=lambda n: kinds[n]["total_ms"])
-    U1 = head["U"]
-    if dom == "k_expert":
-        alg_per_launch = float(np.mean([int(u) * cfg.expert_bytes for u in U1]))
-    elif dom == "k_route":
-        alg_per_launch = float(cfg.router_bytes + H * 2)
-    else:  # reduction: the row's fp32 output
-        alg_per_launch = float(H * 4)
-    achieved = alg_per_launch / (kinds[dom]["avg_us"] * 1e-6) / 1e9
-    traffic = read_traffic(dom)
-    roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src,
-                "alg_bytes_per_launch": alg_per_launch, "avg_launch_us": kinds[dom]["avg_us"],
-                "kernels": kinds, "timing": f"eager profiled pass, {prof_rounds} rounds, CUDA events on the launch stream"}
+    roofline = {"bound": "hbm", "kernel": "k_round", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": read_traffic("k_round", L), "peak_source": peak_src,
+                "alg_bytes_per_launch": alg_per_launch, "avg_launch_us": avg_launch_us,
+                "launch": f"one cooperative launch per {L}-layer round, timed over {args.steps} graph replays",
+                "phases_per_layer_us": phases,
+                "eager_round_us": 1e3 * eager_ms / max(eager_n, 1)}
 
     # end to end through the C ABI with host buffers (pinned), copies inside the timed region
     xh = torch.from_numpy(head["xs"].view(np.int16)).pin_memory()
@@ -377,10 +370,10 @@ def run_ours(args):
                 "us_per_layer": us_layer, "us_per_round": 1e3 * ms_round,
                 "hbm_gbs_per_gpu": value / world, "frac_of_peak": value / world / peak,
                 "tokens_per_round_equiv_per_s": 1.0 / (ms_round * 1e-3),
-                "unique_experts_per_layer": float(np.mean(U1)),
+                "unique_experts_per_layer": float(np.mean(head["U"])),
                 "rows": {"r1": {"us_per_layer": us_layer, "hbm_gbs": value / world,
                                 "frac_of_peak": value / world / peak,
-                                "unique_experts_per_layer": float(np.mean(U1))}, **sweep},
+                                "unique_experts_per_layer": float(np.mean(head["U"]))}, **sweep},
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
                 "gpu_launches": int(head["launches_per_round"] * args.steps)}
         print(json.dumps(line), flush=True)
@@ -390,9 +383,10 @@ def run_ours(args):
     return 0
 
 
-def read_traffic(kernel):
+def read_traffic(kernel, layers):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on the
-    current kernel source (its recorded source digest matches); else None."""
+    current kernel source (its recorded source digest matches); scaled from the
+    captured layer count to `layers` (traffic grows in proportion).  Else None."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     src = os.path.join(ROOT, "spec_verify_layer_gb300", "csrc", "moe_verify.cu")
@@ -401,7 +395,7 @@ def read_traffic(kernel):
         kv = {k.strip(): v.strip() for k, v in kv.items()}
         digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
         if kv.get("kernel") == kernel and kv.get("source_sha256_16") == digest:
-            return float(kv["dram_bytes_per_launch"])
+            return float(kv["dram_bytes_per_launch"]) * layers / float(kv["layers"])
     except Exception:
         pass
     return None

@@ -150,14 +150,19 @@ int32_t moe_last_launch_count(const moe_handle* h);
  * so tests can exercise the MOE_ETIMEOUT path without any hang. */
 int moe_set_wait_limit_ns(moe_handle* h, uint64_t ns);
 
-/* Per-kernel timing of eager (non-graph) calls.  moe_profile(h, 1) starts recording a
- * CUDA event pair around every kernel the handle launches on the caller's stream
- * (and discards earlier records); moe_profile(h, 0) stops.  moe_profile_read
- * synchronizes the recorded events and returns, for one kernel kind (0 = router and
- * top-k, 1 = expert stage, 2 = reduction), the summed device time in ms and the
- * number of launches.  Graph replays are not recorded. */
+/* Timing of eager (non-graph) calls.  moe_profile(h, 1) starts recording a CUDA event
+ * pair around every kernel launch the handle makes on the caller's stream, and
+ * per-phase device timestamps inside moe_round (first use allocates a small device
+ * buffer for them); earlier records are discarded.  moe_profile(h, 0) stops.
+ * moe_profile_read synchronizes the events and returns the summed device time in ms
+ * and the launch count (kind must be 0: the fused round kernel).
+ * moe_profile_phases returns, for the last profiled moe_round, the mean over CTAs and
+ * layers (mean_us) and the per-layer maximum over CTAs averaged over layers (max_us)
+ * of six phases: router GEMV, barrier 1, routing, expert stream, barrier 2, reduction.
+ * n_phases must be >= 6. */
 int moe_profile(moe_handle* h, int enable);
 int moe_profile_read(moe_handle* h, int kind, double* total_ms, int32_t* launches);
+int moe_profile_phases(moe_handle* h, double* mean_us, double* max_us, int32_t n_phases);
 
 const char* moe_strerror(int code);
 

@@ -23,9 +23,10 @@ ABI_SYMBOLS = (
     "moe_create", "moe_destroy", "moe_workspace_bytes", "moe_packed_bytes", "moe_pack_q4",
     "moe_route", "moe_decode_layer", "moe_round", "moe_last_device_status",
     "moe_last_launch_count", "moe_set_wait_limit_ns", "moe_profile", "moe_profile_read",
-    "moe_strerror",
+    "moe_profile_phases", "moe_strerror",
 )
-KIND_ROUTE, KIND_EXPERT, KIND_REDUCE = 0, 1, 2
+KIND_ROUND = 0
+PHASES = ("router", "barrier1", "routing", "experts", "barrier2", "reduce")
 
 
 class moe_dims(ctypes.Structure):
@@ -77,6 +78,8 @@ _lib.moe_profile.argtypes = [_vp, ctypes.c_int]
 _lib.moe_profile.restype = ctypes.c_int
 _lib.moe_profile_read.argtypes = [_vp, ctypes.c_int, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_i32)]
 _lib.moe_profile_read.restype = ctypes.c_int
+_lib.moe_profile_phases.argtypes = [_vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double), _i32]
+_lib.moe_profile_phases.restype = ctypes.c_int
 _lib.moe_strerror.argtypes = [ctypes.c_int]
 _lib.moe_strerror.restype = ctypes.c_char_p
 
@@ -168,3 +171,12 @@ def moe_profile_read(handle: int, kind: int):
     n = _i32()
     _check(_lib.moe_profile_read(handle, int(kind), ctypes.byref(t), ctypes.byref(n)), "moe_profile_read")
     return t.value, n.value
+
+
+def moe_profile_phases(handle: int):
+    """Per-phase device time of the last profiled eager moe_round: {phase: (mean_us, max_us)}."""
+    n = len(PHASES)
+    mean = (ctypes.c_double * n)()
+    mx = (ctypes.c_double * n)()
+    _check(_lib.moe_profile_phases(handle, mean, mx, n), "moe_profile_phases")
+    return {p: (mean[i], mx[i]) for i, p in enumerate(PHASES)}

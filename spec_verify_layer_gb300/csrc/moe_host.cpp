@@ -27,11 +27,6 @@ WsLayout ws_layout(const moe_dims& d, int rows) {
   size_t off = 0;
   L.ctrl = off;     off += 256;
   L.logits = off;   off += up256(R * E * 4);
-  L.ids = off;      off += up256(R * k * 4);
-  L.w = off;        off += up256(R * k * 4);
-  L.uni = off;      off += up256(E * 4);
-  L.csr_off = off;  off += up256((E + 1) * 4);
-  L.csr_pair = off; off += up256(R * k * 4);
   L.partial = off;  off += up256(R * k * (size_t)(d.inter / kSlice) * (size_t)d.hidden * 4);
   L.total = off;
   return L;

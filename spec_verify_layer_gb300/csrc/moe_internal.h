@@ -15,13 +15,15 @@ constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
 constexpr int kMinHidden = 256, kMaxHidden = 2048;
 constexpr int kMaxInter = 4096;
+constexpr int kMaxLayers = 128;  // layers per moe_round call (weight table travels as kernel parameters)
 
 // 0 = valid and supported, MOE_EINVAL, or MOE_EUNSUPPORTED.
 int check_dims(const moe_dims* d);
 
-// Byte offsets of the workspace regions for `rows` rows (each region 256-aligned).
+// Byte offsets of the workspace regions for `rows` rows (each region 256-aligned):
+// grid-barrier words, router logits [rows][E], split-K partials [rows*k][I/32][H].
 struct WsLayout {
-  size_t ctrl, logits, ids, w, uni, csr_off, csr_pair, partial, total;
+  size_t ctrl, logits, partial, total;
 };
 WsLayout ws_layout(const moe_dims& d, int rows);
 

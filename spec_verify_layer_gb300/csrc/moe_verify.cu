@@ -1,25 +1,34 @@
-// GB300 (sm_103a) kernels and C ABI of the MoE layer of a speculative-decoding
-// verify round.  See include/moe_verify.h for the operation and the contract.
+// GB300 (sm_103a) kernel and C ABI of the MoE layer of a speculative-decoding verify
+// round.  See include/moe_verify.h for the operation and the contract.
 //
-// Per layer, three kernels in stream order:
-//   k_route   router GEMV (one warp per expert, canonical fp32 order), then the last
-//             CTA to finish selects each row's top-k, the renormalised weights, the
-//             ascending expert union and a CSR list of (row, rank) pairs per expert.
-//   k_expert  split-K over the expert intermediate dimension: work item = (union
-//             expert u, slice of 32 intermediate rows).  One elected thread stages the
-//             item's gate/up rows, their scales, the matching down K-block and its
-//             scales into shared memory with 1-D bulk TMA copies (one mbarrier); the
-//             CTA then computes g, v, h = silu(g) v for its rows and the down partial
-//             Wd[:, slice] h[slice], written per (row, rank, slice) to the workspace.
-//   k_reduce  out[r][o] = sum_j w[r][j] * sum_s partial[r, j, s][o] in a fixed order,
-//             so a row's result depends only on that row (bitwise).
+// One persistent cooperative kernel (k_round, one CTA per SM) runs a whole round of L
+// layers.  Per layer, with grid-wide barriers B1..B3 in between:
+//   P1  router GEMV: one warp per expert, canonical fp32 order -> logits in the
+//       workspace.  The next layer's router weights are prefetched into L2 while the
+//       current layer streams its experts (they do not depend on any data).
+//   B1
+//   P2  every CTA reads the logits and builds the same routing in shared memory:
+//       per-row top-k (warp per row, redux.sync selection, lower id wins ties),
+//       renormalised weights, the ascending expert union U and, per union expert,
+//       the (row, rank) pairs that picked it.
+//   P3  split-K expert items, item = (union expert, 32-row slice of the intermediate
+//       dimension), handed to CTAs round-robin.  Each CTA double-buffers items in
+//       shared memory: one elected thread issues 1-D bulk TMA copies of the item's
+//       gate/up rows + scales (mbarrier A) and the matching down K-block + scales
+//       (mbarrier B); the CTA computes g, v, h = silu(g) v for each of the expert's
+//       rows as soon as A lands, then the down partial Wd[:, slice] h[slice] once B
+//       lands, and writes it per (row, rank, slice) to the workspace.
+//   B2
+//   P4  out[r][o] = sum_j w[r][j] * sum_s partial[r, j, s][o], a fixed order, so a
+//       row's output depends only on that row (bitwise), whatever shares the round.
+//   B3  (layer l+1's router waits for layer l's output, as a real decode would)
 //
-// Dequantisation in registers without a convert instruction: a nibble n placed in
-// bits [p, p+4) of an otherwise-zero fp32 word is the subnormal n * 2^(p-149), and an
-// fma with x * 2^(87-4m) (m = the nibble's slot) yields n * x * 2^-62 exactly.  A
-// 32-bit word of 8 nibbles therefore costs one AND per weight (plus one shift for the
-// top three nibbles) and one FFMA per weight and row.  The code offset (q = n - 8) is
-// applied once per 32-element block: sum (n-8) x = 2^62 acc - 8 sum x.
+// Dequantisation without a convert instruction: a nibble n placed in bits [p, p+4) of
+// an otherwise-zero fp32 word is the subnormal n * 2^(p-149); an fma with
+// x * 2^(87-4m) (m = the nibble's slot) yields n * x * 2^-62 exactly.  One AND per
+// weight (plus one shift per 8), and packed f32x2 FMAs over pairs of weights.  The
+// code offset (q = n - 8) is applied once per 32-element block:
+// sum (n-8) x = 2^62 acc - 8 sum x.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -33,7 +42,7 @@
 namespace moe {
 namespace {
 
-constexpr int NT = 256;
+constexpr int NT = 512;  // threads per CTA
 constexpr int NW = NT / 32;
 constexpr unsigned kStatusTimeout = 1u;
 constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // 2 s
@@ -41,69 +50,55 @@ constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // 2 s
 // ns (at ~2 GHz) and a few times ns at lower clocks
 constexpr long long kCyclesPerNs = 2;
 constexpr long long kDefaultWaitCycles = (long long)kDefaultWaitNs * kCyclesPerNs;
+constexpr int kPhases = 7;  // phase stamps per layer when profiling
 
-struct Ctrl {
-  unsigned ticket;   // k_route: CTAs that finished their logits
-  unsigned n_union;  // |U| of the current layer
-  unsigned pad[62];
-};
-
-struct LayerArgs {
-  int H, E, k, I, R;
+struct LayerPtrs {
   const float* router;
   const uint8_t* gu_nib;
   const uint16_t* gu_sc;
   const uint8_t* dn_nib;
   const uint16_t* dn_sc;
-  const uint16_t* x;  // [R][H] bf16 bits
-  float* out;         // [R][H]
-  // workspace
-  Ctrl* ctrl;
-  float* logits;   // [R][E]
-  int* ids;        // [R][k]
-  float* w;        // [R][k]
-  int* uni;        // [E]
-  int* csr_off;    // [E+1]
-  int* csr_pair;   // [R*k]
-  float* partial;  // [R*k][I/32][H]
-  // optional caller outputs of moe_route, and the per-layer |U| slot of moe_round
-  int* user_ids;
+};
+
+struct RoundArgs {
+  int H, E, k, I, R, L;
+  int route_only;
+  const uint16_t* x;  // [L][R][H] bf16 bits
+  float* out;         // [L][R][H]
+  int* stats;         // [L] |U| per layer, or null
+  unsigned* bar;      // [0] barrier arrivals, [1] abort flag
+  float* logits;      // [R][E]
+  float* partial;     // [R*k][I/32][H]
+  int* user_ids;      // moe_route outputs (CTA 0 writes them)
   float* user_w;
   int* user_union;
   int* user_nunion;
-  int* stats_slot;
   unsigned* status;
   long long wait_cycles;
+  long long* phase_ts;  // [L][kPhases][grid] globaltimer stamps, or null
+  LayerPtrs layer[kMaxLayers];
 };
 
 // ---------------------------------------------------------------------------------
-// small device helpers
+// device helpers
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+__device__ __forceinline__ long long gtimer() {
+  long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t phase) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(phase)
-      : "memory");
-  return ok != 0;
 }
 
 __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t phase) {
@@ -118,9 +113,21 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t phase) {
   return ok != 0;
 }
 
-// Waits for `phase` of the mbarrier for at most `limit` SM clock cycles; on giving up
-// it raises the timeout bit of the status word and returns false.  The first poll
-// does not block, so a bound of a few cycles gives up deterministically.
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t phase) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(phase)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for `phase` of the mbarrier for at most `limit` SM cycles; on giving up it
+// raises the timeout bit of the status word and returns false.  The first poll does
+// not block, so a bound of a few cycles gives up deterministically.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t phase, unsigned* status,
                                                   long long limit) {
   const long long t0 = clock64();
@@ -144,14 +151,45 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ unsigned ld_relaxed(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
 }
 
-__device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib) {
-  return va > vb || (va == vb && ia < ib);
+// packed pairs of fp32 for fma.rn.f32x2
+typedef unsigned long long f2_t;
+
+__device__ __forceinline__ f2_t f2pack(float lo, float hi) {
+  f2_t r;
+  asm("mov.b64 %0, {%1,%2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+__device__ __forceinline__ float f2sum(f2_t v) {
+  float lo, hi;
+  asm("mov.b64 {%0,%1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return __fadd_rn(lo, hi);
+}
+
+__device__ __forceinline__ void ffma2(f2_t& acc, f2_t a, f2_t b) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
 }
 
 // 2^(87 - 4m) for nibble slots m = 0..4 and 2^(99 - 4m) for m = 5..7 (those three are
@@ -162,121 +200,179 @@ __device__ __forceinline__ float slot_scale(int m) {
   return __int_as_float((127 + e) << 23);
 }
 
-// acc += sum over the 8 nibbles of w of n_m * xs[m] (xs pre-scaled by slot_scale).
-__device__ __forceinline__ void dot8(uint32_t w, const float* xs, float& acc) {
-  acc = __fmaf_rn(__uint_as_float(w & 0x0000000Fu), xs[0], acc);
-  acc = __fmaf_rn(__uint_as_float(w & 0x000000F0u), xs[1], acc);
-  acc = __fmaf_rn(__uint_as_float(w & 0x00000F00u), xs[2], acc);
-  acc = __fmaf_rn(__uint_as_float(w & 0x0000F000u), xs[3], acc);
-  acc = __fmaf_rn(__uint_as_float(w & 0x000F0000u), xs[4], acc);
+// acc += the 8 nibbles of w times xs[4] (pre-scaled pairs), slot pairs (0,1) (2,3) (4,5) (6,7)
+__device__ __forceinline__ void dot8x2(uint32_t w, const f2_t* xs, f2_t& acc) {
   const uint32_t t = w >> 12;
-  acc = __fmaf_rn(__uint_as_float(t & 0x00000F00u), xs[5], acc);
-  acc = __fmaf_rn(__uint_as_float(t & 0x0000F000u), xs[6], acc);
-  acc = __fmaf_rn(__uint_as_float(t & 0x000F0000u), xs[7], acc);
+  ffma2(acc, f2pack(__uint_as_float(w & 0x0000000Fu), __uint_as_float(w & 0x000000F0u)), xs[0]);
+  ffma2(acc, f2pack(__uint_as_float(w & 0x00000F00u), __uint_as_float(w & 0x0000F000u)), xs[1]);
+  ffma2(acc, f2pack(__uint_as_float(w & 0x000F0000u), __uint_as_float(t & 0x00000F00u)), xs[2]);
+  ffma2(acc, f2pack(__uint_as_float(t & 0x0000F000u), __uint_as_float(t & 0x000F0000u)), xs[3]);
 }
 
-// 2^-62 * sum_{k<32} n_k x_k for one 16-byte block of codes.
-__device__ __forceinline__ float dot32(const uint4 nb, const float* xs) {
-  float a0 = 0.f, a1 = 0.f;
-  dot8(nb.x, xs + 0, a0);
-  dot8(nb.y, xs + 8, a1);
-  dot8(nb.z, xs + 16, a0);
-  dot8(nb.w, xs + 24, a1);
-  return __fadd_rn(a0, a1);
+// 2^-62 * sum_{k<32} n_k x_k for one 16-byte block of codes; xs = 16 pre-scaled pairs.
+__device__ __forceinline__ float dot32(const uint4 nb, const f2_t* xs) {
+  f2_t a0 = 0ull, a1 = 0ull;
+  dot8x2(nb.x, xs + 0, a0);
+  dot8x2(nb.y, xs + 4, a1);
+  dot8x2(nb.z, xs + 8, a0);
+  dot8x2(nb.w, xs + 12, a1);
+  return __fadd_rn(f2sum(a0), f2sum(a1));
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
-
 __device__ __forceinline__ float half_bits(uint16_t b) { return __half2float(__ushort_as_half(b)); }
 
-// ---------------------------------------------------------------------------------
-// step 1: router logits, one warp per expert, canonical order
+// float -> unsigned key with the same order; -0 is first folded into +0 so that a
+// signed-zero pair ties (and the lower id wins), as the definition asks.
+__device__ __forceinline__ unsigned order_key(float v) {
+  const unsigned u = __float_as_uint(__fadd_rn(v, 0.0f));
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(unsigned key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
 
-__device__ void router_logits_warp(const LayerArgs& a, int e, int lane) {
-  const int NC = a.H >> 7;  // <= 16
-  const float4* wr = reinterpret_cast<const float4*>(a.router + (size_t)e * a.H) + lane;
-  float4 wv[16];
-#pragma unroll
-  for (int c = 0; c < 16; ++c)
-    if (c < NC) wv[c] = __ldg(wr + 32 * c);
-  for (int r = 0; r < a.R; ++r) {
-    const uint2* xr = reinterpret_cast<const uint2*>(a.x + (size_t)r * a.H) + lane;
-    float p = 0.f;
-#pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      if (c < NC) {
-        const uint2 xv = __ldg(xr + 32 * c);
-        p = __fmaf_rn(wv[c].x, bf16_lo(xv.x), p);
-        p = __fmaf_rn(wv[c].y, bf16_hi(xv.x), p);
-        p = __fmaf_rn(wv[c].z, bf16_lo(xv.y), p);
-        p = __fmaf_rn(wv[c].w, bf16_hi(xv.y), p);
+// ---------------------------------------------------------------------------------
+// grid barrier (all CTAs are co-resident: cooperative launch, one CTA per SM)
+
+struct Sync {
+  unsigned epoch = 0;
+};
+
+// Returns false if the round must be abandoned (a CTA gave up somewhere).
+__device__ bool grid_sync(const RoundArgs& a, Sync& sy) {
+  __shared__ int s_ok;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    sy.epoch += 1;
+    const unsigned target = sy.epoch * gridDim.x;
+    __threadfence();
+    atomicAdd(a.bar, 1u);
+    int ok = 1;
+    const long long t0 = clock64();
+    while (ld_acquire(a.bar) < target) {
+      if (ld_relaxed(a.bar + 1)) {
+        ok = 0;
+        break;
+      }
+      if (clock64() - t0 > a.wait_cycles) {
+        atomicOr(a.status, kStatusTimeout);
+        atomicExch(a.bar + 1, 1u);
+        ok = 0;
+        break;
       }
     }
-    p = warp_sum(p);
-    if (lane == 0) a.logits[(size_t)r * a.E + e] = p;
+    __threadfence();
+    s_ok = ok;
+  }
+  __syncthreads();
+  return s_ok != 0;
+}
+
+__device__ __forceinline__ void stamp(const RoundArgs& a, int l, int ph) {
+  if (a.phase_ts && threadIdx.x == 0)
+    a.phase_ts[((size_t)l * kPhases + ph) * gridDim.x + blockIdx.x] = gtimer();
+}
+
+// ---------------------------------------------------------------------------------
+// P1: router logits, one warp per expert, canonical order
+
+// Lane l accumulates elements 128c + 4l + j for c ascending.  The c-loop runs in groups
+// of 8 (32 weights per lane in registers); for H > 1024 each lane's partial of every
+// row is carried between groups in `carry` (idle staging memory), so the order of the
+// fmas is exactly the canonical one.
+__device__ void router_phase(const RoundArgs& a, const float* router, const uint16_t* x,
+                             float* carry_all) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int NC = a.H >> 7;  // <= 16
+  const int gw = blockIdx.x * NW + warp;
+  float* carry = carry_all + (size_t)warp * a.R * 32;
+  for (int e = gw; e < a.E; e += gridDim.x * NW) {
+    const float4* wr = reinterpret_cast<const float4*>(router + (size_t)e * a.H) + lane;
+    for (int g = 0; g < NC; g += 8) {
+      float4 wv[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        if (g + c < NC) wv[c] = __ldg(wr + 32 * (g + c));
+      const bool last = g + 8 >= NC;
+      for (int r = 0; r < a.R; ++r) {
+        const uint2* xr = reinterpret_cast<const uint2*>(x + (size_t)r * a.H) + lane;
+        float p = (g == 0) ? 0.f : carry[r * 32 + lane];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          if (g + c < NC) {
+            const uint2 xv = __ldg(xr + 32 * (g + c));
+            p = __fmaf_rn(wv[c].x, bf16_lo(xv.x), p);
+            p = __fmaf_rn(wv[c].y, bf16_hi(xv.x), p);
+            p = __fmaf_rn(wv[c].z, bf16_lo(xv.y), p);
+            p = __fmaf_rn(wv[c].w, bf16_hi(xv.y), p);
+          }
+        }
+        if (!last) {
+          carry[r * 32 + lane] = p;
+        } else {
+          p = warp_sum(p);
+          if (lane == 0) a.logits[(size_t)r * a.E + e] = p;
+        }
+      }
+      __syncwarp();
+    }
   }
 }
 
 // ---------------------------------------------------------------------------------
-// steps 2-3: per-row top-k + weights, union, CSR -- executed by one CTA
+// P2: routing tables of one layer, built by every CTA in its shared memory
 
-__device__ void topk_union_cta(const LayerArgs& a) {
-  __shared__ int s_ids[kMaxRows * kMaxTopK];
-  __shared__ unsigned s_mask[kMaxExperts];  // rows that picked expert e
-  __shared__ int s_off[kMaxExperts];        // CSR offset of e
-  __shared__ int s_wf[NW], s_wc[NW];
+struct Tables {
+  int* uni;      // [E] ascending union
+  int* csr_off;  // [E+1] offsets into pair
+  int* pair;     // [R*k] pair index p = r*k + j, grouped by union expert, rows ascending
+  float* w;      // [R*k] renormalised weight of pair p
+  int* n_union;  // [1]
+};
+
+// scratch (inside the staging area, free while routing): mask [E], off_e [E], ids [R*k]
+__device__ int route_phase(const RoundArgs& a, const Tables& T, unsigned* s_mask, int* s_off_e,
+                           int* s_ids, int layer) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int E = a.E, k = a.k, R = a.R;
   for (int e = tid; e < E; e += NT) s_mask[e] = 0u;
-
   const int NE = (E + 31) >> 5;  // <= 32
   for (int r = warp; r < R; r += NW) {
-    float v[32];
-    unsigned taken = 0u;
+    unsigned key[32];
 #pragma unroll
     for (int t = 0; t < 32; ++t) {
       if (t < NE) {
         const int e = lane + 32 * t;
-        if (e < E) {
-          v[t] = __ldcg(a.logits + (size_t)r * E + e);
-        } else {
-          v[t] = -INFINITY;
-          taken |= 1u << t;
-        }
+        key[t] = (e < E) ? order_key(__ldcg(a.logits + (size_t)r * E + e)) : 0u;
       }
     }
     float my_l = 0.f;
     int my_id = 0;
     for (int j = 0; j < k; ++j) {
-      float bv = -INFINITY;
-      int bi = INT_MAX;
+      unsigned bk = 0u;
+      int bt = 0;
 #pragma unroll
-      for (int t = 0; t < 32; ++t) {
-        if (t < NE && !((taken >> t) & 1u)) {
-          const int e = lane + 32 * t;
-          if (ranks_before(v[t], e, bv, bi)) {
-            bv = v[t];
-            bi = e;
-          }
+      for (int t = 0; t < 32; ++t)
+        if (t < NE && key[t] > bk) {  // strict: the first (lowest id) of equal keys stays
+          bk = key[t];
+          bt = t;
         }
-      }
+      const unsigned m = __reduce_max_sync(0xffffffffu, bk);
+      const unsigned cand = (bk == m && m != 0u) ? (unsigned)(lane + 32 * bt) : 0xffffffffu;
+      const unsigned win = __reduce_min_sync(0xffffffffu, cand);
+      if ((int)(win & 31u) == lane) {
 #pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (ranks_before(ov, oi, bv, bi)) {
-          bv = ov;
-          bi = oi;
-        }
+        for (int t = 0; t < 32; ++t)
+          if (t == (int)(win >> 5)) key[t] = 0u;
       }
-      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
       if (lane == j) {
-        my_l = bv;
-        my_id = bi;
+        my_l = key_value(m);
+        my_id = (int)win;
       }
     }
-    // renormalised weights: exp(l_j - l_1) / sum over the k picks, summed in rank order
+    // weights: exp(l_j - l_1) / sum over the k picks, summed in rank order
     const float l1 = __shfl_sync(0xffffffffu, my_l, 0);
     const float ex = (lane < k) ? expf(my_l - l1) : 0.f;
     float den = 0.f;
@@ -285,17 +381,19 @@ __device__ void topk_union_cta(const LayerArgs& a) {
       const float wj = __fdiv_rn(ex, den);
       const int p = r * k + lane;
       s_ids[p] = my_id;
-      a.ids[p] = my_id;
-      a.w[p] = wj;
-      if (a.user_ids) a.user_ids[p] = my_id;
-      if (a.user_w) a.user_w[p] = wj;
+      T.w[p] = wj;
+      if (blockIdx.x == 0) {
+        if (a.user_ids) a.user_ids[p] = my_id;
+        if (a.user_w) a.user_w[p] = wj;
+      }
     }
   }
   __syncthreads();
   for (int p = tid; p < R * k; p += NT) atomicOr(&s_mask[s_ids[p]], 1u << (p / k));
   __syncthreads();
 
-  // exclusive scans over e of (picked ? 1 : 0) and popc(mask): union index, CSR offset
+  // exclusive scans over e of (picked ? 1 : 0) and popc(mask): union index, pair offset
+  __shared__ int s_wf[NW], s_wc[NW];
   const int per = (E + NT - 1) / NT;
   const int e0 = tid * per;
   int lf = 0, lc = 0;
@@ -327,190 +425,314 @@ __device__ void topk_union_cta(const LayerArgs& a) {
   for (int e = e0; e < e0 + per && e < E; ++e) {
     const unsigned m = s_mask[e];
     if (m) {
-      s_off[e] = basec;
-      a.uni[basef] = e;
-      a.csr_off[basef] = basec;
-      if (a.user_union) a.user_union[basef] = e;
+      s_off_e[e] = basec;
+      T.uni[basef] = e;
+      T.csr_off[basef] = basec;
+      if (blockIdx.x == 0 && a.user_union) a.user_union[basef] = e;
       ++basef;
       basec += __popc(m);
     }
   }
   if (tid == NT - 1) {
-    // the last thread's inclusive totals are the union size and the pair count
-    a.ctrl->n_union = (unsigned)basef;
-    a.csr_off[basef] = basec;
-    if (a.user_nunion) *a.user_nunion = basef;
-    if (a.stats_slot) *a.stats_slot = basef;
+    // the last thread's running totals are the union size and the pair count
+    *T.n_union = basef;
+    T.csr_off[basef] = basec;
+    if (blockIdx.x == 0) {
+      if (a.user_nunion) *a.user_nunion = basef;
+      if (a.stats) a.stats[layer] = basef;
+    }
   }
   __syncthreads();
   for (int p = tid; p < R * k; p += NT) {
     const int e = s_ids[p], r = p / k;
-    const int pos = s_off[e] + __popc(s_mask[e] & ((1u << r) - 1u));
-    a.csr_pair[pos] = p;
+    T.pair[s_off_e[e] + __popc(s_mask[e] & ((1u << r) - 1u))] = p;
   }
-}
-
-__global__ void __launch_bounds__(NT) k_route(LayerArgs a) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int e = blockIdx.x * NW + warp;
-  if (e < a.E) router_logits_warp(a, e, lane);
-  __threadfence();
   __syncthreads();
-  __shared__ unsigned s_last;
-  if (threadIdx.x == 0) s_last = (atomicAdd(&a.ctrl->ticket, 1u) == gridDim.x - 1) ? 1u : 0u;
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  topk_union_cta(a);
-  if (threadIdx.x == 0) a.ctrl->ticket = 0u;
+  return *T.n_union;
 }
 
 // ---------------------------------------------------------------------------------
-// steps 4-5a: expert work items
+// P3: expert items
 
-// Shared-memory layout of one staged item (H = hidden):
-//   [0, 32H)    gate/up codes: 2 x 32 rows x H/32 blocks x 16 B
-//   [32H, 36H)  gate/up scales (fp16)
-//   [36H, 52H)  down codes of the slice: H rows x 16 B
-//   [52H, 54H)  down scales (fp16)
-//   then gv[64] floats, h'[32] floats, hsum, mbarrier
+// one staged item: gate/up codes 32H, gate/up scales 4H, down codes 16H, down scales 2H
 __host__ __device__ constexpr size_t stage_bytes(int H) { return (size_t)54 * H; }
-__host__ __device__ constexpr size_t expert_smem_bytes(int H) {
-  return stage_bytes(H) + 64 * 4 + 32 * 4 + 16 + 16;
+
+struct Stage {
+  uint8_t* base;
+  uint32_t bar_a, bar_b;
+};
+
+__device__ void issue_item(const RoundArgs& a, const LayerPtrs& W, const Stage& st, int u, int s) {
+  const size_t H = (size_t)a.H, I = (size_t)a.I, NB = H / 32;
+  // order earlier generic-proxy accesses of this buffer before the async-proxy writes
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  mbar_expect_tx(st.bar_a, (uint32_t)(36 * H));
+  bulk_g2s(smem_u32(st.base), W.gu_nib + (size_t)u * I * H + (size_t)s * 32 * H, (uint32_t)(32 * H),
+           st.bar_a);
+  bulk_g2s(smem_u32(st.base + 32 * H), W.gu_sc + (size_t)u * (I * H / 16) + (size_t)s * 64 * NB,
+           (uint32_t)(4 * H), st.bar_a);
+  mbar_expect_tx(st.bar_b, (uint32_t)(18 * H));
+  bulk_g2s(smem_u32(st.base + 36 * H), W.dn_nib + (size_t)u * (I * H / 2) + (size_t)s * 16 * H,
+           (uint32_t)(16 * H), st.bar_b);
+  bulk_g2s(smem_u32(st.base + 52 * H), W.dn_sc + (size_t)u * (I * H / 32) + (size_t)s * H,
+           (uint32_t)(2 * H), st.bar_b);
 }
 
-template <int NBL>  // blocks of 32 per lane per weight row: ceil(H / 1024)
-__global__ void __launch_bounds__(NT, 2) k_expert(LayerArgs a) {
-  extern __shared__ __align__(128) unsigned char smem[];
+// Computes one staged item for every row of its expert.  Returns false on a timeout.
+// Stage b's state lives in two bitfields: `ph` holds the parity to wait for (bit 2b:
+// gate/up barrier A, bit 2b+1: down barrier B) and `pend` marks copies in flight.  On
+// success both barriers have been consumed (parities flipped, pending bits cleared);
+// on failure `pend` still marks the copies the caller must drain.
+template <int NBL>
+__device__ bool compute_item(const RoundArgs& a, const Tables& T, const Stage& st, int b,
+                             unsigned& ph, unsigned& pend, int ui, int s, const uint16_t* x,
+                             float* s_gv, float* s_h, float* s_hsum) {
   const int H = a.H, NB = H >> 5, NS = a.I >> 5;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  uint8_t* s_gu = smem;
-  const uint16_t* s_gus = reinterpret_cast<const uint16_t*>(smem + 32 * (size_t)H);
-  const uint8_t* s_dn = smem + 36 * (size_t)H;
-  const uint16_t* s_dns = reinterpret_cast<const uint16_t*>(smem + 52 * (size_t)H);
-  float* s_gv = reinterpret_cast<float*>(smem + stage_bytes(H));
-  float* s_h = s_gv + 64;
-  float* s_hsum = s_h + 32;
-  uint64_t* s_bar = reinterpret_cast<uint64_t*>(s_hsum + 4);
-  const uint32_t bar = smem_u32(s_bar);
-  if (tid == 0) mbar_init(bar, 1);
-  __syncthreads();
+  const uint8_t* s_gu = st.base;
+  const uint16_t* s_gus = reinterpret_cast<const uint16_t*>(st.base + 32 * (size_t)H);
+  const uint8_t* s_dn = st.base + 36 * (size_t)H;
+  const uint16_t* s_dns = reinterpret_cast<const uint16_t*>(st.base + 52 * (size_t)H);
 
-  uint32_t phase = 0;
-  const int n_items = (int)__ldcg(&a.ctrl->n_union) * NS;
-  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-    const int ui = it / NS, s = it - (it / NS) * NS;
-    const int u = __ldcg(a.uni + ui);
-    if (tid == 0) {
-      const size_t I = (size_t)a.I, Hs = (size_t)H;
-      // order the previous item's shared-memory reads before the async-proxy writes
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_expect_tx(bar, (uint32_t)stage_bytes(H));
-      bulk_g2s(smem_u32(s_gu), a.gu_nib + (size_t)u * I * Hs + (size_t)s * 32 * Hs, 32 * H, bar);
-      bulk_g2s(smem_u32(s_gus), a.gu_sc + (size_t)u * (I * Hs / 16) + (size_t)s * 64 * NB, 4 * H,
-               bar);
-      bulk_g2s(smem_u32(s_dn), a.dn_nib + (size_t)u * (I * Hs / 2) + (size_t)s * 16 * Hs, 16 * H,
-               bar);
-      bulk_g2s(smem_u32(s_dns), a.dn_sc + (size_t)u * (I * Hs / 32) + (size_t)s * Hs, 2 * H, bar);
-    }
-    const int p0 = __ldcg(a.csr_off + ui), p1 = __ldcg(a.csr_off + ui + 1);
-    bool ok = mbar_wait_bounded(bar, phase, a.status, a.wait_cycles);
-    if (__syncthreads_or(!ok)) {
-      // give the copies in flight a second bounded chance to land, then leave
-      mbar_wait_bounded(bar, phase, a.status, kDefaultWaitCycles);
-      break;
-    }
-    phase ^= 1u;
-
-    for (int pp = p0; pp < p1; ++pp) {
-      const int pair = __ldcg(a.csr_pair + pp);
-      const int r = pair / a.k;
-      // ---- gate / up: warp per weight row, lane per 32-element block ----
-      float xs[NBL][32];
-      float xsum8[NBL];
+  const unsigned bit_a = 1u << (2 * b), bit_b = 2u << (2 * b);
+  bool ok = mbar_wait_bounded(st.bar_a, (ph & bit_a) ? 1u : 0u, a.status, a.wait_cycles);
+  if (__syncthreads_or(!ok)) return false;
+  ph ^= bit_a;
+  pend &= ~bit_a;
+  bool have_b = false;
+  const int p0 = T.csr_off[ui], p1 = T.csr_off[ui + 1];
+  for (int pp = p0; pp < p1; ++pp) {
+    const int pair = T.pair[pp];
+    const int r = pair / a.k;
+    // ---- gate / up: warp per weight row, lane per 32-element block ----
+    // 64 weight rows (32 gate, 32 up) over NW warps; the lane's blocks are visited one
+    // at a time so only one block of pre-scaled activations sits in registers.
+    constexpr int RPW = 64 / NW;
+    float part[RPW];
 #pragma unroll
-      for (int t = 0; t < NBL; ++t) {
-        const int b = lane + 32 * t;
-        xsum8[t] = 0.f;
-        if (b < NB) {
-          const uint4* xp = reinterpret_cast<const uint4*>(a.x + (size_t)r * H + 32 * b);
-          float sum = 0.f;
+    for (int q = 0; q < RPW; ++q) part[q] = 0.f;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint4 v = __ldg(xp + q);
-            const uint32_t wds[4] = {v.x, v.y, v.z, v.w};
+    for (int t = 0; t < NBL; ++t) {
+      const int blk = lane + 32 * t;
+      if (blk < NB) {
+        f2_t xs[16];
+        float sum = 0.f;
+        const uint4* xp = reinterpret_cast<const uint4*>(x + (size_t)r * H + 32 * blk);
 #pragma unroll
-            for (int z = 0; z < 4; ++z) {
-              const float lo = bf16_lo(wds[z]), hi = bf16_hi(wds[z]);
-              const int k0 = 8 * q + 2 * z;
-              xs[t][k0] = lo * slot_scale(k0 & 7);
-              xs[t][k0 + 1] = hi * slot_scale((k0 + 1) & 7);
-              sum = __fadd_rn(sum, lo);
-              sum = __fadd_rn(sum, hi);
-            }
-          }
-          xsum8[t] = -8.f * sum;
-        }
-      }
-      for (int wr = warp; wr < 64; wr += NW) {
-        float part = 0.f;
+        for (int q = 0; q < 4; ++q) {
+          const uint4 v = __ldg(xp + q);
+          const uint32_t wds[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int t = 0; t < NBL; ++t) {
-          const int b = lane + 32 * t;
-          if (b < NB) {
-            const uint4 nb = *reinterpret_cast<const uint4*>(s_gu + ((size_t)wr * NB + b) * 16);
-            const float sc = half_bits(s_gus[wr * NB + b]);
-            const float acc = dot32(nb, xs[t]);
-            part = __fmaf_rn(sc, __fmaf_rn(acc, 0x1p62f, xsum8[t]), part);
+          for (int z = 0; z < 4; ++z) {
+            const float lo = bf16_lo(wds[z]), hi = bf16_hi(wds[z]);
+            const int k0 = 8 * q + 2 * z;  // element index in the block; slots k0&7, +1
+            xs[k0 >> 1] = f2pack(lo * slot_scale(k0 & 7), hi * slot_scale((k0 + 1) & 7));
+            sum = __fadd_rn(sum, lo);
+            sum = __fadd_rn(sum, hi);
           }
         }
-        part = warp_sum(part);
-        if (lane == 0) s_gv[wr] = part;
-      }
-      __syncthreads();
-      // ---- SwiGLU on the slice's 32 intermediate rows ----
-      if (warp == 0) {
-        const float g = s_gv[lane], v = s_gv[32 + lane];
-        const float hh = __fmul_rn(__fdiv_rn(g, __fadd_rn(1.f, expf(-g))), v);
-        s_h[lane] = hh * slot_scale(lane & 7);
-        const float hs = warp_sum(hh);
-        if (lane == 0) *s_hsum = -8.f * hs;
-      }
-      __syncthreads();
-      // ---- down partial: thread per output row, one 32-element K-block each ----
-      float hreg[32];
+        const float xsum8 = -8.f * sum;
 #pragma unroll
-      for (int q = 0; q < 32; ++q) hreg[q] = s_h[q];
-      const float hsum8 = *s_hsum;
-      float* dst = a.partial + ((size_t)pair * NS + s) * H;
-      for (int o = tid; o < H; o += NT) {
-        const uint4 nb = *reinterpret_cast<const uint4*>(s_dn + (size_t)o * 16);
-        const float sc = half_bits(s_dns[o]);
-        const float acc = dot32(nb, hreg);
-        dst[o] = __fmul_rn(sc, __fmaf_rn(acc, 0x1p62f, hsum8));
+        for (int q = 0; q < RPW; ++q) {
+          const int wr = warp + NW * q;
+          const uint4 nb = *reinterpret_cast<const uint4*>(s_gu + ((size_t)wr * NB + blk) * 16);
+          const float sc = half_bits(s_gus[wr * NB + blk]);
+          const float acc = dot32(nb, xs);
+          part[q] = __fmaf_rn(sc, __fmaf_rn(acc, 0x1p62f, xsum8), part[q]);
+        }
       }
+    }
+#pragma unroll
+    for (int q = 0; q < RPW; ++q) {
+      const float v = warp_sum(part[q]);
+      if (lane == 0) s_gv[warp + NW * q] = v;
+    }
+    __syncthreads();
+    // ---- SwiGLU on the slice's 32 intermediate rows ----
+    if (warp == 0) {
+      const float g = s_gv[lane], v = s_gv[32 + lane];
+      const float hh = __fmul_rn(__fdiv_rn(g, __fadd_rn(1.f, expf(-g))), v);
+      s_h[lane] = hh * slot_scale(lane & 7);
+      const float hs = warp_sum(hh);
+      if (lane == 0) *s_hsum = -8.f * hs;
+    }
+    if (!have_b) {
+      ok = mbar_wait_bounded(st.bar_b, (ph & bit_b) ? 1u : 0u, a.status, a.wait_cycles);
+      if (__syncthreads_or(!ok)) return false;
+      ph ^= bit_b;
+      pend &= ~bit_b;
+      have_b = true;
+    } else {
       __syncthreads();
     }
+    // ---- down partial: thread per output row, one 32-element K-block each ----
+    f2_t hreg[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) hreg[q] = f2pack(s_h[2 * q], s_h[2 * q + 1]);
+    const float hsum8 = *s_hsum;
+    float* dst = a.partial + ((size_t)pair * NS + s) * H;
+    for (int o = tid; o < H; o += NT) {
+      const uint4 nb = *reinterpret_cast<const uint4*>(s_dn + (size_t)o * 16);
+      const float sc = half_bits(s_dns[o]);
+      const float acc = dot32(nb, hreg);
+      dst[o] = __fmul_rn(sc, __fmaf_rn(acc, 0x1p62f, hsum8));
+    }
+    // the next row's gate/up may overwrite s_gv only after everyone has read s_h
+    __syncthreads();
+  }
+  if (!have_b) {  // (every union expert has a row, so this only keeps phases paired)
+    ok = mbar_wait_bounded(st.bar_b, (ph & bit_b) ? 1u : 0u, a.status, a.wait_cycles);
+    if (__syncthreads_or(!ok)) return false;
+    ph ^= bit_b;
+    pend &= ~bit_b;
+  }
+  return true;
+}
+
+// ---------------------------------------------------------------------------------
+// P4: fixed-order weighted reduction of the partials into the layer output
+
+__device__ void reduce_phase(const RoundArgs& a, const Tables& T, float* out) {
+  const int H = a.H, k = a.k, NS = a.I >> 5;
+  int kp = 1;
+  while (kp < k) kp <<= 1;  // lanes per output; kp divides 32
+  const int lane = threadIdx.x & 31;
+  const int gbase = lane & ~(kp - 1);
+  const long long total = (long long)a.R * H * kp;
+  for (long long t = (long long)blockIdx.x * NT + threadIdx.x; t < total;
+       t += (long long)gridDim.x * NT) {
+    const int j = (int)(t & (kp - 1));
+    const long long ro = t / kp;
+    const int r = (int)(ro / H), o = (int)(ro - (long long)r * H);
+    float y = 0.f;
+    if (j < k) {
+      const float* src = a.partial + (size_t)(r * k + j) * NS * H + o;
+      for (int s = 0; s < NS; ++s) y = __fadd_rn(y, __ldcg(src + (size_t)s * H));
+    }
+    float acc = 0.f;
+    for (int jj = 0; jj < k; ++jj) {
+      const float yj = __shfl_sync(0xffffffffu, y, gbase + jj);
+      acc = __fmaf_rn(T.w[r * k + jj], yj, acc);
+    }
+    if (j == 0) out[(size_t)r * H + o] = acc;
   }
 }
 
 // ---------------------------------------------------------------------------------
-// step 5b: weighted, fixed-order reduction of the partials
+// shared-memory plan
 
-__global__ void __launch_bounds__(NT) k_reduce(LayerArgs a) {
-  const int o = blockIdx.x * NT + threadIdx.x;
-  const int r = blockIdx.y;
-  if (o >= a.H) return;
-  const int NS = a.I >> 5;
-  float acc = 0.f;
-  for (int j = 0; j < a.k; ++j) {
-    const int pair = r * a.k + j;
-    const float* src = a.partial + (size_t)pair * NS * a.H + o;
-    float y = 0.f;
-    for (int s = 0; s < NS; ++s) y = __fadd_rn(y, __ldcg(src + (size_t)s * a.H));
-    acc = __fmaf_rn(__ldcg(a.w + pair), y, acc);
+struct SmemPlan {
+  size_t stage, stage0, stage1, bars, gv, uni, csr, pair, w, nunion, total;
+};
+
+__host__ __device__ inline size_t up128(size_t x) { return (x + 127) & ~(size_t)127; }
+
+__host__ __device__ inline SmemPlan smem_plan(int H, int E, int R, int k) {
+  SmemPlan p{};
+  p.stage = up128(stage_bytes(H));
+  size_t off = 0;
+  p.stage0 = off;  off += p.stage;
+  p.stage1 = off;  off += p.stage;
+  p.bars = off;    off += 64;
+  p.gv = off;      off += up128((64 + 32 + 4) * 4);
+  p.uni = off;     off += up128((size_t)E * 4);
+  p.csr = off;     off += up128((size_t)(E + 1) * 4);
+  p.pair = off;    off += up128((size_t)R * k * 4);
+  p.w = off;       off += up128((size_t)R * k * 4);
+  p.nunion = off;  off += 128;
+  p.total = off;
+  return p;
+}
+
+template <int NBL>
+__global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundArgs a) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  const int tid = threadIdx.x;
+  const SmemPlan P = smem_plan(a.H, a.E, a.R, a.k);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P.bars);
+  // stage b: buffer at stage0 + b * stage, barriers bars[2b] (A) and bars[2b + 1] (B)
+  auto stage_of = [&](int b) {
+    return Stage{smem + P.stage0 + (size_t)b * P.stage, smem_u32(bars + 2 * b),
+                 smem_u32(bars + 2 * b + 1)};
+  };
+  float* s_gv = reinterpret_cast<float*>(smem + P.gv);
+  float* s_h = s_gv + 64;
+  float* s_hsum = s_h + 32;
+  Tables T{reinterpret_cast<int*>(smem + P.uni), reinterpret_cast<int*>(smem + P.csr),
+           reinterpret_cast<int*>(smem + P.pair), reinterpret_cast<float*>(smem + P.w),
+           reinterpret_cast<int*>(smem + P.nunion)};
+  // routing scratch lives in the (then idle) staging area
+  unsigned* s_mask = reinterpret_cast<unsigned*>(smem + P.stage0);
+  int* s_off_e = reinterpret_cast<int*>(smem + P.stage0 + (size_t)a.E * 4);
+  int* s_ids = reinterpret_cast<int*>(smem + P.stage0 + (size_t)a.E * 8);
+  if (tid == 0) {
+    for (int i = 0; i < 4; ++i) mbar_init(smem_u32(bars + i), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  a.out[(size_t)r * a.H + o] = acc;
+  __syncthreads();
+
+  Sync sy;
+  unsigned ph = 0u;    // parity to wait for: bit 2b = stage b's barrier A, bit 2b+1 = B
+  unsigned pend = 0u;  // copies in flight, same bit layout
+  const int G = gridDim.x, NS = a.I >> 5;
+  const size_t RH = (size_t)a.R * a.H;
+  for (int l = 0; l < a.L; ++l) {
+    const LayerPtrs& W = a.layer[l];
+    const uint16_t* x = a.x + (size_t)l * RH;
+    stamp(a, l, 0);
+    router_phase(a, W.router, x, reinterpret_cast<float*>(smem + P.stage0));
+    stamp(a, l, 1);
+    if (!grid_sync(a, sy)) return;  // B1: all logits written
+    stamp(a, l, 2);
+    const int U = route_phase(a, T, s_mask, s_off_e, s_ids, l);
+    stamp(a, l, 3);
+    if (a.route_only) return;
+    const int n_items = U * NS;
+    for (int n = 0; n < 2; ++n) {
+      const int it = blockIdx.x + n * G;
+      if (it < n_items) {
+        pend |= 3u << (2 * n);  // every thread tracks what thread 0 issues
+        if (tid == 0) issue_item(a, W, stage_of(n), T.uni[it / NS], it % NS);
+      }
+    }
+    if (tid == 0) {
+      if (l + 1 < a.L) {  // the next layer's router weights do not depend on any data
+        const size_t bytes = (size_t)a.E * a.H * 4;
+        const size_t chunk = ((bytes / G) + 15) & ~(size_t)15;
+        const size_t b0 = (size_t)blockIdx.x * chunk;
+        if (b0 < bytes) {
+          const size_t n = (bytes - b0 < chunk) ? bytes - b0 : chunk;
+          prefetch_l2(reinterpret_cast<const char*>(a.layer[l + 1].router) + b0, (uint32_t)n);
+        }
+      }
+    }
+    for (int n = 0;; ++n) {
+      const int it = blockIdx.x + n * G;
+      if (it >= n_items) break;
+      const int b = n & 1;
+      if (!compute_item<NBL>(a, T, stage_of(b), b, ph, pend, it / NS, it % NS, x, s_gv, s_h,
+                             s_hsum)) {
+        // give every copy still in flight a bounded chance to land, then leave
+        for (int q = 0; q < 4; ++q)
+          if (pend & (1u << q))
+            mbar_wait_bounded(smem_u32(bars + q), (ph >> q) & 1u, a.status, kDefaultWaitCycles);
+        if (tid == 0) atomicExch(a.bar + 1, 1u);
+        return;
+      }
+      // compute_item ends with a CTA barrier: the stage is free again
+      const int nxt = it + 2 * G;
+      if (nxt < n_items) {
+        pend |= 3u << (2 * b);
+        if (tid == 0) issue_item(a, W, stage_of(b), T.uni[nxt / NS], nxt % NS);
+      }
+    }
+    stamp(a, l, 4);
+    if (!grid_sync(a, sy)) return;  // B2: all partials written
+    stamp(a, l, 5);
+    reduce_phase(a, T, a.out + (size_t)l * RH);
+    stamp(a, l, 6);
+    if (l + 1 < a.L && !grid_sync(a, sy)) return;  // B3: layer output complete
+  }
 }
 
 }  // namespace
@@ -535,26 +757,22 @@ struct GraphKey {
   }
 };
 
-struct ProfPair {
-  cudaEvent_t start = nullptr, stop = nullptr;
-  int kind = 0;
-};
-
 struct moe_handle {
   moe_dims dims;
   int device = 0;
   int sm_count = 0;
-  int expert_ctas_per_sm = 1;
   unsigned* status = nullptr;
   unsigned long long wait_ns = kDefaultWaitNs;
   int32_t last_launches = 0;
   GraphKey gkey;
   cudaGraphExec_t gexec = nullptr;
   int32_t graph_launches = 0;
-  // per-kernel event timing of eager launches (moe_profile)
+  // profiling of eager calls (moe_profile): event pairs and phase stamps
   bool profiling = false;
-  std::vector<ProfPair> prof;
-  size_t prof_used = 0;
+  std::vector<cudaEvent_t> ev;  // start/stop pairs
+  size_t ev_used = 0;
+  long long* phase_ts = nullptr;  // [kMaxLayers][kPhases][sm_count]
+  int32_t phase_layers = 0;
 };
 
 namespace {
@@ -565,6 +783,7 @@ struct DeviceGuard {
   explicit DeviceGuard(int dev) {
     if (cudaGetDevice(&prev) != cudaSuccess) {
       ok = false;
+      prev = -1;
       return;
     }
     if (prev != dev && cudaSetDevice(dev) != cudaSuccess) ok = false;
@@ -586,91 +805,59 @@ int check_layer(const moe_layer_w* w) {
   return MOE_OK;
 }
 
-LayerArgs make_args(const moe_handle* h, const moe_layer_w* w, const uint16_t* x, int rows,
-                    float* out, void* ws) {
+size_t smem_bytes(const moe_dims& d, int rows) {
+  return smem_plan(d.hidden, d.n_experts, rows, d.top_k).total;
+}
+
+void fill_args(RoundArgs& a, const moe_handle* h, int rows, void* ws) {
   const moe_dims& d = h->dims;
   const WsLayout L = ws_layout(d, rows);
   char* base = static_cast<char*>(ws);
-  LayerArgs a{};
   a.H = d.hidden;
   a.E = d.n_experts;
   a.k = d.top_k;
   a.I = d.inter;
   a.R = rows;
-  a.router = w->router;
-  a.gu_nib = w->gateup_nib;
-  a.gu_sc = w->gateup_scale;
-  a.dn_nib = w->down_nib;
-  a.dn_sc = w->down_scale;
-  a.x = x;
-  a.out = out;
-  a.ctrl = reinterpret_cast<Ctrl*>(base + L.ctrl);
+  a.bar = reinterpret_cast<unsigned*>(base + L.ctrl);
   a.logits = reinterpret_cast<float*>(base + L.logits);
-  a.ids = reinterpret_cast<int*>(base + L.ids);
-  a.w = reinterpret_cast<float*>(base + L.w);
-  a.uni = reinterpret_cast<int*>(base + L.uni);
-  a.csr_off = reinterpret_cast<int*>(base + L.csr_off);
-  a.csr_pair = reinterpret_cast<int*>(base + L.csr_pair);
   a.partial = reinterpret_cast<float*>(base + L.partial);
   a.status = h->status;
   const unsigned long long ns = h->wait_ns < (1ull << 40) ? h->wait_ns : (1ull << 40);
   a.wait_cycles = (long long)ns * kCyclesPerNs;
-  return a;
 }
 
-int expert_grid(const moe_handle* h, int rows) {
-  const moe_dims& d = h->dims;
-  const int max_u = d.n_experts < rows * d.top_k ? d.n_experts : rows * d.top_k;
-  const int max_items = max_u * (d.inter / kSlice);
-  const int cap = h->sm_count * h->expert_ctas_per_sm;
-  return max_items < cap ? max_items : cap;
-}
-
-// Event pair around one launch when profiling eager calls; nullptr otherwise.
-ProfPair* prof_begin(moe_handle* h, bool capturing, int kind, cudaStream_t st) {
-  if (!h->profiling || capturing) return nullptr;
-  if (h->prof_used == h->prof.size()) {
-    ProfPair p;
-    if (cudaEventCreate(&p.start) != cudaSuccess || cudaEventCreate(&p.stop) != cudaSuccess) {
-      cudaGetLastError();
-      return nullptr;
+cudaError_t launch_round(moe_handle* h, const RoundArgs& a, cudaStream_t st, bool capturing) {
+  cudaError_t e = cudaMemsetAsync(a.bar, 0, 256, st);
+  if (e != cudaSuccess) return e;
+  const bool prof = h->profiling && !capturing;
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  if (prof) {
+    while (h->ev.size() < h->ev_used + 2) {
+      cudaEvent_t ev;
+      if (cudaEventCreate(&ev) != cudaSuccess) return cudaGetLastError();
+      h->ev.push_back(ev);
     }
-    h->prof.push_back(p);
+    e0 = h->ev[h->ev_used];
+    e1 = h->ev[h->ev_used + 1];
+    h->ev_used += 2;
+    cudaEventRecord(e0, st);
   }
-  ProfPair* p = &h->prof[h->prof_used++];
-  p->kind = kind;
-  cudaEventRecord(p->start, st);
-  return p;
-}
-
-void prof_end(ProfPair* p, cudaStream_t st) {
-  if (p) cudaEventRecord(p->stop, st);
-}
-
-// Enqueues one layer: route (+ top-k/union), optionally expert + reduce.
-cudaError_t enqueue_layer(moe_handle* h, const LayerArgs& a, bool full, cudaStream_t st,
-                          int32_t* launches, bool capturing = false) {
-  const int H = a.H;
-  ProfPair* p = prof_begin(h, capturing, 0, st);
-  k_route<<<(a.E + NW - 1) / NW, NT, 0, st>>>(a);
-  prof_end(p, st);
-  ++*launches;
-  if (full) {
-    const int grid = expert_grid(h, a.R);
-    const size_t smem = expert_smem_bytes(H);
-    p = prof_begin(h, capturing, 1, st);
-    if (nbl_of(H) == 1)
-      k_expert<1><<<grid, NT, smem, st>>>(a);
-    else
-      k_expert<2><<<grid, NT, smem, st>>>(a);
-    prof_end(p, st);
-    ++*launches;
-    p = prof_begin(h, capturing, 2, st);
-    k_reduce<<<dim3((H + NT - 1) / NT, a.R), NT, 0, st>>>(a);
-    prof_end(p, st);
-    ++*launches;
-  }
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(h->sm_count);
+  cfg.blockDim = dim3(NT);
+  cfg.dynamicSmemBytes = smem_bytes(h->dims, a.R);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (nbl_of(a.H) == 1)
+    e = cudaLaunchKernelEx(&cfg, k_round<1>, a);
+  else
+    e = cudaLaunchKernelEx(&cfg, k_round<2>, a);
+  if (prof) cudaEventRecord(e1, st);
+  return e;
 }
 
 int common_checks(moe_handle* h, const uint16_t* x, int32_t rows, void* ws, size_t ws_bytes) {
@@ -678,6 +865,16 @@ int common_checks(moe_handle* h, const uint16_t* x, int32_t rows, void* ws, size
   if (rows < 1 || rows > h->dims.max_rows) return MOE_EINVAL;
   if (ws_bytes < ws_layout(h->dims, rows).total) return MOE_EWORKSPACE;
   return MOE_OK;
+}
+
+void copy_layers(RoundArgs& a, const moe_layer_w* layers, int32_t L) {
+  for (int32_t l = 0; l < L; ++l) {
+    a.layer[l].router = layers[l].router;
+    a.layer[l].gu_nib = layers[l].gateup_nib;
+    a.layer[l].gu_sc = layers[l].gateup_scale;
+    a.layer[l].dn_nib = layers[l].down_nib;
+    a.layer[l].dn_sc = layers[l].down_scale;
+  }
 }
 
 }  // namespace
@@ -689,6 +886,8 @@ int moe_create(const moe_dims* dims, int device, moe_handle** out) {
   *out = nullptr;
   int rc = check_dims(dims);
   if (rc != MOE_OK) return rc;
+  const size_t smem = smem_bytes(*dims, dims->max_rows);
+  if (smem > 227 * 1024) return MOE_EUNSUPPORTED;
   int ndev = 0;
   if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) {
     cudaGetLastError();
@@ -696,10 +895,12 @@ int moe_create(const moe_dims* dims, int device, moe_handle** out) {
   }
   DeviceGuard g(device);
   if (!g.ok) return MOE_ECUDA;
+  int coop = 0;
   moe_handle* h = new moe_handle();
   h->dims = *dims;
   h->device = device;
   if (cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, device) != cudaSuccess || !coop ||
       cudaMalloc(&h->status, sizeof(unsigned)) != cudaSuccess ||
       cudaMemset(h->status, 0, sizeof(unsigned)) != cudaSuccess) {
     cudaGetLastError();
@@ -707,17 +908,14 @@ int moe_create(const moe_dims* dims, int device, moe_handle** out) {
     delete h;
     return MOE_ECUDA;
   }
-  const size_t smem = expert_smem_bytes(dims->hidden);
   cudaError_t e;
   int occ = 0;
   if (nbl_of(dims->hidden) == 1) {
-    e = cudaFuncSetAttribute(k_expert<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e == cudaSuccess)
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_expert<1>, NT, smem);
+    e = cudaFuncSetAttribute(k_round<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_round<1>, NT, smem);
   } else {
-    e = cudaFuncSetAttribute(k_expert<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e == cudaSuccess)
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_expert<2>, NT, smem);
+    e = cudaFuncSetAttribute(k_round<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_round<2>, NT, smem);
   }
   if (e != cudaSuccess || occ < 1) {
     cudaGetLastError();
@@ -725,7 +923,6 @@ int moe_create(const moe_dims* dims, int device, moe_handle** out) {
     delete h;
     return MOE_ECUDA;
   }
-  h->expert_ctas_per_sm = occ;
   *out = h;
   return MOE_OK;
 }
@@ -735,38 +932,9 @@ void moe_destroy(moe_handle* h) {
   DeviceGuard g(h->device);
   if (h->gexec) cudaGraphExecDestroy(h->gexec);
   if (h->status) cudaFree(h->status);
-  for (ProfPair& p : h->prof) {
-    cudaEventDestroy(p.start);
-    cudaEventDestroy(p.stop);
-  }
+  if (h->phase_ts) cudaFree(h->phase_ts);
+  for (cudaEvent_t e : h->ev) cudaEventDestroy(e);
   delete h;
-}
-
-int moe_profile(moe_handle* h, int enable) {
-  if (!h) return MOE_EINVAL;
-  h->profiling = enable != 0;
-  h->prof_used = 0;
-  return MOE_OK;
-}
-
-int moe_profile_read(moe_handle* h, int kind, double* total_ms, int32_t* launches) {
-  if (!h || !total_ms || !launches || kind < 0 || kind > 2) return MOE_EINVAL;
-  DeviceGuard g(h->device);
-  if (!g.ok) return MOE_ECUDA;
-  double t = 0.0;
-  int32_t n = 0;
-  for (size_t i = 0; i < h->prof_used; ++i) {
-    ProfPair& p = h->prof[i];
-    if (p.kind != kind) continue;
-    if (cudaEventSynchronize(p.stop) != cudaSuccess) return MOE_ECUDA;
-    float ms = 0.f;
-    if (cudaEventElapsedTime(&ms, p.start, p.stop) != cudaSuccess) return MOE_ECUDA;
-    t += ms;
-    ++n;
-  }
-  *total_ms = t;
-  *launches = n;
-  return MOE_OK;
 }
 
 int moe_set_wait_limit_ns(moe_handle* h, uint64_t ns) {
@@ -783,16 +951,19 @@ int moe_route(moe_handle* h, const moe_layer_w* w, const uint16_t* x_bf16, int32
   if (!w || !aligned16(w->router)) return MOE_EINVAL;
   DeviceGuard g(h->device);
   if (!g.ok) return MOE_ECUDA;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  LayerArgs a = make_args(h, w, x_bf16, rows, nullptr, ws);
+  RoundArgs a{};
+  fill_args(a, h, rows, ws);
+  a.L = 1;
+  a.route_only = 1;
+  a.x = x_bf16;
   a.user_ids = topk_ids;
   a.user_w = topk_w;
   a.user_union = union_ids;
   a.user_nunion = n_union;
-  h->last_launches = 0;
-  if (cudaMemsetAsync(a.ctrl, 0, sizeof(Ctrl), st) != cudaSuccess) return MOE_ECUDA;
-  if (enqueue_layer(h, a, false, st, &h->last_launches) != cudaSuccess) return MOE_ECUDA;
-  return MOE_OK;
+  a.layer[0].router = w->router;
+  h->last_launches = 1;
+  return launch_round(h, a, static_cast<cudaStream_t>(stream), false) == cudaSuccess ? MOE_OK
+                                                                                    : MOE_ECUDA;
 }
 
 int moe_decode_layer(moe_handle* h, const moe_layer_w* w, const uint16_t* x_bf16, int32_t rows,
@@ -803,29 +974,15 @@ int moe_decode_layer(moe_handle* h, const moe_layer_w* w, const uint16_t* x_bf16
   if (!aligned16(out)) return MOE_EINVAL;
   DeviceGuard g(h->device);
   if (!g.ok) return MOE_ECUDA;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  LayerArgs a = make_args(h, w, x_bf16, rows, out, ws);
-  h->last_launches = 0;
-  if (cudaMemsetAsync(a.ctrl, 0, sizeof(Ctrl), st) != cudaSuccess) return MOE_ECUDA;
-  if (enqueue_layer(h, a, true, st, &h->last_launches) != cudaSuccess) return MOE_ECUDA;
-  return MOE_OK;
-}
-
-static cudaError_t enqueue_round(moe_handle* h, const moe_layer_w* layers, int32_t L,
-                                 const uint16_t* x, int32_t rows, float* out, int32_t* stats,
-                                 void* ws, cudaStream_t st, int32_t* launches,
-                                 bool capturing = false) {
-  const size_t HR = (size_t)h->dims.hidden * rows;
-  LayerArgs a0 = make_args(h, &layers[0], x, rows, out, ws);
-  cudaError_t e = cudaMemsetAsync(a0.ctrl, 0, sizeof(Ctrl), st);
-  if (e != cudaSuccess) return e;
-  for (int32_t l = 0; l < L; ++l) {
-    LayerArgs a = make_args(h, &layers[l], x + (size_t)l * HR, rows, out + (size_t)l * HR, ws);
-    a.stats_slot = stats ? stats + l : nullptr;
-    e = enqueue_layer(h, a, true, st, launches, capturing);
-    if (e != cudaSuccess) return e;
-  }
-  return cudaSuccess;
+  RoundArgs a{};
+  fill_args(a, h, rows, ws);
+  a.L = 1;
+  a.x = x_bf16;
+  a.out = out;
+  copy_layers(a, w, 1);
+  h->last_launches = 1;
+  return launch_round(h, a, static_cast<cudaStream_t>(stream), false) == cudaSuccess ? MOE_OK
+                                                                                    : MOE_ECUDA;
 }
 
 int moe_round(moe_handle* h, const moe_layer_w* layers, int32_t L, const uint16_t* x_bf16,
@@ -834,18 +991,27 @@ int moe_round(moe_handle* h, const moe_layer_w* layers, int32_t L, const uint16_
   int rc = common_checks(h, x_bf16, rows, ws, ws_bytes);
   if (rc != MOE_OK) return rc;
   if (!layers || L < 1 || !aligned16(out)) return MOE_EINVAL;
+  if (L > kMaxLayers) return MOE_EUNSUPPORTED;
   for (int32_t l = 0; l < L; ++l)
     if ((rc = check_layer(&layers[l])) != MOE_OK) return rc;
   if (use_graph && !stream) return MOE_EINVAL;
   DeviceGuard g(h->device);
   if (!g.ok) return MOE_ECUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  RoundArgs a{};
+  fill_args(a, h, rows, ws);
+  a.L = L;
+  a.x = x_bf16;
+  a.out = out;
+  a.stats = stats;
+  copy_layers(a, layers, L);
   if (!use_graph) {
-    h->last_launches = 0;
-    if (enqueue_round(h, layers, L, x_bf16, rows, out, stats, ws, st, &h->last_launches) !=
-        cudaSuccess)
-      return MOE_ECUDA;
-    return MOE_OK;
+    if (h->profiling && h->phase_ts) {
+      a.phase_ts = h->phase_ts;
+      h->phase_layers = L;
+    }
+    h->last_launches = 1;
+    return launch_round(h, a, st, false) == cudaSuccess ? MOE_OK : MOE_ECUDA;
   }
   GraphKey key;
   key.layers.assign(layers, layers + L);
@@ -863,8 +1029,7 @@ int moe_round(moe_handle* h, const moe_layer_w* layers, int32_t L, const uint16_
     }
     if (cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal) != cudaSuccess)
       return MOE_ECUDA;
-    int32_t n = 0;
-    cudaError_t e = enqueue_round(h, layers, L, x_bf16, rows, out, stats, ws, st, &n, true);
+    cudaError_t e = launch_round(h, a, st, true);
     cudaGraph_t graph = nullptr;
     cudaError_t e2 = cudaStreamEndCapture(st, &graph);
     if (e != cudaSuccess || e2 != cudaSuccess || !graph) {
@@ -880,7 +1045,7 @@ int moe_round(moe_handle* h, const moe_layer_w* layers, int32_t L, const uint16_
       return MOE_ECUDA;
     }
     h->gkey = key;
-    h->graph_launches = n;
+    h->graph_launches = 1;
   }
   if (cudaGraphLaunch(h->gexec, st) != cudaSuccess) return MOE_ECUDA;
   h->last_launches = h->graph_launches;
@@ -899,5 +1064,70 @@ int moe_last_device_status(moe_handle* h, void* stream) {
 }
 
 int32_t moe_last_launch_count(const moe_handle* h) { return h ? h->last_launches : 0; }
+
+int moe_profile(moe_handle* h, int enable) {
+  if (!h) return MOE_EINVAL;
+  h->profiling = enable != 0;
+  h->ev_used = 0;
+  h->phase_layers = 0;
+  if (h->profiling && !h->phase_ts) {
+    DeviceGuard g(h->device);
+    if (!g.ok) return MOE_ECUDA;
+    const size_t n = (size_t)kMaxLayers * kPhases * h->sm_count;
+    if (cudaMalloc(&h->phase_ts, n * sizeof(long long)) != cudaSuccess) {
+      cudaGetLastError();
+      h->phase_ts = nullptr;
+      return MOE_ECUDA;
+    }
+  }
+  return MOE_OK;
+}
+
+int moe_profile_read(moe_handle* h, int kind, double* total_ms, int32_t* launches) {
+  if (!h || !total_ms || !launches || kind != 0) return MOE_EINVAL;
+  DeviceGuard g(h->device);
+  if (!g.ok) return MOE_ECUDA;
+  double t = 0.0;
+  int32_t n = 0;
+  for (size_t i = 0; i + 1 < h->ev_used; i += 2) {
+    if (cudaEventSynchronize(h->ev[i + 1]) != cudaSuccess) return MOE_ECUDA;
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, h->ev[i], h->ev[i + 1]) != cudaSuccess) return MOE_ECUDA;
+    t += ms;
+    ++n;
+  }
+  *total_ms = t;
+  *launches = n;
+  return MOE_OK;
+}
+
+int moe_profile_phases(moe_handle* h, double* mean_us, double* max_us, int32_t n_phases) {
+  if (!h || !mean_us || !max_us || n_phases < kPhases - 1) return MOE_EINVAL;
+  if (!h->phase_ts || h->phase_layers < 1) return MOE_EINVAL;
+  DeviceGuard g(h->device);
+  if (!g.ok) return MOE_ECUDA;
+  const int G = h->sm_count, L = h->phase_layers;
+  std::vector<long long> ts((size_t)L * kPhases * G);
+  if (cudaDeviceSynchronize() != cudaSuccess ||
+      cudaMemcpy(ts.data(), h->phase_ts, ts.size() * sizeof(long long), cudaMemcpyDeviceToHost) !=
+          cudaSuccess)
+    return MOE_ECUDA;
+  for (int p = 0; p + 1 < kPhases; ++p) {
+    double sum = 0.0, mx = 0.0;
+    for (int l = 0; l < L; ++l) {
+      double lmax = 0.0;
+      for (int c = 0; c < G; ++c) {
+        const double d = (double)(ts[((size_t)l * kPhases + p + 1) * G + c] -
+                                  ts[((size_t)l * kPhases + p) * G + c]) * 1e-3;
+        sum += d;
+        if (d > lmax) lmax = d;
+      }
+      mx += lmax;
+    }
+    mean_us[p] = sum / ((double)L * G);
+    max_us[p] = mx / L;
+  }
+  return MOE_OK;
+}
 
 }  // extern "C"

@@ -54,7 +54,7 @@ def run_layer(s, layer, xb):
     mv.moe_decode_layer(s.handle, s.layers[layer].w, x.data_ptr(), R, out.data_ptr(), ws.data_ptr(),
                         ws.numel(), st)
     assert mv.moe_last_device_status(s.handle, st) == mv.MOE_OK
-    assert mv.moe_last_launch_count(s.handle) == 3
+    assert mv.moe_last_launch_count(s.handle) == 1
     return out.cpu().numpy()
 
 
