@@ -84,7 +84,7 @@ typedef struct moe_handle moe_handle;
 /* Validates dims and binds a handle to `device` (queries its SM count, allocates a
  * 4-byte device status word -- the only device allocation the library makes).
  * Supported: hidden a multiple of 256 in [256, 2048], inter a multiple of 32 in
- * [32, 4096], 1 <= top_k <= min(n_experts, 32), n_experts <= 1024, 1 <= max_rows <= 32.
+ * [32, 4096], 1 <= top_k <= min(n_experts, 32), n_experts <= 512, 1 <= max_rows <= 32.
  * MOE_EINVAL for dims that make no sense, MOE_EUNSUPPORTED for sizes outside those
  * ranges, MOE_ECUDA if the device cannot be used.  *out is NULL on failure. */
 int moe_create(const moe_dims* dims, int device, moe_handle** out);
@@ -158,8 +158,8 @@ int moe_set_wait_limit_ns(moe_handle* h, uint64_t ns);
  * and the launch count (kind must be 0: the fused round kernel).
  * moe_profile_phases returns, for the last profiled moe_round, the mean over CTAs and
  * layers (mean_us) and the per-layer maximum over CTAs averaged over layers (max_us)
- * of six phases: router GEMV, barrier 1, routing, expert stream, barrier 2, reduction.
- * n_phases must be >= 6. */
+ * of eight phases: router GEMV, barrier 1, routing, wait for the first staged expert
+ * item, expert stream, barrier 2, reduction, barrier 3.  n_phases must be >= 8. */
 int moe_profile(moe_handle* h, int enable);
 int moe_profile_read(moe_handle* h, int kind, double* total_ms, int32_t* launches);
 int moe_profile_phases(moe_handle* h, double* mean_us, double* max_us, int32_t n_phases);

@@ -26,7 +26,7 @@ ABI_SYMBOLS = (
     "moe_profile_phases", "moe_strerror",
 )
 KIND_ROUND = 0
-PHASES = ("router", "barrier1", "routing", "experts", "barrier2", "reduce")
+PHASES = ("router", "barrier1", "routing", "first_data", "experts", "barrier2", "reduce", "barrier3")
 
 
 class moe_dims(ctypes.Structure):

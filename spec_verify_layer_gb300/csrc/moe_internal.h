@@ -11,7 +11,7 @@ namespace moe {
 
 constexpr int kSlice = 32;     // intermediate rows per expert work item (one down K-block)
 constexpr int kMaxRows = 32;   // rows are tracked in 32-bit masks
-constexpr int kMaxExperts = 1024;
+constexpr int kMaxExperts = 512;   // routing keeps 16 logits per lane in registers
 constexpr int kMaxTopK = 32;
 constexpr int kMinHidden = 256, kMaxHidden = 2048;
 constexpr int kMaxInter = 4096;

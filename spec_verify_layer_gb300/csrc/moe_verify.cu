@@ -50,7 +50,7 @@ constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // 2 s
 // ns (at ~2 GHz) and a few times ns at lower clocks
 constexpr long long kCyclesPerNs = 2;
 constexpr long long kDefaultWaitCycles = (long long)kDefaultWaitNs * kCyclesPerNs;
-constexpr int kPhases = 7;  // phase stamps per layer when profiling
+constexpr int kPhases = 9;  // phase stamps per layer when profiling (8 intervals)
 
 struct LayerPtrs {
   const float* router;
@@ -66,7 +66,7 @@ struct RoundArgs {
   const uint16_t* x;  // [L][R][H] bf16 bits
   float* out;         // [L][R][H]
   int* stats;         // [L] |U| per layer, or null
-  unsigned* bar;      // [0] barrier arrivals, [1] abort flag
+  unsigned* bar;      // [0] barrier arrivals, [33] abort flag
   float* logits;      // [R][E]
   float* partial;     // [R*k][I/32][H]
   int* user_ids;      // moe_route outputs (CTA 0 writes them)
@@ -200,23 +200,41 @@ __device__ __forceinline__ float slot_scale(int m) {
   return __int_as_float((127 + e) << 23);
 }
 
-// acc += the 8 nibbles of w times xs[4] (pre-scaled pairs), slot pairs (0,1) (2,3) (4,5) (6,7)
-__device__ __forceinline__ void dot8x2(uint32_t w, const f2_t* xs, f2_t& acc) {
-  const uint32_t t = w >> 12;
-  ffma2(acc, f2pack(__uint_as_float(w & 0x0000000Fu), __uint_as_float(w & 0x000000F0u)), xs[0]);
-  ffma2(acc, f2pack(__uint_as_float(w & 0x00000F00u), __uint_as_float(w & 0x0000F000u)), xs[1]);
-  ffma2(acc, f2pack(__uint_as_float(w & 0x000F0000u), __uint_as_float(t & 0x00000F00u)), xs[2]);
-  ffma2(acc, f2pack(__uint_as_float(t & 0x0000F000u), __uint_as_float(t & 0x000F0000u)), xs[3]);
+// A 16-byte block is handled as two 64-bit word pairs D0 = {w0, w1}, D1 = {w2, w3} (and
+// the same shifted right by 12 in each half).  ANDing a pair with a slot mask isolates
+// slot m of two words at once -- elements (m, 8+m) of D0 and (16+m, 24+m) of D1 -- as
+// two subnormal floats already laid out as an f32x2 operand.  Activations are kept as
+// matching pairs: xp[m] = (x'[m], x'[8+m]) and xp[8+m] = (x'[16+m], x'[24+m]).
+struct BlockPairs {
+  f2_t d0, d1, t0, t1;
+};
+
+__device__ __forceinline__ BlockPairs block_pairs(const uint4 nb) {
+  BlockPairs b;
+  asm("mov.b64 %0, {%1,%2};" : "=l"(b.d0) : "r"(nb.x), "r"(nb.y));
+  asm("mov.b64 %0, {%1,%2};" : "=l"(b.d1) : "r"(nb.z), "r"(nb.w));
+  asm("mov.b64 %0, {%1,%2};" : "=l"(b.t0) : "r"(nb.x >> 12), "r"(nb.y >> 12));
+  asm("mov.b64 %0, {%1,%2};" : "=l"(b.t1) : "r"(nb.z >> 12), "r"(nb.w >> 12));
+  return b;
 }
 
-// 2^-62 * sum_{k<32} n_k x_k for one 16-byte block of codes; xs = 16 pre-scaled pairs.
-__device__ __forceinline__ float dot32(const uint4 nb, const f2_t* xs) {
-  f2_t a0 = 0ull, a1 = 0ull;
-  dot8x2(nb.x, xs + 0, a0);
-  dot8x2(nb.y, xs + 4, a1);
-  dot8x2(nb.z, xs + 8, a0);
-  dot8x2(nb.w, xs + 12, a1);
-  return __fadd_rn(f2sum(a0), f2sum(a1));
+// slot m's mask in both halves; slots 5..7 are read from the shifted pair
+__device__ __forceinline__ f2_t slot_pair(const BlockPairs& b, int half, int m) {
+  constexpr f2_t M[5] = {0x0000000F0000000Full, 0x000000F0000000F0ull, 0x00000F0000000F00ull,
+                         0x0000F0000000F000ull, 0x000F0000000F0000ull};
+  const f2_t d = half ? b.d1 : b.d0;
+  const f2_t t = half ? b.t1 : b.t0;
+  return (m <= 4) ? (d & M[m]) : (t & M[m - 3]);
+}
+
+// Pre-scaled activation pairs of one 32-element block from 32 floats v[k]:
+// xp[8h + m] = (v[16h + m] * scale(m), v[16h + 8 + m] * scale(m)).
+__device__ __forceinline__ void make_pairs(const float* v, f2_t* xp) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+#pragma unroll
+    for (int m = 0; m < 8; ++m)
+      xp[8 * h + m] = f2pack(v[16 * h + m] * slot_scale(m), v[16 * h + 8 + m] * slot_scale(m));
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
@@ -240,30 +258,38 @@ struct Sync {
   unsigned epoch = 0;
 };
 
-// Returns false if the round must be abandoned (a CTA gave up somewhere).
+// Each CTA's thread 0 adds 1 to one counter with release semantics (ordering the CTA's
+// earlier writes, published to it by the CTA barrier) and polls the counter with
+// acquire loads until every CTA of this epoch has arrived.  On this GPU that costs
+// about 1.2-1.4 us across both dies; a separate release flag, flag arrays, split
+// counters and cluster-first hierarchies all measured slower.  Returns false if the
+// round must be abandoned.
+__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 __device__ bool grid_sync(const RoundArgs& a, Sync& sy) {
   __shared__ int s_ok;
   __syncthreads();
   if (threadIdx.x == 0) {
     sy.epoch += 1;
     const unsigned target = sy.epoch * gridDim.x;
-    __threadfence();
-    atomicAdd(a.bar, 1u);
+    unsigned* abort_flag = a.bar + 33;
+    red_release_add(a.bar, 1u);
     int ok = 1;
     const long long t0 = clock64();
     while (ld_acquire(a.bar) < target) {
-      if (ld_relaxed(a.bar + 1)) {
+      if (ld_relaxed(abort_flag)) {
         ok = 0;
         break;
       }
       if (clock64() - t0 > a.wait_cycles) {
         atomicOr(a.status, kStatusTimeout);
-        atomicExch(a.bar + 1, 1u);
+        atomicExch(abort_flag, 1u);
         ok = 0;
         break;
       }
     }
-    __threadfence();
     s_ok = ok;
   }
   __syncthreads();
@@ -278,45 +304,54 @@ __device__ __forceinline__ void stamp(const RoundArgs& a, int l, int ph) {
 // ---------------------------------------------------------------------------------
 // P1: router logits, one warp per expert, canonical order
 
-// Lane l accumulates elements 128c + 4l + j for c ascending.  The c-loop runs in groups
-// of 8 (32 weights per lane in registers); for H > 1024 each lane's partial of every
-// row is carried between groups in `carry` (idle staging memory), so the order of the
-// fmas is exactly the canonical one.
-__device__ void router_phase(const RoundArgs& a, const float* router, const uint16_t* x,
-                             float* carry_all) {
+// Router rows owned by this CTA: experts e = CTA + grid * q (q = 0, 1, ...).  They are
+// staged into shared memory by one bulk copy per row, issued as soon as the previous
+// layer's expert stream is done (router weights do not depend on any data).
+__device__ __forceinline__ int router_rows_of_cta(int E) {
+  return (E - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+}
+
+__device__ void issue_router_rows(const RoundArgs& a, const float* router, float* s_rw,
+                                  uint32_t bar) {
+  const int n = router_rows_of_cta(a.E);
+  if (n <= 0) return;
+  const uint32_t row_bytes = (uint32_t)a.H * 4u;
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  mbar_expect_tx(bar, row_bytes * (uint32_t)n);
+  for (int q = 0; q < n; ++q) {
+    const int e = blockIdx.x + gridDim.x * q;
+    bulk_g2s(smem_u32(s_rw + (size_t)q * a.H), router + (size_t)e * a.H, row_bytes, bar);
+  }
+}
+
+// Lane l accumulates elements 128c + 4l + j for c ascending, then the xor-butterfly.
+// Warp q of the CTA computes its staged row q for every activation row.
+__device__ void router_phase(const RoundArgs& a, const uint16_t* x, const float* s_rw) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int NC = a.H >> 7;  // <= 16
-  const int gw = blockIdx.x * NW + warp;
-  float* carry = carry_all + (size_t)warp * a.R * 32;
-  for (int e = gw; e < a.E; e += gridDim.x * NW) {
-    const float4* wr = reinterpret_cast<const float4*>(router + (size_t)e * a.H) + lane;
-    for (int g = 0; g < NC; g += 8) {
-      float4 wv[8];
+  const int n = router_rows_of_cta(a.E);
+  for (int q = warp; q < n; q += NW) {
+    const int e = blockIdx.x + gridDim.x * q;
+    const float4* wr = reinterpret_cast<const float4*>(s_rw + (size_t)q * a.H) + lane;
+    for (int r = 0; r < a.R; ++r) {
+      const uint2* xr = reinterpret_cast<const uint2*>(x + (size_t)r * a.H) + lane;
+      uint2 xv[16];
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
-        if (g + c < NC) wv[c] = __ldg(wr + 32 * (g + c));
-      const bool last = g + 8 >= NC;
-      for (int r = 0; r < a.R; ++r) {
-        const uint2* xr = reinterpret_cast<const uint2*>(x + (size_t)r * a.H) + lane;
-        float p = (g == 0) ? 0.f : carry[r * 32 + lane];
+      for (int c = 0; c < 16; ++c)
+        if (c < NC) xv[c] = __ldg(xr + 32 * c);
+      float p = 0.f;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          if (g + c < NC) {
-            const uint2 xv = __ldg(xr + 32 * (g + c));
-            p = __fmaf_rn(wv[c].x, bf16_lo(xv.x), p);
-            p = __fmaf_rn(wv[c].y, bf16_hi(xv.x), p);
-            p = __fmaf_rn(wv[c].z, bf16_lo(xv.y), p);
-            p = __fmaf_rn(wv[c].w, bf16_hi(xv.y), p);
-          }
-        }
-        if (!last) {
-          carry[r * 32 + lane] = p;
-        } else {
-          p = warp_sum(p);
-          if (lane == 0) a.logits[(size_t)r * a.E + e] = p;
+      for (int c = 0; c < 16; ++c) {
+        if (c < NC) {
+          const float4 w = wr[32 * c];
+          p = __fmaf_rn(w.x, bf16_lo(xv[c].x), p);
+          p = __fmaf_rn(w.y, bf16_hi(xv[c].x), p);
+          p = __fmaf_rn(w.z, bf16_lo(xv[c].y), p);
+          p = __fmaf_rn(w.w, bf16_hi(xv[c].y), p);
         }
       }
-      __syncwarp();
+      p = warp_sum(p);
+      if (lane == 0) a.logits[(size_t)r * a.E + e] = p;
     }
   }
 }
@@ -332,46 +367,82 @@ struct Tables {
   int* n_union;  // [1]
 };
 
+// True if (ka, ia) ranks before (kb, ib): larger key, then lower id.
+__device__ __forceinline__ bool ranks_before(unsigned ka, int ia, unsigned kb, int ib) {
+  return ka > kb || (ka == kb && ia < ib);
+}
+
+// Top-k of one row of logits by one warp.  Lane l owns experts l + 32t (t < NE), kept
+// sorted best-first in registers (bitonic network); each of the k rounds takes the
+// warp-wide best head (redux.sync max on the key, then min on the id among equal
+// keys) and the owning lane pops it.  Lane j returns pick j (logit and id).
+template <int NE>
+__device__ __forceinline__ void select_row(const float* row, int E, int k, int lane, float& my_l,
+                                           int& my_id) {
+  unsigned kk[NE];
+  int id[NE];
+#pragma unroll
+  for (int t = 0; t < NE; ++t) {
+    const int e = lane + 32 * t;
+    id[t] = e;
+    kk[t] = (e < E) ? order_key(__ldcg(row + e)) : 0u;
+  }
+#pragma unroll
+  for (int size = 2; size <= NE; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+#pragma unroll
+      for (int i = 0; i < NE; ++i) {
+        const int j = i ^ stride;
+        if (j > i) {
+          const bool up = (i & size) == 0;  // this block sorts best-first
+          const bool sw = up ? ranks_before(kk[j], id[j], kk[i], id[i])
+                             : ranks_before(kk[i], id[i], kk[j], id[j]);
+          if (sw) {
+            const unsigned tk = kk[i];
+            kk[i] = kk[j];
+            kk[j] = tk;
+            const int ti = id[i];
+            id[i] = id[j];
+            id[j] = ti;
+          }
+        }
+      }
+    }
+  }
+  for (int j = 0; j < k; ++j) {
+    const unsigned m = __reduce_max_sync(0xffffffffu, kk[0]);
+    const unsigned cand = (kk[0] == m) ? (unsigned)id[0] : 0xffffffffu;
+    const unsigned win = __reduce_min_sync(0xffffffffu, cand);
+    if ((unsigned)id[0] == win) {
+#pragma unroll
+      for (int t = 0; t + 1 < NE; ++t) {
+        kk[t] = kk[t + 1];
+        id[t] = id[t + 1];
+      }
+      kk[NE - 1] = 0u;
+      id[NE - 1] = INT_MAX;
+    }
+    if (lane == j) {
+      my_l = key_value(m);
+      my_id = (int)win;
+    }
+  }
+}
+
 // scratch (inside the staging area, free while routing): mask [E], off_e [E], ids [R*k]
 __device__ int route_phase(const RoundArgs& a, const Tables& T, unsigned* s_mask, int* s_off_e,
                            int* s_ids, int layer) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int E = a.E, k = a.k, R = a.R;
   for (int e = tid; e < E; e += NT) s_mask[e] = 0u;
-  const int NE = (E + 31) >> 5;  // <= 32
   for (int r = warp; r < R; r += NW) {
-    unsigned key[32];
-#pragma unroll
-    for (int t = 0; t < 32; ++t) {
-      if (t < NE) {
-        const int e = lane + 32 * t;
-        key[t] = (e < E) ? order_key(__ldcg(a.logits + (size_t)r * E + e)) : 0u;
-      }
-    }
     float my_l = 0.f;
     int my_id = 0;
-    for (int j = 0; j < k; ++j) {
-      unsigned bk = 0u;
-      int bt = 0;
-#pragma unroll
-      for (int t = 0; t < 32; ++t)
-        if (t < NE && key[t] > bk) {  // strict: the first (lowest id) of equal keys stays
-          bk = key[t];
-          bt = t;
-        }
-      const unsigned m = __reduce_max_sync(0xffffffffu, bk);
-      const unsigned cand = (bk == m && m != 0u) ? (unsigned)(lane + 32 * bt) : 0xffffffffu;
-      const unsigned win = __reduce_min_sync(0xffffffffu, cand);
-      if ((int)(win & 31u) == lane) {
-#pragma unroll
-        for (int t = 0; t < 32; ++t)
-          if (t == (int)(win >> 5)) key[t] = 0u;
-      }
-      if (lane == j) {
-        my_l = key_value(m);
-        my_id = (int)win;
-      }
-    }
+    if (E <= 128)
+      select_row<4>(a.logits + (size_t)r * E, E, k, lane, my_l, my_id);
+    else  // E <= 512 (moe_create rejects more)
+      select_row<16>(a.logits + (size_t)r * E, E, k, lane, my_l, my_id);
     // weights: exp(l_j - l_1) / sum over the k picks, summed in rank order
     const float l1 = __shfl_sync(0xffffffffu, my_l, 0);
     const float ex = (lane < k) ? expf(my_l - l1) : 0.f;
@@ -479,6 +550,136 @@ __device__ void issue_item(const RoundArgs& a, const LayerPtrs& W, const Stage& 
 }
 
 // Computes one staged item for every row of its expert.  Returns false on a timeout.
+// Computes a group of G rows (pairs g0..g0+G-1 of the item's expert) against the staged
+// item: gate/up for all 64 weight rows, SwiGLU, down partials.  Every extracted weight
+// pair feeds the G rows, so the integer work is shared.  Ends with a CTA barrier.
+template <int NBL, int G>
+__device__ void compute_group(const RoundArgs& a, const Tables& T, const Stage& st, int pp0, int s,
+                              const uint16_t* x, float* s_gv, float* s_h, float* s_hsum,
+                              bool first_down_wait_done) {
+  const int H = a.H, NB = H >> 5, NS = a.I >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint8_t* s_gu = st.base;
+  const uint16_t* s_gus = reinterpret_cast<const uint16_t*>(st.base + 32 * (size_t)H);
+  const uint8_t* s_dn = st.base + 36 * (size_t)H;
+  const uint16_t* s_dns = reinterpret_cast<const uint16_t*>(st.base + 52 * (size_t)H);
+  int pair[G], row[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    pair[g] = T.pair[pp0 + g];
+    row[g] = pair[g] / a.k;
+  }
+  // ---- gate / up: warp per weight row, lane per 32-element block ----
+  constexpr int RPW = 64 / NW;
+  float part[RPW][G];
+#pragma unroll
+  for (int q = 0; q < RPW; ++q)
+#pragma unroll
+    for (int g = 0; g < G; ++g) part[q][g] = 0.f;
+#pragma unroll
+  for (int t = 0; t < NBL; ++t) {
+    const int blk = lane + 32 * t;
+    if (blk < NB) {
+      f2_t xp[G][16];
+      float xsum8[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        // elements 16h + m and 16h + 8 + m come from 16-byte loads 2h and 2h + 1
+        const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)row[g] * H + 32 * blk);
+        float sum = 0.f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint4 ua = __ldg(src + 2 * h), ub = __ldg(src + 2 * h + 1);
+          const uint32_t wa[4] = {ua.x, ua.y, ua.z, ua.w}, wb[4] = {ub.x, ub.y, ub.z, ub.w};
+#pragma unroll
+          for (int m = 0; m < 8; ++m) {
+            const float va = (m & 1) ? bf16_hi(wa[m >> 1]) : bf16_lo(wa[m >> 1]);
+            const float vb = (m & 1) ? bf16_hi(wb[m >> 1]) : bf16_lo(wb[m >> 1]);
+            xp[g][8 * h + m] = f2pack(va * slot_scale(m), vb * slot_scale(m));
+            sum = __fadd_rn(sum, va);
+            sum = __fadd_rn(sum, vb);
+          }
+        }
+        xsum8[g] = -8.f * sum;
+      }
+#pragma unroll
+      for (int q = 0; q < RPW; ++q) {
+        const int wr = warp + NW * q;
+        const uint4 nb = *reinterpret_cast<const uint4*>(s_gu + ((size_t)wr * NB + blk) * 16);
+        const float sc = half_bits(s_gus[wr * NB + blk]);
+        const BlockPairs bp = block_pairs(nb);
+        f2_t acc0[G], acc1[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) acc0[g] = acc1[g] = 0ull;
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+          const f2_t e0 = slot_pair(bp, 0, m), e1 = slot_pair(bp, 1, m);
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            ffma2(acc0[g], e0, xp[g][m]);
+            ffma2(acc1[g], e1, xp[g][8 + m]);
+          }
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float dot = __fadd_rn(f2sum(acc0[g]), f2sum(acc1[g]));
+          part[q][g] = __fmaf_rn(sc, __fmaf_rn(dot, 0x1p62f, xsum8[g]), part[q][g]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < RPW; ++q)
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float v = warp_sum(part[q][g]);
+      if (lane == 0) s_gv[(warp + NW * q) * 2 + g] = v;
+    }
+  __syncthreads();
+  // ---- SwiGLU on the slice's 32 intermediate rows, warp g for row g ----
+  if (warp < G) {
+    const float gg = s_gv[lane * 2 + warp], vv = s_gv[(32 + lane) * 2 + warp];
+    const float hh = __fmul_rn(__fdiv_rn(gg, __fadd_rn(1.f, expf(-gg))), vv);
+    s_h[warp * 32 + lane] = hh;
+    const float hs = warp_sum(hh);
+    if (lane == 0) s_hsum[warp] = -8.f * hs;
+  }
+  __syncthreads();
+  (void)first_down_wait_done;
+  // ---- down partials: thread per output row, one 32-element K-block each ----
+  f2_t hp[G][16];
+  float hsum8[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    make_pairs(s_h + 32 * g, hp[g]);
+    hsum8[g] = s_hsum[g];
+  }
+  for (int o = tid; o < H; o += NT) {
+    const uint4 nb = *reinterpret_cast<const uint4*>(s_dn + (size_t)o * 16);
+    const float sc = half_bits(s_dns[o]);
+    const BlockPairs bp = block_pairs(nb);
+    f2_t acc0[G], acc1[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) acc0[g] = acc1[g] = 0ull;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const f2_t e0 = slot_pair(bp, 0, m), e1 = slot_pair(bp, 1, m);
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        ffma2(acc0[g], e0, hp[g][m]);
+        ffma2(acc1[g], e1, hp[g][8 + m]);
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float dot = __fadd_rn(f2sum(acc0[g]), f2sum(acc1[g]));
+      a.partial[((size_t)pair[g] * NS + s) * H + o] = __fmul_rn(sc, __fmaf_rn(dot, 0x1p62f, hsum8[g]));
+    }
+  }
+  // the next group's gate/up may overwrite s_gv / s_h only after everyone is done here
+  __syncthreads();
+}
+
 // Stage b's state lives in two bitfields: `ph` holds the parity to wait for (bit 2b:
 // gate/up barrier A, bit 2b+1: down barrier B) and `pend` marks copies in flight.  On
 // success both barriers have been consumed (parities flipped, pending bits cleared);
@@ -486,155 +687,90 @@ __device__ void issue_item(const RoundArgs& a, const LayerPtrs& W, const Stage& 
 template <int NBL>
 __device__ bool compute_item(const RoundArgs& a, const Tables& T, const Stage& st, int b,
                              unsigned& ph, unsigned& pend, int ui, int s, const uint16_t* x,
-                             float* s_gv, float* s_h, float* s_hsum) {
-  const int H = a.H, NB = H >> 5, NS = a.I >> 5;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const uint8_t* s_gu = st.base;
-  const uint16_t* s_gus = reinterpret_cast<const uint16_t*>(st.base + 32 * (size_t)H);
-  const uint8_t* s_dn = st.base + 36 * (size_t)H;
-  const uint16_t* s_dns = reinterpret_cast<const uint16_t*>(st.base + 52 * (size_t)H);
-
+                             float* s_gv, float* s_h, float* s_hsum, int stamp_layer) {
   const unsigned bit_a = 1u << (2 * b), bit_b = 2u << (2 * b);
   bool ok = mbar_wait_bounded(st.bar_a, (ph & bit_a) ? 1u : 0u, a.status, a.wait_cycles);
   if (__syncthreads_or(!ok)) return false;
   ph ^= bit_a;
   pend &= ~bit_a;
-  bool have_b = false;
+  if (stamp_layer >= 0) stamp(a, stamp_layer, 4);
+  // the down block is needed only after the first group's gate/up; wait for it here
+  // (gate/up of the first group then overlaps nothing, but keeps the control simple)
+  ok = mbar_wait_bounded(st.bar_b, (ph & bit_b) ? 1u : 0u, a.status, a.wait_cycles);
+  if (__syncthreads_or(!ok)) return false;
+  ph ^= bit_b;
+  pend &= ~bit_b;
   const int p0 = T.csr_off[ui], p1 = T.csr_off[ui + 1];
-  for (int pp = p0; pp < p1; ++pp) {
-    const int pair = T.pair[pp];
-    const int r = pair / a.k;
-    // ---- gate / up: warp per weight row, lane per 32-element block ----
-    // 64 weight rows (32 gate, 32 up) over NW warps; the lane's blocks are visited one
-    // at a time so only one block of pre-scaled activations sits in registers.
-    constexpr int RPW = 64 / NW;
-    float part[RPW];
-#pragma unroll
-    for (int q = 0; q < RPW; ++q) part[q] = 0.f;
-#pragma unroll
-    for (int t = 0; t < NBL; ++t) {
-      const int blk = lane + 32 * t;
-      if (blk < NB) {
-        f2_t xs[16];
-        float sum = 0.f;
-        const uint4* xp = reinterpret_cast<const uint4*>(x + (size_t)r * H + 32 * blk);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint4 v = __ldg(xp + q);
-          const uint32_t wds[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int z = 0; z < 4; ++z) {
-            const float lo = bf16_lo(wds[z]), hi = bf16_hi(wds[z]);
-            const int k0 = 8 * q + 2 * z;  // element index in the block; slots k0&7, +1
-            xs[k0 >> 1] = f2pack(lo * slot_scale(k0 & 7), hi * slot_scale((k0 + 1) & 7));
-            sum = __fadd_rn(sum, lo);
-            sum = __fadd_rn(sum, hi);
-          }
-        }
-        const float xsum8 = -8.f * sum;
-#pragma unroll
-        for (int q = 0; q < RPW; ++q) {
-          const int wr = warp + NW * q;
-          const uint4 nb = *reinterpret_cast<const uint4*>(s_gu + ((size_t)wr * NB + blk) * 16);
-          const float sc = half_bits(s_gus[wr * NB + blk]);
-          const float acc = dot32(nb, xs);
-          part[q] = __fmaf_rn(sc, __fmaf_rn(acc, 0x1p62f, xsum8), part[q]);
-        }
-      }
-    }
-#pragma unroll
-    for (int q = 0; q < RPW; ++q) {
-      const float v = warp_sum(part[q]);
-      if (lane == 0) s_gv[warp + NW * q] = v;
-    }
-    __syncthreads();
-    // ---- SwiGLU on the slice's 32 intermediate rows ----
-    if (warp == 0) {
-      const float g = s_gv[lane], v = s_gv[32 + lane];
-      const float hh = __fmul_rn(__fdiv_rn(g, __fadd_rn(1.f, expf(-g))), v);
-      s_h[lane] = hh * slot_scale(lane & 7);
-      const float hs = warp_sum(hh);
-      if (lane == 0) *s_hsum = -8.f * hs;
-    }
-    if (!have_b) {
-      ok = mbar_wait_bounded(st.bar_b, (ph & bit_b) ? 1u : 0u, a.status, a.wait_cycles);
-      if (__syncthreads_or(!ok)) return false;
-      ph ^= bit_b;
-      pend &= ~bit_b;
-      have_b = true;
-    } else {
-      __syncthreads();
-    }
-    // ---- down partial: thread per output row, one 32-element K-block each ----
-    f2_t hreg[16];
-#pragma unroll
-    for (int q = 0; q < 16; ++q) hreg[q] = f2pack(s_h[2 * q], s_h[2 * q + 1]);
-    const float hsum8 = *s_hsum;
-    float* dst = a.partial + ((size_t)pair * NS + s) * H;
-    for (int o = tid; o < H; o += NT) {
-      const uint4 nb = *reinterpret_cast<const uint4*>(s_dn + (size_t)o * 16);
-      const float sc = half_bits(s_dns[o]);
-      const float acc = dot32(nb, hreg);
-      dst[o] = __fmul_rn(sc, __fmaf_rn(acc, 0x1p62f, hsum8));
-    }
-    // the next row's gate/up may overwrite s_gv only after everyone has read s_h
-    __syncthreads();
-  }
-  if (!have_b) {  // (every union expert has a row, so this only keeps phases paired)
-    ok = mbar_wait_bounded(st.bar_b, (ph & bit_b) ? 1u : 0u, a.status, a.wait_cycles);
-    if (__syncthreads_or(!ok)) return false;
-    ph ^= bit_b;
-    pend &= ~bit_b;
-  }
+  int pp = p0;
+  for (; pp + 2 <= p1; pp += 2) compute_group<NBL, 2>(a, T, st, pp, s, x, s_gv, s_h, s_hsum, true);
+  if (pp < p1) compute_group<NBL, 1>(a, T, st, pp, s, x, s_gv, s_h, s_hsum, true);
   return true;
 }
 
 // ---------------------------------------------------------------------------------
 // P4: fixed-order weighted reduction of the partials into the layer output
 
-__device__ void reduce_phase(const RoundArgs& a, const Tables& T, float* out) {
+// Tile = (row r, 32 consecutive outputs).  Unit u = (rank j, part): a warp sums the
+// partials of slices s = part, part + jw, ... for its 32 outputs (coalesced), then warp
+// 0 combines: y_j = sum over parts in order, out = sum_j w_j y_j in rank order.
+__device__ void reduce_phase(const RoundArgs& a, const Tables& T, float* out, float* s_red) {
   const int H = a.H, k = a.k, NS = a.I >> 5;
-  int kp = 1;
-  while (kp < k) kp <<= 1;  // lanes per output; kp divides 32
-  const int lane = threadIdx.x & 31;
-  const int gbase = lane & ~(kp - 1);
-  const long long total = (long long)a.R * H * kp;
-  for (long long t = (long long)blockIdx.x * NT + threadIdx.x; t < total;
-       t += (long long)gridDim.x * NT) {
-    const int j = (int)(t & (kp - 1));
-    const long long ro = t / kp;
-    const int r = (int)(ro / H), o = (int)(ro - (long long)r * H);
-    float y = 0.f;
-    if (j < k) {
-      const float* src = a.partial + (size_t)(r * k + j) * NS * H + o;
-      for (int s = 0; s < NS; ++s) y = __fadd_rn(y, __ldcg(src + (size_t)s * H));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int jw = (NW / k) > 0 ? (NW / k) : 1;  // warps per rank
+  const int units = k * jw;
+  const int tiles_per_row = H >> 5;
+  const int n_tiles = a.R * tiles_per_row;
+  for (int q = blockIdx.x; q < n_tiles; q += gridDim.x) {
+    const int r = q / tiles_per_row;
+    const int o0 = (q - r * tiles_per_row) * 32;
+    for (int u = warp; u < units; u += NW) {
+      const int j = u / jw, part = u - (u / jw) * jw;
+      const float* src = a.partial + (size_t)(r * k + j) * NS * H + o0 + lane;
+      float y = 0.f;
+#pragma unroll 8
+      for (int s = part; s < NS; s += jw) y = __fadd_rn(y, __ldcg(src + (size_t)s * H));
+      s_red[u * 32 + lane] = y;
     }
-    float acc = 0.f;
-    for (int jj = 0; jj < k; ++jj) {
-      const float yj = __shfl_sync(0xffffffffu, y, gbase + jj);
-      acc = __fmaf_rn(T.w[r * k + jj], yj, acc);
+    __syncthreads();
+    if (warp == 0) {
+      float acc = 0.f;
+      for (int j = 0; j < k; ++j) {
+        float yj = 0.f;
+        for (int part = 0; part < jw; ++part) yj = __fadd_rn(yj, s_red[(j * jw + part) * 32 + lane]);
+        acc = __fmaf_rn(T.w[r * k + j], yj, acc);
+      }
+      out[(size_t)r * H + o0 + lane] = acc;
     }
-    if (j == 0) out[(size_t)r * H + o] = acc;
+    __syncthreads();
   }
 }
 
 // ---------------------------------------------------------------------------------
 // shared-memory plan
 
+constexpr size_t kRouterOffset = 8192;  // reduction scratch (<= 4 KB) sits below
+
 struct SmemPlan {
-  size_t stage, stage0, stage1, bars, gv, uni, csr, pair, w, nunion, total;
+  size_t stage, stage0, stage1, router, bars, gv, uni, csr, pair, w, nunion, total;
+  bool router_fits;
 };
 
 __host__ __device__ inline size_t up128(size_t x) { return (x + 127) & ~(size_t)127; }
 
-__host__ __device__ inline SmemPlan smem_plan(int H, int E, int R, int k) {
+// router_rows = experts per CTA, ceil(E / grid)
+__host__ __device__ inline SmemPlan smem_plan(int H, int E, int R, int k, int router_rows) {
   SmemPlan p{};
   p.stage = up128(stage_bytes(H));
   size_t off = 0;
   p.stage0 = off;  off += p.stage;
   p.stage1 = off;  off += p.stage;
+  // The next layer's router rows live in stage 1 after the reduction scratch: they are
+  // written after the last expert item of a layer and read before the next layer's
+  // first item, while the staging buffers are idle.
+  p.router = p.stage1 + kRouterOffset;
+  p.router_fits = kRouterOffset + (size_t)router_rows * H * 4 <= p.stage;
   p.bars = off;    off += 64;
-  p.gv = off;      off += up128((64 + 32 + 4) * 4);
+  p.gv = off;      off += up128((128 + 64 + 4) * 4);
   p.uni = off;     off += up128((size_t)E * 4);
   p.csr = off;     off += up128((size_t)(E + 1) * 4);
   p.pair = off;    off += up128((size_t)R * k * 4);
@@ -648,16 +784,18 @@ template <int NBL>
 __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundArgs a) {
   extern __shared__ __align__(1024) unsigned char smem[];
   const int tid = threadIdx.x;
-  const SmemPlan P = smem_plan(a.H, a.E, a.R, a.k);
+  const SmemPlan P = smem_plan(a.H, a.E, a.R, a.k, (a.E + (int)gridDim.x - 1) / (int)gridDim.x);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P.bars);
+  const uint32_t bar_router = smem_u32(bars + 4);
+  float* s_rw = reinterpret_cast<float*>(smem + P.router);
   // stage b: buffer at stage0 + b * stage, barriers bars[2b] (A) and bars[2b + 1] (B)
   auto stage_of = [&](int b) {
     return Stage{smem + P.stage0 + (size_t)b * P.stage, smem_u32(bars + 2 * b),
                  smem_u32(bars + 2 * b + 1)};
   };
-  float* s_gv = reinterpret_cast<float*>(smem + P.gv);
-  float* s_h = s_gv + 64;
-  float* s_hsum = s_h + 32;
+  float* s_gv = reinterpret_cast<float*>(smem + P.gv);  // [64 weight rows][2 group rows]
+  float* s_h = s_gv + 128;                               // [2][32] (unscaled)
+  float* s_hsum = s_h + 64;                              // [2]
   Tables T{reinterpret_cast<int*>(smem + P.uni), reinterpret_cast<int*>(smem + P.csr),
            reinterpret_cast<int*>(smem + P.pair), reinterpret_cast<float*>(smem + P.w),
            reinterpret_cast<int*>(smem + P.nunion)};
@@ -666,28 +804,53 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
   int* s_off_e = reinterpret_cast<int*>(smem + P.stage0 + (size_t)a.E * 4);
   int* s_ids = reinterpret_cast<int*>(smem + P.stage0 + (size_t)a.E * 8);
   if (tid == 0) {
-    for (int i = 0; i < 4; ++i) mbar_init(smem_u32(bars + i), 1);
+    for (int i = 0; i < 5; ++i) mbar_init(smem_u32(bars + i), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    issue_router_rows(a, a.layer[0].router, s_rw, bar_router);
   }
   __syncthreads();
+  unsigned ph_router = 0u;
+  bool router_pend = router_rows_of_cta(a.E) > 0;  // layer 0's rows are in flight
 
   Sync sy;
   unsigned ph = 0u;    // parity to wait for: bit 2b = stage b's barrier A, bit 2b+1 = B
   unsigned pend = 0u;  // copies in flight, same bit layout
+  // Leaving early: give every copy still in flight a bounded chance to land (so no
+  // bulk copy targets shared memory of an exited CTA), raise the abort flag, return.
+  auto bail = [&]() {
+    for (int q = 0; q < 4; ++q)
+      if (pend & (1u << q))
+        mbar_wait_bounded(smem_u32(bars + q), (ph >> q) & 1u, a.status, kDefaultWaitCycles);
+    if (router_pend) mbar_wait_bounded(bar_router, ph_router, a.status, kDefaultWaitCycles);
+    if (tid == 0) atomicExch(a.bar + 33, 1u);
+  };
   const int G = gridDim.x, NS = a.I >> 5;
   const size_t RH = (size_t)a.R * a.H;
   for (int l = 0; l < a.L; ++l) {
     const LayerPtrs& W = a.layer[l];
     const uint16_t* x = a.x + (size_t)l * RH;
     stamp(a, l, 0);
-    router_phase(a, W.router, x, reinterpret_cast<float*>(smem + P.stage0));
+    if (router_pend) {
+      const bool ok = mbar_wait_bounded(bar_router, ph_router, a.status, a.wait_cycles);
+      if (__syncthreads_or(!ok)) {
+        bail();
+        return;
+      }
+      ph_router ^= 1u;
+      router_pend = false;
+    }
+    router_phase(a, x, s_rw);
     stamp(a, l, 1);
-    if (!grid_sync(a, sy)) return;  // B1: all logits written
+    if (!grid_sync(a, sy)) {  // B1: all logits written
+      bail();
+      return;
+    }
     stamp(a, l, 2);
     const int U = route_phase(a, T, s_mask, s_off_e, s_ids, l);
     stamp(a, l, 3);
     if (a.route_only) return;
     const int n_items = U * NS;
+    if (blockIdx.x >= n_items) stamp(a, l, 4);  // no item: "first data" = now
     for (int n = 0; n < 2; ++n) {
       const int it = blockIdx.x + n * G;
       if (it < n_items) {
@@ -695,28 +858,13 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
         if (tid == 0) issue_item(a, W, stage_of(n), T.uni[it / NS], it % NS);
       }
     }
-    if (tid == 0) {
-      if (l + 1 < a.L) {  // the next layer's router weights do not depend on any data
-        const size_t bytes = (size_t)a.E * a.H * 4;
-        const size_t chunk = ((bytes / G) + 15) & ~(size_t)15;
-        const size_t b0 = (size_t)blockIdx.x * chunk;
-        if (b0 < bytes) {
-          const size_t n = (bytes - b0 < chunk) ? bytes - b0 : chunk;
-          prefetch_l2(reinterpret_cast<const char*>(a.layer[l + 1].router) + b0, (uint32_t)n);
-        }
-      }
-    }
     for (int n = 0;; ++n) {
       const int it = blockIdx.x + n * G;
       if (it >= n_items) break;
       const int b = n & 1;
       if (!compute_item<NBL>(a, T, stage_of(b), b, ph, pend, it / NS, it % NS, x, s_gv, s_h,
-                             s_hsum)) {
-        // give every copy still in flight a bounded chance to land, then leave
-        for (int q = 0; q < 4; ++q)
-          if (pend & (1u << q))
-            mbar_wait_bounded(smem_u32(bars + q), (ph >> q) & 1u, a.status, kDefaultWaitCycles);
-        if (tid == 0) atomicExch(a.bar + 1, 1u);
+                             s_hsum, n == 0 ? l : -1)) {
+        bail();
         return;
       }
       // compute_item ends with a CTA barrier: the stage is free again
@@ -726,12 +874,24 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
         if (tid == 0) issue_item(a, W, stage_of(b), T.uni[nxt / NS], nxt % NS);
       }
     }
-    stamp(a, l, 4);
-    if (!grid_sync(a, sy)) return;  // B2: all partials written
+    // the next layer's router rows can move in now: they do not depend on any data
+    if (l + 1 < a.L && router_rows_of_cta(a.E) > 0) {
+      router_pend = true;
+      if (tid == 0) issue_router_rows(a, a.layer[l + 1].router, s_rw, bar_router);
+    }
     stamp(a, l, 5);
-    reduce_phase(a, T, a.out + (size_t)l * RH);
+    if (!grid_sync(a, sy)) {  // B2: all partials written
+      bail();
+      return;
+    }
     stamp(a, l, 6);
-    if (l + 1 < a.L && !grid_sync(a, sy)) return;  // B3: layer output complete
+    reduce_phase(a, T, a.out + (size_t)l * RH, reinterpret_cast<float*>(smem + P.stage1));
+    stamp(a, l, 7);
+    if (l + 1 < a.L && !grid_sync(a, sy)) {  // B3: layer output complete
+      bail();
+      return;
+    }
+    stamp(a, l, 8);  // (the last layer has no B3: its interval is zero)
   }
 }
 
@@ -805,8 +965,8 @@ int check_layer(const moe_layer_w* w) {
   return MOE_OK;
 }
 
-size_t smem_bytes(const moe_dims& d, int rows) {
-  return smem_plan(d.hidden, d.n_experts, rows, d.top_k).total;
+size_t smem_bytes(const moe_dims& d, int rows, int grid) {
+  return smem_plan(d.hidden, d.n_experts, rows, d.top_k, (d.n_experts + grid - 1) / grid).total;
 }
 
 void fill_args(RoundArgs& a, const moe_handle* h, int rows, void* ws) {
@@ -845,7 +1005,7 @@ cudaError_t launch_round(moe_handle* h, const RoundArgs& a, cudaStream_t st, boo
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(h->sm_count);
   cfg.blockDim = dim3(NT);
-  cfg.dynamicSmemBytes = smem_bytes(h->dims, a.R);
+  cfg.dynamicSmemBytes = smem_bytes(h->dims, a.R, h->sm_count);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
@@ -886,8 +1046,6 @@ int moe_create(const moe_dims* dims, int device, moe_handle** out) {
   *out = nullptr;
   int rc = check_dims(dims);
   if (rc != MOE_OK) return rc;
-  const size_t smem = smem_bytes(*dims, dims->max_rows);
-  if (smem > 227 * 1024) return MOE_EUNSUPPORTED;
   int ndev = 0;
   if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) {
     cudaGetLastError();
@@ -895,13 +1053,21 @@ int moe_create(const moe_dims* dims, int device, moe_handle** out) {
   }
   DeviceGuard g(device);
   if (!g.ok) return MOE_ECUDA;
-  int coop = 0;
+  int coop = 0, sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, device) != cudaSuccess || !coop) {
+    cudaGetLastError();
+    return MOE_ECUDA;
+  }
+  const size_t smem = smem_bytes(*dims, dims->max_rows, sms);
+  const SmemPlan plan = smem_plan(dims->hidden, dims->n_experts, dims->max_rows, dims->top_k,
+                                  (dims->n_experts + sms - 1) / sms);
+  if (smem + 1024 > 227 * 1024 || !plan.router_fits) return MOE_EUNSUPPORTED;
   moe_handle* h = new moe_handle();
   h->dims = *dims;
   h->device = device;
-  if (cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
-      cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, device) != cudaSuccess || !coop ||
-      cudaMalloc(&h->status, sizeof(unsigned)) != cudaSuccess ||
+  h->sm_count = sms;
+  if (cudaMalloc(&h->status, sizeof(unsigned)) != cudaSuccess ||
       cudaMemset(h->status, 0, sizeof(unsigned)) != cudaSuccess) {
     cudaGetLastError();
     if (h->status) cudaFree(h->status);
