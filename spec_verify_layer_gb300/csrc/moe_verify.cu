@@ -42,7 +42,7 @@
 namespace moe {
 namespace {
 
-constexpr int NT = 512;  // threads per CTA
+constexpr int NT = 256;  // threads per CTA
 constexpr int NW = NT / 32;
 constexpr unsigned kStatusTimeout = 1u;
 constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // 2 s
@@ -550,110 +550,137 @@ __device__ void issue_item(const RoundArgs& a, const LayerPtrs& W, const Stage& 
 }
 
 // Computes one staged item for every row of its expert.  Returns false on a timeout.
-// Computes a group of G rows (pairs g0..g0+G-1 of the item's expert) against the staged
-// item: gate/up for all 64 weight rows, SwiGLU, down partials.  Every extracted weight
-// pair feeds the G rows, so the integer work is shared.  Ends with a CTA barrier.
+// Activation pairs of one 32-element block of one row (see make_pairs), built from
+// the row's bf16 values, plus -8 * (sum of the block's 32 values).
+struct XBlock {
+  f2_t xp[16];
+  float xsum8;
+};
+
+__device__ __forceinline__ void load_xblock(const uint16_t* x, int H, int row, int blk, XBlock& xb) {
+  // elements 16h + m and 16h + 8 + m come from 16-byte loads 2h and 2h + 1
+  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)row * H + 32 * blk);
+  float sum = 0.f;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint4 ua = __ldg(src + 2 * h), ub = __ldg(src + 2 * h + 1);
+    const uint32_t wa[4] = {ua.x, ua.y, ua.z, ua.w}, wb[4] = {ub.x, ub.y, ub.z, ub.w};
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const float va = (m & 1) ? bf16_hi(wa[m >> 1]) : bf16_lo(wa[m >> 1]);
+      const float vb = (m & 1) ? bf16_hi(wb[m >> 1]) : bf16_lo(wb[m >> 1]);
+      xb.xp[8 * h + m] = f2pack(va * slot_scale(m), vb * slot_scale(m));
+      sum = __fadd_rn(sum, va);
+      sum = __fadd_rn(sum, vb);
+    }
+  }
+  xb.xsum8 = -8.f * sum;
+}
+
+// Gate/up mapping: lane = one 32-element block; a weight row of H/32 blocks is covered
+// by NBL warps (warp w takes blocks 32 * (w % NBL) + lane); the NW / NBL warp groups
+// split the 64 weight rows (32 gate, 32 up) of the slice.  Each warp's partial of a row
+// goes to s_part[row][w % NBL] and the NBL partials are added in order afterwards.
+template <int NBL>
+struct GateUpMap {
+  static constexpr int kGroups = NW / NBL;     // warp groups
+  static constexpr int kRows = 64 / kGroups;   // weight rows per warp
+};
+
+// Computes a group of G rows (pairs pp0..pp0+G-1 of the item's expert) against the
+// staged item: gate/up for the 64 weight rows, SwiGLU, then the down partials.  Every
+// extracted weight pair feeds the G rows, so the integer work is shared.  xb[g] holds
+// the lane's activation block of row g.  Waits for the stage's down copies (barrier B)
+// before the first down pass if `need_b`.  Ends with a CTA barrier; false on timeout.
 template <int NBL, int G>
-__device__ void compute_group(const RoundArgs& a, const Tables& T, const Stage& st, int pp0, int s,
-                              const uint16_t* x, float* s_gv, float* s_h, float* s_hsum,
-                              bool first_down_wait_done) {
+__device__ __forceinline__ bool compute_group(const RoundArgs& a, const Tables& T, const Stage& st,
+                                              int pp0, int s, const XBlock (&xb)[G], float* s_part,
+                                              float* s_h, bool& need_b, uint32_t parity_b) {
   const int H = a.H, NB = H >> 5, NS = a.I >> 5;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint8_t* s_gu = st.base;
   const uint16_t* s_gus = reinterpret_cast<const uint16_t*>(st.base + 32 * (size_t)H);
   const uint8_t* s_dn = st.base + 36 * (size_t)H;
   const uint16_t* s_dns = reinterpret_cast<const uint16_t*>(st.base + 52 * (size_t)H);
-  int pair[G], row[G];
+  using Map = GateUpMap<NBL>;
+  const int half = warp % NBL, grp = warp / NBL;
+  const int blk = 32 * half + lane;
+  // ---- gate / up ----
+  float part[Map::kRows][G];
 #pragma unroll
-  for (int g = 0; g < G; ++g) {
-    pair[g] = T.pair[pp0 + g];
-    row[g] = pair[g] / a.k;
-  }
-  // ---- gate / up: warp per weight row, lane per 32-element block ----
-  constexpr int RPW = 64 / NW;
-  float part[RPW][G];
-#pragma unroll
-  for (int q = 0; q < RPW; ++q)
+  for (int q = 0; q < Map::kRows; ++q)
 #pragma unroll
     for (int g = 0; g < G; ++g) part[q][g] = 0.f;
+  if (blk < NB) {
 #pragma unroll
-  for (int t = 0; t < NBL; ++t) {
-    const int blk = lane + 32 * t;
-    if (blk < NB) {
-      f2_t xp[G][16];
-      float xsum8[G];
+    for (int q = 0; q < Map::kRows; ++q) {
+      const int wr = grp + Map::kGroups * q;
+      const uint4 nb = *reinterpret_cast<const uint4*>(s_gu + ((size_t)wr * NB + blk) * 16);
+      const float sc = half_bits(s_gus[wr * NB + blk]);
+      const BlockPairs bp = block_pairs(nb);
+      f2_t acc0[G], acc1[G];
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        // elements 16h + m and 16h + 8 + m come from 16-byte loads 2h and 2h + 1
-        const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)row[g] * H + 32 * blk);
-        float sum = 0.f;
+      for (int g = 0; g < G; ++g) acc0[g] = acc1[g] = 0ull;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint4 ua = __ldg(src + 2 * h), ub = __ldg(src + 2 * h + 1);
-          const uint32_t wa[4] = {ua.x, ua.y, ua.z, ua.w}, wb[4] = {ub.x, ub.y, ub.z, ub.w};
-#pragma unroll
-          for (int m = 0; m < 8; ++m) {
-            const float va = (m & 1) ? bf16_hi(wa[m >> 1]) : bf16_lo(wa[m >> 1]);
-            const float vb = (m & 1) ? bf16_hi(wb[m >> 1]) : bf16_lo(wb[m >> 1]);
-            xp[g][8 * h + m] = f2pack(va * slot_scale(m), vb * slot_scale(m));
-            sum = __fadd_rn(sum, va);
-            sum = __fadd_rn(sum, vb);
-          }
-        }
-        xsum8[g] = -8.f * sum;
-      }
-#pragma unroll
-      for (int q = 0; q < RPW; ++q) {
-        const int wr = warp + NW * q;
-        const uint4 nb = *reinterpret_cast<const uint4*>(s_gu + ((size_t)wr * NB + blk) * 16);
-        const float sc = half_bits(s_gus[wr * NB + blk]);
-        const BlockPairs bp = block_pairs(nb);
-        f2_t acc0[G], acc1[G];
-#pragma unroll
-        for (int g = 0; g < G; ++g) acc0[g] = acc1[g] = 0ull;
-#pragma unroll
-        for (int m = 0; m < 8; ++m) {
-          const f2_t e0 = slot_pair(bp, 0, m), e1 = slot_pair(bp, 1, m);
-#pragma unroll
-          for (int g = 0; g < G; ++g) {
-            ffma2(acc0[g], e0, xp[g][m]);
-            ffma2(acc1[g], e1, xp[g][8 + m]);
-          }
-        }
+      for (int m = 0; m < 8; ++m) {
+        const f2_t e0 = slot_pair(bp, 0, m), e1 = slot_pair(bp, 1, m);
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          const float dot = __fadd_rn(f2sum(acc0[g]), f2sum(acc1[g]));
-          part[q][g] = __fmaf_rn(sc, __fmaf_rn(dot, 0x1p62f, xsum8[g]), part[q][g]);
+          ffma2(acc0[g], e0, xb[g].xp[m]);
+          ffma2(acc1[g], e1, xb[g].xp[8 + m]);
         }
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float dot = __fadd_rn(f2sum(acc0[g]), f2sum(acc1[g]));
+        part[q][g] = __fmaf_rn(sc, __fmaf_rn(dot, 0x1p62f, xb[g].xsum8), part[q][g]);
       }
     }
   }
 #pragma unroll
-  for (int q = 0; q < RPW; ++q)
+  for (int q = 0; q < Map::kRows; ++q)
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       const float v = warp_sum(part[q][g]);
-      if (lane == 0) s_gv[(warp + NW * q) * 2 + g] = v;
+      if (lane == 0) s_part[((grp + Map::kGroups * q) * 2 + g) * NBL + half] = v;
     }
   __syncthreads();
-  // ---- SwiGLU on the slice's 32 intermediate rows, warp g for row g ----
+  // ---- SwiGLU on the slice's 32 intermediate rows, warp g for row g; the scaled h
+  // pairs for the down pass go to s_h in pair order (see make_pairs) ----
   if (warp < G) {
-    const float gg = s_gv[lane * 2 + warp], vv = s_gv[(32 + lane) * 2 + warp];
+    float gg = 0.f, vv = 0.f;
+#pragma unroll
+    for (int hf = 0; hf < NBL; ++hf) {
+      gg = __fadd_rn(gg, s_part[(lane * 2 + warp) * NBL + hf]);
+      vv = __fadd_rn(vv, s_part[((32 + lane) * 2 + warp) * NBL + hf]);
+    }
     const float hh = __fmul_rn(__fdiv_rn(gg, __fadd_rn(1.f, expf(-gg))), vv);
-    s_h[warp * 32 + lane] = hh;
+    // element k = lane: pair index 8 * (k / 16) + (k % 8), component (k / 8) % 2
+    float* hrow = s_h + warp * 36;
+    hrow[2 * (8 * (lane >> 4) + (lane & 7)) + ((lane >> 3) & 1)] = hh * slot_scale(lane & 7);
     const float hs = warp_sum(hh);
-    if (lane == 0) s_hsum[warp] = -8.f * hs;
+    if (lane == 0) hrow[32] = -8.f * hs;
   }
-  __syncthreads();
-  (void)first_down_wait_done;
+  if (need_b) {
+    const bool ok = mbar_wait_bounded(st.bar_b, parity_b, a.status, a.wait_cycles);
+    if (__syncthreads_or(!ok)) return false;
+    need_b = false;
+  } else {
+    __syncthreads();
+  }
   // ---- down partials: thread per output row, one 32-element K-block each ----
   f2_t hp[G][16];
   float hsum8[G];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
-    make_pairs(s_h + 32 * g, hp[g]);
-    hsum8[g] = s_hsum[g];
+    const f2_t* hrow = reinterpret_cast<const f2_t*>(s_h + g * 36);
+#pragma unroll
+    for (int q = 0; q < 16; ++q) hp[g][q] = hrow[q];
+    hsum8[g] = s_h[g * 36 + 32];
   }
+  int pair[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) pair[g] = T.pair[pp0 + g];
   for (int o = tid; o < H; o += NT) {
     const uint4 nb = *reinterpret_cast<const uint4*>(s_dn + (size_t)o * 16);
     const float sc = half_bits(s_dns[o]);
@@ -676,8 +703,9 @@ __device__ void compute_group(const RoundArgs& a, const Tables& T, const Stage& 
       a.partial[((size_t)pair[g] * NS + s) * H + o] = __fmul_rn(sc, __fmaf_rn(dot, 0x1p62f, hsum8[g]));
     }
   }
-  // the next group's gate/up may overwrite s_gv / s_h only after everyone is done here
+  // the next group's gate/up may overwrite s_part / s_h only after everyone is done here
   __syncthreads();
+  return true;
 }
 
 // Stage b's state lives in two bitfields: `ph` holds the parity to wait for (bit 2b:
@@ -685,25 +713,41 @@ __device__ void compute_group(const RoundArgs& a, const Tables& T, const Stage& 
 // success both barriers have been consumed (parities flipped, pending bits cleared);
 // on failure `pend` still marks the copies the caller must drain.
 template <int NBL>
-__device__ bool compute_item(const RoundArgs& a, const Tables& T, const Stage& st, int b,
+__device__ __forceinline__ bool compute_item(const RoundArgs& a, const Tables& T, const Stage& st, int b,
                              unsigned& ph, unsigned& pend, int ui, int s, const uint16_t* x,
-                             float* s_gv, float* s_h, float* s_hsum, int stamp_layer) {
+                             float* s_part, float* s_h, int stamp_layer) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int blk = 32 * (warp % NBL) + lane;
+  const bool has_blk = blk < (a.H >> 5);
   const unsigned bit_a = 1u << (2 * b), bit_b = 2u << (2 * b);
   bool ok = mbar_wait_bounded(st.bar_a, (ph & bit_a) ? 1u : 0u, a.status, a.wait_cycles);
   if (__syncthreads_or(!ok)) return false;
   ph ^= bit_a;
   pend &= ~bit_a;
   if (stamp_layer >= 0) stamp(a, stamp_layer, 4);
-  // the down block is needed only after the first group's gate/up; wait for it here
-  // (gate/up of the first group then overlaps nothing, but keeps the control simple)
-  ok = mbar_wait_bounded(st.bar_b, (ph & bit_b) ? 1u : 0u, a.status, a.wait_cycles);
-  if (__syncthreads_or(!ok)) return false;
-  ph ^= bit_b;
-  pend &= ~bit_b;
+  bool need_b = true;
+  const uint32_t parity_b = (ph & bit_b) ? 1u : 0u;
   const int p0 = T.csr_off[ui], p1 = T.csr_off[ui + 1];
   int pp = p0;
-  for (; pp + 2 <= p1; pp += 2) compute_group<NBL, 2>(a, T, st, pp, s, x, s_gv, s_h, s_hsum, true);
-  if (pp < p1) compute_group<NBL, 1>(a, T, st, pp, s, x, s_gv, s_h, s_hsum, true);
+  for (; pp + 2 <= p1; pp += 2) {
+    XBlock xb2[2];
+    if (has_blk) {
+      load_xblock(x, a.H, T.pair[pp] / a.k, blk, xb2[0]);
+      load_xblock(x, a.H, T.pair[pp + 1] / a.k, blk, xb2[1]);
+    }
+    if (!compute_group<NBL, 2>(a, T, st, pp, s, xb2, s_part, s_h, need_b, parity_b)) return false;
+  }
+  if (pp < p1) {
+    XBlock xb1[1];
+    if (has_blk) load_xblock(x, a.H, T.pair[pp] / a.k, blk, xb1[0]);
+    if (!compute_group<NBL, 1>(a, T, st, pp, s, xb1, s_part, s_h, need_b, parity_b)) return false;
+  }
+  if (need_b) {  // (every union expert has a row, so this only keeps phases paired)
+    ok = mbar_wait_bounded(st.bar_b, parity_b, a.status, a.wait_cycles);
+    if (__syncthreads_or(!ok)) return false;
+  }
+  ph ^= bit_b;
+  pend &= ~bit_b;
   return true;
 }
 
@@ -770,7 +814,7 @@ __host__ __device__ inline SmemPlan smem_plan(int H, int E, int R, int k, int ro
   p.router = p.stage1 + kRouterOffset;
   p.router_fits = kRouterOffset + (size_t)router_rows * H * 4 <= p.stage;
   p.bars = off;    off += 64;
-  p.gv = off;      off += up128((128 + 64 + 4) * 4);
+  p.gv = off;      off += up128((256 + 72) * 4);
   p.uni = off;     off += up128((size_t)E * 4);
   p.csr = off;     off += up128((size_t)(E + 1) * 4);
   p.pair = off;    off += up128((size_t)R * k * 4);
@@ -793,9 +837,8 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
     return Stage{smem + P.stage0 + (size_t)b * P.stage, smem_u32(bars + 2 * b),
                  smem_u32(bars + 2 * b + 1)};
   };
-  float* s_gv = reinterpret_cast<float*>(smem + P.gv);  // [64 weight rows][2 group rows]
-  float* s_h = s_gv + 128;                               // [2][32] (unscaled)
-  float* s_hsum = s_h + 64;                              // [2]
+  float* s_part = reinterpret_cast<float*>(smem + P.gv);  // [64 weight rows][2 group rows][NBL]
+  float* s_h = s_part + 256;                               // [2][36]: 16 h pairs + -8 sum(h)
   Tables T{reinterpret_cast<int*>(smem + P.uni), reinterpret_cast<int*>(smem + P.csr),
            reinterpret_cast<int*>(smem + P.pair), reinterpret_cast<float*>(smem + P.w),
            reinterpret_cast<int*>(smem + P.nunion)};
@@ -862,8 +905,8 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
       const int it = blockIdx.x + n * G;
       if (it >= n_items) break;
       const int b = n & 1;
-      if (!compute_item<NBL>(a, T, stage_of(b), b, ph, pend, it / NS, it % NS, x, s_gv, s_h,
-                             s_hsum, n == 0 ? l : -1)) {
+      if (!compute_item<NBL>(a, T, stage_of(b), b, ph, pend, it / NS, it % NS, x, s_part, s_h,
+                             n == 0 ? l : -1)) {
         bail();
         return;
       }
