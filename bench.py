@@ -54,6 +54,23 @@ def peak_hbm():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def reduce_max(v: float, world: int, device) -> float:
+    """Max of a per-rank scalar over all ranks (the timing rule: slowest rank counts)."""
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_round: float, world: int, ms_round: float) -> float:
+    """Replicas: every rank streams its own round, so the job moves world x the bytes
+    in the slowest rank's time."""
+    return world * bytes_per_round / (ms_round * 1e-3) / 1e9
+
+
 def layer_bytes(cfg, U, rows):
     return U * cfg.expert_bytes + cfg.router_bytes + rows * cfg.hidden * (2 + 4)
 
@@ -245,11 +262,7 @@ def run_ours(args):
             dist.barrier()
 
     def max_over_ranks(v):
-        if world == 1:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_max(v, world, dev)
 
     def time_rounds(rows, sigma, steps, warmup, sampler=None):
         xs, x, out, stats = buffers(rows, sigma)
@@ -290,7 +303,7 @@ def run_ours(args):
 
     ms_round = head["ms_total"] / head["steps"]
     us_layer = 1e3 * ms_round / L
-    value = world * head["bytes_per_round"] / (ms_round * 1e-3) / 1e9   # whole job
+    value = whole_job_gbs(head["bytes_per_round"], world, ms_round)
 
     # rows sweep on the same weights
     sweep = {}
