@@ -164,6 +164,27 @@ int moe_profile(moe_handle* h, int enable);
 int moe_profile_read(moe_handle* h, int kind, double* total_ms, int32_t* launches);
 int moe_profile_phases(moe_handle* h, double* mean_us, double* max_us, int32_t n_phases);
 
+/* Allocation-free moe_decode_layer, for callers that may not allocate device memory at
+ * all (allocation disabled by a surrounding memory pool, allocation-free real-time
+ * loops, hosts that forbid cudaMalloc after start-up).  There is no counterpart on the
+ * pages this layer follows; it is an integration convenience.
+ *   - Needs no handle and no workspace: the scratch (barrier words, logits, split-K
+ *     partials, a status word) is one static device array of MOE_NOALLOC_SCRATCH_BYTES
+ *     that every device loading this library holds until the process exits.
+ *   - Runs on the current device.  Its first call on a device sets that device up
+ *     (looks up the array's device address, the SM count, the kernel's shared-memory
+ *     limit); make that first call before any stream capture on the device.
+ *   - Arguments as for moe_decode_layer.  dev_status, if not NULL, is a caller-owned
+ *     device word that receives the timeout bit (1) if a bounded device wait gives up;
+ *     the caller clears it.  Returns MOE_EWORKSPACE if the layer needs more scratch than
+ *     the array holds (256 + moe_workspace_bytes(dims, rows) > MOE_NOALLOC_SCRATCH_BYTES).
+ *   - Calls no cudaMalloc, cudaFree or allocating routine.  Every call shares the one
+ *     array: calls whose executions overlap on the GPU (different streams, or different
+ *     host threads without ordering) race on it and give wrong results. */
+#define MOE_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+int moe_decode_layer_noalloc(const moe_dims* dims, const moe_layer_w* w, const uint16_t* x_bf16,
+                             int32_t rows, float* out, unsigned* dev_status, void* stream);
+
 const char* moe_strerror(int code);
 
 #ifdef __cplusplus

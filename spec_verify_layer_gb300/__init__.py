@@ -23,8 +23,9 @@ ABI_SYMBOLS = (
     "moe_create", "moe_destroy", "moe_workspace_bytes", "moe_packed_bytes", "moe_pack_q4",
     "moe_route", "moe_decode_layer", "moe_round", "moe_last_device_status",
     "moe_last_launch_count", "moe_set_wait_limit_ns", "moe_profile", "moe_profile_read",
-    "moe_profile_phases", "moe_strerror",
+    "moe_profile_phases", "moe_decode_layer_noalloc", "moe_strerror",
 )
+MOE_NOALLOC_SCRATCH_BYTES = 16 << 20
 KIND_ROUND = 0
 PHASES = ("router", "barrier1", "routing", "first_data", "experts", "barrier2", "reduce", "barrier3")
 
@@ -80,6 +81,9 @@ _lib.moe_profile_read.argtypes = [_vp, ctypes.c_int, ctypes.POINTER(ctypes.c_dou
 _lib.moe_profile_read.restype = ctypes.c_int
 _lib.moe_profile_phases.argtypes = [_vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double), _i32]
 _lib.moe_profile_phases.restype = ctypes.c_int
+_lib.moe_decode_layer_noalloc.argtypes = [ctypes.POINTER(moe_dims), ctypes.POINTER(moe_layer_w), _vp, _i32,
+                                          _vp, _vp, _vp]
+_lib.moe_decode_layer_noalloc.restype = ctypes.c_int
 _lib.moe_strerror.argtypes = [ctypes.c_int]
 _lib.moe_strerror.restype = ctypes.c_char_p
 
@@ -180,3 +184,10 @@ def moe_profile_phases(handle: int):
     mx = (ctypes.c_double * n)()
     _check(_lib.moe_profile_phases(handle, mean, mx, n), "moe_profile_phases")
     return {p: (mean[i], mx[i]) for i, p in enumerate(PHASES)}
+
+
+def moe_decode_layer_noalloc(dims: moe_dims, w: moe_layer_w, x_bf16: int, rows: int, out: int,
+                             dev_status: int, stream: int) -> None:
+    """Allocation-free moe_decode_layer on the current device (static device scratch)."""
+    _check(_lib.moe_decode_layer_noalloc(ctypes.byref(dims), ctypes.byref(w), x_bf16, int(rows), out,
+                                         dev_status, stream), "moe_decode_layer_noalloc")

@@ -35,6 +35,7 @@
 #include <climits>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 #include <vector>
 
 #include "moe_internal.h"
@@ -1340,3 +1341,130 @@ int moe_profile_phases(moe_handle* h, double* mean_us, double* max_us, int32_t n
 }
 
 }  // extern "C"
+
+// =====================================================================================
+// Allocation-free variant of moe_decode_layer.
+//
+// Some callers cannot allocate device memory at all: code that runs inside another
+// framework's memory pool with allocation disabled, allocation-free real-time or
+// embedded loops, or hosts that forbid cudaMalloc after start-up.  For them the
+// workspace (grid-barrier words, router logits, split-K partials) lives in the file-
+// scope array below, which the CUDA runtime places on every device that loads this
+// library and keeps until the process exits.  The caller passes only inputs and
+// outputs; this path calls no cudaMalloc, cudaFree or allocating library routine.
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = (size_t)16 << 20;  // 16 MiB per device
+constexpr int kNoAllocMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+struct NoAllocDevice {
+  bool ready = false;
+  void* scratch = nullptr;  // device address of g_noalloc_scratch on this device
+  int sms = 0;
+};
+
+NoAllocDevice g_noalloc[kNoAllocMaxDevices];
+std::mutex g_noalloc_mu;
+
+// One-time set-up of the current device: the device address of the scratch array (in
+// host code the symbol names a host-side stand-in, not device memory), the SM count,
+// and the kernel's shared-memory attribute.
+int noalloc_setup(int dev, size_t smem, NoAllocDevice** out) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  NoAllocDevice& d = g_noalloc[dev];
+  if (!d.ready) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+      cudaGetLastError();
+      return MOE_ECUDA;
+    }
+    int sms = 0, coop = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess || !coop) {
+      cudaGetLastError();
+      return MOE_ECUDA;
+    }
+    d.scratch = p;
+    d.sms = sms;
+    d.ready = true;
+  }
+  cudaError_t e = cudaFuncSetAttribute(k_round<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_round<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ECUDA;
+  }
+  *out = &d;
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" int moe_decode_layer_noalloc(const moe_dims* dims, const moe_layer_w* w,
+                                        const uint16_t* x_bf16, int32_t rows, float* out,
+                                        unsigned* dev_status, void* stream) {
+  int rc = check_dims(dims);
+  if (rc != MOE_OK) return rc;
+  if ((rc = check_layer(w)) != MOE_OK) return rc;
+  if (!aligned16(x_bf16) || !aligned16(out) || rows < 1 || rows > dims->max_rows)
+    return MOE_EINVAL;
+  if (dev_status && (reinterpret_cast<uintptr_t>(dev_status) & 3u)) return MOE_EINVAL;
+  // the scratch holds the status word (first 256 bytes) and the layer's workspace
+  const WsLayout L = ws_layout(*dims, rows);
+  if (256 + L.total > kNoAllocScratchBytes) return MOE_EWORKSPACE;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) {
+    cudaGetLastError();
+    return MOE_ECUDA;
+  }
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ECUDA;
+  }
+  const size_t smem = smem_bytes(*dims, rows, sms);
+  const SmemPlan plan = smem_plan(dims->hidden, dims->n_experts, rows, dims->top_k,
+                                  (dims->n_experts + sms - 1) / sms);
+  if (smem + 1024 > 227 * 1024 || !plan.router_fits) return MOE_EUNSUPPORTED;
+  NoAllocDevice* d = nullptr;
+  if ((rc = noalloc_setup(dev, smem, &d)) != MOE_OK) return rc;
+  char* base = static_cast<char*>(d->scratch);
+  unsigned* own_status = reinterpret_cast<unsigned*>(base);
+  void* ws = base + 256;
+  RoundArgs a{};
+  const moe_dims& dd = *dims;
+  a.H = dd.hidden;
+  a.E = dd.n_experts;
+  a.k = dd.top_k;
+  a.I = dd.inter;
+  a.R = rows;
+  a.L = 1;
+  a.bar = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + L.ctrl);
+  a.logits = reinterpret_cast<float*>(static_cast<char*>(ws) + L.logits);
+  a.partial = reinterpret_cast<float*>(static_cast<char*>(ws) + L.partial);
+  a.status = dev_status ? dev_status : own_status;
+  a.wait_cycles = kDefaultWaitCycles;
+  a.x = x_bf16;
+  a.out = out;
+  copy_layers(a, w, 1);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // the barrier words must start at zero; logits and partials are fully overwritten
+  if (cudaMemsetAsync(a.bar, 0, 256, st) != cudaSuccess) return MOE_ECUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(sms);
+  cfg.blockDim = dim3(NT);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = (nbl_of(a.H) == 1) ? cudaLaunchKernelEx(&cfg, k_round<1>, a)
+                                           : cudaLaunchKernelEx(&cfg, k_round<2>, a);
+  return e == cudaSuccess ? MOE_OK : MOE_ECUDA;
+}
