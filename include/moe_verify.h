@@ -83,15 +83,16 @@ typedef struct moe_handle moe_handle;
 
 /* Validates dims and binds a handle to `device` (queries its SM count, allocates a
  * 4-byte device status word -- the only device allocation the library makes).
- * Supported: hidden a multiple of 256 in [256, 2048], inter a multiple of 32 in
- * [32, 4096], 1 <= top_k <= min(n_experts, 32), n_experts <= 512, 1 <= max_rows <= 32.
+ * Supported: hidden a multiple of 256 in [256, 2048], inter a multiple of 256 in
+ * [256, 4096], 1 <= top_k <= min(n_experts, 32), n_experts <= 512, 1 <= max_rows <= 32
+ * (and the shared-memory plan must fit one SM).
  * MOE_EINVAL for dims that make no sense, MOE_EUNSUPPORTED for sizes outside those
  * ranges, MOE_ECUDA if the device cannot be used.  *out is NULL on failure. */
 int moe_create(const moe_dims* dims, int device, moe_handle** out);
 void moe_destroy(moe_handle* h);
 
-/* Device workspace (bytes) a call with `rows` rows needs: routing tables and the
- * fp32 split-K partials of the expert stage.  0 for invalid dims/rows. */
+/* Device workspace (bytes) a call with `rows` rows needs: barrier words, router logits
+ * and the fp32 SwiGLU outputs exchanged between CTAs.  0 for invalid dims/rows. */
 size_t moe_workspace_bytes(const moe_dims* dims, int32_t rows);
 
 /* Packed size of ONE expert: part 0 = code bytes, part 1 = scale bytes.  0 if invalid. */
@@ -102,12 +103,12 @@ size_t moe_packed_bytes(const moe_dims* dims, int which, int part);
  *               q_b = up codes [n][I][H],   s_b = up scales [n][I][H/32]
  *   MOE_DOWN:   q_a = down codes [n][H][I], s_a = down scales [n][H][I/32]; q_b, s_b unused
  * into nib_out / scale_out (n * moe_packed_bytes(which, 0 / 1) bytes).  Codes outside
- * [-8, 7] give MOE_EINVAL.  Layout (GB300 kernel order, 32-element blocks, code q
- * stored as the nibble q + 8, element 2t in the low nibble of byte t of its block):
- *   gate/up codes  [E][I/32 slices][2: gate, up][32 rows][H/32 blocks][16 B]
- *   gate/up scales [E][I/32][2][32][H/32]
- *   down codes     [E][I/32 blocks][H rows][16 B]
- *   down scales    [E][I/32][H]                                                  */
+ * [-8, 7] give MOE_EINVAL.  Layout (32-element blocks, code q stored as the nibble
+ * q + 8, element 2t in the low nibble of byte t of its block):
+ *   gate/up codes  [E][I][2: gate, up][H/32 blocks][16 B]   (intermediate row i of an
+ *   gate/up scales [E][I][2][H/32]                           expert: gate, then up)
+ *   down codes     [E][H][I/32 blocks][16 B]                 (output-row major)
+ *   down scales    [E][H][I/32]                                                       */
 int moe_pack_q4(const moe_dims* dims, int which, int32_t n_experts, const int8_t* q_a,
                 const uint16_t* s_a, const int8_t* q_b, const uint16_t* s_b, uint8_t* nib_out,
                 uint16_t* scale_out);
@@ -158,8 +159,8 @@ int moe_set_wait_limit_ns(moe_handle* h, uint64_t ns);
  * and the launch count (kind must be 0: the fused round kernel).
  * moe_profile_phases returns, for the last profiled moe_round, the mean over CTAs and
  * layers (mean_us) and the per-layer maximum over CTAs averaged over layers (max_us)
- * of eight phases: router GEMV, barrier 1, routing, wait for the first staged expert
- * item, expert stream, barrier 2, reduction, barrier 3.  n_phases must be >= 8. */
+ * of eight phases: router GEMV, barrier 1, routing, wait for the first staged gate/up
+ * chunk, gate/up stream, barrier 2, down pass and combine, barrier 3.  n_phases >= 8. */
 int moe_profile(moe_handle* h, int enable);
 int moe_profile_read(moe_handle* h, int kind, double* total_ms, int32_t* launches);
 int moe_profile_phases(moe_handle* h, double* mean_us, double* max_us, int32_t n_phases);
@@ -168,8 +169,8 @@ int moe_profile_phases(moe_handle* h, double* mean_us, double* max_us, int32_t n
  * all (allocation disabled by a surrounding memory pool, allocation-free real-time
  * loops, hosts that forbid cudaMalloc after start-up).  There is no counterpart on the
  * pages this layer follows; it is an integration convenience.
- *   - Needs no handle and no workspace: the scratch (barrier words, logits, split-K
- *     partials, a status word) is one static device array of MOE_NOALLOC_SCRATCH_BYTES
+ *   - Needs no handle and no workspace: the scratch (barrier words, logits, exchanged
+ *     SwiGLU outputs, a status word) is one static device array of MOE_NOALLOC_SCRATCH_BYTES
  *     that every device loading this library holds until the process exits.
  *   - Runs on the current device.  Its first call on a device sets that device up
  *     (looks up the array's device address, the SM count, the kernel's shared-memory

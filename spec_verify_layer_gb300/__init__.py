@@ -27,7 +27,7 @@ ABI_SYMBOLS = (
 )
 MOE_NOALLOC_SCRATCH_BYTES = 16 << 20
 KIND_ROUND = 0
-PHASES = ("router", "barrier1", "routing", "first_data", "experts", "barrier2", "reduce", "barrier3")
+PHASES = ("router", "barrier1", "routing", "first_data", "gateup", "barrier2", "down", "barrier3")
 
 
 class moe_dims(ctypes.Structure):

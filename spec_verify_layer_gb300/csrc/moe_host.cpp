@@ -13,6 +13,7 @@ int check_dims(const moe_dims* d) {
   if (d->top_k > d->n_experts) return MOE_EINVAL;
   if (d->hidden % 128 || d->inter % 32) return MOE_EINVAL;  // block and router-order structure
   if (d->hidden % 256 || d->hidden < kMinHidden || d->hidden > kMaxHidden) return MOE_EUNSUPPORTED;
+  if (d->inter % 256) return MOE_EUNSUPPORTED;  // 16-byte aligned bulk copies of scale rows
   if (d->inter > kMaxInter || d->n_experts > kMaxExperts || d->top_k > kMaxTopK ||
       d->max_rows > kMaxRows)
     return MOE_EUNSUPPORTED;
@@ -27,7 +28,7 @@ WsLayout ws_layout(const moe_dims& d, int rows) {
   size_t off = 0;
   L.ctrl = off;     off += 256;
   L.logits = off;   off += up256(R * E * 4);
-  L.partial = off;  off += up256(R * k * (size_t)(d.inter / kSlice) * (size_t)d.hidden * 4);
+  L.hbuf = off;     off += up256(R * k * (size_t)d.inter * 4);
   L.total = off;
   return L;
 }
@@ -68,38 +69,37 @@ int moe_pack_q4(const moe_dims* dims, int which, int32_t n_experts, const int8_t
   if (rc != MOE_OK) return rc;
   if (n_experts < 1 || !q_a || !s_a || !nib_out || !scale_out) return MOE_EINVAL;
   const size_t H = (size_t)dims->hidden, I = (size_t)dims->inter;
-  const size_t NB = H / 32, NS = I / kSlice;
+  const size_t NB = H / 32, NBI = I / 32;
   if (which == MOE_GATEUP) {
+    // [E][I][2: gate, up][H/32 blocks][16 B], scales [E][I][2][H/32]
     if (!q_b || !s_b) return MOE_EINVAL;
     for (size_t e = 0; e < (size_t)n_experts; ++e) {
       uint8_t* nib = nib_out + e * gu_nib_bytes(*dims);
       uint16_t* sc = scale_out + e * (gu_sc_bytes(*dims) / 2);
-      for (size_t s = 0; s < NS; ++s)
+      for (size_t i = 0; i < I; ++i)
         for (size_t m = 0; m < 2; ++m) {
-          const int8_t* q = (m == 0 ? q_a : q_b) + e * I * H;
-          const uint16_t* sv = (m == 0 ? s_a : s_b) + e * I * NB;
-          for (size_t ii = 0; ii < (size_t)kSlice; ++ii) {
-            size_t i = s * kSlice + ii;
-            size_t base = ((s * 2 + m) * kSlice + ii) * NB;
-            for (size_t b = 0; b < NB; ++b) {
-              if (!pack_block(q + i * H + b * 32, nib + (base + b) * 16)) return MOE_EINVAL;
-              sc[base + b] = sv[i * NB + b];
-            }
+          const int8_t* q = (m == 0 ? q_a : q_b) + e * I * H + i * H;
+          const uint16_t* sv = (m == 0 ? s_a : s_b) + e * I * NB + i * NB;
+          const size_t base = (i * 2 + m) * NB;
+          for (size_t b = 0; b < NB; ++b) {
+            if (!pack_block(q + b * 32, nib + (base + b) * 16)) return MOE_EINVAL;
+            sc[base + b] = sv[b];
           }
         }
     }
     return MOE_OK;
   }
   if (which == MOE_DOWN) {
+    // [E][H][I/32 blocks][16 B], scales [E][H][I/32] (the unpacked order)
     for (size_t e = 0; e < (size_t)n_experts; ++e) {
       uint8_t* nib = nib_out + e * dn_nib_bytes(*dims);
       uint16_t* sc = scale_out + e * (dn_sc_bytes(*dims) / 2);
       const int8_t* q = q_a + e * H * I;
-      const uint16_t* sv = s_a + e * H * NS;
-      for (size_t s = 0; s < NS; ++s)
-        for (size_t o = 0; o < H; ++o) {
-          if (!pack_block(q + o * I + s * 32, nib + (s * H + o) * 16)) return MOE_EINVAL;
-          sc[s * H + o] = sv[o * NS + s];
+      const uint16_t* sv = s_a + e * H * NBI;
+      for (size_t o = 0; o < H; ++o)
+        for (size_t b = 0; b < NBI; ++b) {
+          if (!pack_block(q + o * I + b * 32, nib + (o * NBI + b) * 16)) return MOE_EINVAL;
+          sc[o * NBI + b] = sv[o * NBI + b];
         }
     }
     return MOE_OK;

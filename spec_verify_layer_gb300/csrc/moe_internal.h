@@ -9,7 +9,6 @@
 
 namespace moe {
 
-constexpr int kSlice = 32;     // intermediate rows per expert work item (one down K-block)
 constexpr int kMaxRows = 32;   // rows are tracked in 32-bit masks
 constexpr int kMaxExperts = 512;   // routing keeps 16 logits per lane in registers
 constexpr int kMaxTopK = 32;
@@ -21,9 +20,10 @@ constexpr int kMaxLayers = 128;  // layers per moe_round call (weight table trav
 int check_dims(const moe_dims* d);
 
 // Byte offsets of the workspace regions for `rows` rows (each region 256-aligned):
-// grid-barrier words, router logits [rows][E], split-K partials [rows*k][I/32][H].
+// grid-barrier words, router logits [rows][E], SwiGLU outputs h [rows*k][I] (fp32, one
+// row per routed (row, expert) pair, grouped by expert).
 struct WsLayout {
-  size_t ctrl, logits, partial, total;
+  size_t ctrl, logits, hbuf, total;
 };
 WsLayout ws_layout(const moe_dims& d, int rows);
 

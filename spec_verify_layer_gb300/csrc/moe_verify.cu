@@ -3,24 +3,23 @@
 //
 // One persistent cooperative kernel (k_round, one CTA per SM) runs a whole round of L
 // layers.  Per layer, with grid-wide barriers B1..B3 in between:
-//   P1  router GEMV: one warp per expert, canonical fp32 order -> logits in the
-//       workspace.  The next layer's router weights are prefetched into L2 while the
-//       current layer streams its experts (they do not depend on any data).
+//   P1  router GEMV: this CTA's router rows (staged into shared memory while the
+//       previous layer ran: they depend on no data), canonical fp32 order -> logits.
 //   B1
 //   P2  every CTA reads the logits and builds the same routing in shared memory:
 //       per-row top-k (warp per row, redux.sync selection, lower id wins ties),
 //       renormalised weights, the ascending expert union U and, per union expert,
-//       the (row, rank) pairs that picked it.
-//   P3  split-K expert items, item = (union expert, 32-row slice of the intermediate
-//       dimension), handed to CTAs round-robin.  Each CTA double-buffers items in
-//       shared memory: one elected thread issues 1-D bulk TMA copies of the item's
-//       gate/up rows + scales (mbarrier A) and the matching down K-block + scales
-//       (mbarrier B); the CTA computes g, v, h = silu(g) v for each of the expert's
-//       rows as soon as A lands, then the down partial Wd[:, slice] h[slice] once B
-//       lands, and writes it per (row, rank, slice) to the workspace.
-//   B2
-//   P4  out[r][o] = sum_j w[r][j] * sum_s partial[r, j, s][o], a fixed order, so a
-//       row's output depends only on that row (bitwise), whatever shares the round.
+//       the (row, rank) pairs that picked it (CSR).
+//   P3  gate/up: the U * I units (gate row i + up row i of a union expert) are split
+//       evenly and contiguously across CTAs and streamed through shared-memory slots
+//       with 1-D bulk TMA copies; for every row of the expert a warp computes g and v
+//       and stores h = silu(g) v to the workspace.  Meanwhile the down rows of every
+//       union expert for this CTA's share of the output rows are prefetched.
+//   B2  (every h written)
+//   P4  down: for each union expert in ascending id order, each of this CTA's output
+//       rows o gets y = Wd[o] . h for every row of the expert, accumulated as
+//       out[r][o] += w_{r,e} y in shared memory -- a fixed order, so a row's output
+//       depends only on that row (bitwise), whatever shares the round.
 //   B3  (layer l+1's router waits for layer l's output, as a real decode would)
 //
 // Dequantisation without a convert instruction: a nibble n placed in bits [p, p+4) of
@@ -69,7 +68,7 @@ struct RoundArgs {
   int* stats;         // [L] |U| per layer, or null
   unsigned* bar;      // [0] barrier arrivals, [33] abort flag
   float* logits;      // [R][E]
-  float* partial;     // [R*k][I/32][H]
+  float* hbuf;        // [R*k][I] SwiGLU outputs by CSR position
   int* user_ids;      // moe_route outputs (CTA 0 writes them)
   float* user_w;
   int* user_union;
@@ -152,10 +151,6 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
-__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
 __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
   unsigned v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -226,16 +221,6 @@ __device__ __forceinline__ f2_t slot_pair(const BlockPairs& b, int half, int m) 
   const f2_t d = half ? b.d1 : b.d0;
   const f2_t t = half ? b.t1 : b.t0;
   return (m <= 4) ? (d & M[m]) : (t & M[m - 3]);
-}
-
-// Pre-scaled activation pairs of one 32-element block from 32 floats v[k]:
-// xp[8h + m] = (v[16h + m] * scale(m), v[16h + 8 + m] * scale(m)).
-__device__ __forceinline__ void make_pairs(const float* v, f2_t* xp) {
-#pragma unroll
-  for (int h = 0; h < 2; ++h)
-#pragma unroll
-    for (int m = 0; m < 8; ++m)
-      xp[8 * h + m] = f2pack(v[16 * h + m] * slot_scale(m), v[16 * h + 8 + m] * slot_scale(m));
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
@@ -524,352 +509,314 @@ __device__ int route_phase(const RoundArgs& a, const Tables& T, unsigned* s_mask
 }
 
 // ---------------------------------------------------------------------------------
-// P3: expert items
+// P3: gate/up over an even share of the (union expert, intermediate row) units
+//
+// Unit (ui, i) = gate row i and up row i of union expert ui: H bytes of codes and H/8
+// bytes of scales, contiguous in the packed layout.  CTA c owns units
+// [c N / G, (c+1) N / G) of the N = U * I units, walked in chunks that stop at expert
+// boundaries and at the slot capacity; chunks stream through kGuSlots shared-memory
+// slots (1-D bulk copies, one mbarrier per slot).  For every row of the expert a warp
+// computes g and v of one unit, lane 0 stores h = silu(g) v to the workspace at
+// (CSR position, i).  Down rows of every union expert for this CTA's output rows are
+// prefetched into kDnSlots slots meanwhile (they depend only on the routing).
 
-// one staged item: gate/up codes 32H, gate/up scales 4H, down codes 16H, down scales 2H
-__host__ __device__ constexpr size_t stage_bytes(int H) { return (size_t)54 * H; }
+constexpr int kGuSlots = 3;
+constexpr int kDnSlots = 16;
+constexpr int kMaxChunks = 96;
+constexpr size_t kRouterOffset = 16384;  // router rows sit after the routing scratch
+constexpr int kAccStride = 64;           // output rows per CTA are at most this many
 
-struct Stage {
-  uint8_t* base;
-  uint32_t bar_a, bar_b;
+struct GuChunk {
+  int ui, i0, n;
 };
 
-__device__ void issue_item(const RoundArgs& a, const LayerPtrs& W, const Stage& st, int u, int s) {
-  const size_t H = (size_t)a.H, I = (size_t)a.I, NB = H / 32;
-  // order earlier generic-proxy accesses of this buffer before the async-proxy writes
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  mbar_expect_tx(st.bar_a, (uint32_t)(36 * H));
-  bulk_g2s(smem_u32(st.base), W.gu_nib + (size_t)u * I * H + (size_t)s * 32 * H, (uint32_t)(32 * H),
-           st.bar_a);
-  bulk_g2s(smem_u32(st.base + 32 * H), W.gu_sc + (size_t)u * (I * H / 16) + (size_t)s * 64 * NB,
-           (uint32_t)(4 * H), st.bar_a);
-  mbar_expect_tx(st.bar_b, (uint32_t)(18 * H));
-  bulk_g2s(smem_u32(st.base + 36 * H), W.dn_nib + (size_t)u * (I * H / 2) + (size_t)s * 16 * H,
-           (uint32_t)(16 * H), st.bar_b);
-  bulk_g2s(smem_u32(st.base + 52 * H), W.dn_sc + (size_t)u * (I * H / 32) + (size_t)s * H,
-           (uint32_t)(2 * H), st.bar_b);
-}
-
-// Computes one staged item for every row of its expert.  Returns false on a timeout.
-// Activation pairs of one 32-element block of one row (see make_pairs), built from
-// the row's bf16 values, plus -8 * (sum of the block's 32 values).
-struct XBlock {
-  f2_t xp[16];
-  float xsum8;
-};
-
-__device__ __forceinline__ void load_xblock(const uint16_t* x, int H, int row, int blk, XBlock& xb) {
-  // elements 16h + m and 16h + 8 + m come from 16-byte loads 2h and 2h + 1
-  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)row * H + 32 * blk);
-  float sum = 0.f;
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const uint4 ua = __ldg(src + 2 * h), ub = __ldg(src + 2 * h + 1);
-    const uint32_t wa[4] = {ua.x, ua.y, ua.z, ua.w}, wb[4] = {ub.x, ub.y, ub.z, ub.w};
-#pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      const float va = (m & 1) ? bf16_hi(wa[m >> 1]) : bf16_lo(wa[m >> 1]);
-      const float vb = (m & 1) ? bf16_hi(wb[m >> 1]) : bf16_lo(wb[m >> 1]);
-      xb.xp[8 * h + m] = f2pack(va * slot_scale(m), vb * slot_scale(m));
-      sum = __fadd_rn(sum, va);
-      sum = __fadd_rn(sum, vb);
-    }
-  }
-  xb.xsum8 = -8.f * sum;
-}
-
-// Gate/up mapping: lane = one 32-element block; a weight row of H/32 blocks is covered
-// by NBL warps (warp w takes blocks 32 * (w % NBL) + lane); the NW / NBL warp groups
-// split the 64 weight rows (32 gate, 32 up) of the slice.  Each warp's partial of a row
-// goes to s_part[row][w % NBL] and the NBL partials are added in order afterwards.
-template <int NBL>
-struct GateUpMap {
-  static constexpr int kGroups = NW / NBL;     // warp groups
-  static constexpr int kRows = 64 / kGroups;   // weight rows per warp
-};
-
-// Computes a group of G rows (pairs pp0..pp0+G-1 of the item's expert) against the
-// staged item: gate/up for the 64 weight rows, SwiGLU, then the down partials.  Every
-// extracted weight pair feeds the G rows, so the integer work is shared.  xb[g] holds
-// the lane's activation block of row g.  Waits for the stage's down copies (barrier B)
-// before the first down pass if `need_b`.  Ends with a CTA barrier; false on timeout.
-template <int NBL, int G>
-__device__ __forceinline__ bool compute_group(const RoundArgs& a, const Tables& T, const Stage& st,
-                                              int pp0, int s, const XBlock (&xb)[G], float* s_part,
-                                              float* s_h, bool& need_b, uint32_t parity_b) {
-  const int H = a.H, NB = H >> 5, NS = a.I >> 5;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const uint8_t* s_gu = st.base;
-  const uint16_t* s_gus = reinterpret_cast<const uint16_t*>(st.base + 32 * (size_t)H);
-  const uint8_t* s_dn = st.base + 36 * (size_t)H;
-  const uint16_t* s_dns = reinterpret_cast<const uint16_t*>(st.base + 52 * (size_t)H);
-  using Map = GateUpMap<NBL>;
-  const int half = warp % NBL, grp = warp / NBL;
-  const int blk = 32 * half + lane;
-  // ---- gate / up ----
-  float part[Map::kRows][G];
-#pragma unroll
-  for (int q = 0; q < Map::kRows; ++q)
-#pragma unroll
-    for (int g = 0; g < G; ++g) part[q][g] = 0.f;
-  if (blk < NB) {
-#pragma unroll
-    for (int q = 0; q < Map::kRows; ++q) {
-      const int wr = grp + Map::kGroups * q;
-      const uint4 nb = *reinterpret_cast<const uint4*>(s_gu + ((size_t)wr * NB + blk) * 16);
-      const float sc = half_bits(s_gus[wr * NB + blk]);
-      const BlockPairs bp = block_pairs(nb);
-      f2_t acc0[G], acc1[G];
-#pragma unroll
-      for (int g = 0; g < G; ++g) acc0[g] = acc1[g] = 0ull;
-#pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        const f2_t e0 = slot_pair(bp, 0, m), e1 = slot_pair(bp, 1, m);
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          ffma2(acc0[g], e0, xb[g].xp[m]);
-          ffma2(acc1[g], e1, xb[g].xp[8 + m]);
-        }
-      }
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float dot = __fadd_rn(f2sum(acc0[g]), f2sum(acc1[g]));
-        part[q][g] = __fmaf_rn(sc, __fmaf_rn(dot, 0x1p62f, xb[g].xsum8), part[q][g]);
-      }
-    }
-  }
-#pragma unroll
-  for (int q = 0; q < Map::kRows; ++q)
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float v = warp_sum(part[q][g]);
-      if (lane == 0) s_part[((grp + Map::kGroups * q) * 2 + g) * NBL + half] = v;
-    }
-  __syncthreads();
-  // ---- SwiGLU on the slice's 32 intermediate rows, warp g for row g; the scaled h
-  // pairs for the down pass go to s_h in pair order (see make_pairs) ----
-  if (warp < G) {
-    float gg = 0.f, vv = 0.f;
-#pragma unroll
-    for (int hf = 0; hf < NBL; ++hf) {
-      gg = __fadd_rn(gg, s_part[(lane * 2 + warp) * NBL + hf]);
-      vv = __fadd_rn(vv, s_part[((32 + lane) * 2 + warp) * NBL + hf]);
-    }
-    const float hh = __fmul_rn(__fdiv_rn(gg, __fadd_rn(1.f, expf(-gg))), vv);
-    // element k = lane: pair index 8 * (k / 16) + (k % 8), component (k / 8) % 2
-    float* hrow = s_h + warp * 36;
-    hrow[2 * (8 * (lane >> 4) + (lane & 7)) + ((lane >> 3) & 1)] = hh * slot_scale(lane & 7);
-    const float hs = warp_sum(hh);
-    if (lane == 0) hrow[32] = -8.f * hs;
-  }
-  if (need_b) {
-    const bool ok = mbar_wait_bounded(st.bar_b, parity_b, a.status, a.wait_cycles);
-    if (__syncthreads_or(!ok)) return false;
-    need_b = false;
-  } else {
-    __syncthreads();
-  }
-  // ---- down partials: thread per output row, one 32-element K-block each ----
-  f2_t hp[G][16];
-  float hsum8[G];
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    const f2_t* hrow = reinterpret_cast<const f2_t*>(s_h + g * 36);
-#pragma unroll
-    for (int q = 0; q < 16; ++q) hp[g][q] = hrow[q];
-    hsum8[g] = s_h[g * 36 + 32];
-  }
-  int pair[G];
-#pragma unroll
-  for (int g = 0; g < G; ++g) pair[g] = T.pair[pp0 + g];
-  for (int o = tid; o < H; o += NT) {
-    const uint4 nb = *reinterpret_cast<const uint4*>(s_dn + (size_t)o * 16);
-    const float sc = half_bits(s_dns[o]);
-    const BlockPairs bp = block_pairs(nb);
-    f2_t acc0[G], acc1[G];
-#pragma unroll
-    for (int g = 0; g < G; ++g) acc0[g] = acc1[g] = 0ull;
-#pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      const f2_t e0 = slot_pair(bp, 0, m), e1 = slot_pair(bp, 1, m);
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        ffma2(acc0[g], e0, hp[g][m]);
-        ffma2(acc1[g], e1, hp[g][8 + m]);
-      }
-    }
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float dot = __fadd_rn(f2sum(acc0[g]), f2sum(acc1[g]));
-      a.partial[((size_t)pair[g] * NS + s) * H + o] = __fmul_rn(sc, __fmaf_rn(dot, 0x1p62f, hsum8[g]));
-    }
-  }
-  // the next group's gate/up may overwrite s_part / s_h only after everyone is done here
-  __syncthreads();
-  return true;
-}
-
-// Stage b's state lives in two bitfields: `ph` holds the parity to wait for (bit 2b:
-// gate/up barrier A, bit 2b+1: down barrier B) and `pend` marks copies in flight.  On
-// success both barriers have been consumed (parities flipped, pending bits cleared);
-// on failure `pend` still marks the copies the caller must drain.
-template <int NBL>
-__device__ __forceinline__ bool compute_item(const RoundArgs& a, const Tables& T, const Stage& st, int b,
-                             unsigned& ph, unsigned& pend, int ui, int s, const uint16_t* x,
-                             float* s_part, float* s_h, int stamp_layer) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int blk = 32 * (warp % NBL) + lane;
-  const bool has_blk = blk < (a.H >> 5);
-  const unsigned bit_a = 1u << (2 * b), bit_b = 2u << (2 * b);
-  bool ok = mbar_wait_bounded(st.bar_a, (ph & bit_a) ? 1u : 0u, a.status, a.wait_cycles);
-  if (__syncthreads_or(!ok)) return false;
-  ph ^= bit_a;
-  pend &= ~bit_a;
-  if (stamp_layer >= 0) stamp(a, stamp_layer, 4);
-  bool need_b = true;
-  const uint32_t parity_b = (ph & bit_b) ? 1u : 0u;
-  const int p0 = T.csr_off[ui], p1 = T.csr_off[ui + 1];
-  int pp = p0;
-  for (; pp + 2 <= p1; pp += 2) {
-    XBlock xb2[2];
-    if (has_blk) {
-      load_xblock(x, a.H, T.pair[pp] / a.k, blk, xb2[0]);
-      load_xblock(x, a.H, T.pair[pp + 1] / a.k, blk, xb2[1]);
-    }
-    if (!compute_group<NBL, 2>(a, T, st, pp, s, xb2, s_part, s_h, need_b, parity_b)) return false;
-  }
-  if (pp < p1) {
-    XBlock xb1[1];
-    if (has_blk) load_xblock(x, a.H, T.pair[pp] / a.k, blk, xb1[0]);
-    if (!compute_group<NBL, 1>(a, T, st, pp, s, xb1, s_part, s_h, need_b, parity_b)) return false;
-  }
-  if (need_b) {  // (every union expert has a row, so this only keeps phases paired)
-    ok = mbar_wait_bounded(st.bar_b, parity_b, a.status, a.wait_cycles);
-    if (__syncthreads_or(!ok)) return false;
-  }
-  ph ^= bit_b;
-  pend &= ~bit_b;
-  return true;
-}
-
-// ---------------------------------------------------------------------------------
-// P4: fixed-order weighted reduction of the partials into the layer output
-
-// Tile = (row r, 32 consecutive outputs).  Unit u = (rank j, part): a warp sums the
-// partials of slices s = part, part + jw, ... for its 32 outputs (coalesced), then warp
-// 0 combines: y_j = sum over parts in order, out = sum_j w_j y_j in rank order.
-__device__ void reduce_phase(const RoundArgs& a, const Tables& T, float* out, float* s_red) {
-  const int H = a.H, k = a.k, NS = a.I >> 5;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int jw = (NW / k) > 0 ? (NW / k) : 1;  // warps per rank
-  const int units = k * jw;
-  const int tiles_per_row = H >> 5;
-  const int n_tiles = a.R * tiles_per_row;
-  for (int q = blockIdx.x; q < n_tiles; q += gridDim.x) {
-    const int r = q / tiles_per_row;
-    const int o0 = (q - r * tiles_per_row) * 32;
-    for (int u = warp; u < units; u += NW) {
-      const int j = u / jw, part = u - (u / jw) * jw;
-      const float* src = a.partial + (size_t)(r * k + j) * NS * H + o0 + lane;
-      float y = 0.f;
-#pragma unroll 8
-      for (int s = part; s < NS; s += jw) y = __fadd_rn(y, __ldcg(src + (size_t)s * H));
-      s_red[u * 32 + lane] = y;
-    }
-    __syncthreads();
-    if (warp == 0) {
-      float acc = 0.f;
-      for (int j = 0; j < k; ++j) {
-        float yj = 0.f;
-        for (int part = 0; part < jw; ++part) yj = __fadd_rn(yj, s_red[(j * jw + part) * 32 + lane]);
-        acc = __fmaf_rn(T.w[r * k + j], yj, acc);
-      }
-      out[(size_t)r * H + o0 + lane] = acc;
-    }
-    __syncthreads();
-  }
-}
-
-// ---------------------------------------------------------------------------------
-// shared-memory plan
-
-constexpr size_t kRouterOffset = 8192;  // reduction scratch (<= 4 KB) sits below
-
+// smem plan: GU ring | DN slots | tables | out accumulators | chunk list | barriers
 struct SmemPlan {
-  size_t stage, stage0, stage1, router, bars, gv, uni, csr, pair, w, nunion, total;
+  size_t gu_slot, gu, dn_slot, dn, uni, csr, pair, w, nunion, acc, chunks, bars, total;
+  int gu_cap;     // units per gate/up chunk
+  int max_orows;  // output rows per CTA (ceil(H / grid))
   bool router_fits;
 };
 
 __host__ __device__ inline size_t up128(size_t x) { return (x + 127) & ~(size_t)127; }
 
-// router_rows = experts per CTA, ceil(E / grid)
-__host__ __device__ inline SmemPlan smem_plan(int H, int E, int R, int k, int router_rows) {
+__host__ __device__ inline SmemPlan smem_plan(int H, int I, int E, int R, int k, int grid) {
   SmemPlan p{};
-  p.stage = up128(stage_bytes(H));
+  const size_t unit = (size_t)H + (size_t)H / 8;
+  p.max_orows = (H + grid - 1) / grid;
+  p.dn_slot = up128((size_t)p.max_orows * (I / 2)) + up128((size_t)p.max_orows * (I / 16));
+  const size_t tables = up128((size_t)E * 4) + up128((size_t)(E + 1) * 4) +
+                        2 * up128((size_t)R * k * 4) + 128 + up128((size_t)R * kAccStride * 4) +
+                        up128(kMaxChunks * 12 + 16) + 256;
+  const size_t budget = (size_t)225 * 1024 - tables - kDnSlots * p.dn_slot;
+  size_t cap = (budget / kGuSlots) / unit;
+  if (cap > 64) cap = 64;
+  p.gu_cap = (int)cap;
+  p.gu_slot = up128(cap * unit);
   size_t off = 0;
-  p.stage0 = off;  off += p.stage;
-  p.stage1 = off;  off += p.stage;
-  // The next layer's router rows live in stage 1 after the reduction scratch: they are
-  // written after the last expert item of a layer and read before the next layer's
-  // first item, while the staging buffers are idle.
-  p.router = p.stage1 + kRouterOffset;
-  p.router_fits = kRouterOffset + (size_t)router_rows * H * 4 <= p.stage;
-  p.bars = off;    off += 64;
-  p.gv = off;      off += up128((256 + 72) * 4);
+  p.gu = off;      off += kGuSlots * p.gu_slot;
+  p.dn = off;      off += kDnSlots * p.dn_slot;
   p.uni = off;     off += up128((size_t)E * 4);
   p.csr = off;     off += up128((size_t)(E + 1) * 4);
   p.pair = off;    off += up128((size_t)R * k * 4);
   p.w = off;       off += up128((size_t)R * k * 4);
   p.nunion = off;  off += 128;
+  p.acc = off;     off += up128((size_t)R * kAccStride * 4);
+  p.chunks = off;  off += up128(kMaxChunks * 12 + 16);
+  p.bars = off;    off += 256;
   p.total = off;
+  const int rows_per_cta = (E + grid - 1) / grid;
+  // chunks per CTA <= units / cap + experts spanned (<= units / I + 1) + 1
+  const long long umax = (E < R * k) ? E : (long long)R * k;
+  const long long units = (umax * I + grid - 1) / grid;
+  const long long chunks = (cap ? (units + (long long)cap - 1) / (long long)cap : 1 << 30) + units / I + 2;
+  p.router_fits = cap >= 1 && p.max_orows <= kAccStride && chunks <= kMaxChunks &&
+                  kRouterOffset + (size_t)rows_per_cta * H * 4 <= kGuSlots * p.gu_slot;
   return p;
+}
+
+__device__ void issue_gu_chunk(const RoundArgs& a, const LayerPtrs& W, const Tables& T, uint8_t* dst,
+                               uint32_t bar, const GuChunk& c) {
+  const size_t H = (size_t)a.H, I = (size_t)a.I;
+  const size_t u = (size_t)T.uni[c.ui];
+  const size_t first = u * I + (size_t)c.i0;  // unit index within the layer
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  mbar_expect_tx(bar, (uint32_t)((size_t)c.n * (H + H / 8)));
+  bulk_g2s(smem_u32(dst), W.gu_nib + first * H, (uint32_t)(c.n * H), bar);
+  bulk_g2s(smem_u32(dst + (size_t)c.n * H),
+           reinterpret_cast<const uint8_t*>(W.gu_sc) + first * (H / 8), (uint32_t)(c.n * (H / 8)), bar);
+}
+
+__device__ void issue_dn_chunk(const RoundArgs& a, const LayerPtrs& W, const Tables& T, uint8_t* dst,
+                               uint32_t bar, int ui, int o0, int no, size_t codes_room) {
+  const size_t H = (size_t)a.H, I = (size_t)a.I;
+  const size_t u = (size_t)T.uni[ui];
+  const size_t row0 = u * H + (size_t)o0;
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  mbar_expect_tx(bar, (uint32_t)((size_t)no * (I / 2 + I / 16)));
+  bulk_g2s(smem_u32(dst), W.dn_nib + row0 * (I / 2), (uint32_t)(no * (I / 2)), bar);
+  bulk_g2s(smem_u32(dst + codes_room), reinterpret_cast<const uint8_t*>(W.dn_sc) + row0 * (I / 16),
+           (uint32_t)(no * (I / 16)), bar);
+}
+
+// Activation pairs of one row for the lane's NBL blocks (see make_pairs).
+template <int NBL>
+struct XRow {
+  f2_t xp[NBL][16];
+  float xsum8[NBL];
+};
+
+template <int NBL>
+__device__ __forceinline__ void load_xrow(const uint16_t* x, int H, int row, int lane, XRow<NBL>& xr) {
+  const int NB = H >> 5;
+#pragma unroll
+  for (int t = 0; t < NBL; ++t) {
+    const int blk = lane + 32 * t;
+    xr.xsum8[t] = 0.f;
+    if (blk < NB) {
+      const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)row * H + 32 * blk);
+      float sum = 0.f;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint4 ua = __ldg(src + 2 * h), ub = __ldg(src + 2 * h + 1);
+        const uint32_t wa[4] = {ua.x, ua.y, ua.z, ua.w}, wb[4] = {ub.x, ub.y, ub.z, ub.w};
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+          const float va = (m & 1) ? bf16_hi(wa[m >> 1]) : bf16_lo(wa[m >> 1]);
+          const float vb = (m & 1) ? bf16_hi(wb[m >> 1]) : bf16_lo(wb[m >> 1]);
+          xr.xp[t][8 * h + m] = f2pack(va * slot_scale(m), vb * slot_scale(m));
+          sum = __fadd_rn(sum, va);
+          sum = __fadd_rn(sum, vb);
+        }
+      }
+      xr.xsum8[t] = -8.f * sum;
+    }
+  }
+}
+
+// One 32-element block dot for G activation sets: acc[g] gets 2^-62 sum n_k x_k.
+template <int G>
+__device__ __forceinline__ void block_dot(const uint4 nb, const f2_t* const* xp, float* dot) {
+  const BlockPairs bp = block_pairs(nb);
+  f2_t a0[G], a1[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) a0[g] = a1[g] = 0ull;
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    const f2_t e0 = slot_pair(bp, 0, m), e1 = slot_pair(bp, 1, m);
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      ffma2(a0[g], e0, xp[g][m]);
+      ffma2(a1[g], e1, xp[g][8 + m]);
+    }
+  }
+#pragma unroll
+  for (int g = 0; g < G; ++g) dot[g] = __fadd_rn(f2sum(a0[g]), f2sum(a1[g]));
+}
+
+// Gate/up of one chunk for rows at CSR positions pp .. pp+G-1.
+template <int NBL, int G>
+__device__ __forceinline__ void gateup_rows(const RoundArgs& a, const Tables& T, const uint8_t* slot,
+                                            const GuChunk& c, int pp, const uint16_t* x) {
+  const int H = a.H, NB = H >> 5;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  XRow<NBL> xr[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) load_xrow<NBL>(x, H, T.pair[pp + g] / a.k, lane, xr[g]);
+  const uint8_t* codes = slot;
+  const uint16_t* scales = reinterpret_cast<const uint16_t*>(slot + (size_t)c.n * H);
+  for (int t = warp; t < c.n; t += NW) {
+    float val[2][G];
+#pragma unroll
+    for (int wrow = 0; wrow < 2; ++wrow) {
+      float part[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) part[g] = 0.f;
+#pragma unroll
+      for (int tb = 0; tb < NBL; ++tb) {
+        const int blk = lane + 32 * tb;
+        if (blk < NB) {
+          const size_t w = (size_t)(t * 2 + wrow) * NB + blk;
+          const uint4 nb = *reinterpret_cast<const uint4*>(codes + w * 16);
+          const float sc = half_bits(scales[w]);
+          const f2_t* xps[G];
+#pragma unroll
+          for (int g = 0; g < G; ++g) xps[g] = xr[g].xp[tb];
+          float dot[G];
+          block_dot<G>(nb, xps, dot);
+#pragma unroll
+          for (int g = 0; g < G; ++g)
+            part[g] = __fmaf_rn(sc, __fmaf_rn(dot[g], 0x1p62f, xr[g].xsum8[tb]), part[g]);
+        }
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g) val[wrow][g] = warp_sum(part[g]);
+    }
+    if (lane < G) {
+      float gg = val[0][0], vv = val[1][0];
+#pragma unroll
+      for (int g = 1; g < G; ++g)
+        if (lane == g) {
+          gg = val[0][g];
+          vv = val[1][g];
+        }
+      const float hh = __fmul_rn(__fdiv_rn(gg, __fadd_rn(1.f, expf(-gg))), vv);
+      a.hbuf[(size_t)(pp + lane) * a.I + c.i0 + t] = hh;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------
+// P4: this CTA's output rows [o0, o0 + no) over every union expert, fixed order
+
+template <int G>
+__device__ __forceinline__ void down_rows(const RoundArgs& a, const Tables& T, const uint8_t* slot,
+                                          size_t codes_room, int no, int pp, float* s_acc) {
+  const int I = a.I, NBI = I >> 5;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  f2_t hp[G][16];
+  float hsum8[G];
+  int row[G];
+  float wgt[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    const int pair = T.pair[pp + g];
+    row[g] = pair / a.k;
+    wgt[g] = T.w[pair];
+    hsum8[g] = 0.f;
+    if (lane < NBI) {
+      // pair (16h + m, 16h + 8 + m) = float4 (4h + m/4) and (4h + 2 + m/4), component m % 4
+      const float4* src = reinterpret_cast<const float4*>(a.hbuf + (size_t)(pp + g) * I + 32 * lane);
+      float sum = 0.f;
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int c4 = 0; c4 < 2; ++c4) {
+          const float4 fa = __ldcg(src + 4 * h + c4), fb = __ldcg(src + 4 * h + 2 + c4);
+          const float va[4] = {fa.x, fa.y, fa.z, fa.w}, vb[4] = {fb.x, fb.y, fb.z, fb.w};
+#pragma unroll
+          for (int z = 0; z < 4; ++z) {
+            const int m = 4 * c4 + z;
+            hp[g][8 * h + m] = f2pack(va[z] * slot_scale(m), vb[z] * slot_scale(m));
+            sum = __fadd_rn(sum, va[z]);
+            sum = __fadd_rn(sum, vb[z]);
+          }
+        }
+      hsum8[g] = -8.f * sum;
+    }
+  }
+  const uint8_t* codes = slot;
+  const uint16_t* scales = reinterpret_cast<const uint16_t*>(slot + codes_room);
+  for (int ol = warp; ol < no; ol += NW) {
+    float part[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) part[g] = 0.f;
+    if (lane < NBI) {
+      const uint4 nb = *reinterpret_cast<const uint4*>(codes + ((size_t)ol * NBI + lane) * 16);
+      const float sc = half_bits(scales[ol * NBI + lane]);
+      const f2_t* hps[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) hps[g] = hp[g];
+      float dot[G];
+      block_dot<G>(nb, hps, dot);
+#pragma unroll
+      for (int g = 0; g < G; ++g) part[g] = __fmul_rn(sc, __fmaf_rn(dot[g], 0x1p62f, hsum8[g]));
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float y = warp_sum(part[g]);
+      if (lane == 0) s_acc[row[g] * kAccStride + ol] = __fmaf_rn(wgt[g], y, s_acc[row[g] * kAccStride + ol]);
+    }
+  }
 }
 
 template <int NBL>
 __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundArgs a) {
   extern __shared__ __align__(1024) unsigned char smem[];
   const int tid = threadIdx.x;
-  const SmemPlan P = smem_plan(a.H, a.E, a.R, a.k, (a.E + (int)gridDim.x - 1) / (int)gridDim.x);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P.bars);
-  const uint32_t bar_router = smem_u32(bars + 4);
-  float* s_rw = reinterpret_cast<float*>(smem + P.router);
-  // stage b: buffer at stage0 + b * stage, barriers bars[2b] (A) and bars[2b + 1] (B)
-  auto stage_of = [&](int b) {
-    return Stage{smem + P.stage0 + (size_t)b * P.stage, smem_u32(bars + 2 * b),
-                 smem_u32(bars + 2 * b + 1)};
-  };
-  float* s_part = reinterpret_cast<float*>(smem + P.gv);  // [64 weight rows][2 group rows][NBL]
-  float* s_h = s_part + 256;                               // [2][36]: 16 h pairs + -8 sum(h)
+  const int G = gridDim.x;
+  const SmemPlan P = smem_plan(a.H, a.I, a.E, a.R, a.k, G);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P.bars);  // [0..2] GU, [3..18] DN, [19] router
+  const uint32_t bar_router = smem_u32(bars + 3 + kDnSlots);
+  uint8_t* gu = smem + P.gu;
+  uint8_t* dn = smem + P.dn;
+  float* s_rw = reinterpret_cast<float*>(gu + kRouterOffset);
+  float* s_acc = reinterpret_cast<float*>(smem + P.acc);
+  GuChunk* s_chunks = reinterpret_cast<GuChunk*>(smem + P.chunks);
   Tables T{reinterpret_cast<int*>(smem + P.uni), reinterpret_cast<int*>(smem + P.csr),
            reinterpret_cast<int*>(smem + P.pair), reinterpret_cast<float*>(smem + P.w),
            reinterpret_cast<int*>(smem + P.nunion)};
-  // routing scratch lives in the (then idle) staging area
-  unsigned* s_mask = reinterpret_cast<unsigned*>(smem + P.stage0);
-  int* s_off_e = reinterpret_cast<int*>(smem + P.stage0 + (size_t)a.E * 4);
-  int* s_ids = reinterpret_cast<int*>(smem + P.stage0 + (size_t)a.E * 8);
+  // routing scratch lives in the (then idle) gate/up ring
+  unsigned* s_mask = reinterpret_cast<unsigned*>(gu);
+  int* s_off_e = reinterpret_cast<int*>(gu + (size_t)a.E * 4);
+  int* s_ids = reinterpret_cast<int*>(gu + (size_t)a.E * 8);
   if (tid == 0) {
-    for (int i = 0; i < 5; ++i) mbar_init(smem_u32(bars + i), 1);
+    for (int i = 0; i < 4 + kDnSlots; ++i) mbar_init(smem_u32(bars + i), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     issue_router_rows(a, a.layer[0].router, s_rw, bar_router);
   }
   __syncthreads();
   unsigned ph_router = 0u;
   bool router_pend = router_rows_of_cta(a.E) > 0;  // layer 0's rows are in flight
-
   Sync sy;
-  unsigned ph = 0u;    // parity to wait for: bit 2b = stage b's barrier A, bit 2b+1 = B
-  unsigned pend = 0u;  // copies in flight, same bit layout
+  unsigned gu_ph = 0u, gu_pend = 0u;  // bit q: parity / in flight, GU slot q
+  unsigned dn_ph = 0u, dn_pend = 0u;  // bit q: parity / in flight, DN slot q
   // Leaving early: give every copy still in flight a bounded chance to land (so no
   // bulk copy targets shared memory of an exited CTA), raise the abort flag, return.
   auto bail = [&]() {
-    for (int q = 0; q < 4; ++q)
-      if (pend & (1u << q))
-        mbar_wait_bounded(smem_u32(bars + q), (ph >> q) & 1u, a.status, kDefaultWaitCycles);
+    for (int q = 0; q < kGuSlots; ++q)
+      if (gu_pend & (1u << q))
+        mbar_wait_bounded(smem_u32(bars + q), (gu_ph >> q) & 1u, a.status, kDefaultWaitCycles);
+    for (int q = 0; q < kDnSlots; ++q)
+      if (dn_pend & (1u << q))
+        mbar_wait_bounded(smem_u32(bars + 3 + q), (dn_ph >> q) & 1u, a.status, kDefaultWaitCycles);
     if (router_pend) mbar_wait_bounded(bar_router, ph_router, a.status, kDefaultWaitCycles);
     if (tid == 0) atomicExch(a.bar + 33, 1u);
   };
-  const int G = gridDim.x, NS = a.I >> 5;
   const size_t RH = (size_t)a.R * a.H;
+  const int o0 = (int)(((long long)blockIdx.x * a.H) / G);
+  const int no = (int)(((long long)(blockIdx.x + 1) * a.H) / G) - o0;
+  const size_t codes_room = up128((size_t)P.max_orows * (a.I / 2));
   for (int l = 0; l < a.L; ++l) {
     const LayerPtrs& W = a.layer[l];
     const uint16_t* x = a.x + (size_t)l * RH;
@@ -893,43 +840,102 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
     const int U = route_phase(a, T, s_mask, s_off_e, s_ids, l);
     stamp(a, l, 3);
     if (a.route_only) return;
-    const int n_items = U * NS;
-    if (blockIdx.x >= n_items) stamp(a, l, 4);  // no item: "first data" = now
-    for (int n = 0; n < 2; ++n) {
-      const int it = blockIdx.x + n * G;
-      if (it < n_items) {
-        pend |= 3u << (2 * n);  // every thread tracks what thread 0 issues
-        if (tid == 0) issue_item(a, W, stage_of(n), T.uni[it / NS], it % NS);
+    // ---- plan this CTA's gate/up chunks; issue them and the down prefetch ----
+    if (tid == 0) {
+      const long long N = (long long)U * a.I;
+      long long cur = (blockIdx.x * N) / G;
+      const long long end = ((blockIdx.x + 1) * N) / G;
+      int nc = 0;
+      while (cur < end && nc < kMaxChunks) {
+        const int ui = (int)(cur / a.I), i0 = (int)(cur - (long long)ui * a.I);
+        long long n = end - cur;
+        if (n > a.I - i0) n = a.I - i0;
+        if (n > P.gu_cap) n = P.gu_cap;
+        s_chunks[nc++] = GuChunk{ui, i0, (int)n};
+        cur += n;
+      }
+      if (cur < end) {  // (the host rejects shapes that could get here) never drop work
+        atomicOr(a.status, kStatusTimeout);
+        atomicExch(a.bar + 33, 1u);
+      }
+      *reinterpret_cast<int*>(smem + P.chunks + kMaxChunks * 12) = nc;
+    }
+    __syncthreads();
+    const int n_chunks = *reinterpret_cast<const int*>(smem + P.chunks + kMaxChunks * 12);
+    for (int q = 0; q < kGuSlots && q < n_chunks; ++q) {
+      gu_pend |= 1u << q;
+      if (tid == 0) issue_gu_chunk(a, W, T, gu + q * P.gu_slot, smem_u32(bars + q), s_chunks[q]);
+    }
+    if (no > 0) {
+      for (int q = 0; q < kDnSlots && q < U; ++q) {
+        dn_pend |= 1u << q;
+        if (tid == 0)
+          issue_dn_chunk(a, W, T, dn + q * P.dn_slot, smem_u32(bars + 3 + q), q, o0, no, codes_room);
       }
     }
-    for (int n = 0;; ++n) {
-      const int it = blockIdx.x + n * G;
-      if (it >= n_items) break;
-      const int b = n & 1;
-      if (!compute_item<NBL>(a, T, stage_of(b), b, ph, pend, it / NS, it % NS, x, s_part, s_h,
-                             n == 0 ? l : -1)) {
+    // ---- gate/up ----
+    for (int n = 0; n < n_chunks; ++n) {
+      const int q = n % kGuSlots;
+      const bool ok = mbar_wait_bounded(smem_u32(bars + q), (gu_ph >> q) & 1u, a.status, a.wait_cycles);
+      if (__syncthreads_or(!ok)) {
         bail();
         return;
       }
-      // compute_item ends with a CTA barrier: the stage is free again
-      const int nxt = it + 2 * G;
-      if (nxt < n_items) {
-        pend |= 3u << (2 * b);
-        if (tid == 0) issue_item(a, W, stage_of(b), T.uni[nxt / NS], nxt % NS);
+      gu_ph ^= 1u << q;
+      gu_pend &= ~(1u << q);
+      if (n == 0) stamp(a, l, 4);
+      const GuChunk c = s_chunks[n];
+      const uint8_t* slot = gu + q * P.gu_slot;
+      const int p0 = T.csr_off[c.ui], p1 = T.csr_off[c.ui + 1];
+      for (int pp = p0; pp < p1; ++pp) gateup_rows<NBL, 1>(a, T, slot, c, pp, x);
+      __syncthreads();  // slot q free again
+      if (n + kGuSlots < n_chunks) {
+        gu_pend |= 1u << q;
+        if (tid == 0) issue_gu_chunk(a, W, T, gu + q * P.gu_slot, smem_u32(bars + q), s_chunks[n + kGuSlots]);
       }
     }
-    // the next layer's router rows can move in now: they do not depend on any data
+    if (n_chunks == 0) stamp(a, l, 4);
+    // the next layer's router rows can move in now (the GU ring is idle until then)
     if (l + 1 < a.L && router_rows_of_cta(a.E) > 0) {
       router_pend = true;
       if (tid == 0) issue_router_rows(a, a.layer[l + 1].router, s_rw, bar_router);
     }
     stamp(a, l, 5);
-    if (!grid_sync(a, sy)) {  // B2: all partials written
+    if (!grid_sync(a, sy)) {  // B2: every h written
       bail();
       return;
     }
     stamp(a, l, 6);
-    reduce_phase(a, T, a.out + (size_t)l * RH, reinterpret_cast<float*>(smem + P.stage1));
+    // ---- down: all union experts for this CTA's output rows, ascending expert id ----
+    for (int i = tid; i < a.R * kAccStride; i += NT) s_acc[i] = 0.f;
+    __syncthreads();
+    if (no > 0) {
+      for (int ui = 0; ui < U; ++ui) {
+        const int q = ui % kDnSlots;
+        const bool ok = mbar_wait_bounded(smem_u32(bars + 3 + q), (dn_ph >> q) & 1u, a.status, a.wait_cycles);
+        if (__syncthreads_or(!ok)) {
+          bail();
+          return;
+        }
+        dn_ph ^= 1u << q;
+        dn_pend &= ~(1u << q);
+        const uint8_t* slot = dn + q * P.dn_slot;
+        const int p0 = T.csr_off[ui], p1 = T.csr_off[ui + 1];
+        for (int pp = p0; pp < p1; ++pp) down_rows<1>(a, T, slot, codes_room, no, pp, s_acc);
+        __syncthreads();  // slot q free again
+        if (ui + kDnSlots < U) {
+          dn_pend |= 1u << q;
+          if (tid == 0)
+            issue_dn_chunk(a, W, T, dn + q * P.dn_slot, smem_u32(bars + 3 + q), ui + kDnSlots, o0, no,
+                           codes_room);
+        }
+      }
+      float* out = a.out + (size_t)l * RH;
+      for (int i = tid; i < a.R * no; i += NT) {
+        const int r = i / no, ol = i - (i / no) * no;
+        out[(size_t)r * a.H + o0 + ol] = s_acc[r * kAccStride + ol];
+      }
+    }
     stamp(a, l, 7);
     if (l + 1 < a.L && !grid_sync(a, sy)) {  // B3: layer output complete
       bail();
@@ -1010,7 +1016,7 @@ int check_layer(const moe_layer_w* w) {
 }
 
 size_t smem_bytes(const moe_dims& d, int rows, int grid) {
-  return smem_plan(d.hidden, d.n_experts, rows, d.top_k, (d.n_experts + grid - 1) / grid).total;
+  return smem_plan(d.hidden, d.inter, d.n_experts, rows, d.top_k, grid).total;
 }
 
 void fill_args(RoundArgs& a, const moe_handle* h, int rows, void* ws) {
@@ -1024,7 +1030,7 @@ void fill_args(RoundArgs& a, const moe_handle* h, int rows, void* ws) {
   a.R = rows;
   a.bar = reinterpret_cast<unsigned*>(base + L.ctrl);
   a.logits = reinterpret_cast<float*>(base + L.logits);
-  a.partial = reinterpret_cast<float*>(base + L.partial);
+  a.hbuf = reinterpret_cast<float*>(base + L.hbuf);
   a.status = h->status;
   const unsigned long long ns = h->wait_ns < (1ull << 40) ? h->wait_ns : (1ull << 40);
   a.wait_cycles = (long long)ns * kCyclesPerNs;
@@ -1104,8 +1110,8 @@ int moe_create(const moe_dims* dims, int device, moe_handle** out) {
     return MOE_ECUDA;
   }
   const size_t smem = smem_bytes(*dims, dims->max_rows, sms);
-  const SmemPlan plan = smem_plan(dims->hidden, dims->n_experts, dims->max_rows, dims->top_k,
-                                  (dims->n_experts + sms - 1) / sms);
+  const SmemPlan plan = smem_plan(dims->hidden, dims->inter, dims->n_experts, dims->max_rows,
+                                  dims->top_k, sms);
   if (smem + 1024 > 227 * 1024 || !plan.router_fits) return MOE_EUNSUPPORTED;
   moe_handle* h = new moe_handle();
   h->dims = *dims;
@@ -1348,7 +1354,7 @@ int moe_profile_phases(moe_handle* h, double* mean_us, double* max_us, int32_t n
 // Some callers cannot allocate device memory at all: code that runs inside another
 // framework's memory pool with allocation disabled, allocation-free real-time or
 // embedded loops, or hosts that forbid cudaMalloc after start-up.  For them the
-// workspace (grid-barrier words, router logits, split-K partials) lives in the file-
+// workspace (grid-barrier words, router logits, exchanged SwiGLU outputs) lives in the file-
 // scope array below, which the CUDA runtime places on every device that loads this
 // library and keeps until the process exits.  The caller passes only inputs and
 // outputs; this path calls no cudaMalloc, cudaFree or allocating library routine.
@@ -1427,8 +1433,7 @@ extern "C" int moe_decode_layer_noalloc(const moe_dims* dims, const moe_layer_w*
     return MOE_ECUDA;
   }
   const size_t smem = smem_bytes(*dims, rows, sms);
-  const SmemPlan plan = smem_plan(dims->hidden, dims->n_experts, rows, dims->top_k,
-                                  (dims->n_experts + sms - 1) / sms);
+  const SmemPlan plan = smem_plan(dims->hidden, dims->inter, dims->n_experts, rows, dims->top_k, sms);
   if (smem + 1024 > 227 * 1024 || !plan.router_fits) return MOE_EUNSUPPORTED;
   NoAllocDevice* d = nullptr;
   if ((rc = noalloc_setup(dev, smem, &d)) != MOE_OK) return rc;
@@ -1445,14 +1450,14 @@ extern "C" int moe_decode_layer_noalloc(const moe_dims* dims, const moe_layer_w*
   a.L = 1;
   a.bar = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + L.ctrl);
   a.logits = reinterpret_cast<float*>(static_cast<char*>(ws) + L.logits);
-  a.partial = reinterpret_cast<float*>(static_cast<char*>(ws) + L.partial);
+  a.hbuf = reinterpret_cast<float*>(static_cast<char*>(ws) + L.hbuf);
   a.status = dev_status ? dev_status : own_status;
   a.wait_cycles = kDefaultWaitCycles;
   a.x = x_bf16;
   a.out = out;
   copy_layers(a, w, 1);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // the barrier words must start at zero; logits and partials are fully overwritten
+  // the barrier words must start at zero; logits and h are fully overwritten
   if (cudaMemsetAsync(a.bar, 0, 256, st) != cudaSuccess) return MOE_ECUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(sms);

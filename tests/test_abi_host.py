@@ -60,13 +60,13 @@ def test_workspace_sizes():
     d = dims()
     w1, w16 = mv.moe_workspace_bytes(d, 1), mv.moe_workspace_bytes(d, 16)
     assert 0 < w1 < w16
-    # dominated by split-K partials: rows * k * (I/32) * H fp32
-    assert w16 >= 16 * 8 * 24 * 2048 * 4
+    # dominated by the exchanged SwiGLU outputs: rows * k * I fp32
+    assert w16 >= 16 * 8 * 768 * 4
     assert mv.moe_workspace_bytes(d, 0) == 0 and mv.moe_workspace_bytes(d, 17) == 0
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(hidden=2000), mv.MOE_EINVAL), (dict(inter=100), mv.MOE_EINVAL),
+    (dict(hidden=2000), mv.MOE_EINVAL), (dict(inter=100), mv.MOE_EINVAL), (dict(inter=96), mv.MOE_EUNSUPPORTED),
     (dict(top_k=200), mv.MOE_EINVAL), (dict(top_k=0), mv.MOE_EINVAL),
     (dict(max_rows=0), mv.MOE_EINVAL), (dict(hidden=4096), mv.MOE_EUNSUPPORTED),
     (dict(hidden=384), mv.MOE_EUNSUPPORTED), (dict(max_rows=33), mv.MOE_EUNSUPPORTED),
@@ -100,29 +100,28 @@ def test_null_handle_calls_are_rejected():
 
 # ---- packer: decode the documented layout independently and compare ---------------------
 
-def _decode_gateup(nib, sc, E, H, I):
-    NB, NS = H // 32, I // 32
-    by = nib.reshape(E, NS, 2, 32, NB, 16)
+def _decode_blocks(by):
     lo = (by & 15).astype(np.int8) - 8
     hi = (by >> 4).astype(np.int8) - 8
-    codes = np.stack([lo, hi], axis=-1).reshape(E, NS, 2, 32, NB * 32)
-    q = codes.transpose(0, 2, 1, 3, 4).reshape(E, 2, I, H)
-    s = sc.reshape(E, NS, 2, 32, NB).transpose(0, 2, 1, 3, 4).reshape(E, 2, I, NB)
-    return q[:, 0], q[:, 1], s[:, 0], s[:, 1]
+    return np.stack([lo, hi], axis=-1)
+
+
+def _decode_gateup(nib, sc, E, H, I):
+    # codes [E][I][2: gate, up][H/32][16 B], scales [E][I][2][H/32]
+    NB = H // 32
+    codes = _decode_blocks(nib.reshape(E, I, 2, NB, 16)).reshape(E, I, 2, H)
+    s = sc.reshape(E, I, 2, NB)
+    return codes[:, :, 0], codes[:, :, 1], s[:, :, 0], s[:, :, 1]
 
 
 def _decode_down(nib, sc, E, H, I):
-    NS = I // 32
-    by = nib.reshape(E, NS, H, 16)
-    lo = (by & 15).astype(np.int8) - 8
-    hi = (by >> 4).astype(np.int8) - 8
-    codes = np.stack([lo, hi], axis=-1).reshape(E, NS, H, 32)
-    q = codes.transpose(0, 2, 1, 3).reshape(E, H, I)
-    s = sc.reshape(E, NS, H).transpose(0, 2, 1)
-    return q, s
+    # codes [E][H][I/32][16 B], scales [E][H][I/32]
+    NBI = I // 32
+    codes = _decode_blocks(nib.reshape(E, H, NBI, 16)).reshape(E, H, I)
+    return codes, sc.reshape(E, H, NBI)
 
 
-@pytest.mark.parametrize("H,I,E", [(256, 32, 1), (512, 256, 3), (2048, 96, 2)])
+@pytest.mark.parametrize("H,I,E", [(256, 256, 1), (512, 256, 3), (2048, 512, 2)])
 def test_packer_layout_roundtrip(H, I, E):
     rng = np.random.default_rng(H + I + E)
     d = mv.make_dims(H, max(E, 2), 1, I, 1)
@@ -152,25 +151,27 @@ def test_packer_layout_roundtrip(H, I, E):
 
 def test_packer_one_hot_nibble_order():
     # element 2t -> low nibble of byte t, element 2t+1 -> high nibble, stored as q + 8
-    H, I = 256, 32
+    H, I = 256, 256
     d = mv.make_dims(H, 2, 1, I, 1)
     qd = np.zeros((1, H, I), np.int8)
-    qd[0, 5, 3] = 7   # o = 5, i = 3: block s = 0, byte 1, high nibble
-    sd = np.zeros((1, H, 1), np.uint16)
+    qd[0, 5, 35] = 7   # o = 5, i = 35: block 1 of row 5, byte 1, high nibble
+    sd = np.zeros((1, H, I // 32), np.uint16)
     nib = np.zeros(mv.moe_packed_bytes(d, 1, 0), np.uint8)
     sc = np.zeros(mv.moe_packed_bytes(d, 1, 1) // 2, np.uint16)
     mv.moe_pack_q4(d, mv.MOE_DOWN, 1, qd.ctypes.data, sd.ctypes.data, None, None, nib.ctypes.data, sc.ctypes.data)
-    blk = nib[5 * 16:6 * 16]
+    off = (5 * (I // 32) + 1) * 16
+    blk = nib[off:off + 16]
     assert blk[1] == (8 | (15 << 4))
     assert all(b == 0x88 for i, b in enumerate(blk) if i != 1)
+    assert (np.delete(nib, np.arange(off, off + 16)) == 0x88).all()
 
 
 def test_packer_rejects_out_of_range_codes():
-    H, I = 256, 32
+    H, I = 256, 256
     d = mv.make_dims(H, 2, 1, I, 1)
     qd = np.zeros((1, H, I), np.int8)
     qd[0, 0, 0] = 8
-    sd = np.zeros((1, H, 1), np.uint16)
+    sd = np.zeros((1, H, I // 32), np.uint16)
     nib = np.zeros(mv.moe_packed_bytes(d, 1, 0), np.uint8)
     sc = np.zeros(mv.moe_packed_bytes(d, 1, 1) // 2, np.uint16)
     with pytest.raises(mv.MoeError) as ei:
