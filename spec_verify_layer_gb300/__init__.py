@@ -25,7 +25,7 @@ ABI_SYMBOLS = (
     "moe_last_launch_count", "moe_set_wait_limit_ns", "moe_profile", "moe_profile_read",
     "moe_profile_phases", "moe_decode_layer_noalloc", "moe_strerror",
 )
-MOE_NOALLOC_SCRATCH_BYTES = 16 << 20
+MOE_NOALLOC_SCRATCH_BYTES = 4 << 20
 KIND_ROUND = 0
 PHASES = ("router", "barrier1", "routing", "first_data", "gateup", "barrier2", "down", "barrier3")
 

@@ -62,6 +62,7 @@ struct LayerPtrs {
 
 struct RoundArgs {
   int H, E, k, I, R, L;
+  int Rmax;  // the handle's max_rows: the shared-memory plan is sized by it, not by R
   int route_only;
   const uint16_t* x;  // [L][R][H] bf16 bits
   float* out;         // [L][R][H]
@@ -775,7 +776,7 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
   extern __shared__ __align__(1024) unsigned char smem[];
   const int tid = threadIdx.x;
   const int G = gridDim.x;
-  const SmemPlan P = smem_plan(a.H, a.I, a.E, a.R, a.k, G);
+  const SmemPlan P = smem_plan(a.H, a.I, a.E, a.Rmax, a.k, G);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P.bars);  // [0..2] GU, [3..18] DN, [19] router
   const uint32_t bar_router = smem_u32(bars + 3 + kDnSlots);
   uint8_t* gu = smem + P.gu;
@@ -1028,6 +1029,7 @@ void fill_args(RoundArgs& a, const moe_handle* h, int rows, void* ws) {
   a.k = d.top_k;
   a.I = d.inter;
   a.R = rows;
+  a.Rmax = d.max_rows;
   a.bar = reinterpret_cast<unsigned*>(base + L.ctrl);
   a.logits = reinterpret_cast<float*>(base + L.logits);
   a.hbuf = reinterpret_cast<float*>(base + L.hbuf);
@@ -1055,7 +1057,7 @@ cudaError_t launch_round(moe_handle* h, const RoundArgs& a, cudaStream_t st, boo
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(h->sm_count);
   cfg.blockDim = dim3(NT);
-  cfg.dynamicSmemBytes = smem_bytes(h->dims, a.R, h->sm_count);
+  cfg.dynamicSmemBytes = smem_bytes(h->dims, h->dims.max_rows, h->sm_count);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
@@ -1361,7 +1363,7 @@ int moe_profile_phases(moe_handle* h, double* mean_us, double* max_us, int32_t n
 
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = (size_t)16 << 20;  // 16 MiB per device
+constexpr size_t kNoAllocScratchBytes = (size_t)4 << 20;  // 4 MiB per device
 constexpr int kNoAllocMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
@@ -1432,8 +1434,9 @@ extern "C" int moe_decode_layer_noalloc(const moe_dims* dims, const moe_layer_w*
     cudaGetLastError();
     return MOE_ECUDA;
   }
-  const size_t smem = smem_bytes(*dims, rows, sms);
-  const SmemPlan plan = smem_plan(dims->hidden, dims->inter, dims->n_experts, rows, dims->top_k, sms);
+  const size_t smem = smem_bytes(*dims, dims->max_rows, sms);
+  const SmemPlan plan =
+      smem_plan(dims->hidden, dims->inter, dims->n_experts, dims->max_rows, dims->top_k, sms);
   if (smem + 1024 > 227 * 1024 || !plan.router_fits) return MOE_EUNSUPPORTED;
   NoAllocDevice* d = nullptr;
   if ((rc = noalloc_setup(dev, smem, &d)) != MOE_OK) return rc;
@@ -1447,6 +1450,7 @@ extern "C" int moe_decode_layer_noalloc(const moe_dims* dims, const moe_layer_w*
   a.k = dd.top_k;
   a.I = dd.inter;
   a.R = rows;
+  a.Rmax = dd.max_rows;
   a.L = 1;
   a.bar = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + L.ctrl);
   a.logits = reinterpret_cast<float*>(static_cast<char*>(ws) + L.logits);

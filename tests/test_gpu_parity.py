@@ -272,3 +272,30 @@ def test_bounded_wait_reports_timeout_without_hanging():
         assert_close(got, ref, "after timeout")
     finally:
         s.close()
+
+
+def test_calls_with_fewer_rows_than_the_handle_allows():
+    """A handle sized for 16 rows serves 1-row and 16-row calls (shared-memory plan is
+    fixed by the handle, not by the call)."""
+    cfg = syngen.CONFIGS["a3b_r1"]
+    s = Stack(cfg, n_layers=1, max_rows=16)
+    try:
+        router = syngen.router(cfg, 0)
+        for R, sigma in ((1, 0.0), (16, 0.1)):
+            xb = s.rows(0, R, sigma)
+            got = run_layer(s, 0, xb)
+            rt = oracle.route(router, xb, cfg.top_k)
+            ref = oracle.layer(router, xb, cfg.top_k, rt.union, syngen.experts_stacked(cfg, 0, rt.union))
+            assert_close(got, ref, f"max_rows 16, R={R}")
+        dev = s.device
+        xs = np.stack([s.rows(0, 1, 0.0)])
+        x = torch.from_numpy(xs.view(np.int16)).to(dev)
+        out = torch.empty((1, 1, cfg.hidden), device=dev)
+        ws = s.ws(1)
+        st = torch.cuda.Stream(dev)
+        mv.moe_round(s.handle, [s.layers[0].w], x.data_ptr(), 1, out.data_ptr(), None, ws.data_ptr(), ws.numel(),
+                     True, st.cuda_stream)
+        assert mv.moe_last_device_status(s.handle, st.cuda_stream) == mv.MOE_OK
+        np.testing.assert_array_equal(out.cpu().numpy()[0], run_layer(s, 0, xs[0]))
+    finally:
+        s.close()

@@ -52,10 +52,15 @@ def test_noalloc_matches_decode_layer_twice(name, rows, sigma):
 
 
 def test_noalloc_rejects_layers_beyond_its_scratch():
-    cfg = syngen.CONFIGS["a3b_r16"]
-    dims = mv.make_dims(cfg.hidden, cfg.experts, cfg.top_k, cfg.inter, 16)
-    need = 256 + mv.moe_workspace_bytes(dims, 16)
+    # 32 rows x top-32 x intermediate 2048 needs 8 MiB of exchanged activations
+    dims = mv.make_dims(2048, 64, 32, 2048, 32)
+    need = 256 + mv.moe_workspace_bytes(dims, 32)
     assert need > mv.MOE_NOALLOC_SCRATCH_BYTES
     w = mv.make_layer_w(256, 256, 256, 256, 256)  # never dereferenced: rejected first
-    rc = mv.lib().moe_decode_layer_noalloc(ctypes.byref(dims), ctypes.byref(w), 256, 16, 256, None, None)
+    rc = mv.lib().moe_decode_layer_noalloc(ctypes.byref(dims), ctypes.byref(w), 256, 32, 256, None, None)
     assert rc == mv.MOE_EWORKSPACE
+    # every workload shape of this layer fits
+    for name in ("tiny", "a3b_r1", "a3b_r4", "a3b_r16", "e512_r3"):
+        cfg = syngen.CONFIGS[name]
+        d = mv.make_dims(cfg.hidden, cfg.experts, cfg.top_k, cfg.inter, cfg.rows)
+        assert 256 + mv.moe_workspace_bytes(d, cfg.rows) <= mv.MOE_NOALLOC_SCRATCH_BYTES
