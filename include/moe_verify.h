@@ -159,8 +159,10 @@ int moe_set_wait_limit_ns(moe_handle* h, uint64_t ns);
  * and the launch count (kind must be 0: the fused round kernel).
  * moe_profile_phases returns, for the last profiled moe_round, the mean over CTAs and
  * layers (mean_us) and the per-layer maximum over CTAs averaged over layers (max_us)
- * of eight phases: router GEMV, barrier 1, routing, wait for the first staged gate/up
- * chunk, gate/up stream, barrier 2, down pass and combine, barrier 3.  n_phases >= 8. */
+ * of twelve phases: router GEMV, barrier 1, routing, wait for the first staged gate/up
+ * chunk, gate/up until the last chunk has landed, gate/up after it, barrier 2, wait for
+ * the first exchanged h rows, down pass until the last down or h rows have landed, down
+ * pass after it, output write, barrier 3.  n_phases >= 12. */
 int moe_profile(moe_handle* h, int enable);
 int moe_profile_read(moe_handle* h, int kind, double* total_ms, int32_t* launches);
 int moe_profile_phases(moe_handle* h, double* mean_us, double* max_us, int32_t n_phases);

@@ -27,7 +27,8 @@ ABI_SYMBOLS = (
 )
 MOE_NOALLOC_SCRATCH_BYTES = 4 << 20
 KIND_ROUND = 0
-PHASES = ("router", "barrier1", "routing", "first_data", "gateup", "barrier2", "down", "barrier3")
+PHASES = ("router", "barrier1", "routing", "first_data", "gateup_stream", "gateup_tail",
+          "barrier2", "down_wait", "down_stream", "down_tail", "out_write", "barrier3")
 
 
 class moe_dims(ctypes.Structure):

@@ -50,7 +50,7 @@ constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // 2 s
 // ns (at ~2 GHz) and a few times ns at lower clocks
 constexpr long long kCyclesPerNs = 2;
 constexpr long long kDefaultWaitCycles = (long long)kDefaultWaitNs * kCyclesPerNs;
-constexpr int kPhases = 9;  // phase stamps per layer when profiling (8 intervals)
+constexpr int kPhases = 13;  // phase stamps per layer when profiling (12 intervals)
 
 struct LayerPtrs {
   const float* router;
@@ -522,10 +522,14 @@ __device__ int route_phase(const RoundArgs& a, const Tables& T, unsigned* s_mask
 // prefetched into kDnSlots slots meanwhile (they depend only on the routing).
 
 constexpr int kGuSlots = 3;
-constexpr int kDnSlots = 16;
+constexpr int kDnSlots = 11;
+constexpr size_t kXBytes = 32768;  // the layer's bf16 rows, staged once per layer when they fit
 constexpr int kMaxChunks = 96;
-constexpr size_t kRouterOffset = 16384;  // router rows sit after the routing scratch
-constexpr int kAccStride = 64;           // output rows per CTA are at most this many
+// Inside the gate/up ring, idle outside the gate/up stream: the next layer's router rows
+// at offset 0 (consumed before the routing scratch, also at offset 0, is written) and,
+// from kHOffset on, two slots of exchanged h rows for the down pass.
+constexpr size_t kHOffset = 32768;
+constexpr int kAccStride = 64;  // output rows per CTA are at most this many
 
 struct GuChunk {
   int ui, i0, n;
@@ -533,8 +537,10 @@ struct GuChunk {
 
 // smem plan: GU ring | DN slots | tables | out accumulators | chunk list | barriers
 struct SmemPlan {
-  size_t gu_slot, gu, dn_slot, dn, uni, csr, pair, w, nunion, acc, chunks, bars, total;
+  size_t gu_slot, gu, dn_slot, dn, xrows, uni, csr, pair, w, nunion, acc, chunks, bars, total;
+  size_t h_slot;  // bytes per h slot (two slots from gu + kHOffset)
   int gu_cap;     // units per gate/up chunk
+  int h_rows;     // h rows (CSR positions) per h slot
   int max_orows;  // output rows per CTA (ceil(H / grid))
   bool router_fits;
 };
@@ -549,7 +555,7 @@ __host__ __device__ inline SmemPlan smem_plan(int H, int I, int E, int R, int k,
   const size_t tables = up128((size_t)E * 4) + up128((size_t)(E + 1) * 4) +
                         2 * up128((size_t)R * k * 4) + 128 + up128((size_t)R * kAccStride * 4) +
                         up128(kMaxChunks * 12 + 16) + 256;
-  const size_t budget = (size_t)225 * 1024 - tables - kDnSlots * p.dn_slot;
+  const size_t budget = (size_t)225 * 1024 - tables - kDnSlots * p.dn_slot - kXBytes;
   size_t cap = (budget / kGuSlots) / unit;
   if (cap > 64) cap = 64;
   p.gu_cap = (int)cap;
@@ -557,6 +563,7 @@ __host__ __device__ inline SmemPlan smem_plan(int H, int I, int E, int R, int k,
   size_t off = 0;
   p.gu = off;      off += kGuSlots * p.gu_slot;
   p.dn = off;      off += kDnSlots * p.dn_slot;
+  p.xrows = off;   off += kXBytes;
   p.uni = off;     off += up128((size_t)E * 4);
   p.csr = off;     off += up128((size_t)(E + 1) * 4);
   p.pair = off;    off += up128((size_t)R * k * 4);
@@ -571,8 +578,11 @@ __host__ __device__ inline SmemPlan smem_plan(int H, int I, int E, int R, int k,
   const long long umax = (E < R * k) ? E : (long long)R * k;
   const long long units = (umax * I + grid - 1) / grid;
   const long long chunks = (cap ? (units + (long long)cap - 1) / (long long)cap : 1 << 30) + units / I + 2;
-  p.router_fits = cap >= 1 && p.max_orows <= kAccStride && chunks <= kMaxChunks &&
-                  kRouterOffset + (size_t)rows_per_cta * H * 4 <= kGuSlots * p.gu_slot;
+  const size_t ring = kGuSlots * p.gu_slot;
+  p.h_slot = ring > kHOffset ? ((ring - kHOffset) / 2) & ~(size_t)127 : 0;
+  p.h_rows = (int)(p.h_slot / ((size_t)I * 4));
+  p.router_fits = cap >= 1 && p.max_orows <= kAccStride && chunks <= kMaxChunks && p.h_rows >= 1 &&
+                  (size_t)rows_per_cta * H * 4 <= kHOffset;
   return p;
 }
 
@@ -609,6 +619,7 @@ struct XRow {
 
 template <int NBL>
 __device__ __forceinline__ void load_xrow(const uint16_t* x, int H, int row, int lane, XRow<NBL>& xr) {
+  // x: the layer's rows, in shared memory when staged (else global, read-only)
   const int NB = H >> 5;
 #pragma unroll
   for (int t = 0; t < NBL; ++t) {
@@ -619,7 +630,7 @@ __device__ __forceinline__ void load_xrow(const uint16_t* x, int H, int row, int
       float sum = 0.f;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const uint4 ua = __ldg(src + 2 * h), ub = __ldg(src + 2 * h + 1);
+        const uint4 ua = src[2 * h], ub = src[2 * h + 1];
         const uint32_t wa[4] = {ua.x, ua.y, ua.z, ua.w}, wb[4] = {ub.x, ub.y, ub.z, ub.w};
 #pragma unroll
         for (int m = 0; m < 8; ++m) {
@@ -702,7 +713,9 @@ __device__ __forceinline__ void gateup_rows(const RoundArgs& a, const Tables& T,
           vv = val[1][g];
         }
       const float hh = __fmul_rn(__fdiv_rn(gg, __fadd_rn(1.f, expf(-gg))), vv);
-      a.hbuf[(size_t)(pp + lane) * a.I + c.i0 + t] = hh;
+      // h row layout: element i = 32 b + 4 q + z at float index (q * I/32 + b) * 4 + z
+      const int i = c.i0 + t, b = i >> 5, q = (i >> 2) & 7, z = i & 3;
+      a.hbuf[(size_t)(pp + lane) * a.I + ((size_t)q * (a.I >> 5) + b) * 4 + z] = hh;
     }
   }
 }
@@ -710,9 +723,13 @@ __device__ __forceinline__ void gateup_rows(const RoundArgs& a, const Tables& T,
 // ---------------------------------------------------------------------------------
 // P4: this CTA's output rows [o0, o0 + no) over every union expert, fixed order
 
+// Down pass for h rows at CSR positions pp .. pp+G-1, whose h rows sit in shared memory
+// at s_hrows (row stride I floats, block-interleaved: lane b reads float4 q at
+// (q * I/32 + b) * 4, so a warp's loads are conflict-free).
 template <int G>
 __device__ __forceinline__ void down_rows(const RoundArgs& a, const Tables& T, const uint8_t* slot,
-                                          size_t codes_room, int no, int pp, float* s_acc) {
+                                          size_t codes_room, int no, int pp, const float* s_hrows,
+                                          float* s_acc) {
   const int I = a.I, NBI = I >> 5;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   f2_t hp[G][16];
@@ -727,13 +744,13 @@ __device__ __forceinline__ void down_rows(const RoundArgs& a, const Tables& T, c
     hsum8[g] = 0.f;
     if (lane < NBI) {
       // pair (16h + m, 16h + 8 + m) = float4 (4h + m/4) and (4h + 2 + m/4), component m % 4
-      const float4* src = reinterpret_cast<const float4*>(a.hbuf + (size_t)(pp + g) * I + 32 * lane);
+      const float4* src = reinterpret_cast<const float4*>(s_hrows + (size_t)g * I) + lane;
       float sum = 0.f;
 #pragma unroll
       for (int h = 0; h < 2; ++h)
 #pragma unroll
         for (int c4 = 0; c4 < 2; ++c4) {
-          const float4 fa = __ldcg(src + 4 * h + c4), fb = __ldcg(src + 4 * h + 2 + c4);
+          const float4 fa = src[(4 * h + c4) * NBI], fb = src[(4 * h + 2 + c4) * NBI];
           const float va[4] = {fa.x, fa.y, fa.z, fa.w}, vb[4] = {fb.x, fb.y, fb.z, fb.w};
 #pragma unroll
           for (int z = 0; z < 4; ++z) {
@@ -771,17 +788,44 @@ __device__ __forceinline__ void down_rows(const RoundArgs& a, const Tables& T, c
   }
 }
 
+// h batches for the down pass: consecutive CSR positions (all union experts, in order)
+// in runs of <= h_rows; the h rows of consecutive positions are contiguous.
+struct HBatch {
+  int pa, pb;
+};
+
+__device__ __forceinline__ bool next_hbatch(const Tables& T, int U, int h_rows, HBatch& cur) {
+  const int total = T.csr_off[U];
+  if (cur.pb >= total) return false;
+  const int pa = cur.pb;
+  cur = HBatch{pa, (pa + h_rows < total) ? pa + h_rows : total};
+  return true;
+}
+
+__device__ __forceinline__ void issue_hbatch(const RoundArgs& a, uint8_t* dst, uint32_t bar,
+                                             const HBatch& hb) {
+  const size_t bytes = (size_t)(hb.pb - hb.pa) * a.I * 4;
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  mbar_expect_tx(bar, (uint32_t)bytes);
+  bulk_g2s(smem_u32(dst), a.hbuf + (size_t)hb.pa * a.I, (uint32_t)bytes, bar);
+}
+
 template <int NBL>
 __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundArgs a) {
   extern __shared__ __align__(1024) unsigned char smem[];
   const int tid = threadIdx.x;
   const int G = gridDim.x;
   const SmemPlan P = smem_plan(a.H, a.I, a.E, a.Rmax, a.k, G);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P.bars);  // [0..2] GU, [3..18] DN, [19] router
+  // barriers: [0..2] GU slots, [3..3+kDnSlots) DN slots, then router, 2 h slots, x rows
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P.bars);
   const uint32_t bar_router = smem_u32(bars + 3 + kDnSlots);
+  const int bar_h0 = 4 + kDnSlots;
+  const uint32_t bar_x = smem_u32(bars + 6 + kDnSlots);
+  uint16_t* s_x = reinterpret_cast<uint16_t*>(smem + P.xrows);
+  const bool x_staged = (size_t)a.R * a.H * 2 <= kXBytes;
   uint8_t* gu = smem + P.gu;
   uint8_t* dn = smem + P.dn;
-  float* s_rw = reinterpret_cast<float*>(gu + kRouterOffset);
+  float* s_rw = reinterpret_cast<float*>(gu);
   float* s_acc = reinterpret_cast<float*>(smem + P.acc);
   GuChunk* s_chunks = reinterpret_cast<GuChunk*>(smem + P.chunks);
   Tables T{reinterpret_cast<int*>(smem + P.uni), reinterpret_cast<int*>(smem + P.csr),
@@ -792,7 +836,7 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
   int* s_off_e = reinterpret_cast<int*>(gu + (size_t)a.E * 4);
   int* s_ids = reinterpret_cast<int*>(gu + (size_t)a.E * 8);
   if (tid == 0) {
-    for (int i = 0; i < 4 + kDnSlots; ++i) mbar_init(smem_u32(bars + i), 1);
+    for (int i = 0; i < 7 + kDnSlots; ++i) mbar_init(smem_u32(bars + i), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     issue_router_rows(a, a.layer[0].router, s_rw, bar_router);
   }
@@ -802,6 +846,9 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
   Sync sy;
   unsigned gu_ph = 0u, gu_pend = 0u;  // bit q: parity / in flight, GU slot q
   unsigned dn_ph = 0u, dn_pend = 0u;  // bit q: parity / in flight, DN slot q
+  unsigned h_ph = 0u, h_pend = 0u;    // bit q: parity / in flight, h slot q
+  unsigned x_ph = 0u;
+  bool x_pend = false;
   // Leaving early: give every copy still in flight a bounded chance to land (so no
   // bulk copy targets shared memory of an exited CTA), raise the abort flag, return.
   auto bail = [&]() {
@@ -811,7 +858,11 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
     for (int q = 0; q < kDnSlots; ++q)
       if (dn_pend & (1u << q))
         mbar_wait_bounded(smem_u32(bars + 3 + q), (dn_ph >> q) & 1u, a.status, kDefaultWaitCycles);
+    for (int q = 0; q < 2; ++q)
+      if (h_pend & (1u << q))
+        mbar_wait_bounded(smem_u32(bars + bar_h0 + q), (h_ph >> q) & 1u, a.status, kDefaultWaitCycles);
     if (router_pend) mbar_wait_bounded(bar_router, ph_router, a.status, kDefaultWaitCycles);
+    if (x_pend) mbar_wait_bounded(bar_x, x_ph, a.status, kDefaultWaitCycles);
     if (tid == 0) atomicExch(a.bar + 33, 1u);
   };
   const size_t RH = (size_t)a.R * a.H;
@@ -822,6 +873,16 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
     const LayerPtrs& W = a.layer[l];
     const uint16_t* x = a.x + (size_t)l * RH;
     stamp(a, l, 0);
+    // this layer's rows into shared memory for the gate/up pass (the previous layer's
+    // gate/up pass is long done with the buffer)
+    if (x_staged && !a.route_only) {
+      x_pend = true;
+      if (tid == 0) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_expect_tx(bar_x, (uint32_t)(RH * 2));
+        bulk_g2s(smem_u32(s_x), x, (uint32_t)(RH * 2), bar_x);
+      }
+    }
     if (router_pend) {
       const bool ok = mbar_wait_bounded(bar_router, ph_router, a.status, a.wait_cycles);
       if (__syncthreads_or(!ok)) {
@@ -875,6 +936,17 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
       }
     }
     // ---- gate/up ----
+    const uint16_t* xg = x;
+    if (x_pend) {
+      const bool ok = mbar_wait_bounded(bar_x, x_ph, a.status, a.wait_cycles);
+      if (__syncthreads_or(!ok)) {
+        bail();
+        return;
+      }
+      x_ph ^= 1u;
+      x_pend = false;
+      xg = s_x;
+    }
     for (int n = 0; n < n_chunks; ++n) {
       const int q = n % kGuSlots;
       const bool ok = mbar_wait_bounded(smem_u32(bars + q), (gu_ph >> q) & 1u, a.status, a.wait_cycles);
@@ -885,64 +957,109 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
       gu_ph ^= 1u << q;
       gu_pend &= ~(1u << q);
       if (n == 0) stamp(a, l, 4);
+      stamp(a, l, 5);  // (the last chunk's stamp stays)
       const GuChunk c = s_chunks[n];
       const uint8_t* slot = gu + q * P.gu_slot;
       const int p0 = T.csr_off[c.ui], p1 = T.csr_off[c.ui + 1];
-      for (int pp = p0; pp < p1; ++pp) gateup_rows<NBL, 1>(a, T, slot, c, pp, x);
+      for (int pp = p0; pp < p1; ++pp) gateup_rows<NBL, 1>(a, T, slot, c, pp, xg);
       __syncthreads();  // slot q free again
       if (n + kGuSlots < n_chunks) {
         gu_pend |= 1u << q;
         if (tid == 0) issue_gu_chunk(a, W, T, gu + q * P.gu_slot, smem_u32(bars + q), s_chunks[n + kGuSlots]);
       }
     }
-    if (n_chunks == 0) stamp(a, l, 4);
+    if (n_chunks == 0) {
+      stamp(a, l, 4);
+      stamp(a, l, 5);
+    }
     // the next layer's router rows can move in now (the GU ring is idle until then)
     if (l + 1 < a.L && router_rows_of_cta(a.E) > 0) {
       router_pend = true;
       if (tid == 0) issue_router_rows(a, a.layer[l + 1].router, s_rw, bar_router);
     }
-    stamp(a, l, 5);
+    stamp(a, l, 6);
     if (!grid_sync(a, sy)) {  // B2: every h written
       bail();
       return;
     }
-    stamp(a, l, 6);
+    stamp(a, l, 7);
     // ---- down: all union experts for this CTA's output rows, ascending expert id ----
     for (int i = tid; i < a.R * kAccStride; i += NT) s_acc[i] = 0.f;
     __syncthreads();
     if (no > 0) {
-      for (int ui = 0; ui < U; ++ui) {
-        const int q = ui % kDnSlots;
-        const bool ok = mbar_wait_bounded(smem_u32(bars + 3 + q), (dn_ph >> q) & 1u, a.status, a.wait_cycles);
-        if (__syncthreads_or(!ok)) {
+      // h rows come in batches of consecutive CSR positions through two slots
+      HBatch hb_issue{0, 0}, hb{0, 0};
+      for (int q = 0; q < 2; ++q) {
+        if (!next_hbatch(T, U, P.h_rows, hb_issue)) break;
+        h_pend |= 1u << q;
+        if (tid == 0) issue_hbatch(a, gu + kHOffset + q * P.h_slot, smem_u32(bars + bar_h0 + q), hb_issue);
+      }
+      int cur_ui = -1;
+      for (int n = 0; next_hbatch(T, U, P.h_rows, hb); ++n) {
+        const int qh = n & 1;
+        const bool okh = mbar_wait_bounded(smem_u32(bars + bar_h0 + qh), (h_ph >> qh) & 1u, a.status, a.wait_cycles);
+        if (__syncthreads_or(!okh)) {
           bail();
           return;
         }
-        dn_ph ^= 1u << q;
-        dn_pend &= ~(1u << q);
-        const uint8_t* slot = dn + q * P.dn_slot;
-        const int p0 = T.csr_off[ui], p1 = T.csr_off[ui + 1];
-        for (int pp = p0; pp < p1; ++pp) down_rows<1>(a, T, slot, codes_room, no, pp, s_acc);
-        __syncthreads();  // slot q free again
-        if (ui + kDnSlots < U) {
-          dn_pend |= 1u << q;
-          if (tid == 0)
-            issue_dn_chunk(a, W, T, dn + q * P.dn_slot, smem_u32(bars + 3 + q), ui + kDnSlots, o0, no,
-                           codes_room);
+        h_ph ^= 1u << qh;
+        h_pend &= ~(1u << qh);
+        if (n == 0) stamp(a, l, 8);
+        stamp(a, l, 9);
+        const float* s_hrows = reinterpret_cast<const float*>(gu + kHOffset + qh * P.h_slot);
+        for (int pp = hb.pa; pp < hb.pb; ++pp) {
+          if (pp >= (cur_ui < 0 ? 0 : T.csr_off[cur_ui + 1])) {
+            // the next expert: its down rows must have landed; the previous expert's
+            // slot is refilled with a later expert (everyone is past it)
+            const int prev = cur_ui;
+            do {
+              ++cur_ui;
+            } while (pp >= T.csr_off[cur_ui + 1]);
+            __syncthreads();
+            if (prev >= 0 && prev + kDnSlots < U) {
+              const int qd = prev % kDnSlots;
+              dn_pend |= 1u << qd;
+              if (tid == 0)
+                issue_dn_chunk(a, W, T, dn + qd * P.dn_slot, smem_u32(bars + 3 + qd), prev + kDnSlots, o0, no,
+                               codes_room);
+            }
+            const int qd = cur_ui % kDnSlots;
+            const bool okd = mbar_wait_bounded(smem_u32(bars + 3 + qd), (dn_ph >> qd) & 1u, a.status, a.wait_cycles);
+            if (__syncthreads_or(!okd)) {
+              bail();
+              return;
+            }
+            dn_ph ^= 1u << qd;
+            dn_pend &= ~(1u << qd);
+            stamp(a, l, 9);  // (the last wait's stamp stays)
+          }
+          down_rows<1>(a, T, dn + (cur_ui % kDnSlots) * P.dn_slot, codes_room, no, pp,
+                       s_hrows + (size_t)(pp - hb.pa) * a.I, s_acc);
+        }
+        __syncthreads();  // h slot qh free again
+        if (next_hbatch(T, U, P.h_rows, hb_issue)) {
+          h_pend |= 1u << qh;
+          if (tid == 0) issue_hbatch(a, gu + kHOffset + qh * P.h_slot, smem_u32(bars + bar_h0 + qh), hb_issue);
         }
       }
+      stamp(a, l, 10);
       float* out = a.out + (size_t)l * RH;
       for (int i = tid; i < a.R * no; i += NT) {
         const int r = i / no, ol = i - (i / no) * no;
         out[(size_t)r * a.H + o0 + ol] = s_acc[r * kAccStride + ol];
       }
     }
-    stamp(a, l, 7);
+    if (no <= 0 || U == 0) {
+      stamp(a, l, 8);
+      stamp(a, l, 9);
+      stamp(a, l, 10);
+    }
+    stamp(a, l, 11);
     if (l + 1 < a.L && !grid_sync(a, sy)) {  // B3: layer output complete
       bail();
       return;
     }
-    stamp(a, l, 8);  // (the last layer has no B3: its interval is zero)
+    stamp(a, l, 12);  // (the last layer has no B3: its interval is zero)
   }
 }
 
