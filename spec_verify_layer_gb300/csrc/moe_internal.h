@@ -20,8 +20,9 @@ constexpr int kMaxLayers = 128;  // layers per moe_round call (weight table trav
 int check_dims(const moe_dims* d);
 
 // Byte offsets of the workspace regions for `rows` rows (each region 256-aligned):
-// grid-barrier words, router logits [rows][E], SwiGLU outputs h [rows*k][I] (fp32, one
-// row per routed (row, expert) pair, grouped by expert).
+// grid-barrier words, router logits [rows][E], weighted SwiGLU outputs h' [rows*k][I]
+// (fp32, one row per routed (row, expert) pair, grouped by expert, in the kernel's
+// operand-pair order).
 struct WsLayout {
   size_t ctrl, logits, hbuf, total;
 };

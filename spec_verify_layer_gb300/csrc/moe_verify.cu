@@ -12,14 +12,17 @@
 //       the (row, rank) pairs that picked it (CSR).
 //   P3  gate/up: the U * I units (gate row i + up row i of a union expert) are split
 //       evenly and contiguously across CTAs and streamed through shared-memory slots
-//       with 1-D bulk TMA copies; for every row of the expert a warp computes g and v
-//       and stores h = silu(g) v to the workspace.  Meanwhile the down rows of every
-//       union expert for this CTA's share of the output rows are prefetched.
-//   B2  (every h written)
-//   P4  down: for each union expert in ascending id order, each of this CTA's output
-//       rows o gets y = Wd[o] . h for every row of the expert, accumulated as
-//       out[r][o] += w_{r,e} y in shared memory -- a fixed order, so a row's output
-//       depends only on that row (bitwise), whatever shares the round.
+//       with 1-D bulk TMA copies; a warp takes two units at a time for two rows of
+//       the expert at a time and stores h' = w silu(g) v (w the row's routing weight)
+//       to the workspace, already in the operand layout the down pass consumes.
+//       Meanwhile the down rows of every union expert for this CTA's share of the
+//       output rows are prefetched.
+//   B2  (every h' written)
+//   P4  down: the h' rows come back by bulk copy in waves of up to 8 CSR positions,
+//       one warp per position over all of this CTA's output rows o: y = Wd[o] . h'.
+//       Each row's y are added in CSR order (its experts ascending) in shared memory
+//       -- a fixed order, so a row's output depends only on that row (bitwise),
+//       whatever shares the round.
 //   B3  (layer l+1's router waits for layer l's output, as a real decode would)
 //
 // Dequantisation without a convert instruction: a nibble n placed in bits [p, p+4) of
@@ -69,7 +72,7 @@ struct RoundArgs {
   int* stats;         // [L] |U| per layer, or null
   unsigned* bar;      // [0] barrier arrivals, [33] abort flag
   float* logits;      // [R][E]
-  float* hbuf;        // [R*k][I] SwiGLU outputs by CSR position
+  float* hbuf;        // [R*k][I] weighted SwiGLU outputs h' by CSR position, pair layout
   int* user_ids;      // moe_route outputs (CTA 0 writes them)
   float* user_w;
   int* user_union;
@@ -255,14 +258,19 @@ __device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-__device__ bool grid_sync(const RoundArgs& a, Sync& sy) {
-  __shared__ int s_ok;
+// Arrival half: the CTA's earlier writes are published by the CTA barrier and the
+// release add.  Work that touches nothing other CTAs write may sit between the halves.
+__device__ __forceinline__ void grid_arrive(const RoundArgs& a, Sync& sy) {
   __syncthreads();
+  sy.epoch += 1;
+  if (threadIdx.x == 0) red_release_add(a.bar, 1u);
+}
+
+__device__ bool grid_wait(const RoundArgs& a, const Sync& sy) {
+  __shared__ int s_ok;
   if (threadIdx.x == 0) {
-    sy.epoch += 1;
     const unsigned target = sy.epoch * gridDim.x;
     unsigned* abort_flag = a.bar + 33;
-    red_release_add(a.bar, 1u);
     int ok = 1;
     const long long t0 = clock64();
     while (ld_acquire(a.bar) < target) {
@@ -281,6 +289,11 @@ __device__ bool grid_sync(const RoundArgs& a, Sync& sy) {
   }
   __syncthreads();
   return s_ok != 0;
+}
+
+__device__ __forceinline__ bool grid_sync(const RoundArgs& a, Sync& sy) {
+  grid_arrive(a, sy);
+  return grid_wait(a, sy);
 }
 
 __device__ __forceinline__ void stamp(const RoundArgs& a, int l, int ph) {
@@ -523,7 +536,9 @@ __device__ int route_phase(const RoundArgs& a, const Tables& T, unsigned* s_mask
 
 constexpr int kGuSlots = 3;
 constexpr int kDnSlots = 11;
-constexpr size_t kXBytes = 32768;  // the layer's bf16 rows, staged once per layer when they fit
+// the layer's rows as operand pairs plus block sums (4 rows at hidden 2048), staged once
+// per layer when they fit
+constexpr size_t kXBytes = 33792;
 constexpr int kMaxChunks = 96;
 // Inside the gate/up ring, idle outside the gate/up stream: the next layer's router rows
 // at offset 0 (consumed before the routing scratch, also at offset 0, is written) and,
@@ -535,9 +550,11 @@ struct GuChunk {
   int ui, i0, n;
 };
 
-// smem plan: GU ring | DN slots | tables | out accumulators | chunk list | barriers
+// smem plan: GU ring | DN slots | x pairs | tables | out accumulators | wave outputs |
+// chunk list | barriers
 struct SmemPlan {
-  size_t gu_slot, gu, dn_slot, dn, xrows, uni, csr, pair, w, nunion, acc, chunks, bars, total;
+  size_t gu_slot, gu, dn_slot, dn, xrows, uni, csr, pair, w, nunion, acc, ybuf, chunks, bars, total;
+  size_t ring;    // bytes of the gate/up ring (>= kGuSlots * gu_slot)
   size_t h_slot;  // bytes per h slot (two slots from gu + kHOffset)
   int gu_cap;     // units per gate/up chunk
   int h_rows;     // h rows (CSR positions) per h slot
@@ -554,14 +571,19 @@ __host__ __device__ inline SmemPlan smem_plan(int H, int I, int E, int R, int k,
   p.dn_slot = up128((size_t)p.max_orows * (I / 2)) + up128((size_t)p.max_orows * (I / 16));
   const size_t tables = up128((size_t)E * 4) + up128((size_t)(E + 1) * 4) +
                         2 * up128((size_t)R * k * 4) + 128 + up128((size_t)R * kAccStride * 4) +
-                        up128(kMaxChunks * 12 + 16) + 256;
-  const size_t budget = (size_t)225 * 1024 - tables - kDnSlots * p.dn_slot - kXBytes;
-  size_t cap = (budget / kGuSlots) / unit;
-  if (cap > 64) cap = 64;
+                        up128((size_t)NW * kAccStride * 4) + up128(kMaxChunks * 12 + 16) + 256;
+  const size_t fixed = tables + kDnSlots * p.dn_slot + kXBytes;
+  const size_t limit = (size_t)225 * 1024;
+  size_t cap = fixed < limit ? ((limit - fixed) / kGuSlots) / unit : 0;
+  if (cap > 2 * NW) cap = 2 * NW;  // a chunk is one pass of the warps over unit pairs
   p.gu_cap = (int)cap;
   p.gu_slot = up128(cap * unit);
+  // small shapes: keep room behind kHOffset for full waves of exchanged h rows
+  p.ring = kGuSlots * p.gu_slot;
+  const size_t want = kHOffset + 2 * up128((size_t)NW * I * 4);
+  if (p.ring < want && fixed + want <= limit) p.ring = want;
   size_t off = 0;
-  p.gu = off;      off += kGuSlots * p.gu_slot;
+  p.gu = off;      off += p.ring;
   p.dn = off;      off += kDnSlots * p.dn_slot;
   p.xrows = off;   off += kXBytes;
   p.uni = off;     off += up128((size_t)E * 4);
@@ -570,6 +592,7 @@ __host__ __device__ inline SmemPlan smem_plan(int H, int I, int E, int R, int k,
   p.w = off;       off += up128((size_t)R * k * 4);
   p.nunion = off;  off += 128;
   p.acc = off;     off += up128((size_t)R * kAccStride * 4);
+  p.ybuf = off;    off += up128((size_t)NW * kAccStride * 4);
   p.chunks = off;  off += up128(kMaxChunks * 12 + 16);
   p.bars = off;    off += 256;
   p.total = off;
@@ -578,8 +601,7 @@ __host__ __device__ inline SmemPlan smem_plan(int H, int I, int E, int R, int k,
   const long long umax = (E < R * k) ? E : (long long)R * k;
   const long long units = (umax * I + grid - 1) / grid;
   const long long chunks = (cap ? (units + (long long)cap - 1) / (long long)cap : 1 << 30) + units / I + 2;
-  const size_t ring = kGuSlots * p.gu_slot;
-  p.h_slot = ring > kHOffset ? ((ring - kHOffset) / 2) & ~(size_t)127 : 0;
+  p.h_slot = p.ring > kHOffset ? ((p.ring - kHOffset) / 2) & ~(size_t)127 : 0;
   p.h_rows = (int)(p.h_slot / ((size_t)I * 4));
   p.router_fits = cap >= 1 && p.max_orows <= kAccStride && chunks <= kMaxChunks && p.h_rows >= 1 &&
                   (size_t)rows_per_cta * H * 4 <= kHOffset;
@@ -610,43 +632,99 @@ __device__ void issue_dn_chunk(const RoundArgs& a, const LayerPtrs& W, const Tab
            (uint32_t)(no * (I / 16)), bar);
 }
 
-// Activation pairs of one row for the lane's NBL blocks (see make_pairs).
-template <int NBL>
-struct XRow {
-  f2_t xp[NBL][16];
-  float xsum8[NBL];
-};
+// ---------------------------------------------------------------------------------
+// Operand pairs.  The word pairs above consume a block's 32 elements as 16 f32x2
+// operands: pair p holds elements (16(p/8) + p%8, 16(p/8) + 8 + p%8), pre-scaled by
+// slot_scale(p%8).  Activations (once per layer) and exchanged h rows (by their
+// producer) are kept in this form, block-interleaved: float4 c of block b (pairs 2c
+// and 2c+1) sits at float4 index c * NBlk + b, so lane b's eight 16-byte loads are
+// conflict-free.
 
-template <int NBL>
-__device__ __forceinline__ void load_xrow(const uint16_t* x, int H, int row, int lane, XRow<NBL>& xr) {
-  // x: the layer's rows, in shared memory when staged (else global, read-only)
-  const int NB = H >> 5;
+// Float index of element j of block b in a pair-layout row of NBlk blocks.
+__device__ __forceinline__ int pair_index(int b, int j, int NBlk) {
+  const int p = ((j >> 4) << 3) | (j & 7);
+  return (((p >> 1) * NBlk + b) << 2) | ((p & 1) << 1) | ((j >> 3) & 1);
+}
+
+__device__ __forceinline__ void f2unpack(f2_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0,%1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+// 2^-(exponent of slot_scale(m)): exact inverse of the slot factor.
+__device__ __forceinline__ float inv_slot_scale(int m) {
+  const int e = (m <= 4) ? 87 - 4 * m : 99 - 4 * m;
+  return __int_as_float((127 - e) << 23);
+}
+
+// One block of bf16 activations (four 16-byte words, elements 0..31) -> its 16
+// operand pairs and -8 times the block sum (summed pair by pair).
+__device__ __forceinline__ void convert_block(const uint4 (&u)[4], f2_t (&xp)[16], float& xsum8) {
+  float sum = 0.f;
 #pragma unroll
-  for (int t = 0; t < NBL; ++t) {
-    const int blk = lane + 32 * t;
-    xr.xsum8[t] = 0.f;
-    if (blk < NB) {
-      const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)row * H + 32 * blk);
-      float sum = 0.f;
+  for (int h = 0; h < 2; ++h) {
+    const uint4 ua = u[2 * h], ub = u[2 * h + 1];
+    const uint32_t wa[4] = {ua.x, ua.y, ua.z, ua.w}, wb[4] = {ub.x, ub.y, ub.z, ub.w};
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const uint4 ua = src[2 * h], ub = src[2 * h + 1];
-        const uint32_t wa[4] = {ua.x, ua.y, ua.z, ua.w}, wb[4] = {ub.x, ub.y, ub.z, ub.w};
-#pragma unroll
-        for (int m = 0; m < 8; ++m) {
-          const float va = (m & 1) ? bf16_hi(wa[m >> 1]) : bf16_lo(wa[m >> 1]);
-          const float vb = (m & 1) ? bf16_hi(wb[m >> 1]) : bf16_lo(wb[m >> 1]);
-          xr.xp[t][8 * h + m] = f2pack(va * slot_scale(m), vb * slot_scale(m));
-          sum = __fadd_rn(sum, va);
-          sum = __fadd_rn(sum, vb);
-        }
-      }
-      xr.xsum8[t] = -8.f * sum;
+    for (int m = 0; m < 8; ++m) {
+      const float va = (m & 1) ? bf16_hi(wa[m >> 1]) : bf16_lo(wa[m >> 1]);
+      const float vb = (m & 1) ? bf16_hi(wb[m >> 1]) : bf16_lo(wb[m >> 1]);
+      xp[8 * h + m] = f2pack(va * slot_scale(m), vb * slot_scale(m));
+      sum = __fadd_rn(sum, va);
+      sum = __fadd_rn(sum, vb);
     }
+  }
+  xsum8 = -8.f * sum;
+}
+
+// This layer's rows as operand pairs in shared memory: s_xp [R][8][NB] float4 and
+// s_xs [R][NB] (-8 x block sums).  Done while the router barrier completes.
+__device__ void stage_xpairs(const RoundArgs& a, const uint16_t* x, float4* s_xp, float* s_xs) {
+  const int NB = a.H >> 5;
+  for (int idx = threadIdx.x; idx < a.R * NB; idx += NT) {
+    const int r = idx / NB, b = idx - r * NB;
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)r * a.H + 32 * b);
+    uint4 u[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) u[i] = __ldg(src + i);
+    f2_t xp[16];
+    float xs;
+    convert_block(u, xp, xs);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      float a0, a1, b0, b1;
+      f2unpack(xp[2 * c], a0, a1);
+      f2unpack(xp[2 * c + 1], b0, b1);
+      s_xp[((size_t)r * 8 + c) * NB + b] = make_float4(a0, a1, b0, b1);
+    }
+    s_xs[r * NB + b] = xs;
   }
 }
 
-// One 32-element block dot for G activation sets: acc[g] gets 2^-62 sum n_k x_k.
+// Operand pairs of block blk of one row: from the staged pairs (XS) or converted from
+// the bf16 row in global memory (rows too many to stage).
+template <bool XS>
+__device__ __forceinline__ void load_xblock(const RoundArgs& a, const uint16_t* x, const float4* s_xp,
+                                            const float* s_xs, int row, int blk, f2_t (&xp)[16],
+                                            float& xsum8) {
+  const int NB = a.H >> 5;
+  if (XS) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const float4 f = s_xp[((size_t)row * 8 + c) * NB + blk];
+      xp[2 * c] = f2pack(f.x, f.y);
+      xp[2 * c + 1] = f2pack(f.z, f.w);
+    }
+    xsum8 = s_xs[row * NB + blk];
+  } else {
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)row * a.H + 32 * blk);
+    uint4 u[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) u[i] = __ldg(src + i);
+    convert_block(u, xp, xsum8);
+  }
+}
+
+// One 32-element block dot for G activation sets: dot[g] = 2^-62 sum n_k x_k.
 template <int G>
 __device__ __forceinline__ void block_dot(const uint4 nb, const f2_t* const* xp, float* dot) {
   const BlockPairs bp = block_pairs(nb);
@@ -666,167 +744,195 @@ __device__ __forceinline__ void block_dot(const uint4 nb, const f2_t* const* xp,
   for (int g = 0; g < G; ++g) dot[g] = __fadd_rn(f2sum(a0[g]), f2sum(a1[g]));
 }
 
-// Gate/up of one chunk for rows at CSR positions pp .. pp+G-1.
-template <int NBL, int G>
-__device__ __forceinline__ void gateup_rows(const RoundArgs& a, const Tables& T, const uint8_t* slot,
-                                            const GuChunk& c, int pp, const uint16_t* x) {
-  const int H = a.H, NB = H >> 5;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  XRow<NBL> xr[G];
+// V values per lane (V a power of two <= 16) summed over the warp; value v ends in
+// lanes [v 32/V, (v+1) 32/V).  Each value is summed over the same xor tree of lane bits
+// 4..0 as warp_sum (only the operand order of commutative adds differs), so its result
+// does not depend on the slot it travels in.
+template <int V>
+__device__ __forceinline__ float warp_sum_multi(float (&v)[V], int lane) {
+  constexpr int LOGV = (V >= 16) ? 4 : (V >= 8) ? 3 : (V >= 4) ? 2 : (V >= 2) ? 1 : 0;
+  static_assert((1 << LOGV) == V, "V must be a power of two <= 16");
 #pragma unroll
-  for (int g = 0; g < G; ++g) load_xrow<NBL>(x, H, T.pair[pp + g] / a.k, lane, xr[g]);
+  for (int s = 0; s < LOGV; ++s) {
+    const int n = V >> s, o = 16 >> s;
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      const float send = upper ? v[i] : v[i + n / 2];
+      const float keep = upper ? v[i + n / 2] : v[i];
+      v[i] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, o));
+    }
+  }
+  float s = v[0];
+#pragma unroll
+  for (int o = 16 >> LOGV; o >= 1; o >>= 1) s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, o));
+  return s;
+}
+
+// Gate/up of units t0 and (if has1) t0 + NW of chunk c for the rows at CSR positions
+// pp .. pp+G-1: per lane its NBL blocks of the four weight rows, one multi-value
+// reduction, then the lane holding a (unit, row) gate value takes the up value from the
+// next lane group and stores h' = w silu(g) v, pre-scaled, in pair layout.
+template <int NBL, int G, bool XS>
+__device__ __forceinline__ void gateup_units(const RoundArgs& a, const Tables& T, const uint8_t* slot,
+                                             const GuChunk& c, int t0, bool has1, int pp,
+                                             const uint16_t* x, const float4* s_xp, const float* s_xs) {
+  const int H = a.H, NB = H >> 5;
+  const int lane = threadIdx.x & 31;
+  int row[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) row[g] = T.pair[pp + g] / a.k;
   const uint8_t* codes = slot;
   const uint16_t* scales = reinterpret_cast<const uint16_t*>(slot + (size_t)c.n * H);
-  for (int t = warp; t < c.n; t += NW) {
-    float val[2][G];
+  constexpr int V = 4 * G;  // value (u G + g) 2 + wrow
+  float v[V];
 #pragma unroll
-    for (int wrow = 0; wrow < 2; ++wrow) {
-      float part[G];
+  for (int i = 0; i < V; ++i) v[i] = 0.f;
 #pragma unroll
-      for (int g = 0; g < G; ++g) part[g] = 0.f;
+  for (int tb = 0; tb < NBL; ++tb) {
+    const int blk = lane + 32 * tb;
+    if (blk < NB) {
+      f2_t xp[G][16];
+      float xsum8[G];
 #pragma unroll
-      for (int tb = 0; tb < NBL; ++tb) {
-        const int blk = lane + 32 * tb;
-        if (blk < NB) {
-          const size_t w = (size_t)(t * 2 + wrow) * NB + blk;
-          const uint4 nb = *reinterpret_cast<const uint4*>(codes + w * 16);
-          const float sc = half_bits(scales[w]);
-          const f2_t* xps[G];
+      for (int g = 0; g < G; ++g) load_xblock<XS>(a, x, s_xp, s_xs, row[g], blk, xp[g], xsum8[g]);
+      const f2_t* xps[G];
 #pragma unroll
-          for (int g = 0; g < G; ++g) xps[g] = xr[g].xp[tb];
-          float dot[G];
-          block_dot<G>(nb, xps, dot);
+      for (int g = 0; g < G; ++g) xps[g] = xp[g];
 #pragma unroll
-          for (int g = 0; g < G; ++g)
-            part[g] = __fmaf_rn(sc, __fmaf_rn(dot[g], 0x1p62f, xr[g].xsum8[tb]), part[g]);
+      for (int u = 0; u < 2; ++u) {
+        if (u == 0 || has1) {
+          const int t = t0 + u * NW;
+#pragma unroll
+          for (int wrow = 0; wrow < 2; ++wrow) {
+            const size_t w = (size_t)(t * 2 + wrow) * NB + blk;
+            const uint4 nb = *reinterpret_cast<const uint4*>(codes + w * 16);
+            const float sc = half_bits(scales[w]);
+            float dot[G];
+            block_dot<G>(nb, xps, dot);
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+              float& acc = v[(u * G + g) * 2 + wrow];
+              acc = __fmaf_rn(sc, __fmaf_rn(dot[g], 0x1p62f, xsum8[g]), acc);
+            }
+          }
         }
       }
-#pragma unroll
-      for (int g = 0; g < G; ++g) val[wrow][g] = warp_sum(part[g]);
     }
-    if (lane < G) {
-      float gg = val[0][0], vv = val[1][0];
-#pragma unroll
-      for (int g = 1; g < G; ++g)
-        if (lane == g) {
-          gg = val[0][g];
-          vv = val[1][g];
-        }
-      const float hh = __fmul_rn(__fdiv_rn(gg, __fadd_rn(1.f, expf(-gg))), vv);
-      // h row layout: element i = 32 b + 4 q + z at float index (q * I/32 + b) * 4 + z
-      const int i = c.i0 + t, b = i >> 5, q = (i >> 2) & 7, z = i & 3;
-      a.hbuf[(size_t)(pp + lane) * a.I + ((size_t)q * (a.I >> 5) + b) * 4 + z] = hh;
+  }
+  const float s = warp_sum_multi<V>(v, lane);
+  constexpr int LPV = 32 / V;  // lanes per value
+  const float up = __shfl_down_sync(0xffffffffu, s, LPV);
+  const int vi = lane / LPV;
+  if ((lane % LPV) == 0 && (vi & 1) == 0) {
+    const int si = vi >> 1, u = si / G, g = si - u * G;
+    if (u == 0 || has1) {
+      const int i = c.i0 + t0 + u * NW, j = i & 31;
+      const int pair = T.pair[pp + g];
+      const float hh = __fmul_rn(__fdiv_rn(s, __fadd_rn(1.f, expf(-s))), up);
+      const float hw = __fmul_rn(T.w[pair], hh);
+      a.hbuf[(size_t)(pp + g) * a.I + pair_index(i >> 5, j, a.I >> 5)] = hw * slot_scale(j & 7);
     }
+  }
+}
+
+// Gate/up of one staged chunk: warp w takes units w and w + NW (chunks hold at most
+// 2 NW units; larger ones loop), rows of the expert two at a time.
+template <int NBL, bool XS>
+__device__ __forceinline__ void gateup_chunk(const RoundArgs& a, const Tables& T, const uint8_t* slot,
+                                             const GuChunk& c, const uint16_t* x, const float4* s_xp,
+                                             const float* s_xs) {
+  const int warp = threadIdx.x >> 5;
+  const int p0 = T.csr_off[c.ui], p1 = T.csr_off[c.ui + 1];
+  for (int t0 = warp; t0 < c.n; t0 += 2 * NW) {
+    const bool has1 = t0 + NW < c.n;
+    int pp = p0;
+    for (; pp + 1 < p1; pp += 2) gateup_units<NBL, 2, XS>(a, T, slot, c, t0, has1, pp, x, s_xp, s_xs);
+    if (pp < p1) gateup_units<NBL, 1, XS>(a, T, slot, c, t0, has1, pp, x, s_xp, s_xs);
   }
 }
 
 // ---------------------------------------------------------------------------------
-// P4: this CTA's output rows [o0, o0 + no) over every union expert, fixed order
+// P4: this CTA's output rows [o0, o0 + no), a wave of CSR positions at a time
 
-// Down pass for h rows at CSR positions pp .. pp+G-1, whose h rows sit in shared memory
-// at s_hrows (row stride I floats, block-interleaved: lane b reads float4 q at
-// (q * I/32 + b) * 4, so a warp's loads are conflict-free).
-template <int G>
-__device__ __forceinline__ void down_rows(const RoundArgs& a, const Tables& T, const uint8_t* slot,
-                                          size_t codes_room, int no, int pp, const float* s_hrows,
-                                          float* s_acc) {
-  const int I = a.I, NBI = I >> 5;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  f2_t hp[G][16];
-  float hsum8[G];
-  int row[G];
-  float wgt[G];
+// y of one CSR position over this CTA's output rows: the position's h' row (pair
+// layout, shared memory) against each output row's down codes of its expert; y[ol]
+// to s_yw.  Lanes >= I/32 hold no block.
+__device__ __forceinline__ void down_position(const RoundArgs& a, const uint8_t* dslot, size_t codes_room,
+                                              int no, const float4* s_h, float* s_yw) {
+  const int NBI = a.I >> 5;
+  const int lane = threadIdx.x & 31;
+  f2_t hp[16];
+  float hsum8 = 0.f;
+  if (lane < NBI) {
 #pragma unroll
-  for (int g = 0; g < G; ++g) {
-    const int pair = T.pair[pp + g];
-    row[g] = pair / a.k;
-    wgt[g] = T.w[pair];
-    hsum8[g] = 0.f;
-    if (lane < NBI) {
-      // pair (16h + m, 16h + 8 + m) = float4 (4h + m/4) and (4h + 2 + m/4), component m % 4
-      const float4* src = reinterpret_cast<const float4*>(s_hrows + (size_t)g * I) + lane;
-      float sum = 0.f;
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int c4 = 0; c4 < 2; ++c4) {
-          const float4 fa = src[(4 * h + c4) * NBI], fb = src[(4 * h + 2 + c4) * NBI];
-          const float va[4] = {fa.x, fa.y, fa.z, fa.w}, vb[4] = {fb.x, fb.y, fb.z, fb.w};
-#pragma unroll
-          for (int z = 0; z < 4; ++z) {
-            const int m = 4 * c4 + z;
-            hp[g][8 * h + m] = f2pack(va[z] * slot_scale(m), vb[z] * slot_scale(m));
-            sum = __fadd_rn(sum, va[z]);
-            sum = __fadd_rn(sum, vb[z]);
-          }
-        }
-      hsum8[g] = -8.f * sum;
+    for (int c = 0; c < 8; ++c) {
+      const float4 f = s_h[c * NBI + lane];
+      hp[2 * c] = f2pack(f.x, f.y);
+      hp[2 * c + 1] = f2pack(f.z, f.w);
     }
+    // -8 x the block sum of h', undoing each slot's power-of-two factor exactly
+    float sum = 0.f;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      float a0, a1, b0, b1;
+      f2unpack(hp[m], a0, a1);
+      f2unpack(hp[8 + m], b0, b1);
+      sum = __fmaf_rn(__fadd_rn(__fadd_rn(a0, a1), __fadd_rn(b0, b1)), inv_slot_scale(m), sum);
+    }
+    hsum8 = -8.f * sum;
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) hp[i] = 0ull;
   }
-  const uint8_t* codes = slot;
-  const uint16_t* scales = reinterpret_cast<const uint16_t*>(slot + codes_room);
-  for (int ol = warp; ol < no; ol += NW) {
-    float part[G];
+  const uint8_t* codes = dslot;
+  const uint16_t* scales = reinterpret_cast<const uint16_t*>(dslot + codes_room);
+  const f2_t* hps[1] = {hp};
+  for (int ob = 0; ob < no; ob += 8) {
+    float part[8];
 #pragma unroll
-    for (int g = 0; g < G; ++g) part[g] = 0.f;
-    if (lane < NBI) {
-      const uint4 nb = *reinterpret_cast<const uint4*>(codes + ((size_t)ol * NBI + lane) * 16);
-      const float sc = half_bits(scales[ol * NBI + lane]);
-      const f2_t* hps[G];
-#pragma unroll
-      for (int g = 0; g < G; ++g) hps[g] = hp[g];
-      float dot[G];
-      block_dot<G>(nb, hps, dot);
-#pragma unroll
-      for (int g = 0; g < G; ++g) part[g] = __fmul_rn(sc, __fmaf_rn(dot[g], 0x1p62f, hsum8[g]));
+    for (int jj = 0; jj < 8; ++jj) {
+      part[jj] = 0.f;
+      const int ol = ob + jj;
+      if (lane < NBI && ol < no) {
+        const uint4 nb = *reinterpret_cast<const uint4*>(codes + ((size_t)ol * NBI + lane) * 16);
+        const float sc = half_bits(scales[ol * NBI + lane]);
+        float dot[1];
+        block_dot<1>(nb, hps, dot);
+        part[jj] = __fmul_rn(sc, __fmaf_rn(dot[0], 0x1p62f, hsum8));
+      }
     }
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float y = warp_sum(part[g]);
-      if (lane == 0) s_acc[row[g] * kAccStride + ol] = __fmaf_rn(wgt[g], y, s_acc[row[g] * kAccStride + ol]);
-    }
+    const float y = warp_sum_multi<8>(part, lane);
+    if ((lane & 3) == 0 && ob + (lane >> 2) < no) s_yw[ob + (lane >> 2)] = y;
   }
 }
 
-// h batches for the down pass: consecutive CSR positions (all union experts, in order)
-// in runs of <= h_rows; the h rows of consecutive positions are contiguous.
-struct HBatch {
-  int pa, pb;
-};
-
-__device__ __forceinline__ bool next_hbatch(const Tables& T, int U, int h_rows, HBatch& cur) {
-  const int total = T.csr_off[U];
-  if (cur.pb >= total) return false;
-  const int pa = cur.pb;
-  cur = HBatch{pa, (pa + h_rows < total) ? pa + h_rows : total};
-  return true;
-}
-
-__device__ __forceinline__ void issue_hbatch(const RoundArgs& a, uint8_t* dst, uint32_t bar,
-                                             const HBatch& hb) {
-  const size_t bytes = (size_t)(hb.pb - hb.pa) * a.I * 4;
+// Exchanged h rows of CSR positions [pa, pb) (contiguous in the workspace) -> slot.
+__device__ __forceinline__ void issue_hbatch(const RoundArgs& a, uint8_t* dst, uint32_t bar, int pa, int pb) {
+  const size_t bytes = (size_t)(pb - pa) * a.I * 4;
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   mbar_expect_tx(bar, (uint32_t)bytes);
-  bulk_g2s(smem_u32(dst), a.hbuf + (size_t)hb.pa * a.I, (uint32_t)bytes, bar);
+  bulk_g2s(smem_u32(dst), a.hbuf + (size_t)pa * a.I, (uint32_t)bytes, bar);
 }
 
 template <int NBL>
 __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundArgs a) {
   extern __shared__ __align__(1024) unsigned char smem[];
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5;
   const int G = gridDim.x;
   const SmemPlan P = smem_plan(a.H, a.I, a.E, a.Rmax, a.k, G);
-  // barriers: [0..2] GU slots, [3..3+kDnSlots) DN slots, then router, 2 h slots, x rows
+  // mbarriers: kGuSlots GU slots, kDnSlots DN slots, the router rows, two h slots
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P.bars);
-  const uint32_t bar_router = smem_u32(bars + 3 + kDnSlots);
-  const int bar_h0 = 4 + kDnSlots;
-  const uint32_t bar_x = smem_u32(bars + 6 + kDnSlots);
-  uint16_t* s_x = reinterpret_cast<uint16_t*>(smem + P.xrows);
-  const bool x_staged = (size_t)a.R * a.H * 2 <= kXBytes;
+  const int bar_dn0 = kGuSlots, bar_h0 = kGuSlots + kDnSlots + 1;
+  const uint32_t bar_router = smem_u32(bars + kGuSlots + kDnSlots);
   uint8_t* gu = smem + P.gu;
   uint8_t* dn = smem + P.dn;
+  float4* s_xp = reinterpret_cast<float4*>(smem + P.xrows);
+  float* s_xs = reinterpret_cast<float*>(smem + P.xrows + (size_t)a.R * a.H * 4);
+  const bool x_staged = (size_t)a.R * a.H * 4 + (size_t)a.R * (a.H >> 5) * 4 <= kXBytes;
   float* s_rw = reinterpret_cast<float*>(gu);
   float* s_acc = reinterpret_cast<float*>(smem + P.acc);
+  float* s_y = reinterpret_cast<float*>(smem + P.ybuf);
   GuChunk* s_chunks = reinterpret_cast<GuChunk*>(smem + P.chunks);
   Tables T{reinterpret_cast<int*>(smem + P.uni), reinterpret_cast<int*>(smem + P.csr),
            reinterpret_cast<int*>(smem + P.pair), reinterpret_cast<float*>(smem + P.w),
@@ -836,7 +942,7 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
   int* s_off_e = reinterpret_cast<int*>(gu + (size_t)a.E * 4);
   int* s_ids = reinterpret_cast<int*>(gu + (size_t)a.E * 8);
   if (tid == 0) {
-    for (int i = 0; i < 7 + kDnSlots; ++i) mbar_init(smem_u32(bars + i), 1);
+    for (int i = 0; i < bar_h0 + 2; ++i) mbar_init(smem_u32(bars + i), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     issue_router_rows(a, a.layer[0].router, s_rw, bar_router);
   }
@@ -847,8 +953,6 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
   unsigned gu_ph = 0u, gu_pend = 0u;  // bit q: parity / in flight, GU slot q
   unsigned dn_ph = 0u, dn_pend = 0u;  // bit q: parity / in flight, DN slot q
   unsigned h_ph = 0u, h_pend = 0u;    // bit q: parity / in flight, h slot q
-  unsigned x_ph = 0u;
-  bool x_pend = false;
   // Leaving early: give every copy still in flight a bounded chance to land (so no
   // bulk copy targets shared memory of an exited CTA), raise the abort flag, return.
   auto bail = [&]() {
@@ -857,32 +961,34 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
         mbar_wait_bounded(smem_u32(bars + q), (gu_ph >> q) & 1u, a.status, kDefaultWaitCycles);
     for (int q = 0; q < kDnSlots; ++q)
       if (dn_pend & (1u << q))
-        mbar_wait_bounded(smem_u32(bars + 3 + q), (dn_ph >> q) & 1u, a.status, kDefaultWaitCycles);
+        mbar_wait_bounded(smem_u32(bars + bar_dn0 + q), (dn_ph >> q) & 1u, a.status, kDefaultWaitCycles);
     for (int q = 0; q < 2; ++q)
       if (h_pend & (1u << q))
         mbar_wait_bounded(smem_u32(bars + bar_h0 + q), (h_ph >> q) & 1u, a.status, kDefaultWaitCycles);
     if (router_pend) mbar_wait_bounded(bar_router, ph_router, a.status, kDefaultWaitCycles);
-    if (x_pend) mbar_wait_bounded(bar_x, x_ph, a.status, kDefaultWaitCycles);
     if (tid == 0) atomicExch(a.bar + 33, 1u);
+  };
+  // waits for one mbarrier phase with every thread; false (after bail) if it gave up
+  auto wait_all = [&](int bi, unsigned& ph, unsigned& pend, int q) -> bool {
+    const bool ok = mbar_wait_bounded(smem_u32(bars + bi), (ph >> q) & 1u, a.status, a.wait_cycles);
+    if (__syncthreads_or(!ok)) {
+      bail();
+      return false;
+    }
+    ph ^= 1u << q;
+    pend &= ~(1u << q);
+    return true;
   };
   const size_t RH = (size_t)a.R * a.H;
   const int o0 = (int)(((long long)blockIdx.x * a.H) / G);
   const int no = (int)(((long long)(blockIdx.x + 1) * a.H) / G) - o0;
   const size_t codes_room = up128((size_t)P.max_orows * (a.I / 2));
+  const int WV = P.h_rows < NW ? P.h_rows : NW;  // CSR positions per down wave
+  auto hslot = [&](int q) { return gu + kHOffset + (size_t)q * P.h_slot; };
   for (int l = 0; l < a.L; ++l) {
     const LayerPtrs& W = a.layer[l];
     const uint16_t* x = a.x + (size_t)l * RH;
     stamp(a, l, 0);
-    // this layer's rows into shared memory for the gate/up pass (the previous layer's
-    // gate/up pass is long done with the buffer)
-    if (x_staged && !a.route_only) {
-      x_pend = true;
-      if (tid == 0) {
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_expect_tx(bar_x, (uint32_t)(RH * 2));
-        bulk_g2s(smem_u32(s_x), x, (uint32_t)(RH * 2), bar_x);
-      }
-    }
     if (router_pend) {
       const bool ok = mbar_wait_bounded(bar_router, ph_router, a.status, a.wait_cycles);
       if (__syncthreads_or(!ok)) {
@@ -894,7 +1000,10 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
     }
     router_phase(a, x, s_rw);
     stamp(a, l, 1);
-    if (!grid_sync(a, sy)) {  // B1: all logits written
+    // B1 (all logits written); the activation pairs are built while it completes
+    grid_arrive(a, sy);
+    if (x_staged && !a.route_only) stage_xpairs(a, x, s_xp, s_xs);
+    if (!grid_wait(a, sy)) {
       bail();
       return;
     }
@@ -932,36 +1041,21 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
       for (int q = 0; q < kDnSlots && q < U; ++q) {
         dn_pend |= 1u << q;
         if (tid == 0)
-          issue_dn_chunk(a, W, T, dn + q * P.dn_slot, smem_u32(bars + 3 + q), q, o0, no, codes_room);
+          issue_dn_chunk(a, W, T, dn + q * P.dn_slot, smem_u32(bars + bar_dn0 + q), q, o0, no, codes_room);
       }
     }
     // ---- gate/up ----
-    const uint16_t* xg = x;
-    if (x_pend) {
-      const bool ok = mbar_wait_bounded(bar_x, x_ph, a.status, a.wait_cycles);
-      if (__syncthreads_or(!ok)) {
-        bail();
-        return;
-      }
-      x_ph ^= 1u;
-      x_pend = false;
-      xg = s_x;
-    }
     for (int n = 0; n < n_chunks; ++n) {
       const int q = n % kGuSlots;
-      const bool ok = mbar_wait_bounded(smem_u32(bars + q), (gu_ph >> q) & 1u, a.status, a.wait_cycles);
-      if (__syncthreads_or(!ok)) {
-        bail();
-        return;
-      }
-      gu_ph ^= 1u << q;
-      gu_pend &= ~(1u << q);
+      if (!wait_all(q, gu_ph, gu_pend, q)) return;
       if (n == 0) stamp(a, l, 4);
       stamp(a, l, 5);  // (the last chunk's stamp stays)
       const GuChunk c = s_chunks[n];
       const uint8_t* slot = gu + q * P.gu_slot;
-      const int p0 = T.csr_off[c.ui], p1 = T.csr_off[c.ui + 1];
-      for (int pp = p0; pp < p1; ++pp) gateup_rows<NBL, 1>(a, T, slot, c, pp, xg);
+      if (x_staged)
+        gateup_chunk<NBL, true>(a, T, slot, c, x, s_xp, s_xs);
+      else
+        gateup_chunk<NBL, false>(a, T, slot, c, x, s_xp, s_xs);
       __syncthreads();  // slot q free again
       if (n + kGuSlots < n_chunks) {
         gu_pend |= 1u << q;
@@ -983,73 +1077,74 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
       return;
     }
     stamp(a, l, 7);
-    // ---- down: all union experts for this CTA's output rows, ascending expert id ----
+    // ---- down: waves of WV consecutive CSR positions, one warp per position ----
     for (int i = tid; i < a.R * kAccStride; i += NT) s_acc[i] = 0.f;
     __syncthreads();
     if (no > 0) {
-      // h rows come in batches of consecutive CSR positions through two slots
-      HBatch hb_issue{0, 0}, hb{0, 0};
-      for (int q = 0; q < 2; ++q) {
-        if (!next_hbatch(T, U, P.h_rows, hb_issue)) break;
+      const int total = T.csr_off[U];
+      for (int q = 0; q < 2 && q * WV < total; ++q) {
         h_pend |= 1u << q;
-        if (tid == 0) issue_hbatch(a, gu + kHOffset + q * P.h_slot, smem_u32(bars + bar_h0 + q), hb_issue);
+        if (tid == 0) issue_hbatch(a, hslot(q), smem_u32(bars + bar_h0 + q), q * WV, min((q + 1) * WV, total));
       }
-      int cur_ui = -1;
-      for (int n = 0; next_hbatch(T, U, P.h_rows, hb); ++n) {
+      int waited = -1;  // DN slots of union experts [0, waited] have landed
+      int rel = 0;      // union experts [0, rel) are finished and their slots reused
+      for (int n = 0, pa = 0; pa < total; ++n, pa += WV) {
+        const int pb = min(pa + WV, total);
         const int qh = n & 1;
-        const bool okh = mbar_wait_bounded(smem_u32(bars + bar_h0 + qh), (h_ph >> qh) & 1u, a.status, a.wait_cycles);
-        if (__syncthreads_or(!okh)) {
-          bail();
-          return;
-        }
-        h_ph ^= 1u << qh;
-        h_pend &= ~(1u << qh);
+        if (!wait_all(bar_h0 + qh, h_ph, h_pend, qh)) return;
         if (n == 0) stamp(a, l, 8);
-        stamp(a, l, 9);
-        const float* s_hrows = reinterpret_cast<const float*>(gu + kHOffset + qh * P.h_slot);
-        for (int pp = hb.pa; pp < hb.pb; ++pp) {
-          if (pp >= (cur_ui < 0 ? 0 : T.csr_off[cur_ui + 1])) {
-            // the next expert: its down rows must have landed; the previous expert's
-            // slot is refilled with a later expert (everyone is past it)
-            const int prev = cur_ui;
-            do {
-              ++cur_ui;
-            } while (pp >= T.csr_off[cur_ui + 1]);
-            __syncthreads();
-            if (prev >= 0 && prev + kDnSlots < U) {
-              const int qd = prev % kDnSlots;
-              dn_pend |= 1u << qd;
-              if (tid == 0)
-                issue_dn_chunk(a, W, T, dn + qd * P.dn_slot, smem_u32(bars + 3 + qd), prev + kDnSlots, o0, no,
-                               codes_room);
-            }
-            const int qd = cur_ui % kDnSlots;
-            const bool okd = mbar_wait_bounded(smem_u32(bars + 3 + qd), (dn_ph >> qd) & 1u, a.status, a.wait_cycles);
-            if (__syncthreads_or(!okd)) {
-              bail();
-              return;
-            }
-            dn_ph ^= 1u << qd;
-            dn_pend &= ~(1u << qd);
-            stamp(a, l, 9);  // (the last wait's stamp stays)
-          }
-          down_rows<1>(a, T, dn + (cur_ui % kDnSlots) * P.dn_slot, codes_room, no, pp,
-                       s_hrows + (size_t)(pp - hb.pa) * a.I, s_acc);
+        // every expert up to the one holding position pb - 1 must have landed
+        int ui_last = waited < 0 ? 0 : waited;
+        while (T.csr_off[ui_last + 1] <= pb - 1) ++ui_last;
+        while (waited < ui_last) {
+          ++waited;
+          const int qd = waited % kDnSlots;
+          if (!wait_all(bar_dn0 + qd, dn_ph, dn_pend, qd)) return;
         }
-        __syncthreads();  // h slot qh free again
-        if (next_hbatch(T, U, P.h_rows, hb_issue)) {
+        stamp(a, l, 9);  // (the last wave's stamp stays)
+        if (warp < pb - pa) {
+          const int pp = pa + warp;
+          int ui = rel;
+          while (T.csr_off[ui + 1] <= pp) ++ui;
+          down_position(a, dn + (size_t)(ui % kDnSlots) * P.dn_slot, codes_room, no,
+                        reinterpret_cast<const float4*>(hslot(qh) + (size_t)(pp - pa) * a.I * 4),
+                        s_y + warp * kAccStride);
+        }
+        __syncthreads();
+        // combine in CSR order: for each row its experts ascending
+        for (int i = tid; i < a.R * no; i += NT) {
+          const int r = i / no, ol = i - r * no;
+          float acc = s_acc[r * kAccStride + ol];
+          for (int pp = pa; pp < pb; ++pp)
+            if (T.pair[pp] / a.k == r) acc = __fadd_rn(acc, s_y[(pp - pa) * kAccStride + ol]);
+          s_acc[r * kAccStride + ol] = acc;
+        }
+        // experts finished by this wave hand their slots to later experts
+        while (rel < U && T.csr_off[rel + 1] <= pb) {
+          if (rel + kDnSlots < U) {
+            const int qd = rel % kDnSlots;
+            dn_pend |= 1u << qd;
+            if (tid == 0)
+              issue_dn_chunk(a, W, T, dn + (size_t)qd * P.dn_slot, smem_u32(bars + bar_dn0 + qd), rel + kDnSlots,
+                             o0, no, codes_room);
+          }
+          ++rel;
+        }
+        // the wave after next into this h slot
+        const int na = pa + 2 * WV;
+        if (na < total) {
           h_pend |= 1u << qh;
-          if (tid == 0) issue_hbatch(a, gu + kHOffset + qh * P.h_slot, smem_u32(bars + bar_h0 + qh), hb_issue);
+          if (tid == 0) issue_hbatch(a, hslot(qh), smem_u32(bars + bar_h0 + qh), na, min(na + WV, total));
         }
       }
+      __syncthreads();
       stamp(a, l, 10);
       float* out = a.out + (size_t)l * RH;
       for (int i = tid; i < a.R * no; i += NT) {
         const int r = i / no, ol = i - (i / no) * no;
         out[(size_t)r * a.H + o0 + ol] = s_acc[r * kAccStride + ol];
       }
-    }
-    if (no <= 0 || U == 0) {
+    } else {
       stamp(a, l, 8);
       stamp(a, l, 9);
       stamp(a, l, 10);
