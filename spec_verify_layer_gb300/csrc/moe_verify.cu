@@ -45,7 +45,7 @@
 namespace moe {
 namespace {
 
-constexpr int NT = 256;  // threads per CTA
+constexpr int NT = 512;  // threads per CTA
 constexpr int NW = NT / 32;
 constexpr unsigned kStatusTimeout = 1u;
 constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // 2 s
@@ -365,6 +365,8 @@ struct Tables {
   int* pair;     // [R*k] pair index p = r*k + j, grouped by union expert, rows ascending
   float* w;      // [R*k] renormalised weight of pair p
   int* n_union;  // [1]
+  int* pos_ui;   // [R*k] union index of the expert at each CSR position
+  int* pos_row;  // [R*k] row at each CSR position
 };
 
 // True if (ka, ia) ranks before (kb, ib): larger key, then lower id.
@@ -430,12 +432,13 @@ __device__ __forceinline__ void select_row(const float* row, int E, int k, int l
   }
 }
 
-// scratch (inside the staging area, free while routing): mask [E], off_e [E], ids [R*k]
+// scratch (inside the staging area, free while routing): mask [E] (zeroed by the
+// caller beforehand), off_e [E], ids [R*k], union index [E]
 __device__ int route_phase(const RoundArgs& a, const Tables& T, unsigned* s_mask, int* s_off_e,
-                           int* s_ids, int layer) {
+                           int* s_ids, int* s_ui, int layer) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int E = a.E, k = a.k, R = a.R;
-  for (int e = tid; e < E; e += NT) s_mask[e] = 0u;
+  // rows: top-k, renormalised weights, row bits of each picked expert
   for (int r = warp; r < R; r += NW) {
     float my_l = 0.f;
     int my_id = 0;
@@ -443,16 +446,16 @@ __device__ int route_phase(const RoundArgs& a, const Tables& T, unsigned* s_mask
       select_row<4>(a.logits + (size_t)r * E, E, k, lane, my_l, my_id);
     else  // E <= 512 (moe_create rejects more)
       select_row<16>(a.logits + (size_t)r * E, E, k, lane, my_l, my_id);
-    // weights: exp(l_j - l_1) / sum over the k picks, summed in rank order
+    // weights: exp(l_j - l_1) / sum over the k picks (a warp sum: a fixed order per row)
     const float l1 = __shfl_sync(0xffffffffu, my_l, 0);
     const float ex = (lane < k) ? expf(my_l - l1) : 0.f;
-    float den = 0.f;
-    for (int j = 0; j < k; ++j) den = __fadd_rn(den, __shfl_sync(0xffffffffu, ex, j));
+    const float den = warp_sum(ex);
     if (lane < k) {
       const float wj = __fdiv_rn(ex, den);
       const int p = r * k + lane;
       s_ids[p] = my_id;
       T.w[p] = wj;
+      atomicOr(&s_mask[my_id], 1u << r);
       if (blockIdx.x == 0) {
         if (a.user_ids) a.user_ids[p] = my_id;
         if (a.user_w) a.user_w[p] = wj;
@@ -460,63 +463,57 @@ __device__ int route_phase(const RoundArgs& a, const Tables& T, unsigned* s_mask
     }
   }
   __syncthreads();
-  for (int p = tid; p < R * k; p += NT) atomicOr(&s_mask[s_ids[p]], 1u << (p / k));
-  __syncthreads();
-
-  // exclusive scans over e of (picked ? 1 : 0) and popc(mask): union index, pair offset
-  __shared__ int s_wf[NW], s_wc[NW];
-  const int per = (E + NT - 1) / NT;
-  const int e0 = tid * per;
-  int lf = 0, lc = 0;
-  for (int e = e0; e < e0 + per && e < E; ++e) {
-    const unsigned m = s_mask[e];
-    lf += (m != 0u);
-    lc += __popc(m);
-  }
-  int incf = lf, incc = lc;
+  // one warp: exclusive scans over e of (picked ? 1 : 0) and popc(mask) give the union
+  // index and the CSR offset of every picked expert (lane l owns a contiguous range)
+  if (warp == 0) {
+    const int per = (E + 31) >> 5;  // <= 16
+    const int e0 = lane * per, e1 = min(e0 + per, E);
+    int lf = 0, lc = 0;
+    for (int e = e0; e < e1; ++e) {
+      const unsigned m = s_mask[e];
+      lf += (m != 0u);
+      lc += __popc(m);
+    }
+    int incf = lf, incc = lc;
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int tf = __shfl_up_sync(0xffffffffu, incf, o);
-    const int tc = __shfl_up_sync(0xffffffffu, incc, o);
-    if (lane >= o) {
-      incf += tf;
-      incc += tc;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int tf = __shfl_up_sync(0xffffffffu, incf, o);
+      const int tc = __shfl_up_sync(0xffffffffu, incc, o);
+      if (lane >= o) {
+        incf += tf;
+        incc += tc;
+      }
     }
-  }
-  if (lane == 31) {
-    s_wf[warp] = incf;
-    s_wc[warp] = incc;
-  }
-  __syncthreads();
-  int basef = incf - lf, basec = incc - lc;
-  for (int w2 = 0; w2 < warp; ++w2) {
-    basef += s_wf[w2];
-    basec += s_wc[w2];
-  }
-  for (int e = e0; e < e0 + per && e < E; ++e) {
-    const unsigned m = s_mask[e];
-    if (m) {
-      s_off_e[e] = basec;
-      T.uni[basef] = e;
+    int basef = incf - lf, basec = incc - lc;
+    for (int e = e0; e < e1; ++e) {
+      const unsigned m = s_mask[e];
+      if (m) {
+        s_off_e[e] = basec;
+        s_ui[e] = basef;
+        T.uni[basef] = e;
+        T.csr_off[basef] = basec;
+        if (blockIdx.x == 0 && a.user_union) a.user_union[basef] = e;
+        ++basef;
+        basec += __popc(m);
+      }
+    }
+    if (lane == 31) {
+      // the last lane's running totals are the union size and the pair count
+      *T.n_union = basef;
       T.csr_off[basef] = basec;
-      if (blockIdx.x == 0 && a.user_union) a.user_union[basef] = e;
-      ++basef;
-      basec += __popc(m);
-    }
-  }
-  if (tid == NT - 1) {
-    // the last thread's running totals are the union size and the pair count
-    *T.n_union = basef;
-    T.csr_off[basef] = basec;
-    if (blockIdx.x == 0) {
-      if (a.user_nunion) *a.user_nunion = basef;
-      if (a.stats) a.stats[layer] = basef;
+      if (blockIdx.x == 0) {
+        if (a.user_nunion) *a.user_nunion = basef;
+        if (a.stats) a.stats[layer] = basef;
+      }
     }
   }
   __syncthreads();
   for (int p = tid; p < R * k; p += NT) {
     const int e = s_ids[p], r = p / k;
-    T.pair[s_off_e[e] + __popc(s_mask[e] & ((1u << r) - 1u))] = p;
+    const int pos = s_off_e[e] + __popc(s_mask[e] & ((1u << r) - 1u));
+    T.pair[pos] = p;
+    T.pos_row[pos] = r;
+    T.pos_ui[pos] = s_ui[e];
   }
   __syncthreads();
   return *T.n_union;
@@ -553,7 +550,8 @@ struct GuChunk {
 // smem plan: GU ring | DN slots | x pairs | tables | out accumulators | wave outputs |
 // chunk list | barriers
 struct SmemPlan {
-  size_t gu_slot, gu, dn_slot, dn, xrows, uni, csr, pair, w, nunion, acc, ybuf, chunks, bars, total;
+  size_t gu_slot, gu, dn_slot, dn, xrows, uni, csr, pair, w, pos_ui, pos_row, nunion, acc, ybuf, chunks, bars,
+      total;
   size_t ring;    // bytes of the gate/up ring (>= kGuSlots * gu_slot)
   size_t h_slot;  // bytes per h slot (two slots from gu + kHOffset)
   int gu_cap;     // units per gate/up chunk
@@ -570,12 +568,12 @@ __host__ __device__ inline SmemPlan smem_plan(int H, int I, int E, int R, int k,
   p.max_orows = (H + grid - 1) / grid;
   p.dn_slot = up128((size_t)p.max_orows * (I / 2)) + up128((size_t)p.max_orows * (I / 16));
   const size_t tables = up128((size_t)E * 4) + up128((size_t)(E + 1) * 4) +
-                        2 * up128((size_t)R * k * 4) + 128 + up128((size_t)R * kAccStride * 4) +
+                        4 * up128((size_t)R * k * 4) + 128 + up128((size_t)R * kAccStride * 4) +
                         up128((size_t)NW * kAccStride * 4) + up128(kMaxChunks * 12 + 16) + 256;
   const size_t fixed = tables + kDnSlots * p.dn_slot + kXBytes;
   const size_t limit = (size_t)225 * 1024;
   size_t cap = fixed < limit ? ((limit - fixed) / kGuSlots) / unit : 0;
-  if (cap > 2 * NW) cap = 2 * NW;  // a chunk is one pass of the warps over unit pairs
+  if (cap > NW) cap = NW;  // a chunk is one pass of the warps, a unit each
   p.gu_cap = (int)cap;
   p.gu_slot = up128(cap * unit);
   // small shapes: keep room behind kHOffset for full waves of exchanged h rows
@@ -590,6 +588,8 @@ __host__ __device__ inline SmemPlan smem_plan(int H, int I, int E, int R, int k,
   p.csr = off;     off += up128((size_t)(E + 1) * 4);
   p.pair = off;    off += up128((size_t)R * k * 4);
   p.w = off;       off += up128((size_t)R * k * 4);
+  p.pos_ui = off;  off += up128((size_t)R * k * 4);
+  p.pos_row = off; off += up128((size_t)R * k * 4);
   p.nunion = off;  off += 128;
   p.acc = off;     off += up128((size_t)R * kAccStride * 4);
   p.ybuf = off;    off += up128((size_t)NW * kAccStride * 4);
@@ -769,22 +769,22 @@ __device__ __forceinline__ float warp_sum_multi(float (&v)[V], int lane) {
   return s;
 }
 
-// Gate/up of units t0 and (if has1) t0 + NW of chunk c for the rows at CSR positions
-// pp .. pp+G-1: per lane its NBL blocks of the four weight rows, one multi-value
-// reduction, then the lane holding a (unit, row) gate value takes the up value from the
-// next lane group and stores h' = w silu(g) v, pre-scaled, in pair layout.
+// Gate/up of unit t of chunk c for the rows at CSR positions pp .. pp+G-1: per lane
+// its NBL blocks of the gate and up rows, one multi-value reduction, then the lane
+// holding a row's gate value takes the up value from the next lane group and stores
+// h' = w silu(g) v, pre-scaled, in pair layout.
 template <int NBL, int G, bool XS>
-__device__ __forceinline__ void gateup_units(const RoundArgs& a, const Tables& T, const uint8_t* slot,
-                                             const GuChunk& c, int t0, bool has1, int pp,
-                                             const uint16_t* x, const float4* s_xp, const float* s_xs) {
+__device__ __forceinline__ void gateup_unit(const RoundArgs& a, const Tables& T, const uint8_t* slot,
+                                            const GuChunk& c, int t, int pp, const uint16_t* x,
+                                            const float4* s_xp, const float* s_xs) {
   const int H = a.H, NB = H >> 5;
   const int lane = threadIdx.x & 31;
   int row[G];
 #pragma unroll
-  for (int g = 0; g < G; ++g) row[g] = T.pair[pp + g] / a.k;
+  for (int g = 0; g < G; ++g) row[g] = T.pos_row[pp + g];
   const uint8_t* codes = slot;
   const uint16_t* scales = reinterpret_cast<const uint16_t*>(slot + (size_t)c.n * H);
-  constexpr int V = 4 * G;  // value (u G + g) 2 + wrow
+  constexpr int V = 2 * G;  // value 2 g + wrow
   float v[V];
 #pragma unroll
   for (int i = 0; i < V; ++i) v[i] = 0.f;
@@ -800,22 +800,16 @@ __device__ __forceinline__ void gateup_units(const RoundArgs& a, const Tables& T
 #pragma unroll
       for (int g = 0; g < G; ++g) xps[g] = xp[g];
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        if (u == 0 || has1) {
-          const int t = t0 + u * NW;
+      for (int wrow = 0; wrow < 2; ++wrow) {
+        const size_t w = (size_t)(t * 2 + wrow) * NB + blk;
+        const uint4 nb = *reinterpret_cast<const uint4*>(codes + w * 16);
+        const float sc = half_bits(scales[w]);
+        float dot[G];
+        block_dot<G>(nb, xps, dot);
 #pragma unroll
-          for (int wrow = 0; wrow < 2; ++wrow) {
-            const size_t w = (size_t)(t * 2 + wrow) * NB + blk;
-            const uint4 nb = *reinterpret_cast<const uint4*>(codes + w * 16);
-            const float sc = half_bits(scales[w]);
-            float dot[G];
-            block_dot<G>(nb, xps, dot);
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-              float& acc = v[(u * G + g) * 2 + wrow];
-              acc = __fmaf_rn(sc, __fmaf_rn(dot[g], 0x1p62f, xsum8[g]), acc);
-            }
-          }
+        for (int g = 0; g < G; ++g) {
+          float& acc = v[2 * g + wrow];
+          acc = __fmaf_rn(sc, __fmaf_rn(dot[g], 0x1p62f, xsum8[g]), acc);
         }
       }
     }
@@ -825,41 +819,39 @@ __device__ __forceinline__ void gateup_units(const RoundArgs& a, const Tables& T
   const float up = __shfl_down_sync(0xffffffffu, s, LPV);
   const int vi = lane / LPV;
   if ((lane % LPV) == 0 && (vi & 1) == 0) {
-    const int si = vi >> 1, u = si / G, g = si - u * G;
-    if (u == 0 || has1) {
-      const int i = c.i0 + t0 + u * NW, j = i & 31;
-      const int pair = T.pair[pp + g];
-      const float hh = __fmul_rn(__fdiv_rn(s, __fadd_rn(1.f, expf(-s))), up);
-      const float hw = __fmul_rn(T.w[pair], hh);
-      a.hbuf[(size_t)(pp + g) * a.I + pair_index(i >> 5, j, a.I >> 5)] = hw * slot_scale(j & 7);
-    }
+    const int g = vi >> 1;
+    const int i = c.i0 + t, j = i & 31;
+    const int pair = T.pair[pp + g];
+    const float hh = __fmul_rn(__fdiv_rn(s, __fadd_rn(1.f, expf(-s))), up);
+    const float hw = __fmul_rn(T.w[pair], hh);
+    a.hbuf[(size_t)(pp + g) * a.I + pair_index(i >> 5, j, a.I >> 5)] = hw * slot_scale(j & 7);
   }
 }
 
-// Gate/up of one staged chunk: warp w takes units w and w + NW (chunks hold at most
-// 2 NW units; larger ones loop), rows of the expert two at a time.
+// Gate/up of one staged chunk (at most NW units): warp w takes unit w, the rows of the
+// expert two at a time when the activations are staged.
 template <int NBL, bool XS>
 __device__ __forceinline__ void gateup_chunk(const RoundArgs& a, const Tables& T, const uint8_t* slot,
                                              const GuChunk& c, const uint16_t* x, const float4* s_xp,
                                              const float* s_xs) {
   const int warp = threadIdx.x >> 5;
   const int p0 = T.csr_off[c.ui], p1 = T.csr_off[c.ui + 1];
-  for (int t0 = warp; t0 < c.n; t0 += 2 * NW) {
-    const bool has1 = t0 + NW < c.n;
+  for (int t = warp; t < c.n; t += NW) {
     int pp = p0;
-    for (; pp + 1 < p1; pp += 2) gateup_units<NBL, 2, XS>(a, T, slot, c, t0, has1, pp, x, s_xp, s_xs);
-    if (pp < p1) gateup_units<NBL, 1, XS>(a, T, slot, c, t0, has1, pp, x, s_xp, s_xs);
+    if (XS)  // (converting two rows from global memory at once would not fit the registers)
+      for (; pp + 1 < p1; pp += 2) gateup_unit<NBL, 2, XS>(a, T, slot, c, t, pp, x, s_xp, s_xs);
+    for (; pp < p1; ++pp) gateup_unit<NBL, 1, XS>(a, T, slot, c, t, pp, x, s_xp, s_xs);
   }
 }
 
 // ---------------------------------------------------------------------------------
 // P4: this CTA's output rows [o0, o0 + no), a wave of CSR positions at a time
 
-// y of one CSR position over this CTA's output rows: the position's h' row (pair
-// layout, shared memory) against each output row's down codes of its expert; y[ol]
-// to s_yw.  Lanes >= I/32 hold no block.
+// y of one CSR position over this CTA's output rows [ob0, ob1): the position's h' row
+// (pair layout, shared memory) against each output row's down codes of its expert;
+// y[ol] to s_yw.  Lanes >= I/32 hold no block.
 __device__ __forceinline__ void down_position(const RoundArgs& a, const uint8_t* dslot, size_t codes_room,
-                                              int no, const float4* s_h, float* s_yw) {
+                                              int ob0, int ob1, const float4* s_h, float* s_yw) {
   const int NBI = a.I >> 5;
   const int lane = threadIdx.x & 31;
   f2_t hp[16];
@@ -888,13 +880,13 @@ __device__ __forceinline__ void down_position(const RoundArgs& a, const uint8_t*
   const uint8_t* codes = dslot;
   const uint16_t* scales = reinterpret_cast<const uint16_t*>(dslot + codes_room);
   const f2_t* hps[1] = {hp};
-  for (int ob = 0; ob < no; ob += 8) {
-    float part[8];
+  for (int ob = ob0; ob < ob1; ob += 4) {
+    float part[4];
 #pragma unroll
-    for (int jj = 0; jj < 8; ++jj) {
+    for (int jj = 0; jj < 4; ++jj) {
       part[jj] = 0.f;
       const int ol = ob + jj;
-      if (lane < NBI && ol < no) {
+      if (lane < NBI && ol < ob1) {
         const uint4 nb = *reinterpret_cast<const uint4*>(codes + ((size_t)ol * NBI + lane) * 16);
         const float sc = half_bits(scales[ol * NBI + lane]);
         float dot[1];
@@ -902,8 +894,8 @@ __device__ __forceinline__ void down_position(const RoundArgs& a, const uint8_t*
         part[jj] = __fmul_rn(sc, __fmaf_rn(dot[0], 0x1p62f, hsum8));
       }
     }
-    const float y = warp_sum_multi<8>(part, lane);
-    if ((lane & 3) == 0 && ob + (lane >> 2) < no) s_yw[ob + (lane >> 2)] = y;
+    const float y = warp_sum_multi<4>(part, lane);
+    if ((lane & 7) == 0 && ob + (lane >> 3) < ob1) s_yw[ob + (lane >> 3)] = y;
   }
 }
 
@@ -913,6 +905,28 @@ __device__ __forceinline__ void issue_hbatch(const RoundArgs& a, uint8_t* dst, u
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   mbar_expect_tx(bar, (uint32_t)bytes);
   bulk_g2s(smem_u32(dst), a.hbuf + (size_t)pa * a.I, (uint32_t)bytes, bar);
+}
+
+// Leaving early: gives every copy still in flight a bounded chance to land (so no bulk
+// copy targets shared memory of an exited CTA) and raises the abort flag.  Out of line:
+// it never runs on the normal path.
+__device__ __noinline__ void drain_and_abort(const RoundArgs& a, const uint64_t* bars, unsigned gu_pend,
+                                             unsigned gu_ph, unsigned dn_pend, unsigned dn_ph,
+                                             unsigned h_pend, unsigned h_ph, bool router_pend,
+                                             unsigned ph_router) {
+  for (int q = 0; q < kGuSlots; ++q)
+    if (gu_pend & (1u << q))
+      mbar_wait_bounded(smem_u32(bars + q), (gu_ph >> q) & 1u, a.status, kDefaultWaitCycles);
+  for (int q = 0; q < kDnSlots; ++q)
+    if (dn_pend & (1u << q))
+      mbar_wait_bounded(smem_u32(bars + kGuSlots + q), (dn_ph >> q) & 1u, a.status, kDefaultWaitCycles);
+  for (int q = 0; q < 2; ++q)
+    if (h_pend & (1u << q))
+      mbar_wait_bounded(smem_u32(bars + kGuSlots + kDnSlots + 1 + q), (h_ph >> q) & 1u, a.status,
+                        kDefaultWaitCycles);
+  if (router_pend)
+    mbar_wait_bounded(smem_u32(bars + kGuSlots + kDnSlots), ph_router, a.status, kDefaultWaitCycles);
+  if (threadIdx.x == 0) atomicExch(a.bar + 33, 1u);
 }
 
 template <int NBL>
@@ -934,13 +948,15 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
   float* s_acc = reinterpret_cast<float*>(smem + P.acc);
   float* s_y = reinterpret_cast<float*>(smem + P.ybuf);
   GuChunk* s_chunks = reinterpret_cast<GuChunk*>(smem + P.chunks);
-  Tables T{reinterpret_cast<int*>(smem + P.uni), reinterpret_cast<int*>(smem + P.csr),
-           reinterpret_cast<int*>(smem + P.pair), reinterpret_cast<float*>(smem + P.w),
-           reinterpret_cast<int*>(smem + P.nunion)};
+  Tables T{reinterpret_cast<int*>(smem + P.uni),     reinterpret_cast<int*>(smem + P.csr),
+           reinterpret_cast<int*>(smem + P.pair),    reinterpret_cast<float*>(smem + P.w),
+           reinterpret_cast<int*>(smem + P.nunion),  reinterpret_cast<int*>(smem + P.pos_ui),
+           reinterpret_cast<int*>(smem + P.pos_row)};
   // routing scratch lives in the (then idle) gate/up ring
   unsigned* s_mask = reinterpret_cast<unsigned*>(gu);
   int* s_off_e = reinterpret_cast<int*>(gu + (size_t)a.E * 4);
   int* s_ids = reinterpret_cast<int*>(gu + (size_t)a.E * 8);
+  int* s_ui = reinterpret_cast<int*>(gu + (size_t)a.E * 8 + (size_t)a.R * a.k * 4);
   if (tid == 0) {
     for (int i = 0; i < bar_h0 + 2; ++i) mbar_init(smem_u32(bars + i), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -953,20 +969,8 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
   unsigned gu_ph = 0u, gu_pend = 0u;  // bit q: parity / in flight, GU slot q
   unsigned dn_ph = 0u, dn_pend = 0u;  // bit q: parity / in flight, DN slot q
   unsigned h_ph = 0u, h_pend = 0u;    // bit q: parity / in flight, h slot q
-  // Leaving early: give every copy still in flight a bounded chance to land (so no
-  // bulk copy targets shared memory of an exited CTA), raise the abort flag, return.
   auto bail = [&]() {
-    for (int q = 0; q < kGuSlots; ++q)
-      if (gu_pend & (1u << q))
-        mbar_wait_bounded(smem_u32(bars + q), (gu_ph >> q) & 1u, a.status, kDefaultWaitCycles);
-    for (int q = 0; q < kDnSlots; ++q)
-      if (dn_pend & (1u << q))
-        mbar_wait_bounded(smem_u32(bars + bar_dn0 + q), (dn_ph >> q) & 1u, a.status, kDefaultWaitCycles);
-    for (int q = 0; q < 2; ++q)
-      if (h_pend & (1u << q))
-        mbar_wait_bounded(smem_u32(bars + bar_h0 + q), (h_ph >> q) & 1u, a.status, kDefaultWaitCycles);
-    if (router_pend) mbar_wait_bounded(bar_router, ph_router, a.status, kDefaultWaitCycles);
-    if (tid == 0) atomicExch(a.bar + 33, 1u);
+    drain_and_abort(a, bars, gu_pend, gu_ph, dn_pend, dn_ph, h_pend, h_ph, router_pend, ph_router);
   };
   // waits for one mbarrier phase with every thread; false (after bail) if it gave up
   auto wait_all = [&](int bi, unsigned& ph, unsigned& pend, int q) -> bool {
@@ -983,7 +987,9 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
   const int o0 = (int)(((long long)blockIdx.x * a.H) / G);
   const int no = (int)(((long long)(blockIdx.x + 1) * a.H) / G) - o0;
   const size_t codes_room = up128((size_t)P.max_orows * (a.I / 2));
-  const int WV = P.h_rows < NW ? P.h_rows : NW;  // CSR positions per down wave
+  // CSR positions per down wave: at most one per warp, per h-slot row, and per DN slot
+  // (a wave spans at most WV experts, all inside the window of issued DN slots)
+  const int WV = min(min(P.h_rows, NW), kDnSlots);
   auto hslot = [&](int q) { return gu + kHOffset + (size_t)q * P.h_slot; };
   for (int l = 0; l < a.L; ++l) {
     const LayerPtrs& W = a.layer[l];
@@ -1002,28 +1008,35 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
     stamp(a, l, 1);
     // B1 (all logits written); the activation pairs are built while it completes
     grid_arrive(a, sy);
+    for (int e = tid; e < a.E; e += NT) s_mask[e] = 0u;  // (the router rows there are consumed)
     if (x_staged && !a.route_only) stage_xpairs(a, x, s_xp, s_xs);
     if (!grid_wait(a, sy)) {
       bail();
       return;
     }
     stamp(a, l, 2);
-    const int U = route_phase(a, T, s_mask, s_off_e, s_ids, l);
+    const int U = route_phase(a, T, s_mask, s_off_e, s_ids, s_ui, l);
     stamp(a, l, 3);
     if (a.route_only) return;
     // ---- plan this CTA's gate/up chunks; issue them and the down prefetch ----
     if (tid == 0) {
-      const long long N = (long long)U * a.I;
-      long long cur = (blockIdx.x * N) / G;
-      const long long end = ((blockIdx.x + 1) * N) / G;
+      // U * I * grid < 2^31 (U <= 512, I <= 4096, grid <= 1024), so 32-bit math is exact
+      const unsigned N = (unsigned)U * (unsigned)a.I;
+      int cur = (int)((blockIdx.x * N) / (unsigned)G);
+      const int end = (int)(((blockIdx.x + 1) * N) / (unsigned)G);
       int nc = 0;
+      int ui = cur / a.I, i0 = cur - ui * a.I;
       while (cur < end && nc < kMaxChunks) {
-        const int ui = (int)(cur / a.I), i0 = (int)(cur - (long long)ui * a.I);
-        long long n = end - cur;
+        int n = end - cur;
         if (n > a.I - i0) n = a.I - i0;
         if (n > P.gu_cap) n = P.gu_cap;
-        s_chunks[nc++] = GuChunk{ui, i0, (int)n};
+        s_chunks[nc++] = GuChunk{ui, i0, n};
         cur += n;
+        i0 += n;
+        if (i0 == a.I) {
+          ++ui;
+          i0 = 0;
+        }
       }
       if (cur < end) {  // (the host rejects shapes that could get here) never drop work
         atomicOr(a.status, kStatusTimeout);
@@ -1033,22 +1046,29 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
     }
     __syncthreads();
     const int n_chunks = *reinterpret_cast<const int*>(smem + P.chunks + kMaxChunks * 12);
-    for (int q = 0; q < kGuSlots && q < n_chunks; ++q) {
-      gu_pend |= 1u << q;
-      if (tid == 0) issue_gu_chunk(a, W, T, gu + q * P.gu_slot, smem_u32(bars + q), s_chunks[q]);
-    }
-    if (no > 0) {
-      for (int q = 0; q < kDnSlots && q < U; ++q) {
-        dn_pend |= 1u << q;
-        if (tid == 0)
-          issue_dn_chunk(a, W, T, dn + q * P.dn_slot, smem_u32(bars + bar_dn0 + q), q, o0, no, codes_room);
+    gu_pend |= (1u << min(kGuSlots, n_chunks)) - 1u;
+    if (tid < min(kGuSlots, n_chunks)) issue_gu_chunk(a, W, T, gu + tid * P.gu_slot, smem_u32(bars + tid), s_chunks[tid]);
+    // the down prefetch goes out once the first gate/up chunk has landed, so it does not
+    // delay that chunk (it is needed only after B2)
+    auto issue_dn_prefetch = [&]() {
+      if (no > 0) {
+        const int nq = min(U, kDnSlots);
+        dn_pend |= (1u << nq) - 1u;
+        if (tid == 0) {
+#pragma unroll 1
+          for (int q = 0; q < nq; ++q)
+            issue_dn_chunk(a, W, T, dn + q * P.dn_slot, smem_u32(bars + bar_dn0 + q), q, o0, no, codes_room);
+        }
       }
-    }
+    };
     // ---- gate/up ----
     for (int n = 0; n < n_chunks; ++n) {
       const int q = n % kGuSlots;
       if (!wait_all(q, gu_ph, gu_pend, q)) return;
-      if (n == 0) stamp(a, l, 4);
+      if (n == 0) {
+        stamp(a, l, 4);
+        issue_dn_prefetch();
+      }
       stamp(a, l, 5);  // (the last chunk's stamp stays)
       const GuChunk c = s_chunks[n];
       const uint8_t* slot = gu + q * P.gu_slot;
@@ -1065,6 +1085,7 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
     if (n_chunks == 0) {
       stamp(a, l, 4);
       stamp(a, l, 5);
+      issue_dn_prefetch();
     }
     // the next layer's router rows can move in now (the GU ring is idle until then)
     if (l + 1 < a.L && router_rows_of_cta(a.E) > 0) {
@@ -1086,50 +1107,67 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
         h_pend |= 1u << q;
         if (tid == 0) issue_hbatch(a, hslot(q), smem_u32(bars + bar_h0 + q), q * WV, min((q + 1) * WV, total));
       }
-      int waited = -1;  // DN slots of union experts [0, waited] have landed
-      int rel = 0;      // union experts [0, rel) are finished and their slots reused
+      int waited = 0;  // the DN slots of union experts [0, waited) have landed
+      int rel = 0;     // union experts [0, rel) are finished and their slots reused
       for (int n = 0, pa = 0; pa < total; ++n, pa += WV) {
         const int pb = min(pa + WV, total);
         const int qh = n & 1;
         if (!wait_all(bar_h0 + qh, h_ph, h_pend, qh)) return;
         if (n == 0) stamp(a, l, 8);
-        // every expert up to the one holding position pb - 1 must have landed
-        int ui_last = waited < 0 ? 0 : waited;
-        while (T.csr_off[ui_last + 1] <= pb - 1) ++ui_last;
-        while (waited < ui_last) {
-          ++waited;
-          const int qd = waited % kDnSlots;
-          if (!wait_all(bar_dn0 + qd, dn_ph, dn_pend, qd)) return;
+        // the experts of this wave's positions must have landed: one waiting thread per slot
+        const int need = T.pos_ui[pb - 1] + 1;
+        if (need > waited) {
+          bool ok = true;
+          if (tid < need - waited) {
+            const int qd = (waited + tid) % kDnSlots;
+            ok = mbar_wait_bounded(smem_u32(bars + bar_dn0 + qd), (dn_ph >> qd) & 1u, a.status, a.wait_cycles);
+          }
+          if (__syncthreads_or(!ok)) {
+            bail();
+            return;
+          }
+          for (int u = waited; u < need; ++u) {
+            const int qd = u % kDnSlots;
+            dn_ph ^= 1u << qd;
+            dn_pend &= ~(1u << qd);
+          }
+          waited = need;
         }
         stamp(a, l, 9);  // (the last wave's stamp stays)
-        if (warp < pb - pa) {
-          const int pp = pa + warp;
-          int ui = rel;
-          while (T.csr_off[ui + 1] <= pp) ++ui;
-          down_position(a, dn + (size_t)(ui % kDnSlots) * P.dn_slot, codes_room, no,
-                        reinterpret_cast<const float4*>(hslot(qh) + (size_t)(pp - pa) * a.I * 4),
-                        s_y + warp * kAccStride);
+        {
+          // positions of the wave over the warps; spare warps split a position's rows
+          const int npos = pb - pa, wpp = NW / npos;
+          const int pi = warp / wpp, part = warp - pi * wpp;
+          if (pi < npos) {
+            const int pp = pa + pi;
+            const int ui = T.pos_ui[pp];
+            down_position(a, dn + (size_t)(ui % kDnSlots) * P.dn_slot, codes_room, (part * no) / wpp,
+                          ((part + 1) * no) / wpp,
+                          reinterpret_cast<const float4*>(hslot(qh) + (size_t)pi * a.I * 4),
+                          s_y + pi * kAccStride);
+          }
         }
         __syncthreads();
         // combine in CSR order: for each row its experts ascending
         for (int i = tid; i < a.R * no; i += NT) {
           const int r = i / no, ol = i - r * no;
           float acc = s_acc[r * kAccStride + ol];
+#pragma unroll 4
           for (int pp = pa; pp < pb; ++pp)
-            if (T.pair[pp] / a.k == r) acc = __fadd_rn(acc, s_y[(pp - pa) * kAccStride + ol]);
+            if (T.pos_row[pp] == r) acc = __fadd_rn(acc, s_y[(pp - pa) * kAccStride + ol]);
           s_acc[r * kAccStride + ol] = acc;
         }
-        // experts finished by this wave hand their slots to later experts
-        while (rel < U && T.csr_off[rel + 1] <= pb) {
-          if (rel + kDnSlots < U) {
-            const int qd = rel % kDnSlots;
-            dn_pend |= 1u << qd;
-            if (tid == 0)
-              issue_dn_chunk(a, W, T, dn + (size_t)qd * P.dn_slot, smem_u32(bars + bar_dn0 + qd), rel + kDnSlots,
-                             o0, no, codes_room);
-          }
-          ++rel;
+        // experts finished by this wave hand their slots to later experts (one issuing
+        // thread per slot)
+        const int rel_new = (pb < total) ? T.pos_ui[pb] : U;
+        if (tid < rel_new - rel && rel + tid + kDnSlots < U) {
+          const int e = rel + tid, qd = e % kDnSlots;
+          issue_dn_chunk(a, W, T, dn + (size_t)qd * P.dn_slot, smem_u32(bars + bar_dn0 + qd), e + kDnSlots, o0, no,
+                         codes_room);
         }
+        for (int e = rel; e < rel_new; ++e)
+          if (e + kDnSlots < U) dn_pend |= 1u << (e % kDnSlots);
+        rel = rel_new;
         // the wave after next into this h slot
         const int na = pa + 2 * WV;
         if (na < total) {
