@@ -532,6 +532,9 @@ __device__ int route_phase(const RoundArgs& a, const Tables& T, unsigned* s_mask
 // prefetched into kDnSlots slots meanwhile (they depend only on the routing).
 
 constexpr int kGuSlots = 3;
+// gate/up chunks issued before the first one lands (the rest of the ring follows it):
+// copies in flight share the bandwidth, so a chunk issued alone arrives sooner
+constexpr int kGuFirst = 1;
 constexpr int kDnSlots = 11;
 // the layer's rows as operand pairs plus block sums (4 rows at hidden 2048), staged once
 // per layer when they fit
@@ -1046,8 +1049,9 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
     }
     __syncthreads();
     const int n_chunks = *reinterpret_cast<const int*>(smem + P.chunks + kMaxChunks * 12);
-    gu_pend |= (1u << min(kGuSlots, n_chunks)) - 1u;
-    if (tid < min(kGuSlots, n_chunks)) issue_gu_chunk(a, W, T, gu + tid * P.gu_slot, smem_u32(bars + tid), s_chunks[tid]);
+    const int n_first = min(kGuFirst, n_chunks), n_ring = min(kGuSlots, n_chunks);
+    gu_pend |= (1u << n_first) - 1u;
+    if (tid < n_first) issue_gu_chunk(a, W, T, gu + tid * P.gu_slot, smem_u32(bars + tid), s_chunks[tid]);
     // the down prefetch goes out once the first gate/up chunk has landed, so it does not
     // delay that chunk (it is needed only after B2)
     auto issue_dn_prefetch = [&]() {
@@ -1067,6 +1071,9 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
       if (!wait_all(q, gu_ph, gu_pend, q)) return;
       if (n == 0) {
         stamp(a, l, 4);
+        gu_pend |= ((1u << n_ring) - 1u) & ~((1u << n_first) - 1u);
+        if (tid >= n_first && tid < n_ring)
+          issue_gu_chunk(a, W, T, gu + tid * P.gu_slot, smem_u32(bars + tid), s_chunks[tid]);
         issue_dn_prefetch();
       }
       stamp(a, l, 5);  // (the last chunk's stamp stays)
