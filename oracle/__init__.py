@@ -57,6 +57,12 @@ def lib():
         L.oracle_layer.restype = i32
         L.oracle_layer_dense.argtypes = [i32] * 5 + [vp] * 9
         L.oracle_layer_dense.restype = i32
+        L.oracle_route_tail.argtypes = [i32] * 5 + [vp] * 9
+        L.oracle_route_tail.restype = i32
+        L.oracle_layer_tail.argtypes = [i32] * 6 + [vp, vp, i32] + [vp] * 8
+        L.oracle_layer_tail.restype = i32
+        L.oracle_layer_dense_tail.argtypes = [i32] * 6 + [vp] * 9
+        L.oracle_layer_dense_tail.restype = i32
         L.oracle_expert_ffn.argtypes = [i32, i32] + [vp] * 8
         L.oracle_expert_ffn.restype = i32
         L.oracle_unique_expert_bytes.argtypes = [i32, i32, i32]
@@ -89,11 +95,14 @@ class Route:
     logits: np.ndarray   # [R][E] fp32 (canonical order)
     ids: np.ndarray      # [R][k] int32, rank order
     w: np.ndarray        # [R][k] fp64
-    union: np.ndarray    # [U] int32 ascending
+    union: np.ndarray    # [U] int32 ascending (after the tail skip, if any)
     gap64: np.ndarray    # [R] fp64 gap between k-th and (k+1)-th exact logit
+    keep: np.ndarray = None  # [R][k] bool: the pick's expert is evaluated
 
 
-def route(router: np.ndarray, x_bf16: np.ndarray, k: int) -> Route:
+def route(router: np.ndarray, x_bf16: np.ndarray, k: int, tail_rank: int = 0) -> Route:
+    """Routing of one layer; ``tail_rank`` > 0 drops union experts that every row
+    picking them has at 1-based rank >= tail_rank (no renormalisation)."""
     router = np.ascontiguousarray(router, np.float32)
     x_bf16 = np.ascontiguousarray(x_bf16, np.uint16)
     E, H = router.shape
@@ -101,17 +110,18 @@ def route(router: np.ndarray, x_bf16: np.ndarray, k: int) -> Route:
     logits = np.empty((R, E), np.float32)
     ids = np.empty((R, k), np.int32)
     w = np.empty((R, k), np.float64)
+    keep = np.empty((R, k), np.uint8)
     uni = np.empty(E, np.int32)
     nu = np.zeros(1, np.int32)
     gap = np.empty(R, np.float64)
-    rc = lib().oracle_route(H, E, k, R, _p(router), _p(x_bf16), _p(logits), _p(ids), _p(w),
-                            _p(uni), _p(nu), _p(gap))
+    rc = lib().oracle_route_tail(H, E, k, R, int(tail_rank), _p(router), _p(x_bf16), _p(logits),
+                                 _p(ids), _p(w), _p(keep), _p(uni), _p(nu), _p(gap))
     if rc != 0:
         raise ValueError(f"oracle_route rejected the dimensions (rc={rc})")
-    return Route(logits, ids, w, uni[: nu[0]].copy(), gap)
+    return Route(logits, ids, w, uni[: nu[0]].copy(), gap, keep.astype(bool))
 
 
-def layer(router, x_bf16, k: int, prov_ids, ew) -> np.ndarray:
+def layer(router, x_bf16, k: int, prov_ids, ew, tail_rank: int = 0) -> np.ndarray:
     """Output rows [R][H] (fp64).  ``ew`` holds the stacked weights of the experts
     ``prov_ids`` (an object with qg, sg, qu, su, qd, sd arrays, leading axis P)."""
     router = np.ascontiguousarray(router, np.float32)
@@ -121,9 +131,9 @@ def layer(router, x_bf16, k: int, prov_ids, ew) -> np.ndarray:
     I = ew.qg.shape[1]
     prov = np.ascontiguousarray(prov_ids, np.int32)
     out = np.empty((R, H), np.float64)
-    rc = lib().oracle_layer(H, E, k, I, R, _p(router), _p(x_bf16), prov.size, _p(prov),
-                            _p(ew.qg), _p(ew.sg), _p(ew.qu), _p(ew.su), _p(ew.qd), _p(ew.sd),
-                            _p(out))
+    rc = lib().oracle_layer_tail(H, E, k, I, R, int(tail_rank), _p(router), _p(x_bf16), prov.size,
+                                 _p(prov), _p(ew.qg), _p(ew.sg), _p(ew.qu), _p(ew.su), _p(ew.qd),
+                                 _p(ew.sd), _p(out))
     if rc == -2:
         raise KeyError("a routed expert's weights were not provided to the oracle")
     if rc != 0:
@@ -131,7 +141,7 @@ def layer(router, x_bf16, k: int, prov_ids, ew) -> np.ndarray:
     return out
 
 
-def layer_dense(router, x_bf16, k: int, ew) -> np.ndarray:
+def layer_dense(router, x_bf16, k: int, ew, tail_rank: int = 0) -> np.ndarray:
     """Brute force: all E experts evaluated for every row (ew holds all E experts)."""
     router = np.ascontiguousarray(router, np.float32)
     x_bf16 = np.ascontiguousarray(x_bf16, np.uint16)
@@ -140,8 +150,9 @@ def layer_dense(router, x_bf16, k: int, ew) -> np.ndarray:
     I = ew.qg.shape[1]
     assert ew.qg.shape[0] == E
     out = np.empty((R, H), np.float64)
-    rc = lib().oracle_layer_dense(H, E, k, I, R, _p(router), _p(x_bf16), _p(ew.qg), _p(ew.sg),
-                                  _p(ew.qu), _p(ew.su), _p(ew.qd), _p(ew.sd), _p(out))
+    rc = lib().oracle_layer_dense_tail(H, E, k, I, R, int(tail_rank), _p(router), _p(x_bf16),
+                                       _p(ew.qg), _p(ew.sg), _p(ew.qu), _p(ew.su), _p(ew.qd),
+                                       _p(ew.sd), _p(out))
     if rc != 0:
         raise ValueError(f"oracle_layer_dense rejected the dimensions (rc={rc})")
     return out
@@ -163,7 +174,7 @@ def unique_expert_bytes(H: int, I: int, n_union: int) -> int:
     return int(lib().oracle_unique_expert_bytes(H, I, n_union))
 
 
-def layer_from_generator(cfg, layer_idx: int, x_bf16=None):
+def layer_from_generator(cfg, layer_idx: int, x_bf16=None, tail_rank: int = 0):
     """Route one generated layer, generate only the union experts, evaluate it.
 
     Returns (Route, out[R][H] fp64).  Inputs come from the shared seeded generator.
@@ -171,7 +182,7 @@ def layer_from_generator(cfg, layer_idx: int, x_bf16=None):
     import syngen
     router = syngen.router(cfg, layer_idx)
     x = syngen.rows(cfg, layer_idx) if x_bf16 is None else x_bf16
-    rt = route(router, x, cfg.top_k)
+    rt = route(router, x, cfg.top_k, tail_rank)
     ew = syngen.experts_stacked(cfg, layer_idx, rt.union)
-    out = layer(router, x, cfg.top_k, rt.union, ew)
+    out = layer(router, x, cfg.top_k, rt.union, ew, tail_rank)
     return rt, out

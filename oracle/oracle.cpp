@@ -17,6 +17,11 @@
 //   a4  for each routed (row, expert): g = Wg x, v = Wu x, h = silu(g) * v,
 //       silu(g) = g / (1 + exp(-g)), with W = fp16 scale * int4 code.
 //   a5  y = Wd h;  out[r] = sum_j w_j * y_{r, ids[r][j]}  (j in rank order).
+//   Optional routing tail skip (Avalon README, "Numbers" for the RX 7900 XT: experts
+//   that every token of a verification routes only at rank 7 or lower are skipped):
+//   with threshold T > 0, a union expert is dropped when every row that picked it has
+//   it at 1-based rank >= T; the picks of dropped experts contribute nothing and the
+//   remaining weights are not renormalised (the page says nothing about it).
 //
 // Precision (readings of points the pages leave open; each is listed in the design
 // notes):
@@ -90,11 +95,13 @@ struct Routing {
   std::vector<float> logits;  // [R][E]
   std::vector<int32_t> ids;   // [R][k]
   std::vector<double> w;      // [R][k]
-  std::vector<int32_t> uni;   // ascending
+  std::vector<char> keep;     // [R][k]: the pick's expert is evaluated (not tail-skipped)
+  std::vector<int32_t> uni;   // ascending, after the tail skip
   std::vector<double> gap64;  // [R]
 };
 
-int route(int H, int E, int k, int R, const float* router, const uint16_t* xb, Routing& out) {
+int route(int H, int E, int k, int R, const float* router, const uint16_t* xb, Routing& out,
+          int tail_rank = 0) {
   if (H <= 0 || H % 128 || E <= 0 || k <= 0 || k > E || R <= 0) return -1;
   out.logits.assign((size_t)R * E, 0.0f);
   out.ids.assign((size_t)R * k, -1);
@@ -148,9 +155,17 @@ int route(int H, int E, int k, int R, const float* router, const uint16_t* xb, R
       out.gap64[r] = INFINITY;
     }
   }
+  // tail skip: an expert survives if some row picked it at 1-based rank < tail_rank
+  std::vector<char> alive(E, 0);
+  for (int r = 0; r < R; ++r)
+    for (int j = 0; j < k; ++j)
+      if (tail_rank <= 0 || j + 1 < tail_rank) alive[out.ids[(size_t)r * k + j]] = 1;
+  out.keep.assign((size_t)R * k, 0);
+  for (int r = 0; r < R; ++r)
+    for (int j = 0; j < k; ++j) out.keep[(size_t)r * k + j] = alive[out.ids[(size_t)r * k + j]];
   out.uni.clear();
   for (int e = 0; e < E; ++e)
-    if (hit[e]) out.uni.push_back(e);
+    if (hit[e] && alive[e]) out.uni.push_back(e);
   return 0;
 }
 
@@ -210,6 +225,18 @@ void ffn_of(int H, int I, const Provided& pv, int p, const float* x, double* y) 
 
 extern "C" {
 
+int oracle_route_tail(int H, int E, int k, int R, int tail_rank, const float* router,
+                      const uint16_t* x_bf16, float* logits, int32_t* ids, double* w, uint8_t* keep,
+                      int32_t* union_ids, int32_t* n_union, double* gap64);
+int oracle_layer_tail(int H, int E, int k, int I, int R, int tail_rank, const float* router,
+                      const uint16_t* x_bf16, int P, const int32_t* prov_ids, const int8_t* qg,
+                      const uint16_t* sg, const int8_t* qu, const uint16_t* su, const int8_t* qd,
+                      const uint16_t* sd, double* out);
+int oracle_layer_dense_tail(int H, int E, int k, int I, int R, int tail_rank, const float* router,
+                            const uint16_t* x_bf16, const int8_t* qg, const uint16_t* sg,
+                            const int8_t* qu, const uint16_t* su, const int8_t* qd,
+                            const uint16_t* sd, double* out);
+
 double oracle_half_to_double(uint16_t b) { return half_bits_to_double(b); }
 float oracle_bf16_to_float(uint16_t b) { return bf16_bits_to_float(b); }
 
@@ -223,8 +250,19 @@ float oracle_canonical_logit(const float* w, const float* x, int H) {
 int oracle_route(int H, int E, int k, int R, const float* router, const uint16_t* x_bf16,
                  float* logits, int32_t* ids, double* w, int32_t* union_ids, int32_t* n_union,
                  double* gap64) {
+  return oracle_route_tail(H, E, k, R, 0, router, x_bf16, logits, ids, w, nullptr, union_ids,
+                           n_union, gap64);
+}
+
+// oracle_route with the tail skip at threshold tail_rank (0 = off); keep [R][k] (may be
+// NULL) receives 1 for picks whose expert is evaluated.
+int oracle_route_tail(int H, int E, int k, int R, int tail_rank, const float* router,
+                      const uint16_t* x_bf16, float* logits, int32_t* ids, double* w, uint8_t* keep,
+                      int32_t* union_ids, int32_t* n_union, double* gap64) {
   Routing rt;
-  if (route(H, E, k, R, router, x_bf16, rt)) return -1;
+  if (route(H, E, k, R, router, x_bf16, rt, tail_rank)) return -1;
+  if (keep)
+    for (size_t i = 0; i < rt.keep.size(); ++i) keep[i] = (uint8_t)rt.keep[i];
   std::memcpy(logits, rt.logits.data(), rt.logits.size() * sizeof(float));
   std::memcpy(ids, rt.ids.data(), rt.ids.size() * sizeof(int32_t));
   std::memcpy(w, rt.w.data(), rt.w.size() * sizeof(double));
@@ -241,9 +279,18 @@ int oracle_layer(int H, int E, int k, int I, int R, const float* router, const u
                  int P, const int32_t* prov_ids, const int8_t* qg, const uint16_t* sg,
                  const int8_t* qu, const uint16_t* su, const int8_t* qd, const uint16_t* sd,
                  double* out) {
+  return oracle_layer_tail(H, E, k, I, R, 0, router, x_bf16, P, prov_ids, qg, sg, qu, su, qd, sd,
+                           out);
+}
+
+// oracle_layer with the tail skip at threshold tail_rank (0 = off).
+int oracle_layer_tail(int H, int E, int k, int I, int R, int tail_rank, const float* router,
+                      const uint16_t* x_bf16, int P, const int32_t* prov_ids, const int8_t* qg,
+                      const uint16_t* sg, const int8_t* qu, const uint16_t* su, const int8_t* qd,
+                      const uint16_t* sd, double* out) {
   if (I <= 0 || I % 32) return -1;
   Routing rt;
-  if (route(H, E, k, R, router, x_bf16, rt)) return -1;
+  if (route(H, E, k, R, router, x_bf16, rt, tail_rank)) return -1;
   Provided pv{P, prov_ids, qg, qu, qd, sg, su, sd};
   std::vector<int> slot(E, -1);
   for (int e : rt.uni) {
@@ -257,6 +304,7 @@ int oracle_layer(int H, int E, int k, int I, int R, const float* router, const u
     double* o = out + (size_t)r * H;
     for (int h = 0; h < H; ++h) o[h] = 0.0;
     for (int j = 0; j < k; ++j) {
+      if (!rt.keep[(size_t)r * k + j]) continue;
       int e = rt.ids[(size_t)r * k + j];
       ffn_of(H, I, pv, slot[e], x.data(), y.data());
       double wj = rt.w[(size_t)r * k + j];
@@ -273,9 +321,17 @@ int oracle_layer_dense(int H, int E, int k, int I, int R, const float* router,
                        const uint16_t* x_bf16, const int8_t* qg, const uint16_t* sg,
                        const int8_t* qu, const uint16_t* su, const int8_t* qd,
                        const uint16_t* sd, double* out) {
+  return oracle_layer_dense_tail(H, E, k, I, R, 0, router, x_bf16, qg, sg, qu, su, qd, sd, out);
+}
+
+// oracle_layer_dense with the tail skip (a dropped pick's gate entry stays 0).
+int oracle_layer_dense_tail(int H, int E, int k, int I, int R, int tail_rank, const float* router,
+                            const uint16_t* x_bf16, const int8_t* qg, const uint16_t* sg,
+                            const int8_t* qu, const uint16_t* su, const int8_t* qd,
+                            const uint16_t* sd, double* out) {
   if (I <= 0 || I % 32) return -1;
   Routing rt;
-  if (route(H, E, k, R, router, x_bf16, rt)) return -1;
+  if (route(H, E, k, R, router, x_bf16, rt, tail_rank)) return -1;
   std::vector<int32_t> all(E);
   for (int e = 0; e < E; ++e) all[e] = e;
   Provided pv{E, all.data(), qg, qu, qd, sg, su, sd};
@@ -284,7 +340,8 @@ int oracle_layer_dense(int H, int E, int k, int I, int R, const float* router,
   for (int r = 0; r < R; ++r) {
     for (int h = 0; h < H; ++h) x[h] = bf16_bits_to_float(x_bf16[(size_t)r * H + h]);
     for (int e = 0; e < E; ++e) gate[e] = 0.0;
-    for (int j = 0; j < k; ++j) gate[rt.ids[(size_t)r * k + j]] = rt.w[(size_t)r * k + j];
+    for (int j = 0; j < k; ++j)
+      if (rt.keep[(size_t)r * k + j]) gate[rt.ids[(size_t)r * k + j]] = rt.w[(size_t)r * k + j];
     double* o = out + (size_t)r * H;
     for (int h = 0; h < H; ++h) o[h] = 0.0;
     for (int e = 0; e < E; ++e) {

@@ -352,3 +352,87 @@ def test_generated_full_size_layer_routes_sanely():
     assert cfg.top_k <= rt.union.size <= 32
     # the fp64 shadow order agrees with the fp32 decision unless the gap is tiny
     assert (rt.gap64 > 0).all() or (rt.gap64 >= 0).all()
+
+
+# ---- routing tail skip (Avalon README, "Numbers": experts that every token of a
+# verification routes only at rank 7 or lower are skipped) ---------------------------
+
+def _ranked_router(row_logits):
+    """Router whose logits for one-hot row r (x = e_r) are exactly row_logits[r]:
+    Wr[e][r] = row_logits[r][e], zero elsewhere, H = 128."""
+    R, E = len(row_logits), len(row_logits[0])
+    H = 128
+    router = np.zeros((E, H), np.float32)
+    for r in range(R):
+        for e in range(E):
+            router[e, r] = row_logits[r][e]
+    xb = np.zeros((R, H), np.uint16)
+    for r in range(R):
+        xb[r, r] = bf16(1.0)
+    return router, xb
+
+
+# Hand-built ranks (k = 4).  Row 0 ranks experts 0, 1, 2, 3 (1-based ranks 1..4); row 1
+# ranks 0, 1, 4, 5.  So expert 2 and 4 are only ever rank 3, experts 3 and 5 only rank 4.
+TAIL_LOGITS_A = [[8.0, 7.0, 6.0, 5.0, 1.0, 0.5, 0.0, -1.0],
+                 [8.0, 7.0, 0.0, -1.0, 6.0, 5.0, -2.0, -3.0]]
+# Row 1 now ranks 0, 3, 1, 4: expert 3 is rank 4 in row 0 but rank 2 in row 1.
+TAIL_LOGITS_B = [[8.0, 7.0, 6.0, 5.0, 1.0, 0.5, 0.0, -1.0],
+                 [8.0, 7.0, 0.0, 7.5, 6.0, -1.0, -2.0, -3.0]]
+
+
+@pytest.mark.parametrize("tail, union", [(0, [0, 1, 2, 3, 4, 5]), (5, [0, 1, 2, 3, 4, 5]),
+                                         (4, [0, 1, 2, 4]), (3, [0, 1]), (2, [0]), (1, [])])
+def test_tail_skip_union_hand_built(tail, union):
+    router, xb = _ranked_router(TAIL_LOGITS_A)
+    rt = oracle.route(router, xb, 4, tail)
+    np.testing.assert_array_equal(rt.ids, [[0, 1, 2, 3], [0, 1, 4, 5]])
+    assert rt.union.tolist() == union
+    for r in range(2):
+        for j in range(4):
+            assert rt.keep[r, j] == (rt.ids[r, j] in union)
+
+
+def test_tail_skip_keeps_an_expert_ranked_high_by_any_row():
+    router, xb = _ranked_router(TAIL_LOGITS_B)
+    rt = oracle.route(router, xb, 4, 3)
+    np.testing.assert_array_equal(rt.ids, [[0, 1, 2, 3], [0, 3, 1, 4]])
+    # expert 3: rank 4 in row 0, rank 2 in row 1 -> kept; 2 and 4 are only rank 3
+    assert rt.union.tolist() == [0, 1, 3]
+    np.testing.assert_array_equal(rt.keep, [[1, 1, 0, 1], [1, 1, 1, 0]])
+
+
+def test_tail_skip_weights_are_not_renormalised():
+    router, xb = _ranked_router(TAIL_LOGITS_A)
+    full = oracle.route(router, xb, 4, 0)
+    skip = oracle.route(router, xb, 4, 3)
+    np.testing.assert_array_equal(full.w, skip.w)
+    # row 0's kept weights are the first two softmax terms of logits 8, 7, 6, 5
+    ex = np.exp(np.array([8.0, 7.0, 6.0, 5.0]) - 8.0)
+    np.testing.assert_allclose(skip.w[0, :2], ex[:2] / ex.sum(), rtol=1e-15)
+
+
+def test_tail_skip_layer_equals_dense_with_dropped_gates(tiny4):
+    cfg, router, xb, ew = tiny4
+    for tail in (1, 2, 3):
+        rt = oracle.route(router, xb, cfg.top_k, tail)
+        out = oracle.layer(router, xb, cfg.top_k, np.arange(cfg.experts), ew, tail)
+        dense = oracle.layer_dense(router, xb, cfg.top_k, ew, tail)
+        scale = max(np.abs(dense).max(), 1e-30)
+        np.testing.assert_allclose(out, dense, rtol=1e-12, atol=1e-12 * scale)
+        if tail == 1:
+            assert rt.union.size == 0
+            assert not out.any()
+    # a threshold past k drops nothing: bitwise the plain layer
+    plain = oracle.layer(router, xb, cfg.top_k, np.arange(cfg.experts), ew)
+    past = oracle.layer(router, xb, cfg.top_k, np.arange(cfg.experts), ew, cfg.top_k + 1)
+    np.testing.assert_array_equal(plain, past)
+
+
+def test_tail_skip_union_grows_with_threshold():
+    cfg = syngen.CONFIGS["a3b_r4"]
+    router = syngen.router(cfg, 0)
+    xb = syngen.rows(cfg, 0)
+    sizes = [oracle.route(router, xb, cfg.top_k, t).union.size for t in range(1, cfg.top_k + 2)]
+    assert sizes[0] == 0 and all(a <= b for a, b in zip(sizes, sizes[1:]))
+    assert sizes[-1] == oracle.route(router, xb, cfg.top_k).union.size
