@@ -316,6 +316,19 @@ def run_ours(args):
                              "unique_experts_per_layer": float(np.mean(r["U"])),
                              "picks_per_layer": rows * cfg.top_k,
                              "tokens_per_round_equiv_per_s": rows / (msr * 1e-3)}
+    # the same 4-row round with the routing tail skip at the page's rank 7 (an
+    # approximation: experts every row ranks 7th or lower are not evaluated)
+    mv.moe_set_tail_skip(handle, 7)
+    try:
+        r = time_rounds(4, 0.5, max(20, args.steps // 4), max(args.warmup, 3))
+    finally:
+        mv.moe_set_tail_skip(handle, 0)
+    msr = r["ms_total"] / r["steps"]
+    gbs = r["bytes_per_round"] / (msr * 1e-3) / 1e9
+    sweep["r4_tail7"] = {"workload": "a3b_r4 with routing tail skip at rank 7", "us_per_layer": 1e3 * msr / L,
+                         "us_per_round": 1e3 * msr, "hbm_gbs": gbs, "frac_of_peak": gbs / peak,
+                         "unique_experts_per_layer": float(np.mean(r["U"])),
+                         "tokens_per_round_equiv_per_s": 4 / (msr * 1e-3)}
 
     # The round is one kernel launch (k_round): its average launch duration is the timed
     # region's per-step time, from CUDA events on the launching stream.  A separate

@@ -151,6 +151,18 @@ int32_t moe_last_launch_count(const moe_handle* h);
  * so tests can exercise the MOE_ETIMEOUT path without any hang. */
 int moe_set_wait_limit_ns(moe_handle* h, uint64_t ns);
 
+/* Routing tail skip (an approximation; off by default).  Avalon README, "Numbers" (RX
+ * 7900 XT): experts that every token of a verification routes only at rank 7 or lower
+ * are skipped.  With rank = T > 0, every later moe_route / moe_decode_layer / moe_round
+ * call of this handle drops a union expert when each row that picked it has it at
+ * 1-based rank >= T (T = 7 is the page's setting): the expert leaves the union
+ * (union_ids, n_union and stats shrink), its picks contribute nothing to the output,
+ * and the remaining weights are not renormalised (the page does not say; this is the
+ * reading taken).  topk_ids / topk_w still report every row's k picks.  rank = 0 turns
+ * it off; T = 1 drops every expert (output 0); T > k drops none.  Returns MOE_EINVAL for
+ * a NULL handle or rank < 0.  moe_decode_layer_noalloc never skips. */
+int moe_set_tail_skip(moe_handle* h, int32_t rank);
+
 /* Timing of eager (non-graph) calls.  moe_profile(h, 1) starts recording a CUDA event
  * pair around every kernel launch the handle makes on the caller's stream, and
  * per-phase device timestamps inside moe_round (first use allocates a small device

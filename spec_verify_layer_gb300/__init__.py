@@ -22,7 +22,8 @@ MOE_GATEUP, MOE_DOWN = 0, 1
 ABI_SYMBOLS = (
     "moe_create", "moe_destroy", "moe_workspace_bytes", "moe_packed_bytes", "moe_pack_q4",
     "moe_route", "moe_decode_layer", "moe_round", "moe_last_device_status",
-    "moe_last_launch_count", "moe_set_wait_limit_ns", "moe_profile", "moe_profile_read",
+    "moe_last_launch_count", "moe_set_wait_limit_ns", "moe_set_tail_skip", "moe_profile",
+    "moe_profile_read",
     "moe_profile_phases", "moe_decode_layer_noalloc", "moe_strerror",
 )
 MOE_NOALLOC_SCRATCH_BYTES = 4 << 20
@@ -76,6 +77,8 @@ _lib.moe_last_launch_count.argtypes = [_vp]
 _lib.moe_last_launch_count.restype = _i32
 _lib.moe_set_wait_limit_ns.argtypes = [_vp, ctypes.c_uint64]
 _lib.moe_set_wait_limit_ns.restype = ctypes.c_int
+_lib.moe_set_tail_skip.argtypes = [_vp, ctypes.c_int32]
+_lib.moe_set_tail_skip.restype = ctypes.c_int
 _lib.moe_profile.argtypes = [_vp, ctypes.c_int]
 _lib.moe_profile.restype = ctypes.c_int
 _lib.moe_profile_read.argtypes = [_vp, ctypes.c_int, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_i32)]
@@ -164,6 +167,11 @@ def moe_last_launch_count(handle: int) -> int:
 
 def moe_set_wait_limit_ns(handle: int, ns: int) -> None:
     _check(_lib.moe_set_wait_limit_ns(handle, int(ns)), "moe_set_wait_limit_ns")
+
+
+def moe_set_tail_skip(handle: int, rank: int) -> None:
+    """Routing tail skip threshold (1-based rank; 0 = off); see the header."""
+    _check(_lib.moe_set_tail_skip(handle, int(rank)), "moe_set_tail_skip")
 
 
 def moe_profile(handle: int, enable: bool) -> None:

@@ -67,6 +67,7 @@ struct RoundArgs {
   int H, E, k, I, R, L;
   int Rmax;  // the handle's max_rows: the shared-memory plan is sized by it, not by R
   int route_only;
+  int tail_rank;  // > 0: drop union experts every picking row has at 1-based rank >= it
   const uint16_t* x;  // [L][R][H] bf16 bits
   float* out;         // [L][R][H]
   int* stats;         // [L] |U| per layer, or null
@@ -433,9 +434,15 @@ __device__ __forceinline__ void select_row(const float* row, int E, int k, int l
 }
 
 // scratch (inside the staging area, free while routing): mask [E] (zeroed by the
-// caller beforehand), off_e [E], ids [R*k], union index [E]
+// caller beforehand), off_e [E], ids [R*k], union index [E], best rank [E] (set to
+// INT_MAX by the caller beforehand).
+//
+// Tail skip (Avalon README, "Numbers": experts that every token of a verification
+// routes only at rank 7 or lower are skipped): with a.tail_rank = T > 0 an expert whose
+// best 1-based rank over the rows that picked it is >= T leaves the union; its picks
+// are not evaluated and the other weights are not renormalised.
 __device__ int route_phase(const RoundArgs& a, const Tables& T, unsigned* s_mask, int* s_off_e,
-                           int* s_ids, int* s_ui, int layer) {
+                           int* s_ids, int* s_ui, int* s_rank, int layer) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int E = a.E, k = a.k, R = a.R;
   // rows: top-k, renormalised weights, row bits of each picked expert
@@ -456,6 +463,7 @@ __device__ int route_phase(const RoundArgs& a, const Tables& T, unsigned* s_mask
       s_ids[p] = my_id;
       T.w[p] = wj;
       atomicOr(&s_mask[my_id], 1u << r);
+      if (a.tail_rank > 0) atomicMin(&s_rank[my_id], lane);
       if (blockIdx.x == 0) {
         if (a.user_ids) a.user_ids[p] = my_id;
         if (a.user_w) a.user_w[p] = wj;
@@ -470,7 +478,11 @@ __device__ int route_phase(const RoundArgs& a, const Tables& T, unsigned* s_mask
     const int e0 = lane * per, e1 = min(e0 + per, E);
     int lf = 0, lc = 0;
     for (int e = e0; e < e1; ++e) {
-      const unsigned m = s_mask[e];
+      unsigned m = s_mask[e];
+      if (m && a.tail_rank > 0 && s_rank[e] + 1 >= a.tail_rank) {
+        m = 0u;  // tail-skipped: out of the union, its picks are dropped
+        s_mask[e] = 0u;
+      }
       lf += (m != 0u);
       lc += __popc(m);
     }
@@ -510,6 +522,7 @@ __device__ int route_phase(const RoundArgs& a, const Tables& T, unsigned* s_mask
   __syncthreads();
   for (int p = tid; p < R * k; p += NT) {
     const int e = s_ids[p], r = p / k;
+    if (s_mask[e] == 0u) continue;  // (tail-skipped)
     const int pos = s_off_e[e] + __popc(s_mask[e] & ((1u << r) - 1u));
     T.pair[pos] = p;
     T.pos_row[pos] = r;
@@ -960,6 +973,7 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
   int* s_off_e = reinterpret_cast<int*>(gu + (size_t)a.E * 4);
   int* s_ids = reinterpret_cast<int*>(gu + (size_t)a.E * 8);
   int* s_ui = reinterpret_cast<int*>(gu + (size_t)a.E * 8 + (size_t)a.R * a.k * 4);
+  int* s_rank = s_ui + a.E;
   if (tid == 0) {
     for (int i = 0; i < bar_h0 + 2; ++i) mbar_init(smem_u32(bars + i), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -1011,14 +1025,17 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
     stamp(a, l, 1);
     // B1 (all logits written); the activation pairs are built while it completes
     grid_arrive(a, sy);
-    for (int e = tid; e < a.E; e += NT) s_mask[e] = 0u;  // (the router rows there are consumed)
+    for (int e = tid; e < a.E; e += NT) {  // (the router rows there are consumed)
+      s_mask[e] = 0u;
+      s_rank[e] = INT_MAX;
+    }
     if (x_staged && !a.route_only) stage_xpairs(a, x, s_xp, s_xs);
     if (!grid_wait(a, sy)) {
       bail();
       return;
     }
     stamp(a, l, 2);
-    const int U = route_phase(a, T, s_mask, s_off_e, s_ids, s_ui, l);
+    const int U = route_phase(a, T, s_mask, s_off_e, s_ids, s_ui, s_rank, l);
     stamp(a, l, 3);
     if (a.route_only) return;
     // ---- plan this CTA's gate/up chunks; issue them and the down prefetch ----
@@ -1214,10 +1231,12 @@ using namespace moe;
 struct GraphKey {
   std::vector<moe_layer_w> layers;
   int32_t rows = 0;
+  int32_t tail_rank = 0;
   const void *x = nullptr, *out = nullptr, *stats = nullptr, *ws = nullptr, *stream = nullptr;
   size_t ws_bytes = 0;
   bool operator==(const GraphKey& o) const {
-    if (rows != o.rows || x != o.x || out != o.out || stats != o.stats || ws != o.ws ||
+    if (rows != o.rows || tail_rank != o.tail_rank || x != o.x || out != o.out || stats != o.stats ||
+        ws != o.ws ||
         stream != o.stream || ws_bytes != o.ws_bytes || layers.size() != o.layers.size())
       return false;
     return layers.empty() ||
@@ -1231,6 +1250,7 @@ struct moe_handle {
   int sm_count = 0;
   unsigned* status = nullptr;
   unsigned long long wait_ns = kDefaultWaitNs;
+  int32_t tail_rank = 0;
   int32_t last_launches = 0;
   GraphKey gkey;
   cudaGraphExec_t gexec = nullptr;
@@ -1273,6 +1293,22 @@ int check_layer(const moe_layer_w* w) {
   return MOE_OK;
 }
 
+// The dynamic shared-memory limit is an attribute of the kernel function, shared by
+// every handle: raise it once to the device's opt-in maximum (minus the kernel's static
+// shared memory), so a handle created later with a smaller plan cannot lower it below
+// what an earlier handle launches with.
+template <int NBL>
+cudaError_t allow_max_dynamic_smem(int device) {
+  int optin = 0;
+  cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
+  cudaFuncAttributes fa{};
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, k_round<NBL>);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_round<NBL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             optin - (int)fa.sharedSizeBytes);
+  return e;
+}
+
 size_t smem_bytes(const moe_dims& d, int rows, int grid) {
   return smem_plan(d.hidden, d.inter, d.n_experts, rows, d.top_k, grid).total;
 }
@@ -1291,6 +1327,7 @@ void fill_args(RoundArgs& a, const moe_handle* h, int rows, void* ws) {
   a.logits = reinterpret_cast<float*>(base + L.logits);
   a.hbuf = reinterpret_cast<float*>(base + L.hbuf);
   a.status = h->status;
+  a.tail_rank = h->tail_rank;
   const unsigned long long ns = h->wait_ns < (1ull << 40) ? h->wait_ns : (1ull << 40);
   a.wait_cycles = (long long)ns * kCyclesPerNs;
 }
@@ -1386,10 +1423,10 @@ int moe_create(const moe_dims* dims, int device, moe_handle** out) {
   cudaError_t e;
   int occ = 0;
   if (nbl_of(dims->hidden) == 1) {
-    e = cudaFuncSetAttribute(k_round<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = allow_max_dynamic_smem<1>(device);
     if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_round<1>, NT, smem);
   } else {
-    e = cudaFuncSetAttribute(k_round<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = allow_max_dynamic_smem<2>(device);
     if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_round<2>, NT, smem);
   }
   if (e != cudaSuccess || occ < 1) {
@@ -1415,6 +1452,12 @@ void moe_destroy(moe_handle* h) {
 int moe_set_wait_limit_ns(moe_handle* h, uint64_t ns) {
   if (!h) return MOE_EINVAL;
   h->wait_ns = ns ? ns : kDefaultWaitNs;
+  return MOE_OK;
+}
+
+int moe_set_tail_skip(moe_handle* h, int32_t rank) {
+  if (!h || rank < 0) return MOE_EINVAL;
+  h->tail_rank = rank;
   return MOE_OK;
 }
 
@@ -1491,6 +1534,7 @@ int moe_round(moe_handle* h, const moe_layer_w* layers, int32_t L, const uint16_
   GraphKey key;
   key.layers.assign(layers, layers + L);
   key.rows = rows;
+  key.tail_rank = h->tail_rank;
   key.x = x_bf16;
   key.out = out;
   key.stats = stats;
@@ -1656,9 +1700,9 @@ int noalloc_setup(int dev, size_t smem, NoAllocDevice** out) {
     d.sms = sms;
     d.ready = true;
   }
-  cudaError_t e = cudaFuncSetAttribute(k_round<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(k_round<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  (void)smem;  // (checked against the device limit by the caller)
+  cudaError_t e = allow_max_dynamic_smem<1>(dev);
+  if (e == cudaSuccess) e = allow_max_dynamic_smem<2>(dev);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return MOE_ECUDA;

@@ -299,3 +299,56 @@ def test_calls_with_fewer_rows_than_the_handle_allows():
         np.testing.assert_array_equal(out.cpu().numpy()[0], run_layer(s, 0, xs[0]))
     finally:
         s.close()
+
+
+# ---- routing tail skip ----------------------------------------------------------------
+
+TAIL_CASES = {"tiny": [(3, 0.5)], "a3b_r1": [(4, 0.5), (16, 0.1)], "e512_r3": [(3, 0.5)]}
+
+
+def test_tail_skip_matches_oracle(stack):
+    """With the tail skip on, the union (after the skip) is bit-exact and the outputs
+    match the oracle's mirror of the rule; rank 1 drops everything, rank k+1 nothing."""
+    cfg = stack.cfg
+    k = cfg.top_k
+    ranks = sorted({1, max(1, k - 1), min(7, k), k + 1})
+    try:
+        for tail in ranks:
+            mv.moe_set_tail_skip(stack.handle, tail)
+            for R, sigma in TAIL_CASES[cfg.name]:
+                xb = stack.rows(1, R, sigma)
+                router = syngen.router(cfg, 1)
+                rt = oracle.route(router, xb, k, tail)
+                ids, w, uni = run_route(stack, 1, xb)
+                np.testing.assert_array_equal(ids, rt.ids)
+                np.testing.assert_array_equal(uni, rt.union)
+                got = run_layer(stack, 1, xb)
+                if rt.union.size == 0:
+                    assert not got.any(), "every expert skipped: the output must be zero"
+                    continue
+                ref = oracle.layer(router, xb, k, rt.union, syngen.experts_stacked(cfg, 1, rt.union), tail)
+                assert_close(got, ref, f"{cfg.name} R={R} tail {tail}")
+    finally:
+        mv.moe_set_tail_skip(stack.handle, 0)
+
+
+def test_tail_skip_setter_rejects_negative_rank(stack):
+    with pytest.raises(mv.MoeError):
+        mv.moe_set_tail_skip(stack.handle, -1)
+
+
+def test_a_later_handle_with_a_smaller_plan_keeps_earlier_handles_working(stack):
+    """The kernel's dynamic shared-memory limit is shared by all handles; creating a
+    handle for a small shape must not lower it below what a bigger handle launches."""
+    small = syngen.CONFIGS["tiny"]
+    h2 = mv.moe_create(mv.make_dims(small.hidden, small.experts, small.top_k, small.inter, 1), 0)
+    try:
+        xb = stack.rows(0, 1, 0.0)
+        got = run_layer(stack, 0, xb)
+        router = syngen.router(stack.cfg, 0)
+        rt = oracle.route(router, xb, stack.cfg.top_k)
+        ref = oracle.layer(router, xb, stack.cfg.top_k, rt.union,
+                           syngen.experts_stacked(stack.cfg, 0, rt.union))
+        assert_close(got, ref, f"{stack.cfg.name} after a second handle")
+    finally:
+        mv.moe_destroy(h2)

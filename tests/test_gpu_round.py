@@ -17,7 +17,7 @@ from gpu_helpers import Stack, assert_close, stream_of
 pytestmark = pytest.mark.gpu
 
 
-def round_case(stack, cfg, n_rows, sigma, use_graph, check_layers):
+def round_case(stack, cfg, n_rows, sigma, use_graph, check_layers, tail=0):
     dev = stack.device
     L = len(stack.layers)
     H = cfg.hidden
@@ -41,12 +41,13 @@ def round_case(stack, cfg, n_rows, sigma, use_graph, check_layers):
     st = stats.cpu().numpy()
     got = out.cpu().numpy()
     for l in range(L):
-        rt = oracle.route(syngen.router(cfg, l), xs[l], cfg.top_k)
+        rt = oracle.route(syngen.router(cfg, l), xs[l], cfg.top_k, tail)
         assert st[l] == rt.union.size, f"layer {l}: |U| {st[l]} vs {rt.union.size}"
     for l in check_layers:
         router = syngen.router(cfg, l)
-        rt = oracle.route(router, xs[l], cfg.top_k)
-        ref = oracle.layer(router, xs[l], cfg.top_k, rt.union, syngen.experts_stacked(cfg, l, rt.union))
+        rt = oracle.route(router, xs[l], cfg.top_k, tail)
+        ref = oracle.layer(router, xs[l], cfg.top_k, rt.union, syngen.experts_stacked(cfg, l, rt.union),
+                           tail)
         assert_close(got[l], ref, f"{cfg.name} R={n_rows} layer {l}")
     return got, st
 
@@ -89,3 +90,20 @@ def test_e512_round():
         round_case(s, cfg, cfg.rows, cfg.row_sigma, True, check_layers=(0, 23, 47))
     finally:
         s.close()
+
+
+def test_a3b_round_tail_skip(a3b_stack):
+    """The 4-row round with the page's tail skip (rank 7): |U| per layer as the oracle's
+    mirror of the rule, sampled layers within tolerance; switching the skip off again
+    re-captures the round graph (the setting is part of its key)."""
+    cfg = syngen.CONFIGS["a3b_r4"]
+    _, plain = round_case(a3b_stack, cfg, cfg.rows, cfg.row_sigma, True, check_layers=())
+    try:
+        mv.moe_set_tail_skip(a3b_stack.handle, 7)
+        _, skipped = round_case(a3b_stack, cfg, cfg.rows, cfg.row_sigma, True, check_layers=(0, 39),
+                                tail=7)
+    finally:
+        mv.moe_set_tail_skip(a3b_stack.handle, 0)
+    assert (skipped <= plain).all() and skipped.sum() < plain.sum()
+    _, again = round_case(a3b_stack, cfg, cfg.rows, cfg.row_sigma, True, check_layers=())
+    np.testing.assert_array_equal(again, plain)
