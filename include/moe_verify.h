@@ -77,6 +77,18 @@ typedef struct moe_layer_w {
   const uint16_t* gateup_scale;
   const uint8_t* down_nib;
   const uint16_t* down_scale;
+  /* Expert -> slot indirection (AlphaInfer docs, section 2: "which expert lives where"
+   * is per-round ingress data written into fixed buffers; section 5.1: one shared slot
+   * bank across layers).  NULL: expert e's packed weights are entry e of the four
+   * arrays above (as moe_pack_q4 writes them for a layer).  Otherwise a DEVICE int32
+   * array [n_experts]: expert e's weights are entry slot_of_expert[e] of a bank of
+   * n_slots entries that the four pointers address (one moe_pack_q4 entry per slot;
+   * several layers may share one bank).  The kernel reads the table during the call,
+   * so a captured round (moe_round with use_graph) picks up new table contents
+   * without being rebuilt.  A slot outside [0, n_slots) is not read: the layer
+   * computes with slot 0 instead and moe_last_device_status returns MOE_EINVAL. */
+  const int32_t* slot_of_expert;
+  int32_t n_slots;
 } moe_layer_w;
 
 typedef struct moe_handle moe_handle;
@@ -138,7 +150,8 @@ int moe_round(moe_handle* h, const moe_layer_w* layers, int32_t L, const uint16_
               void* stream);
 
 /* Synchronizes `stream`, reads and clears the handle's device status word.
- * MOE_OK, MOE_ETIMEOUT (a bounded device wait gave up), or MOE_ECUDA. */
+ * MOE_OK, MOE_ETIMEOUT (a bounded device wait gave up), MOE_EINVAL (a slot table entry
+ * was outside [0, n_slots)), or MOE_ECUDA. */
 int moe_last_device_status(moe_handle* h, void* stream);
 
 /* Number of kernel launches the most recent moe_route / moe_decode_layer /

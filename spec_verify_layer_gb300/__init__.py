@@ -40,7 +40,8 @@ class moe_dims(ctypes.Structure):
 class moe_layer_w(ctypes.Structure):
     _fields_ = [("router", ctypes.c_void_p), ("gateup_nib", ctypes.c_void_p),
                 ("gateup_scale", ctypes.c_void_p), ("down_nib", ctypes.c_void_p),
-                ("down_scale", ctypes.c_void_p)]
+                ("down_scale", ctypes.c_void_p), ("slot_of_expert", ctypes.c_void_p),
+                ("n_slots", ctypes.c_int32)]
 
 
 class MoeError(RuntimeError):
@@ -105,8 +106,13 @@ def make_dims(hidden: int, n_experts: int, top_k: int, inter: int, max_rows: int
     return moe_dims(hidden, n_experts, top_k, inter, max_rows)
 
 
-def make_layer_w(router: int, gateup_nib: int, gateup_scale: int, down_nib: int, down_scale: int) -> moe_layer_w:
-    return moe_layer_w(router, gateup_nib, gateup_scale, down_nib, down_scale)
+def make_layer_w(router: int, gateup_nib: int, gateup_scale: int, down_nib: int, down_scale: int,
+                 slot_of_expert: int = 0, n_slots: int = 0) -> moe_layer_w:
+    """Device pointers of one layer; slot_of_expert (device int32 [E], or 0) maps each
+    expert to an entry of a bank of n_slots packed experts that the four weight pointers
+    address."""
+    return moe_layer_w(router, gateup_nib, gateup_scale, down_nib, down_scale, slot_of_expert or None,
+                       int(n_slots))
 
 
 def moe_strerror(code: int) -> str:

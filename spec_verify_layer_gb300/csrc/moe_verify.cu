@@ -48,6 +48,7 @@ namespace {
 constexpr int NT = 512;  // threads per CTA
 constexpr int NW = NT / 32;
 constexpr unsigned kStatusTimeout = 1u;
+constexpr unsigned kStatusBadSlot = 2u;
 constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // 2 s
 // device waits count SM cycles: 2 cycles per requested ns bounds the wall time between
 // ns (at ~2 GHz) and a few times ns at lower clocks
@@ -61,6 +62,8 @@ struct LayerPtrs {
   const uint16_t* gu_sc;
   const uint8_t* dn_nib;
   const uint16_t* dn_sc;
+  const int32_t* slot;  // expert -> bank slot, or null (slot = expert)
+  int n_slots;
 };
 
 struct RoundArgs {
@@ -368,6 +371,7 @@ struct Tables {
   int* n_union;  // [1]
   int* pos_ui;   // [R*k] union index of the expert at each CSR position
   int* pos_row;  // [R*k] row at each CSR position
+  int* slot;     // [E] bank slot of each expert this layer
 };
 
 // True if (ka, ia) ranks before (kb, ib): larger key, then lower id.
@@ -566,8 +570,8 @@ struct GuChunk {
 // smem plan: GU ring | DN slots | x pairs | tables | out accumulators | wave outputs |
 // chunk list | barriers
 struct SmemPlan {
-  size_t gu_slot, gu, dn_slot, dn, xrows, uni, csr, pair, w, pos_ui, pos_row, nunion, acc, ybuf, chunks, bars,
-      total;
+  size_t gu_slot, gu, dn_slot, dn, xrows, uni, csr, pair, w, pos_ui, pos_row, slot, nunion, acc, ybuf, chunks,
+      bars, total;
   size_t ring;    // bytes of the gate/up ring (>= kGuSlots * gu_slot)
   size_t h_slot;  // bytes per h slot (two slots from gu + kHOffset)
   int gu_cap;     // units per gate/up chunk
@@ -584,7 +588,8 @@ __host__ __device__ inline SmemPlan smem_plan(int H, int I, int E, int R, int k,
   p.max_orows = (H + grid - 1) / grid;
   p.dn_slot = up128((size_t)p.max_orows * (I / 2)) + up128((size_t)p.max_orows * (I / 16));
   const size_t tables = up128((size_t)E * 4) + up128((size_t)(E + 1) * 4) +
-                        4 * up128((size_t)R * k * 4) + 128 + up128((size_t)R * kAccStride * 4) +
+                        4 * up128((size_t)R * k * 4) + up128((size_t)E * 4) + 128 +
+                        up128((size_t)R * kAccStride * 4) +
                         up128((size_t)NW * kAccStride * 4) + up128(kMaxChunks * 12 + 16) + 256;
   const size_t fixed = tables + kDnSlots * p.dn_slot + kXBytes;
   const size_t limit = (size_t)225 * 1024;
@@ -606,6 +611,7 @@ __host__ __device__ inline SmemPlan smem_plan(int H, int I, int E, int R, int k,
   p.w = off;       off += up128((size_t)R * k * 4);
   p.pos_ui = off;  off += up128((size_t)R * k * 4);
   p.pos_row = off; off += up128((size_t)R * k * 4);
+  p.slot = off;    off += up128((size_t)E * 4);
   p.nunion = off;  off += 128;
   p.acc = off;     off += up128((size_t)R * kAccStride * 4);
   p.ybuf = off;    off += up128((size_t)NW * kAccStride * 4);
@@ -627,8 +633,8 @@ __host__ __device__ inline SmemPlan smem_plan(int H, int I, int E, int R, int k,
 __device__ void issue_gu_chunk(const RoundArgs& a, const LayerPtrs& W, const Tables& T, uint8_t* dst,
                                uint32_t bar, const GuChunk& c) {
   const size_t H = (size_t)a.H, I = (size_t)a.I;
-  const size_t u = (size_t)T.uni[c.ui];
-  const size_t first = u * I + (size_t)c.i0;  // unit index within the layer
+  const size_t u = (size_t)T.slot[T.uni[c.ui]];
+  const size_t first = u * I + (size_t)c.i0;  // unit index within the bank
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   mbar_expect_tx(bar, (uint32_t)((size_t)c.n * (H + H / 8)));
   bulk_g2s(smem_u32(dst), W.gu_nib + first * H, (uint32_t)(c.n * H), bar);
@@ -639,7 +645,7 @@ __device__ void issue_gu_chunk(const RoundArgs& a, const LayerPtrs& W, const Tab
 __device__ void issue_dn_chunk(const RoundArgs& a, const LayerPtrs& W, const Tables& T, uint8_t* dst,
                                uint32_t bar, int ui, int o0, int no, size_t codes_room) {
   const size_t H = (size_t)a.H, I = (size_t)a.I;
-  const size_t u = (size_t)T.uni[ui];
+  const size_t u = (size_t)T.slot[T.uni[ui]];
   const size_t row0 = u * H + (size_t)o0;
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   mbar_expect_tx(bar, (uint32_t)((size_t)no * (I / 2 + I / 16)));
@@ -967,7 +973,7 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
   Tables T{reinterpret_cast<int*>(smem + P.uni),     reinterpret_cast<int*>(smem + P.csr),
            reinterpret_cast<int*>(smem + P.pair),    reinterpret_cast<float*>(smem + P.w),
            reinterpret_cast<int*>(smem + P.nunion),  reinterpret_cast<int*>(smem + P.pos_ui),
-           reinterpret_cast<int*>(smem + P.pos_row)};
+           reinterpret_cast<int*>(smem + P.pos_row), reinterpret_cast<int*>(smem + P.slot)};
   // routing scratch lives in the (then idle) gate/up ring
   unsigned* s_mask = reinterpret_cast<unsigned*>(gu);
   int* s_off_e = reinterpret_cast<int*>(gu + (size_t)a.E * 4);
@@ -1028,6 +1034,17 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
     for (int e = tid; e < a.E; e += NT) {  // (the router rows there are consumed)
       s_mask[e] = 0u;
       s_rank[e] = INT_MAX;
+      // this layer's expert -> slot table (ingress data); an entry outside the bank is
+      // reported and replaced by slot 0, so no copy leaves the bank
+      int sl = e;
+      if (W.slot) {
+        sl = __ldg(W.slot + e);
+        if ((unsigned)sl >= (unsigned)W.n_slots) {
+          atomicOr(a.status, kStatusBadSlot);
+          sl = 0;
+        }
+      }
+      T.slot[e] = sl;
     }
     if (x_staged && !a.route_only) stage_xpairs(a, x, s_xp, s_xs);
     if (!grid_wait(a, sy)) {
@@ -1290,6 +1307,8 @@ int check_layer(const moe_layer_w* w) {
   if (!aligned16(w->router) || !aligned16(w->gateup_nib) || !aligned16(w->gateup_scale) ||
       !aligned16(w->down_nib) || !aligned16(w->down_scale))
     return MOE_EINVAL;
+  if (w->slot_of_expert && (w->n_slots < 1 || (reinterpret_cast<uintptr_t>(w->slot_of_expert) & 3u)))
+    return MOE_EINVAL;
   return MOE_OK;
 }
 
@@ -1380,6 +1399,8 @@ void copy_layers(RoundArgs& a, const moe_layer_w* layers, int32_t L) {
     a.layer[l].gu_sc = layers[l].gateup_scale;
     a.layer[l].dn_nib = layers[l].down_nib;
     a.layer[l].dn_sc = layers[l].down_scale;
+    a.layer[l].slot = layers[l].slot_of_expert;
+    a.layer[l].n_slots = layers[l].n_slots;
   }
 }
 
@@ -1579,7 +1600,8 @@ int moe_last_device_status(moe_handle* h, void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MOE_ECUDA;
   if (cudaMemcpy(&v, h->status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ECUDA;
   if (cudaMemset(h->status, 0, sizeof(unsigned)) != cudaSuccess) return MOE_ECUDA;
-  return (v & kStatusTimeout) ? MOE_ETIMEOUT : MOE_OK;
+  if (v & kStatusTimeout) return MOE_ETIMEOUT;
+  return (v & kStatusBadSlot) ? MOE_EINVAL : MOE_OK;
 }
 
 int32_t moe_last_launch_count(const moe_handle* h) { return h ? h->last_launches : 0; }
