@@ -293,6 +293,19 @@ def run_ours(args):
                 "launches_per_round": launches_per_round, "t_wall": (t_wall0, t_wall1),
                 "x": x, "out": out, "xs": xs}
 
+    def profile_phases(rows, x, out, n_rounds):
+        """Eager rounds with per-phase device timestamps (outside every timed region)."""
+        stats_p = torch.zeros(L, dtype=torch.int32, device=dev)
+        mv.moe_profile(handle, True)
+        with torch.cuda.stream(stream):
+            for _ in range(n_rounds):
+                mv.moe_round(handle, wl, x.data_ptr(), rows, out.data_ptr(), stats_p.data_ptr(), ws.data_ptr(),
+                             ws.numel(), False, st)
+        eager_ms, eager_n = mv.moe_profile_read(handle, mv.KIND_ROUND)
+        ph = {k: {"mean_us": v[0], "max_us": v[1]} for k, v in mv.moe_profile_phases(handle).items()}
+        mv.moe_profile(handle, False)
+        return ph, eager_ms, eager_n
+
     peak, peak_src = peak_hbm()
     sampler = ClockSampler(local)
     sampler.start()
@@ -316,6 +329,7 @@ def run_ours(args):
                              "unique_experts_per_layer": float(np.mean(r["U"])),
                              "picks_per_layer": rows * cfg.top_k,
                              "tokens_per_round_equiv_per_s": rows / (msr * 1e-3)}
+        sweep[f"r{rows}"]["phases_per_layer_us"] = profile_phases(rows, r["x"], r["out"], 3)[0]
     # the same 4-row round with the routing tail skip at the page's rank 7 (an
     # approximation: experts every row ranks 7th or lower are not evaluated)
     mv.moe_set_tail_skip(handle, 7)
@@ -339,14 +353,7 @@ def run_ours(args):
     prof_rounds = max(3, min(20, args.steps // 50))
     x1, out1 = head["x"], head["out"]
     stats1 = torch.zeros(L, dtype=torch.int32, device=dev)
-    mv.moe_profile(handle, True)
-    with torch.cuda.stream(stream):
-        for _ in range(prof_rounds):
-            mv.moe_round(handle, wl, x1.data_ptr(), 1, out1.data_ptr(), stats1.data_ptr(), ws.data_ptr(),
-                         ws.numel(), False, st)
-    eager_ms, eager_n = mv.moe_profile_read(handle, mv.KIND_ROUND)
-    phases = {k: {"mean_us": v[0], "max_us": v[1]} for k, v in mv.moe_profile_phases(handle).items()}
-    mv.moe_profile(handle, False)
+    phases, eager_ms, eager_n = profile_phases(1, x1, out1, prof_rounds)
     roofline = {"bound": "hbm", "kernel": "k_round", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": read_traffic("k_round", L), "peak_source": peak_src,
                 "alg_bytes_per_launch": alg_per_launch, "avg_launch_us": avg_launch_us,

@@ -31,6 +31,7 @@
 // weight (plus one shift per 8), and packed f32x2 FMAs over pairs of weights.  The
 // code offset (q = n - 8) is applied once per 32-element block:
 // sum (n-8) x = 2^62 acc - 8 sum x.
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -921,6 +922,250 @@ __device__ __forceinline__ void down_position(const RoundArgs& a, const uint8_t*
   }
 }
 
+// ---------------------------------------------------------------------------------
+// Wide verify rounds (at least kMmaRows rows): gate/up and down on the tensor cores
+// (mma.sync m16n8k16, bf16 operands, fp32 accumulation).
+//
+// A nibble n in the low four bits of a bf16 whose other bits are those of 128.0 is the
+// bf16 value 128 + n, exactly; one mask-and-or per pair of weights (two nibbles 16 bits
+// apart land in the two halves of a bf16x2 register).  Inside each 32-element block the
+// MMA's k order is permuted so that thread t's A fragments for the block's two k16 steps
+// are exactly the eight nibbles of 32-bit word t of a row's 16-byte block:
+//   step 0: k (2t, 2t+1) <- elements (8t, 8t+4),   k (2t+8, 2t+9) <- (8t+1, 8t+5)
+//   step 1: k (2t, 2t+1) <- (8t+2, 8t+6),          k (2t+8, 2t+9) <- (8t+3, 8t+7)
+// The B fragments (activations, or the exchanged h' split into bf16 hi + lo) follow the
+// same permutation.  A block's MMAs give D = sum (128 + n) b; the layer needs
+// sum (n - 8) b = D - 136 sum b, times the row's block scale: the bias is one fp32
+// constant per (column, block), computed once.  Every tile's K range is split in the
+// same kKParts parts whatever the other rows are, and the parts are added in a fixed
+// order, so a row's result does not depend on the rows it shares the round with.
+
+constexpr int kMmaRows = 8;
+constexpr int kKParts = 4;
+constexpr int kTilesPerRound = NW / kKParts;  // tiles in flight (one warp per tile part)
+// scratch of the tensor-core path inside the activation-pair region (unused then)
+constexpr size_t kMmaCorrX = 0;          // [R][H/32] fp32: 136 x block sums of the rows
+constexpr size_t kMmaPart = 8192;        // [NW][16][8] fp32 partial tiles
+constexpr size_t kMmaCorrH = 16384;      // [wave][I/32] fp32: 136 x block sums of h'
+constexpr size_t kMmaTiles = 22528;      // [64][3] int: down tiles of a wave
+constexpr int kMmaMaxTiles = 64;
+
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// A 32-bit word of codes (eight nibbles, elements 0..7 of the word) -> four bf16 pairs
+// (128 + n): (0, 4), (1, 5), (2, 6), (3, 7).
+__device__ __forceinline__ void dq_word(uint32_t w, uint32_t (&p)[4]) {
+  constexpr uint32_t M = 0x000F000Fu, C = 0x43004300u;
+  p[0] = (w & M) | C;
+  p[1] = ((w >> 4) & M) | C;
+  p[2] = ((w >> 8) & M) | C;
+  p[3] = ((w >> 12) & M) | C;
+}
+
+// Eight bf16 activations (elements 8t .. 8t+7 of a block) -> the same pairs.
+__device__ __forceinline__ void bfrag_x(uint4 v, uint32_t (&b)[4]) {
+  b[0] = __byte_perm(v.x, v.z, 0x5410);
+  b[1] = __byte_perm(v.x, v.z, 0x7632);
+  b[2] = __byte_perm(v.y, v.w, 0x5410);
+  b[3] = __byte_perm(v.y, v.w, 0x7632);
+}
+
+__device__ __forceinline__ float bf16_bits_f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+// 136 x the block sums of this layer's rows (fixed order), for the gate/up bias term.
+__device__ void mma_corr_x(const RoundArgs& a, const uint16_t* x, float* s_cx) {
+  const int NB = a.H >> 5;
+  for (int idx = threadIdx.x; idx < a.R * NB; idx += NT) {
+    const int r = idx / NB, b = idx - r * NB;
+    const uint16_t* src = x + (size_t)r * a.H + 32 * b;
+    float s = 0.f;
+#pragma unroll 8
+    for (int j = 0; j < 32; ++j) s = __fadd_rn(s, bf16_bits_f(__ldg(src + j)));
+    s_cx[idx] = __fmul_rn(136.f, s);
+  }
+}
+
+// Gate/up of one staged chunk on the tensor cores: tiles of 16 weight rows (8 units,
+// gate and up interleaved) x 8 of the expert's rows, one warp per (tile, K part); the
+// parts are added in order, then h' = w silu(g) v is stored split into bf16 hi + lo in
+// the down pass's fragment order.
+__device__ void gateup_chunk_mma(const RoundArgs& a, const Tables& T, const uint8_t* slot, const GuChunk& c,
+                                 const uint16_t* x, const float* s_cx, float* s_part) {
+  const int H = a.H, NB = H >> 5, NBI = a.I >> 5;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  const int p0 = T.csr_off[c.ui], Re = T.csr_off[c.ui + 1] - p0;
+  const int NTN = (Re + 7) >> 3, combos = ((2 * c.n + 15) >> 4) * NTN;
+  const uint8_t* codes = slot;
+  const uint16_t* scales = reinterpret_cast<const uint16_t*>(slot + (size_t)c.n * H);
+  uint16_t* hb = reinterpret_cast<uint16_t*>(a.hbuf);
+  for (int cb0 = 0; cb0 < combos; cb0 += kTilesPerRound) {
+    const int cb = cb0 + warp / kKParts, kp = warp % kKParts;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    if (cb < combos) {
+      const int mt = cb / NTN, nt = cb - mt * NTN;
+      const int ra = mt * 16 + g, rb = ra + 8;  // weight rows of the chunk (2 unit + gate/up)
+      const bool va = ra < 2 * c.n, vb = rb < 2 * c.n;
+      // columns past the expert's rows repeat its last row; their results are dropped
+      const int xr = T.pos_row[p0 + min(nt * 8 + g, Re - 1)];
+      const int r0 = T.pos_row[p0 + min(nt * 8 + 2 * t, Re - 1)];
+      const int r1 = T.pos_row[p0 + min(nt * 8 + 2 * t + 1, Re - 1)];
+      const uint4* xrow = reinterpret_cast<const uint4*>(x + (size_t)xr * H) + t;
+      const int b0 = (kp * NB) / kKParts, b1 = ((kp + 1) * NB) / kKParts;
+#pragma unroll 4
+      for (int b = b0; b < b1; ++b) {
+        const uint32_t wa = va ? *reinterpret_cast<const uint32_t*>(codes + ((size_t)ra * NB + b) * 16 + 4 * t) : 0u;
+        const uint32_t wb = vb ? *reinterpret_cast<const uint32_t*>(codes + ((size_t)rb * NB + b) * 16 + 4 * t) : 0u;
+        const uint4 xv = __ldg(xrow + 4 * b);
+        uint32_t pa[4], pb[4], bf[4];
+        dq_word(wa, pa);
+        dq_word(wb, pb);
+        bfrag_x(xv, bf);
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_bf16(d, pa[0], pb[0], pa[1], pb[1], bf[0], bf[1]);
+        mma_bf16(d, pa[2], pb[2], pa[3], pb[3], bf[2], bf[3]);
+        const float sa = va ? half_bits(scales[(size_t)ra * NB + b]) : 0.f;
+        const float sb = vb ? half_bits(scales[(size_t)rb * NB + b]) : 0.f;
+        const float k0 = s_cx[r0 * NB + b], k1 = s_cx[r1 * NB + b];
+        acc[0] = __fmaf_rn(sa, __fsub_rn(d[0], k0), acc[0]);
+        acc[1] = __fmaf_rn(sa, __fsub_rn(d[1], k1), acc[1]);
+        acc[2] = __fmaf_rn(sb, __fsub_rn(d[2], k0), acc[2]);
+        acc[3] = __fmaf_rn(sb, __fsub_rn(d[3], k1), acc[3]);
+      }
+    }
+    float* part = s_part + warp * 128;  // [16 rows][8 columns]
+    part[g * 8 + 2 * t] = acc[0];
+    part[g * 8 + 2 * t + 1] = acc[1];
+    part[(g + 8) * 8 + 2 * t] = acc[2];
+    part[(g + 8) * 8 + 2 * t + 1] = acc[3];
+    __syncthreads();
+    for (int i = threadIdx.x; i < kTilesPerRound * 64; i += NT) {
+      const int cl = i >> 6, uu = (i >> 3) & 7, cc = i & 7;
+      const int cb = cb0 + cl;
+      if (cb >= combos) continue;
+      const int mt = cb / NTN, nt = cb - mt * NTN;
+      const int u = mt * 8 + uu, col = nt * 8 + cc;
+      if (u >= c.n || col >= Re) continue;
+      float gs = 0.f, vs = 0.f;
+#pragma unroll
+      for (int kp = 0; kp < kKParts; ++kp) {
+        const float* P = s_part + (cl * kKParts + kp) * 128;
+        gs = __fadd_rn(gs, P[(2 * uu) * 8 + cc]);
+        vs = __fadd_rn(vs, P[(2 * uu + 1) * 8 + cc]);
+      }
+      const int pp = p0 + col;
+      const float hh = __fmul_rn(__fdiv_rn(gs, __fadd_rn(1.f, expf(-gs))), vs);
+      const float hw = __fmul_rn(T.w[T.pair[pp]], hh);
+      const __nv_bfloat16 hi = __float2bfloat16_rn(hw);
+      const __nv_bfloat16 lo = __float2bfloat16_rn(__fsub_rn(hw, __bfloat162float(hi)));
+      const int i2 = c.i0 + u, j = i2 & 31, e = j & 7;
+      const size_t base = (((size_t)pp * NBI + (i2 >> 5)) * 4 + (j >> 3)) * 16 + 2 * (e & 3) + (e >> 2);
+      hb[base] = __bfloat16_as_ushort(hi);
+      hb[base + 8] = __bfloat16_as_ushort(lo);
+    }
+    __syncthreads();
+  }
+}
+
+// Down pass of one wave on the tensor cores.  The wave's CSR positions [pa, pb) (h'
+// rows in shared memory at hs, hi + lo bf16 in fragment order) are cut into tiles of
+// up to 8 consecutive positions of one expert; each tile x each 16 of this CTA's output
+// rows, K = I split in kKParts parts, one warp per part; hi and lo as two MMAs per k16
+// step.  y[position][output row] goes to s_y.
+__device__ void down_wave_mma(const RoundArgs& a, const Tables& T, const uint8_t* dn, size_t dn_slot,
+                              size_t codes_room, int no, int pa, int pb, const uint8_t* hs, float* s_ch,
+                              float* s_part, int* s_tiles, float* s_y) {
+  const int NBI = a.I >> 5;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  // 136 x the block sums of the wave's h' (hi + lo), fixed order
+  for (int idx = threadIdx.x; idx < (pb - pa) * NBI; idx += NT) {
+    const uint16_t* v = reinterpret_cast<const uint16_t*>(hs + (size_t)idx * 128);
+    float s = 0.f;
+#pragma unroll 8
+    for (int q = 0; q < 64; ++q) s = __fadd_rn(s, bf16_bits_f(v[q]));
+    s_ch[idx] = __fmul_rn(136.f, s);
+  }
+  if (threadIdx.x == 0) {
+    int n = 0;
+    for (int p = pa; p < pb && n < kMmaMaxTiles;) {
+      const int ui = T.pos_ui[p];
+      int q = p;
+      while (q < pb && q - p < 8 && T.pos_ui[q] == ui) ++q;
+      s_tiles[3 * n] = p - pa;
+      s_tiles[3 * n + 1] = q - p;
+      s_tiles[3 * n + 2] = ui;
+      ++n;
+      p = q;
+    }
+    s_tiles[3 * kMmaMaxTiles] = n;
+  }
+  __syncthreads();
+  const int NTMo = (no + 15) >> 4;
+  const int combos = s_tiles[3 * kMmaMaxTiles] * NTMo;
+  for (int cb0 = 0; cb0 < combos; cb0 += kTilesPerRound) {
+    const int cb = cb0 + warp / kKParts, kp = warp % kKParts;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    if (cb < combos) {
+      const int ti = cb / NTMo, mt = cb - ti * NTMo;
+      const int q0 = s_tiles[3 * ti], cnt = s_tiles[3 * ti + 1], ui = s_tiles[3 * ti + 2];
+      const uint8_t* codes = dn + (size_t)(ui % kDnSlots) * dn_slot;
+      const uint16_t* scales = reinterpret_cast<const uint16_t*>(codes + codes_room);
+      const int ra = mt * 16 + g, rb = ra + 8;  // output rows of this CTA
+      const bool va = ra < no, vb = rb < no;
+      const int qg = q0 + min(g, cnt - 1);
+      const int qc0 = q0 + min(2 * t, cnt - 1), qc1 = q0 + min(2 * t + 1, cnt - 1);
+      const int b0 = (kp * NBI) / kKParts, b1 = ((kp + 1) * NBI) / kKParts;
+#pragma unroll 2
+      for (int b = b0; b < b1; ++b) {
+        const uint32_t wa = va ? *reinterpret_cast<const uint32_t*>(codes + ((size_t)ra * NBI + b) * 16 + 4 * t) : 0u;
+        const uint32_t wb = vb ? *reinterpret_cast<const uint32_t*>(codes + ((size_t)rb * NBI + b) * 16 + 4 * t) : 0u;
+        const uint4* hv = reinterpret_cast<const uint4*>(hs + ((size_t)qg * NBI + b) * 128 + 32 * t);
+        const uint4 hi = hv[0], lo = hv[1];
+        uint32_t pa4[4], pb4[4];
+        dq_word(wa, pa4);
+        dq_word(wb, pb4);
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_bf16(d, pa4[0], pb4[0], pa4[1], pb4[1], hi.x, hi.y);
+        mma_bf16(d, pa4[0], pb4[0], pa4[1], pb4[1], lo.x, lo.y);
+        mma_bf16(d, pa4[2], pb4[2], pa4[3], pb4[3], hi.z, hi.w);
+        mma_bf16(d, pa4[2], pb4[2], pa4[3], pb4[3], lo.z, lo.w);
+        const float sa = va ? half_bits(scales[(size_t)ra * NBI + b]) : 0.f;
+        const float sb = vb ? half_bits(scales[(size_t)rb * NBI + b]) : 0.f;
+        const float k0 = s_ch[qc0 * NBI + b], k1 = s_ch[qc1 * NBI + b];
+        acc[0] = __fmaf_rn(sa, __fsub_rn(d[0], k0), acc[0]);
+        acc[1] = __fmaf_rn(sa, __fsub_rn(d[1], k1), acc[1]);
+        acc[2] = __fmaf_rn(sb, __fsub_rn(d[2], k0), acc[2]);
+        acc[3] = __fmaf_rn(sb, __fsub_rn(d[3], k1), acc[3]);
+      }
+    }
+    float* part = s_part + warp * 128;
+    part[g * 8 + 2 * t] = acc[0];
+    part[g * 8 + 2 * t + 1] = acc[1];
+    part[(g + 8) * 8 + 2 * t] = acc[2];
+    part[(g + 8) * 8 + 2 * t + 1] = acc[3];
+    __syncthreads();
+    for (int i = threadIdx.x; i < kTilesPerRound * 128; i += NT) {
+      const int cl = i >> 7, r = (i >> 3) & 15, cc = i & 7;
+      const int cb = cb0 + cl;
+      if (cb >= combos) continue;
+      const int ti = cb / NTMo, mt = cb - ti * NTMo;
+      const int ol = mt * 16 + r;
+      if (ol >= no || cc >= s_tiles[3 * ti + 1]) continue;
+      float y = 0.f;
+#pragma unroll
+      for (int kp = 0; kp < kKParts; ++kp) y = __fadd_rn(y, s_part[(cl * kKParts + kp) * 128 + r * 8 + cc]);
+      s_y[(s_tiles[3 * ti] + cc) * kAccStride + ol] = y;
+    }
+    __syncthreads();
+  }
+}
+
 // Exchanged h rows of CSR positions [pa, pb) (contiguous in the workspace) -> slot.
 __device__ __forceinline__ void issue_hbatch(const RoundArgs& a, uint8_t* dst, uint32_t bar, int pa, int pb) {
   const size_t bytes = (size_t)(pb - pa) * a.I * 4;
@@ -965,7 +1210,12 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
   uint8_t* dn = smem + P.dn;
   float4* s_xp = reinterpret_cast<float4*>(smem + P.xrows);
   float* s_xs = reinterpret_cast<float*>(smem + P.xrows + (size_t)a.R * a.H * 4);
-  const bool x_staged = (size_t)a.R * a.H * 4 + (size_t)a.R * (a.H >> 5) * 4 <= kXBytes;
+  const bool mma = a.R >= kMmaRows;  // wide rounds: tensor-core gate/up and down
+  const bool x_staged = !mma && (size_t)a.R * a.H * 4 + (size_t)a.R * (a.H >> 5) * 4 <= kXBytes;
+  float* s_cx = reinterpret_cast<float*>(smem + P.xrows + kMmaCorrX);
+  float* s_mpart = reinterpret_cast<float*>(smem + P.xrows + kMmaPart);
+  float* s_ch = reinterpret_cast<float*>(smem + P.xrows + kMmaCorrH);
+  int* s_tiles = reinterpret_cast<int*>(smem + P.xrows + kMmaTiles);
   float* s_rw = reinterpret_cast<float*>(gu);
   float* s_acc = reinterpret_cast<float*>(smem + P.acc);
   float* s_y = reinterpret_cast<float*>(smem + P.ybuf);
@@ -1047,6 +1297,7 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
       T.slot[e] = sl;
     }
     if (x_staged && !a.route_only) stage_xpairs(a, x, s_xp, s_xs);
+    if (mma && !a.route_only) mma_corr_x(a, x, s_cx);
     if (!grid_wait(a, sy)) {
       bail();
       return;
@@ -1113,7 +1364,9 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
       stamp(a, l, 5);  // (the last chunk's stamp stays)
       const GuChunk c = s_chunks[n];
       const uint8_t* slot = gu + q * P.gu_slot;
-      if (x_staged)
+      if (mma)
+        gateup_chunk_mma(a, T, slot, c, x, s_cx, s_mpart);
+      else if (x_staged)
         gateup_chunk<NBL, true>(a, T, slot, c, x, s_xp, s_xs);
       else
         gateup_chunk<NBL, false>(a, T, slot, c, x, s_xp, s_xs);
@@ -1175,7 +1428,9 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
           waited = need;
         }
         stamp(a, l, 9);  // (the last wave's stamp stays)
-        {
+        if (mma) {
+          down_wave_mma(a, T, dn, P.dn_slot, codes_room, no, pa, pb, hslot(qh), s_ch, s_mpart, s_tiles, s_y);
+        } else {
           // positions of the wave over the warps; spare warps split a position's rows
           const int npos = pb - pa, wpp = NW / npos;
           const int pi = warp / wpp, part = warp - pi * wpp;

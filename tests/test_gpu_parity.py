@@ -352,3 +352,18 @@ def test_a_later_handle_with_a_smaller_plan_keeps_earlier_handles_working(stack)
         assert_close(got, ref, f"{stack.cfg.name} after a second handle")
     finally:
         mv.moe_destroy(h2)
+
+
+def test_wide_rounds_rows_are_independent_bitwise(stack):
+    """Rounds of >= 8 rows run on the tensor cores; there too a row's output is
+    bit-identical at any position and whatever other rows share the round."""
+    cfg = stack.cfg
+    xa = stack.rows(0, 16, 0.5)
+    full = run_layer(stack, 0, xa)
+    perm = np.roll(np.arange(16), 5)
+    rot = run_layer(stack, 0, xa[perm].copy())
+    np.testing.assert_array_equal(rot, full[perm])
+    other = syngen.rows(cfg, 1, 16, 0.5)
+    mixed = np.concatenate([xa[:8], other[8:]])
+    got = run_layer(stack, 0, mixed)
+    np.testing.assert_array_equal(got[:8], full[:8])
