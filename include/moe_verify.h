@@ -120,7 +120,10 @@ size_t moe_packed_bytes(const moe_dims* dims, int which, int part);
  *   gate/up codes  [E][I][2: gate, up][H/32 blocks][16 B]   (intermediate row i of an
  *   gate/up scales [E][I][2][H/32]                           expert: gate, then up)
  *   down codes     [E][H][I/32 blocks][16 B]                 (output-row major)
- *   down scales    [E][H][I/32]                                                       */
+ *   down scales    [E][H][I/32]
+ * where, within each row, the code block and the scale of logical block b are stored at
+ * position b ^ (key & 7), key = i for the gate and up rows of intermediate index i and
+ * key = o for down row o. */
 int moe_pack_q4(const moe_dims* dims, int which, int32_t n_experts, const int8_t* q_a,
                 const uint16_t* s_a, const int8_t* q_b, const uint16_t* s_b, uint8_t* nib_out,
                 uint16_t* scale_out);

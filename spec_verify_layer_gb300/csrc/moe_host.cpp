@@ -71,7 +71,8 @@ int moe_pack_q4(const moe_dims* dims, int which, int32_t n_experts, const int8_t
   const size_t H = (size_t)dims->hidden, I = (size_t)dims->inter;
   const size_t NB = H / 32, NBI = I / 32;
   if (which == MOE_GATEUP) {
-    // [E][I][2: gate, up][H/32 blocks][16 B], scales [E][I][2][H/32]
+    // [E][I][2: gate, up][H/32 blocks][16 B], scales [E][I][2][H/32]; block b of row
+    // (i, m) at position block_pos(b, i)
     if (!q_b || !s_b) return MOE_EINVAL;
     for (size_t e = 0; e < (size_t)n_experts; ++e) {
       uint8_t* nib = nib_out + e * gu_nib_bytes(*dims);
@@ -82,15 +83,16 @@ int moe_pack_q4(const moe_dims* dims, int which, int32_t n_experts, const int8_t
           const uint16_t* sv = (m == 0 ? s_a : s_b) + e * I * NB + i * NB;
           const size_t base = (i * 2 + m) * NB;
           for (size_t b = 0; b < NB; ++b) {
-            if (!pack_block(q + b * 32, nib + (base + b) * 16)) return MOE_EINVAL;
-            sc[base + b] = sv[b];
+            const size_t pb = (size_t)block_pos((int)b, (int)i);
+            if (!pack_block(q + b * 32, nib + (base + pb) * 16)) return MOE_EINVAL;
+            sc[base + pb] = sv[b];
           }
         }
     }
     return MOE_OK;
   }
   if (which == MOE_DOWN) {
-    // [E][H][I/32 blocks][16 B], scales [E][H][I/32] (the unpacked order)
+    // [E][H][I/32 blocks][16 B], scales [E][H][I/32]; block b of row o at block_pos(b, o)
     for (size_t e = 0; e < (size_t)n_experts; ++e) {
       uint8_t* nib = nib_out + e * dn_nib_bytes(*dims);
       uint16_t* sc = scale_out + e * (dn_sc_bytes(*dims) / 2);
@@ -98,8 +100,9 @@ int moe_pack_q4(const moe_dims* dims, int which, int32_t n_experts, const int8_t
       const uint16_t* sv = s_a + e * H * NBI;
       for (size_t o = 0; o < H; ++o)
         for (size_t b = 0; b < NBI; ++b) {
-          if (!pack_block(q + o * I + b * 32, nib + (o * NBI + b) * 16)) return MOE_EINVAL;
-          sc[o * NBI + b] = sv[o * NBI + b];
+          const size_t pb = (size_t)block_pos((int)b, (int)o);
+          if (!pack_block(q + o * I + b * 32, nib + (o * NBI + pb) * 16)) return MOE_EINVAL;
+          sc[o * NBI + pb] = sv[o * NBI + b];
         }
     }
     return MOE_OK;

@@ -28,6 +28,22 @@ struct WsLayout {
 };
 WsLayout ws_layout(const moe_dims& d, int rows);
 
+#ifdef __CUDACC__
+#define MOE_HD __host__ __device__
+#else
+#define MOE_HD
+#endif
+
+// Packed rows store their 32-element blocks permuted: logical block b sits at position
+// b ^ (key & 7), codes and scales alike (rows have a multiple of 8 blocks); the key is
+// the output row o of a down row and the intermediate index i of a gate/up row (gate
+// and up of one i share it).  The same logical block of 8 consecutive down rows, or of
+// the gate/up rows of 4 consecutive units, then falls in 8 (4) different 16-byte bank
+// groups of shared memory, so the tensor-core fragment loads of one block of 8 rows
+// have no (at most 2-way) bank conflicts; a warp reading the blocks of one row (lane
+// per block) reads a permutation of them, conflict-free.
+MOE_HD inline int block_pos(int b, int key) { return b ^ (key & 7); }
+
 // Per-expert packed sizes (bytes).
 inline size_t gu_nib_bytes(const moe_dims& d) { return (size_t)d.inter * d.hidden; }
 inline size_t gu_sc_bytes(const moe_dims& d) { return (size_t)d.inter * d.hidden / 8; }

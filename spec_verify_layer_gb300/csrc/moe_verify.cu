@@ -330,15 +330,17 @@ __device__ void issue_router_rows(const RoundArgs& a, const float* router, float
 }
 
 // Lane l accumulates elements 128c + 4l + j for c ascending, then the xor-butterfly.
-// Warp q of the CTA computes its staged row q for every activation row.
+// The warps share out the (staged router row, activation row) pairs.
 __device__ void router_phase(const RoundArgs& a, const uint16_t* x, const float* s_rw) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int NC = a.H >> 7;  // <= 16
   const int n = router_rows_of_cta(a.E);
-  for (int q = warp; q < n; q += NW) {
+  // (router row, activation row) pairs over the warps
+  for (int pq = warp; pq < n * a.R; pq += NW) {
+    const int q = pq / a.R, r = pq - q * a.R;
     const int e = blockIdx.x + gridDim.x * q;
     const float4* wr = reinterpret_cast<const float4*>(s_rw + (size_t)q * a.H) + lane;
-    for (int r = 0; r < a.R; ++r) {
+    {
       const uint2* xr = reinterpret_cast<const uint2*>(x + (size_t)r * a.H) + lane;
       uint2 xv[16];
 #pragma unroll
@@ -373,6 +375,7 @@ struct Tables {
   int* pos_ui;   // [R*k] union index of the expert at each CSR position
   int* pos_row;  // [R*k] row at each CSR position
   int* slot;     // [E] bank slot of each expert this layer
+  int* pick_pos; // [R*k] CSR position of pick (r, j), or -1 if tail-skipped
 };
 
 // True if (ka, ia) ranks before (kb, ib): larger key, then lower id.
@@ -527,8 +530,10 @@ __device__ int route_phase(const RoundArgs& a, const Tables& T, unsigned* s_mask
   __syncthreads();
   for (int p = tid; p < R * k; p += NT) {
     const int e = s_ids[p], r = p / k;
+    T.pick_pos[p] = -1;
     if (s_mask[e] == 0u) continue;  // (tail-skipped)
     const int pos = s_off_e[e] + __popc(s_mask[e] & ((1u << r) - 1u));
+    T.pick_pos[p] = pos;
     T.pair[pos] = p;
     T.pos_row[pos] = r;
     T.pos_ui[pos] = s_ui[e];
@@ -571,8 +576,8 @@ struct GuChunk {
 // smem plan: GU ring | DN slots | x pairs | tables | out accumulators | wave outputs |
 // chunk list | barriers
 struct SmemPlan {
-  size_t gu_slot, gu, dn_slot, dn, xrows, uni, csr, pair, w, pos_ui, pos_row, slot, nunion, acc, ybuf, chunks,
-      bars, total;
+  size_t gu_slot, gu, dn_slot, dn, xrows, uni, csr, pair, w, pos_ui, pos_row, slot, pick, nunion, acc, ybuf,
+      chunks, bars, total;
   size_t ring;    // bytes of the gate/up ring (>= kGuSlots * gu_slot)
   size_t h_slot;  // bytes per h slot (two slots from gu + kHOffset)
   int gu_cap;     // units per gate/up chunk
@@ -589,7 +594,7 @@ __host__ __device__ inline SmemPlan smem_plan(int H, int I, int E, int R, int k,
   p.max_orows = (H + grid - 1) / grid;
   p.dn_slot = up128((size_t)p.max_orows * (I / 2)) + up128((size_t)p.max_orows * (I / 16));
   const size_t tables = up128((size_t)E * 4) + up128((size_t)(E + 1) * 4) +
-                        4 * up128((size_t)R * k * 4) + up128((size_t)E * 4) + 128 +
+                        5 * up128((size_t)R * k * 4) + up128((size_t)E * 4) + 128 +
                         up128((size_t)R * kAccStride * 4) +
                         up128((size_t)NW * kAccStride * 4) + up128(kMaxChunks * 12 + 16) + 256;
   const size_t fixed = tables + kDnSlots * p.dn_slot + kXBytes;
@@ -613,6 +618,7 @@ __host__ __device__ inline SmemPlan smem_plan(int H, int I, int E, int R, int k,
   p.pos_ui = off;  off += up128((size_t)R * k * 4);
   p.pos_row = off; off += up128((size_t)R * k * 4);
   p.slot = off;    off += up128((size_t)E * 4);
+  p.pick = off;    off += up128((size_t)R * k * 4);
   p.nunion = off;  off += 128;
   p.acc = off;     off += up128((size_t)R * kAccStride * 4);
   p.ybuf = off;    off += up128((size_t)NW * kAccStride * 4);
@@ -811,6 +817,7 @@ __device__ __forceinline__ void gateup_unit(const RoundArgs& a, const Tables& T,
   float v[V];
 #pragma unroll
   for (int i = 0; i < V; ++i) v[i] = 0.f;
+  const int sw = (c.i0 + t) & 7;
 #pragma unroll
   for (int tb = 0; tb < NBL; ++tb) {
     const int blk = lane + 32 * tb;
@@ -824,7 +831,9 @@ __device__ __forceinline__ void gateup_unit(const RoundArgs& a, const Tables& T,
       for (int g = 0; g < G; ++g) xps[g] = xp[g];
 #pragma unroll
       for (int wrow = 0; wrow < 2; ++wrow) {
-        const size_t w = (size_t)(t * 2 + wrow) * NB + blk;
+        // unit t of the chunk is intermediate row i0 + t of the expert: its blocks sit at
+        // blk ^ ((i0 + t) & 7), gate and up alike
+        const size_t w = (size_t)(t * 2 + wrow) * NB + (blk ^ sw);
         const uint4 nb = *reinterpret_cast<const uint4*>(codes + w * 16);
         const float sc = half_bits(scales[w]);
         float dot[G];
@@ -874,7 +883,7 @@ __device__ __forceinline__ void gateup_chunk(const RoundArgs& a, const Tables& T
 // (pair layout, shared memory) against each output row's down codes of its expert;
 // y[ol] to s_yw.  Lanes >= I/32 hold no block.
 __device__ __forceinline__ void down_position(const RoundArgs& a, const uint8_t* dslot, size_t codes_room,
-                                              int ob0, int ob1, const float4* s_h, float* s_yw) {
+                                              int o0, int ob0, int ob1, const float4* s_h, float* s_yw) {
   const int NBI = a.I >> 5;
   const int lane = threadIdx.x & 31;
   f2_t hp[16];
@@ -910,8 +919,9 @@ __device__ __forceinline__ void down_position(const RoundArgs& a, const uint8_t*
       part[jj] = 0.f;
       const int ol = ob + jj;
       if (lane < NBI && ol < ob1) {
-        const uint4 nb = *reinterpret_cast<const uint4*>(codes + ((size_t)ol * NBI + lane) * 16);
-        const float sc = half_bits(scales[ol * NBI + lane]);
+        const int pos = block_pos(lane, o0 + ol);
+        const uint4 nb = *reinterpret_cast<const uint4*>(codes + ((size_t)ol * NBI + pos) * 16);
+        const float sc = half_bits(scales[ol * NBI + pos]);
         float dot[1];
         block_dot<1>(nb, hps, dot);
         part[jj] = __fmul_rn(sc, __fmaf_rn(dot[0], 0x1p62f, hsum8));
@@ -935,8 +945,8 @@ __device__ __forceinline__ void down_position(const RoundArgs& a, const uint8_t*
 //   step 1: k (2t, 2t+1) <- (8t+2, 8t+6),          k (2t+8, 2t+9) <- (8t+3, 8t+7)
 // The B fragments (activations, or the exchanged h' split into bf16 hi + lo) follow the
 // same permutation.  A block's MMAs give D = sum (128 + n) b; the layer needs
-// sum (n - 8) b = D - 136 sum b, times the row's block scale: the bias is one fp32
-// constant per (column, block), computed once.  Every tile's K range is split in the
+// sum (n - 8) b = D - 136 sum b, times the row's block scale: the bias term of a
+// (column, block) is summed from the B fragments the lanes already hold.  Every tile's K range is split in the
 // same kKParts parts whatever the other rows are, and the parts are added in a fixed
 // order, so a row's result does not depend on the rows it shares the round with.
 
@@ -944,11 +954,11 @@ constexpr int kMmaRows = 8;
 constexpr int kKParts = 4;
 constexpr int kTilesPerRound = NW / kKParts;  // tiles in flight (one warp per tile part)
 // scratch of the tensor-core path inside the activation-pair region (unused then)
-constexpr size_t kMmaCorrX = 0;          // [R][H/32] fp32: 136 x block sums of the rows
-constexpr size_t kMmaPart = 8192;        // [NW][16][8] fp32 partial tiles
-constexpr size_t kMmaCorrH = 16384;      // [wave][I/32] fp32: 136 x block sums of h'
-constexpr size_t kMmaTiles = 22528;      // [64][3] int: down tiles of a wave
-constexpr int kMmaMaxTiles = 64;
+constexpr int kMmaMaxPos = 256;          // CSR positions (rows x top-k) of a wide round
+constexpr int kMmaMaxTiles = kMmaMaxPos;
+constexpr size_t kMmaPart = 0;           // [NW][16][8] fp32 partial tiles
+constexpr size_t kMmaY = 8192;           // [kMmaMaxPos][16] fp32: y per position and output row
+constexpr size_t kMmaTiles = kMmaY + (size_t)kMmaMaxPos * 16 * 4;  // [kMmaMaxTiles][3] int + count
 
 __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
@@ -977,27 +987,13 @@ __device__ __forceinline__ void bfrag_x(uint4 v, uint32_t (&b)[4]) {
   b[3] = __byte_perm(v.y, v.w, 0x7632);
 }
 
-__device__ __forceinline__ float bf16_bits_f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
-
-// 136 x the block sums of this layer's rows (fixed order), for the gate/up bias term.
-__device__ void mma_corr_x(const RoundArgs& a, const uint16_t* x, float* s_cx) {
-  const int NB = a.H >> 5;
-  for (int idx = threadIdx.x; idx < a.R * NB; idx += NT) {
-    const int r = idx / NB, b = idx - r * NB;
-    const uint16_t* src = x + (size_t)r * a.H + 32 * b;
-    float s = 0.f;
-#pragma unroll 8
-    for (int j = 0; j < 32; ++j) s = __fadd_rn(s, bf16_bits_f(__ldg(src + j)));
-    s_cx[idx] = __fmul_rn(136.f, s);
-  }
-}
 
 // Gate/up of one staged chunk on the tensor cores: tiles of 16 weight rows (8 units,
 // gate and up interleaved) x 8 of the expert's rows, one warp per (tile, K part); the
 // parts are added in order, then h' = w silu(g) v is stored split into bf16 hi + lo in
 // the down pass's fragment order.
 __device__ void gateup_chunk_mma(const RoundArgs& a, const Tables& T, const uint8_t* slot, const GuChunk& c,
-                                 const uint16_t* x, const float* s_cx, float* s_part) {
+                                 const uint16_t* x, float* s_part) {
   const int H = a.H, NB = H >> 5, NBI = a.I >> 5;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const int p0 = T.csr_off[c.ui], Re = T.csr_off[c.ui + 1] - p0;
@@ -1014,14 +1010,13 @@ __device__ void gateup_chunk_mma(const RoundArgs& a, const Tables& T, const uint
       const bool va = ra < 2 * c.n, vb = rb < 2 * c.n;
       // columns past the expert's rows repeat its last row; their results are dropped
       const int xr = T.pos_row[p0 + min(nt * 8 + g, Re - 1)];
-      const int r0 = T.pos_row[p0 + min(nt * 8 + 2 * t, Re - 1)];
-      const int r1 = T.pos_row[p0 + min(nt * 8 + 2 * t + 1, Re - 1)];
       const uint4* xrow = reinterpret_cast<const uint4*>(x + (size_t)xr * H) + t;
       const int b0 = (kp * NB) / kKParts, b1 = ((kp + 1) * NB) / kKParts;
 #pragma unroll 4
       for (int b = b0; b < b1; ++b) {
-        const uint32_t wa = va ? *reinterpret_cast<const uint32_t*>(codes + ((size_t)ra * NB + b) * 16 + 4 * t) : 0u;
-        const uint32_t wb = vb ? *reinterpret_cast<const uint32_t*>(codes + ((size_t)rb * NB + b) * 16 + 4 * t) : 0u;
+        const int pa_ = block_pos(b, c.i0 + (ra >> 1)), pb_ = block_pos(b, c.i0 + (rb >> 1));
+        const uint32_t wa = va ? *reinterpret_cast<const uint32_t*>(codes + ((size_t)ra * NB + pa_) * 16 + 4 * t) : 0u;
+        const uint32_t wb = vb ? *reinterpret_cast<const uint32_t*>(codes + ((size_t)rb * NB + pb_) * 16 + 4 * t) : 0u;
         const uint4 xv = __ldg(xrow + 4 * b);
         uint32_t pa[4], pb[4], bf[4];
         dq_word(wa, pa);
@@ -1030,9 +1025,23 @@ __device__ void gateup_chunk_mma(const RoundArgs& a, const Tables& T, const uint
         float d[4] = {0.f, 0.f, 0.f, 0.f};
         mma_bf16(d, pa[0], pb[0], pa[1], pb[1], bf[0], bf[1]);
         mma_bf16(d, pa[2], pb[2], pa[3], pb[3], bf[2], bf[3]);
-        const float sa = va ? half_bits(scales[(size_t)ra * NB + b]) : 0.f;
-        const float sb = vb ? half_bits(scales[(size_t)rb * NB + b]) : 0.f;
-        const float k0 = s_cx[r0 * NB + b], k1 = s_cx[r1 * NB + b];
+        const float sa = va ? half_bits(scales[(size_t)ra * NB + pa_]) : 0.f;
+        const float sb = vb ? half_bits(scales[(size_t)rb * NB + pb_]) : 0.f;
+        // bias: 136 x the block sum of the activation row of each D column, from the B
+        // fragments (8 elements per lane in order, then the lanes of the column group)
+        float cs = 0.f;
+        {
+          const uint32_t w4[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            cs = __fadd_rn(cs, bf16_lo(w4[q]));
+            cs = __fadd_rn(cs, bf16_hi(w4[q]));
+          }
+          cs = __fadd_rn(cs, __shfl_xor_sync(0xffffffffu, cs, 1));
+          cs = __fadd_rn(cs, __shfl_xor_sync(0xffffffffu, cs, 2));
+        }
+        const float k0 = __fmul_rn(136.f, __shfl_sync(0xffffffffu, cs, 8 * t));
+        const float k1 = __fmul_rn(136.f, __shfl_sync(0xffffffffu, cs, 8 * t + 4));
         acc[0] = __fmaf_rn(sa, __fsub_rn(d[0], k0), acc[0]);
         acc[1] = __fmaf_rn(sa, __fsub_rn(d[1], k1), acc[1]);
         acc[2] = __fmaf_rn(sb, __fsub_rn(d[2], k0), acc[2]);
@@ -1073,97 +1082,79 @@ __device__ void gateup_chunk_mma(const RoundArgs& a, const Tables& T, const uint
   }
 }
 
-// Down pass of one wave on the tensor cores.  The wave's CSR positions [pa, pb) (h'
-// rows in shared memory at hs, hi + lo bf16 in fragment order) are cut into tiles of
-// up to 8 consecutive positions of one expert; each tile x each 16 of this CTA's output
-// rows, K = I split in kKParts parts, one warp per part; hi and lo as two MMAs per k16
-// step.  y[position][output row] goes to s_y.
-__device__ void down_wave_mma(const RoundArgs& a, const Tables& T, const uint8_t* dn, size_t dn_slot,
-                              size_t codes_room, int no, int pa, int pb, const uint8_t* hs, float* s_ch,
-                              float* s_part, int* s_tiles, float* s_y) {
+// One round of the wide down pass on the tensor cores: up to kTilesPerRound tiles (up
+// to 8 consecutive CSR positions of one expert x this CTA's output rows, at most 16),
+// K = I split in kKParts parts, one warp per part; B = h' (hi + lo bf16, fragment order)
+// read from the workspace through L2, two MMAs per k16 step; the bias term of each
+// (position, block) summed from the fragments.  y[position][output row] -> s_yall.
+__device__ void down_round_mma(const RoundArgs& a, const uint8_t* dn, size_t dn_slot, size_t codes_room, int o0,
+                               int no, const int* s_tiles, int cb0, int n_tiles, float* s_part, float* s_yall) {
   const int NBI = a.I >> 5;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-  // 136 x the block sums of the wave's h' (hi + lo), fixed order
-  for (int idx = threadIdx.x; idx < (pb - pa) * NBI; idx += NT) {
-    const uint16_t* v = reinterpret_cast<const uint16_t*>(hs + (size_t)idx * 128);
-    float s = 0.f;
-#pragma unroll 8
-    for (int q = 0; q < 64; ++q) s = __fadd_rn(s, bf16_bits_f(v[q]));
-    s_ch[idx] = __fmul_rn(136.f, s);
-  }
-  if (threadIdx.x == 0) {
-    int n = 0;
-    for (int p = pa; p < pb && n < kMmaMaxTiles;) {
-      const int ui = T.pos_ui[p];
-      int q = p;
-      while (q < pb && q - p < 8 && T.pos_ui[q] == ui) ++q;
-      s_tiles[3 * n] = p - pa;
-      s_tiles[3 * n + 1] = q - p;
-      s_tiles[3 * n + 2] = ui;
-      ++n;
-      p = q;
+  const uint8_t* hb = reinterpret_cast<const uint8_t*>(a.hbuf);
+  const int ti = cb0 + warp / kKParts, kp = warp % kKParts;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  if (ti < n_tiles) {
+    const int p0 = s_tiles[3 * ti], cnt = s_tiles[3 * ti + 1], ui = s_tiles[3 * ti + 2];
+    const uint8_t* codes = dn + (size_t)(ui % kDnSlots) * dn_slot;
+    const uint16_t* scales = reinterpret_cast<const uint16_t*>(codes + codes_room);
+    const int ra = g, rb = g + 8;  // output rows of this CTA
+    const bool va = ra < no, vb = rb < no;
+    // columns past the tile's positions repeat its last one; their results are dropped
+    const int pg = p0 + min(g, cnt - 1);
+    const int b0 = (kp * NBI) / kKParts, b1 = ((kp + 1) * NBI) / kKParts;
+#pragma unroll 3
+    for (int b = b0; b < b1; ++b) {
+      const int pa_ = block_pos(b, o0 + ra), pb_ = block_pos(b, o0 + rb);
+      const uint32_t wa = va ? *reinterpret_cast<const uint32_t*>(codes + ((size_t)ra * NBI + pa_) * 16 + 4 * t) : 0u;
+      const uint32_t wb = vb ? *reinterpret_cast<const uint32_t*>(codes + ((size_t)rb * NBI + pb_) * 16 + 4 * t) : 0u;
+      const uint4* hv = reinterpret_cast<const uint4*>(hb + (((size_t)pg * NBI + b) * 4 + t) * 32);
+      const uint4 hi = __ldcg(hv), lo = __ldcg(hv + 1);
+      uint32_t pa4[4], pb4[4];
+      dq_word(wa, pa4);
+      dq_word(wb, pb4);
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      mma_bf16(d, pa4[0], pb4[0], pa4[1], pb4[1], hi.x, hi.y);
+      mma_bf16(d, pa4[0], pb4[0], pa4[1], pb4[1], lo.x, lo.y);
+      mma_bf16(d, pa4[2], pb4[2], pa4[3], pb4[3], hi.z, hi.w);
+      mma_bf16(d, pa4[2], pb4[2], pa4[3], pb4[3], lo.z, lo.w);
+      const float sa = va ? half_bits(scales[(size_t)ra * NBI + pa_]) : 0.f;
+      const float sb = vb ? half_bits(scales[(size_t)rb * NBI + pb_]) : 0.f;
+      float cs = 0.f;
+      {
+        const uint32_t w8[8] = {hi.x, hi.y, hi.z, hi.w, lo.x, lo.y, lo.z, lo.w};
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          cs = __fadd_rn(cs, bf16_lo(w8[q]));
+          cs = __fadd_rn(cs, bf16_hi(w8[q]));
+        }
+        cs = __fadd_rn(cs, __shfl_xor_sync(0xffffffffu, cs, 1));
+        cs = __fadd_rn(cs, __shfl_xor_sync(0xffffffffu, cs, 2));
+      }
+      const float k0 = __fmul_rn(136.f, __shfl_sync(0xffffffffu, cs, 8 * t));
+      const float k1 = __fmul_rn(136.f, __shfl_sync(0xffffffffu, cs, 8 * t + 4));
+      acc[0] = __fmaf_rn(sa, __fsub_rn(d[0], k0), acc[0]);
+      acc[1] = __fmaf_rn(sa, __fsub_rn(d[1], k1), acc[1]);
+      acc[2] = __fmaf_rn(sb, __fsub_rn(d[2], k0), acc[2]);
+      acc[3] = __fmaf_rn(sb, __fsub_rn(d[3], k1), acc[3]);
     }
-    s_tiles[3 * kMmaMaxTiles] = n;
+  }
+  float* part = s_part + warp * 128;
+  part[g * 8 + 2 * t] = acc[0];
+  part[g * 8 + 2 * t + 1] = acc[1];
+  part[(g + 8) * 8 + 2 * t] = acc[2];
+  part[(g + 8) * 8 + 2 * t + 1] = acc[3];
+  __syncthreads();
+  for (int i = threadIdx.x; i < kTilesPerRound * 128; i += NT) {
+    const int cl = i >> 7, r = (i >> 3) & 15, cc = i & 7;
+    const int tj = cb0 + cl;
+    if (tj >= n_tiles || r >= no || cc >= s_tiles[3 * tj + 1]) continue;
+    float y = 0.f;
+#pragma unroll
+    for (int kp2 = 0; kp2 < kKParts; ++kp2) y = __fadd_rn(y, s_part[(cl * kKParts + kp2) * 128 + r * 8 + cc]);
+    s_yall[(s_tiles[3 * tj] + cc) * 16 + r] = y;
   }
   __syncthreads();
-  const int NTMo = (no + 15) >> 4;
-  const int combos = s_tiles[3 * kMmaMaxTiles] * NTMo;
-  for (int cb0 = 0; cb0 < combos; cb0 += kTilesPerRound) {
-    const int cb = cb0 + warp / kKParts, kp = warp % kKParts;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    if (cb < combos) {
-      const int ti = cb / NTMo, mt = cb - ti * NTMo;
-      const int q0 = s_tiles[3 * ti], cnt = s_tiles[3 * ti + 1], ui = s_tiles[3 * ti + 2];
-      const uint8_t* codes = dn + (size_t)(ui % kDnSlots) * dn_slot;
-      const uint16_t* scales = reinterpret_cast<const uint16_t*>(codes + codes_room);
-      const int ra = mt * 16 + g, rb = ra + 8;  // output rows of this CTA
-      const bool va = ra < no, vb = rb < no;
-      const int qg = q0 + min(g, cnt - 1);
-      const int qc0 = q0 + min(2 * t, cnt - 1), qc1 = q0 + min(2 * t + 1, cnt - 1);
-      const int b0 = (kp * NBI) / kKParts, b1 = ((kp + 1) * NBI) / kKParts;
-#pragma unroll 2
-      for (int b = b0; b < b1; ++b) {
-        const uint32_t wa = va ? *reinterpret_cast<const uint32_t*>(codes + ((size_t)ra * NBI + b) * 16 + 4 * t) : 0u;
-        const uint32_t wb = vb ? *reinterpret_cast<const uint32_t*>(codes + ((size_t)rb * NBI + b) * 16 + 4 * t) : 0u;
-        const uint4* hv = reinterpret_cast<const uint4*>(hs + ((size_t)qg * NBI + b) * 128 + 32 * t);
-        const uint4 hi = hv[0], lo = hv[1];
-        uint32_t pa4[4], pb4[4];
-        dq_word(wa, pa4);
-        dq_word(wb, pb4);
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_bf16(d, pa4[0], pb4[0], pa4[1], pb4[1], hi.x, hi.y);
-        mma_bf16(d, pa4[0], pb4[0], pa4[1], pb4[1], lo.x, lo.y);
-        mma_bf16(d, pa4[2], pb4[2], pa4[3], pb4[3], hi.z, hi.w);
-        mma_bf16(d, pa4[2], pb4[2], pa4[3], pb4[3], lo.z, lo.w);
-        const float sa = va ? half_bits(scales[(size_t)ra * NBI + b]) : 0.f;
-        const float sb = vb ? half_bits(scales[(size_t)rb * NBI + b]) : 0.f;
-        const float k0 = s_ch[qc0 * NBI + b], k1 = s_ch[qc1 * NBI + b];
-        acc[0] = __fmaf_rn(sa, __fsub_rn(d[0], k0), acc[0]);
-        acc[1] = __fmaf_rn(sa, __fsub_rn(d[1], k1), acc[1]);
-        acc[2] = __fmaf_rn(sb, __fsub_rn(d[2], k0), acc[2]);
-        acc[3] = __fmaf_rn(sb, __fsub_rn(d[3], k1), acc[3]);
-      }
-    }
-    float* part = s_part + warp * 128;
-    part[g * 8 + 2 * t] = acc[0];
-    part[g * 8 + 2 * t + 1] = acc[1];
-    part[(g + 8) * 8 + 2 * t] = acc[2];
-    part[(g + 8) * 8 + 2 * t + 1] = acc[3];
-    __syncthreads();
-    for (int i = threadIdx.x; i < kTilesPerRound * 128; i += NT) {
-      const int cl = i >> 7, r = (i >> 3) & 15, cc = i & 7;
-      const int cb = cb0 + cl;
-      if (cb >= combos) continue;
-      const int ti = cb / NTMo, mt = cb - ti * NTMo;
-      const int ol = mt * 16 + r;
-      if (ol >= no || cc >= s_tiles[3 * ti + 1]) continue;
-      float y = 0.f;
-#pragma unroll
-      for (int kp = 0; kp < kKParts; ++kp) y = __fadd_rn(y, s_part[(cl * kKParts + kp) * 128 + r * 8 + cc]);
-      s_y[(s_tiles[3 * ti] + cc) * kAccStride + ol] = y;
-    }
-    __syncthreads();
-  }
 }
 
 // Exchanged h rows of CSR positions [pa, pb) (contiguous in the workspace) -> slot.
@@ -1210,11 +1201,12 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
   uint8_t* dn = smem + P.dn;
   float4* s_xp = reinterpret_cast<float4*>(smem + P.xrows);
   float* s_xs = reinterpret_cast<float*>(smem + P.xrows + (size_t)a.R * a.H * 4);
-  const bool mma = a.R >= kMmaRows;  // wide rounds: tensor-core gate/up and down
+  // wide rounds: tensor-core gate/up and down (positions and output rows within the
+  // shared-memory scratch of that path)
+  const bool mma = a.R >= kMmaRows && a.R * a.k <= kMmaMaxPos && P.max_orows <= 16;
   const bool x_staged = !mma && (size_t)a.R * a.H * 4 + (size_t)a.R * (a.H >> 5) * 4 <= kXBytes;
-  float* s_cx = reinterpret_cast<float*>(smem + P.xrows + kMmaCorrX);
   float* s_mpart = reinterpret_cast<float*>(smem + P.xrows + kMmaPart);
-  float* s_ch = reinterpret_cast<float*>(smem + P.xrows + kMmaCorrH);
+  float* s_yall = reinterpret_cast<float*>(smem + P.xrows + kMmaY);
   int* s_tiles = reinterpret_cast<int*>(smem + P.xrows + kMmaTiles);
   float* s_rw = reinterpret_cast<float*>(gu);
   float* s_acc = reinterpret_cast<float*>(smem + P.acc);
@@ -1223,7 +1215,8 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
   Tables T{reinterpret_cast<int*>(smem + P.uni),     reinterpret_cast<int*>(smem + P.csr),
            reinterpret_cast<int*>(smem + P.pair),    reinterpret_cast<float*>(smem + P.w),
            reinterpret_cast<int*>(smem + P.nunion),  reinterpret_cast<int*>(smem + P.pos_ui),
-           reinterpret_cast<int*>(smem + P.pos_row), reinterpret_cast<int*>(smem + P.slot)};
+           reinterpret_cast<int*>(smem + P.pos_row), reinterpret_cast<int*>(smem + P.slot),
+           reinterpret_cast<int*>(smem + P.pick)};
   // routing scratch lives in the (then idle) gate/up ring
   unsigned* s_mask = reinterpret_cast<unsigned*>(gu);
   int* s_off_e = reinterpret_cast<int*>(gu + (size_t)a.E * 4);
@@ -1297,7 +1290,6 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
       T.slot[e] = sl;
     }
     if (x_staged && !a.route_only) stage_xpairs(a, x, s_xp, s_xs);
-    if (mma && !a.route_only) mma_corr_x(a, x, s_cx);
     if (!grid_wait(a, sy)) {
       bail();
       return;
@@ -1365,7 +1357,7 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
       const GuChunk c = s_chunks[n];
       const uint8_t* slot = gu + q * P.gu_slot;
       if (mma)
-        gateup_chunk_mma(a, T, slot, c, x, s_cx, s_mpart);
+        gateup_chunk_mma(a, T, slot, c, x, s_mpart);
       else if (x_staged)
         gateup_chunk<NBL, true>(a, T, slot, c, x, s_xp, s_xs);
       else
@@ -1392,10 +1384,78 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
       return;
     }
     stamp(a, l, 7);
-    // ---- down: waves of WV consecutive CSR positions, one warp per position ----
-    for (int i = tid; i < a.R * kAccStride; i += NT) s_acc[i] = 0.f;
-    __syncthreads();
-    if (no > 0) {
+    if (mma && no > 0) {
+      // ---- wide down: tiles of one expert's positions on the tensor cores ----
+      const int total = T.csr_off[U];
+      if (tid == 0) {
+        int n = 0;
+        for (int p = 0; p < total && n < kMmaMaxTiles;) {
+          const int ui = T.pos_ui[p];
+          int q = p;
+          while (q < total && q - p < 8 && T.pos_ui[q] == ui) ++q;
+          s_tiles[3 * n] = p;
+          s_tiles[3 * n + 1] = q - p;
+          s_tiles[3 * n + 2] = ui;
+          ++n;
+          p = q;
+        }
+        s_tiles[3 * kMmaMaxTiles] = n;
+      }
+      __syncthreads();
+      stamp(a, l, 8);
+      const int n_tiles = s_tiles[3 * kMmaMaxTiles];
+      int waited = 0, rel = 0;
+      for (int cb0 = 0; cb0 < n_tiles; cb0 += kTilesPerRound) {
+        const int cb1 = min(cb0 + kTilesPerRound, n_tiles);
+        // the round's experts must have landed: one waiting thread per slot
+        const int need = s_tiles[3 * (cb1 - 1) + 2] + 1;
+        if (need > waited) {
+          bool ok = true;
+          if (tid < need - waited) {
+            const int qd = (waited + tid) % kDnSlots;
+            ok = mbar_wait_bounded(smem_u32(bars + bar_dn0 + qd), (dn_ph >> qd) & 1u, a.status, a.wait_cycles);
+          }
+          if (__syncthreads_or(!ok)) {
+            bail();
+            return;
+          }
+          for (int u = waited; u < need; ++u) {
+            const int qd = u % kDnSlots;
+            dn_ph ^= 1u << qd;
+            dn_pend &= ~(1u << qd);
+          }
+          waited = need;
+        }
+        stamp(a, l, 9);  // (the last round's stamp stays)
+        down_round_mma(a, dn, P.dn_slot, codes_room, o0, no, s_tiles, cb0, n_tiles, s_mpart, s_yall);
+        // experts whose tiles are all done hand their slots to later experts
+        const int rel_new = (cb1 < n_tiles) ? s_tiles[3 * cb1 + 2] : U;
+        if (tid < rel_new - rel && rel + tid + kDnSlots < U) {
+          const int e = rel + tid, qd = e % kDnSlots;
+          issue_dn_chunk(a, W, T, dn + (size_t)qd * P.dn_slot, smem_u32(bars + bar_dn0 + qd), e + kDnSlots, o0, no,
+                         codes_room);
+        }
+        for (int e = rel; e < rel_new; ++e)
+          if (e + kDnSlots < U) dn_pend |= 1u << (e % kDnSlots);
+        rel = rel_new;
+      }
+      if (n_tiles == 0) stamp(a, l, 9);
+      stamp(a, l, 10);
+      // each row's picks in rank order
+      float* out = a.out + (size_t)l * RH;
+      for (int i = tid; i < a.R * no; i += NT) {
+        const int r = i / no, ol = i - r * no;
+        float acc = 0.f;
+        for (int j = 0; j < a.k; ++j) {
+          const int pp = T.pick_pos[r * a.k + j];
+          if (pp >= 0) acc = __fadd_rn(acc, s_yall[pp * 16 + ol]);
+        }
+        out[(size_t)r * a.H + o0 + ol] = acc;
+      }
+    } else if (no > 0) {
+      // ---- down: waves of WV consecutive CSR positions, one warp per position ----
+      for (int i = tid; i < a.R * kAccStride; i += NT) s_acc[i] = 0.f;
+      __syncthreads();
       const int total = T.csr_off[U];
       for (int q = 0; q < 2 && q * WV < total; ++q) {
         h_pend |= 1u << q;
@@ -1428,16 +1488,14 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
           waited = need;
         }
         stamp(a, l, 9);  // (the last wave's stamp stays)
-        if (mma) {
-          down_wave_mma(a, T, dn, P.dn_slot, codes_room, no, pa, pb, hslot(qh), s_ch, s_mpart, s_tiles, s_y);
-        } else {
+        {
           // positions of the wave over the warps; spare warps split a position's rows
           const int npos = pb - pa, wpp = NW / npos;
           const int pi = warp / wpp, part = warp - pi * wpp;
           if (pi < npos) {
             const int pp = pa + pi;
             const int ui = T.pos_ui[pp];
-            down_position(a, dn + (size_t)(ui % kDnSlots) * P.dn_slot, codes_room, (part * no) / wpp,
+            down_position(a, dn + (size_t)(ui % kDnSlots) * P.dn_slot, codes_room, o0, (part * no) / wpp,
                           ((part + 1) * no) / wpp,
                           reinterpret_cast<const float4*>(hslot(qh) + (size_t)pi * a.I * 4),
                           s_y + pi * kAccStride);

@@ -106,19 +106,33 @@ def _decode_blocks(by):
     return np.stack([lo, hi], axis=-1)
 
 
+def _unswizzle(arr, rows, nb):
+    # logical block b of a row with key k is stored at position b ^ (k & 7)
+    pos = np.arange(nb)[None, :] ^ (np.asarray(rows)[:, None] & 7)
+    return np.take_along_axis(arr, pos.reshape(pos.shape + (1,) * (arr.ndim - 2)), axis=1)
+
+
 def _decode_gateup(nib, sc, E, H, I):
-    # codes [E][I][2: gate, up][H/32][16 B], scales [E][I][2][H/32]
+    # codes [E][I][2: gate, up][H/32][16 B], scales [E][I][2][H/32]; key of row (i, m) = i
     NB = H // 32
-    codes = _decode_blocks(nib.reshape(E, I, 2, NB, 16)).reshape(E, I, 2, H)
-    s = sc.reshape(E, I, 2, NB)
+    rows = np.arange(2 * I) // 2
+    by = nib.reshape(E, 2 * I, NB, 16)
+    s = sc.reshape(E, 2 * I, NB)
+    by = np.stack([_unswizzle(by[e], rows, NB) for e in range(E)])
+    s = np.stack([_unswizzle(s[e], rows, NB) for e in range(E)])
+    codes = _decode_blocks(by).reshape(E, I, 2, H)
+    s = s.reshape(E, I, 2, NB)
     return codes[:, :, 0], codes[:, :, 1], s[:, :, 0], s[:, :, 1]
 
 
 def _decode_down(nib, sc, E, H, I):
-    # codes [E][H][I/32][16 B], scales [E][H][I/32]
+    # codes [E][H][I/32][16 B], scales [E][H][I/32]; row r = o
     NBI = I // 32
-    codes = _decode_blocks(nib.reshape(E, H, NBI, 16)).reshape(E, H, I)
-    return codes, sc.reshape(E, H, NBI)
+    rows = np.arange(H)
+    by = np.stack([_unswizzle(b, rows, NBI) for b in nib.reshape(E, H, NBI, 16)])
+    s = np.stack([_unswizzle(x, rows, NBI) for x in sc.reshape(E, H, NBI)])
+    codes = _decode_blocks(by).reshape(E, H, I)
+    return codes, s
 
 
 @pytest.mark.parametrize("H,I,E", [(256, 256, 1), (512, 256, 3), (2048, 512, 2)])
@@ -154,12 +168,12 @@ def test_packer_one_hot_nibble_order():
     H, I = 256, 256
     d = mv.make_dims(H, 2, 1, I, 1)
     qd = np.zeros((1, H, I), np.int8)
-    qd[0, 5, 35] = 7   # o = 5, i = 35: block 1 of row 5, byte 1, high nibble
+    qd[0, 5, 35] = 7   # o = 5, i = 35: block 1 of row 5 (stored at position 1 ^ 5), byte 1, high nibble
     sd = np.zeros((1, H, I // 32), np.uint16)
     nib = np.zeros(mv.moe_packed_bytes(d, 1, 0), np.uint8)
     sc = np.zeros(mv.moe_packed_bytes(d, 1, 1) // 2, np.uint16)
     mv.moe_pack_q4(d, mv.MOE_DOWN, 1, qd.ctypes.data, sd.ctypes.data, None, None, nib.ctypes.data, sc.ctypes.data)
-    off = (5 * (I // 32) + 1) * 16
+    off = (5 * (I // 32) + (1 ^ 5)) * 16
     blk = nib[off:off + 16]
     assert blk[1] == (8 | (15 << 4))
     assert all(b == 0x88 for i, b in enumerate(blk) if i != 1)
