@@ -95,6 +95,8 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+__device__ __forceinline__ int lane_of(int tid) { return tid & 31; }
+
 __device__ __forceinline__ long long gtimer() {
   long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -955,6 +957,7 @@ constexpr int kKParts = 4;
 constexpr int kTilesPerRound = NW / kKParts;  // tiles in flight (one warp per tile part)
 // scratch of the tensor-core path inside the activation-pair region (unused then)
 constexpr int kMmaMaxPos = 256;          // CSR positions (rows x top-k) of a wide round
+static_assert(kMmaMaxPos <= NT, "one thread per position when the wide down tiles are listed");
 constexpr int kMmaMaxTiles = kMmaMaxPos;
 constexpr size_t kMmaPart = 0;           // [NW][16][8] fp32 partial tiles
 constexpr size_t kMmaY = 8192;           // [kMmaMaxPos][16] fp32: y per position and output row
@@ -1387,21 +1390,35 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
     if (mma && no > 0) {
       // ---- wide down: tiles of one expert's positions on the tensor cores ----
       const int total = T.csr_off[U];
-      if (tid == 0) {
-        int n = 0;
-        for (int p = 0; p < total && n < kMmaMaxTiles;) {
-          const int ui = T.pos_ui[p];
-          int q = p;
-          while (q < total && q - p < 8 && T.pos_ui[q] == ui) ++q;
-          s_tiles[3 * n] = p;
-          s_tiles[3 * n + 1] = q - p;
-          s_tiles[3 * n + 2] = ui;
-          ++n;
-          p = q;
+      {
+        // a tile starts at every 8th position of an expert's run; its index is the
+        // number of tile starts before it (ballot counts per warp, then the warps before)
+        const int p = tid;
+        int ui = 0, off = 0;
+        bool start = false;
+        if (p < total) {
+          ui = T.pos_ui[p];
+          off = p - T.csr_off[ui];
+          start = (off & 7) == 0;
         }
-        s_tiles[3 * kMmaMaxTiles] = n;
+        const unsigned bal = __ballot_sync(0xffffffffu, start);
+        int* s_wcnt = s_tiles + 3 * kMmaMaxTiles + 1;  // [NW] tile starts per warp
+        if (lane_of(tid) == 0) s_wcnt[warp] = __popc(bal);
+        __syncthreads();
+        if (start) {
+          int n = __popc(bal & ((1u << lane_of(tid)) - 1u));
+          for (int w2 = 0; w2 < warp; ++w2) n += s_wcnt[w2];
+          s_tiles[3 * n] = p;
+          s_tiles[3 * n + 1] = min(8, T.csr_off[ui + 1] - p);
+          s_tiles[3 * n + 2] = ui;
+        }
+        if (tid == 0) {
+          int n = 0;
+          for (int w2 = 0; w2 < NW; ++w2) n += s_wcnt[w2];
+          s_tiles[3 * kMmaMaxTiles] = n;
+        }
+        __syncthreads();
       }
-      __syncthreads();
       stamp(a, l, 8);
       const int n_tiles = s_tiles[3 * kMmaMaxTiles];
       int waited = 0, rel = 0;
