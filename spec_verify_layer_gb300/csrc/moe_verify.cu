@@ -564,7 +564,6 @@ constexpr int kDnSlots = 11;
 // the layer's rows as operand pairs plus block sums (4 rows at hidden 2048), staged once
 // per layer when they fit
 constexpr size_t kXBytes = 33792;
-constexpr int kMaxChunks = 96;
 // Inside the gate/up ring, idle outside the gate/up stream: the next layer's router rows
 // at offset 0 (consumed before the routing scratch, also at offset 0, is written) and,
 // from kHOffset on, two slots of exchanged h rows for the down pass.
@@ -598,7 +597,7 @@ __host__ __device__ inline SmemPlan smem_plan(int H, int I, int E, int R, int k,
   const size_t tables = up128((size_t)E * 4) + up128((size_t)(E + 1) * 4) +
                         5 * up128((size_t)R * k * 4) + up128((size_t)E * 4) + 128 +
                         up128((size_t)R * kAccStride * 4) +
-                        up128((size_t)NW * kAccStride * 4) + up128(kMaxChunks * 12 + 16) + 256;
+                        up128((size_t)NW * kAccStride * 4) + up128(kGuSlots * 12 + 16) + 256;
   const size_t fixed = tables + kDnSlots * p.dn_slot + kXBytes;
   const size_t limit = (size_t)225 * 1024;
   size_t cap = fixed < limit ? ((limit - fixed) / kGuSlots) / unit : 0;
@@ -624,17 +623,13 @@ __host__ __device__ inline SmemPlan smem_plan(int H, int I, int E, int R, int k,
   p.nunion = off;  off += 128;
   p.acc = off;     off += up128((size_t)R * kAccStride * 4);
   p.ybuf = off;    off += up128((size_t)NW * kAccStride * 4);
-  p.chunks = off;  off += up128(kMaxChunks * 12 + 16);
+  p.chunks = off;  off += up128(kGuSlots * 12 + 16);
   p.bars = off;    off += 256;
   p.total = off;
   const int rows_per_cta = (E + grid - 1) / grid;
-  // chunks per CTA <= units / cap + experts spanned (<= units / I + 1) + 1
-  const long long umax = (E < R * k) ? E : (long long)R * k;
-  const long long units = (umax * I + grid - 1) / grid;
-  const long long chunks = (cap ? (units + (long long)cap - 1) / (long long)cap : 1 << 30) + units / I + 2;
   p.h_slot = p.ring > kHOffset ? ((p.ring - kHOffset) / 2) & ~(size_t)127 : 0;
   p.h_rows = (int)(p.h_slot / ((size_t)I * 4));
-  p.router_fits = cap >= 1 && p.max_orows <= kAccStride && chunks <= kMaxChunks && p.h_rows >= 1 &&
+  p.router_fits = cap >= 1 && p.max_orows <= kAccStride && p.h_rows >= 1 &&
                   (size_t)rows_per_cta * H * 4 <= kHOffset;
   return p;
 }
@@ -1190,7 +1185,9 @@ __device__ __noinline__ void drain_and_abort(const RoundArgs& a, const uint64_t*
   if (threadIdx.x == 0) atomicExch(a.bar + 33, 1u);
 }
 
-template <int NBL>
+// NBL: 32-element blocks per lane along H (1 up to H 1024, 2 above).  WIDE: the round
+// has enough rows for the tensor-core gate/up and down (wide_round() on the host).
+template <int NBL, bool WIDE>
 __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundArgs a) {
   extern __shared__ __align__(1024) unsigned char smem[];
   const int tid = threadIdx.x, warp = tid >> 5;
@@ -1204,9 +1201,7 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
   uint8_t* dn = smem + P.dn;
   float4* s_xp = reinterpret_cast<float4*>(smem + P.xrows);
   float* s_xs = reinterpret_cast<float*>(smem + P.xrows + (size_t)a.R * a.H * 4);
-  // wide rounds: tensor-core gate/up and down (positions and output rows within the
-  // shared-memory scratch of that path)
-  const bool mma = a.R >= kMmaRows && a.R * a.k <= kMmaMaxPos && P.max_orows <= 16;
+  constexpr bool mma = WIDE;  // tensor-core gate/up and down
   const bool x_staged = !mma && (size_t)a.R * a.H * 4 + (size_t)a.R * (a.H >> 5) * 4 <= kXBytes;
   float* s_mpart = reinterpret_cast<float*>(smem + P.xrows + kMmaPart);
   float* s_yall = reinterpret_cast<float*>(smem + P.xrows + kMmaY);
@@ -1301,34 +1296,103 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
     const int U = route_phase(a, T, s_mask, s_off_e, s_ids, s_ui, s_rank, l);
     stamp(a, l, 3);
     if (a.route_only) return;
-    // ---- plan this CTA's gate/up chunks; issue them and the down prefetch ----
-    if (tid == 0) {
-      // U * I * grid < 2^31 (U <= 512, I <= 4096, grid <= 1024), so 32-bit math is exact
+    // ---- this CTA's share of the gate/up units; chunks issued through the ring ----
+    // Units are shared out by work, not by count: a unit of an expert with R_e rows costs
+    // about ceil(R_e / 2) passes on the fp32 path (rows go two at a time) and
+    // ceil(R_e / 16) on the tensor cores, so CTAs whose units belong to experts with many
+    // rows get fewer of them.  (One row: every weight is 1, an even split by count.)
+    // Thread 0 cuts chunks lazily (stopping at expert boundaries and the slot size) and
+    // leaves the descriptor of chunk n in ring entry n % kGuSlots when it issues it.
+    // thread 0's chunk cursor lives in shared memory (cur, end, expert, offset), so no
+    // thread carries it in registers through the gate/up loop
+    int* s_cursor = reinterpret_cast<int*>(smem + P.chunks + kGuSlots * 12 + 4);
+    auto next_chunk = [&]() {
+      int cur = s_cursor[0], ui = s_cursor[2], i0 = s_cursor[3];
+      int nn = s_cursor[1] - cur;
+      if (nn > a.I - i0) nn = a.I - i0;
+      if (nn > P.gu_cap) nn = P.gu_cap;
+      const GuChunk ch{ui, i0, nn};
+      cur += nn;
+      i0 += nn;
+      if (i0 == a.I) {
+        ++ui;
+        i0 = 0;
+      }
+      s_cursor[0] = cur;
+      s_cursor[2] = ui;
+      s_cursor[3] = i0;
+      return ch;
+    };
+    int g_cur = 0, g_end = 0;
+    if (a.R == 1) {
+      // one row: every unit costs the same, an even split by count
+      // (U * I * grid < 2^31: U <= 512, I <= 4096, grid <= 1024)
       const unsigned N = (unsigned)U * (unsigned)a.I;
-      int cur = (int)((blockIdx.x * N) / (unsigned)G);
-      const int end = (int)(((blockIdx.x + 1) * N) / (unsigned)G);
-      int nc = 0;
-      int ui = cur / a.I, i0 = cur - ui * a.I;
-      while (cur < end && nc < kMaxChunks) {
-        int n = end - cur;
-        if (n > a.I - i0) n = a.I - i0;
-        if (n > P.gu_cap) n = P.gu_cap;
-        s_chunks[nc++] = GuChunk{ui, i0, n};
-        cur += n;
-        i0 += n;
-        if (i0 == a.I) {
-          ++ui;
-          i0 = 0;
+      g_cur = (int)((blockIdx.x * N) / (unsigned)G);
+      g_end = (int)(((blockIdx.x + 1) * N) / (unsigned)G);
+    } else if (warp == 0) {
+      // work per expert, prefix over lanes (lane l owns a contiguous run of experts), then
+      // the lane whose run holds a target finds the unit there.  Work totals stay below
+      // 2^25 (U I <= 2^21 units, weights <= 16), so 32-bit integers hold them; the targets
+      // c W / G are taken in double (exact products below 2^53) and floored, the same way
+      // by neighbouring CTAs, so the ranges tile the units.
+      auto weight = [&](int ui) {
+        const int re = T.csr_off[ui + 1] - T.csr_off[ui];
+        return mma ? (re + 15) >> 4 : (re + 1) >> 1;
+      };
+      const int lane = tid & 31, per = (U + 31) >> 5;
+      const int e0 = min(lane * per, U), e1 = min(e0 + per, U);
+      int mine = 0;
+      for (int ui = e0; ui < e1; ++ui) mine += a.I * weight(ui);
+      int inc = mine;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int tv = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += tv;
+      }
+      const int wt_total = __shfl_sync(0xffffffffu, inc, 31), base = inc - mine;
+      auto unit_at = [&](int target) {
+        const bool here = target >= base && target < inc;
+        int res = U * a.I;
+        if (here) {
+          int cum = base;
+          for (int ui = e0; ui < e1; ++ui) {
+            const int w = weight(ui), ew = a.I * w;
+            if (target < cum + ew) {
+              res = ui * a.I + (target - cum) / w;
+              break;
+            }
+            cum += ew;
+          }
         }
+        const unsigned owner = __ballot_sync(0xffffffffu, here);
+        return owner ? __shfl_sync(0xffffffffu, res, __ffs(owner) - 1) : U * a.I;
+      };
+      const double wg = (double)wt_total / (double)G;
+      g_cur = unit_at((int)floor(wg * (double)blockIdx.x));
+      g_end = unit_at(blockIdx.x + 1 == (unsigned)G ? wt_total : (int)floor(wg * (double)(blockIdx.x + 1)));
+    }
+    if (tid == 0) {
+      s_cursor[0] = g_cur;
+      s_cursor[1] = g_end;
+      s_cursor[2] = g_cur / a.I;
+      s_cursor[3] = g_cur - (g_cur / a.I) * a.I;
+    }
+    if (tid == 0) {
+      // count the chunks (same cuts as next_chunk), then describe the first ring's worth
+      int nc = 0;
+      for (int cur = g_cur, i0 = s_cursor[3]; cur < g_end; ++nc) {
+        int nn = g_end - cur;
+        if (nn > a.I - i0) nn = a.I - i0;
+        if (nn > P.gu_cap) nn = P.gu_cap;
+        cur += nn;
+        i0 = (i0 + nn == a.I) ? 0 : i0 + nn;
       }
-      if (cur < end) {  // (the host rejects shapes that could get here) never drop work
-        atomicOr(a.status, kStatusTimeout);
-        atomicExch(a.bar + 33, 1u);
-      }
-      *reinterpret_cast<int*>(smem + P.chunks + kMaxChunks * 12) = nc;
+      for (int q = 0; q < kGuSlots && q < nc; ++q) s_chunks[q] = next_chunk();
+      *reinterpret_cast<int*>(smem + P.chunks + kGuSlots * 12) = nc;
     }
     __syncthreads();
-    const int n_chunks = *reinterpret_cast<const int*>(smem + P.chunks + kMaxChunks * 12);
+    const int n_chunks = *reinterpret_cast<const int*>(smem + P.chunks + kGuSlots * 12);
     const int n_first = min(kGuFirst, n_chunks), n_ring = min(kGuSlots, n_chunks);
     gu_pend |= (1u << n_first) - 1u;
     if (tid < n_first) issue_gu_chunk(a, W, T, gu + tid * P.gu_slot, smem_u32(bars + tid), s_chunks[tid]);
@@ -1357,7 +1421,7 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
         issue_dn_prefetch();
       }
       stamp(a, l, 5);  // (the last chunk's stamp stays)
-      const GuChunk c = s_chunks[n];
+      const GuChunk c = s_chunks[q];
       const uint8_t* slot = gu + q * P.gu_slot;
       if (mma)
         gateup_chunk_mma(a, T, slot, c, x, s_mpart);
@@ -1368,7 +1432,10 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
       __syncthreads();  // slot q free again
       if (n + kGuSlots < n_chunks) {
         gu_pend |= 1u << q;
-        if (tid == 0) issue_gu_chunk(a, W, T, gu + q * P.gu_slot, smem_u32(bars + q), s_chunks[n + kGuSlots]);
+        if (tid == 0) {
+          s_chunks[q] = next_chunk();
+          issue_gu_chunk(a, W, T, gu + q * P.gu_slot, smem_u32(bars + q), s_chunks[q]);
+        }
       }
     }
     if (n_chunks == 0) {
@@ -1646,16 +1713,42 @@ int check_layer(const moe_layer_w* w) {
 // every handle: raise it once to the device's opt-in maximum (minus the kernel's static
 // shared memory), so a handle created later with a smaller plan cannot lower it below
 // what an earlier handle launches with.
-template <int NBL>
+template <int NBL, bool WIDE>
 cudaError_t allow_max_dynamic_smem(int device) {
   int optin = 0;
   cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
   cudaFuncAttributes fa{};
-  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, k_round<NBL>);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, k_round<NBL, WIDE>);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(k_round<NBL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(k_round<NBL, WIDE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              optin - (int)fa.sharedSizeBytes);
   return e;
+}
+
+// Both kernels of one NBL may serve a handle: raise their limits and check that one CTA
+// of each fits an SM with `smem` bytes.
+template <int NBL>
+cudaError_t prepare_kernels(int device, size_t smem, int& occ) {
+  int o1 = 0, o2 = 0;
+  cudaError_t e = allow_max_dynamic_smem<NBL, false>(device);
+  if (e == cudaSuccess) e = allow_max_dynamic_smem<NBL, true>(device);
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o1, k_round<NBL, false>, NT, smem);
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o2, k_round<NBL, true>, NT, smem);
+  occ = o1 < o2 ? o1 : o2;
+  return e;
+}
+
+// Rounds of at least kMmaRows rows whose positions and this grid's output rows per CTA fit
+// the tensor-core path's shared-memory scratch run on the tensor cores.
+bool wide_round(const moe_dims& d, int rows, int grid) {
+  const SmemPlan p = smem_plan(d.hidden, d.inter, d.n_experts, d.max_rows, d.top_k, grid);
+  return rows >= kMmaRows && rows * d.top_k <= kMmaMaxPos && p.max_orows <= 16;
+}
+
+cudaError_t launch_kernel(const cudaLaunchConfig_t& cfg, const RoundArgs& a, bool wide) {
+  if (nbl_of(a.H) == 1)
+    return wide ? cudaLaunchKernelEx(&cfg, k_round<1, true>, a) : cudaLaunchKernelEx(&cfg, k_round<1, false>, a);
+  return wide ? cudaLaunchKernelEx(&cfg, k_round<2, true>, a) : cudaLaunchKernelEx(&cfg, k_round<2, false>, a);
 }
 
 size_t smem_bytes(const moe_dims& d, int rows, int grid) {
@@ -1707,10 +1800,7 @@ cudaError_t launch_round(moe_handle* h, const RoundArgs& a, cudaStream_t st, boo
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (nbl_of(a.H) == 1)
-    e = cudaLaunchKernelEx(&cfg, k_round<1>, a);
-  else
-    e = cudaLaunchKernelEx(&cfg, k_round<2>, a);
+  e = launch_kernel(cfg, a, !a.route_only && wide_round(h->dims, a.R, h->sm_count));
   if (prof) cudaEventRecord(e1, st);
   return e;
 }
@@ -1773,13 +1863,7 @@ int moe_create(const moe_dims* dims, int device, moe_handle** out) {
   }
   cudaError_t e;
   int occ = 0;
-  if (nbl_of(dims->hidden) == 1) {
-    e = allow_max_dynamic_smem<1>(device);
-    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_round<1>, NT, smem);
-  } else {
-    e = allow_max_dynamic_smem<2>(device);
-    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_round<2>, NT, smem);
-  }
+  e = (nbl_of(dims->hidden) == 1) ? prepare_kernels<1>(device, smem, occ) : prepare_kernels<2>(device, smem, occ);
   if (e != cudaSuccess || occ < 1) {
     cudaGetLastError();
     cudaFree(h->status);
@@ -2053,8 +2137,10 @@ int noalloc_setup(int dev, size_t smem, NoAllocDevice** out) {
     d.ready = true;
   }
   (void)smem;  // (checked against the device limit by the caller)
-  cudaError_t e = allow_max_dynamic_smem<1>(dev);
-  if (e == cudaSuccess) e = allow_max_dynamic_smem<2>(dev);
+  cudaError_t e = allow_max_dynamic_smem<1, false>(dev);
+  if (e == cudaSuccess) e = allow_max_dynamic_smem<1, true>(dev);
+  if (e == cudaSuccess) e = allow_max_dynamic_smem<2, false>(dev);
+  if (e == cudaSuccess) e = allow_max_dynamic_smem<2, true>(dev);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return MOE_ECUDA;
@@ -2126,7 +2212,6 @@ extern "C" int moe_decode_layer_noalloc(const moe_dims* dims, const moe_layer_w*
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = (nbl_of(a.H) == 1) ? cudaLaunchKernelEx(&cfg, k_round<1>, a)
-                                           : cudaLaunchKernelEx(&cfg, k_round<2>, a);
+  const cudaError_t e = launch_kernel(cfg, a, wide_round(dd, rows, sms));
   return e == cudaSuccess ? MOE_OK : MOE_ECUDA;
 }
