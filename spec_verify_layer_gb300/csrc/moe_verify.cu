@@ -451,8 +451,12 @@ __device__ __forceinline__ void select_row(const float* row, int E, int k, int l
 // routes only at rank 7 or lower are skipped): with a.tail_rank = T > 0 an expert whose
 // best 1-based rank over the rows that picked it is >= T leaves the union; its picks
 // are not evaluated and the other weights are not renormalised.
+// It also cuts this CTA's share of the gate/up units into s_range[0..1] (first, end):
+// units are shared out by work, a unit of an expert with R_e rows costing about
+// ceil(R_e / 2) passes on the fp32 path (rows go two at a time) and ceil(R_e / 16) on
+// the tensor cores (wide != 0); one row is an even split by count.
 __device__ int route_phase(const RoundArgs& a, const Tables& T, unsigned* s_mask, int* s_off_e,
-                           int* s_ids, int* s_ui, int* s_rank, int layer) {
+                           int* s_ids, int* s_ui, int* s_rank, int layer, int wide, int* s_range) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int E = a.E, k = a.k, R = a.R;
   // rows: top-k, renormalised weights, row bits of each picked expert
@@ -486,7 +490,8 @@ __device__ int route_phase(const RoundArgs& a, const Tables& T, unsigned* s_mask
   if (warp == 0) {
     const int per = (E + 31) >> 5;  // <= 16
     const int e0 = lane * per, e1 = min(e0 + per, E);
-    int lf = 0, lc = 0;
+    auto weight = [&](unsigned m) { const int re = __popc(m); return wide ? (re + 15) >> 4 : (re + 1) >> 1; };
+    int lf = 0, lc = 0, lw = 0;
     for (int e = e0; e < e1; ++e) {
       unsigned m = s_mask[e];
       if (m && a.tail_rank > 0 && s_rank[e] + 1 >= a.tail_rank) {
@@ -495,18 +500,62 @@ __device__ int route_phase(const RoundArgs& a, const Tables& T, unsigned* s_mask
       }
       lf += (m != 0u);
       lc += __popc(m);
+      if (m) lw += a.I * weight(m);
     }
-    int incf = lf, incc = lc;
+    int incf = lf, incc = lc, incw = lw;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int tf = __shfl_up_sync(0xffffffffu, incf, o);
       const int tc = __shfl_up_sync(0xffffffffu, incc, o);
+      const int tw = __shfl_up_sync(0xffffffffu, incw, o);
       if (lane >= o) {
         incf += tf;
         incc += tc;
+        incw += tw;
       }
     }
     int basef = incf - lf, basec = incc - lc;
+    // this CTA's unit range: the targets t(c) ~ c W / G are computed the same way by
+    // neighbouring CTAs (in fp32; monotone in c, t(0) = 0, t(G) = W), so the ranges
+    // tile the units.
+    {
+      const int G = gridDim.x, c = blockIdx.x;
+      const int U = __shfl_sync(0xffffffffu, incf, 31);
+      if (R == 1) {
+        const unsigned N = (unsigned)U * (unsigned)a.I;  // < 2^31 (U <= 512, I <= 4096)
+        if (lane == 0) {
+          s_range[0] = (int)((c * N) / (unsigned)G);
+          s_range[1] = (int)(((c + 1) * N) / (unsigned)G);
+        }
+      } else {
+        const int wt_total = __shfl_sync(0xffffffffu, incw, 31), basew = incw - lw;
+        const float wg = (float)wt_total / (float)G;
+        const int tgt[2] = {c == 0 ? 0 : min((int)(wg * (float)c), wt_total),
+                            c + 1 == G ? wt_total : min((int)(wg * (float)(c + 1)), wt_total)};
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const bool here = tgt[q] >= basew && tgt[q] < incw;
+          int res = U * a.I;
+          if (here) {
+            int cum = basew, ui = basef;
+            for (int e = e0; e < e1; ++e) {
+              const unsigned m = s_mask[e];
+              if (!m) continue;
+              const int w = weight(m), ew = a.I * w;
+              if (tgt[q] < cum + ew) {
+                res = ui * a.I + (tgt[q] - cum) / w;
+                break;
+              }
+              cum += ew;
+              ++ui;
+            }
+          }
+          const unsigned owner = __ballot_sync(0xffffffffu, here);
+          res = owner ? __shfl_sync(0xffffffffu, res, __ffs(owner) - 1) : U * a.I;
+          if (lane == 0) s_range[q] = res;
+        }
+      }
+    }
     for (int e = e0; e < e1; ++e) {
       const unsigned m = s_mask[e];
       if (m) {
@@ -1293,16 +1342,14 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
       return;
     }
     stamp(a, l, 2);
-    const int U = route_phase(a, T, s_mask, s_off_e, s_ids, s_ui, s_rank, l);
+    int* s_range = reinterpret_cast<int*>(smem + P.chunks + kGuSlots * 12 + 20);
+    const int U = route_phase(a, T, s_mask, s_off_e, s_ids, s_ui, s_rank, l, mma ? 1 : 0, s_range);
     stamp(a, l, 3);
     if (a.route_only) return;
-    // ---- this CTA's share of the gate/up units; chunks issued through the ring ----
-    // Units are shared out by work, not by count: a unit of an expert with R_e rows costs
-    // about ceil(R_e / 2) passes on the fp32 path (rows go two at a time) and
-    // ceil(R_e / 16) on the tensor cores, so CTAs whose units belong to experts with many
-    // rows get fewer of them.  (One row: every weight is 1, an even split by count.)
-    // Thread 0 cuts chunks lazily (stopping at expert boundaries and the slot size) and
-    // leaves the descriptor of chunk n in ring entry n % kGuSlots when it issues it.
+    // ---- this CTA's share of the gate/up units (cut during routing); chunks issued
+    // through the ring: thread 0 cuts them lazily (stopping at expert boundaries and the
+    // slot size) and leaves the descriptor of chunk n in ring entry n % kGuSlots when it
+    // issues it ----
     // thread 0's chunk cursor lives in shared memory (cur, end, expert, offset), so no
     // thread carries it in registers through the gate/up loop
     int* s_cursor = reinterpret_cast<int*>(smem + P.chunks + kGuSlots * 12 + 4);
@@ -1323,55 +1370,7 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
       s_cursor[3] = i0;
       return ch;
     };
-    int g_cur = 0, g_end = 0;
-    if (a.R == 1) {
-      // one row: every unit costs the same, an even split by count
-      // (U * I * grid < 2^31: U <= 512, I <= 4096, grid <= 1024)
-      const unsigned N = (unsigned)U * (unsigned)a.I;
-      g_cur = (int)((blockIdx.x * N) / (unsigned)G);
-      g_end = (int)(((blockIdx.x + 1) * N) / (unsigned)G);
-    } else if (warp == 0) {
-      // work per expert, prefix over lanes (lane l owns a contiguous run of experts), then
-      // the lane whose run holds a target finds the unit there.  Work totals stay below
-      // 2^25 (U I <= 2^21 units, weights <= 16), so 32-bit integers hold them; the targets
-      // c W / G are taken in double (exact products below 2^53) and floored, the same way
-      // by neighbouring CTAs, so the ranges tile the units.
-      auto weight = [&](int ui) {
-        const int re = T.csr_off[ui + 1] - T.csr_off[ui];
-        return mma ? (re + 15) >> 4 : (re + 1) >> 1;
-      };
-      const int lane = tid & 31, per = (U + 31) >> 5;
-      const int e0 = min(lane * per, U), e1 = min(e0 + per, U);
-      int mine = 0;
-      for (int ui = e0; ui < e1; ++ui) mine += a.I * weight(ui);
-      int inc = mine;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int tv = __shfl_up_sync(0xffffffffu, inc, o);
-        if (lane >= o) inc += tv;
-      }
-      const int wt_total = __shfl_sync(0xffffffffu, inc, 31), base = inc - mine;
-      auto unit_at = [&](int target) {
-        const bool here = target >= base && target < inc;
-        int res = U * a.I;
-        if (here) {
-          int cum = base;
-          for (int ui = e0; ui < e1; ++ui) {
-            const int w = weight(ui), ew = a.I * w;
-            if (target < cum + ew) {
-              res = ui * a.I + (target - cum) / w;
-              break;
-            }
-            cum += ew;
-          }
-        }
-        const unsigned owner = __ballot_sync(0xffffffffu, here);
-        return owner ? __shfl_sync(0xffffffffu, res, __ffs(owner) - 1) : U * a.I;
-      };
-      const double wg = (double)wt_total / (double)G;
-      g_cur = unit_at((int)floor(wg * (double)blockIdx.x));
-      g_end = unit_at(blockIdx.x + 1 == (unsigned)G ? wt_total : (int)floor(wg * (double)(blockIdx.x + 1)));
-    }
+    const int g_cur = s_range[0], g_end = s_range[1];
     if (tid == 0) {
       s_cursor[0] = g_cur;
       s_cursor[1] = g_end;
