@@ -42,6 +42,9 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--layers", type=int, default=0, help="override the stack depth (0 = 40)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rows", type=int, default=1, choices=[1, 4, 16],
+                    help="rows of the headline round (1 = the decode-width workload; 4 and 16 "
+                         "put that round first, e.g. to profile its first launch)")
     return ap.parse_args()
 
 
@@ -310,7 +313,9 @@ def run_ours(args):
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
-    head = time_rounds(1, 0.0, args.steps, max(args.warmup, 3))
+    SIGMA = {1: 0.0, 4: 0.5, 16: 0.1}
+    R0 = args.rows
+    head = time_rounds(R0, SIGMA[R0], args.steps, max(args.warmup, 3))
     sampler.stop()
     clocks = sampler.summary(*head["t_wall"])
 
@@ -320,7 +325,8 @@ def run_ours(args):
 
     # rows sweep on the same weights
     sweep = {}
-    for rows, sigma, name in ((4, 0.5, "a3b_r4"), (16, 0.1, "a3b_r16")):
+    for rows in (r for r in (1, 4, 16) if r != R0):
+        sigma, name = SIGMA[rows], f"a3b_r{rows}"
         r = time_rounds(rows, sigma, max(20, args.steps // 4), max(args.warmup, 3))
         msr = r["ms_total"] / r["steps"]
         gbs = r["bytes_per_round"] / (msr * 1e-3) / 1e9
@@ -353,9 +359,9 @@ def run_ours(args):
     prof_rounds = max(3, min(20, args.steps // 50))
     x1, out1 = head["x"], head["out"]
     stats1 = torch.zeros(L, dtype=torch.int32, device=dev)
-    phases, eager_ms, eager_n = profile_phases(1, x1, out1, prof_rounds)
+    phases, eager_ms, eager_n = profile_phases(R0, x1, out1, prof_rounds)
     roofline = {"bound": "hbm", "kernel": "k_round", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "traffic": read_traffic("k_round", L), "peak_source": peak_src,
+                "frac": achieved / peak, "traffic": read_traffic("k_round", L, R0), "peak_source": peak_src,
                 "alg_bytes_per_launch": alg_per_launch, "avg_launch_us": avg_launch_us,
                 "launch": f"one cooperative launch per {L}-layer round, timed over {args.steps} graph replays",
                 "phases_per_layer_us": phases,
@@ -363,12 +369,12 @@ def run_ours(args):
 
     # end to end through the C ABI with host buffers (pinned), copies inside the timed region
     xh = torch.from_numpy(head["xs"].view(np.int16)).pin_memory()
-    oh = torch.empty((L, 1, H), dtype=torch.float32).pin_memory()
+    oh = torch.empty((L, R0, H), dtype=torch.float32).pin_memory()
     e2e_steps = max(10, min(args.steps, 500))
     with torch.cuda.stream(stream):
         for _ in range(3):
             x1.copy_(xh, non_blocking=True)
-            mv.moe_round(handle, wl, x1.data_ptr(), 1, out1.data_ptr(), stats1.data_ptr(), ws.data_ptr(),
+            mv.moe_round(handle, wl, x1.data_ptr(), R0, out1.data_ptr(), stats1.data_ptr(), ws.data_ptr(),
                          ws.numel(), True, st)
             oh.copy_(out1, non_blocking=True)
             stream.synchronize()
@@ -377,7 +383,7 @@ def run_ours(args):
     with torch.cuda.stream(stream):
         for _ in range(e2e_steps):
             x1.copy_(xh, non_blocking=True)
-            mv.moe_round(handle, wl, x1.data_ptr(), 1, out1.data_ptr(), stats1.data_ptr(), ws.data_ptr(),
+            mv.moe_round(handle, wl, x1.data_ptr(), R0, out1.data_ptr(), stats1.data_ptr(), ws.data_ptr(),
                          ws.numel(), True, st)
             oh.copy_(out1, non_blocking=True)
             stream.synchronize()
@@ -399,12 +405,12 @@ def run_ours(args):
                 "warmup": max(args.warmup, 3), "ms_per_step": ms_round, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f32",
                 "data": "synthetic (seeded counter-based generator; random int4 weights, bf16 rows)",
-                "config": workload_config(cfg, 1, L),
+                "config": workload_config(cfg, R0, L),
                 "us_per_layer": us_layer, "us_per_round": 1e3 * ms_round,
                 "hbm_gbs_per_gpu": value / world, "frac_of_peak": value / world / peak,
-                "tokens_per_round_equiv_per_s": 1.0 / (ms_round * 1e-3),
+                "tokens_per_round_equiv_per_s": R0 / (ms_round * 1e-3),
                 "unique_experts_per_layer": float(np.mean(head["U"])),
-                "rows": {"r1": {"us_per_layer": us_layer, "hbm_gbs": value / world,
+                "rows": {f"r{R0}": {"us_per_layer": us_layer, "hbm_gbs": value / world,
                                 "frac_of_peak": value / world / peak,
                                 "unique_experts_per_layer": float(np.mean(head["U"]))}, **sweep},
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
@@ -416,10 +422,11 @@ def run_ours(args):
     return 0
 
 
-def read_traffic(kernel, layers):
+def read_traffic(kernel, layers, rows):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on the
-    current kernel source (its recorded source digest matches); scaled from the
-    captured layer count to `layers` (traffic grows in proportion).  Else None."""
+    current kernel source (its recorded source digest matches) for a round of `rows`
+    rows; scaled from the captured layer count to `layers` (traffic grows in
+    proportion).  Else None."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     src = os.path.join(ROOT, "spec_verify_layer_gb300", "csrc", "moe_verify.cu")
@@ -427,7 +434,7 @@ def read_traffic(kernel, layers):
         kv = dict(l.split(":", 1) for l in open(path) if ":" in l and not l.startswith("#"))
         kv = {k.strip(): v.strip() for k, v in kv.items()}
         digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        if kv.get("kernel") == kernel and kv.get("source_sha256_16") == digest:
+        if kv.get("kernel") == kernel and kv.get("source_sha256_16") == digest and int(kv.get("rows", "1")) == rows:
             return float(kv["dram_bytes_per_launch"]) * layers / float(kv["layers"])
     except Exception:
         pass
