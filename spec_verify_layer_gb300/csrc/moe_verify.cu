@@ -95,7 +95,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ int lane_of(int tid) { return tid & 31; }
 
 __device__ __forceinline__ long long gtimer() {
   long long t;
@@ -984,28 +983,29 @@ __device__ __forceinline__ void down_position(const RoundArgs& a, const uint8_t*
 //
 // A nibble n in the low four bits of a bf16 whose other bits are those of 128.0 is the
 // bf16 value 128 + n, exactly; one mask-and-or per pair of weights (two nibbles 16 bits
-// apart land in the two halves of a bf16x2 register).  Inside each 32-element block the
-// MMA's k order is permuted so that thread t's A fragments for the block's two k16 steps
-// are exactly the eight nibbles of 32-bit word t of a row's 16-byte block:
+// apart land in the two halves of a bf16x2 register), and one bf16x2 subtraction of 136
+// gives n - 8, again exactly.  Inside each 32-element block the MMA's k order is
+// permuted so that thread t's A fragments for the block's two k16 steps are exactly
+// the eight nibbles of 32-bit word t of a row's 16-byte block:
 //   step 0: k (2t, 2t+1) <- elements (8t, 8t+4),   k (2t+8, 2t+9) <- (8t+1, 8t+5)
 //   step 1: k (2t, 2t+1) <- (8t+2, 8t+6),          k (2t+8, 2t+9) <- (8t+3, 8t+7)
 // The B fragments (activations, or the exchanged h' split into bf16 hi + lo) follow the
-// same permutation.  A block's MMAs give D = sum (128 + n) b; the layer needs
-// sum (n - 8) b = D - 136 sum b, times the row's block scale: the bias term of a
-// (column, block) is summed from the B fragments the lanes already hold.  Every tile's K range is split in the
-// same kKParts parts whatever the other rows are, and the parts are added in a fixed
-// order, so a row's result does not depend on the rows it shares the round with.
+// same permutation.  A block's MMAs give sum (n - 8) b, which the block scale then
+// multiplies into the fp32 accumulator.  Each warp keeps one A tile (16 weight rows x
+// one K part) in registers for up to two n-tiles (16 expert rows or positions).  Every
+// tile's K range is split in the same fixed parts whatever the other rows are, and the
+// parts are added in a fixed order, so a row's result does not depend on the rows it
+// shares the round with.
 
 constexpr int kMmaRows = 8;
-constexpr int kKParts = 4;
-constexpr int kTilesPerRound = NW / kKParts;  // tiles in flight (one warp per tile part)
+constexpr int kKPartsGu = 8;  // K parts of a gate/up tile (hidden blocks)
+constexpr int kKPartsDn = 4;  // K parts of a down tile (intermediate blocks)
+static_assert(NW % kKPartsGu == 0 && NW % kKPartsDn == 0, "a tile's K parts run in one round");
 // scratch of the tensor-core path inside the activation-pair region (unused then)
 constexpr int kMmaMaxPos = 256;          // CSR positions (rows x top-k) of a wide round
-static_assert(kMmaMaxPos <= NT, "one thread per position when the wide down tiles are listed");
-constexpr int kMmaMaxTiles = kMmaMaxPos;
-constexpr size_t kMmaPart = 0;           // [NW][16][8] fp32 partial tiles
-constexpr size_t kMmaY = 8192;           // [kMmaMaxPos][16] fp32: y per position and output row
-constexpr size_t kMmaTiles = kMmaY + (size_t)kMmaMaxPos * 16 * 4;  // [kMmaMaxTiles][3] int + count
+constexpr size_t kMmaPart = 0;           // [NW][2][16][8] fp32 partial tiles
+constexpr size_t kMmaY = (size_t)NW * 256 * 4;  // [kMmaMaxPos][16] fp32: y per position and output row
+static_assert(kMmaY + (size_t)kMmaMaxPos * 16 * 4 <= kXBytes, "wide scratch fits the activation region");
 
 __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
@@ -1017,13 +1017,14 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
 }
 
 // A 32-bit word of codes (eight nibbles, elements 0..7 of the word) -> four bf16 pairs
-// (128 + n): (0, 4), (1, 5), (2, 6), (3, 7).
+// (n - 8): (0, 4), (1, 5), (2, 6), (3, 7).
 __device__ __forceinline__ void dq_word(uint32_t w, uint32_t (&p)[4]) {
-  constexpr uint32_t M = 0x000F000Fu, C = 0x43004300u;
-  p[0] = (w & M) | C;
-  p[1] = ((w >> 4) & M) | C;
-  p[2] = ((w >> 8) & M) | C;
-  p[3] = ((w >> 12) & M) | C;
+  constexpr uint32_t M = 0x000F000Fu, C = 0x43004300u, B136 = 0x43084308u;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t v = ((w >> (4 * q)) & M) | C;  // 128 + n
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(p[q]) : "r"(v), "r"(B136));
+  }
 }
 
 // Eight bf16 activations (elements 8t .. 8t+7 of a block) -> the same pairs.
@@ -1034,94 +1035,101 @@ __device__ __forceinline__ void bfrag_x(uint4 v, uint32_t (&b)[4]) {
   b[3] = __byte_perm(v.y, v.w, 0x7632);
 }
 
+// A warp's partial tiles ([2 n-tiles][16 rows][8 columns]) -> its scratch.
+__device__ __forceinline__ void store_part(float* part, const float (&acc)[2][4], int g, int t) {
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    *reinterpret_cast<float2*>(part + nt * 128 + g * 8 + 2 * t) = make_float2(acc[nt][0], acc[nt][1]);
+    *reinterpret_cast<float2*>(part + nt * 128 + (g + 8) * 8 + 2 * t) = make_float2(acc[nt][2], acc[nt][3]);
+  }
+}
 
-// Gate/up of one staged chunk on the tensor cores: tiles of 16 weight rows (8 units,
-// gate and up interleaved) x 8 of the expert's rows, one warp per (tile, K part); the
-// parts are added in order, then h' = w silu(g) v is stored split into bf16 hi + lo in
-// the down pass's fragment order.
+// Gate/up of one staged chunk on the tensor cores.  A tile = 8 units of the chunk (A
+// row g: the gate row of unit g, row g + 8: its up row, so the eight lanes' rows have
+// eight different block swizzles) x up to 16 of the expert's rows (two n-tiles) x one
+// of kKPartsGu K parts; one warp per tile part.  The parts are added in order, then
+// h' = w silu(g) v is stored split into bf16 hi + lo in the down pass's fragment order.
 __device__ void gateup_chunk_mma(const RoundArgs& a, const Tables& T, const uint8_t* slot, const GuChunk& c,
                                  const uint16_t* x, float* s_part) {
   const int H = a.H, NB = H >> 5, NBI = a.I >> 5;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const int p0 = T.csr_off[c.ui], Re = T.csr_off[c.ui + 1] - p0;
-  const int NTN = (Re + 7) >> 3, combos = ((2 * c.n + 15) >> 4) * NTN;
+  const int NTP = (Re + 15) >> 4, MT = (c.n + 7) >> 3, n_asg = MT * NTP * kKPartsGu;
   const uint8_t* codes = slot;
   const uint16_t* scales = reinterpret_cast<const uint16_t*>(slot + (size_t)c.n * H);
   uint16_t* hb = reinterpret_cast<uint16_t*>(a.hbuf);
-  for (int cb0 = 0; cb0 < combos; cb0 += kTilesPerRound) {
-    const int cb = cb0 + warp / kKParts, kp = warp % kKParts;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    if (cb < combos) {
-      const int mt = cb / NTN, nt = cb - mt * NTN;
-      const int ra = mt * 16 + g, rb = ra + 8;  // weight rows of the chunk (2 unit + gate/up)
-      const bool va = ra < 2 * c.n, vb = rb < 2 * c.n;
+  for (int j0 = 0; j0 < n_asg; j0 += NW) {
+    const int j = j0 + warp;
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    if (j < n_asg) {
+      const int gi = j / kKPartsGu, kp = j - gi * kKPartsGu;
+      const int mt = gi / NTP, ntp = gi - mt * NTP;
+      // units past the chunk repeat its last one; their results are dropped
+      const int u = min(mt * 8 + g, c.n - 1), kk = (c.i0 + u) & 7;
+      const uint32_t* wg = reinterpret_cast<const uint32_t*>(codes + (size_t)(2 * u) * NB * 16) + t;
+      const uint32_t* wu = wg + NB * 4;
+      const uint16_t* sg_ = scales + (size_t)(2 * u) * NB;
+      const uint16_t* su_ = sg_ + NB;
       // columns past the expert's rows repeat its last row; their results are dropped
-      const int xr = T.pos_row[p0 + min(nt * 8 + g, Re - 1)];
-      const uint4* xrow = reinterpret_cast<const uint4*>(x + (size_t)xr * H) + t;
-      const int b0 = (kp * NB) / kKParts, b1 = ((kp + 1) * NB) / kKParts;
-#pragma unroll 4
+      const int c0 = ntp * 16 + g;
+      const bool two = ntp * 16 + 8 < Re;
+      const uint4* x0 = reinterpret_cast<const uint4*>(x + (size_t)T.pos_row[p0 + min(c0, Re - 1)] * H) + t;
+      const uint4* x1 = reinterpret_cast<const uint4*>(x + (size_t)T.pos_row[p0 + min(c0 + 8, Re - 1)] * H) + t;
+      const int b0 = (kp * NB) / kKPartsGu, b1 = ((kp + 1) * NB) / kKPartsGu;
+#pragma unroll 2
       for (int b = b0; b < b1; ++b) {
-        const int pa_ = block_pos(b, c.i0 + (ra >> 1)), pb_ = block_pos(b, c.i0 + (rb >> 1));
-        const uint32_t wa = va ? *reinterpret_cast<const uint32_t*>(codes + ((size_t)ra * NB + pa_) * 16 + 4 * t) : 0u;
-        const uint32_t wb = vb ? *reinterpret_cast<const uint32_t*>(codes + ((size_t)rb * NB + pb_) * 16 + 4 * t) : 0u;
-        const uint4 xv = __ldg(xrow + 4 * b);
-        uint32_t pa[4], pb[4], bf[4];
-        dq_word(wa, pa);
-        dq_word(wb, pb);
-        bfrag_x(xv, bf);
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_bf16(d, pa[0], pb[0], pa[1], pb[1], bf[0], bf[1]);
-        mma_bf16(d, pa[2], pb[2], pa[3], pb[3], bf[2], bf[3]);
-        const float sa = va ? half_bits(scales[(size_t)ra * NB + pa_]) : 0.f;
-        const float sb = vb ? half_bits(scales[(size_t)rb * NB + pb_]) : 0.f;
-        // bias: 136 x the block sum of the activation row of each D column, from the B
-        // fragments (8 elements per lane in order, then the lanes of the column group)
-        float cs = 0.f;
+        const int pb = b ^ kk;
+        uint32_t pg[4], pu[4];
+        dq_word(wg[4 * pb], pg);
+        dq_word(wu[4 * pb], pu);
+        const float sg = half_bits(sg_[pb]), su = half_bits(su_[pb]);
         {
-          const uint32_t w4[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            cs = __fadd_rn(cs, bf16_lo(w4[q]));
-            cs = __fadd_rn(cs, bf16_hi(w4[q]));
-          }
-          cs = __fadd_rn(cs, __shfl_xor_sync(0xffffffffu, cs, 1));
-          cs = __fadd_rn(cs, __shfl_xor_sync(0xffffffffu, cs, 2));
+          uint32_t bf[4];
+          bfrag_x(__ldg(x0 + 4 * b), bf);
+          float d[4] = {0.f, 0.f, 0.f, 0.f};
+          mma_bf16(d, pg[0], pu[0], pg[1], pu[1], bf[0], bf[1]);
+          mma_bf16(d, pg[2], pu[2], pg[3], pu[3], bf[2], bf[3]);
+          acc[0][0] = __fmaf_rn(sg, d[0], acc[0][0]);
+          acc[0][1] = __fmaf_rn(sg, d[1], acc[0][1]);
+          acc[0][2] = __fmaf_rn(su, d[2], acc[0][2]);
+          acc[0][3] = __fmaf_rn(su, d[3], acc[0][3]);
         }
-        const float k0 = __fmul_rn(136.f, __shfl_sync(0xffffffffu, cs, 8 * t));
-        const float k1 = __fmul_rn(136.f, __shfl_sync(0xffffffffu, cs, 8 * t + 4));
-        acc[0] = __fmaf_rn(sa, __fsub_rn(d[0], k0), acc[0]);
-        acc[1] = __fmaf_rn(sa, __fsub_rn(d[1], k1), acc[1]);
-        acc[2] = __fmaf_rn(sb, __fsub_rn(d[2], k0), acc[2]);
-        acc[3] = __fmaf_rn(sb, __fsub_rn(d[3], k1), acc[3]);
+        if (two) {
+          uint32_t bf[4];
+          bfrag_x(__ldg(x1 + 4 * b), bf);
+          float d[4] = {0.f, 0.f, 0.f, 0.f};
+          mma_bf16(d, pg[0], pu[0], pg[1], pu[1], bf[0], bf[1]);
+          mma_bf16(d, pg[2], pu[2], pg[3], pu[3], bf[2], bf[3]);
+          acc[1][0] = __fmaf_rn(sg, d[0], acc[1][0]);
+          acc[1][1] = __fmaf_rn(sg, d[1], acc[1][1]);
+          acc[1][2] = __fmaf_rn(su, d[2], acc[1][2]);
+          acc[1][3] = __fmaf_rn(su, d[3], acc[1][3]);
+        }
       }
     }
-    float* part = s_part + warp * 128;  // [16 rows][8 columns]
-    part[g * 8 + 2 * t] = acc[0];
-    part[g * 8 + 2 * t + 1] = acc[1];
-    part[(g + 8) * 8 + 2 * t] = acc[2];
-    part[(g + 8) * 8 + 2 * t + 1] = acc[3];
+    store_part(s_part + warp * 256, acc, g, t);
     __syncthreads();
-    for (int i = threadIdx.x; i < kTilesPerRound * 64; i += NT) {
-      const int cl = i >> 6, uu = (i >> 3) & 7, cc = i & 7;
-      const int cb = cb0 + cl;
-      if (cb >= combos) continue;
-      const int mt = cb / NTN, nt = cb - mt * NTN;
-      const int u = mt * 8 + uu, col = nt * 8 + cc;
+    for (int i = threadIdx.x; i < (NW / kKPartsGu) * 128; i += NT) {
+      const int gl = i >> 7, nt = (i >> 6) & 1, uu = (i >> 3) & 7, cc = i & 7;
+      const int gi = j0 / kKPartsGu + gl;
+      if (gi >= MT * NTP) continue;
+      const int mt = gi / NTP, ntp = gi - mt * NTP;
+      const int u = mt * 8 + uu, col = ntp * 16 + nt * 8 + cc;
       if (u >= c.n || col >= Re) continue;
       float gs = 0.f, vs = 0.f;
 #pragma unroll
-      for (int kp = 0; kp < kKParts; ++kp) {
-        const float* P = s_part + (cl * kKParts + kp) * 128;
-        gs = __fadd_rn(gs, P[(2 * uu) * 8 + cc]);
-        vs = __fadd_rn(vs, P[(2 * uu + 1) * 8 + cc]);
+      for (int kp = 0; kp < kKPartsGu; ++kp) {
+        const float* P = s_part + (gl * kKPartsGu + kp) * 256 + nt * 128;
+        gs = __fadd_rn(gs, P[uu * 8 + cc]);
+        vs = __fadd_rn(vs, P[64 + uu * 8 + cc]);
       }
       const int pp = p0 + col;
       const float hh = __fmul_rn(__fdiv_rn(gs, __fadd_rn(1.f, expf(-gs))), vs);
       const float hw = __fmul_rn(T.w[T.pair[pp]], hh);
       const __nv_bfloat16 hi = __float2bfloat16_rn(hw);
       const __nv_bfloat16 lo = __float2bfloat16_rn(__fsub_rn(hw, __bfloat162float(hi)));
-      const int i2 = c.i0 + u, j = i2 & 31, e = j & 7;
-      const size_t base = (((size_t)pp * NBI + (i2 >> 5)) * 4 + (j >> 3)) * 16 + 2 * (e & 3) + (e >> 2);
+      const int i2 = c.i0 + u, jj = i2 & 31, e = jj & 7;
+      const size_t base = (((size_t)pp * NBI + (i2 >> 5)) * 4 + (jj >> 3)) * 16 + 2 * (e & 3) + (e >> 2);
       hb[base] = __bfloat16_as_ushort(hi);
       hb[base + 8] = __bfloat16_as_ushort(lo);
     }
@@ -1129,77 +1137,86 @@ __device__ void gateup_chunk_mma(const RoundArgs& a, const Tables& T, const uint
   }
 }
 
-// One round of the wide down pass on the tensor cores: up to kTilesPerRound tiles (up
-// to 8 consecutive CSR positions of one expert x this CTA's output rows, at most 16),
-// K = I split in kKParts parts, one warp per part; B = h' (hi + lo bf16, fragment order)
-// read from the workspace through L2, two MMAs per k16 step; the bias term of each
-// (position, block) summed from the fragments.  y[position][output row] -> s_yall.
-__device__ void down_round_mma(const RoundArgs& a, const uint8_t* dn, size_t dn_slot, size_t codes_room, int o0,
-                               int no, const int* s_tiles, int cb0, int n_tiles, float* s_part, float* s_yall) {
+// One round of the wide down pass on the tensor cores: NW tile parts.  Assignment j ->
+// position group j / kKPartsDn (group = up to 16 consecutive CSR positions of one
+// expert: `gpe` groups per expert) and K part j % kKPartsDn; a tile = this CTA's output
+// rows (at most 16) x the group's positions (two n-tiles).  B = h' (hi + lo bf16,
+// fragment order) read from the workspace through L2, two MMAs per k16 step and n-tile.
+// y[position][output row] -> s_yall.
+__device__ void down_round_mma(const RoundArgs& a, const Tables& T, const uint8_t* dn, size_t dn_slot,
+                               size_t codes_room, int o0, int no, int j0, int n_asg, int gpe, float* s_part,
+                               float* s_yall) {
   const int NBI = a.I >> 5;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const uint8_t* hb = reinterpret_cast<const uint8_t*>(a.hbuf);
-  const int ti = cb0 + warp / kKParts, kp = warp % kKParts;
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  if (ti < n_tiles) {
-    const int p0 = s_tiles[3 * ti], cnt = s_tiles[3 * ti + 1], ui = s_tiles[3 * ti + 2];
-    const uint8_t* codes = dn + (size_t)(ui % kDnSlots) * dn_slot;
-    const uint16_t* scales = reinterpret_cast<const uint16_t*>(codes + codes_room);
-    const int ra = g, rb = g + 8;  // output rows of this CTA
-    const bool va = ra < no, vb = rb < no;
-    // columns past the tile's positions repeat its last one; their results are dropped
-    const int pg = p0 + min(g, cnt - 1);
-    const int b0 = (kp * NBI) / kKParts, b1 = ((kp + 1) * NBI) / kKParts;
-#pragma unroll 3
-    for (int b = b0; b < b1; ++b) {
-      const int pa_ = block_pos(b, o0 + ra), pb_ = block_pos(b, o0 + rb);
-      const uint32_t wa = va ? *reinterpret_cast<const uint32_t*>(codes + ((size_t)ra * NBI + pa_) * 16 + 4 * t) : 0u;
-      const uint32_t wb = vb ? *reinterpret_cast<const uint32_t*>(codes + ((size_t)rb * NBI + pb_) * 16 + 4 * t) : 0u;
-      const uint4* hv = reinterpret_cast<const uint4*>(hb + (((size_t)pg * NBI + b) * 4 + t) * 32);
-      const uint4 hi = __ldcg(hv), lo = __ldcg(hv + 1);
-      uint32_t pa4[4], pb4[4];
-      dq_word(wa, pa4);
-      dq_word(wb, pb4);
-      float d[4] = {0.f, 0.f, 0.f, 0.f};
-      mma_bf16(d, pa4[0], pb4[0], pa4[1], pb4[1], hi.x, hi.y);
-      mma_bf16(d, pa4[0], pb4[0], pa4[1], pb4[1], lo.x, lo.y);
-      mma_bf16(d, pa4[2], pb4[2], pa4[3], pb4[3], hi.z, hi.w);
-      mma_bf16(d, pa4[2], pb4[2], pa4[3], pb4[3], lo.z, lo.w);
-      const float sa = va ? half_bits(scales[(size_t)ra * NBI + pa_]) : 0.f;
-      const float sb = vb ? half_bits(scales[(size_t)rb * NBI + pb_]) : 0.f;
-      float cs = 0.f;
-      {
-        const uint32_t w8[8] = {hi.x, hi.y, hi.z, hi.w, lo.x, lo.y, lo.z, lo.w};
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          cs = __fadd_rn(cs, bf16_lo(w8[q]));
-          cs = __fadd_rn(cs, bf16_hi(w8[q]));
+  const int j = j0 + warp;
+  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  if (j < n_asg) {
+    const int gi = j / kKPartsDn, kp = j - gi * kKPartsDn;
+    const int ui = gi / gpe, p0 = T.csr_off[ui] + 16 * (gi - ui * gpe);
+    const int cnt = min(16, T.csr_off[ui + 1] - p0);
+    if (cnt > 0) {
+      const uint8_t* codes = dn + (size_t)(ui % kDnSlots) * dn_slot;
+      const uint16_t* scales = reinterpret_cast<const uint16_t*>(codes + codes_room);
+      // output rows past this CTA's repeat its last one; their results are dropped
+      const int ra = min(g, no - 1), rb = min(g + 8, no - 1);
+      const int ka = (o0 + ra) & 7, kb = (o0 + rb) & 7;
+      const uint32_t* wa_ = reinterpret_cast<const uint32_t*>(codes + (size_t)ra * NBI * 16) + t;
+      const uint32_t* wb_ = reinterpret_cast<const uint32_t*>(codes + (size_t)rb * NBI * 16) + t;
+      const uint16_t* sa_ = scales + (size_t)ra * NBI;
+      const uint16_t* sb_ = scales + (size_t)rb * NBI;
+      // columns past the group's positions repeat its last one; their results are dropped
+      const bool two = cnt > 8;
+      const uint4* h0 = reinterpret_cast<const uint4*>(hb + (size_t)(p0 + min(g, cnt - 1)) * NBI * 128) + 2 * t;
+      const uint4* h1 = reinterpret_cast<const uint4*>(hb + (size_t)(p0 + min(g + 8, cnt - 1)) * NBI * 128) + 2 * t;
+      const int b0 = (kp * NBI) / kKPartsDn, b1 = ((kp + 1) * NBI) / kKPartsDn;
+#pragma unroll 2
+      for (int b = b0; b < b1; ++b) {
+        const int pa = b ^ ka, pb = b ^ kb;
+        uint32_t fa[4], fb[4];
+        dq_word(wa_[4 * pa], fa);
+        dq_word(wb_[4 * pb], fb);
+        const float sa = half_bits(sa_[pa]), sb = half_bits(sb_[pb]);
+        {
+          const uint4 hi = __ldcg(h0 + 8 * b), lo = __ldcg(h0 + 8 * b + 1);
+          float d[4] = {0.f, 0.f, 0.f, 0.f};
+          mma_bf16(d, fa[0], fb[0], fa[1], fb[1], hi.x, hi.y);
+          mma_bf16(d, fa[0], fb[0], fa[1], fb[1], lo.x, lo.y);
+          mma_bf16(d, fa[2], fb[2], fa[3], fb[3], hi.z, hi.w);
+          mma_bf16(d, fa[2], fb[2], fa[3], fb[3], lo.z, lo.w);
+          acc[0][0] = __fmaf_rn(sa, d[0], acc[0][0]);
+          acc[0][1] = __fmaf_rn(sa, d[1], acc[0][1]);
+          acc[0][2] = __fmaf_rn(sb, d[2], acc[0][2]);
+          acc[0][3] = __fmaf_rn(sb, d[3], acc[0][3]);
         }
-        cs = __fadd_rn(cs, __shfl_xor_sync(0xffffffffu, cs, 1));
-        cs = __fadd_rn(cs, __shfl_xor_sync(0xffffffffu, cs, 2));
+        if (two) {
+          const uint4 hi = __ldcg(h1 + 8 * b), lo = __ldcg(h1 + 8 * b + 1);
+          float d[4] = {0.f, 0.f, 0.f, 0.f};
+          mma_bf16(d, fa[0], fb[0], fa[1], fb[1], hi.x, hi.y);
+          mma_bf16(d, fa[0], fb[0], fa[1], fb[1], lo.x, lo.y);
+          mma_bf16(d, fa[2], fb[2], fa[3], fb[3], hi.z, hi.w);
+          mma_bf16(d, fa[2], fb[2], fa[3], fb[3], lo.z, lo.w);
+          acc[1][0] = __fmaf_rn(sa, d[0], acc[1][0]);
+          acc[1][1] = __fmaf_rn(sa, d[1], acc[1][1]);
+          acc[1][2] = __fmaf_rn(sb, d[2], acc[1][2]);
+          acc[1][3] = __fmaf_rn(sb, d[3], acc[1][3]);
+        }
       }
-      const float k0 = __fmul_rn(136.f, __shfl_sync(0xffffffffu, cs, 8 * t));
-      const float k1 = __fmul_rn(136.f, __shfl_sync(0xffffffffu, cs, 8 * t + 4));
-      acc[0] = __fmaf_rn(sa, __fsub_rn(d[0], k0), acc[0]);
-      acc[1] = __fmaf_rn(sa, __fsub_rn(d[1], k1), acc[1]);
-      acc[2] = __fmaf_rn(sb, __fsub_rn(d[2], k0), acc[2]);
-      acc[3] = __fmaf_rn(sb, __fsub_rn(d[3], k1), acc[3]);
     }
   }
-  float* part = s_part + warp * 128;
-  part[g * 8 + 2 * t] = acc[0];
-  part[g * 8 + 2 * t + 1] = acc[1];
-  part[(g + 8) * 8 + 2 * t] = acc[2];
-  part[(g + 8) * 8 + 2 * t + 1] = acc[3];
+  store_part(s_part + warp * 256, acc, g, t);
   __syncthreads();
-  for (int i = threadIdx.x; i < kTilesPerRound * 128; i += NT) {
-    const int cl = i >> 7, r = (i >> 3) & 15, cc = i & 7;
-    const int tj = cb0 + cl;
-    if (tj >= n_tiles || r >= no || cc >= s_tiles[3 * tj + 1]) continue;
+  for (int i = threadIdx.x; i < (NW / kKPartsDn) * 256; i += NT) {
+    const int gl = i >> 8, nt = (i >> 7) & 1, r = (i >> 3) & 15, cc = i & 7;
+    const int gi = j0 / kKPartsDn + gl;
+    if (gi * kKPartsDn >= n_asg || r >= no) continue;
+    const int ui = gi / gpe, p0 = T.csr_off[ui] + 16 * (gi - ui * gpe);
+    const int pos = nt * 8 + cc;
+    if (pos >= T.csr_off[ui + 1] - p0) continue;
     float y = 0.f;
 #pragma unroll
-    for (int kp2 = 0; kp2 < kKParts; ++kp2) y = __fadd_rn(y, s_part[(cl * kKParts + kp2) * 128 + r * 8 + cc]);
-    s_yall[(s_tiles[3 * tj] + cc) * 16 + r] = y;
+    for (int kp = 0; kp < kKPartsDn; ++kp) y = __fadd_rn(y, s_part[(gl * kKPartsDn + kp) * 256 + nt * 128 + r * 8 + cc]);
+    s_yall[(p0 + pos) * 16 + r] = y;
   }
   __syncthreads();
 }
@@ -1254,7 +1271,6 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
   const bool x_staged = !mma && (size_t)a.R * a.H * 4 + (size_t)a.R * (a.H >> 5) * 4 <= kXBytes;
   float* s_mpart = reinterpret_cast<float*>(smem + P.xrows + kMmaPart);
   float* s_yall = reinterpret_cast<float*>(smem + P.xrows + kMmaY);
-  int* s_tiles = reinterpret_cast<int*>(smem + P.xrows + kMmaTiles);
   float* s_rw = reinterpret_cast<float*>(gu);
   float* s_acc = reinterpret_cast<float*>(smem + P.acc);
   float* s_y = reinterpret_cast<float*>(smem + P.ybuf);
@@ -1454,44 +1470,15 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
     }
     stamp(a, l, 7);
     if (mma && no > 0) {
-      // ---- wide down: tiles of one expert's positions on the tensor cores ----
-      const int total = T.csr_off[U];
-      {
-        // a tile starts at every 8th position of an expert's run; its index is the
-        // number of tile starts before it (ballot counts per warp, then the warps before)
-        const int p = tid;
-        int ui = 0, off = 0;
-        bool start = false;
-        if (p < total) {
-          ui = T.pos_ui[p];
-          off = p - T.csr_off[ui];
-          start = (off & 7) == 0;
-        }
-        const unsigned bal = __ballot_sync(0xffffffffu, start);
-        int* s_wcnt = s_tiles + 3 * kMmaMaxTiles + 1;  // [NW] tile starts per warp
-        if (lane_of(tid) == 0) s_wcnt[warp] = __popc(bal);
-        __syncthreads();
-        if (start) {
-          int n = __popc(bal & ((1u << lane_of(tid)) - 1u));
-          for (int w2 = 0; w2 < warp; ++w2) n += s_wcnt[w2];
-          s_tiles[3 * n] = p;
-          s_tiles[3 * n + 1] = min(8, T.csr_off[ui + 1] - p);
-          s_tiles[3 * n + 2] = ui;
-        }
-        if (tid == 0) {
-          int n = 0;
-          for (int w2 = 0; w2 < NW; ++w2) n += s_wcnt[w2];
-          s_tiles[3 * kMmaMaxTiles] = n;
-        }
-        __syncthreads();
-      }
+      // ---- wide down: groups of up to 16 of one expert's positions on the tensor cores ----
+      const int gpe = (a.R + 15) >> 4;  // position groups per expert
+      const int per_e = gpe * kKPartsDn, n_asg = U * per_e;
       stamp(a, l, 8);
-      const int n_tiles = s_tiles[3 * kMmaMaxTiles];
       int waited = 0, rel = 0;
-      for (int cb0 = 0; cb0 < n_tiles; cb0 += kTilesPerRound) {
-        const int cb1 = min(cb0 + kTilesPerRound, n_tiles);
+      for (int j0 = 0; j0 < n_asg; j0 += NW) {
+        const int j1 = min(j0 + NW, n_asg);
         // the round's experts must have landed: one waiting thread per slot
-        const int need = s_tiles[3 * (cb1 - 1) + 2] + 1;
+        const int need = (j1 - 1) / per_e + 1;
         if (need > waited) {
           bool ok = true;
           if (tid < need - waited) {
@@ -1510,9 +1497,9 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
           waited = need;
         }
         stamp(a, l, 9);  // (the last round's stamp stays)
-        down_round_mma(a, dn, P.dn_slot, codes_room, o0, no, s_tiles, cb0, n_tiles, s_mpart, s_yall);
-        // experts whose tiles are all done hand their slots to later experts
-        const int rel_new = (cb1 < n_tiles) ? s_tiles[3 * cb1 + 2] : U;
+        down_round_mma(a, T, dn, P.dn_slot, codes_room, o0, no, j0, n_asg, gpe, s_mpart, s_yall);
+        // experts whose groups are all done hand their slots to later experts
+        const int rel_new = (j1 < n_asg) ? j1 / per_e : U;
         if (tid < rel_new - rel && rel + tid + kDnSlots < U) {
           const int e = rel + tid, qd = e % kDnSlots;
           issue_dn_chunk(a, W, T, dn + (size_t)qd * P.dn_slot, smem_u32(bars + bar_dn0 + qd), e + kDnSlots, o0, no,
@@ -1522,7 +1509,7 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
           if (e + kDnSlots < U) dn_pend |= 1u << (e % kDnSlots);
         rel = rel_new;
       }
-      if (n_tiles == 0) stamp(a, l, 9);
+      if (n_asg == 0) stamp(a, l, 9);
       stamp(a, l, 10);
       // each row's picks in rank order
       float* out = a.out + (size_t)l * RH;
