@@ -152,13 +152,34 @@ int moe_round(moe_handle* h, const moe_layer_w* layers, int32_t L, const uint16_
               int32_t rows, float* out, int32_t* stats, void* ws, size_t ws_bytes, int use_graph,
               void* stream);
 
+/* Prefill-width layer: steps 1-5 for many token rows at once (a prompt's tokens), the
+ * infero README's MoE prefill path ("Beyond plain text decode": a counting sort of the
+ * (token, expert) picks by expert, then one GEMM per expert).  Same weights, routing
+ * (canonical router order, ties to the lower id, renormalised top-k weights) and
+ * output definition as moe_decode_layer, for 1 <= tokens <= 65536:
+ *   out[t] = sum_j w_{t,j} Wd_{e_j} (silu(Wg_{e_j} x_t) * (Wu_{e_j} x_t)).
+ * Gate/up and down run on the tensor cores (bf16 operands that are exact for the int4
+ * codes and the bf16 rows, fp32 accumulation per 32-element block, h' split into bf16
+ * hi + lo), so a token's output equals moe_decode_layer's within the layer tolerance,
+ * not bitwise; it does not depend on the other tokens of the call.
+ * x_bf16 [tokens][H] device, out [tokens][H] fp32 device (both 16-byte aligned);
+ * expert_counts: device int32 [E] receiving the picks per expert, or NULL.
+ * ws: device workspace (16-byte aligned) of at least moe_prefill_workspace_bytes.
+ * The handle's max_rows does not limit tokens.  MOE_EINVAL for bad arguments,
+ * MOE_EWORKSPACE for a short workspace; slot-table entries outside the bank are
+ * reported by moe_last_device_status.  Enqueues 7 kernels and one memset. */
+size_t moe_prefill_workspace_bytes(const moe_dims* dims, int32_t tokens);
+int moe_prefill_layer(moe_handle* h, const moe_layer_w* w, const uint16_t* x_bf16, int32_t tokens,
+                      float* out, int32_t* expert_counts, void* ws, size_t ws_bytes, void* stream);
+
 /* Synchronizes `stream`, reads and clears the handle's device status word.
  * MOE_OK, MOE_ETIMEOUT (a bounded device wait gave up), MOE_EINVAL (a slot table entry
  * was outside [0, n_slots)), or MOE_ECUDA. */
 int moe_last_device_status(moe_handle* h, void* stream);
 
 /* Number of kernel launches the most recent moe_route / moe_decode_layer /
- * moe_round call enqueued (a graph replay counts the kernels inside it). */
+ * moe_round / moe_prefill_layer call enqueued (a graph replay counts the kernels
+ * inside it). */
 int32_t moe_last_launch_count(const moe_handle* h);
 
 /* Bound on every device-side wait of this handle's kernels (default 2 s; 0 restores

@@ -24,7 +24,8 @@ ABI_SYMBOLS = (
     "moe_route", "moe_decode_layer", "moe_round", "moe_last_device_status",
     "moe_last_launch_count", "moe_set_wait_limit_ns", "moe_set_tail_skip", "moe_profile",
     "moe_profile_read",
-    "moe_profile_phases", "moe_decode_layer_noalloc", "moe_strerror",
+    "moe_profile_phases", "moe_decode_layer_noalloc", "moe_prefill_workspace_bytes",
+    "moe_prefill_layer", "moe_strerror",
 )
 MOE_NOALLOC_SCRATCH_BYTES = 4 << 20
 KIND_ROUND = 0
@@ -89,6 +90,10 @@ _lib.moe_profile_phases.restype = ctypes.c_int
 _lib.moe_decode_layer_noalloc.argtypes = [ctypes.POINTER(moe_dims), ctypes.POINTER(moe_layer_w), _vp, _i32,
                                           _vp, _vp, _vp]
 _lib.moe_decode_layer_noalloc.restype = ctypes.c_int
+_lib.moe_prefill_workspace_bytes.argtypes = [ctypes.POINTER(moe_dims), _i32]
+_lib.moe_prefill_workspace_bytes.restype = _sz
+_lib.moe_prefill_layer.argtypes = [_vp, ctypes.POINTER(moe_layer_w), _vp, _i32, _vp, _vp, _vp, _sz, _vp]
+_lib.moe_prefill_layer.restype = ctypes.c_int
 _lib.moe_strerror.argtypes = [ctypes.c_int]
 _lib.moe_strerror.restype = ctypes.c_char_p
 
@@ -154,6 +159,16 @@ def moe_decode_layer(handle: int, w: moe_layer_w, x_bf16: int, rows: int, out: i
                      ws_bytes: int, stream: int) -> None:
     _check(_lib.moe_decode_layer(handle, ctypes.byref(w), x_bf16, int(rows), out, ws, int(ws_bytes),
                                  stream), "moe_decode_layer")
+
+
+def moe_prefill_workspace_bytes(dims: moe_dims, tokens: int) -> int:
+    return int(_lib.moe_prefill_workspace_bytes(ctypes.byref(dims), int(tokens)))
+
+
+def moe_prefill_layer(handle: int, w: moe_layer_w, x_bf16: int, tokens: int, out: int, expert_counts: int,
+                      ws: int, ws_bytes: int, stream: int) -> None:
+    _check(_lib.moe_prefill_layer(handle, ctypes.byref(w), x_bf16, int(tokens), out, expert_counts, ws,
+                                  int(ws_bytes), stream), "moe_prefill_layer")
 
 
 def moe_round(handle: int, layers, x_bf16: int, rows: int, out: int, stats: int, ws: int,

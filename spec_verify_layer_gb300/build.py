@@ -7,8 +7,9 @@ import sys
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
-SOURCES = [os.path.join(HERE, "csrc", f) for f in ("moe_verify.cu", "moe_host.cpp")]
-HEADERS = [os.path.join(HERE, "csrc", "moe_internal.h"), os.path.join(ROOT, "include", "moe_verify.h")]
+SOURCES = [os.path.join(HERE, "csrc", f) for f in ("moe_verify.cu", "moe_prefill.cu", "moe_host.cpp")]
+HEADERS = [os.path.join(HERE, "csrc", f) for f in ("moe_internal.h", "moe_common.cuh")] + [
+    os.path.join(ROOT, "include", "moe_verify.h")]
 OUT = os.path.join(HERE, "libmoeverify.so")
 
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo", "-O3", "-std=c++17",

@@ -33,6 +33,27 @@ WsLayout ws_layout(const moe_dims& d, int rows) {
   return L;
 }
 
+PrefillWs prefill_ws_layout(const moe_dims& d, int tokens) {
+  const size_t T = (size_t)tokens, E = (size_t)d.n_experts, P = T * (size_t)d.top_k;
+  PrefillWs w{};
+  size_t off = 0;
+  w.logits = off;   off += up256(T * E * 4);
+  w.ids = off;      off += up256(P * 4);
+  w.w = off;        off += up256(P * 4);
+  w.counts = off;   off += up256(E * 4);
+  w.offs = off;     off += up256((E + 1) * 4);
+  w.cursor = off;   off += up256(E * 4);
+  w.tiles_gu = off; off += up256((E + 1) * 4);
+  w.tiles_dn = off; off += up256((E + 1) * 4);
+  w.pos_tok = off;  off += up256(P * 4);
+  w.pos_pick = off; off += up256(P * 4);
+  w.pick_pos = off; off += up256(P * 4);
+  w.hbuf = off;     off += up256(P * (size_t)d.inter * 4);
+  w.ybuf = off;     off += up256(P * (size_t)d.hidden * 4);
+  w.total = off;
+  return w;
+}
+
 }  // namespace moe
 
 using namespace moe;
@@ -42,6 +63,11 @@ extern "C" {
 size_t moe_workspace_bytes(const moe_dims* dims, int32_t rows) {
   if (check_dims(dims) != MOE_OK || rows < 1 || rows > dims->max_rows) return 0;
   return ws_layout(*dims, rows).total;
+}
+
+size_t moe_prefill_workspace_bytes(const moe_dims* dims, int32_t tokens) {
+  if (check_dims(dims) != MOE_OK || tokens < 1 || tokens > kMaxPrefillTokens) return 0;
+  return prefill_ws_layout(*dims, tokens).total;
 }
 
 size_t moe_packed_bytes(const moe_dims* dims, int which, int part) {

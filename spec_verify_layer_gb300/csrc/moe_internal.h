@@ -44,6 +44,49 @@ WsLayout ws_layout(const moe_dims& d, int rows);
 // per block) reads a permutation of them, conflict-free.
 MOE_HD inline int block_pos(int b, int key) { return b ^ (key & 7); }
 
+// Prefill-width layer (moe_prefill.cu): tokens per call, device arguments, workspace.
+constexpr int kMaxPrefillTokens = 65536;
+
+struct PrefillArgs {
+  int H, E, k, I, T;
+  const uint16_t* x;  // [T][H] bf16 bits
+  float* out;         // [T][H]
+  const float* router;
+  const uint8_t* gu_nib;
+  const uint16_t* gu_sc;
+  const uint8_t* dn_nib;
+  const uint16_t* dn_sc;
+  const int32_t* slot;  // expert -> bank slot, or null
+  int n_slots;
+  // workspace
+  float* logits;     // [T][E]
+  int* ids;          // [T*k] expert of pick t*k + j (rank order)
+  float* w;          // [T*k] renormalised weight of each pick
+  int* counts;       // [E] picks per expert
+  int* offs;         // [E+1] start of each expert's run of positions
+  int* cursor;       // [E] scatter cursors
+  int* tiles_gu;     // [E+1] prefix of gate/up token tiles per expert
+  int* tiles_dn;     // [E+1] prefix of down token tiles per expert
+  int* pos_tok;      // [T*k] token at each position
+  int* pos_pick;     // [T*k] pick at each position
+  int* pick_pos;     // [T*k] position of each pick
+  uint16_t* hbuf;    // [T*k][I] h' as bf16 hi + lo in the down operand order
+  float* ybuf;       // [T*k][H] down output of each position
+  int* user_counts;  // [E] or null
+  unsigned* status;
+};
+
+// Byte offsets of the prefill workspace regions (each 256-aligned).
+struct PrefillWs {
+  size_t logits, ids, w, counts, offs, cursor, tiles_gu, tiles_dn, pos_tok, pos_pick, pick_pos, hbuf,
+      ybuf, total;
+};
+PrefillWs prefill_ws_layout(const moe_dims& d, int tokens);
+
+// Enqueues the prefill kernels on `stream` (a cudaStream_t); returns a cudaError_t code
+// and the number of kernels launched.
+int prefill_launch(const PrefillArgs& a, int* launches, void* stream);
+
 // Per-expert packed sizes (bytes).
 inline size_t gu_nib_bytes(const moe_dims& d) { return (size_t)d.inter * d.hidden; }
 inline size_t gu_sc_bytes(const moe_dims& d) { return (size_t)d.inter * d.hidden / 8; }
