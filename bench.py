@@ -48,6 +48,15 @@ def parse():
     return ap.parse_args()
 
 
+def peak_bf16():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
 def peak_hbm():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -350,6 +359,12 @@ def run_ours(args):
                          "unique_experts_per_layer": float(np.mean(r["U"])),
                          "tokens_per_round_equiv_per_s": 4 / (msr * 1e-3)}
 
+    # The prefill-width layer (many tokens per call: counting sort by expert, per-expert
+    # GEMMs): PF_T tokens of diverse rows, layers cycling so every call streams distinct
+    # weights; device time over the calls.
+    sweep["prefill"] = prefill_leg(mv, cfg, wl, handle, dev, stream, L, max(10, args.steps // 50),
+                                   max(args.warmup, 3))
+
     # The round is one kernel launch (k_round): its average launch duration is the timed
     # region's per-step time, from CUDA events on the launching stream.  A separate
     # eager pass records where the time goes inside it (device timestamps per phase).
@@ -420,6 +435,51 @@ def run_ours(args):
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+PF_T = 2048
+
+
+def prefill_leg(mv, cfg, wl, handle, dev, stream, L, steps, warmup):
+    import numpy as np
+    import torch
+    import syngen
+    T = PF_T
+    xs = [torch.from_numpy(syngen.rows(cfg, l, T, 1.0).view(np.int16)).to(dev) for l in range(min(L, 4))]
+    out = torch.empty((T, cfg.hidden), dtype=torch.float32, device=dev)
+    counts = torch.zeros(cfg.experts, dtype=torch.int32, device=dev)
+    nbytes = mv.moe_prefill_workspace_bytes(mv.make_dims(cfg.hidden, cfg.experts, cfg.top_k, cfg.inter, 16), T)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    st = stream.cuda_stream
+
+    def call(i):
+        l = i % L
+        mv.moe_prefill_layer(handle, wl[l], xs[l % len(xs)].data_ptr(), T, out.data_ptr(), counts.data_ptr(),
+                             ws.data_ptr(), nbytes, st)
+
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            call(i)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(steps):
+            call(warmup + i)
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    assert mv.moe_last_device_status(handle, st) == mv.MOE_OK
+    us = 1e3 * e0.elapsed_time(e1) / steps
+    U = int((counts.cpu().numpy() > 0).sum())
+    flops = 2.0 * T * cfg.experts * cfg.hidden + 6.0 * T * cfg.top_k * cfg.hidden * cfg.inter
+    byts = layer_bytes(cfg, U, T)
+    peak, src = peak_bf16()
+    tflops = flops / (us * 1e-6) / 1e12
+    return {"workload": f"{T} tokens (rows x0 + 1.0 N(0,1)) of the {cfg.name} layer, one moe_prefill_layer call",
+            "tokens": T, "us_per_layer": us, "tokens_per_s": T / (us * 1e-6), "tflops": tflops,
+            "bf16_peak_tflops": peak, "peak_source": src, "frac_of_bf16_peak": tflops / peak,
+            "alg_flops": flops, "unique_experts": U, "hbm_gbs": byts / (us * 1e-6) / 1e9,
+            "launches_per_call": mv.moe_last_launch_count(handle), "steps": steps}
 
 
 def read_traffic(kernel, layers, rows):
