@@ -372,10 +372,211 @@ struct Tables {
 // units are shared out by work, a unit of an expert with R_e rows costing about
 // ceil(R_e / 2) passes on the fp32 path (rows go two at a time) and ceil(R_e / 16) on
 // the tensor cores (wide != 0); one row is an even split by count.
+// One row without tail skip (E a power of two, 32 <= E <= NT): the whole routing by
+// expert-parallel counting, no sequential rounds.  The rank of expert i is the number of
+// experts that rank before it (larger logit, or equal logit and lower id), counted over
+// quarters of the row by four threads; the k experts of rank < k are the picks (the
+// same set and order as select_row), and a ballot over the experts in id order gives
+// each pick its union index (the union is the k picks, ascending).  T.w[j] receives
+// pick j's logit; softmax_one turns it into the weight.  This CTA's unit range is the
+// even split of the k I units.
+__device__ __forceinline__ bool route_one_ok(const RoundArgs& a) {
+  return a.R == 1 && a.tail_rank == 0 && a.E <= NT && a.E >= 32 && (a.E & (a.E - 1)) == 0;
+}
+
+__device__ __forceinline__ int ranks_before_u(unsigned kj, int j, unsigned ki, int i) {
+  return (kj > ki || (kj == ki && j < i)) ? 1 : 0;
+}
+
+__device__ void route_one(const RoundArgs& a, const Tables& T, unsigned* s_key, int* s_cnt, int* s_wc, int layer,
+                          int* s_range) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, E = a.E, k = a.k;
+  const int lgE = __ffs(E) - 1, QE = E >> 2;
+  if (tid == 0) {
+    const unsigned N = (unsigned)k * (unsigned)a.I, G = gridDim.x, c = blockIdx.x;
+    s_range[0] = (int)((c * N) / G);
+    s_range[1] = (int)(((c + 1) * N) / G);
+  }
+  unsigned ki = 0;
+  if (tid < E) {
+    ki = order_key(__ldcg(a.logits + tid));
+    s_key[tid] = ki;
+  }
+  __syncthreads();
+  for (int task = tid; task < 4 * E; task += NT) {
+    const int q = task >> lgE, i = task & (E - 1), j0 = q * QE;
+    const unsigned kv = s_key[i];
+    const uint4* row = reinterpret_cast<const uint4*>(s_key + j0);
+    int cnt = 0;
+    if (j0 + QE <= i || j0 > i) {
+      // a quarter wholly below i ranks key j before i when kj >= ki, wholly above when
+      // kj > ki (keys of finite logits are >= 1, so kj >= ki is kj > ki - 1)
+      const unsigned th = (j0 > i) ? kv : kv - 1u;
+#pragma unroll 8
+      for (int j4 = 0; j4 < (QE >> 2); ++j4) {
+        const uint4 v = row[j4];
+        cnt += (v.x > th) + (v.y > th) + (v.z > th) + (v.w > th);
+      }
+    } else {
+#pragma unroll 8
+      for (int j4 = 0; j4 < (QE >> 2); ++j4) {
+        const uint4 v = row[j4];
+        const int j = j0 + 4 * j4;
+        cnt += ranks_before_u(v.x, j, kv, i) + ranks_before_u(v.y, j + 1, kv, i) +
+               ranks_before_u(v.z, j + 2, kv, i) + ranks_before_u(v.w, j + 3, kv, i);
+      }
+    }
+    s_cnt[task] = cnt;
+  }
+  __syncthreads();
+  const int rank = (tid < E) ? s_cnt[tid] + s_cnt[E + tid] + s_cnt[2 * E + tid] + s_cnt[3 * E + tid] : k;
+  const bool picked = rank < k;
+  const unsigned b = __ballot_sync(0xffffffffu, picked);
+  if (lane == 0) s_wc[warp] = __popc(b);
+  __syncthreads();
+  int ui = __popc(b & ((1u << lane) - 1u));
+  for (int w = 0; w < warp; ++w) ui += s_wc[w];
+  if (picked && ui < k) {  // (exactly k are picked unless a logit is NaN, which is undefined)
+    T.uni[ui] = tid;
+    T.csr_off[ui] = ui;
+    T.pos_ui[ui] = ui;
+    T.pos_row[ui] = 0;
+    T.pair[ui] = rank;
+    T.pick_pos[rank] = ui;
+    T.w[rank] = key_value(ki);
+    if (blockIdx.x == 0) {
+      if (a.user_ids) a.user_ids[rank] = tid;
+      if (a.user_union) a.user_union[ui] = tid;
+    }
+  }
+  if (tid == 0) {
+    T.csr_off[k] = k;
+    *T.n_union = k;
+    if (blockIdx.x == 0) {
+      if (a.user_nunion) *a.user_nunion = k;
+      if (a.stats) a.stats[layer] = k;
+    }
+  }
+  __syncthreads();
+}
+
+// Weights of route_one's picks (one warp): T.w[j] holds pick j's logit; w_j =
+// exp(l_j - l_1) / sum over the k picks, the same warp sum as the general path.
+__device__ void softmax_one(const RoundArgs& a, const Tables& T) {
+  const int lane = threadIdx.x & 31, k = a.k;
+  const float l = (lane < k) ? T.w[lane] : 0.f;
+  const float l1 = __shfl_sync(0xffffffffu, l, 0);
+  const float ex = (lane < k) ? expf(l - l1) : 0.f;
+  const float den = warp_sum(ex);
+  if (lane < k) {
+    const float w = __fdiv_rn(ex, den);
+    T.w[lane] = w;
+    if (blockIdx.x == 0 && a.user_w) a.user_w[lane] = w;
+  }
+}
+
+// Union, CSR tables and this CTA's unit range for rounds of at most 32 picks (no tail
+// skip), by one warp: the picks, keyed (expert, row), are sorted across the lanes
+// (bitonic network over xor partners); a pick that starts a run of one expert opens a
+// union entry, and the ballot of those gives every pick its union index.  Same tables
+// and the same unit cut as the general scan below.  s_ids holds the picks' experts.
+__device__ void route_small(const RoundArgs& a, const Tables& T, const int* s_ids, int layer, int wide,
+                            int* s_range) {
+  const int lane = threadIdx.x & 31, k = a.k, P = a.R * k;
+  constexpr unsigned FULL = 0xffffffffu;
+  const bool live = lane < P;
+  unsigned key = live ? ((unsigned)s_ids[lane] << 5) | (unsigned)(lane / k) : FULL;
+  int pick = lane;
+  // the network over the first NS lanes (NS = the power of two >= P) sorts them
+  const int NS = P <= 8 ? 8 : (P <= 16 ? 16 : 32);
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+    if (size > NS) break;
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const unsigned ok = __shfl_xor_sync(FULL, key, stride);
+      const int op = __shfl_xor_sync(FULL, pick, stride);
+      const bool keep_min = ((lane & size) == 0) == ((lane & stride) == 0);
+      const bool sw = keep_min ? (ok < key) : (ok > key);
+      key = sw ? ok : key;
+      pick = sw ? op : pick;
+    }
+  }
+  const int e = (int)(key >> 5), r = (int)(key & 31u);
+  const unsigned prev = __shfl_up_sync(FULL, key, 1);
+  const bool first = live && (lane == 0 || (prev >> 5) != (key >> 5));
+  const unsigned fb = __ballot_sync(FULL, first);
+  const int U = __popc(fb);
+  const unsigned le = (lane == 31) ? FULL : ((2u << lane) - 1u);
+  const int ui = __popc(fb & le) - 1;
+  if (live) {
+    T.pos_ui[lane] = ui;
+    T.pos_row[lane] = r;
+    T.pair[lane] = pick;
+    T.pick_pos[pick] = lane;
+  }
+  if (first) {
+    T.uni[ui] = e;
+    T.csr_off[ui] = lane;
+    if (blockIdx.x == 0 && a.user_union) a.user_union[ui] = e;
+  }
+  if (lane == 0) {
+    T.csr_off[U] = P;
+    *T.n_union = U;
+    if (blockIdx.x == 0) {
+      if (a.user_nunion) *a.user_nunion = U;
+      if (a.stats) a.stats[layer] = U;
+    }
+  }
+  const int G = gridDim.x, c = blockIdx.x;
+  if (a.R == 1) {
+    const unsigned N = (unsigned)U * (unsigned)a.I;
+    if (lane == 0) {
+      s_range[0] = (int)((c * N) / (unsigned)G);
+      s_range[1] = (int)(((c + 1) * N) / (unsigned)G);
+    }
+    return;
+  }
+  __syncwarp();
+  // union expert u = lane: its rows R_e and work weight, prefix over the union
+  int wu = 0;
+  if (lane < U) {
+    const int re = T.csr_off[lane + 1] - T.csr_off[lane];
+    wu = wide ? (re + 15) >> 4 : (re + 1) >> 1;
+  }
+  const int lw = a.I * wu;
+  int incw = lw;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int tw = __shfl_up_sync(FULL, incw, o);
+    if (lane >= o) incw += tw;
+  }
+  const int wt_total = __shfl_sync(FULL, incw, 31), basew = incw - lw;
+  const float wg = (float)wt_total / (float)G;
+  const int tgt[2] = {c == 0 ? 0 : min((int)(wg * (float)c), wt_total),
+                      c + 1 == G ? wt_total : min((int)(wg * (float)(c + 1)), wt_total)};
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const bool here = lane < U && tgt[q] >= basew && tgt[q] < incw;
+    const unsigned owner = __ballot_sync(FULL, here);
+    int res = U * a.I;
+    if (owner) res = __shfl_sync(FULL, lane * a.I + (tgt[q] - basew) / max(wu, 1), __ffs(owner) - 1);
+    if (lane == 0) s_range[q] = res;
+  }
+}
+
 __device__ int route_phase(const RoundArgs& a, const Tables& T, unsigned* s_mask, int* s_off_e,
                            int* s_ids, int* s_ui, int* s_rank, int layer, int wide, int* s_range) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int E = a.E, k = a.k, R = a.R;
+  const bool small = R * k <= 32 && a.tail_rank == 0;
+  // route_one's scratch: keys [E] (16-byte aligned: read as uint4), counts [4 E], warp sums
+  unsigned* s_key = reinterpret_cast<unsigned*>((reinterpret_cast<uintptr_t>(s_rank + E) + 15) & ~(uintptr_t)15);
+  if (route_one_ok(a)) {  // (weights: softmax_one, by the caller)
+    route_one(a, T, s_key, reinterpret_cast<int*>(s_key + NT), reinterpret_cast<int*>(s_key + 5 * NT), layer,
+              s_range);
+    return k;
+  }
   // rows: top-k, renormalised weights, row bits of each picked expert
   for (int r = warp; r < R; r += NW) {
     float my_l = 0.f;
@@ -393,7 +594,7 @@ __device__ int route_phase(const RoundArgs& a, const Tables& T, unsigned* s_mask
       const int p = r * k + lane;
       s_ids[p] = my_id;
       T.w[p] = wj;
-      atomicOr(&s_mask[my_id], 1u << r);
+      if (!small) atomicOr(&s_mask[my_id], 1u << r);
       if (a.tail_rank > 0) atomicMin(&s_rank[my_id], lane);
       if (blockIdx.x == 0) {
         if (a.user_ids) a.user_ids[p] = my_id;
@@ -402,6 +603,11 @@ __device__ int route_phase(const RoundArgs& a, const Tables& T, unsigned* s_mask
     }
   }
   __syncthreads();
+  if (small) {
+    if (warp == 0) route_small(a, T, s_ids, layer, wide, s_range);
+    __syncthreads();
+    return *T.n_union;
+  }
   // one warp: exclusive scans over e of (picked ? 1 : 0) and popc(mask) give the union
   // index and the CSR offset of every picked expert (lane l owns a contiguous range)
   if (warp == 0) {
@@ -1243,7 +1449,11 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
     int* s_range = reinterpret_cast<int*>(smem + P.chunks + kGuSlots * 12 + 20);
     const int U = route_phase(a, T, s_mask, s_off_e, s_ids, s_ui, s_rank, l, mma ? 1 : 0, s_range);
     stamp(a, l, 3);
-    if (a.route_only) return;
+    const bool one = route_one_ok(a);  // the picks' weights are still to be computed
+    if (a.route_only) {
+      if (one && warp == 1) softmax_one(a, T);
+      return;
+    }
     // ---- this CTA's share of the gate/up units (cut during routing); chunks issued
     // through the ring: thread 0 cuts them lazily (stopping at expert boundaries and the
     // slot size) and leaves the descriptor of chunk n in ring entry n % kGuSlots when it
@@ -1287,12 +1497,16 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
       }
       for (int q = 0; q < kGuSlots && q < nc; ++q) s_chunks[q] = next_chunk();
       *reinterpret_cast<int*>(smem + P.chunks + kGuSlots * 12) = nc;
+      // the first chunk goes out at once (thread 0 is its only issuer)
+      static_assert(kGuFirst == 1, "thread 0 issues the first chunk");
+      if (nc > 0) issue_gu_chunk(a, W, T, gu, smem_u32(bars), s_chunks[0]);
+    } else if (one && warp == 1) {
+      softmax_one(a, T);  // meanwhile
     }
     __syncthreads();
     const int n_chunks = *reinterpret_cast<const int*>(smem + P.chunks + kGuSlots * 12);
     const int n_first = min(kGuFirst, n_chunks), n_ring = min(kGuSlots, n_chunks);
     gu_pend |= (1u << n_first) - 1u;
-    if (tid < n_first) issue_gu_chunk(a, W, T, gu + tid * P.gu_slot, smem_u32(bars + tid), s_chunks[tid]);
     // the down prefetch goes out once the first gate/up chunk has landed, so it does not
     // delay that chunk (it is needed only after B2)
     auto issue_dn_prefetch = [&]() {
