@@ -1081,10 +1081,12 @@ __device__ __forceinline__ void down_position(const RoundArgs& a, const uint8_t*
   const uint8_t* codes = dslot;
   const uint16_t* scales = reinterpret_cast<const uint16_t*>(dslot + codes_room);
   const f2_t* hps[1] = {hp};
-  for (int ob = ob0; ob < ob1; ob += 4) {
-    float part[4];
+  // rows in groups of DG, one multi-value reduction per group
+  constexpr int DG = 8;
+  for (int ob = ob0; ob < ob1; ob += DG) {
+    float part[DG];
 #pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
+    for (int jj = 0; jj < DG; ++jj) {
       part[jj] = 0.f;
       const int ol = ob + jj;
       if (lane < NBI && ol < ob1) {
@@ -1096,8 +1098,9 @@ __device__ __forceinline__ void down_position(const RoundArgs& a, const uint8_t*
         part[jj] = __fmul_rn(sc, __fmaf_rn(dot[0], 0x1p62f, hsum8));
       }
     }
-    const float y = warp_sum_multi<4>(part, lane);
-    if ((lane & 7) == 0 && ob + (lane >> 3) < ob1) s_yw[ob + (lane >> 3)] = y;
+    const float y = warp_sum_multi<DG>(part, lane);
+    constexpr int LPV = 32 / DG;
+    if ((lane % LPV) == 0 && ob + lane / LPV < ob1) s_yw[ob + lane / LPV] = y;
   }
 }
 
