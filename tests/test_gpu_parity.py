@@ -16,7 +16,7 @@ pytestmark = pytest.mark.gpu
 
 SHAPES = ["tiny", "a3b_r1", "e512_r3"]   # distinct layer shapes (a3b_r4 / a3b_r16 share a3b_r1's)
 ROWS = {"tiny": [(1, 0.0), (3, 0.5), (4, 0.5)], "a3b_r1": [(1, 0.0), (4, 0.5), (16, 0.1)],
-        "e512_r3": [(3, 0.5)]}
+        "e512_r3": [(1, 0.0), (1, 1.0), (3, 0.5)]}
 
 
 @pytest.fixture(scope="module", params=SHAPES)
@@ -174,6 +174,37 @@ def test_forced_router_ties_pick_lower_id():
         got = run_layer(s, 0, xb)
         ref = oracle.layer(router, xb, cfg.top_k, np.arange(8), syngen.experts_stacked(cfg, 0, range(8)))
         assert_close(got, ref, "ties")
+    finally:
+        s.close()
+
+
+def test_one_row_counting_path_ties_pick_lower_id():
+    """One-row rounds rank the experts by counting (E a power of two >= 32): three
+    experts with identical router rows tie at the top for the row and must come out in
+    id order, the same as the oracle, and the row's output must equal the same row's
+    inside a three-row round (which takes the selection-rounds path) bit for bit."""
+    cfg = syngen.CONFIGS["tiny"].with_(experts=64, top_k=4)
+    s = Stack(cfg, n_layers=1)
+    try:
+        xb = s.rows(0, 3, 0.5)
+        x0 = np.array([oracle.bf16_to_float(int(v)) for v in xb[0]], dtype=np.float32)
+        router = syngen.router(cfg, 0).copy()
+        router[40] = 0.05 * x0      # far above every other logit of row 0
+        router[3] = router[40]
+        router[10] = router[40]
+        router[50] = router[20]     # a tie lower down
+        s.layers[0].router.copy_(torch.from_numpy(router))
+        ids, w, uni = run_route(s, 0, xb[:1].copy())
+        rt = oracle.route(router, xb[:1], cfg.top_k)
+        np.testing.assert_array_equal(ids, rt.ids)
+        np.testing.assert_array_equal(uni, rt.union)
+        assert list(ids[0][:3]) == [3, 10, 40]
+        assert np.abs(w - rt.w).max() <= TOL_W
+        alone = run_layer(s, 0, xb[:1].copy())
+        full = run_layer(s, 0, xb)
+        np.testing.assert_array_equal(alone[0], full[0])
+        ref = oracle.layer(router, xb[:1], cfg.top_k, rt.union, syngen.experts_stacked(cfg, 0, rt.union))
+        assert_close(alone, ref, "one-row ties")
     finally:
         s.close()
 
