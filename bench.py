@@ -305,6 +305,41 @@ def run_ours(args):
                 "launches_per_round": launches_per_round, "t_wall": (t_wall0, t_wall1),
                 "x": x, "out": out, "xs": xs}
 
+    def round_percentiles(rows, x, out, n):
+        """Per-replay device times of the round graph (an event pair around each replay,
+        outside the timed region): p10 / p50 / p90 in us per round."""
+        stats_q = torch.zeros(L, dtype=torch.int32, device=dev)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        with torch.cuda.stream(stream):
+            for a0, a1 in evs:
+                a0.record(stream)
+                mv.moe_round(handle, wl, x.data_ptr(), rows, out.data_ptr(), stats_q.data_ptr(), ws.data_ptr(),
+                             ws.numel(), True, st)
+                a1.record(stream)
+        torch.cuda.synchronize(dev)
+        t = sorted(1e3 * a0.elapsed_time(a1) for a0, a1 in evs)
+        return {"p10": t[n // 10], "p50": t[n // 2], "p90": t[(9 * n) // 10], "replays": n}
+
+    def single_layers(rows, x, out, n):
+        """One moe_decode_layer launch per layer, rotating over the L distinct layers
+        (eager, stream-ordered): us per layer, for the fused round's launch saving."""
+        with torch.cuda.stream(stream):
+            for l in range(L):
+                mv.moe_decode_layer(handle, wl[l], x[l].data_ptr(), rows, out[l].data_ptr(), ws.data_ptr(),
+                                    ws.numel(), st)
+        torch.cuda.synchronize(dev)
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a0.record(stream)
+            for i in range(n):
+                l = i % L
+                mv.moe_decode_layer(handle, wl[l], x[l].data_ptr(), rows, out[l].data_ptr(), ws.data_ptr(),
+                                    ws.numel(), st)
+            a1.record(stream)
+        torch.cuda.synchronize(dev)
+        assert mv.moe_last_device_status(handle, st) == mv.MOE_OK
+        return {"us_per_layer": 1e3 * a0.elapsed_time(a1) / n, "launches": n}
+
     def profile_phases(rows, x, out, n_rounds):
         """Eager rounds with per-phase device timestamps (outside every timed region)."""
         stats_p = torch.zeros(L, dtype=torch.int32, device=dev)
@@ -402,12 +437,16 @@ def run_ours(args):
     achieved = alg_per_launch / (avg_launch_us * 1e-6) / 1e9
     prof_rounds = max(3, min(20, args.steps // 50))
     phases, eager_ms, eager_n = profile_phases(R0, x1, out1, prof_rounds)
+    pct = round_percentiles(R0, x1, out1, max(20, min(200, args.steps // 10)))
+    single = single_layers(R0, x1, out1, max(L, min(4 * L, args.steps)))
     roofline = {"bound": "hbm", "kernel": "k_round", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": read_traffic("k_round", L, R0), "peak_source": peak_src,
                 "alg_bytes_per_launch": alg_per_launch, "avg_launch_us": avg_launch_us,
                 "launch": f"one cooperative launch per {L}-layer round, timed over {args.steps} graph replays",
                 "phases_per_layer_us": phases,
-                "eager_round_us": 1e3 * eager_ms / max(eager_n, 1)}
+                "eager_round_us": 1e3 * eager_ms / max(eager_n, 1),
+                "round_us_percentiles": pct,
+                "single_layer_launches": single}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
