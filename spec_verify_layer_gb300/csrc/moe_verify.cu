@@ -908,9 +908,10 @@ __device__ __forceinline__ void load_xblock(const RoundArgs& a, const uint16_t* 
   if (XS) {
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
-      const float4 f = s_xp[((size_t)row * 8 + c) * NB + blk];
-      xp[2 * c] = f2pack(f.x, f.y);
-      xp[2 * c + 1] = f2pack(f.z, f.w);
+      // a float4 of pairs is two f32x2 operands as stored: load them as such
+      const ulonglong2 f = *reinterpret_cast<const ulonglong2*>(s_xp + ((size_t)row * 8 + c) * NB + blk);
+      xp[2 * c] = f.x;
+      xp[2 * c + 1] = f.y;
     }
     xsum8 = s_xs[row * NB + blk];
   } else {
@@ -1060,9 +1061,9 @@ __device__ __forceinline__ void down_position(const RoundArgs& a, const uint8_t*
   if (lane < NBI) {
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
-      const float4 f = s_h[c * NBI + lane];
-      hp[2 * c] = f2pack(f.x, f.y);
-      hp[2 * c + 1] = f2pack(f.z, f.w);
+      const ulonglong2 f = *reinterpret_cast<const ulonglong2*>(s_h + c * NBI + lane);
+      hp[2 * c] = f.x;
+      hp[2 * c + 1] = f.y;
     }
     // -8 x the block sum of h', undoing each slot's power-of-two factor exactly
     float sum = 0.f;
