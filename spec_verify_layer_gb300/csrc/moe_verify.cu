@@ -369,8 +369,9 @@ struct Tables {
 // best 1-based rank over the rows that picked it is >= T leaves the union; its picks
 // are not evaluated and the other weights are not renormalised.
 // It also cuts this CTA's share of the gate/up units into s_range[0..1] (first, end):
-// units are shared out by work, a unit of an expert with R_e rows costing about
-// ceil(R_e / 2) passes on the fp32 path (rows go two at a time) and ceil(R_e / 16) on
+// units are shared out by work, a unit of an expert with R_e rows weighing 2 + 2 R_e on
+// the fp32 path (a fixed share for the weight stream plus the per-row FMA work; the
+// measured chunk times at 1, 2 and 4 rows go about 1 : 1.4 : 2.7) and ceil(R_e / 16) on
 // the tensor cores (wide != 0); one row is an even split by count.
 // One row without tail skip (E a power of two, 32 <= E <= NT): the whole routing by
 // expert-parallel counting, no sequential rounds.  The rank of expert i is the number of
@@ -542,7 +543,7 @@ __device__ void route_small(const RoundArgs& a, const Tables& T, const int* s_id
   int wu = 0;
   if (lane < U) {
     const int re = T.csr_off[lane + 1] - T.csr_off[lane];
-    wu = wide ? (re + 15) >> 4 : (re + 1) >> 1;
+    wu = wide ? (re + 15) >> 4 : 2 + 2 * re;
   }
   const int lw = a.I * wu;
   int incw = lw;
@@ -613,7 +614,7 @@ __device__ int route_phase(const RoundArgs& a, const Tables& T, unsigned* s_mask
   if (warp == 0) {
     const int per = (E + 31) >> 5;  // <= 16
     const int e0 = lane * per, e1 = min(e0 + per, E);
-    auto weight = [&](unsigned m) { const int re = __popc(m); return wide ? (re + 15) >> 4 : (re + 1) >> 1; };
+    auto weight = [&](unsigned m) { const int re = __popc(m); return wide ? (re + 15) >> 4 : 2 + 2 * re; };
     int lf = 0, lc = 0, lw = 0;
     for (int e = e0; e < e1; ++e) {
       unsigned m = s_mask[e];
