@@ -11,12 +11,13 @@
 //       renormalised weights, the ascending expert union U and, per union expert,
 //       the (row, rank) pairs that picked it (CSR).
 //   P3  gate/up: the U * I units (gate row i + up row i of a union expert) are split
-//       evenly and contiguously across CTAs and streamed through shared-memory slots
-//       with 1-D bulk TMA copies; a warp takes two units at a time for two rows of
-//       the expert at a time and stores h' = w silu(g) v (w the row's routing weight)
+//       contiguously across CTAs by work and streamed through shared-memory slots
+//       with 1-D bulk TMA copies; a warp takes one unit of a chunk, for two rows of
+//       the expert at a time, and stores h' = w silu(g) v (w the row's routing weight)
 //       to the workspace, already in the operand layout the down pass consumes.
 //       Meanwhile the down rows of every union expert for this CTA's share of the
-//       output rows are prefetched.
+//       output rows are prefetched, issued by a warp left without a unit in the first
+//       chunk.
 //   B2  (every h' written)
 //   P4  down: the h' rows come back by bulk copy in waves of up to 8 CSR positions,
 //       one warp per position over all of this CTA's output rows o: y = Wd[o] . h'.
@@ -1047,6 +1048,60 @@ __device__ __forceinline__ void gateup_chunk(const RoundArgs& a, const Tables& T
   }
 }
 
+// Gate/up of one staged chunk when the round has one row: the operand pairs of each
+// lane's first block of the row (xr) stay in registers for the whole layer, so a unit
+// reads only its codes, scales and the second block's pairs from shared memory (both
+// blocks in registers would not fit beside the rest of the kernel).  Same operations in
+// the same order as gateup_unit with one row, so the results are the same bits.
+template <int NBL>
+__device__ __forceinline__ void gateup_chunk_r1(const RoundArgs& a, const Tables& T, const uint8_t* slot,
+                                                const GuChunk& c, const f2_t (&xr)[16], const float4* s_xp,
+                                                const float* s_xs) {
+  const int H = a.H, NB = H >> 5;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int pp = T.csr_off[c.ui];
+  const uint8_t* codes = slot;
+  const uint16_t* scales = reinterpret_cast<const uint16_t*>(slot + (size_t)c.n * H);
+  for (int t = warp; t < c.n; t += NW) {
+    float v[2] = {0.f, 0.f};
+    const int sw = (c.i0 + t) & 7;
+#pragma unroll
+    for (int tb = 0; tb < NBL; ++tb) {
+      const int blk = lane + 32 * tb;
+      if (blk < NB) {
+        f2_t xq[16];
+        float xs;
+        if (tb == 0) {
+#pragma unroll
+          for (int m = 0; m < 16; ++m) xq[m] = xr[m];
+          xs = s_xs[blk];
+        } else {
+          load_xblock<true>(a, nullptr, s_xp, s_xs, 0, blk, xq, xs);
+        }
+        const f2_t* xps[1] = {xq};
+#pragma unroll
+        for (int wrow = 0; wrow < 2; ++wrow) {
+          const size_t w = (size_t)(t * 2 + wrow) * NB + (blk ^ sw);
+          const uint4 nb = *reinterpret_cast<const uint4*>(codes + w * 16);
+          const float sc = half_bits(scales[w]);
+          float dot[1];
+          block_dot<1>(nb, xps, dot);
+          v[wrow] = __fmaf_rn(sc, __fmaf_rn(dot[0], 0x1p62f, xs), v[wrow]);
+        }
+      }
+    }
+    const float s = warp_sum_multi<2>(v, lane);
+    const float up = __shfl_down_sync(0xffffffffu, s, 16);
+    if (lane == 0) {
+      const int i = c.i0 + t, j = i & 31;
+      const int pair = T.pair[pp];
+      const float hh = __fmul_rn(__fdiv_rn(s, __fadd_rn(1.f, expf(-s))), up);
+      const float hw = __fmul_rn(T.w[pair], hh);
+      a.hbuf[(size_t)pp * a.I + pair_index(i >> 5, j, a.I >> 5)] = hw * slot_scale(j & 7);
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------------
 // P4: this CTA's output rows [o0, o0 + no), a wave of CSR positions at a time
 
@@ -1466,11 +1521,14 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
     // thread 0's chunk cursor lives in shared memory (cur, end, expert, offset), so no
     // thread carries it in registers through the gate/up loop
     int* s_cursor = reinterpret_cast<int*>(smem + P.chunks + kGuSlots * 12 + 4);
-    auto next_chunk = [&]() {
+    // on the CUDA-core path the first chunk leaves the last warp without a unit: that
+    // warp issues the rest of the ring and the down prefetch while the others compute
+    const int cap0 = mma ? P.gu_cap : min(P.gu_cap, NW - 1);
+    auto next_chunk = [&](int cap) {
       int cur = s_cursor[0], ui = s_cursor[2], i0 = s_cursor[3];
       int nn = s_cursor[1] - cur;
       if (nn > a.I - i0) nn = a.I - i0;
-      if (nn > P.gu_cap) nn = P.gu_cap;
+      if (nn > cap) nn = cap;
       const GuChunk ch{ui, i0, nn};
       cur += nn;
       i0 += nn;
@@ -1496,11 +1554,12 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
       for (int cur = g_cur, i0 = s_cursor[3]; cur < g_end; ++nc) {
         int nn = g_end - cur;
         if (nn > a.I - i0) nn = a.I - i0;
-        if (nn > P.gu_cap) nn = P.gu_cap;
+        const int cap = nc == 0 ? cap0 : P.gu_cap;
+        if (nn > cap) nn = cap;
         cur += nn;
         i0 = (i0 + nn == a.I) ? 0 : i0 + nn;
       }
-      for (int q = 0; q < kGuSlots && q < nc; ++q) s_chunks[q] = next_chunk();
+      for (int q = 0; q < kGuSlots && q < nc; ++q) s_chunks[q] = next_chunk(q == 0 ? cap0 : P.gu_cap);
       *reinterpret_cast<int*>(smem + P.chunks + kGuSlots * 12) = nc;
       // the first chunk goes out at once (thread 0 is its only issuer)
       static_assert(kGuFirst == 1, "thread 0 issues the first chunk");
@@ -1514,11 +1573,12 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
     gu_pend |= (1u << n_first) - 1u;
     // the down prefetch goes out once the first gate/up chunk has landed, so it does not
     // delay that chunk (it is needed only after B2)
+    const int iss = mma ? 0 : NT - 32;  // first thread of the issuing warp
     auto issue_dn_prefetch = [&]() {
       if (no > 0) {
         const int nq = min(U, kDnSlots);
         dn_pend |= (1u << nq) - 1u;
-        if (tid == 0) {
+        if (tid == iss) {
 #pragma unroll 1
           for (int q = 0; q < nq; ++q)
             issue_dn_chunk(a, W, T, dn + q * P.dn_slot, smem_u32(bars + bar_dn0 + q), q, o0, no, codes_room);
@@ -1526,34 +1586,63 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
       }
     };
     // ---- gate/up ----
-    for (int n = 0; n < n_chunks; ++n) {
-      const int q = n % kGuSlots;
-      if (!wait_all(q, gu_ph, gu_pend, q)) return;
-      if (n == 0) {
-        stamp(a, l, 4);
-        gu_pend |= ((1u << n_ring) - 1u) & ~((1u << n_first) - 1u);
-        if (tid >= n_first && tid < n_ring)
-          issue_gu_chunk(a, W, T, gu + tid * P.gu_slot, smem_u32(bars + tid), s_chunks[tid]);
-        issue_dn_prefetch();
-      }
-      stamp(a, l, 5);  // (the last chunk's stamp stays)
-      const GuChunk c = s_chunks[q];
-      const uint8_t* slot = gu + q * P.gu_slot;
-      if (mma)
-        gateup_chunk_mma(a, T, slot, c, x, s_mpart);
-      else if (x_staged)
-        gateup_chunk<NBL, true>(a, T, slot, c, x, s_xp, s_xs);
-      else
-        gateup_chunk<NBL, false>(a, T, slot, c, x, s_xp, s_xs);
-      __syncthreads();  // slot q free again
-      if (n + kGuSlots < n_chunks) {
-        gu_pend |= 1u << q;
-        if (tid == 0) {
-          s_chunks[q] = next_chunk();
-          issue_gu_chunk(a, W, T, gu + q * P.gu_slot, smem_u32(bars + q), s_chunks[q]);
+    auto gu_loop = [&](auto&& compute) -> bool {
+      for (int n = 0; n < n_chunks; ++n) {
+        const int q = n % kGuSlots;
+        if (!wait_all(q, gu_ph, gu_pend, q)) return false;
+        if (n == 0) {
+          stamp(a, l, 4);
+          gu_pend |= ((1u << n_ring) - 1u) & ~((1u << n_first) - 1u);
+          const int qi = tid - iss;
+          if (qi >= n_first && qi < n_ring)
+            issue_gu_chunk(a, W, T, gu + qi * P.gu_slot, smem_u32(bars + qi), s_chunks[qi]);
+          issue_dn_prefetch();
+        }
+        stamp(a, l, 5);  // (the last chunk's stamp stays)
+        const GuChunk c = s_chunks[q];
+        const uint8_t* slot = gu + q * P.gu_slot;
+        compute(slot, c);
+        __syncthreads();  // slot q free again
+        if (n + kGuSlots < n_chunks) {
+          gu_pend |= 1u << q;
+          if (tid == 0) {
+            s_chunks[q] = next_chunk(P.gu_cap);
+            issue_gu_chunk(a, W, T, gu + q * P.gu_slot, smem_u32(bars + q), s_chunks[q]);
+          }
         }
       }
+      return true;
+    };
+    bool gu_ok;
+    if (!mma && x_staged && a.R == 1) {
+      // one row: the lane's first block of activation pairs lives in registers
+      const int NB = a.H >> 5, lane = tid & 31;
+      f2_t xr[16];
+      if (lane < NB) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const ulonglong2 f = *reinterpret_cast<const ulonglong2*>(s_xp + (size_t)c * NB + lane);
+          xr[2 * c] = f.x;
+          xr[2 * c + 1] = f.y;
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) xr[c] = 0ull;
+      }
+      gu_ok = gu_loop([&](const uint8_t* slot, const GuChunk& c) {
+        gateup_chunk_r1<NBL>(a, T, slot, c, xr, s_xp, s_xs);
+      });
+    } else {
+      gu_ok = gu_loop([&](const uint8_t* slot, const GuChunk& c) {
+        if (mma)
+          gateup_chunk_mma(a, T, slot, c, x, s_mpart);
+        else if (x_staged)
+          gateup_chunk<NBL, true>(a, T, slot, c, x, s_xp, s_xs);
+        else
+          gateup_chunk<NBL, false>(a, T, slot, c, x, s_xp, s_xs);
+      });
     }
+    if (!gu_ok) return;
     if (n_chunks == 0) {
       stamp(a, l, 4);
       stamp(a, l, 5);
