@@ -423,6 +423,19 @@ def run_ours(args):
                          "unique_experts_per_layer": float(np.mean(r["U"])),
                          "tokens_per_round_equiv_per_s": 4 / (msr * 1e-3)}
 
+    # The price of a verify column: rounds of R = 1..16 rows on the same 40-layer stack
+    # (the draft rows at sigma 0.5 around the first row, as for 4 rows), a short timing
+    # each; R <= 7 runs on the CUDA cores, R >= 8 on the tensor cores.
+    by_rows = {}
+    for rows in range(1, 17):
+        r = time_rounds(rows, 0.0 if rows == 1 else 0.5, max(20, args.steps // 40), max(args.warmup, 3))
+        msr = r["ms_total"] / r["steps"]
+        gbs = r["bytes_per_round"] / (msr * 1e-3) / 1e9
+        by_rows[str(rows)] = {"us_per_layer": round(1e3 * msr / L, 3), "hbm_gbs": round(gbs, 1),
+                              "unique_experts_per_layer": round(float(np.mean(r["U"])), 3)}
+    sweep["rows_sweep"] = {"workload": "a3b layers, R = 1..16 rows, draft rows at sigma 0.5",
+                           "by_rows": by_rows}
+
     # The prefill-width layer (many tokens per call: counting sort by expert, per-expert
     # GEMMs): PF_T tokens of diverse rows, layers cycling so every call streams distinct
     # weights; device time over the calls.
