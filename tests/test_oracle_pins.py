@@ -182,6 +182,27 @@ def test_single_expert_is_plain_swiglu_mlp():
     np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
 
 
+def test_one_hot_row_and_single_codes_closed_form():
+    """A one-hot row meeting one nonzero gate code, one up code and one down code: the
+    layer reduces to one product chain, out[o] = sd * qd * silu(sg * qg * a) * (su * qu * a),
+    and every other output is exactly zero (silu(0) * 0)."""
+    rng = np.random.default_rng(5)
+    H, I = 256, 64
+    j0, i0, o0, a = 77, 41, 200, 1.5
+    ew = _rand_experts(rng, 1, H, I, zero=True)
+    ew.qg[0, i0, j0], ew.sg[0, i0, j0 // 32] = 3, f16(0.25)
+    ew.qu[0, i0, j0], ew.su[0, i0, j0 // 32] = -2, f16(0.5)
+    ew.qd[0, o0, i0], ew.sd[0, o0, i0 // 32] = 5, f16(0.125)
+    row = np.zeros(H, np.uint16)
+    row[j0] = bf16(a)
+    out = oracle.layer(np.zeros((1, H), np.float32), row[None, :], 1, [0], ew)
+    g, v = 0.25 * 3 * a, 0.5 * -2 * a
+    want = 0.125 * 5 * silu(g) * v
+    assert abs(out[0, o0] - want) <= 1e-12 * abs(want)
+    rest = np.delete(out[0], o0)
+    assert (rest == 0).all()
+
+
 def test_expert_ffn_matches_single_expert_layer():
     rng = np.random.default_rng(21)
     H, I = 128, 64
