@@ -29,8 +29,12 @@ ABI_SYMBOLS = (
 )
 MOE_NOALLOC_SCRATCH_BYTES = 4 << 20
 KIND_ROUND = 0
-PHASES = ("router", "barrier1", "routing", "first_data", "gateup_stream", "gateup_tail",
-          "barrier2", "down_wait", "down_stream", "down_tail", "out_write", "barrier3")
+# phase intervals of a profiled moe_round, by the kernel that ran it (the library returns
+# how many it wrote): the split kernel (rows below 8) and the tensor-core kernel
+PHASES_SPLIT = ("finish_router", "barrier1", "routing", "first_data", "units_before_last", "last_unit",
+                "barrier3")
+PHASES_WIDE = ("router", "barrier1", "routing", "first_data", "gateup_stream", "gateup_tail",
+               "barrier2", "h_wait", "down", "down_tail", "out_write", "barrier3")
 
 
 class moe_dims(ctypes.Structure):
@@ -209,11 +213,14 @@ def moe_profile_read(handle: int, kind: int):
 
 def moe_profile_phases(handle: int):
     """Per-phase device time of the last profiled eager moe_round: {phase: (mean_us, max_us)}."""
-    n = len(PHASES)
+    n = len(PHASES_WIDE)
     mean = (ctypes.c_double * n)()
     mx = (ctypes.c_double * n)()
-    _check(_lib.moe_profile_phases(handle, mean, mx, n), "moe_profile_phases")
-    return {p: (mean[i], mx[i]) for i, p in enumerate(PHASES)}
+    got = int(_lib.moe_profile_phases(handle, mean, mx, n))
+    if got < 0:
+        _check(got, "moe_profile_phases")
+    names = PHASES_SPLIT if got == len(PHASES_SPLIT) else PHASES_WIDE
+    return {p: (mean[i], mx[i]) for i, p in enumerate(names[:got])}
 
 
 def moe_decode_layer_noalloc(dims: moe_dims, w: moe_layer_w, x_bf16: int, rows: int, out: int,

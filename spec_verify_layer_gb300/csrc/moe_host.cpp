@@ -29,6 +29,7 @@ WsLayout ws_layout(const moe_dims& d, int rows) {
   L.ctrl = off;     off += 256;
   L.logits = off;   off += up256(R * E * 4);
   L.hbuf = off;     off += up256(R * k * (size_t)d.inter * 4);
+  L.acc = off;      off += up256((size_t)kAccCopies * R * (size_t)d.hidden * 8);
   L.total = off;
   return L;
 }
@@ -118,17 +119,17 @@ int moe_pack_q4(const moe_dims* dims, int which, int32_t n_experts, const int8_t
     return MOE_OK;
   }
   if (which == MOE_DOWN) {
-    // [E][H][I/32 blocks][16 B], scales [E][H][I/32]; block b of row o at block_pos(b, o)
+    // block-major: codes [E][I/32 blocks][H rows][16 B], scales [E][I/32][H]; block b of
+    // every output row of an expert is one contiguous run of H blocks
     for (size_t e = 0; e < (size_t)n_experts; ++e) {
       uint8_t* nib = nib_out + e * dn_nib_bytes(*dims);
       uint16_t* sc = scale_out + e * (dn_sc_bytes(*dims) / 2);
       const int8_t* q = q_a + e * H * I;
       const uint16_t* sv = s_a + e * H * NBI;
-      for (size_t o = 0; o < H; ++o)
-        for (size_t b = 0; b < NBI; ++b) {
-          const size_t pb = (size_t)block_pos((int)b, (int)o);
-          if (!pack_block(q + o * I + b * 32, nib + (o * NBI + pb) * 16)) return MOE_EINVAL;
-          sc[o * NBI + pb] = sv[o * NBI + b];
+      for (size_t b = 0; b < NBI; ++b)
+        for (size_t o = 0; o < H; ++o) {
+          if (!pack_block(q + o * I + b * 32, nib + (b * H + o) * 16)) return MOE_EINVAL;
+          sc[b * H + o] = sv[o * NBI + b];
         }
     }
     return MOE_OK;

@@ -21,10 +21,12 @@ int check_dims(const moe_dims* d);
 
 // Byte offsets of the workspace regions for `rows` rows (each region 256-aligned):
 // grid-barrier words, router logits [rows][E], weighted SwiGLU outputs h' [rows*k][I]
-// (fp32, one row per routed (row, expert) pair, grouped by expert, in the kernel's
-// operand-pair order).
+// (exchanged between CTAs by the tensor-core kernel: one row per routed (row, expert)
+// pair, grouped by expert, as bf16 hi + lo in fragment order), and the split kernel's
+// output accumulators [kAccCopies][rows][H] (int64, 2^32-scaled).
+constexpr int kAccCopies = 8;
 struct WsLayout {
-  size_t ctrl, logits, hbuf, total;
+  size_t ctrl, logits, hbuf, acc, total;
 };
 WsLayout ws_layout(const moe_dims& d, int rows);
 

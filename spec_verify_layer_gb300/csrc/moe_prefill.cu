@@ -329,8 +329,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_down(PrefillArgs a) {
   const int o0 = blockIdx.y * kDnRows;
   const int H = a.H, NBI = a.I >> 5;
   const int sl = slot_of(a, e);
-  const uint8_t* codes = a.dn_nib + ((size_t)sl * H + o0) * NBI * 16;
-  const uint16_t* scales = a.dn_sc + ((size_t)sl * H + o0) * NBI;
+  // block-major down layout: block b of rows o0.. of the expert at (sl NBI + b) H + o0
+  const uint8_t* codes = a.dn_nib + ((size_t)sl * NBI * H + o0) * 16;
+  const uint16_t* scales = a.dn_sc + (size_t)sl * NBI * H + o0;
   const uint8_t* hb = reinterpret_cast<const uint8_t*>(a.hbuf);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
   const int wm = warp >> 1, wn = warp & 1;
@@ -340,12 +341,17 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_down(PrefillArgs a) {
     uint8_t* A = smem + st * kStageBytes;
     uint8_t* S = A + kACodes;
     uint8_t* B = S + kAScales;
+    // A: row r's block c of this stage at A + r 128 + (c ^ (r & 7)) 16 (eight rows of one
+    // block fall in eight bank groups); S: scale of (r, c) at S[c 128 + r]
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const int idx = tid + kPfThreads * i, r = idx >> 3, c = idx & 7;
-      cp_async16(smem_addr(A + r * 128 + c * 16), codes + ((size_t)r * NBI + 8 * q + c) * 16);
+      const int idx = tid + kPfThreads * i, c = idx >> 7, r = idx & 127;
+      cp_async16(smem_addr(A + r * 128 + ((c ^ (r & 7)) * 16)), codes + ((size_t)(8 * q + c) * H + r) * 16);
     }
-    if (tid < kARows) cp_async16(smem_addr(S + tid * 16), scales + (size_t)tid * NBI + 8 * q);
+    if (tid < kARows) {
+      const int c = tid >> 4, ch = tid & 15;
+      cp_async16(smem_addr(S + c * 256 + ch * 16), scales + (size_t)(8 * q + c) * H + ch * 8);
+    }
 #pragma unroll
     for (int i = 0; i < 8; ++i) {  // B: 32 positions x 64 pieces (8 blocks x 4 lanes x hi, lo)
       const int idx = tid + kPfThreads * i, tk = idx >> 6, c = idx & 63;
@@ -387,11 +393,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_down(PrefillArgs a) {
 #pragma unroll
       for (int mi = 0; mi < 2; ++mi) {
         const int ra = 16 * (2 * wm + mi) + g, rb = ra + 8;
-        const int sa = b ^ ((o0 + ra) & 7), sb = b ^ ((o0 + rb) & 7);
+        const int sa = b ^ (ra & 7), sb = b ^ (rb & 7);
         uint32_t fa[4], fb[4];
         dq_word(*reinterpret_cast<const uint32_t*>(A + ra * 128 + sa * 16 + 4 * t), fa);
         dq_word(*reinterpret_cast<const uint32_t*>(A + rb * 128 + sb * 16 + 4 * t), fb);
-        const float ska = half_bits(S[ra * 8 + sa]), skb = half_bits(S[rb * 8 + sb]);
+        const float ska = half_bits(S[b * 128 + ra]), skb = half_bits(S[b * 128 + rb]);
 #pragma unroll
         for (int ni = 0; ni < 2; ++ni) {
           const uint4 hi = hv[ni][0], lo = hv[ni][1];

@@ -1,30 +1,27 @@
 // GB300 (sm_103a) kernel and C ABI of the MoE layer of a speculative-decoding verify
 // round.  See include/moe_verify.h for the operation and the contract.
 //
-// One persistent cooperative kernel (k_round, one CTA per SM) runs a whole round of L
-// layers.  Per layer, with grid-wide barriers B1..B3 in between:
+// A round of L layers is one persistent cooperative launch (one CTA per SM).  Two
+// kernels share the router and routing phases:
+//
+// k_split (rounds of fewer than kMmaRows rows; the CUDA cores).  Per layer:
 //   P1  router GEMV: this CTA's router rows (staged into shared memory while the
-//       previous layer ran: they depend on no data), canonical fp32 order -> logits.
+//       previous layer ran: they depend on no data), canonical fp32 order -> logits;
+//       meanwhile the previous layer's output slice of this CTA is finished.
 //   B1
 //   P2  every CTA reads the logits and builds the same routing in shared memory:
-//       per-row top-k (warp per row, redux.sync selection, lower id wins ties),
-//       renormalised weights, the ascending expert union U and, per union expert,
-//       the (row, rank) pairs that picked it (CSR).
-//   P3  gate/up: the U * I units (gate row i + up row i of a union expert) are split
-//       contiguously across CTAs by work and streamed through shared-memory slots
-//       with 1-D bulk TMA copies; a warp takes one unit of a chunk, for two rows of
-//       the expert at a time, and stores h' = w silu(g) v (w the row's routing weight)
-//       to the workspace, already in the operand layout the down pass consumes.
-//       Meanwhile the down rows of every union expert for this CTA's share of the
-//       output rows are prefetched, issued by a warp left without a unit in the first
-//       chunk.
-//   B2  (every h' written)
-//   P4  down: the h' rows come back by bulk copy in waves of up to 8 CSR positions,
-//       one warp per position over all of this CTA's output rows o: y = Wd[o] . h'.
-//       Each row's y are added in CSR order (its experts ascending) in shared memory
-//       -- a fixed order, so a row's output depends only on that row (bitwise),
-//       whatever shares the round.
+//       per-row top-k (lower id wins ties), renormalised weights, the ascending expert
+//       union U and, per union expert, the rows that picked it (CSR).
+//   P3  the U * I/32 work units (union expert, 32-wide slice of the intermediate
+//       dimension) are split contiguously across CTAs by work; a CTA streams each unit's
+//       gate/up rows and down block column through shared memory, computes the SwiGLU
+//       outputs of the slice and their share of the down product for every output, and
+//       adds it as exact 2^32-scaled integers into the workspace accumulators.
 //   B3  (layer l+1's router waits for layer l's output, as a real decode would)
+//
+// k_round (wider rounds; the tensor cores): gate/up split by intermediate index, the
+// SwiGLU outputs exchanged through the workspace under a second grid barrier, the down
+// product by output row (see the section "Wide verify rounds" below).
 //
 // Dequantisation without a convert instruction: a nibble n placed in bits [p, p+4) of
 // an otherwise-zero fp32 word is the subnormal n * 2^(p-149); an fma with
@@ -79,7 +76,8 @@ struct RoundArgs {
   int* stats;         // [L] |U| per layer, or null
   unsigned* bar;      // [0] barrier arrivals, [33] abort flag
   float* logits;      // [R][E]
-  float* hbuf;        // [R*k][I] weighted SwiGLU outputs h' by CSR position, pair layout
+  float* hbuf;        // [R*k][I] weighted SwiGLU outputs h' by CSR position (tensor-core rounds)
+  unsigned long long* acc;  // [kSplitCopies][R][H] 2^32-scaled output accumulators (split rounds)
   int* user_ids;      // moe_route outputs (CTA 0 writes them)
   float* user_w;
   int* user_union;
@@ -391,11 +389,11 @@ __device__ __forceinline__ int ranks_before_u(unsigned kj, int j, unsigned ki, i
 }
 
 __device__ void route_one(const RoundArgs& a, const Tables& T, unsigned* s_key, int* s_cnt, int* s_wc, int layer,
-                          int* s_range) {
+                          int upe, int* s_range) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, E = a.E, k = a.k;
   const int lgE = __ffs(E) - 1, QE = E >> 2;
   if (tid == 0) {
-    const unsigned N = (unsigned)k * (unsigned)a.I, G = gridDim.x, c = blockIdx.x;
+    const unsigned N = (unsigned)k * (unsigned)upe, G = gridDim.x, c = blockIdx.x;
     s_range[0] = (int)((c * N) / G);
     s_range[1] = (int)(((c + 1) * N) / G);
   }
@@ -482,7 +480,7 @@ __device__ void softmax_one(const RoundArgs& a, const Tables& T) {
 // (bitonic network over xor partners); a pick that starts a run of one expert opens a
 // union entry, and the ballot of those gives every pick its union index.  Same tables
 // and the same unit cut as the general scan below.  s_ids holds the picks' experts.
-__device__ void route_small(const RoundArgs& a, const Tables& T, const int* s_ids, int layer, int wide,
+__device__ void route_small(const RoundArgs& a, const Tables& T, const int* s_ids, int layer, int wide, int upe,
                             int* s_range) {
   const int lane = threadIdx.x & 31, k = a.k, P = a.R * k;
   constexpr unsigned FULL = 0xffffffffu;
@@ -532,7 +530,7 @@ __device__ void route_small(const RoundArgs& a, const Tables& T, const int* s_id
   }
   const int G = gridDim.x, c = blockIdx.x;
   if (a.R == 1) {
-    const unsigned N = (unsigned)U * (unsigned)a.I;
+    const unsigned N = (unsigned)U * (unsigned)upe;
     if (lane == 0) {
       s_range[0] = (int)((c * N) / (unsigned)G);
       s_range[1] = (int)(((c + 1) * N) / (unsigned)G);
@@ -546,7 +544,7 @@ __device__ void route_small(const RoundArgs& a, const Tables& T, const int* s_id
     const int re = T.csr_off[lane + 1] - T.csr_off[lane];
     wu = wide ? (re + 15) >> 4 : 2 + 2 * re;
   }
-  const int lw = a.I * wu;
+  const int lw = upe * wu;
   int incw = lw;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -561,21 +559,21 @@ __device__ void route_small(const RoundArgs& a, const Tables& T, const int* s_id
   for (int q = 0; q < 2; ++q) {
     const bool here = lane < U && tgt[q] >= basew && tgt[q] < incw;
     const unsigned owner = __ballot_sync(FULL, here);
-    int res = U * a.I;
-    if (owner) res = __shfl_sync(FULL, lane * a.I + (tgt[q] - basew) / max(wu, 1), __ffs(owner) - 1);
+    int res = U * upe;
+    if (owner) res = __shfl_sync(FULL, lane * upe + (tgt[q] - basew) / max(wu, 1), __ffs(owner) - 1);
     if (lane == 0) s_range[q] = res;
   }
 }
 
 __device__ int route_phase(const RoundArgs& a, const Tables& T, unsigned* s_mask, int* s_off_e,
-                           int* s_ids, int* s_ui, int* s_rank, int layer, int wide, int* s_range) {
+                           int* s_ids, int* s_ui, int* s_rank, int layer, int wide, int upe, int* s_range) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int E = a.E, k = a.k, R = a.R;
   const bool small = R * k <= 32 && a.tail_rank == 0;
   // route_one's scratch: keys [E] (16-byte aligned: read as uint4), counts [4 E], warp sums
   unsigned* s_key = reinterpret_cast<unsigned*>((reinterpret_cast<uintptr_t>(s_rank + E) + 15) & ~(uintptr_t)15);
   if (route_one_ok(a)) {  // (weights: softmax_one, by the caller)
-    route_one(a, T, s_key, reinterpret_cast<int*>(s_key + NT), reinterpret_cast<int*>(s_key + 5 * NT), layer,
+    route_one(a, T, s_key, reinterpret_cast<int*>(s_key + NT), reinterpret_cast<int*>(s_key + 5 * NT), layer, upe,
               s_range);
     return k;
   }
@@ -606,7 +604,7 @@ __device__ int route_phase(const RoundArgs& a, const Tables& T, unsigned* s_mask
   }
   __syncthreads();
   if (small) {
-    if (warp == 0) route_small(a, T, s_ids, layer, wide, s_range);
+    if (warp == 0) route_small(a, T, s_ids, layer, wide, upe, s_range);
     __syncthreads();
     return *T.n_union;
   }
@@ -625,7 +623,7 @@ __device__ int route_phase(const RoundArgs& a, const Tables& T, unsigned* s_mask
       }
       lf += (m != 0u);
       lc += __popc(m);
-      if (m) lw += a.I * weight(m);
+      if (m) lw += upe * weight(m);
     }
     int incf = lf, incc = lc, incw = lw;
 #pragma unroll
@@ -647,7 +645,7 @@ __device__ int route_phase(const RoundArgs& a, const Tables& T, unsigned* s_mask
       const int G = gridDim.x, c = blockIdx.x;
       const int U = __shfl_sync(0xffffffffu, incf, 31);
       if (R == 1) {
-        const unsigned N = (unsigned)U * (unsigned)a.I;  // < 2^31 (U <= 512, I <= 4096)
+        const unsigned N = (unsigned)U * (unsigned)upe;  // < 2^31 (U <= 512, upe <= 4096)
         if (lane == 0) {
           s_range[0] = (int)((c * N) / (unsigned)G);
           s_range[1] = (int)(((c + 1) * N) / (unsigned)G);
@@ -660,15 +658,15 @@ __device__ int route_phase(const RoundArgs& a, const Tables& T, unsigned* s_mask
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
           const bool here = tgt[q] >= basew && tgt[q] < incw;
-          int res = U * a.I;
+          int res = U * upe;
           if (here) {
             int cum = basew, ui = basef;
             for (int e = e0; e < e1; ++e) {
               const unsigned m = s_mask[e];
               if (!m) continue;
-              const int w = weight(m), ew = a.I * w;
+              const int w = weight(m), ew = upe * w;
               if (tgt[q] < cum + ew) {
-                res = ui * a.I + (tgt[q] - cum) / w;
+                res = ui * upe + (tgt[q] - cum) / w;
                 break;
               }
               cum += ew;
@@ -676,7 +674,7 @@ __device__ int route_phase(const RoundArgs& a, const Tables& T, unsigned* s_mask
             }
           }
           const unsigned owner = __ballot_sync(0xffffffffu, here);
-          res = owner ? __shfl_sync(0xffffffffu, res, __ffs(owner) - 1) : U * a.I;
+          res = owner ? __shfl_sync(0xffffffffu, res, __ffs(owner) - 1) : U * upe;
           if (lane == 0) s_range[q] = res;
         }
       }
@@ -719,141 +717,14 @@ __device__ int route_phase(const RoundArgs& a, const Tables& T, unsigned* s_mask
 }
 
 // ---------------------------------------------------------------------------------
-// P3: gate/up over an even share of the (union expert, intermediate row) units
-//
-// Unit (ui, i) = gate row i and up row i of union expert ui: H bytes of codes and H/8
-// bytes of scales, contiguous in the packed layout.  CTA c owns units
-// [c N / G, (c+1) N / G) of the N = U * I units, walked in chunks that stop at expert
-// boundaries and at the slot capacity; chunks stream through kGuSlots shared-memory
-// slots (1-D bulk copies, one mbarrier per slot).  For every row of the expert a warp
-// computes g and v of one unit, lane 0 stores h = silu(g) v to the workspace at
-// (CSR position, i).  Down rows of every union expert for this CTA's output rows are
-// prefetched into kDnSlots slots meanwhile (they depend only on the routing).
-
-constexpr int kGuSlots = 3;
-// gate/up chunks issued before the first one lands (the rest of the ring follows it):
-// copies in flight share the bandwidth, so a chunk issued alone arrives sooner
-constexpr int kGuFirst = 1;
-constexpr int kDnSlots = 11;
-// the layer's rows as operand pairs plus block sums (4 rows at hidden 2048), staged once
-// per layer when they fit
-constexpr size_t kXBytes = 33792;
-// Inside the gate/up ring, idle outside the gate/up stream: the next layer's router rows
-// at offset 0 (consumed before the routing scratch, also at offset 0, is written) and,
-// from kHOffset on, two slots of exchanged h rows for the down pass.
-constexpr size_t kHOffset = 32768;
-constexpr int kAccStride = 64;  // output rows per CTA are at most this many
-
-struct GuChunk {
-  int ui, i0, n;
-};
-
-// smem plan: GU ring | DN slots | x pairs | tables | out accumulators | wave outputs |
-// chunk list | barriers
-struct SmemPlan {
-  size_t gu_slot, gu, dn_slot, dn, xrows, uni, csr, pair, w, pos_ui, pos_row, slot, pick, nunion, acc, ybuf,
-      chunks, bars, total;
-  size_t ring;    // bytes of the gate/up ring (>= kGuSlots * gu_slot)
-  size_t h_slot;  // bytes per h slot (two slots from gu + kHOffset)
-  int gu_cap;     // units per gate/up chunk
-  int h_rows;     // h rows (CSR positions) per h slot
-  int max_orows;  // output rows per CTA (ceil(H / grid))
-  bool router_fits;
-};
-
-__host__ __device__ inline size_t up128(size_t x) { return (x + 127) & ~(size_t)127; }
-
-__host__ __device__ inline SmemPlan smem_plan(int H, int I, int E, int R, int k, int grid) {
-  SmemPlan p{};
-  const size_t unit = (size_t)H + (size_t)H / 8;
-  p.max_orows = (H + grid - 1) / grid;
-  p.dn_slot = up128((size_t)p.max_orows * (I / 2)) + up128((size_t)p.max_orows * (I / 16));
-  const size_t tables = up128((size_t)E * 4) + up128((size_t)(E + 1) * 4) +
-                        5 * up128((size_t)R * k * 4) + up128((size_t)E * 4) + 128 +
-                        up128((size_t)R * kAccStride * 4) +
-                        up128((size_t)NW * kAccStride * 4) + up128(kGuSlots * 12 + 16) + 256;
-  const size_t fixed = tables + kDnSlots * p.dn_slot + kXBytes;
-  const size_t limit = (size_t)225 * 1024;
-  size_t cap = fixed < limit ? ((limit - fixed) / kGuSlots) / unit : 0;
-  if (cap > NW) cap = NW;  // a chunk is one pass of the warps, a unit each
-  p.gu_cap = (int)cap;
-  p.gu_slot = up128(cap * unit);
-  // small shapes: keep room behind kHOffset for full waves of exchanged h rows
-  p.ring = kGuSlots * p.gu_slot;
-  const size_t want = kHOffset + 2 * up128((size_t)NW * I * 4);
-  if (p.ring < want && fixed + want <= limit) p.ring = want;
-  size_t off = 0;
-  p.gu = off;      off += p.ring;
-  p.dn = off;      off += kDnSlots * p.dn_slot;
-  p.xrows = off;   off += kXBytes;
-  p.uni = off;     off += up128((size_t)E * 4);
-  p.csr = off;     off += up128((size_t)(E + 1) * 4);
-  p.pair = off;    off += up128((size_t)R * k * 4);
-  p.w = off;       off += up128((size_t)R * k * 4);
-  p.pos_ui = off;  off += up128((size_t)R * k * 4);
-  p.pos_row = off; off += up128((size_t)R * k * 4);
-  p.slot = off;    off += up128((size_t)E * 4);
-  p.pick = off;    off += up128((size_t)R * k * 4);
-  p.nunion = off;  off += 128;
-  p.acc = off;     off += up128((size_t)R * kAccStride * 4);
-  p.ybuf = off;    off += up128((size_t)NW * kAccStride * 4);
-  p.chunks = off;  off += up128(kGuSlots * 12 + 16);
-  p.bars = off;    off += 256;
-  p.total = off;
-  const int rows_per_cta = (E + grid - 1) / grid;
-  p.h_slot = p.ring > kHOffset ? ((p.ring - kHOffset) / 2) & ~(size_t)127 : 0;
-  p.h_rows = (int)(p.h_slot / ((size_t)I * 4));
-  p.router_fits = cap >= 1 && p.max_orows <= kAccStride && p.h_rows >= 1 &&
-                  (size_t)rows_per_cta * H * 4 <= kHOffset;
-  return p;
-}
-
-__device__ void issue_gu_chunk(const RoundArgs& a, const LayerPtrs& W, const Tables& T, uint8_t* dst,
-                               uint32_t bar, const GuChunk& c) {
-  const size_t H = (size_t)a.H, I = (size_t)a.I;
-  const size_t u = (size_t)T.slot[T.uni[c.ui]];
-  const size_t first = u * I + (size_t)c.i0;  // unit index within the bank
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  mbar_expect_tx(bar, (uint32_t)((size_t)c.n * (H + H / 8)));
-  bulk_g2s(smem_u32(dst), W.gu_nib + first * H, (uint32_t)(c.n * H), bar);
-  bulk_g2s(smem_u32(dst + (size_t)c.n * H),
-           reinterpret_cast<const uint8_t*>(W.gu_sc) + first * (H / 8), (uint32_t)(c.n * (H / 8)), bar);
-}
-
-__device__ void issue_dn_chunk(const RoundArgs& a, const LayerPtrs& W, const Tables& T, uint8_t* dst,
-                               uint32_t bar, int ui, int o0, int no, size_t codes_room) {
-  const size_t H = (size_t)a.H, I = (size_t)a.I;
-  const size_t u = (size_t)T.slot[T.uni[ui]];
-  const size_t row0 = u * H + (size_t)o0;
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  mbar_expect_tx(bar, (uint32_t)((size_t)no * (I / 2 + I / 16)));
-  bulk_g2s(smem_u32(dst), W.dn_nib + row0 * (I / 2), (uint32_t)(no * (I / 2)), bar);
-  bulk_g2s(smem_u32(dst + codes_room), reinterpret_cast<const uint8_t*>(W.dn_sc) + row0 * (I / 16),
-           (uint32_t)(no * (I / 16)), bar);
-}
-
-// ---------------------------------------------------------------------------------
 // Operand pairs.  The word pairs above consume a block's 32 elements as 16 f32x2
 // operands: pair p holds elements (16(p/8) + p%8, 16(p/8) + 8 + p%8), pre-scaled by
-// slot_scale(p%8).  Activations (once per layer) and exchanged h rows (by their
-// producer) are kept in this form, block-interleaved: float4 c of block b (pairs 2c
-// and 2c+1) sits at float4 index c * NBlk + b, so lane b's eight 16-byte loads are
-// conflict-free.
-
-// Float index of element j of block b in a pair-layout row of NBlk blocks.
-__device__ __forceinline__ int pair_index(int b, int j, int NBlk) {
-  const int p = ((j >> 4) << 3) | (j & 7);
-  return (((p >> 1) * NBlk + b) << 2) | ((p & 1) << 1) | ((j >> 3) & 1);
-}
+// slot_scale(p%8).  Activations are kept in this form once per layer, block-interleaved:
+// float4 c of block b (pairs 2c and 2c+1) sits at float4 index c * NBlk + b, so lane b's
+// eight 16-byte loads are conflict-free.
 
 __device__ __forceinline__ void f2unpack(f2_t v, float& lo, float& hi) {
   asm("mov.b64 {%0,%1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-
-// 2^-(exponent of slot_scale(m)): exact inverse of the slot factor.
-__device__ __forceinline__ float inv_slot_scale(int m) {
-  const int e = (m <= 4) ? 87 - 4 * m : 99 - 4 * m;
-  return __int_as_float((127 - e) << 23);
 }
 
 // One block of bf16 activations (four 16-byte words, elements 0..31) -> its 16
@@ -970,200 +841,563 @@ __device__ __forceinline__ float warp_sum_multi(float (&v)[V], int lane) {
   return s;
 }
 
-// Gate/up of unit t of chunk c for the rows at CSR positions pp .. pp+G-1: per lane
-// its NBL blocks of the gate and up rows, one multi-value reduction, then the lane
-// holding a row's gate value takes the up value from the next lane group and stores
-// h' = w silu(g) v, pre-scaled, in pair layout.
-template <int NBL, int G, bool XS>
-__device__ __forceinline__ void gateup_unit(const RoundArgs& a, const Tables& T, const uint8_t* slot,
-                                            const GuChunk& c, int t, int pp, const uint16_t* x,
-                                            const float4* s_xp, const float* s_xs) {
-  const int H = a.H, NB = H >> 5;
-  const int lane = threadIdx.x & 31;
-  int row[G];
-#pragma unroll
-  for (int g = 0; g < G; ++g) row[g] = T.pos_row[pp + g];
-  const uint8_t* codes = slot;
-  const uint16_t* scales = reinterpret_cast<const uint16_t*>(slot + (size_t)c.n * H);
-  constexpr int V = 2 * G;  // value 2 g + wrow
-  float v[V];
-#pragma unroll
-  for (int i = 0; i < V; ++i) v[i] = 0.f;
-  const int sw = (c.i0 + t) & 7;
-#pragma unroll
-  for (int tb = 0; tb < NBL; ++tb) {
-    const int blk = lane + 32 * tb;
-    if (blk < NB) {
-      f2_t xp[G][16];
-      float xsum8[G];
-#pragma unroll
-      for (int g = 0; g < G; ++g) load_xblock<XS>(a, x, s_xp, s_xs, row[g], blk, xp[g], xsum8[g]);
-      const f2_t* xps[G];
-#pragma unroll
-      for (int g = 0; g < G; ++g) xps[g] = xp[g];
-#pragma unroll
-      for (int wrow = 0; wrow < 2; ++wrow) {
-        // unit t of the chunk is intermediate row i0 + t of the expert: its blocks sit at
-        // blk ^ ((i0 + t) & 7), gate and up alike
-        const size_t w = (size_t)(t * 2 + wrow) * NB + (blk ^ sw);
-        const uint4 nb = *reinterpret_cast<const uint4*>(codes + w * 16);
-        const float sc = half_bits(scales[w]);
-        float dot[G];
-        block_dot<G>(nb, xps, dot);
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          float& acc = v[2 * g + wrow];
-          acc = __fmaf_rn(sc, __fmaf_rn(dot[g], 0x1p62f, xsum8[g]), acc);
-        }
-      }
+// Leaving early: gives every copy still in flight a bounded chance to land (so no bulk
+// copy targets shared memory of an exited CTA) and raises the abort flag.  Copies in
+// flight are the slots of pieces [j0, j1) of a ring of `nslot` slots (slot j % nslot,
+// parity (j / nslot) & 1), the router rows, and any extra single-use barriers.  Out of
+// line: it never runs on the normal path.
+__device__ __noinline__ void drain_and_abort(const RoundArgs& a, const uint64_t* bars, int nslot, long long j0,
+                                             long long j1, bool router_pend, uint32_t bar_router,
+                                             unsigned ph_router) {
+  if (threadIdx.x == 0) {
+    for (long long j = j0; j < j1; ++j) {
+      const int q = (int)(j % nslot);
+      mbar_wait_bounded(smem_u32(bars + q), (unsigned)((j / nslot) & 1), a.status, kDefaultWaitCycles);
     }
+    if (router_pend) mbar_wait_bounded(bar_router, ph_router, a.status, kDefaultWaitCycles);
+    atomicExch(a.bar + 33, 1u);
   }
-  const float s = warp_sum_multi<V>(v, lane);
-  constexpr int LPV = 32 / V;  // lanes per value
-  const float up = __shfl_down_sync(0xffffffffu, s, LPV);
-  const int vi = lane / LPV;
-  if ((lane % LPV) == 0 && (vi & 1) == 0) {
-    const int g = vi >> 1;
-    const int i = c.i0 + t, j = i & 31;
-    const int pair = T.pair[pp + g];
-    const float hh = __fmul_rn(__fdiv_rn(s, __fadd_rn(1.f, expf(-s))), up);
-    const float hw = __fmul_rn(T.w[pair], hh);
-    a.hbuf[(size_t)(pp + g) * a.I + pair_index(i >> 5, j, a.I >> 5)] = hw * slot_scale(j & 7);
-  }
-}
-
-// Gate/up of one staged chunk (at most NW units): warp w takes unit w, the rows of the
-// expert two at a time when the activations are staged.
-template <int NBL, bool XS>
-__device__ __forceinline__ void gateup_chunk(const RoundArgs& a, const Tables& T, const uint8_t* slot,
-                                             const GuChunk& c, const uint16_t* x, const float4* s_xp,
-                                             const float* s_xs) {
-  const int warp = threadIdx.x >> 5;
-  const int p0 = T.csr_off[c.ui], p1 = T.csr_off[c.ui + 1];
-  for (int t = warp; t < c.n; t += NW) {
-    int pp = p0;
-    if (XS)  // (converting two rows from global memory at once would not fit the registers)
-      for (; pp + 1 < p1; pp += 2) gateup_unit<NBL, 2, XS>(a, T, slot, c, t, pp, x, s_xp, s_xs);
-    for (; pp < p1; ++pp) gateup_unit<NBL, 1, XS>(a, T, slot, c, t, pp, x, s_xp, s_xs);
-  }
-}
-
-// Gate/up of one staged chunk when the round has one row: the operand pairs of each
-// lane's first block of the row (xr) stay in registers for the whole layer, so a unit
-// reads only its codes, scales and the second block's pairs from shared memory (both
-// blocks in registers would not fit beside the rest of the kernel).  Same operations in
-// the same order as gateup_unit with one row, so the results are the same bits.
-template <int NBL>
-__device__ __forceinline__ void gateup_chunk_r1(const RoundArgs& a, const Tables& T, const uint8_t* slot,
-                                                const GuChunk& c, const f2_t (&xr)[16], const float4* s_xp,
-                                                const float* s_xs) {
-  const int H = a.H, NB = H >> 5;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int pp = T.csr_off[c.ui];
-  const uint8_t* codes = slot;
-  const uint16_t* scales = reinterpret_cast<const uint16_t*>(slot + (size_t)c.n * H);
-  for (int t = warp; t < c.n; t += NW) {
-    float v[2] = {0.f, 0.f};
-    const int sw = (c.i0 + t) & 7;
-#pragma unroll
-    for (int tb = 0; tb < NBL; ++tb) {
-      const int blk = lane + 32 * tb;
-      if (blk < NB) {
-        f2_t xq[16];
-        float xs;
-        if (tb == 0) {
-#pragma unroll
-          for (int m = 0; m < 16; ++m) xq[m] = xr[m];
-          xs = s_xs[blk];
-        } else {
-          load_xblock<true>(a, nullptr, s_xp, s_xs, 0, blk, xq, xs);
-        }
-        const f2_t* xps[1] = {xq};
-#pragma unroll
-        for (int wrow = 0; wrow < 2; ++wrow) {
-          const size_t w = (size_t)(t * 2 + wrow) * NB + (blk ^ sw);
-          const uint4 nb = *reinterpret_cast<const uint4*>(codes + w * 16);
-          const float sc = half_bits(scales[w]);
-          float dot[1];
-          block_dot<1>(nb, xps, dot);
-          v[wrow] = __fmaf_rn(sc, __fmaf_rn(dot[0], 0x1p62f, xs), v[wrow]);
-        }
-      }
-    }
-    const float s = warp_sum_multi<2>(v, lane);
-    const float up = __shfl_down_sync(0xffffffffu, s, 16);
-    if (lane == 0) {
-      const int i = c.i0 + t, j = i & 31;
-      const int pair = T.pair[pp];
-      const float hh = __fmul_rn(__fdiv_rn(s, __fadd_rn(1.f, expf(-s))), up);
-      const float hw = __fmul_rn(T.w[pair], hh);
-      a.hbuf[(size_t)pp * a.I + pair_index(i >> 5, j, a.I >> 5)] = hw * slot_scale(j & 7);
-    }
-  }
+  __syncthreads();
 }
 
 // ---------------------------------------------------------------------------------
-// P4: this CTA's output rows [o0, o0 + no), a wave of CSR positions at a time
+// Split-K rounds: the CUDA-core path (fewer than kMmaRows rows).
+//
+// Work unit (ui, s) = union expert ui, K-slice s: intermediate indices [32 s, 32 s + 32).
+// Its bytes are the gate and up rows of those 32 indices (contiguous in the packed
+// layout) and block s of every one of the expert's H down rows (contiguous in the
+// block-major down layout): 3 * 32 * H / 2 code bytes and 3 * 32 * H / 16 scale bytes.
+// The CTA that owns the unit computes, for every row r that picked the expert,
+//   h'_r[i] = w_r silu(Wg[i] . x_r) (Wu[i] . x_r)         i in the slice
+//   y_r[o]  = sum_{i in slice} Wd[o][i] h'_r[i]            every output o
+// and adds y_r[o] * 2^32, rounded to an integer, into an int64 accumulator of row r.
+// Integer adds are exact, so the accumulated value (and the fp32 output rounded from it)
+// does not depend on the order of the adds, on how the units were shared out, or on the
+// other rows of the round: a row's output is a function of that row alone, bit for bit.
+// The adds go to one of kSplitCopies copies of the accumulator (by CTA), which keeps the
+// number of adds that meet at one address small; after the layer's closing grid barrier
+// each CTA sums the copies of its own output slice, writes the fp32 output and clears
+// them.  No exchange of SwiGLU outputs between CTAs is needed, so a layer has two grid
+// barriers (logits, layer end) instead of three, and the down products are computed
+// while the stream is still running.
+//
+// Bytes are streamed as pieces of 9 H bytes into a ring of shared-memory slots (1-D bulk
+// copies, one mbarrier per slot): four gate/up pieces (8 intermediate indices: 16 rows
+// of H/2 code bytes, then their H/8-byte scale rows) and two down pieces (H/2 rows of
+// one 16-byte block, then their fp16 scales) per unit, in unit order.
 
-// y of one CSR position over this CTA's output rows [ob0, ob1): the position's h' row
-// (pair layout, shared memory) against each output row's down codes of its expert;
-// y[ol] to s_yw.  Lanes >= I/32 hold no block.
-__device__ __forceinline__ void down_position(const RoundArgs& a, const uint8_t* dslot, size_t codes_room,
-                                              int o0, int ob0, int ob1, const float4* s_h, float* s_yw) {
-  const int NBI = a.I >> 5;
-  const int lane = threadIdx.x & 31;
-  f2_t hp[16];
-  float hsum8 = 0.f;
-  if (lane < NBI) {
+constexpr int kSplitCopies = kAccCopies;
+constexpr int kSplitMaxSlots = 16;
+constexpr int kGuPieces = 4;  // gate/up pieces per unit (8 intermediate indices each)
+constexpr int kDnPieces = 2;  // down pieces per unit (H/2 output rows each)
+constexpr int kPieces = kGuPieces + kDnPieces;
+constexpr int kSplitPhases = 8;  // phase stamps per layer when profiling the split kernel
+
+struct SplitPlan {
+  size_t slot_bytes, ring, router, xp, xs, part, hp, uni, csr, pair, w, pos_ui, pos_row, slot, pick, nunion, misc,
+      bars, total;
+  int nslot, ng;
+  bool x_staged, ok;
+};
+
+__host__ __device__ inline size_t up128(size_t x) { return (x + 127) & ~(size_t)127; }
+
+// Shared-memory plan of the split kernel for R rows; the activation pairs are staged when
+// they leave room for at least six slots.
+__host__ __device__ inline SplitPlan split_plan(int H, int I, int E, int R, int k, int grid) {
+  SplitPlan p{};
+  const int NB = H >> 5;
+  p.ng = (NB + 31) >> 5;
+  p.slot_bytes = (size_t)9 * H;
+  const size_t rk = (size_t)R * k;
+  const size_t router = up128((size_t)((E + grid - 1) / grid) * H * 4);
+  const size_t part = up128((size_t)64 * p.ng * R * 4);
+  const size_t hp = up128((size_t)R * 36 * 4);
+  const size_t tables = up128((size_t)E * 4) + up128((size_t)(E + 1) * 4) + 5 * up128(rk * 4) +
+                        up128((size_t)E * 4) + 128;
+  const size_t misc = 256, bars = 256;
+  const size_t limit = (size_t)225 * 1024;
+  size_t fixed = router + part + hp + tables + misc + bars;
+  const size_t xbytes = up128((size_t)R * H * 4) + up128((size_t)R * NB * 4);
+  p.x_staged = fixed + xbytes + 6 * p.slot_bytes <= limit;
+  if (p.x_staged) fixed += xbytes;
+  int ns = fixed < limit ? (int)((limit - fixed) / p.slot_bytes) : 0;
+  if (ns > kSplitMaxSlots) ns = kSplitMaxSlots;
+  p.nslot = ns;
+  size_t off = 0;
+  p.ring = off;    off += (size_t)ns * p.slot_bytes;
+  p.router = off;  off += router;
+  p.xp = off;      off += p.x_staged ? up128((size_t)R * H * 4) : 0;
+  p.xs = off;      off += p.x_staged ? up128((size_t)R * NB * 4) : 0;
+  p.part = off;    off += part;
+  p.hp = off;      off += hp;
+  p.uni = off;     off += up128((size_t)E * 4);
+  p.csr = off;     off += up128((size_t)(E + 1) * 4);
+  p.pair = off;    off += up128(rk * 4);
+  p.w = off;       off += up128(rk * 4);
+  p.pos_ui = off;  off += up128(rk * 4);
+  p.pos_row = off; off += up128(rk * 4);
+  p.slot = off;    off += up128((size_t)E * 4);
+  p.pick = off;    off += up128(rk * 4);
+  p.nunion = off;  off += 128;
+  p.misc = off;    off += misc;
+  p.bars = off;    off += bars;
+  p.total = off;
+  // routing scratch lives in the (then idle) ring: mask, offsets, ids, union index, best
+  // rank, and the one-row counting path's keys, counts and warp sums
+  const size_t scratch = ((size_t)4 * E + rk) * 4 + 16 + (size_t)(5 * NT + NW) * 4;
+  p.ok = ns >= kPieces && (size_t)ns * p.slot_bytes >= scratch;
+  return p;
+}
+
+// Piece j of this CTA's units (unit u0 + j / kPieces, piece j % kPieces) -> ring slot.
+__device__ __forceinline__ void issue_piece(const RoundArgs& a, const LayerPtrs& W, const Tables& T, int NS, int u0,
+                                            int j, uint8_t* dst, uint32_t bar) {
+  const size_t H = (size_t)a.H;
+  const int u = u0 + j / kPieces, pc = j - (j / kPieces) * kPieces;
+  const int ui = u / NS, s = u - ui * NS;
+  const size_t sl = (size_t)T.slot[T.uni[ui]];
+  const uint8_t* src_c;
+  const uint8_t* src_s;
+  if (pc < kGuPieces) {
+    const size_t i0 = sl * (size_t)a.I + (size_t)s * 32 + (size_t)pc * 8;  // first intermediate index
+    src_c = W.gu_nib + i0 * H;
+    src_s = reinterpret_cast<const uint8_t*>(W.gu_sc) + i0 * (H / 8);
+  } else {
+    const size_t row0 = (sl * (size_t)NS + (size_t)s) * H + (size_t)(pc - kGuPieces) * (H / 2);
+    src_c = W.dn_nib + row0 * 16;
+    src_s = reinterpret_cast<const uint8_t*>(W.dn_sc) + row0 * 2;
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  mbar_expect_tx(bar, (uint32_t)(9 * H));
+  bulk_g2s(smem_u32(dst), src_c, (uint32_t)(8 * H), bar);
+  bulk_g2s(smem_u32(dst + 8 * H), src_s, (uint32_t)H, bar);
+}
+
+// Gate/up of 4 consecutive rows rp0 .. rp0 + 3 of a gate/up piece (row rp of the piece =
+// intermediate index i0 + rp / 2, gate for even rp, up for odd) for G activation sets:
+// lane = hidden block b (32 kg + lane of the warp's K group), one block dot per row and
+// set; v[s][j] = that block's contribution to row rp0 + j for set s.
+template <int G>
+__device__ __forceinline__ void split_gu_rows4(const uint8_t* piece, int H, int rp0, int b, bool valid,
+                                               const f2_t* const* xps, const float* xs8, float (&v)[G][4]) {
+  const int NB = H >> 5;
+  const uint16_t* scales = reinterpret_cast<const uint16_t*>(piece + (size_t)8 * H);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int rp = rp0 + j;
+    if (valid) {
+      // block b of the row of intermediate index i sits at b ^ (i & 7); i & 7 = (rp / 2) & 7
+      const int pb = b ^ ((rp >> 1) & 7);
+      const uint4 nb = *reinterpret_cast<const uint4*>(piece + ((size_t)rp * NB + pb) * 16);
+      const float sc = half_bits(scales[rp * NB + pb]);
+      float dot[G];
+      block_dot<G>(nb, xps, dot);
+#pragma unroll
+      for (int g = 0; g < G; ++g) v[g][j] = __fmul_rn(sc, __fmaf_rn(dot[g], 0x1p62f, xs8[g]));
+    } else {
+#pragma unroll
+      for (int g = 0; g < G; ++g) v[g][j] = 0.f;
+    }
+  }
+}
+
+// Reduces one set's 4 values over the warp and stores the row sums as partials of K
+// group kg: s_part[((row0 + j) * NG + kg) * Rs + pr].
+__device__ __forceinline__ void split_store_part(float (&v)[4], int lane, float* s_part, int row0, int NG, int kg,
+                                                 int Rs, int pr) {
+  const float s = warp_sum_multi<4>(v, lane);
+  if ((lane & 7) == 0) s_part[((row0 + (lane >> 3)) * NG + kg) * Rs + pr] = s;
+}
+
+// The gate/up pass of one unit for this warp: rows [rb RPW, (rb + 1) RPW) of the unit's
+// 64 (RPW = 4 NG, all in one piece), K group kg, every activation row of the expert (CSR
+// positions p0 .. p0 + Re - 1), two at a time, four weight rows at a time.  XR: one row
+// whose pairs live in registers.
+template <int NG, bool XR, bool XS>
+__device__ __forceinline__ void split_gateup(const RoundArgs& a, const Tables& T, const uint8_t* piece, int rb,
+                                             int kg, int p0, int Re, const f2_t (&xr)[16], float xsr,
+                                             const float4* s_xp, const float* s_xs, const uint16_t* x,
+                                             float* s_part) {
+  constexpr int RPW = 4 * NG;
+  const int lane = threadIdx.x & 31, NB = a.H >> 5;
+  const int b = 32 * kg + lane;
+  const bool valid = b < NB;
+  const int row0 = rb * RPW;
+  if (XR) {
+    const f2_t* xps[1] = {xr};
+#pragma unroll
+    for (int h = 0; h < RPW; h += 4) {
+      float v[1][4];
+      split_gu_rows4<1>(piece, a.H, (row0 + h) & 15, b, valid, xps, &xsr, v);
+      split_store_part(v[0], lane, s_part, row0 + h, NG, kg, a.R, 0);
+    }
+    return;
+  }
+  int pr = 0;
+  for (; pr + 1 < Re; pr += 2) {
+    f2_t x0[16], x1[16];
+    float xs8[2] = {0.f, 0.f};
+    if (valid) {
+      load_xblock<XS>(a, x, s_xp, s_xs, T.pos_row[p0 + pr], b, x0, xs8[0]);
+      load_xblock<XS>(a, x, s_xp, s_xs, T.pos_row[p0 + pr + 1], b, x1, xs8[1]);
+    }
+    const f2_t* xps[2] = {x0, x1};
+#pragma unroll 1
+    for (int h = 0; h < RPW; h += 4) {
+      float v[2][4];
+      split_gu_rows4<2>(piece, a.H, (row0 + h) & 15, b, valid, xps, xs8, v);
+      split_store_part(v[0], lane, s_part, row0 + h, NG, kg, a.R, pr);
+      split_store_part(v[1], lane, s_part, row0 + h, NG, kg, a.R, pr + 1);
+    }
+  }
+  if (pr < Re) {
+    f2_t x0[16];
+    float xs8 = 0.f;
+    if (valid) load_xblock<XS>(a, x, s_xp, s_xs, T.pos_row[p0 + pr], b, x0, xs8);
+    const f2_t* xps[1] = {x0};
+#pragma unroll 1
+    for (int h = 0; h < RPW; h += 4) {
+      float v[1][4];
+      split_gu_rows4<1>(piece, a.H, (row0 + h) & 15, b, valid, xps, &xs8, v);
+      split_store_part(v[0], lane, s_part, row0 + h, NG, kg, a.R, pr);
+    }
+  }
+}
+
+// The multi-row gate/up pass runs out of line: it then has the register file to itself
+// (inlined into the kernel, the kernel's live state pushes its operand pairs to local
+// memory); the one-row pass keeps the activation pairs in the kernel's registers.
+template <int NG, bool XS>
+__device__ __noinline__ void split_gateup_rows(const RoundArgs& a, const Tables& T, const uint8_t* piece, int rb,
+                                               int kg, int p0, int Re, const float4* s_xp, const float* s_xs,
+                                               const uint16_t* x, float* s_part) {
+  f2_t none[16];
+  split_gateup<NG, false, XS>(a, T, piece, rb, kg, p0, Re, none, 0.f, s_xp, s_xs, x, s_part);
+}
+
+// SwiGLU of one unit: warp per activation row (CSR position p0 + pr), lane = index i of
+// the slice.  g and v add the K groups' partials in group order; h' = w silu(g) v is
+// stored in pair layout (pre-scaled by its slot factor) with -8 sum h' after it.
+__device__ __forceinline__ void split_swiglu(const RoundArgs& a, const Tables& T, const float* s_part, int NG,
+                                             int p0, int Re, float* s_hp) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int pr = warp; pr < Re; pr += NW) {
+    float gs = s_part[((2 * lane) * NG) * a.R + pr], vs = s_part[((2 * lane + 1) * NG) * a.R + pr];
+    for (int g = 1; g < NG; ++g) {
+      gs = __fadd_rn(gs, s_part[((2 * lane) * NG + g) * a.R + pr]);
+      vs = __fadd_rn(vs, s_part[((2 * lane + 1) * NG + g) * a.R + pr]);
+    }
+    const float hh = __fmul_rn(__fdiv_rn(gs, __fadd_rn(1.f, expf(-gs))), vs);
+    const float hw = __fmul_rn(T.w[T.pair[p0 + pr]], hh);
+    const int p = ((lane >> 4) << 3) | (lane & 7);
+    s_hp[pr * 36 + 2 * p + ((lane >> 3) & 1)] = hw * slot_scale(lane & 7);
+    const float sum = warp_sum(hw);
+    if (lane == 0) s_hp[pr * 36 + 32] = -8.f * sum;
+  }
+}
+
+// Down products of one unit for this thread's output rows o = tid + NT j, activation
+// sets pr .. pr + G - 1: y -> 2^32-scaled integers added into this CTA's accumulator copy.
+template <int G>
+__device__ __forceinline__ void split_down_rows(const RoundArgs& a, const Tables& T, const uint8_t* dn0,
+                                                const uint8_t* dn1, const float* s_hp, int p0, int pr,
+                                                unsigned long long* acc_copy) {
+  f2_t hp[G][16];
+  float hs8[G];
+  int row[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    const ulonglong2* src = reinterpret_cast<const ulonglong2*>(s_hp + (pr + g) * 36);
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
-      const ulonglong2 f = *reinterpret_cast<const ulonglong2*>(s_h + c * NBI + lane);
-      hp[2 * c] = f.x;
-      hp[2 * c + 1] = f.y;
+      const ulonglong2 f = src[c];
+      hp[g][2 * c] = f.x;
+      hp[g][2 * c + 1] = f.y;
     }
-    // -8 x the block sum of h', undoing each slot's power-of-two factor exactly
-    float sum = 0.f;
-#pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      float a0, a1, b0, b1;
-      f2unpack(hp[m], a0, a1);
-      f2unpack(hp[8 + m], b0, b1);
-      sum = __fmaf_rn(__fadd_rn(__fadd_rn(a0, a1), __fadd_rn(b0, b1)), inv_slot_scale(m), sum);
-    }
-    hsum8 = -8.f * sum;
-  } else {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) hp[i] = 0ull;
+    hs8[g] = s_hp[(pr + g) * 36 + 32];
+    row[g] = T.pos_row[p0 + pr + g];
   }
-  const uint8_t* codes = dslot;
-  const uint16_t* scales = reinterpret_cast<const uint16_t*>(dslot + codes_room);
-  const f2_t* hps[1] = {hp};
-  // rows in groups of DG, one multi-value reduction per group
-  constexpr int DG = 8;
-  for (int ob = ob0; ob < ob1; ob += DG) {
-    float part[DG];
+  const f2_t* hps[G];
 #pragma unroll
-    for (int jj = 0; jj < DG; ++jj) {
-      part[jj] = 0.f;
-      const int ol = ob + jj;
-      if (lane < NBI && ol < ob1) {
-        const int pos = block_pos(lane, o0 + ol);
-        const uint4 nb = *reinterpret_cast<const uint4*>(codes + ((size_t)ol * NBI + pos) * 16);
-        const float sc = half_bits(scales[ol * NBI + pos]);
-        float dot[1];
-        block_dot<1>(nb, hps, dot);
-        part[jj] = __fmul_rn(sc, __fmaf_rn(dot[0], 0x1p62f, hsum8));
+  for (int g = 0; g < G; ++g) hps[g] = hp[g];
+  const int H = a.H, HH = H >> 1;
+#pragma unroll 1
+  for (int o = (int)threadIdx.x; o < H; o += NT) {
+    const uint8_t* pc = (o < HH) ? dn0 : dn1;
+    const int ol = (o < HH) ? o : o - HH;
+    const uint4 nb = *reinterpret_cast<const uint4*>(pc + (size_t)ol * 16);
+    const float sc = half_bits(reinterpret_cast<const uint16_t*>(pc + (size_t)8 * H)[ol]);
+    float dot[G];
+    block_dot<G>(nb, hps, dot);
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float y = __fmul_rn(sc, __fmaf_rn(dot[g], 0x1p62f, hs8[g]));
+      const long long q = __float2ll_rn(y * 4294967296.0f);
+      atomicAdd(acc_copy + (size_t)row[g] * H + o, (unsigned long long)q);
+    }
+  }
+}
+
+__device__ __noinline__ void split_down(const RoundArgs& a, const Tables& T, const uint8_t* dn0, const uint8_t* dn1,
+                                           const float* s_hp, int p0, int Re, unsigned long long* acc_copy) {
+  int pr = 0;
+  for (; pr + 1 < Re; pr += 2) split_down_rows<2>(a, T, dn0, dn1, s_hp, p0, pr, acc_copy);
+  if (pr < Re) split_down_rows<1>(a, T, dn0, dn1, s_hp, p0, pr, acc_copy);
+}
+
+// This CTA's output slice [o0, o0 + no) of a finished layer: sum of the accumulator
+// copies -> fp32 output; the copies are cleared for the next layer.  Threads from
+// `first` on do it.
+__device__ __forceinline__ void split_finish(const RoundArgs& a, float* out, int o0, int no, int first) {
+  const size_t stride = (size_t)a.R * a.H;
+  for (int i = (int)threadIdx.x - first; i < a.R * no; i += NT - first) {
+    if (i < 0) break;
+    const int r = i / no, o = o0 + (i - r * no);
+    unsigned long long* p = a.acc + (size_t)r * a.H + o;
+    unsigned long long s = 0ull;
+#pragma unroll
+    for (int c = 0; c < kSplitCopies; ++c) s += __ldcg(p + c * stride);
+#pragma unroll
+    for (int c = 0; c < kSplitCopies; ++c) __stcg(p + c * stride, 0ull);
+    out[(size_t)r * a.H + o] = __fmul_rn(__ll2float_rn((long long)s), 0x1p-32f);
+  }
+}
+
+__device__ __forceinline__ void split_stamp(const RoundArgs& a, int l, int ph) {
+  if (a.phase_ts && threadIdx.x == 0)
+    a.phase_ts[((size_t)l * kSplitPhases + ph) * gridDim.x + blockIdx.x] = gtimer();
+}
+
+// NG: hidden blocks in groups of 32 lanes (1 up to H 1024, 2 above).  XR: one row, its
+// activation pairs in registers.  XS: the rows are staged as pairs in shared memory.
+template <int NG, bool XR, bool XS>
+__global__ void __launch_bounds__(NT, 1) k_split(const __grid_constant__ RoundArgs a) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = gridDim.x, H = a.H, NB = H >> 5, NS = a.I >> 5;
+  const SplitPlan P = split_plan(a.H, a.I, a.E, a.R, a.k, G);
+  const int nslot = P.nslot;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P.bars);
+  const uint32_t bar_router = smem_u32(bars + nslot);
+  uint8_t* ring = smem + P.ring;
+  float* s_rw = reinterpret_cast<float*>(smem + P.router);
+  float4* s_xp = reinterpret_cast<float4*>(smem + P.xp);
+  float* s_xs = reinterpret_cast<float*>(smem + P.xs);
+  float* s_part = reinterpret_cast<float*>(smem + P.part);
+  float* s_hp = reinterpret_cast<float*>(smem + P.hp);
+  int* s_range = reinterpret_cast<int*>(smem + P.misc);
+  Tables T{reinterpret_cast<int*>(smem + P.uni),     reinterpret_cast<int*>(smem + P.csr),
+           reinterpret_cast<int*>(smem + P.pair),    reinterpret_cast<float*>(smem + P.w),
+           reinterpret_cast<int*>(smem + P.nunion),  reinterpret_cast<int*>(smem + P.pos_ui),
+           reinterpret_cast<int*>(smem + P.pos_row), reinterpret_cast<int*>(smem + P.slot),
+           reinterpret_cast<int*>(smem + P.pick)};
+  unsigned* s_mask = reinterpret_cast<unsigned*>(ring);
+  int* s_off_e = reinterpret_cast<int*>(ring + (size_t)a.E * 4);
+  int* s_ids = reinterpret_cast<int*>(ring + (size_t)a.E * 8);
+  int* s_ui = reinterpret_cast<int*>(ring + (size_t)a.E * 8 + (size_t)a.R * a.k * 4);
+  int* s_rank = s_ui + a.E;
+  const int o0 = (int)(((long long)blockIdx.x * H) / G);
+  const int no = (int)(((long long)(blockIdx.x + 1) * H) / G) - o0;
+  const int fin0 = NT / 2;  // first thread of the output finishing pass
+  unsigned long long* acc_copy = a.acc + (size_t)(blockIdx.x % kSplitCopies) * a.R * H;
+  if (tid == 0) {
+    for (int i = 0; i <= nslot; ++i) mbar_init(smem_u32(bars + i), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    issue_router_rows(a, a.layer[0].router, s_rw, bar_router);
+  }
+  // the accumulator copies of this CTA's output slice start at zero (ordered before any
+  // other CTA's adds by the first grid barrier)
+  if (!a.route_only)
+    for (int i = tid; i < kSplitCopies * a.R * no; i += NT) {
+      const int c = i / (a.R * no), rem = i - c * (a.R * no), r = rem / no;
+      __stcg(a.acc + ((size_t)c * a.R + r) * H + o0 + (rem - r * no), 0ull);
+    }
+  __syncthreads();
+  unsigned ph_router = 0u;
+  const bool has_rows = router_rows_of_cta(a.E) > 0;
+  bool router_pend = has_rows;  // layer 0's rows are in flight
+  Sync sy;
+  long long jbase = 0;  // pieces issued by this CTA in earlier layers (ring position)
+  auto slot_of = [&](long long J) { return (int)(J % nslot); };
+  auto par_of = [&](long long J) { return (unsigned)((J / nslot) & 1); };
+  for (int l = 0; l < a.L; ++l) {
+    const LayerPtrs& W = a.layer[l];
+    const uint16_t* x = a.x + (size_t)l * a.R * H;
+    split_stamp(a, l, 0);
+    if (l > 0) split_finish(a, a.out + (size_t)(l - 1) * a.R * H, o0, no, fin0);
+    if (tid == 0 && l + 1 < a.L)  // the next layer's rows into L2 (its router reads them)
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(x + (size_t)a.R * H),
+                   "r"((unsigned)(a.R * H * 2))
+                   : "memory");
+    if (router_pend) {
+      const bool ok = mbar_wait_bounded(bar_router, ph_router, a.status, a.wait_cycles);
+      if (__syncthreads_or(!ok)) {
+        drain_and_abort(a, bars, nslot, 0, 0, true, bar_router, ph_router);
+        return;
+      }
+      ph_router ^= 1u;
+      router_pend = false;
+    }
+    router_phase(a, x, s_rw);
+    split_stamp(a, l, 1);
+    grid_arrive(a, sy);  // B1 (all logits written)
+    // the router rows are consumed: the next layer's move in
+    if (tid == 0 && l + 1 < a.L) issue_router_rows(a, a.layer[l + 1].router, s_rw, bar_router);
+    router_pend = has_rows && l + 1 < a.L;
+    for (int e = tid; e < a.E; e += NT) {
+      s_mask[e] = 0u;
+      s_rank[e] = INT_MAX;
+      int sl = e;
+      if (W.slot) {
+        sl = __ldg(W.slot + e);
+        if ((unsigned)sl >= (unsigned)W.n_slots) {
+          atomicOr(a.status, kStatusBadSlot);
+          sl = 0;
+        }
+      }
+      T.slot[e] = sl;
+    }
+    if (XS && !a.route_only) stage_xpairs(a, x, s_xp, s_xs);
+    if (!grid_wait(a, sy)) {
+      drain_and_abort(a, bars, nslot, 0, 0, router_pend, bar_router, ph_router);
+      return;
+    }
+    split_stamp(a, l, 2);
+    const int U = route_phase(a, T, s_mask, s_off_e, s_ids, s_ui, s_rank, l, 0, NS, s_range);
+    const bool one = route_one_ok(a);
+    if (a.route_only) {
+      if (one && warp == 1) softmax_one(a, T);
+      return;
+    }
+    (void)U;
+    const int u_beg = s_range[0], u_end = s_range[1];
+    const int nu = u_end - u_beg, npieces = nu * kPieces;
+    const int n_init = min(nslot, npieces);
+    if (tid == 0)
+      for (int j = 0; j < n_init; ++j) {
+        const long long J = jbase + j;
+        issue_piece(a, W, T, NS, u_beg, j, ring + (size_t)slot_of(J) * P.slot_bytes, smem_u32(bars + slot_of(J)));
+      }
+    if (one && warp == 1) softmax_one(a, T);
+    // one row: this lane's block of activation pairs in registers for the whole layer
+    f2_t xr[16];
+    float xsr = 0.f;
+    if (XR) {
+      const int b = 32 * (warp % NG) + lane;
+      if (b < NB) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const ulonglong2 f = *reinterpret_cast<const ulonglong2*>(s_xp + (size_t)c * NB + b);
+          xr[2 * c] = f.x;
+          xr[2 * c + 1] = f.y;
+        }
+        xsr = s_xs[b];
+      } else {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) xr[c] = 0ull;
       }
     }
-    const float y = warp_sum_multi<DG>(part, lane);
-    constexpr int LPV = 32 / DG;
-    if ((lane % LPV) == 0 && ob + lane / LPV < ob1) s_yw[ob + lane / LPV] = y;
+    split_stamp(a, l, 3);
+    __syncthreads();
+    int issued = n_init;  // pieces of this layer issued so far (thread 0's count, uniform)
+    long long consumed = jbase;
+    const int rb = warp / NG, kg = warp % NG;
+    const int my_piece = (rb * 4 * NG) >> 4;  // the gate/up piece holding this warp's rows
+    bool stamped = false;
+    for (int t = 0; t < nu; ++t) {
+      const int u = u_beg + t, ui = u / NS;
+      const int p0 = T.csr_off[ui], Re = T.csr_off[ui + 1] - p0;
+      if (t + 1 == nu) split_stamp(a, l, 5);
+      // ---- gate/up: each warp waits for its own piece ----
+      {
+        const long long J = jbase + (long long)t * kPieces + my_piece;
+        bool ok = mbar_wait_bounded(smem_u32(bars + slot_of(J)), par_of(J), a.status, a.wait_cycles);
+        if (ok) {
+          if (!stamped && warp == 0) {
+            split_stamp(a, l, 4);
+            stamped = true;
+          }
+          if (XR)
+            split_gateup<NG, true, true>(a, T, ring + (size_t)slot_of(J) * P.slot_bytes, rb, kg, p0, Re, xr, xsr,
+                                         s_xp, s_xs, x, s_part);
+          else
+            split_gateup_rows<NG, XS>(a, T, ring + (size_t)slot_of(J) * P.slot_bytes, rb, kg, p0, Re, s_xp, s_xs, x,
+                                      s_part);
+        }
+        if (__syncthreads_or(!ok)) {
+          drain_and_abort(a, bars, nslot, consumed, jbase + issued, router_pend, bar_router, ph_router);
+          return;
+        }
+      }
+      consumed = jbase + (long long)t * kPieces + kGuPieces;
+      if (tid == 0)
+        for (int q = 0; q < kGuPieces; ++q) {
+          const int j = t * kPieces + q + nslot;
+          if (j < npieces) {
+            const long long J = jbase + j;
+            issue_piece(a, W, T, NS, u_beg, j, ring + (size_t)slot_of(J) * P.slot_bytes, smem_u32(bars + slot_of(J)));
+          }
+        }
+      issued = min(npieces, max(issued, t * kPieces + kGuPieces + nslot));
+      split_swiglu(a, T, s_part, NG, p0, Re, s_hp);
+      __syncthreads();
+      // ---- down: every thread waits for both down pieces ----
+      {
+        const long long J0 = jbase + (long long)t * kPieces + kGuPieces, J1 = J0 + 1;
+        bool ok = mbar_wait_bounded(smem_u32(bars + slot_of(J0)), par_of(J0), a.status, a.wait_cycles) &&
+                  mbar_wait_bounded(smem_u32(bars + slot_of(J1)), par_of(J1), a.status, a.wait_cycles);
+        if (ok)
+          split_down(a, T, ring + (size_t)slot_of(J0) * P.slot_bytes, ring + (size_t)slot_of(J1) * P.slot_bytes, s_hp,
+                     p0, Re, acc_copy);
+        if (__syncthreads_or(!ok)) {
+          drain_and_abort(a, bars, nslot, consumed, jbase + issued, router_pend, bar_router, ph_router);
+          return;
+        }
+      }
+      consumed = jbase + (long long)(t + 1) * kPieces;
+      if (tid == 0)
+        for (int q = kGuPieces; q < kPieces; ++q) {
+          const int j = t * kPieces + q + nslot;
+          if (j < npieces) {
+            const long long J = jbase + j;
+            issue_piece(a, W, T, NS, u_beg, j, ring + (size_t)slot_of(J) * P.slot_bytes, smem_u32(bars + slot_of(J)));
+          }
+        }
+      issued = min(npieces, max(issued, (t + 1) * kPieces + nslot));
+    }
+    if (nu == 0) {
+      split_stamp(a, l, 4);
+      split_stamp(a, l, 5);
+    }
+    jbase += npieces;
+    split_stamp(a, l, 6);
+    if (!grid_sync(a, sy)) {  // B3: every add of this layer is in
+      drain_and_abort(a, bars, nslot, 0, 0, router_pend, bar_router, ph_router);
+      return;
+    }
+    split_stamp(a, l, 7);
   }
+  split_finish(a, a.out + (size_t)(a.L - 1) * a.R * H, o0, no, fin0);
 }
 
 // ---------------------------------------------------------------------------------
 // Wide verify rounds (at least kMmaRows rows): gate/up and down on the tensor cores
-// (mma.sync m16n8k16, bf16 operands, fp32 accumulation).
+// (mma.sync m16n8k16, bf16 operands, fp32 accumulation), SwiGLU outputs exchanged
+// between CTAs through the workspace.
+//
+// Per layer, with grid-wide barriers B1..B3 in between:
+//   P1  router GEMV (as above)
+//   B1
+//   P2  routing (as above)
+//   P3  gate/up: the U * I units (gate row i + up row i of a union expert) are split
+//       contiguously across CTAs by work and streamed through shared-memory slots with
+//       1-D bulk copies; h' = w silu(g) v goes to the workspace split into bf16 hi + lo.
+//       Meanwhile this CTA's down rows of every union expert are prefetched into L2.
+//   B2  (every h' written)
+//   P4  down: this CTA's output rows x groups of up to 16 of an expert's positions on the
+//       tensor cores; each row's picks are added in rank order.
+//   B3  (layer l+1's router waits for layer l's output)
 //
 // A nibble n in the low four bits of a bf16 whose other bits are those of 128.0 is the
 // bf16 value 128 + n, exactly; one mask-and-or per pair of weights (two nibbles 16 bits
@@ -1185,12 +1419,74 @@ constexpr int kMmaRows = 8;
 constexpr int kKPartsGu = 8;  // K parts of a gate/up tile (hidden blocks)
 constexpr int kKPartsDn = 4;  // K parts of a down tile (intermediate blocks)
 static_assert(NW % kKPartsGu == 0 && NW % kKPartsDn == 0, "a tile's K parts run in one round");
-// scratch of the tensor-core path inside the activation-pair region (unused then)
+constexpr int kGuSlots = 3;
+// scratch of the tensor-core path
 constexpr int kMmaMaxPos = 256;          // CSR positions (rows x top-k) of a wide round
 constexpr size_t kMmaPart = 0;           // [NW][2][16][8] fp32 partial tiles
 constexpr size_t kMmaY = (size_t)NW * 256 * 4;  // [kMmaMaxPos][16] fp32: y per position and output row
-static_assert(kMmaY + (size_t)kMmaMaxPos * 16 * 4 <= kXBytes, "wide scratch fits the activation region");
+constexpr size_t kMmaScratch = kMmaY + (size_t)kMmaMaxPos * 16 * 4;
 
+struct GuChunk {
+  int ui, i0, n;
+};
+
+// smem plan of the wide kernel: GU ring | MMA scratch | tables | chunk list | barriers
+struct WidePlan {
+  size_t gu_slot, gu, scratch, uni, csr, pair, w, pos_ui, pos_row, slot, pick, nunion, chunks, bars, total;
+  size_t ring;
+  int gu_cap;     // units per gate/up chunk
+  int max_orows;  // output rows per CTA (ceil(H / grid))
+  bool ok;
+};
+
+__host__ __device__ inline WidePlan wide_plan(int H, int I, int E, int R, int k, int grid) {
+  WidePlan p{};
+  const size_t unit = (size_t)H + (size_t)H / 8;
+  p.max_orows = (H + grid - 1) / grid;
+  const size_t tables = up128((size_t)E * 4) + up128((size_t)(E + 1) * 4) + 5 * up128((size_t)R * k * 4) +
+                        up128((size_t)E * 4) + 128 + up128(kGuSlots * 12 + 64) + 256;
+  const size_t fixed = tables + kMmaScratch;
+  const size_t limit = (size_t)225 * 1024;
+  size_t cap = fixed < limit ? ((limit - fixed) / kGuSlots) / unit : 0;
+  if (cap > NW) cap = NW;  // a chunk is one pass of the warps
+  p.gu_cap = (int)cap;
+  p.gu_slot = up128(cap * unit);
+  const int rows_per_cta = (E + grid - 1) / grid;
+  p.ring = kGuSlots * p.gu_slot;
+  const size_t scratch_need = ((size_t)4 * E + (size_t)R * k) * 4 + 16 + (size_t)(5 * NT + NW) * 4;
+  const size_t router_need = (size_t)rows_per_cta * H * 4;
+  if (p.ring < scratch_need) p.ring = up128(scratch_need);
+  if (p.ring < router_need) p.ring = up128(router_need);
+  size_t off = 0;
+  p.gu = off;      off += p.ring;
+  p.scratch = off; off += kMmaScratch;
+  p.uni = off;     off += up128((size_t)E * 4);
+  p.csr = off;     off += up128((size_t)(E + 1) * 4);
+  p.pair = off;    off += up128((size_t)R * k * 4);
+  p.w = off;       off += up128((size_t)R * k * 4);
+  p.pos_ui = off;  off += up128((size_t)R * k * 4);
+  p.pos_row = off; off += up128((size_t)R * k * 4);
+  p.slot = off;    off += up128((size_t)E * 4);
+  p.pick = off;    off += up128((size_t)R * k * 4);
+  p.nunion = off;  off += 128;
+  p.chunks = off;  off += up128(kGuSlots * 12 + 64);
+  p.bars = off;    off += 256;
+  p.total = off;
+  p.ok = cap >= 8 && p.max_orows <= 16 && (size_t)R * k <= kMmaMaxPos && p.total <= limit;
+  return p;
+}
+
+__device__ void issue_gu_chunk(const RoundArgs& a, const LayerPtrs& W, const Tables& T, uint8_t* dst,
+                               uint32_t bar, const GuChunk& c) {
+  const size_t H = (size_t)a.H, I = (size_t)a.I;
+  const size_t u = (size_t)T.slot[T.uni[c.ui]];
+  const size_t first = u * I + (size_t)c.i0;  // unit index within the bank
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  mbar_expect_tx(bar, (uint32_t)((size_t)c.n * (H + H / 8)));
+  bulk_g2s(smem_u32(dst), W.gu_nib + first * H, (uint32_t)(c.n * H), bar);
+  bulk_g2s(smem_u32(dst + (size_t)c.n * H),
+           reinterpret_cast<const uint8_t*>(W.gu_sc) + first * (H / 8), (uint32_t)(c.n * (H / 8)), bar);
+}
 
 // Gate/up of one staged chunk on the tensor cores.  A tile = 8 units of the chunk (A
 // row g: the gate row of unit g, row g + 8: its up row, so the eight lanes' rows have
@@ -1267,9 +1563,9 @@ __device__ void gateup_chunk_mma(const RoundArgs& a, const Tables& T, const uint
       float gs = 0.f, vs = 0.f;
 #pragma unroll
       for (int kp = 0; kp < kKPartsGu; ++kp) {
-        const float* P = s_part + (gl * kKPartsGu + kp) * 256 + nt * 128;
-        gs = __fadd_rn(gs, P[uu * 8 + cc]);
-        vs = __fadd_rn(vs, P[64 + uu * 8 + cc]);
+        const float* Pp = s_part + (gl * kKPartsGu + kp) * 256 + nt * 128;
+        gs = __fadd_rn(gs, Pp[uu * 8 + cc]);
+        vs = __fadd_rn(vs, Pp[64 + uu * 8 + cc]);
       }
       const int pp = p0 + col;
       const float hh = __fmul_rn(__fdiv_rn(gs, __fadd_rn(1.f, expf(-gs))), vs);
@@ -1288,13 +1584,15 @@ __device__ void gateup_chunk_mma(const RoundArgs& a, const Tables& T, const uint
 // One round of the wide down pass on the tensor cores: NW tile parts.  Assignment j ->
 // position group j / kKPartsDn (group = up to 16 consecutive CSR positions of one
 // expert: `gpe` groups per expert) and K part j % kKPartsDn; a tile = this CTA's output
-// rows (at most 16) x the group's positions (two n-tiles).  B = h' (hi + lo bf16,
-// fragment order) read from the workspace through L2, two MMAs per k16 step and n-tile.
-// y[position][output row] -> s_yall.
-__device__ void down_round_mma(const RoundArgs& a, const Tables& T, const uint8_t* dn, size_t dn_slot,
-                               size_t codes_room, int o0, int no, int j0, int n_asg, int gpe, float* s_part,
-                               float* s_yall) {
-  const int NBI = a.I >> 5;
+// rows (at most 16) x the group's positions (two n-tiles).  A = the down codes of this
+// CTA's rows, read from global memory (block-major: block b of rows o0.. of an expert is
+// contiguous, so the eight rows of a fragment are one 128-byte line; prefetched into L2
+// once the routing was known); B = h' (hi + lo bf16, fragment order) read from the
+// workspace through L2, two MMAs per k16 step and n-tile.  y[position][output row] ->
+// s_yall.
+__device__ void down_round_mma(const RoundArgs& a, const LayerPtrs& W, const Tables& T, int o0, int no, int j0,
+                               int n_asg, int gpe, float* s_part, float* s_yall) {
+  const int NBI = a.I >> 5, H = a.H;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const uint8_t* hb = reinterpret_cast<const uint8_t*>(a.hbuf);
   const int j = j0 + warp;
@@ -1304,50 +1602,64 @@ __device__ void down_round_mma(const RoundArgs& a, const Tables& T, const uint8_
     const int ui = gi / gpe, p0 = T.csr_off[ui] + 16 * (gi - ui * gpe);
     const int cnt = min(16, T.csr_off[ui + 1] - p0);
     if (cnt > 0) {
-      const uint8_t* codes = dn + (size_t)(ui % kDnSlots) * dn_slot;
-      const uint16_t* scales = reinterpret_cast<const uint16_t*>(codes + codes_room);
+      const size_t sl = (size_t)T.slot[T.uni[ui]];
       // output rows past this CTA's repeat its last one; their results are dropped
       const int ra = min(g, no - 1), rb = min(g + 8, no - 1);
-      const int ka = (o0 + ra) & 7, kb = (o0 + rb) & 7;
-      const uint32_t* wa_ = reinterpret_cast<const uint32_t*>(codes + (size_t)ra * NBI * 16) + t;
-      const uint32_t* wb_ = reinterpret_cast<const uint32_t*>(codes + (size_t)rb * NBI * 16) + t;
-      const uint16_t* sa_ = scales + (size_t)ra * NBI;
-      const uint16_t* sb_ = scales + (size_t)rb * NBI;
+      const size_t rowa = sl * NBI * H + o0 + ra, rowb = sl * NBI * H + o0 + rb;
+      const uint32_t* wa_ = reinterpret_cast<const uint32_t*>(W.dn_nib + rowa * 16) + t;
+      const uint32_t* wb_ = reinterpret_cast<const uint32_t*>(W.dn_nib + rowb * 16) + t;
+      const uint16_t* sa_ = W.dn_sc + rowa;
+      const uint16_t* sb_ = W.dn_sc + rowb;
+      const size_t bstride_w = (size_t)H * 4;  // 32-bit words between blocks of one row
       // columns past the group's positions repeat its last one; their results are dropped
       const bool two = cnt > 8;
       const uint4* h0 = reinterpret_cast<const uint4*>(hb + (size_t)(p0 + min(g, cnt - 1)) * NBI * 128) + 2 * t;
       const uint4* h1 = reinterpret_cast<const uint4*>(hb + (size_t)(p0 + min(g + 8, cnt - 1)) * NBI * 128) + 2 * t;
       const int b0 = (kp * NBI) / kKPartsDn, b1 = ((kp + 1) * NBI) / kKPartsDn;
-#pragma unroll 2
-      for (int b = b0; b < b1; ++b) {
-        const int pa = b ^ ka, pb = b ^ kb;
-        uint32_t fa[4], fb[4];
-        dq_word(wa_[4 * pa], fa);
-        dq_word(wb_[4 * pb], fb);
-        const float sa = half_bits(sa_[pa]), sb = half_bits(sb_[pb]);
-        {
-          const uint4 hi = __ldcg(h0 + 8 * b), lo = __ldcg(h0 + 8 * b + 1);
-          float d[4] = {0.f, 0.f, 0.f, 0.f};
-          mma_bf16(d, fa[0], fb[0], fa[1], fb[1], hi.x, hi.y);
-          mma_bf16(d, fa[0], fb[0], fa[1], fb[1], lo.x, lo.y);
-          mma_bf16(d, fa[2], fb[2], fa[3], fb[3], hi.z, hi.w);
-          mma_bf16(d, fa[2], fb[2], fa[3], fb[3], lo.z, lo.w);
-          acc[0][0] = __fmaf_rn(sa, d[0], acc[0][0]);
-          acc[0][1] = __fmaf_rn(sa, d[1], acc[0][1]);
-          acc[0][2] = __fmaf_rn(sb, d[2], acc[0][2]);
-          acc[0][3] = __fmaf_rn(sb, d[3], acc[0][3]);
+      for (int bb = b0; bb < b1; bb += 4) {
+        // the codes and scales of up to four blocks are loaded before any is used
+        uint32_t wa[4], wb[4];
+        float sa[4], sb[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int b = min(bb + q, b1 - 1);
+          wa[q] = __ldg(wa_ + (size_t)b * bstride_w);
+          wb[q] = __ldg(wb_ + (size_t)b * bstride_w);
+          sa[q] = half_bits(__ldg(sa_ + (size_t)b * H));
+          sb[q] = half_bits(__ldg(sb_ + (size_t)b * H));
         }
-        if (two) {
-          const uint4 hi = __ldcg(h1 + 8 * b), lo = __ldcg(h1 + 8 * b + 1);
-          float d[4] = {0.f, 0.f, 0.f, 0.f};
-          mma_bf16(d, fa[0], fb[0], fa[1], fb[1], hi.x, hi.y);
-          mma_bf16(d, fa[0], fb[0], fa[1], fb[1], lo.x, lo.y);
-          mma_bf16(d, fa[2], fb[2], fa[3], fb[3], hi.z, hi.w);
-          mma_bf16(d, fa[2], fb[2], fa[3], fb[3], lo.z, lo.w);
-          acc[1][0] = __fmaf_rn(sa, d[0], acc[1][0]);
-          acc[1][1] = __fmaf_rn(sa, d[1], acc[1][1]);
-          acc[1][2] = __fmaf_rn(sb, d[2], acc[1][2]);
-          acc[1][3] = __fmaf_rn(sb, d[3], acc[1][3]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int b = bb + q;
+          if (b < b1) {
+            uint32_t fa[4], fb[4];
+            dq_word(wa[q], fa);
+            dq_word(wb[q], fb);
+            {
+              const uint4 hi = __ldcg(h0 + 8 * b), lo = __ldcg(h0 + 8 * b + 1);
+              float d[4] = {0.f, 0.f, 0.f, 0.f};
+              mma_bf16(d, fa[0], fb[0], fa[1], fb[1], hi.x, hi.y);
+              mma_bf16(d, fa[0], fb[0], fa[1], fb[1], lo.x, lo.y);
+              mma_bf16(d, fa[2], fb[2], fa[3], fb[3], hi.z, hi.w);
+              mma_bf16(d, fa[2], fb[2], fa[3], fb[3], lo.z, lo.w);
+              acc[0][0] = __fmaf_rn(sa[q], d[0], acc[0][0]);
+              acc[0][1] = __fmaf_rn(sa[q], d[1], acc[0][1]);
+              acc[0][2] = __fmaf_rn(sb[q], d[2], acc[0][2]);
+              acc[0][3] = __fmaf_rn(sb[q], d[3], acc[0][3]);
+            }
+            if (two) {
+              const uint4 hi = __ldcg(h1 + 8 * b), lo = __ldcg(h1 + 8 * b + 1);
+              float d[4] = {0.f, 0.f, 0.f, 0.f};
+              mma_bf16(d, fa[0], fb[0], fa[1], fb[1], hi.x, hi.y);
+              mma_bf16(d, fa[0], fb[0], fa[1], fb[1], lo.x, lo.y);
+              mma_bf16(d, fa[2], fb[2], fa[3], fb[3], hi.z, hi.w);
+              mma_bf16(d, fa[2], fb[2], fa[3], fb[3], lo.z, lo.w);
+              acc[1][0] = __fmaf_rn(sa[q], d[0], acc[1][0]);
+              acc[1][1] = __fmaf_rn(sa[q], d[1], acc[1][1]);
+              acc[1][2] = __fmaf_rn(sb[q], d[2], acc[1][2]);
+              acc[1][3] = __fmaf_rn(sb[q], d[3], acc[1][3]);
+            }
+          }
         }
       }
     }
@@ -1369,59 +1681,34 @@ __device__ void down_round_mma(const RoundArgs& a, const Tables& T, const uint8_
   __syncthreads();
 }
 
-// Exchanged h rows of CSR positions [pa, pb) (contiguous in the workspace) -> slot.
-__device__ __forceinline__ void issue_hbatch(const RoundArgs& a, uint8_t* dst, uint32_t bar, int pa, int pb) {
-  const size_t bytes = (size_t)(pb - pa) * a.I * 4;
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  mbar_expect_tx(bar, (uint32_t)bytes);
-  bulk_g2s(smem_u32(dst), a.hbuf + (size_t)pa * a.I, (uint32_t)bytes, bar);
+// This CTA's down rows [o0, o0 + no) of every union expert into L2 (they depend only on
+// the routing and are read by the down pass after the h exchange): per expert and block,
+// one bulk prefetch of the codes and one of the scales (rounded out to 16 bytes).
+__device__ void prefetch_down_rows(const RoundArgs& a, const LayerPtrs& W, const Tables& T, int U, int o0, int no) {
+  const int NBI = a.I >> 5, H = a.H;
+  for (int i = threadIdx.x; i < U * NBI; i += NT) {
+    const int ui = i / NBI, b = i - ui * NBI;
+    const size_t row = ((size_t)T.slot[T.uni[ui]] * NBI + b) * H + o0;
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(W.dn_nib + row * 16), "r"((unsigned)(no * 16))
+                 : "memory");
+    const uintptr_t s0 = reinterpret_cast<uintptr_t>(W.dn_sc + row) & ~(uintptr_t)15;
+    const uintptr_t s1 = (reinterpret_cast<uintptr_t>(W.dn_sc + row + no) + 15) & ~(uintptr_t)15;
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(s0), "r"((unsigned)(s1 - s0)) : "memory");
+  }
 }
 
-// Leaving early: gives every copy still in flight a bounded chance to land (so no bulk
-// copy targets shared memory of an exited CTA) and raises the abort flag.  Out of line:
-// it never runs on the normal path.
-__device__ __noinline__ void drain_and_abort(const RoundArgs& a, const uint64_t* bars, unsigned gu_pend,
-                                             unsigned gu_ph, unsigned dn_pend, unsigned dn_ph,
-                                             unsigned h_pend, unsigned h_ph, bool router_pend,
-                                             unsigned ph_router) {
-  for (int q = 0; q < kGuSlots; ++q)
-    if (gu_pend & (1u << q))
-      mbar_wait_bounded(smem_u32(bars + q), (gu_ph >> q) & 1u, a.status, kDefaultWaitCycles);
-  for (int q = 0; q < kDnSlots; ++q)
-    if (dn_pend & (1u << q))
-      mbar_wait_bounded(smem_u32(bars + kGuSlots + q), (dn_ph >> q) & 1u, a.status, kDefaultWaitCycles);
-  for (int q = 0; q < 2; ++q)
-    if (h_pend & (1u << q))
-      mbar_wait_bounded(smem_u32(bars + kGuSlots + kDnSlots + 1 + q), (h_ph >> q) & 1u, a.status,
-                        kDefaultWaitCycles);
-  if (router_pend)
-    mbar_wait_bounded(smem_u32(bars + kGuSlots + kDnSlots), ph_router, a.status, kDefaultWaitCycles);
-  if (threadIdx.x == 0) atomicExch(a.bar + 33, 1u);
-}
-
-// NBL: 32-element blocks per lane along H (1 up to H 1024, 2 above).  WIDE: the round
-// has enough rows for the tensor-core gate/up and down (wide_round() on the host).
-template <int NBL, bool WIDE>
 __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundArgs a) {
   extern __shared__ __align__(1024) unsigned char smem[];
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x;
   const int G = gridDim.x;
-  const SmemPlan P = smem_plan(a.H, a.I, a.E, a.Rmax, a.k, G);
-  // mbarriers: kGuSlots GU slots, kDnSlots DN slots, the router rows, two h slots
+  const WidePlan P = wide_plan(a.H, a.I, a.E, a.R, a.k, G);
+  // mbarriers: kGuSlots GU slots, the router rows
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P.bars);
-  const int bar_dn0 = kGuSlots, bar_h0 = kGuSlots + kDnSlots + 1;
-  const uint32_t bar_router = smem_u32(bars + kGuSlots + kDnSlots);
+  const uint32_t bar_router = smem_u32(bars + kGuSlots);
   uint8_t* gu = smem + P.gu;
-  uint8_t* dn = smem + P.dn;
-  float4* s_xp = reinterpret_cast<float4*>(smem + P.xrows);
-  float* s_xs = reinterpret_cast<float*>(smem + P.xrows + (size_t)a.R * a.H * 4);
-  constexpr bool mma = WIDE;  // tensor-core gate/up and down
-  const bool x_staged = !mma && (size_t)a.R * a.H * 4 + (size_t)a.R * (a.H >> 5) * 4 <= kXBytes;
-  float* s_mpart = reinterpret_cast<float*>(smem + P.xrows + kMmaPart);
-  float* s_yall = reinterpret_cast<float*>(smem + P.xrows + kMmaY);
+  float* s_mpart = reinterpret_cast<float*>(smem + P.scratch + kMmaPart);
+  float* s_yall = reinterpret_cast<float*>(smem + P.scratch + kMmaY);
   float* s_rw = reinterpret_cast<float*>(gu);
-  float* s_acc = reinterpret_cast<float*>(smem + P.acc);
-  float* s_y = reinterpret_cast<float*>(smem + P.ybuf);
   GuChunk* s_chunks = reinterpret_cast<GuChunk*>(smem + P.chunks);
   Tables T{reinterpret_cast<int*>(smem + P.uni),     reinterpret_cast<int*>(smem + P.csr),
            reinterpret_cast<int*>(smem + P.pair),    reinterpret_cast<float*>(smem + P.w),
@@ -1435,7 +1722,7 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
   int* s_ui = reinterpret_cast<int*>(gu + (size_t)a.E * 8 + (size_t)a.R * a.k * 4);
   int* s_rank = s_ui + a.E;
   if (tid == 0) {
-    for (int i = 0; i < bar_h0 + 2; ++i) mbar_init(smem_u32(bars + i), 1);
+    for (int i = 0; i < kGuSlots + 1; ++i) mbar_init(smem_u32(bars + i), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     issue_router_rows(a, a.layer[0].router, s_rw, bar_router);
   }
@@ -1443,31 +1730,19 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
   unsigned ph_router = 0u;
   bool router_pend = router_rows_of_cta(a.E) > 0;  // layer 0's rows are in flight
   Sync sy;
-  unsigned gu_ph = 0u, gu_pend = 0u;  // bit q: parity / in flight, GU slot q
-  unsigned dn_ph = 0u, dn_pend = 0u;  // bit q: parity / in flight, DN slot q
-  unsigned h_ph = 0u, h_pend = 0u;    // bit q: parity / in flight, h slot q
-  auto bail = [&]() {
-    drain_and_abort(a, bars, gu_pend, gu_ph, dn_pend, dn_ph, h_pend, h_ph, router_pend, ph_router);
-  };
-  // waits for one mbarrier phase with every thread; false (after bail) if it gave up
-  auto wait_all = [&](int bi, unsigned& ph, unsigned& pend, int q) -> bool {
-    const bool ok = mbar_wait_bounded(smem_u32(bars + bi), (ph >> q) & 1u, a.status, a.wait_cycles);
-    if (__syncthreads_or(!ok)) {
-      bail();
-      return false;
-    }
-    ph ^= 1u << q;
-    pend &= ~(1u << q);
-    return true;
-  };
+  unsigned gu_ph = 0u;            // bit q: parity of GU slot q
   const size_t RH = (size_t)a.R * a.H;
   const int o0 = (int)(((long long)blockIdx.x * a.H) / G);
   const int no = (int)(((long long)(blockIdx.x + 1) * a.H) / G) - o0;
-  const size_t codes_room = up128((size_t)P.max_orows * (a.I / 2));
-  // CSR positions per down wave: at most one per warp, per h-slot row, and per DN slot
-  // (a wave spans at most WV experts, all inside the window of issued DN slots)
-  const int WV = min(min(P.h_rows, NW), kDnSlots);
-  auto hslot = [&](int q) { return gu + kHOffset + (size_t)q * P.h_slot; };
+  // the GU slots in flight: bit q set
+  unsigned gu_pend = 0u;
+  auto bail = [&]() {
+    if (tid == 0) {
+      for (int q = 0; q < kGuSlots; ++q)
+        if (gu_pend & (1u << q)) mbar_wait_bounded(smem_u32(bars + q), (gu_ph >> q) & 1u, a.status, kDefaultWaitCycles);
+    }
+    drain_and_abort(a, bars, 1, 0, 0, router_pend, bar_router, ph_router);
+  };
   for (int l = 0; l < a.L; ++l) {
     const LayerPtrs& W = a.layer[l];
     const uint16_t* x = a.x + (size_t)l * RH;
@@ -1483,13 +1758,10 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
     }
     router_phase(a, x, s_rw);
     stamp(a, l, 1);
-    // B1 (all logits written); the activation pairs are built while it completes
-    grid_arrive(a, sy);
+    grid_arrive(a, sy);  // B1 (all logits written)
     for (int e = tid; e < a.E; e += NT) {  // (the router rows there are consumed)
       s_mask[e] = 0u;
       s_rank[e] = INT_MAX;
-      // this layer's expert -> slot table (ingress data); an entry outside the bank is
-      // reported and replaced by slot 0, so no copy leaves the bank
       int sl = e;
       if (W.slot) {
         sl = __ldg(W.slot + e);
@@ -1500,30 +1772,18 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
       }
       T.slot[e] = sl;
     }
-    if (x_staged && !a.route_only) stage_xpairs(a, x, s_xp, s_xs);
     if (!grid_wait(a, sy)) {
       bail();
       return;
     }
     stamp(a, l, 2);
     int* s_range = reinterpret_cast<int*>(smem + P.chunks + kGuSlots * 12 + 20);
-    const int U = route_phase(a, T, s_mask, s_off_e, s_ids, s_ui, s_rank, l, mma ? 1 : 0, s_range);
+    const int U = route_phase(a, T, s_mask, s_off_e, s_ids, s_ui, s_rank, l, 1, a.I, s_range);
     stamp(a, l, 3);
-    const bool one = route_one_ok(a);  // the picks' weights are still to be computed
-    if (a.route_only) {
-      if (one && warp == 1) softmax_one(a, T);
-      return;
-    }
     // ---- this CTA's share of the gate/up units (cut during routing); chunks issued
     // through the ring: thread 0 cuts them lazily (stopping at expert boundaries and the
-    // slot size) and leaves the descriptor of chunk n in ring entry n % kGuSlots when it
-    // issues it ----
-    // thread 0's chunk cursor lives in shared memory (cur, end, expert, offset), so no
-    // thread carries it in registers through the gate/up loop
+    // slot size) and leaves the descriptor of chunk n in ring entry n % kGuSlots ----
     int* s_cursor = reinterpret_cast<int*>(smem + P.chunks + kGuSlots * 12 + 4);
-    // on the CUDA-core path the first chunk leaves the last warp without a unit: that
-    // warp issues the rest of the ring and the down prefetch while the others compute
-    const int cap0 = mma ? P.gu_cap : min(P.gu_cap, NW - 1);
     auto next_chunk = [&](int cap) {
       int cur = s_cursor[0], ui = s_cursor[2], i0 = s_cursor[3];
       int nn = s_cursor[1] - cur;
@@ -1547,106 +1807,51 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
       s_cursor[1] = g_end;
       s_cursor[2] = g_cur / a.I;
       s_cursor[3] = g_cur - (g_cur / a.I) * a.I;
-    }
-    if (tid == 0) {
-      // count the chunks (same cuts as next_chunk), then describe the first ring's worth
       int nc = 0;
       for (int cur = g_cur, i0 = s_cursor[3]; cur < g_end; ++nc) {
         int nn = g_end - cur;
         if (nn > a.I - i0) nn = a.I - i0;
-        const int cap = nc == 0 ? cap0 : P.gu_cap;
-        if (nn > cap) nn = cap;
+        if (nn > P.gu_cap) nn = P.gu_cap;
         cur += nn;
         i0 = (i0 + nn == a.I) ? 0 : i0 + nn;
       }
-      for (int q = 0; q < kGuSlots && q < nc; ++q) s_chunks[q] = next_chunk(q == 0 ? cap0 : P.gu_cap);
+      for (int q = 0; q < kGuSlots && q < nc; ++q) {
+        s_chunks[q] = next_chunk(P.gu_cap);
+        issue_gu_chunk(a, W, T, gu + q * P.gu_slot, smem_u32(bars + q), s_chunks[q]);
+      }
       *reinterpret_cast<int*>(smem + P.chunks + kGuSlots * 12) = nc;
-      // the first chunk goes out at once (thread 0 is its only issuer)
-      static_assert(kGuFirst == 1, "thread 0 issues the first chunk");
-      if (nc > 0) issue_gu_chunk(a, W, T, gu, smem_u32(bars), s_chunks[0]);
-    } else if (one && warp == 1) {
-      softmax_one(a, T);  // meanwhile
     }
+    // this CTA's down rows of every union expert are needed after B2: into L2 now
+    if (no > 0) prefetch_down_rows(a, W, T, U, o0, no);
     __syncthreads();
     const int n_chunks = *reinterpret_cast<const int*>(smem + P.chunks + kGuSlots * 12);
-    const int n_first = min(kGuFirst, n_chunks), n_ring = min(kGuSlots, n_chunks);
-    gu_pend |= (1u << n_first) - 1u;
-    // the down prefetch goes out once the first gate/up chunk has landed, so it does not
-    // delay that chunk (it is needed only after B2)
-    const int iss = mma ? 0 : NT - 32;  // first thread of the issuing warp
-    auto issue_dn_prefetch = [&]() {
-      if (no > 0) {
-        const int nq = min(U, kDnSlots);
-        dn_pend |= (1u << nq) - 1u;
-        if (tid == iss) {
-#pragma unroll 1
-          for (int q = 0; q < nq; ++q)
-            issue_dn_chunk(a, W, T, dn + q * P.dn_slot, smem_u32(bars + bar_dn0 + q), q, o0, no, codes_room);
-        }
-      }
-    };
+    gu_pend = (1u << min(kGuSlots, n_chunks)) - 1u;
     // ---- gate/up ----
-    auto gu_loop = [&](auto&& compute) -> bool {
-      for (int n = 0; n < n_chunks; ++n) {
-        const int q = n % kGuSlots;
-        if (!wait_all(q, gu_ph, gu_pend, q)) return false;
-        if (n == 0) {
-          stamp(a, l, 4);
-          gu_pend |= ((1u << n_ring) - 1u) & ~((1u << n_first) - 1u);
-          const int qi = tid - iss;
-          if (qi >= n_first && qi < n_ring)
-            issue_gu_chunk(a, W, T, gu + qi * P.gu_slot, smem_u32(bars + qi), s_chunks[qi]);
-          issue_dn_prefetch();
-        }
-        stamp(a, l, 5);  // (the last chunk's stamp stays)
-        const GuChunk c = s_chunks[q];
-        const uint8_t* slot = gu + q * P.gu_slot;
-        compute(slot, c);
-        __syncthreads();  // slot q free again
-        if (n + kGuSlots < n_chunks) {
-          gu_pend |= 1u << q;
-          if (tid == 0) {
-            s_chunks[q] = next_chunk(P.gu_cap);
-            issue_gu_chunk(a, W, T, gu + q * P.gu_slot, smem_u32(bars + q), s_chunks[q]);
-          }
+    for (int n = 0; n < n_chunks; ++n) {
+      const int q = n % kGuSlots;
+      const bool ok = mbar_wait_bounded(smem_u32(bars + q), (gu_ph >> q) & 1u, a.status, a.wait_cycles);
+      if (__syncthreads_or(!ok)) {
+        bail();
+        return;
+      }
+      gu_ph ^= 1u << q;
+      gu_pend &= ~(1u << q);
+      if (n == 0) stamp(a, l, 4);
+      stamp(a, l, 5);  // (the last chunk's stamp stays)
+      const GuChunk c = s_chunks[q];
+      gateup_chunk_mma(a, T, gu + q * P.gu_slot, c, x, s_mpart);
+      __syncthreads();  // slot q free again
+      if (n + kGuSlots < n_chunks) {
+        gu_pend |= 1u << q;
+        if (tid == 0) {
+          s_chunks[q] = next_chunk(P.gu_cap);
+          issue_gu_chunk(a, W, T, gu + q * P.gu_slot, smem_u32(bars + q), s_chunks[q]);
         }
       }
-      return true;
-    };
-    bool gu_ok;
-    if (!mma && x_staged && a.R == 1) {
-      // one row: the lane's first block of activation pairs lives in registers
-      const int NB = a.H >> 5, lane = tid & 31;
-      f2_t xr[16];
-      if (lane < NB) {
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const ulonglong2 f = *reinterpret_cast<const ulonglong2*>(s_xp + (size_t)c * NB + lane);
-          xr[2 * c] = f.x;
-          xr[2 * c + 1] = f.y;
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < 16; ++c) xr[c] = 0ull;
-      }
-      gu_ok = gu_loop([&](const uint8_t* slot, const GuChunk& c) {
-        gateup_chunk_r1<NBL>(a, T, slot, c, xr, s_xp, s_xs);
-      });
-    } else {
-      gu_ok = gu_loop([&](const uint8_t* slot, const GuChunk& c) {
-        if (mma)
-          gateup_chunk_mma(a, T, slot, c, x, s_mpart);
-        else if (x_staged)
-          gateup_chunk<NBL, true>(a, T, slot, c, x, s_xp, s_xs);
-        else
-          gateup_chunk<NBL, false>(a, T, slot, c, x, s_xp, s_xs);
-      });
     }
-    if (!gu_ok) return;
     if (n_chunks == 0) {
       stamp(a, l, 4);
       stamp(a, l, 5);
-      issue_dn_prefetch();
     }
     // the next layer's router rows can move in now (the GU ring is idle until then)
     if (l + 1 < a.L && router_rows_of_cta(a.E) > 0) {
@@ -1659,47 +1864,13 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
       return;
     }
     stamp(a, l, 7);
-    if (mma && no > 0) {
+    stamp(a, l, 8);
+    if (no > 0) {
       // ---- wide down: groups of up to 16 of one expert's positions on the tensor cores ----
       const int gpe = (a.R + 15) >> 4;  // position groups per expert
       const int per_e = gpe * kKPartsDn, n_asg = U * per_e;
-      stamp(a, l, 8);
-      int waited = 0, rel = 0;
-      for (int j0 = 0; j0 < n_asg; j0 += NW) {
-        const int j1 = min(j0 + NW, n_asg);
-        // the round's experts must have landed: one waiting thread per slot
-        const int need = (j1 - 1) / per_e + 1;
-        if (need > waited) {
-          bool ok = true;
-          if (tid < need - waited) {
-            const int qd = (waited + tid) % kDnSlots;
-            ok = mbar_wait_bounded(smem_u32(bars + bar_dn0 + qd), (dn_ph >> qd) & 1u, a.status, a.wait_cycles);
-          }
-          if (__syncthreads_or(!ok)) {
-            bail();
-            return;
-          }
-          for (int u = waited; u < need; ++u) {
-            const int qd = u % kDnSlots;
-            dn_ph ^= 1u << qd;
-            dn_pend &= ~(1u << qd);
-          }
-          waited = need;
-        }
-        stamp(a, l, 9);  // (the last round's stamp stays)
-        down_round_mma(a, T, dn, P.dn_slot, codes_room, o0, no, j0, n_asg, gpe, s_mpart, s_yall);
-        // experts whose groups are all done hand their slots to later experts
-        const int rel_new = (j1 < n_asg) ? j1 / per_e : U;
-        if (tid < rel_new - rel && rel + tid + kDnSlots < U) {
-          const int e = rel + tid, qd = e % kDnSlots;
-          issue_dn_chunk(a, W, T, dn + (size_t)qd * P.dn_slot, smem_u32(bars + bar_dn0 + qd), e + kDnSlots, o0, no,
-                         codes_room);
-        }
-        for (int e = rel; e < rel_new; ++e)
-          if (e + kDnSlots < U) dn_pend |= 1u << (e % kDnSlots);
-        rel = rel_new;
-      }
-      if (n_asg == 0) stamp(a, l, 9);
+      for (int j0 = 0; j0 < n_asg; j0 += NW) down_round_mma(a, W, T, o0, no, j0, n_asg, gpe, s_mpart, s_yall);
+      stamp(a, l, 9);
       stamp(a, l, 10);
       // each row's picks in rank order
       float* out = a.out + (size_t)l * RH;
@@ -1712,92 +1883,7 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
         }
         out[(size_t)r * a.H + o0 + ol] = acc;
       }
-    } else if (no > 0) {
-      // ---- down: waves of WV consecutive CSR positions, one warp per position ----
-      for (int i = tid; i < a.R * kAccStride; i += NT) s_acc[i] = 0.f;
-      __syncthreads();
-      const int total = T.csr_off[U];
-      for (int q = 0; q < 2 && q * WV < total; ++q) {
-        h_pend |= 1u << q;
-        if (tid == 0) issue_hbatch(a, hslot(q), smem_u32(bars + bar_h0 + q), q * WV, min((q + 1) * WV, total));
-      }
-      int waited = 0;  // the DN slots of union experts [0, waited) have landed
-      int rel = 0;     // union experts [0, rel) are finished and their slots reused
-      for (int n = 0, pa = 0; pa < total; ++n, pa += WV) {
-        const int pb = min(pa + WV, total);
-        const int qh = n & 1;
-        if (!wait_all(bar_h0 + qh, h_ph, h_pend, qh)) return;
-        if (n == 0) stamp(a, l, 8);
-        // the experts of this wave's positions must have landed: one waiting thread per slot
-        const int need = T.pos_ui[pb - 1] + 1;
-        if (need > waited) {
-          bool ok = true;
-          if (tid < need - waited) {
-            const int qd = (waited + tid) % kDnSlots;
-            ok = mbar_wait_bounded(smem_u32(bars + bar_dn0 + qd), (dn_ph >> qd) & 1u, a.status, a.wait_cycles);
-          }
-          if (__syncthreads_or(!ok)) {
-            bail();
-            return;
-          }
-          for (int u = waited; u < need; ++u) {
-            const int qd = u % kDnSlots;
-            dn_ph ^= 1u << qd;
-            dn_pend &= ~(1u << qd);
-          }
-          waited = need;
-        }
-        stamp(a, l, 9);  // (the last wave's stamp stays)
-        {
-          // positions of the wave over the warps; spare warps split a position's rows
-          const int npos = pb - pa, wpp = NW / npos;
-          const int pi = warp / wpp, part = warp - pi * wpp;
-          if (pi < npos) {
-            const int pp = pa + pi;
-            const int ui = T.pos_ui[pp];
-            down_position(a, dn + (size_t)(ui % kDnSlots) * P.dn_slot, codes_room, o0, (part * no) / wpp,
-                          ((part + 1) * no) / wpp,
-                          reinterpret_cast<const float4*>(hslot(qh) + (size_t)pi * a.I * 4),
-                          s_y + pi * kAccStride);
-          }
-        }
-        __syncthreads();
-        // combine in CSR order: for each row its experts ascending
-        for (int i = tid; i < a.R * no; i += NT) {
-          const int r = i / no, ol = i - r * no;
-          float acc = s_acc[r * kAccStride + ol];
-#pragma unroll 4
-          for (int pp = pa; pp < pb; ++pp)
-            if (T.pos_row[pp] == r) acc = __fadd_rn(acc, s_y[(pp - pa) * kAccStride + ol]);
-          s_acc[r * kAccStride + ol] = acc;
-        }
-        // experts finished by this wave hand their slots to later experts (one issuing
-        // thread per slot)
-        const int rel_new = (pb < total) ? T.pos_ui[pb] : U;
-        if (tid < rel_new - rel && rel + tid + kDnSlots < U) {
-          const int e = rel + tid, qd = e % kDnSlots;
-          issue_dn_chunk(a, W, T, dn + (size_t)qd * P.dn_slot, smem_u32(bars + bar_dn0 + qd), e + kDnSlots, o0, no,
-                         codes_room);
-        }
-        for (int e = rel; e < rel_new; ++e)
-          if (e + kDnSlots < U) dn_pend |= 1u << (e % kDnSlots);
-        rel = rel_new;
-        // the wave after next into this h slot
-        const int na = pa + 2 * WV;
-        if (na < total) {
-          h_pend |= 1u << qh;
-          if (tid == 0) issue_hbatch(a, hslot(qh), smem_u32(bars + bar_h0 + qh), na, min(na + WV, total));
-        }
-      }
-      __syncthreads();
-      stamp(a, l, 10);
-      float* out = a.out + (size_t)l * RH;
-      for (int i = tid; i < a.R * no; i += NT) {
-        const int r = i / no, ol = i - (i / no) * no;
-        out[(size_t)r * a.H + o0 + ol] = s_acc[r * kAccStride + ol];
-      }
     } else {
-      stamp(a, l, 8);
       stamp(a, l, 9);
       stamp(a, l, 10);
     }
@@ -1851,6 +1937,8 @@ struct moe_handle {
   size_t ev_used = 0;
   long long* phase_ts = nullptr;  // [kMaxLayers][kPhases][sm_count]
   int32_t phase_layers = 0;
+  int last_kind = 0;   // kernel of the most recent launch (kKindSplit / kKindWide)
+  int phase_kind = 0;  // kernel of the last profiled round
 };
 
 namespace {
@@ -1873,8 +1961,6 @@ struct DeviceGuard {
 
 bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int nbl_of(int H) { return (H + 1023) / 1024; }
-
 int check_layer(const moe_layer_w* w) {
   if (!w) return MOE_EINVAL;
   if (!aligned16(w->router) || !aligned16(w->gateup_nib) || !aligned16(w->gateup_scale) ||
@@ -1885,50 +1971,88 @@ int check_layer(const moe_layer_w* w) {
   return MOE_OK;
 }
 
+typedef void (*KernelFn)(RoundArgs);
+enum { kKindSplit = 0, kKindWide = 1 };
+
+// The kernel instantiations that can serve a hidden size: the split kernel with one row
+// in registers, with staged rows, with rows read from global memory; the wide kernel.
+struct KernelSet {
+  KernelFn split_xr, split_xs, split_gx, wide;
+};
+
+KernelSet kernels_for(int H) {
+  if ((((H >> 5) + 31) >> 5) == 1)
+    return {k_split<1, true, true>, k_split<1, false, true>, k_split<1, false, false>, k_round};
+  return {k_split<2, true, true>, k_split<2, false, true>, k_split<2, false, false>, k_round};
+}
+
+struct Choice {
+  KernelFn fn = nullptr;
+  size_t smem = 0;
+  int kind = kKindSplit;
+};
+
+// The kernel of a call with `rows` rows: the tensor cores for rounds of at least
+// kMmaRows rows whose plan fits, the split kernel otherwise.  False if neither fits.
+bool choose_kernel(const moe_dims& d, int rows, int grid, bool route_only, Choice& c) {
+  const KernelSet ks = kernels_for(d.hidden);
+  if (!route_only && rows >= kMmaRows) {
+    const WidePlan w = wide_plan(d.hidden, d.inter, d.n_experts, rows, d.top_k, grid);
+    if (w.ok) {
+      c.fn = ks.wide;
+      c.smem = w.total;
+      c.kind = kKindWide;
+      return true;
+    }
+  }
+  const SplitPlan sp = split_plan(d.hidden, d.inter, d.n_experts, rows, d.top_k, grid);
+  if (!sp.ok) return false;
+  c.fn = (rows == 1 && sp.x_staged) ? ks.split_xr : (sp.x_staged ? ks.split_xs : ks.split_gx);
+  c.smem = sp.total;
+  c.kind = kKindSplit;
+  return true;
+}
+
 // The dynamic shared-memory limit is an attribute of the kernel function, shared by
 // every handle: raise it once to the device's opt-in maximum (minus the kernel's static
 // shared memory), so a handle created later with a smaller plan cannot lower it below
 // what an earlier handle launches with.
-template <int NBL, bool WIDE>
-cudaError_t allow_max_dynamic_smem(int device) {
+cudaError_t allow_max_dynamic_smem(int device, KernelFn fn) {
   int optin = 0;
   cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
   cudaFuncAttributes fa{};
-  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, k_round<NBL, WIDE>);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, fn);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(k_round<NBL, WIDE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             optin - (int)fa.sharedSizeBytes);
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - (int)fa.sharedSizeBytes);
   return e;
 }
 
-// Both kernels of one NBL may serve a handle: raise their limits and check that one CTA
-// of each fits an SM with `smem` bytes.
-template <int NBL>
-cudaError_t prepare_kernels(int device, size_t smem, int& occ) {
-  int o1 = 0, o2 = 0;
-  cudaError_t e = allow_max_dynamic_smem<NBL, false>(device);
-  if (e == cudaSuccess) e = allow_max_dynamic_smem<NBL, true>(device);
-  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o1, k_round<NBL, false>, NT, smem);
-  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o2, k_round<NBL, true>, NT, smem);
-  occ = o1 < o2 ? o1 : o2;
+// Raises the limits of every kernel that can serve hidden size H.
+cudaError_t prepare_kernels(int device, int H) {
+  const KernelSet ks = kernels_for(H);
+  cudaError_t e = allow_max_dynamic_smem(device, ks.split_xr);
+  if (e == cudaSuccess) e = allow_max_dynamic_smem(device, ks.split_xs);
+  if (e == cudaSuccess) e = allow_max_dynamic_smem(device, ks.split_gx);
+  if (e == cudaSuccess) e = allow_max_dynamic_smem(device, ks.wide);
   return e;
 }
 
-// Rounds of at least kMmaRows rows whose positions and this grid's output rows per CTA fit
-// the tensor-core path's shared-memory scratch run on the tensor cores.
-bool wide_round(const moe_dims& d, int rows, int grid) {
-  const SmemPlan p = smem_plan(d.hidden, d.inter, d.n_experts, d.max_rows, d.top_k, grid);
-  return rows >= kMmaRows && rows * d.top_k <= kMmaMaxPos && p.max_orows <= 16;
-}
-
-cudaError_t launch_kernel(const cudaLaunchConfig_t& cfg, const RoundArgs& a, bool wide) {
-  if (nbl_of(a.H) == 1)
-    return wide ? cudaLaunchKernelEx(&cfg, k_round<1, true>, a) : cudaLaunchKernelEx(&cfg, k_round<1, false>, a);
-  return wide ? cudaLaunchKernelEx(&cfg, k_round<2, true>, a) : cudaLaunchKernelEx(&cfg, k_round<2, false>, a);
-}
-
-size_t smem_bytes(const moe_dims& d, int rows, int grid) {
-  return smem_plan(d.hidden, d.inter, d.n_experts, rows, d.top_k, grid).total;
+// Every row count 1..max_rows (and routing alone) has a kernel whose plan fits and of
+// which one CTA fits an SM.  MOE_EUNSUPPORTED if not, MOE_ECUDA on a runtime error.
+int check_plans(const moe_dims& d, int grid) {
+  if ((size_t)((d.n_experts + grid - 1) / grid) * d.hidden * 4 > (size_t)64 * 1024) return MOE_EUNSUPPORTED;
+  for (int rows = 1; rows <= d.max_rows; ++rows)
+    for (int ro = 0; ro < 2; ++ro) {
+      Choice c;
+      if (!choose_kernel(d, rows, grid, ro != 0, c)) return MOE_EUNSUPPORTED;
+      int occ = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, c.fn, NT, c.smem) != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ECUDA;
+      }
+      if (occ < 1) return MOE_EUNSUPPORTED;
+    }
+  return MOE_OK;
 }
 
 void fill_args(RoundArgs& a, const moe_handle* h, int rows, void* ws) {
@@ -1944,6 +2068,7 @@ void fill_args(RoundArgs& a, const moe_handle* h, int rows, void* ws) {
   a.bar = reinterpret_cast<unsigned*>(base + L.ctrl);
   a.logits = reinterpret_cast<float*>(base + L.logits);
   a.hbuf = reinterpret_cast<float*>(base + L.hbuf);
+  a.acc = reinterpret_cast<unsigned long long*>(base + L.acc);
   a.status = h->status;
   a.tail_rank = h->tail_rank;
   const unsigned long long ns = h->wait_ns < (1ull << 40) ? h->wait_ns : (1ull << 40);
@@ -1966,17 +2091,20 @@ cudaError_t launch_round(moe_handle* h, const RoundArgs& a, cudaStream_t st, boo
     h->ev_used += 2;
     cudaEventRecord(e0, st);
   }
+  Choice c;
+  if (!choose_kernel(h->dims, a.R, h->sm_count, a.route_only != 0, c)) return cudaErrorInvalidValue;
+  h->last_kind = c.kind;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(h->sm_count);
   cfg.blockDim = dim3(NT);
-  cfg.dynamicSmemBytes = smem_bytes(h->dims, h->dims.max_rows, h->sm_count);
+  cfg.dynamicSmemBytes = c.smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = launch_kernel(cfg, a, !a.route_only && wide_round(h->dims, a.R, h->sm_count));
+  e = cudaLaunchKernelEx(&cfg, c.fn, a);
   if (prof) cudaEventRecord(e1, st);
   return e;
 }
@@ -2022,10 +2150,12 @@ int moe_create(const moe_dims* dims, int device, moe_handle** out) {
     cudaGetLastError();
     return MOE_ECUDA;
   }
-  const size_t smem = smem_bytes(*dims, dims->max_rows, sms);
-  const SmemPlan plan = smem_plan(dims->hidden, dims->inter, dims->n_experts, dims->max_rows,
-                                  dims->top_k, sms);
-  if (smem + 1024 > 227 * 1024 || !plan.router_fits) return MOE_EUNSUPPORTED;
+  cudaError_t e = prepare_kernels(device, dims->hidden);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ECUDA;
+  }
+  if ((rc = check_plans(*dims, sms)) != MOE_OK) return rc;
   moe_handle* h = new moe_handle();
   h->dims = *dims;
   h->device = device;
@@ -2034,15 +2164,6 @@ int moe_create(const moe_dims* dims, int device, moe_handle** out) {
       cudaMemset(h->status, 0, sizeof(unsigned)) != cudaSuccess) {
     cudaGetLastError();
     if (h->status) cudaFree(h->status);
-    delete h;
-    return MOE_ECUDA;
-  }
-  cudaError_t e;
-  int occ = 0;
-  e = (nbl_of(dims->hidden) == 1) ? prepare_kernels<1>(device, smem, occ) : prepare_kernels<2>(device, smem, occ);
-  if (e != cudaSuccess || occ < 1) {
-    cudaGetLastError();
-    cudaFree(h->status);
     delete h;
     return MOE_ECUDA;
   }
@@ -2189,7 +2310,9 @@ int moe_round(moe_handle* h, const moe_layer_w* layers, int32_t L, const uint16_
       h->phase_layers = L;
     }
     h->last_launches = 1;
-    return launch_round(h, a, st, false) == cudaSuccess ? MOE_OK : MOE_ECUDA;
+    const cudaError_t e = launch_round(h, a, st, false);
+    if (a.phase_ts) h->phase_kind = h->last_kind;
+    return e == cudaSuccess ? MOE_OK : MOE_ECUDA;
   }
   GraphKey key;
   key.layers.assign(layers, layers + L);
@@ -2282,23 +2405,25 @@ int moe_profile_read(moe_handle* h, int kind, double* total_ms, int32_t* launche
 }
 
 int moe_profile_phases(moe_handle* h, double* mean_us, double* max_us, int32_t n_phases) {
-  if (!h || !mean_us || !max_us || n_phases < kPhases - 1) return MOE_EINVAL;
+  if (!h || !mean_us || !max_us) return MOE_EINVAL;
   if (!h->phase_ts || h->phase_layers < 1) return MOE_EINVAL;
+  const int stamps = h->phase_kind == kKindWide ? kPhases : kSplitPhases;
+  if (n_phases < stamps - 1) return MOE_EINVAL;
   DeviceGuard g(h->device);
   if (!g.ok) return MOE_ECUDA;
   const int G = h->sm_count, L = h->phase_layers;
-  std::vector<long long> ts((size_t)L * kPhases * G);
+  std::vector<long long> ts((size_t)L * stamps * G);
   if (cudaDeviceSynchronize() != cudaSuccess ||
       cudaMemcpy(ts.data(), h->phase_ts, ts.size() * sizeof(long long), cudaMemcpyDeviceToHost) !=
           cudaSuccess)
     return MOE_ECUDA;
-  for (int p = 0; p + 1 < kPhases; ++p) {
+  for (int p = 0; p + 1 < stamps; ++p) {
     double sum = 0.0, mx = 0.0;
     for (int l = 0; l < L; ++l) {
       double lmax = 0.0;
       for (int c = 0; c < G; ++c) {
-        const double d = (double)(ts[((size_t)l * kPhases + p + 1) * G + c] -
-                                  ts[((size_t)l * kPhases + p) * G + c]) * 1e-3;
+        const double d = (double)(ts[((size_t)l * stamps + p + 1) * G + c] -
+                                  ts[((size_t)l * stamps + p) * G + c]) * 1e-3;
         sum += d;
         if (d > lmax) lmax = d;
       }
@@ -2307,7 +2432,7 @@ int moe_profile_phases(moe_handle* h, double* mean_us, double* max_us, int32_t n
     mean_us[p] = sum / ((double)L * G);
     max_us[p] = mx / L;
   }
-  return MOE_OK;
+  return stamps - 1;
 }
 
 }  // extern "C"
@@ -2318,10 +2443,11 @@ int moe_profile_phases(moe_handle* h, double* mean_us, double* max_us, int32_t n
 // Some callers cannot allocate device memory at all: code that runs inside another
 // framework's memory pool with allocation disabled, allocation-free real-time or
 // embedded loops, or hosts that forbid cudaMalloc after start-up.  For them the
-// workspace (grid-barrier words, router logits, exchanged SwiGLU outputs) lives in the file-
-// scope array below, which the CUDA runtime places on every device that loads this
-// library and keeps until the process exits.  The caller passes only inputs and
-// outputs; this path calls no cudaMalloc, cudaFree or allocating library routine.
+// workspace (grid-barrier words, router logits, exchanged SwiGLU outputs, output
+// accumulators) lives in the file-scope array below, which the CUDA runtime places on
+// every device that loads this library and keeps until the process exits.  The caller
+// passes only inputs, outputs and a status word; this path calls no cudaMalloc, cudaFree
+// or allocating library routine.
 
 namespace {
 
@@ -2341,8 +2467,8 @@ std::mutex g_noalloc_mu;
 
 // One-time set-up of the current device: the device address of the scratch array (in
 // host code the symbol names a host-side stand-in, not device memory), the SM count,
-// and the kernel's shared-memory attribute.
-int noalloc_setup(int dev, size_t smem, NoAllocDevice** out) {
+// and the kernels' shared-memory limits.
+int noalloc_setup(int dev, NoAllocDevice** out) {
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
   NoAllocDevice& d = g_noalloc[dev];
   if (!d.ready) {
@@ -2357,18 +2483,13 @@ int noalloc_setup(int dev, size_t smem, NoAllocDevice** out) {
       cudaGetLastError();
       return MOE_ECUDA;
     }
+    if (prepare_kernels(dev, 256) != cudaSuccess || prepare_kernels(dev, kMaxHidden) != cudaSuccess) {
+      cudaGetLastError();
+      return MOE_ECUDA;
+    }
     d.scratch = p;
     d.sms = sms;
     d.ready = true;
-  }
-  (void)smem;  // (checked against the device limit by the caller)
-  cudaError_t e = allow_max_dynamic_smem<1, false>(dev);
-  if (e == cudaSuccess) e = allow_max_dynamic_smem<1, true>(dev);
-  if (e == cudaSuccess) e = allow_max_dynamic_smem<2, false>(dev);
-  if (e == cudaSuccess) e = allow_max_dynamic_smem<2, true>(dev);
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    return MOE_ECUDA;
   }
   *out = &d;
   return MOE_OK;
@@ -2382,31 +2503,23 @@ extern "C" int moe_decode_layer_noalloc(const moe_dims* dims, const moe_layer_w*
   int rc = check_dims(dims);
   if (rc != MOE_OK) return rc;
   if ((rc = check_layer(w)) != MOE_OK) return rc;
-  if (!aligned16(x_bf16) || !aligned16(out) || rows < 1 || rows > dims->max_rows)
-    return MOE_EINVAL;
-  if (dev_status && (reinterpret_cast<uintptr_t>(dev_status) & 3u)) return MOE_EINVAL;
-  // the scratch holds the status word (first 256 bytes) and the layer's workspace
+  if (!aligned16(x_bf16) || !aligned16(out) || rows < 1 || rows > dims->max_rows) return MOE_EINVAL;
+  // the status word is where a kernel reports what it found; without it errors are lost
+  if (!dev_status || (reinterpret_cast<uintptr_t>(dev_status) & 3u)) return MOE_EINVAL;
   const WsLayout L = ws_layout(*dims, rows);
-  if (256 + L.total > kNoAllocScratchBytes) return MOE_EWORKSPACE;
+  if (L.total > kNoAllocScratchBytes) return MOE_EWORKSPACE;
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) {
     cudaGetLastError();
     return MOE_ECUDA;
   }
-  int sms = 0;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-    cudaGetLastError();
-    return MOE_ECUDA;
-  }
-  const size_t smem = smem_bytes(*dims, dims->max_rows, sms);
-  const SmemPlan plan =
-      smem_plan(dims->hidden, dims->inter, dims->n_experts, dims->max_rows, dims->top_k, sms);
-  if (smem + 1024 > 227 * 1024 || !plan.router_fits) return MOE_EUNSUPPORTED;
   NoAllocDevice* d = nullptr;
-  if ((rc = noalloc_setup(dev, smem, &d)) != MOE_OK) return rc;
-  char* base = static_cast<char*>(d->scratch);
-  unsigned* own_status = reinterpret_cast<unsigned*>(base);
-  void* ws = base + 256;
+  if ((rc = noalloc_setup(dev, &d)) != MOE_OK) return rc;
+  Choice c;
+  if (!choose_kernel(*dims, rows, d->sms, false, c) ||
+      (size_t)((dims->n_experts + d->sms - 1) / d->sms) * dims->hidden * 4 > (size_t)64 * 1024)
+    return MOE_EUNSUPPORTED;
+  char* ws = static_cast<char*>(d->scratch);
   RoundArgs a{};
   const moe_dims& dd = *dims;
   a.H = dd.hidden;
@@ -2416,27 +2529,29 @@ extern "C" int moe_decode_layer_noalloc(const moe_dims* dims, const moe_layer_w*
   a.R = rows;
   a.Rmax = dd.max_rows;
   a.L = 1;
-  a.bar = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + L.ctrl);
-  a.logits = reinterpret_cast<float*>(static_cast<char*>(ws) + L.logits);
-  a.hbuf = reinterpret_cast<float*>(static_cast<char*>(ws) + L.hbuf);
-  a.status = dev_status ? dev_status : own_status;
+  a.bar = reinterpret_cast<unsigned*>(ws + L.ctrl);
+  a.logits = reinterpret_cast<float*>(ws + L.logits);
+  a.hbuf = reinterpret_cast<float*>(ws + L.hbuf);
+  a.acc = reinterpret_cast<unsigned long long*>(ws + L.acc);
+  a.status = dev_status;
   a.wait_cycles = kDefaultWaitCycles;
   a.x = x_bf16;
   a.out = out;
   copy_layers(a, w, 1);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // the barrier words must start at zero; logits and h are fully overwritten
+  // the barrier words must start at zero; logits, h and the accumulators are written
+  // (the accumulators cleared) by the kernel itself
   if (cudaMemsetAsync(a.bar, 0, 256, st) != cudaSuccess) return MOE_ECUDA;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(sms);
+  cfg.gridDim = dim3(d->sms);
   cfg.blockDim = dim3(NT);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = c.smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = launch_kernel(cfg, a, wide_round(dd, rows, sms));
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, c.fn, a);
   return e == cudaSuccess ? MOE_OK : MOE_ECUDA;
 }

@@ -126,13 +126,12 @@ def _decode_gateup(nib, sc, E, H, I):
 
 
 def _decode_down(nib, sc, E, H, I):
-    # codes [E][H][I/32][16 B], scales [E][H][I/32]; row r = o
+    # codes [E][I/32][H][16 B], scales [E][I/32][H]: block b of output row o at b * H + o
     NBI = I // 32
-    rows = np.arange(H)
-    by = np.stack([_unswizzle(b, rows, NBI) for b in nib.reshape(E, H, NBI, 16)])
-    s = np.stack([_unswizzle(x, rows, NBI) for x in sc.reshape(E, H, NBI)])
-    codes = _decode_blocks(by).reshape(E, H, I)
-    return codes, s
+    by = nib.reshape(E, NBI, H, 16).transpose(0, 2, 1, 3)
+    s = sc.reshape(E, NBI, H).transpose(0, 2, 1)
+    codes = _decode_blocks(np.ascontiguousarray(by)).reshape(E, H, I)
+    return codes, np.ascontiguousarray(s)
 
 
 @pytest.mark.parametrize("H,I,E", [(256, 256, 1), (512, 256, 3), (2048, 512, 2)])
@@ -168,12 +167,12 @@ def test_packer_one_hot_nibble_order():
     H, I = 256, 256
     d = mv.make_dims(H, 2, 1, I, 1)
     qd = np.zeros((1, H, I), np.int8)
-    qd[0, 5, 35] = 7   # o = 5, i = 35: block 1 of row 5 (stored at position 1 ^ 5), byte 1, high nibble
+    qd[0, 5, 35] = 7   # o = 5, i = 35: block 1 of row 5 (stored at block-major position 1 * H + 5), byte 1, high nibble
     sd = np.zeros((1, H, I // 32), np.uint16)
     nib = np.zeros(mv.moe_packed_bytes(d, 1, 0), np.uint8)
     sc = np.zeros(mv.moe_packed_bytes(d, 1, 1) // 2, np.uint16)
     mv.moe_pack_q4(d, mv.MOE_DOWN, 1, qd.ctypes.data, sd.ctypes.data, None, None, nib.ctypes.data, sc.ctypes.data)
-    off = (5 * (I // 32) + (1 ^ 5)) * 16
+    off = (1 * H + 5) * 16
     blk = nib[off:off + 16]
     assert blk[1] == (8 | (15 << 4))
     assert all(b == 0x88 for i, b in enumerate(blk) if i != 1)
