@@ -233,7 +233,7 @@ int moe_profile_phases(moe_handle* h, double* mean_us, double* max_us, int32_t n
  *   - Calls no cudaMalloc, cudaFree or allocating routine.  Every call shares the one
  *     array: calls whose executions overlap on the GPU (different streams, or different
  *     host threads without ordering) race on it and give wrong results. */
-#define MOE_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)
+#define MOE_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
 int moe_decode_layer_noalloc(const moe_dims* dims, const moe_layer_w* w, const uint16_t* x_bf16,
                              int32_t rows, float* out, unsigned* dev_status, void* stream);
 

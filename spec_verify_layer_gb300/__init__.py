@@ -27,12 +27,12 @@ ABI_SYMBOLS = (
     "moe_profile_phases", "moe_decode_layer_noalloc", "moe_prefill_workspace_bytes",
     "moe_prefill_layer", "moe_strerror",
 )
-MOE_NOALLOC_SCRATCH_BYTES = 4 << 20
+MOE_NOALLOC_SCRATCH_BYTES = 8 << 20
 KIND_ROUND = 0
 # phase intervals of a profiled moe_round, by the kernel that ran it (the library returns
 # how many it wrote): the split kernel (rows below 8) and the tensor-core kernel
-PHASES_SPLIT = ("finish_router", "barrier1", "routing", "first_data", "units_before_last", "last_unit",
-                "barrier3")
+PHASES_SPLIT = ("finish_router", "barrier1", "routing", "issue", "first_data", "units_before_last",
+                "last_gateup", "last_swiglu", "last_down_wait", "last_down", "barrier3")
 PHASES_WIDE = ("router", "barrier1", "routing", "first_data", "gateup_stream", "gateup_tail",
                "barrier2", "h_wait", "down", "down_tail", "out_write", "barrier3")
 

@@ -29,7 +29,7 @@ WsLayout ws_layout(const moe_dims& d, int rows) {
   L.ctrl = off;     off += 256;
   L.logits = off;   off += up256(R * E * 4);
   L.hbuf = off;     off += up256(R * k * (size_t)d.inter * 4);
-  L.acc = off;      off += up256((size_t)kAccCopies * R * (size_t)d.hidden * 8);
+  L.acc = off;      off += up256((size_t)2 * kAccCopies * R * (size_t)d.hidden * 8);
   L.total = off;
   return L;
 }

@@ -23,7 +23,7 @@ int check_dims(const moe_dims* d);
 // grid-barrier words, router logits [rows][E], weighted SwiGLU outputs h' [rows*k][I]
 // (exchanged between CTAs by the tensor-core kernel: one row per routed (row, expert)
 // pair, grouped by expert, as bf16 hi + lo in fragment order), and the split kernel's
-// output accumulators [kAccCopies][rows][H] (int64, 2^32-scaled).
+// output accumulators [2 (layer parity)][kAccCopies][rows][H] (int64, 2^32-scaled).
 constexpr int kAccCopies = 8;
 struct WsLayout {
   size_t ctrl, logits, hbuf, acc, total;

@@ -77,7 +77,7 @@ struct RoundArgs {
   unsigned* bar;      // [0] barrier arrivals, [33] abort flag
   float* logits;      // [R][E]
   float* hbuf;        // [R*k][I] weighted SwiGLU outputs h' by CSR position (tensor-core rounds)
-  unsigned long long* acc;  // [kSplitCopies][R][H] 2^32-scaled output accumulators (split rounds)
+  unsigned long long* acc;  // [2][kSplitCopies][R][H] 2^32-scaled output accumulators (split rounds)
   int* user_ids;      // moe_route outputs (CTA 0 writes them)
   float* user_w;
   int* user_union;
@@ -171,60 +171,6 @@ __device__ __forceinline__ unsigned ld_relaxed(const unsigned* p) {
   unsigned v;
   asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
-}
-
-// packed pairs of fp32 for fma.rn.f32x2
-typedef unsigned long long f2_t;
-
-__device__ __forceinline__ f2_t f2pack(float lo, float hi) {
-  f2_t r;
-  asm("mov.b64 %0, {%1,%2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-
-__device__ __forceinline__ float f2sum(f2_t v) {
-  float lo, hi;
-  asm("mov.b64 {%0,%1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-  return __fadd_rn(lo, hi);
-}
-
-__device__ __forceinline__ void ffma2(f2_t& acc, f2_t a, f2_t b) {
-  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
-}
-
-// 2^(87 - 4m) for nibble slots m = 0..4 and 2^(99 - 4m) for m = 5..7 (those three are
-// read after a 12-bit right shift): the factor that turns the subnormal n * 2^e_m into
-// n * x * 2^-62 under an fma.
-__device__ __forceinline__ float slot_scale(int m) {
-  const int e = (m <= 4) ? 87 - 4 * m : 99 - 4 * m;
-  return __int_as_float((127 + e) << 23);
-}
-
-// A 16-byte block is handled as two 64-bit word pairs D0 = {w0, w1}, D1 = {w2, w3} (and
-// the same shifted right by 12 in each half).  ANDing a pair with a slot mask isolates
-// slot m of two words at once -- elements (m, 8+m) of D0 and (16+m, 24+m) of D1 -- as
-// two subnormal floats already laid out as an f32x2 operand.  Activations are kept as
-// matching pairs: xp[m] = (x'[m], x'[8+m]) and xp[8+m] = (x'[16+m], x'[24+m]).
-struct BlockPairs {
-  f2_t d0, d1, t0, t1;
-};
-
-__device__ __forceinline__ BlockPairs block_pairs(const uint4 nb) {
-  BlockPairs b;
-  asm("mov.b64 %0, {%1,%2};" : "=l"(b.d0) : "r"(nb.x), "r"(nb.y));
-  asm("mov.b64 %0, {%1,%2};" : "=l"(b.d1) : "r"(nb.z), "r"(nb.w));
-  asm("mov.b64 %0, {%1,%2};" : "=l"(b.t0) : "r"(nb.x >> 12), "r"(nb.y >> 12));
-  asm("mov.b64 %0, {%1,%2};" : "=l"(b.t1) : "r"(nb.z >> 12), "r"(nb.w >> 12));
-  return b;
-}
-
-// slot m's mask in both halves; slots 5..7 are read from the shifted pair
-__device__ __forceinline__ f2_t slot_pair(const BlockPairs& b, int half, int m) {
-  constexpr f2_t M[5] = {0x0000000F0000000Full, 0x000000F0000000F0ull, 0x00000F0000000F00ull,
-                         0x0000F0000000F000ull, 0x000F0000000F0000ull};
-  const f2_t d = half ? b.d1 : b.d0;
-  const f2_t t = half ? b.t1 : b.t0;
-  return (m <= 4) ? (d & M[m]) : (t & M[m - 3]);
 }
 
 // ---------------------------------------------------------------------------------
@@ -717,39 +663,140 @@ __device__ int route_phase(const RoundArgs& a, const Tables& T, unsigned* s_mask
 }
 
 // ---------------------------------------------------------------------------------
-// Operand pairs.  The word pairs above consume a block's 32 elements as 16 f32x2
-// operands: pair p holds elements (16(p/8) + p%8, 16(p/8) + 8 + p%8), pre-scaled by
-// slot_scale(p%8).  Activations are kept in this form once per layer, block-interleaved:
-// float4 c of block b (pairs 2c and 2c+1) sits at float4 index c * NBlk + b, so lane b's
-// eight 16-byte loads are conflict-free.
+// Integer block dots.  A 32-element block of codes is four 32-bit words; word w holds
+// elements 8w .. 8w+7, element 8w + 2j in the low nibble and 8w + 2j + 1 in the high
+// nibble of byte j.  (w & 0x0F0F0F0F) gives the even elements' codes n as four bytes,
+// (w & 0xF0F0F0F0) the odd elements' codes as 16 n, both without a shift.  The other
+// operand is a block in fixed point: V_k = v_k 2^s as a signed integer of 16 bits (two
+// byte digits, for the bf16 rows) or 24 bits (three digits, for the fp32 SwiGLU outputs),
+// s chosen per block from its largest |v|; digit d of the elements in the same even/odd
+// byte order.  dp4a then gives, exactly, per digit d:
+//   A_d = sum over even k of n_k V_kd,   C_d = sum over odd k of 16 n_k V_kd,
+// and 16 sum_k (n_k - 8) V_kd = 16 A_d + C_d - 128 sum_k V_kd  (= E_d, exact in int32).
+// The block's sum (n - 8) v is 2^-s / 16 * sum_d 256^d E_d, formed in fp32.  A bf16 value
+// within a factor 2^7 of its block's largest is exact in 16 bits; smaller ones are rounded
+// to the block's 2^-s grid (an error below 2^-15 of the block maximum).  The 24-bit form
+// keeps an fp32 value to 2^-22 of its block's maximum.
+//
+// Operand layouts (u32 words): digit word q = (d * 2 + parity) * 4 + w holds digit d of
+// elements 8w + parity + 2j in byte j (j = 0..3).  Per block, after the digit words: the
+// correction terms K_d = -128 sum_k V_kd (int) and the factor 2^-s / 16 (float).
 
-__device__ __forceinline__ void f2unpack(f2_t v, float& lo, float& hi) {
-  asm("mov.b64 {%0,%1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+__device__ __forceinline__ int dp4a_uu(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
 }
 
-// One block of bf16 activations (four 16-byte words, elements 0..31) -> its 16
-// operand pairs and -8 times the block sum (summed pair by pair).
-__device__ __forceinline__ void convert_block(const uint4 (&u)[4], f2_t (&xp)[16], float& xsum8) {
-  float sum = 0.f;
+// Codes of one block as even / odd nibble bytes.
+struct NibBytes {
+  uint32_t lo[4], hi[4];
+};
+__device__ __forceinline__ NibBytes nib_bytes(const uint4 nb) {
+  NibBytes n;
+  const uint32_t w[4] = {nb.x, nb.y, nb.z, nb.w};
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const uint4 ua = u[2 * h], ub = u[2 * h + 1];
-    const uint32_t wa[4] = {ua.x, ua.y, ua.z, ua.w}, wb[4] = {ub.x, ub.y, ub.z, ub.w};
-#pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      const float va = (m & 1) ? bf16_hi(wa[m >> 1]) : bf16_lo(wa[m >> 1]);
-      const float vb = (m & 1) ? bf16_hi(wb[m >> 1]) : bf16_lo(wb[m >> 1]);
-      xp[8 * h + m] = f2pack(va * slot_scale(m), vb * slot_scale(m));
-      sum = __fadd_rn(sum, va);
-      sum = __fadd_rn(sum, vb);
-    }
+  for (int i = 0; i < 4; ++i) {
+    n.lo[i] = w[i] & 0x0F0F0F0Fu;
+    n.hi[i] = w[i] & 0xF0F0F0F0u;
   }
-  xsum8 = -8.f * sum;
+  return n;
 }
 
-// This layer's rows as operand pairs in shared memory: s_xp [R][8][NB] float4 and
-// s_xs [R][NB] (-8 x block sums).  Done while the router barrier completes.
-__device__ void stage_xpairs(const RoundArgs& a, const uint16_t* x, float4* s_xp, float* s_xs) {
+// A 16-bit operand block (two digits) in registers: digit words and K_0, K_1, factor.
+struct Op16 {
+  uint32_t d[16];
+  int k0, k1;
+  float f;
+};
+// A 24-bit operand block (three digits).
+struct Op24 {
+  uint32_t d[24];
+  int k0, k1, k2;
+  float f;
+};
+
+// sum over the block of (n - 8) v for a 16-bit operand.
+__device__ __forceinline__ float bdot16(const NibBytes& n, const Op16& x) {
+  int a0 = 0, c0 = 0, a1 = 0, c1 = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    a0 = dp4a_uu(n.lo[i], x.d[i], a0);
+    c0 = dp4a_uu(n.hi[i], x.d[4 + i], c0);
+    a1 = dp4a_us(n.lo[i], x.d[8 + i], a1);
+    c1 = dp4a_us(n.hi[i], x.d[12 + i], c1);
+  }
+  const int e0 = 16 * a0 + c0 + x.k0, e1 = 16 * a1 + c1 + x.k1;
+  return __fmul_rn(__fmaf_rn((float)e1, 256.f, (float)e0), x.f);
+}
+
+// sum over the block of (n - 8) v for a 24-bit operand.
+__device__ __forceinline__ float bdot24(const NibBytes& n, const Op24& h) {
+  int a0 = 0, c0 = 0, a1 = 0, c1 = 0, a2 = 0, c2 = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    a0 = dp4a_uu(n.lo[i], h.d[i], a0);
+    c0 = dp4a_uu(n.hi[i], h.d[4 + i], c0);
+    a1 = dp4a_uu(n.lo[i], h.d[8 + i], a1);
+    c1 = dp4a_uu(n.hi[i], h.d[12 + i], c1);
+    a2 = dp4a_us(n.lo[i], h.d[16 + i], a2);
+    c2 = dp4a_us(n.hi[i], h.d[20 + i], c2);
+  }
+  const int e0 = 16 * a0 + c0 + h.k0, e1 = 16 * a1 + c1 + h.k1, e2 = 16 * a2 + c2 + h.k2;
+  return __fmul_rn(__fmaf_rn((float)e2, 65536.f, __fmaf_rn((float)e1, 256.f, (float)e0)), h.f);
+}
+
+// Byte j of digit word q for element e of a block: q = (d * 2 + (e & 1)) * 4 + (e >> 3),
+// j = (e & 7) >> 1.
+__device__ __forceinline__ int digit_word(int d, int e) { return (d * 2 + (e & 1)) * 4 + (e >> 3); }
+
+// One block of 32 bf16 values (four 16-byte words) -> its 16-bit operand (digit words,
+// K_0, K_1, factor).  s = 14 - e, e the unbiased exponent of the largest |value| (at
+// least -113 so that 2^s stays a normal float): |V| < 2^15.
+__device__ __forceinline__ void x_block_to_op16(const uint4 (&u)[4], Op16& op) {
+  uint32_t v[16];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[4 * i] = u[i].x;
+    v[4 * i + 1] = u[i].y;
+    v[4 * i + 2] = u[i].z;
+    v[4 * i + 3] = u[i].w;
+  }
+  uint32_t mx = 0u;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) mx = max(mx, max(v[i] & 0x7FFFu, (v[i] >> 16) & 0x7FFFu));
+  const int E = max((int)(mx >> 7), 14);  // biased exponent of the largest |x|
+  const float scale = __int_as_float((268 - E) << 23);   // 2^(141 - E) = 2^(14 - e)
+  // 2^(E - 145) = 2^-s / 16 (a subnormal float below E = 19)
+  op.f = E >= 19 ? __int_as_float((E - 18) << 23) : __int_as_float(1 << (E + 4));
+#pragma unroll
+  for (int q = 0; q < 16; ++q) op.d[q] = 0u;
+  int s0 = 0, s1 = 0;
+#pragma unroll
+  for (int e = 0; e < 32; ++e) {
+    const float xv = (e & 1) ? bf16_hi(v[e >> 1]) : bf16_lo(v[e >> 1]);
+    const int X = __float2int_rn(xv * scale);
+    const int d0 = X & 0xFF, d1 = X >> 8;
+    s0 += d0;
+    s1 += d1;
+    const int j = (e & 7) >> 1;
+    op.d[digit_word(0, e)] |= (uint32_t)d0 << (8 * j);
+    op.d[digit_word(1, e)] |= ((uint32_t)d1 & 0xFFu) << (8 * j);
+  }
+  op.k0 = -128 * s0;
+  op.k1 = -128 * s1;
+}
+
+// This layer's rows as 16-bit operands in shared memory: s_xd [R][4][NB] uint4 (digit
+// words 4c .. 4c+3 of block b at uint4 index c * NB + b, conflict-free for lane = block)
+// and s_xk [R][NB] uint4 (K_0, K_1, factor bits, 0).  Done while the router barrier
+// completes.
+__device__ void stage_xdigits(const RoundArgs& a, const uint16_t* x, uint4* s_xd, uint4* s_xk) {
   const int NB = a.H >> 5;
   for (int idx = threadIdx.x; idx < a.R * NB; idx += NT) {
     const int r = idx / NB, b = idx - r * NB;
@@ -757,63 +804,41 @@ __device__ void stage_xpairs(const RoundArgs& a, const uint16_t* x, float4* s_xp
     uint4 u[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) u[i] = __ldg(src + i);
-    f2_t xp[16];
-    float xs;
-    convert_block(u, xp, xs);
+    Op16 op;
+    x_block_to_op16(u, op);
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      float a0, a1, b0, b1;
-      f2unpack(xp[2 * c], a0, a1);
-      f2unpack(xp[2 * c + 1], b0, b1);
-      s_xp[((size_t)r * 8 + c) * NB + b] = make_float4(a0, a1, b0, b1);
-    }
-    s_xs[r * NB + b] = xs;
+    for (int c = 0; c < 4; ++c)
+      s_xd[((size_t)r * 4 + c) * NB + b] = make_uint4(op.d[4 * c], op.d[4 * c + 1], op.d[4 * c + 2], op.d[4 * c + 3]);
+    s_xk[(size_t)r * NB + b] = make_uint4((uint32_t)op.k0, (uint32_t)op.k1, __float_as_uint(op.f), 0u);
   }
 }
 
-// Operand pairs of block blk of one row: from the staged pairs (XS) or converted from
-// the bf16 row in global memory (rows too many to stage).
+// The 16-bit operand of block blk of one row: from the staged digits (XS) or converted
+// from the bf16 row in global memory (rows too many to stage).
 template <bool XS>
-__device__ __forceinline__ void load_xblock(const RoundArgs& a, const uint16_t* x, const float4* s_xp,
-                                            const float* s_xs, int row, int blk, f2_t (&xp)[16],
-                                            float& xsum8) {
+__device__ __forceinline__ void load_xop(const RoundArgs& a, const uint16_t* x, const uint4* s_xd, const uint4* s_xk,
+                                         int row, int blk, Op16& op) {
   const int NB = a.H >> 5;
   if (XS) {
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      // a float4 of pairs is two f32x2 operands as stored: load them as such
-      const ulonglong2 f = *reinterpret_cast<const ulonglong2*>(s_xp + ((size_t)row * 8 + c) * NB + blk);
-      xp[2 * c] = f.x;
-      xp[2 * c + 1] = f.y;
+    for (int c = 0; c < 4; ++c) {
+      const uint4 v = s_xd[((size_t)row * 4 + c) * NB + blk];
+      op.d[4 * c] = v.x;
+      op.d[4 * c + 1] = v.y;
+      op.d[4 * c + 2] = v.z;
+      op.d[4 * c + 3] = v.w;
     }
-    xsum8 = s_xs[row * NB + blk];
+    const uint4 k = s_xk[(size_t)row * NB + blk];
+    op.k0 = (int)k.x;
+    op.k1 = (int)k.y;
+    op.f = __uint_as_float(k.z);
   } else {
     const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)row * a.H + 32 * blk);
     uint4 u[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) u[i] = __ldg(src + i);
-    convert_block(u, xp, xsum8);
+    x_block_to_op16(u, op);
   }
-}
-
-// One 32-element block dot for G activation sets: dot[g] = 2^-62 sum n_k x_k.
-template <int G>
-__device__ __forceinline__ void block_dot(const uint4 nb, const f2_t* const* xp, float* dot) {
-  const BlockPairs bp = block_pairs(nb);
-  f2_t a0[G], a1[G];
-#pragma unroll
-  for (int g = 0; g < G; ++g) a0[g] = a1[g] = 0ull;
-#pragma unroll
-  for (int m = 0; m < 8; ++m) {
-    const f2_t e0 = slot_pair(bp, 0, m), e1 = slot_pair(bp, 1, m);
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      ffma2(a0[g], e0, xp[g][m]);
-      ffma2(a1[g], e1, xp[g][8 + m]);
-    }
-  }
-#pragma unroll
-  for (int g = 0; g < G; ++g) dot[g] = __fadd_rn(f2sum(a0[g]), f2sum(a1[g]));
 }
 
 // V values per lane (V a power of two <= 16) summed over the warp; value v ends in
@@ -891,10 +916,10 @@ constexpr int kSplitMaxSlots = 16;
 constexpr int kGuPieces = 4;  // gate/up pieces per unit (8 intermediate indices each)
 constexpr int kDnPieces = 2;  // down pieces per unit (H/2 output rows each)
 constexpr int kPieces = kGuPieces + kDnPieces;
-constexpr int kSplitPhases = 8;  // phase stamps per layer when profiling the split kernel
+constexpr int kSplitPhases = 12;  // phase stamps per layer when profiling the split kernel
 
 struct SplitPlan {
-  size_t slot_bytes, ring, router, xp, xs, part, hp, uni, csr, pair, w, pos_ui, pos_row, slot, pick, nunion, misc,
+  size_t slot_bytes, ring, router, xd, xk, part, hd, uni, csr, pair, w, pos_ui, pos_row, slot, pick, nunion, misc,
       bars, total;
   int nslot, ng;
   bool x_staged, ok;
@@ -902,7 +927,7 @@ struct SplitPlan {
 
 __host__ __device__ inline size_t up128(size_t x) { return (x + 127) & ~(size_t)127; }
 
-// Shared-memory plan of the split kernel for R rows; the activation pairs are staged when
+// Shared-memory plan of the split kernel for R rows; the rows' operands are staged when
 // they leave room for at least six slots.
 __host__ __device__ inline SplitPlan split_plan(int H, int I, int E, int R, int k, int grid) {
   SplitPlan p{};
@@ -912,13 +937,13 @@ __host__ __device__ inline SplitPlan split_plan(int H, int I, int E, int R, int 
   const size_t rk = (size_t)R * k;
   const size_t router = up128((size_t)((E + grid - 1) / grid) * H * 4);
   const size_t part = up128((size_t)64 * p.ng * R * 4);
-  const size_t hp = up128((size_t)R * 36 * 4);
+  const size_t hd = up128((size_t)R * 28 * 4);
   const size_t tables = up128((size_t)E * 4) + up128((size_t)(E + 1) * 4) + 5 * up128(rk * 4) +
                         up128((size_t)E * 4) + 128;
   const size_t misc = 256, bars = 256;
   const size_t limit = (size_t)225 * 1024;
-  size_t fixed = router + part + hp + tables + misc + bars;
-  const size_t xbytes = up128((size_t)R * H * 4) + up128((size_t)R * NB * 4);
+  size_t fixed = router + part + hd + tables + misc + bars;
+  const size_t xbytes = up128((size_t)R * H * 2) + up128((size_t)R * NB * 16);
   p.x_staged = fixed + xbytes + 6 * p.slot_bytes <= limit;
   if (p.x_staged) fixed += xbytes;
   int ns = fixed < limit ? (int)((limit - fixed) / p.slot_bytes) : 0;
@@ -927,10 +952,10 @@ __host__ __device__ inline SplitPlan split_plan(int H, int I, int E, int R, int 
   size_t off = 0;
   p.ring = off;    off += (size_t)ns * p.slot_bytes;
   p.router = off;  off += router;
-  p.xp = off;      off += p.x_staged ? up128((size_t)R * H * 4) : 0;
-  p.xs = off;      off += p.x_staged ? up128((size_t)R * NB * 4) : 0;
+  p.xd = off;      off += p.x_staged ? up128((size_t)R * H * 2) : 0;
+  p.xk = off;      off += p.x_staged ? up128((size_t)R * NB * 16) : 0;
   p.part = off;    off += part;
-  p.hp = off;      off += hp;
+  p.hd = off;      off += hd;
   p.uni = off;     off += up128((size_t)E * 4);
   p.csr = off;     off += up128((size_t)(E + 1) * 4);
   p.pair = off;    off += up128(rk * 4);
@@ -946,9 +971,12 @@ __host__ __device__ inline SplitPlan split_plan(int H, int I, int E, int R, int 
   // routing scratch lives in the (then idle) ring: mask, offsets, ids, union index, best
   // rank, and the one-row counting path's keys, counts and warp sums
   const size_t scratch = ((size_t)4 * E + rk) * 4 + 16 + (size_t)(5 * NT + NW) * 4;
-  p.ok = ns >= kPieces && (size_t)ns * p.slot_bytes >= scratch;
+  p.ok = ns >= kGuPieces && (size_t)ns * p.slot_bytes >= scratch;
   return p;
 }
+
+// The split kernel's plan, in shared memory (written once per launch by thread 0).
+__shared__ SplitPlan g_splan;
 
 // Piece j of this CTA's units (unit u0 + j / kPieces, piece j % kPieces) -> ring slot.
 __device__ __forceinline__ void issue_piece(const RoundArgs& a, const LayerPtrs& W, const Tables& T, int NS, int u0,
@@ -974,113 +1002,129 @@ __device__ __forceinline__ void issue_piece(const RoundArgs& a, const LayerPtrs&
   bulk_g2s(smem_u32(dst + 8 * H), src_s, (uint32_t)H, bar);
 }
 
-// Gate/up of 4 consecutive rows rp0 .. rp0 + 3 of a gate/up piece (row rp of the piece =
-// intermediate index i0 + rp / 2, gate for even rp, up for odd) for G activation sets:
-// lane = hidden block b (32 kg + lane of the warp's K group), one block dot per row and
-// set; v[s][j] = that block's contribution to row rp0 + j for set s.
-template <int G>
-__device__ __forceinline__ void split_gu_rows4(const uint8_t* piece, int H, int rp0, int b, bool valid,
-                                               const f2_t* const* xps, const float* xs8, float (&v)[G][4]) {
+// ---- the split kernel's unit passes ----
+
+// Gate/up of N consecutive rows rp0 .. rp0 + N - 1 of a gate/up piece (row rp of the
+// piece = intermediate index i0 + rp / 2, gate for even rp, up for odd) for G activation
+// rows: lane = hidden block b (32 kg + lane of the warp's K group), one block dot per row
+// and activation row; v[g][j] = that block's contribution to row rp0 + j for activation
+// g.  The codes and scales of all N rows are loaded before any is used.
+template <int N, int G>
+__device__ __forceinline__ void split_gu_rows(const uint8_t* piece, int H, int rp0, int b, bool valid,
+                                              const Op16* xs, float (&v)[G][N]) {
   const int NB = H >> 5;
   const uint16_t* scales = reinterpret_cast<const uint16_t*>(piece + (size_t)8 * H);
+  uint4 nb[N];
+  float sc[N];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
+  for (int j = 0; j < N; ++j) {
     const int rp = rp0 + j;
-    if (valid) {
-      // block b of the row of intermediate index i sits at b ^ (i & 7); i & 7 = (rp / 2) & 7
-      const int pb = b ^ ((rp >> 1) & 7);
-      const uint4 nb = *reinterpret_cast<const uint4*>(piece + ((size_t)rp * NB + pb) * 16);
-      const float sc = half_bits(scales[rp * NB + pb]);
-      float dot[G];
-      block_dot<G>(nb, xps, dot);
+    // block b of the row of intermediate index i sits at b ^ (i & 7); i & 7 = (rp / 2) & 7
+    const int pb = (b ^ ((rp >> 1) & 7)) & (valid ? 0xFFFF : 0);
+    nb[j] = *reinterpret_cast<const uint4*>(piece + ((size_t)rp * NB + pb) * 16);
+    sc[j] = valid ? half_bits(scales[rp * NB + pb]) : 0.f;
+  }
 #pragma unroll
-      for (int g = 0; g < G; ++g) v[g][j] = __fmul_rn(sc, __fmaf_rn(dot[g], 0x1p62f, xs8[g]));
-    } else {
+  for (int j = 0; j < N; ++j) {
+    const NibBytes n = nib_bytes(nb[j]);
 #pragma unroll
-      for (int g = 0; g < G; ++g) v[g][j] = 0.f;
+    for (int g = 0; g < G; ++g) {
+      const float t = __fmul_rn(sc[j], bdot16(n, xs[g]));
+      v[g][j] = valid ? t : 0.f;  // (a lane past the row's blocks holds no operand)
     }
   }
 }
 
-// Reduces one set's 4 values over the warp and stores the row sums as partials of K
-// group kg: s_part[((row0 + j) * NG + kg) * Rs + pr].
-__device__ __forceinline__ void split_store_part(float (&v)[4], int lane, float* s_part, int row0, int NG, int kg,
+// Reduces one activation row's N values over the warp and stores the row sums as
+// partials of K group kg: s_part[((row0 + j) * NG + kg) * Rs + pr].
+template <int N>
+__device__ __forceinline__ void split_store_part(float (&v)[N], int lane, float* s_part, int row0, int NG, int kg,
                                                  int Rs, int pr) {
-  const float s = warp_sum_multi<4>(v, lane);
-  if ((lane & 7) == 0) s_part[((row0 + (lane >> 3)) * NG + kg) * Rs + pr] = s;
+  const float s = warp_sum_multi<N>(v, lane);
+  constexpr int LPV = 32 / N;
+  if ((lane % LPV) == 0) s_part[((row0 + lane / LPV) * NG + kg) * Rs + pr] = s;
 }
 
 // The gate/up pass of one unit for this warp: rows [rb RPW, (rb + 1) RPW) of the unit's
 // 64 (RPW = 4 NG, all in one piece), K group kg, every activation row of the expert (CSR
-// positions p0 .. p0 + Re - 1), two at a time, four weight rows at a time.  XR: one row
-// whose pairs live in registers.
+// positions p0 .. p0 + Re - 1), two at a time (their code bytes are extracted once), four
+// weight rows at a time.  XR: one row whose operand the caller holds in registers.
 template <int NG, bool XR, bool XS>
 __device__ __forceinline__ void split_gateup(const RoundArgs& a, const Tables& T, const uint8_t* piece, int rb,
-                                             int kg, int p0, int Re, const f2_t (&xr)[16], float xsr,
-                                             const float4* s_xp, const float* s_xs, const uint16_t* x,
-                                             float* s_part) {
+                                             int kg, int p0, int Re, const Op16& xr, const uint4* s_xd,
+                                             const uint4* s_xk, const uint16_t* x, float* s_part) {
   constexpr int RPW = 4 * NG;
   const int lane = threadIdx.x & 31, NB = a.H >> 5;
   const int b = 32 * kg + lane;
   const bool valid = b < NB;
   const int row0 = rb * RPW;
   if (XR) {
-    const f2_t* xps[1] = {xr};
-#pragma unroll
-    for (int h = 0; h < RPW; h += 4) {
-      float v[1][4];
-      split_gu_rows4<1>(piece, a.H, (row0 + h) & 15, b, valid, xps, &xsr, v);
-      split_store_part(v[0], lane, s_part, row0 + h, NG, kg, a.R, 0);
-    }
+    // all of the warp's rows in one pass: one reduction, RPW independent block dots
+    float v[1][RPW];
+    split_gu_rows<RPW, 1>(piece, a.H, row0 & 15, b, valid, &xr, v);
+    split_store_part<RPW>(v[0], lane, s_part, row0, NG, kg, a.R, 0);
     return;
   }
   int pr = 0;
   for (; pr + 1 < Re; pr += 2) {
-    f2_t x0[16], x1[16];
-    float xs8[2] = {0.f, 0.f};
+    Op16 xo[2];
     if (valid) {
-      load_xblock<XS>(a, x, s_xp, s_xs, T.pos_row[p0 + pr], b, x0, xs8[0]);
-      load_xblock<XS>(a, x, s_xp, s_xs, T.pos_row[p0 + pr + 1], b, x1, xs8[1]);
+      load_xop<XS>(a, x, s_xd, s_xk, T.pos_row[p0 + pr], b, xo[0]);
+      load_xop<XS>(a, x, s_xd, s_xk, T.pos_row[p0 + pr + 1], b, xo[1]);
     }
-    const f2_t* xps[2] = {x0, x1};
 #pragma unroll 1
     for (int h = 0; h < RPW; h += 4) {
       float v[2][4];
-      split_gu_rows4<2>(piece, a.H, (row0 + h) & 15, b, valid, xps, xs8, v);
-      split_store_part(v[0], lane, s_part, row0 + h, NG, kg, a.R, pr);
-      split_store_part(v[1], lane, s_part, row0 + h, NG, kg, a.R, pr + 1);
+      split_gu_rows<4, 2>(piece, a.H, (row0 + h) & 15, b, valid, xo, v);
+      split_store_part<4>(v[0], lane, s_part, row0 + h, NG, kg, a.R, pr);
+      split_store_part<4>(v[1], lane, s_part, row0 + h, NG, kg, a.R, pr + 1);
     }
   }
   if (pr < Re) {
-    f2_t x0[16];
-    float xs8 = 0.f;
-    if (valid) load_xblock<XS>(a, x, s_xp, s_xs, T.pos_row[p0 + pr], b, x0, xs8);
-    const f2_t* xps[1] = {x0};
+    Op16 xo[1];
+    if (valid) load_xop<XS>(a, x, s_xd, s_xk, T.pos_row[p0 + pr], b, xo[0]);
 #pragma unroll 1
     for (int h = 0; h < RPW; h += 4) {
       float v[1][4];
-      split_gu_rows4<1>(piece, a.H, (row0 + h) & 15, b, valid, xps, &xs8, v);
-      split_store_part(v[0], lane, s_part, row0 + h, NG, kg, a.R, pr);
+      split_gu_rows<4, 1>(piece, a.H, (row0 + h) & 15, b, valid, xo, v);
+      split_store_part<4>(v[0], lane, s_part, row0 + h, NG, kg, a.R, pr);
     }
   }
 }
 
-// The multi-row gate/up pass runs out of line: it then has the register file to itself
-// (inlined into the kernel, the kernel's live state pushes its operand pairs to local
-// memory); the one-row pass keeps the activation pairs in the kernel's registers.
 template <int NG, bool XS>
-__device__ __noinline__ void split_gateup_rows(const RoundArgs& a, const Tables& T, const uint8_t* piece, int rb,
-                                               int kg, int p0, int Re, const float4* s_xp, const float* s_xs,
-                                               const uint16_t* x, float* s_part) {
-  f2_t none[16];
-  split_gateup<NG, false, XS>(a, T, piece, rb, kg, p0, Re, none, 0.f, s_xp, s_xs, x, s_part);
+__device__ __forceinline__ void split_gateup_rows(const RoundArgs& a, const Tables& T, const uint8_t* piece, int rb,
+                                                  int kg, int p0, int Re, const uint4* s_xd, const uint4* s_xk,
+                                                  const uint16_t* x, float* s_part) {
+  Op16 none;
+  split_gateup<NG, false, XS>(a, T, piece, rb, kg, p0, Re, none, s_xd, s_xk, x, s_part);
+}
+
+// One row: this lane's block operand (row 0) comes from shared memory into registers
+// once per unit and serves the warp's rows of the unit.
+template <int NG>
+__device__ __forceinline__ void split_gateup_one(const RoundArgs& a, const Tables& T, const uint8_t* piece, int rb,
+                                                 int kg, int p0, const uint4* s_xd, const uint4* s_xk,
+                                                 float* s_part) {
+  const int NB = a.H >> 5, b = 32 * kg + (threadIdx.x & 31);
+  Op16 xr;
+  if (b < NB) {
+    load_xop<true>(a, nullptr, s_xd, s_xk, 0, b, xr);
+  } else {
+#pragma unroll
+    for (int q = 0; q < 16; ++q) xr.d[q] = 0u;
+    xr.k0 = xr.k1 = 0;
+    xr.f = 0.f;
+  }
+  split_gateup<NG, true, true>(a, T, piece, rb, kg, p0, 1, xr, s_xd, s_xk, nullptr, s_part);
 }
 
 // SwiGLU of one unit: warp per activation row (CSR position p0 + pr), lane = index i of
-// the slice.  g and v add the K groups' partials in group order; h' = w silu(g) v is
-// stored in pair layout (pre-scaled by its slot factor) with -8 sum h' after it.
+// the slice.  g and v add the K groups' partials in group order; h' = w silu(g) v.  The
+// 32 values of h' go to s_hd[pr] as a 24-bit operand for the down pass: 24 digit words,
+// then K_0, K_1, K_2 and the factor (28 words).
 __device__ __forceinline__ void split_swiglu(const RoundArgs& a, const Tables& T, const float* s_part, int NG,
-                                             int p0, int Re, float* s_hp) {
+                                             int p0, int Re, uint32_t* s_hd) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int pr = warp; pr < Re; pr += NW) {
     float gs = s_part[((2 * lane) * NG) * a.R + pr], vs = s_part[((2 * lane + 1) * NG) * a.R + pr];
@@ -1090,71 +1134,120 @@ __device__ __forceinline__ void split_swiglu(const RoundArgs& a, const Tables& T
     }
     const float hh = __fmul_rn(__fdiv_rn(gs, __fadd_rn(1.f, expf(-gs))), vs);
     const float hw = __fmul_rn(T.w[T.pair[p0 + pr]], hh);
-    const int p = ((lane >> 4) << 3) | (lane & 7);
-    s_hp[pr * 36 + 2 * p + ((lane >> 3) & 1)] = hw * slot_scale(lane & 7);
-    const float sum = warp_sum(hw);
-    if (lane == 0) s_hp[pr * 36 + 32] = -8.f * sum;
+    // s = 21 - e, e the unbiased exponent of the largest |h'| of the slice (at least
+    // -105): |H| <= 2^22, three byte digits
+    const unsigned mx = __reduce_max_sync(0xffffffffu, __float_as_uint(hw) & 0x7FFFFFFFu);
+    const int E = max((int)(mx >> 23), 22);
+    const float scale = __int_as_float((275 - E) << 23);  // 2^(148 - E)
+    const int Hq = __float2int_rn(__fmul_rn(hw, scale));
+    const int d0 = Hq & 0xFF, d1 = (Hq >> 8) & 0xFF, d2 = Hq >> 16;
+    uint8_t* row = reinterpret_cast<uint8_t*>(s_hd + pr * 28);
+    const int j = (lane & 7) >> 1;
+    row[digit_word(0, lane) * 4 + j] = (uint8_t)d0;
+    row[digit_word(1, lane) * 4 + j] = (uint8_t)d1;
+    row[digit_word(2, lane) * 4 + j] = (uint8_t)(d2 & 0xFF);
+    const int s0 = (int)__reduce_add_sync(0xffffffffu, (unsigned)d0);
+    const int s1 = (int)__reduce_add_sync(0xffffffffu, (unsigned)d1);
+    const int s2 = (int)__reduce_add_sync(0xffffffffu, (unsigned)d2);
+    if (lane == 0) {
+      s_hd[pr * 28 + 24] = (uint32_t)(-128 * s0);
+      s_hd[pr * 28 + 25] = (uint32_t)(-128 * s1);
+      s_hd[pr * 28 + 26] = (uint32_t)(-128 * s2);
+      // 2^(E - 152) = 2^-s / 16 (a subnormal float below E = 26)
+      s_hd[pr * 28 + 27] = E >= 26 ? (uint32_t)((E - 25) << 23) : (1u << (E - 3));
+    }
   }
 }
 
-// Down products of one unit for this thread's output rows o = tid + NT j, activation
-// sets pr .. pr + G - 1: y -> 2^32-scaled integers added into this CTA's accumulator copy.
+// Fire-and-forget add at L2 (no value comes back, so the thread does not wait for it).
+__device__ __forceinline__ void red_add_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// This thread's down rows o = tid + NT j (j < kDnRowsPerThread) of a unit: codes and
+// scales, loaded from the two down pieces before the SwiGLU barrier.
+constexpr int kDnRowsPerThread = (kMaxHidden + NT - 1) / NT;
+struct DnRows {
+  uint4 nb[kDnRowsPerThread];
+  float sc[kDnRowsPerThread];
+};
+
+__device__ __forceinline__ void load_dn_rows(int H, const uint8_t* dn0, const uint8_t* dn1, DnRows& d) {
+  const int HH = H >> 1;
+#pragma unroll
+  for (int j = 0; j < kDnRowsPerThread; ++j) {
+    const int o = (int)threadIdx.x + NT * j;
+    if (o < H) {
+      const uint8_t* pc = (o < HH) ? dn0 : dn1;
+      const int ol = (o < HH) ? o : o - HH;
+      d.nb[j] = *reinterpret_cast<const uint4*>(pc + (size_t)ol * 16);
+      d.sc[j] = half_bits(reinterpret_cast<const uint16_t*>(pc + (size_t)8 * H)[ol]);
+    } else {
+      d.nb[j] = make_uint4(0u, 0u, 0u, 0u);
+      d.sc[j] = 0.f;
+    }
+  }
+}
+
+// Down products of one unit for this thread's rows, activation positions pr .. pr + G - 1:
+// y -> 2^32-scaled integers added into this CTA's accumulator copy.
 template <int G>
-__device__ __forceinline__ void split_down_rows(const RoundArgs& a, const Tables& T, const uint8_t* dn0,
-                                                const uint8_t* dn1, const float* s_hp, int p0, int pr,
-                                                unsigned long long* acc_copy) {
-  f2_t hp[G][16];
-  float hs8[G];
+__device__ __forceinline__ void split_down_rows(const RoundArgs& a, const Tables& T, const DnRows& d,
+                                                const uint32_t* s_hd, int p0, int pr, unsigned long long* acc_copy) {
+  Op24 hop[G];
   int row[G];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
-    const ulonglong2* src = reinterpret_cast<const ulonglong2*>(s_hp + (pr + g) * 36);
+    const uint4* src = reinterpret_cast<const uint4*>(s_hd + (pr + g) * 28);
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const ulonglong2 f = src[c];
-      hp[g][2 * c] = f.x;
-      hp[g][2 * c + 1] = f.y;
+    for (int c = 0; c < 6; ++c) {
+      const uint4 v = src[c];
+      hop[g].d[4 * c] = v.x;
+      hop[g].d[4 * c + 1] = v.y;
+      hop[g].d[4 * c + 2] = v.z;
+      hop[g].d[4 * c + 3] = v.w;
     }
-    hs8[g] = s_hp[(pr + g) * 36 + 32];
+    const uint4 k = src[6];
+    hop[g].k0 = (int)k.x;
+    hop[g].k1 = (int)k.y;
+    hop[g].k2 = (int)k.z;
+    hop[g].f = __uint_as_float(k.w);
     row[g] = T.pos_row[p0 + pr + g];
   }
-  const f2_t* hps[G];
+  const int H = a.H;
 #pragma unroll
-  for (int g = 0; g < G; ++g) hps[g] = hp[g];
-  const int H = a.H, HH = H >> 1;
-#pragma unroll 1
-  for (int o = (int)threadIdx.x; o < H; o += NT) {
-    const uint8_t* pc = (o < HH) ? dn0 : dn1;
-    const int ol = (o < HH) ? o : o - HH;
-    const uint4 nb = *reinterpret_cast<const uint4*>(pc + (size_t)ol * 16);
-    const float sc = half_bits(reinterpret_cast<const uint16_t*>(pc + (size_t)8 * H)[ol]);
-    float dot[G];
-    block_dot<G>(nb, hps, dot);
+  for (int j = 0; j < kDnRowsPerThread; ++j) {
+    const int o = (int)threadIdx.x + NT * j;
+    if (o < H) {
+      const NibBytes n = nib_bytes(d.nb[j]);
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float y = __fmul_rn(sc, __fmaf_rn(dot[g], 0x1p62f, hs8[g]));
-      const long long q = __float2ll_rn(y * 4294967296.0f);
-      atomicAdd(acc_copy + (size_t)row[g] * H + o, (unsigned long long)q);
+      for (int g = 0; g < G; ++g) {
+        const float y = __fmul_rn(d.sc[j], bdot24(n, hop[g]));
+        const long long q = __float2ll_rn(y * 4294967296.0f);
+        red_add_u64(acc_copy + (size_t)row[g] * H + o, (unsigned long long)q);
+      }
     }
   }
 }
 
-__device__ __noinline__ void split_down(const RoundArgs& a, const Tables& T, const uint8_t* dn0, const uint8_t* dn1,
-                                           const float* s_hp, int p0, int Re, unsigned long long* acc_copy) {
+__device__ __forceinline__ void split_down(const RoundArgs& a, const Tables& T, const DnRows& d, const uint32_t* s_hd,
+                                           int p0, int Re, unsigned long long* acc_copy) {
   int pr = 0;
-  for (; pr + 1 < Re; pr += 2) split_down_rows<2>(a, T, dn0, dn1, s_hp, p0, pr, acc_copy);
-  if (pr < Re) split_down_rows<1>(a, T, dn0, dn1, s_hp, p0, pr, acc_copy);
+  for (; pr + 1 < Re; pr += 2) split_down_rows<2>(a, T, d, s_hd, p0, pr, acc_copy);
+  if (pr < Re) split_down_rows<1>(a, T, d, s_hd, p0, pr, acc_copy);
 }
 
 // This CTA's output slice [o0, o0 + no) of a finished layer: sum of the accumulator
 // copies -> fp32 output; the copies are cleared for the next layer.  Threads from
 // `first` on do it.
-__device__ __forceinline__ void split_finish(const RoundArgs& a, float* out, int o0, int no, int first) {
+__device__ __forceinline__ void split_finish(const RoundArgs& a, int layer, int o0, int no, int first) {
   const size_t stride = (size_t)a.R * a.H;
+  float* out = a.out + (size_t)layer * stride;
+  unsigned long long* buf = a.acc + (size_t)(layer & 1) * kSplitCopies * stride;
   for (int i = (int)threadIdx.x - first; i < a.R * no; i += NT - first) {
     if (i < 0) break;
     const int r = i / no, o = o0 + (i - r * no);
-    unsigned long long* p = a.acc + (size_t)r * a.H + o;
+    unsigned long long* p = buf + (size_t)r * a.H + o;
     unsigned long long s = 0ull;
 #pragma unroll
     for (int c = 0; c < kSplitCopies; ++c) s += __ldcg(p + c * stride);
@@ -1169,23 +1262,131 @@ __device__ __forceinline__ void split_stamp(const RoundArgs& a, int l, int ph) {
     a.phase_ts[((size_t)l * kSplitPhases + ph) * gridDim.x + blockIdx.x] = gtimer();
 }
 
+// The units [u_beg, u_end) of layer l (pieces [jbase, jbase + 6 (u_end - u_beg)) of this
+// CTA's ring sequence, the first n_init already issued).  Out of line, so that the unit
+// loop has the register file to itself; false (after draining) if a wait gave up.
+template <int NG, bool XR, bool XS>
+__device__ __noinline__ bool split_units(const RoundArgs& a, int l, unsigned char* smem, long long jbase, int u_beg,
+                                         int u_end, int n_init, bool router_pend, uint32_t bar_router,
+                                         unsigned ph_router) {
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int H = a.H, NS = a.I >> 5;
+  const SplitPlan& P = g_splan;
+  const int nslot = P.nslot;
+  // ring position of this layer's first piece; piece jbase + j sits in slot (s0 + j) % nslot
+  const unsigned s0 = (unsigned)(jbase % nslot), par0 = (unsigned)((jbase / nslot) & 1);
+  auto slot_of = [&](long long J) { return (int)((s0 + (unsigned)(J - jbase)) % (unsigned)nslot); };
+  auto par_of = [&](long long J) { return (par0 + (s0 + (unsigned)(J - jbase)) / (unsigned)nslot) & 1u; };
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P.bars);
+  uint8_t* ring = smem + P.ring;
+  const uint4* s_xd = reinterpret_cast<const uint4*>(smem + P.xd);
+  const uint4* s_xk = reinterpret_cast<const uint4*>(smem + P.xk);
+  float* s_part = reinterpret_cast<float*>(smem + P.part);
+  uint32_t* s_hd = reinterpret_cast<uint32_t*>(smem + P.hd);
+  const Tables T{reinterpret_cast<int*>(smem + P.uni),     reinterpret_cast<int*>(smem + P.csr),
+                 reinterpret_cast<int*>(smem + P.pair),    reinterpret_cast<float*>(smem + P.w),
+                 reinterpret_cast<int*>(smem + P.nunion),  reinterpret_cast<int*>(smem + P.pos_ui),
+                 reinterpret_cast<int*>(smem + P.pos_row), reinterpret_cast<int*>(smem + P.slot),
+                 reinterpret_cast<int*>(smem + P.pick)};
+  const LayerPtrs& W = a.layer[l];
+  const uint16_t* x = a.x + (size_t)l * a.R * H;
+  // layer l adds into accumulator buffer l & 1, copy blockIdx % kSplitCopies
+  unsigned long long* acc_copy = a.acc + ((size_t)(l & 1) * kSplitCopies + blockIdx.x % kSplitCopies) * a.R * H;
+  const int nu = u_end - u_beg, npieces = nu * kPieces;
+  int issued = n_init;  // pieces of this layer issued so far (thread 0's count, uniform)
+  long long consumed = jbase;
+  const int rb = warp / NG, kg = warp % NG;
+  const int my_piece = (rb * 4 * NG) >> 4;  // the gate/up piece holding this warp's rows
+  bool stamped = false;
+  for (int t = 0; t < nu; ++t) {
+    const int u = u_beg + t, ui = u / NS;
+    const int p0 = T.csr_off[ui], Re = T.csr_off[ui + 1] - p0;
+    if (t + 1 == nu && t > 0) split_stamp(a, l, 6);
+    // ---- gate/up: each warp waits for its own piece ----
+    {
+      const long long J = jbase + (long long)t * kPieces + my_piece;
+      bool ok = mbar_wait_bounded(smem_u32(bars + slot_of(J)), par_of(J), a.status, a.wait_cycles);
+      if (ok) {
+        if (!stamped && warp == 0) {
+          split_stamp(a, l, 5);
+          if (nu == 1) split_stamp(a, l, 6);
+          stamped = true;
+        }
+        if (XR)
+          split_gateup_one<NG>(a, T, ring + (size_t)slot_of(J) * P.slot_bytes, rb, kg, p0, s_xd, s_xk, s_part);
+        else
+          split_gateup_rows<NG, XS>(a, T, ring + (size_t)slot_of(J) * P.slot_bytes, rb, kg, p0, Re, s_xd, s_xk, x,
+                                    s_part);
+      }
+      if (__syncthreads_or(!ok)) {
+        drain_and_abort(a, bars, nslot, consumed, jbase + issued, router_pend, bar_router, ph_router);
+        return false;
+      }
+    }
+    if (t + 1 == nu) split_stamp(a, l, 7);
+    consumed = jbase + (long long)t * kPieces + kGuPieces;
+    if (tid < kGuPieces) {
+      const int j = t * kPieces + tid + nslot;
+      if (j < npieces) {
+        const long long J = jbase + j;
+        issue_piece(a, W, T, NS, u_beg, j, ring + (size_t)slot_of(J) * P.slot_bytes, smem_u32(bars + slot_of(J)));
+      }
+    }
+    issued = min(npieces, max(issued, t * kPieces + kGuPieces + nslot));
+    // the down pieces (usually landed by now) are waited and this thread's rows loaded
+    // while the SwiGLU warps work
+    DnRows dr;
+    {
+      const long long J0 = jbase + (long long)t * kPieces + kGuPieces, J1 = J0 + 1;
+      split_swiglu(a, T, s_part, NG, p0, Re, s_hd);  // (warps below Re; the others go on)
+      const bool ok = mbar_wait_bounded(smem_u32(bars + slot_of(J0)), par_of(J0), a.status, a.wait_cycles) &&
+                      mbar_wait_bounded(smem_u32(bars + slot_of(J1)), par_of(J1), a.status, a.wait_cycles);
+      if (ok) load_dn_rows(H, ring + (size_t)slot_of(J0) * P.slot_bytes, ring + (size_t)slot_of(J1) * P.slot_bytes, dr);
+      if (__syncthreads_or(!ok)) {
+        drain_and_abort(a, bars, nslot, consumed, jbase + issued, router_pend, bar_router, ph_router);
+        return false;
+      }
+    }
+    if (t + 1 == nu) {
+      split_stamp(a, l, 8);
+      split_stamp(a, l, 9);
+    }
+    split_down(a, T, dr, s_hd, p0, Re, acc_copy);
+    __syncthreads();
+    consumed = jbase + (long long)(t + 1) * kPieces;
+    if (tid < kDnPieces) {
+      const int j = t * kPieces + kGuPieces + tid + nslot;
+      if (j < npieces) {
+        const long long J = jbase + j;
+        issue_piece(a, W, T, NS, u_beg, j, ring + (size_t)slot_of(J) * P.slot_bytes, smem_u32(bars + slot_of(J)));
+      }
+    }
+    issued = min(npieces, max(issued, (t + 1) * kPieces + nslot));
+  }
+  if (nu == 0)
+    for (int ph = 5; ph <= 9; ++ph) split_stamp(a, l, ph);
+  return true;
+}
+
 // NG: hidden blocks in groups of 32 lanes (1 up to H 1024, 2 above).  XR: one row, its
 // activation pairs in registers.  XS: the rows are staged as pairs in shared memory.
 template <int NG, bool XR, bool XS>
 __global__ void __launch_bounds__(NT, 1) k_split(const __grid_constant__ RoundArgs a) {
   extern __shared__ __align__(1024) unsigned char smem[];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int G = gridDim.x, H = a.H, NB = H >> 5, NS = a.I >> 5;
-  const SplitPlan P = split_plan(a.H, a.I, a.E, a.R, a.k, G);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int G = gridDim.x, H = a.H, NS = a.I >> 5;
+  // the plan lives in shared memory: its fields are read where they are used instead of
+  // being held in registers across the layer loop
+  if (tid == 0) g_splan = split_plan(a.H, a.I, a.E, a.R, a.k, G);
+  __syncthreads();
+  const SplitPlan& P = g_splan;
   const int nslot = P.nslot;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P.bars);
   const uint32_t bar_router = smem_u32(bars + nslot);
   uint8_t* ring = smem + P.ring;
   float* s_rw = reinterpret_cast<float*>(smem + P.router);
-  float4* s_xp = reinterpret_cast<float4*>(smem + P.xp);
-  float* s_xs = reinterpret_cast<float*>(smem + P.xs);
-  float* s_part = reinterpret_cast<float*>(smem + P.part);
-  float* s_hp = reinterpret_cast<float*>(smem + P.hp);
+  uint4* s_xd = reinterpret_cast<uint4*>(smem + P.xd);
+  uint4* s_xk = reinterpret_cast<uint4*>(smem + P.xk);
   int* s_range = reinterpret_cast<int*>(smem + P.misc);
   Tables T{reinterpret_cast<int*>(smem + P.uni),     reinterpret_cast<int*>(smem + P.csr),
            reinterpret_cast<int*>(smem + P.pair),    reinterpret_cast<float*>(smem + P.w),
@@ -1200,7 +1401,6 @@ __global__ void __launch_bounds__(NT, 1) k_split(const __grid_constant__ RoundAr
   const int o0 = (int)(((long long)blockIdx.x * H) / G);
   const int no = (int)(((long long)(blockIdx.x + 1) * H) / G) - o0;
   const int fin0 = NT / 2;  // first thread of the output finishing pass
-  unsigned long long* acc_copy = a.acc + (size_t)(blockIdx.x % kSplitCopies) * a.R * H;
   if (tid == 0) {
     for (int i = 0; i <= nslot; ++i) mbar_init(smem_u32(bars + i), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -1209,7 +1409,7 @@ __global__ void __launch_bounds__(NT, 1) k_split(const __grid_constant__ RoundAr
   // the accumulator copies of this CTA's output slice start at zero (ordered before any
   // other CTA's adds by the first grid barrier)
   if (!a.route_only)
-    for (int i = tid; i < kSplitCopies * a.R * no; i += NT) {
+    for (int i = tid; i < 2 * kSplitCopies * a.R * no; i += NT) {
       const int c = i / (a.R * no), rem = i - c * (a.R * no), r = rem / no;
       __stcg(a.acc + ((size_t)c * a.R + r) * H + o0 + (rem - r * no), 0ull);
     }
@@ -1220,12 +1420,10 @@ __global__ void __launch_bounds__(NT, 1) k_split(const __grid_constant__ RoundAr
   Sync sy;
   long long jbase = 0;  // pieces issued by this CTA in earlier layers (ring position)
   auto slot_of = [&](long long J) { return (int)(J % nslot); };
-  auto par_of = [&](long long J) { return (unsigned)((J / nslot) & 1); };
   for (int l = 0; l < a.L; ++l) {
     const LayerPtrs& W = a.layer[l];
     const uint16_t* x = a.x + (size_t)l * a.R * H;
     split_stamp(a, l, 0);
-    if (l > 0) split_finish(a, a.out + (size_t)(l - 1) * a.R * H, o0, no, fin0);
     if (tid == 0 && l + 1 < a.L)  // the next layer's rows into L2 (its router reads them)
       asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(x + (size_t)a.R * H),
                    "r"((unsigned)(a.R * H * 2))
@@ -1258,7 +1456,7 @@ __global__ void __launch_bounds__(NT, 1) k_split(const __grid_constant__ RoundAr
       }
       T.slot[e] = sl;
     }
-    if (XS && !a.route_only) stage_xpairs(a, x, s_xp, s_xs);
+    if (XS && !a.route_only) stage_xdigits(a, x, s_xd, s_xk);
     if (!grid_wait(a, sy)) {
       drain_and_abort(a, bars, nslot, 0, 0, router_pend, bar_router, ph_router);
       return;
@@ -1271,114 +1469,32 @@ __global__ void __launch_bounds__(NT, 1) k_split(const __grid_constant__ RoundAr
       return;
     }
     (void)U;
+    split_stamp(a, l, 3);
     const int u_beg = s_range[0], u_end = s_range[1];
     const int nu = u_end - u_beg, npieces = nu * kPieces;
     const int n_init = min(nslot, npieces);
-    if (tid == 0)
-      for (int j = 0; j < n_init; ++j) {
-        const long long J = jbase + j;
-        issue_piece(a, W, T, NS, u_beg, j, ring + (size_t)slot_of(J) * P.slot_bytes, smem_u32(bars + slot_of(J)));
-      }
+    // one issuing thread per piece
+    if (tid < n_init) {
+      const long long J = jbase + tid;
+      issue_piece(a, W, T, NS, u_beg, tid, ring + (size_t)slot_of(J) * P.slot_bytes, smem_u32(bars + slot_of(J)));
+    }
     if (one && warp == 1) softmax_one(a, T);
-    // one row: this lane's block of activation pairs in registers for the whole layer
-    f2_t xr[16];
-    float xsr = 0.f;
-    if (XR) {
-      const int b = 32 * (warp % NG) + lane;
-      if (b < NB) {
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const ulonglong2 f = *reinterpret_cast<const ulonglong2*>(s_xp + (size_t)c * NB + b);
-          xr[2 * c] = f.x;
-          xr[2 * c + 1] = f.y;
-        }
-        xsr = s_xs[b];
-      } else {
-#pragma unroll
-        for (int c = 0; c < 16; ++c) xr[c] = 0ull;
-      }
-    }
-    split_stamp(a, l, 3);
+    // the previous layer's output slice (upper half of the threads) while this layer's
+    // first bytes are on their way: every add of that layer went into the other
+    // accumulator buffer and is in (its closing barrier is behind us)
+    if (l > 0) split_finish(a, l - 1, o0, no, fin0);
+    split_stamp(a, l, 4);
     __syncthreads();
-    int issued = n_init;  // pieces of this layer issued so far (thread 0's count, uniform)
-    long long consumed = jbase;
-    const int rb = warp / NG, kg = warp % NG;
-    const int my_piece = (rb * 4 * NG) >> 4;  // the gate/up piece holding this warp's rows
-    bool stamped = false;
-    for (int t = 0; t < nu; ++t) {
-      const int u = u_beg + t, ui = u / NS;
-      const int p0 = T.csr_off[ui], Re = T.csr_off[ui + 1] - p0;
-      if (t + 1 == nu) split_stamp(a, l, 5);
-      // ---- gate/up: each warp waits for its own piece ----
-      {
-        const long long J = jbase + (long long)t * kPieces + my_piece;
-        bool ok = mbar_wait_bounded(smem_u32(bars + slot_of(J)), par_of(J), a.status, a.wait_cycles);
-        if (ok) {
-          if (!stamped && warp == 0) {
-            split_stamp(a, l, 4);
-            stamped = true;
-          }
-          if (XR)
-            split_gateup<NG, true, true>(a, T, ring + (size_t)slot_of(J) * P.slot_bytes, rb, kg, p0, Re, xr, xsr,
-                                         s_xp, s_xs, x, s_part);
-          else
-            split_gateup_rows<NG, XS>(a, T, ring + (size_t)slot_of(J) * P.slot_bytes, rb, kg, p0, Re, s_xp, s_xs, x,
-                                      s_part);
-        }
-        if (__syncthreads_or(!ok)) {
-          drain_and_abort(a, bars, nslot, consumed, jbase + issued, router_pend, bar_router, ph_router);
-          return;
-        }
-      }
-      consumed = jbase + (long long)t * kPieces + kGuPieces;
-      if (tid == 0)
-        for (int q = 0; q < kGuPieces; ++q) {
-          const int j = t * kPieces + q + nslot;
-          if (j < npieces) {
-            const long long J = jbase + j;
-            issue_piece(a, W, T, NS, u_beg, j, ring + (size_t)slot_of(J) * P.slot_bytes, smem_u32(bars + slot_of(J)));
-          }
-        }
-      issued = min(npieces, max(issued, t * kPieces + kGuPieces + nslot));
-      split_swiglu(a, T, s_part, NG, p0, Re, s_hp);
-      __syncthreads();
-      // ---- down: every thread waits for both down pieces ----
-      {
-        const long long J0 = jbase + (long long)t * kPieces + kGuPieces, J1 = J0 + 1;
-        bool ok = mbar_wait_bounded(smem_u32(bars + slot_of(J0)), par_of(J0), a.status, a.wait_cycles) &&
-                  mbar_wait_bounded(smem_u32(bars + slot_of(J1)), par_of(J1), a.status, a.wait_cycles);
-        if (ok)
-          split_down(a, T, ring + (size_t)slot_of(J0) * P.slot_bytes, ring + (size_t)slot_of(J1) * P.slot_bytes, s_hp,
-                     p0, Re, acc_copy);
-        if (__syncthreads_or(!ok)) {
-          drain_and_abort(a, bars, nslot, consumed, jbase + issued, router_pend, bar_router, ph_router);
-          return;
-        }
-      }
-      consumed = jbase + (long long)(t + 1) * kPieces;
-      if (tid == 0)
-        for (int q = kGuPieces; q < kPieces; ++q) {
-          const int j = t * kPieces + q + nslot;
-          if (j < npieces) {
-            const long long J = jbase + j;
-            issue_piece(a, W, T, NS, u_beg, j, ring + (size_t)slot_of(J) * P.slot_bytes, smem_u32(bars + slot_of(J)));
-          }
-        }
-      issued = min(npieces, max(issued, (t + 1) * kPieces + nslot));
-    }
-    if (nu == 0) {
-      split_stamp(a, l, 4);
-      split_stamp(a, l, 5);
-    }
+    if (!split_units<NG, XR, XS>(a, l, smem, jbase, u_beg, u_end, n_init, router_pend, bar_router, ph_router)) return;
     jbase += npieces;
-    split_stamp(a, l, 6);
+    split_stamp(a, l, 10);
     if (!grid_sync(a, sy)) {  // B3: every add of this layer is in
       drain_and_abort(a, bars, nslot, 0, 0, router_pend, bar_router, ph_router);
       return;
     }
-    split_stamp(a, l, 7);
+    split_stamp(a, l, 11);
   }
-  split_finish(a, a.out + (size_t)(a.L - 1) * a.R * H, o0, no, fin0);
+  split_finish(a, a.L - 1, o0, no, fin0);
 }
 
 // ---------------------------------------------------------------------------------
@@ -2451,7 +2567,7 @@ int moe_profile_phases(moe_handle* h, double* mean_us, double* max_us, int32_t n
 
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = (size_t)4 << 20;  // 4 MiB per device
+constexpr size_t kNoAllocScratchBytes = (size_t)8 << 20;  // 8 MiB per device
 constexpr int kNoAllocMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];

@@ -101,7 +101,7 @@ def test_noalloc_argument_errors_launch_nothing():
     # without a status word the kernel's findings would be lost: refused
     small = mv.make_dims(256, 8, 2, 256, 1)
     assert lib.moe_decode_layer_noalloc(ctypes.byref(small), ctypes.byref(w), p, 1, p, None, None) == mv.MOE_EINVAL
-    # 32 rows x top-32 x intermediate 2048 needs 8 MiB of exchanged activations
+    # 32 rows x top-32 x intermediate 2048: 8 MiB of exchanged activations alone
     dims = mv.make_dims(2048, 64, 32, 2048, 32)
     assert mv.moe_workspace_bytes(dims, 32) > mv.MOE_NOALLOC_SCRATCH_BYTES
     rc = lib.moe_decode_layer_noalloc(ctypes.byref(dims), ctypes.byref(w), p, 32, p, status.data_ptr(), None)
