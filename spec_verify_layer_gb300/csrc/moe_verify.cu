@@ -912,7 +912,7 @@ __device__ __noinline__ void drain_and_abort(const RoundArgs& a, const uint64_t*
 // one 16-byte block, then their fp16 scales) per unit, in unit order.
 
 constexpr int kSplitCopies = kAccCopies;
-constexpr int kSplitMaxSlots = 16;
+constexpr int kSplitMaxSlots = 6;  // more slots measured slower (the ring crowds out L1)
 constexpr int kGuPieces = 4;  // gate/up pieces per unit (8 intermediate indices each)
 constexpr int kDnPieces = 2;  // down pieces per unit (H/2 output rows each)
 constexpr int kPieces = kGuPieces + kDnPieces;
@@ -1263,10 +1263,11 @@ __device__ __forceinline__ void split_stamp(const RoundArgs& a, int l, int ph) {
 }
 
 // The units [u_beg, u_end) of layer l (pieces [jbase, jbase + 6 (u_end - u_beg)) of this
-// CTA's ring sequence, the first n_init already issued).  Out of line, so that the unit
-// loop has the register file to itself; false (after draining) if a wait gave up.
+// CTA's ring sequence, the first n_init already issued); false (after draining) if a wait
+// gave up.  Inlined: a call would save and restore the kernel's live registers through
+// local memory, which the large shared-memory carve-out leaves little L1 for.
 template <int NG, bool XR, bool XS>
-__device__ __noinline__ bool split_units(const RoundArgs& a, int l, unsigned char* smem, long long jbase, int u_beg,
+__device__ __forceinline__ bool split_units(const RoundArgs& a, int l, unsigned char* smem, long long jbase, int u_beg,
                                          int u_end, int n_init, bool router_pend, uint32_t bar_router,
                                          unsigned ph_router) {
   const int tid = threadIdx.x, warp = tid >> 5;
@@ -1457,6 +1458,10 @@ __global__ void __launch_bounds__(NT, 1) k_split(const __grid_constant__ RoundAr
       T.slot[e] = sl;
     }
     if (XS && !a.route_only) stage_xdigits(a, x, s_xd, s_xk);
+    // the previous layer's output slice (upper half of the threads) while the logits
+    // barrier completes: every add of that layer went into the other accumulator buffer
+    // and is in (its closing barrier is behind us)
+    if (l > 0 && !a.route_only) split_finish(a, l - 1, o0, no, fin0);
     if (!grid_wait(a, sy)) {
       drain_and_abort(a, bars, nslot, 0, 0, router_pend, bar_router, ph_router);
       return;
@@ -1479,10 +1484,6 @@ __global__ void __launch_bounds__(NT, 1) k_split(const __grid_constant__ RoundAr
       issue_piece(a, W, T, NS, u_beg, tid, ring + (size_t)slot_of(J) * P.slot_bytes, smem_u32(bars + slot_of(J)));
     }
     if (one && warp == 1) softmax_one(a, T);
-    // the previous layer's output slice (upper half of the threads) while this layer's
-    // first bytes are on their way: every add of that layer went into the other
-    // accumulator buffer and is in (its closing barrier is behind us)
-    if (l > 0) split_finish(a, l - 1, o0, no, fin0);
     split_stamp(a, l, 4);
     __syncthreads();
     if (!split_units<NG, XR, XS>(a, l, smem, jbase, u_beg, u_end, n_init, router_pend, bar_router, ph_router)) return;
