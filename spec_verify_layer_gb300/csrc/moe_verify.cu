@@ -1047,8 +1047,9 @@ __device__ __forceinline__ void split_store_part(float (&v)[N], int lane, float*
 
 // The gate/up pass of one unit for this warp: rows [rb RPW, (rb + 1) RPW) of the unit's
 // 64 (RPW = 4 NG, all in one piece), K group kg, every activation row of the expert (CSR
-// positions p0 .. p0 + Re - 1), two at a time (their code bytes are extracted once), four
-// weight rows at a time.  XR: one row whose operand the caller holds in registers.
+// positions p0 .. p0 + Re - 1) one after the other, four weight rows at a time (two rows
+// at once, sharing the code bytes, measured slower: the operands no longer fit the
+// registers).  XR: one row whose operand the caller holds in registers.
 template <int NG, bool XR, bool XS>
 __device__ __forceinline__ void split_gateup(const RoundArgs& a, const Tables& T, const uint8_t* piece, int rb,
                                              int kg, int p0, int Re, const Op16& xr, const uint4* s_xd,
@@ -1065,22 +1066,7 @@ __device__ __forceinline__ void split_gateup(const RoundArgs& a, const Tables& T
     split_store_part<RPW>(v[0], lane, s_part, row0, NG, kg, a.R, 0);
     return;
   }
-  int pr = 0;
-  for (; pr + 1 < Re; pr += 2) {
-    Op16 xo[2];
-    if (valid) {
-      load_xop<XS>(a, x, s_xd, s_xk, T.pos_row[p0 + pr], b, xo[0]);
-      load_xop<XS>(a, x, s_xd, s_xk, T.pos_row[p0 + pr + 1], b, xo[1]);
-    }
-#pragma unroll 1
-    for (int h = 0; h < RPW; h += 4) {
-      float v[2][4];
-      split_gu_rows<4, 2>(piece, a.H, (row0 + h) & 15, b, valid, xo, v);
-      split_store_part<4>(v[0], lane, s_part, row0 + h, NG, kg, a.R, pr);
-      split_store_part<4>(v[1], lane, s_part, row0 + h, NG, kg, a.R, pr + 1);
-    }
-  }
-  if (pr < Re) {
+  for (int pr = 0; pr < Re; ++pr) {
     Op16 xo[1];
     if (valid) load_xop<XS>(a, x, s_xd, s_xk, T.pos_row[p0 + pr], b, xo[0]);
 #pragma unroll 1
@@ -1189,52 +1175,37 @@ __device__ __forceinline__ void load_dn_rows(int H, const uint8_t* dn0, const ui
   }
 }
 
-// Down products of one unit for this thread's rows, activation positions pr .. pr + G - 1:
-// y -> 2^32-scaled integers added into this CTA's accumulator copy.
-template <int G>
-__device__ __forceinline__ void split_down_rows(const RoundArgs& a, const Tables& T, const DnRows& d,
-                                                const uint32_t* s_hd, int p0, int pr, unsigned long long* acc_copy) {
-  Op24 hop[G];
-  int row[G];
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    const uint4* src = reinterpret_cast<const uint4*>(s_hd + (pr + g) * 28);
+// Down products of one unit for this thread's rows, every activation position of the
+// expert in turn: y -> 2^32-scaled integers added into this CTA's accumulator copy.
+__device__ __forceinline__ void split_down(const RoundArgs& a, const Tables& T, const DnRows& d, const uint32_t* s_hd,
+                                           int p0, int Re, unsigned long long* acc_copy) {
+  const int H = a.H;
+  for (int pr = 0; pr < Re; ++pr) {
+    Op24 hop;
+    const uint4* src = reinterpret_cast<const uint4*>(s_hd + pr * 28);
 #pragma unroll
     for (int c = 0; c < 6; ++c) {
       const uint4 v = src[c];
-      hop[g].d[4 * c] = v.x;
-      hop[g].d[4 * c + 1] = v.y;
-      hop[g].d[4 * c + 2] = v.z;
-      hop[g].d[4 * c + 3] = v.w;
+      hop.d[4 * c] = v.x;
+      hop.d[4 * c + 1] = v.y;
+      hop.d[4 * c + 2] = v.z;
+      hop.d[4 * c + 3] = v.w;
     }
     const uint4 k = src[6];
-    hop[g].k0 = (int)k.x;
-    hop[g].k1 = (int)k.y;
-    hop[g].k2 = (int)k.z;
-    hop[g].f = __uint_as_float(k.w);
-    row[g] = T.pos_row[p0 + pr + g];
-  }
-  const int H = a.H;
+    hop.k0 = (int)k.x;
+    hop.k1 = (int)k.y;
+    hop.k2 = (int)k.z;
+    hop.f = __uint_as_float(k.w);
+    unsigned long long* acc_row = acc_copy + (size_t)T.pos_row[p0 + pr] * H;
 #pragma unroll
-  for (int j = 0; j < kDnRowsPerThread; ++j) {
-    const int o = (int)threadIdx.x + NT * j;
-    if (o < H) {
-      const NibBytes n = nib_bytes(d.nb[j]);
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float y = __fmul_rn(d.sc[j], bdot24(n, hop[g]));
-        const long long q = __float2ll_rn(y * 4294967296.0f);
-        red_add_u64(acc_copy + (size_t)row[g] * H + o, (unsigned long long)q);
+    for (int j = 0; j < kDnRowsPerThread; ++j) {
+      const int o = (int)threadIdx.x + NT * j;
+      if (o < H) {
+        const float y = __fmul_rn(d.sc[j], bdot24(nib_bytes(d.nb[j]), hop));
+        red_add_u64(acc_row + o, (unsigned long long)__float2ll_rn(y * 4294967296.0f));
       }
     }
   }
-}
-
-__device__ __forceinline__ void split_down(const RoundArgs& a, const Tables& T, const DnRows& d, const uint32_t* s_hd,
-                                           int p0, int Re, unsigned long long* acc_copy) {
-  int pr = 0;
-  for (; pr + 1 < Re; pr += 2) split_down_rows<2>(a, T, d, s_hd, p0, pr, acc_copy);
-  if (pr < Re) split_down_rows<1>(a, T, d, s_hd, p0, pr, acc_copy);
 }
 
 // This CTA's output slice [o0, o0 + no) of a finished layer: sum of the accumulator
