@@ -42,6 +42,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--layers", type=int, default=0, help="override the stack depth (0 = 40)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e512-layers", type=int, default=0, help="override the 512-expert stack depth (0 = 48)")
     ap.add_argument("--rows", type=int, default=1, choices=[1, 4, 16],
                     help="rows of the headline round (1 = the decode-width workload; 4 and 16 "
                          "put that round first, e.g. to profile its first launch)")
@@ -229,6 +230,79 @@ def run_reference(args):
 
 # ---- our arm ---------------------------------------------------------------------------------
 
+def pin_one_core():
+    """Pins the calling process to one host core (the CPU baseline is single-threaded and
+    stated as 1 of N cores); returns (core, host_cores, previous affinity)."""
+    host = os.cpu_count() or 1
+    try:
+        prev = os.sched_getaffinity(0)
+        core = max(prev)
+        os.sched_setaffinity(0, {core})
+        return core, host, prev
+    except (AttributeError, OSError):
+        return None, host, None
+
+
+def unpin(prev):
+    if prev is not None:
+        try:
+            os.sched_setaffinity(0, prev)
+        except OSError:
+            pass
+
+
+def cpu_baseline_leg(cfg, layers, budget_s, rows, sigma, note):
+    """The oracle as it stands, single-threaded, pinned to one host core, on a bounded
+    sample of whole layers of the workload (input generation outside the timing)."""
+    core, host, prev = pin_one_core()
+    try:
+        t, b, n = oracle_sample(cfg, layers, budget_s, rows=rows, sigma=sigma)
+    finally:
+        unpin(prev)
+    return {"value": b / t / 1e9, "unit": UNIT, "cores": 1, "host_cores": host, "pinned_core": core,
+            "kind": "oracle", "us_per_layer": 1e6 * t / n,
+            "sample": f"{n} layers of {note} ({rows} row(s)), oracle route + layer only, one of {host} host "
+                      f"cores (pinned), ~{budget_s:.0f} s of CPU work"}
+
+
+class StackRun:
+    """One workload's stack of layers on the device plus a handle and a workspace."""
+
+    def __init__(self, mv, cfg, L, max_rows, dev, stream):
+        import numpy as np  # noqa: F401
+        import syngen
+        from spec_verify_layer_gb300.weights import Packer, workspace
+        self.mv, self.cfg, self.L, self.dev, self.stream = mv, cfg, L, dev, stream
+        self.dims = mv.make_dims(cfg.hidden, cfg.experts, cfg.top_k, cfg.inter, max_rows)
+        packer = Packer(self.dims)
+        self.layers = []
+        for l in range(L):
+            packer.pack_all(lambda e, l=l: syngen.expert(cfg, l, e))
+            self.layers.append(packer.upload(syngen.router(cfg, l), dev))
+        self.wl = [ly.w for ly in self.layers]
+        self.handle = mv.moe_create(self.dims, dev.index or 0)
+        self.ws = workspace(self.dims, max_rows, dev)
+
+    def close(self):
+        self.mv.moe_destroy(self.handle)
+        self.layers = []
+
+    def buffers(self, rows, sigma):
+        import numpy as np
+        import torch
+        import syngen
+        xs = np.stack([syngen.rows(self.cfg, l, rows, sigma) for l in range(self.L)])
+        x = torch.from_numpy(xs.view(np.int16)).to(self.dev)
+        out = torch.empty((self.L, rows, self.cfg.hidden), dtype=torch.float32, device=self.dev)
+        stats = torch.zeros(self.L, dtype=torch.int32, device=self.dev)
+        return xs, x, out, stats
+
+    def replay(self, rows, x, out, stats, graph=True):
+        self.mv.moe_round(self.handle, self.wl, x.data_ptr(), rows, out.data_ptr(),
+                          stats.data_ptr() if stats is not None else None, self.ws.data_ptr(), self.ws.numel(),
+                          graph, self.stream.cuda_stream)
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -236,7 +310,6 @@ def run_ours(args):
 
     import spec_verify_layer_gb300 as mv  # fails loudly when the library is missing
     import syngen
-    from spec_verify_layer_gb300.weights import Packer, workspace
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -245,29 +318,12 @@ def run_ours(args):
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
 
     cfg = syngen.CONFIGS["a3b_r1"]
     L = args.layers or cfg.layers
     H = cfg.hidden
-    max_rows = 16
-    dims = mv.make_dims(H, cfg.experts, cfg.top_k, cfg.inter, max_rows)
-    packer = Packer(dims)
-    layers = []
-    for l in range(L):
-        packer.pack_all(lambda e, l=l: syngen.expert(cfg, l, e))
-        layers.append(packer.upload(syngen.router(cfg, l), dev))
-    wl = [ly.w for ly in layers]
-    handle = mv.moe_create(dims, local)
-    ws = workspace(dims, max_rows, dev)
-    stream = torch.cuda.Stream(dev)
-    st = stream.cuda_stream
-
-    def buffers(rows, sigma):
-        xs = np.stack([syngen.rows(cfg, l, rows, sigma) for l in range(L)])
-        x = torch.from_numpy(xs.view(np.int16)).to(dev)
-        out = torch.empty((L, rows, H), dtype=torch.float32, device=dev)
-        stats = torch.zeros(L, dtype=torch.int32, device=dev)
-        return xs, x, out, stats
+    a3b = StackRun(mv, cfg, L, 16, dev, stream)
 
     def barrier():
         if world > 1:
@@ -276,13 +332,12 @@ def run_ours(args):
     def max_over_ranks(v):
         return reduce_max(v, world, dev)
 
-    def time_rounds(rows, sigma, steps, warmup, sampler=None):
-        xs, x, out, stats = buffers(rows, sigma)
+    def time_rounds(sr, rows, sigma, steps, warmup):
+        xs, x, out, stats = sr.buffers(rows, sigma)
         with torch.cuda.stream(stream):
             for _ in range(warmup):
-                mv.moe_round(handle, wl, x.data_ptr(), rows, out.data_ptr(), stats.data_ptr(),
-                             ws.data_ptr(), ws.numel(), True, st)
-        launches_per_round = mv.moe_last_launch_count(handle)
+                sr.replay(rows, x, out, stats)
+        launches_per_round = mv.moe_last_launch_count(sr.handle)
         torch.cuda.synchronize(dev)
         barrier()
         torch.cuda.synchronize(dev)
@@ -291,67 +346,75 @@ def run_ours(args):
         with torch.cuda.stream(stream):
             e0.record(stream)
             for _ in range(steps):
-                mv.moe_round(handle, wl, x.data_ptr(), rows, out.data_ptr(), stats.data_ptr(),
-                             ws.data_ptr(), ws.numel(), True, st)
+                sr.replay(rows, x, out, stats)
             e1.record(stream)
         torch.cuda.synchronize(dev)
         t_wall1 = time.time()
         barrier()
         ms = max_over_ranks(e0.elapsed_time(e1))
-        assert mv.moe_last_device_status(handle, st) == mv.MOE_OK
+        assert mv.moe_last_device_status(sr.handle, stream.cuda_stream) == mv.MOE_OK
         U = stats.cpu().numpy()
-        per_round_bytes = sum(layer_bytes(cfg, int(u), rows) for u in U)
+        per_round_bytes = sum(layer_bytes(sr.cfg, int(u), rows) for u in U)
         return {"ms_total": ms, "steps": steps, "U": U, "bytes_per_round": per_round_bytes,
                 "launches_per_round": launches_per_round, "t_wall": (t_wall0, t_wall1),
                 "x": x, "out": out, "xs": xs}
 
-    def round_percentiles(rows, x, out, n):
+    def round_percentiles(sr, rows, x, out, n):
         """Per-replay device times of the round graph (an event pair around each replay,
         outside the timed region): p10 / p50 / p90 in us per round."""
-        stats_q = torch.zeros(L, dtype=torch.int32, device=dev)
+        stats_q = torch.zeros(sr.L, dtype=torch.int32, device=dev)
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
         with torch.cuda.stream(stream):
             for a0, a1 in evs:
                 a0.record(stream)
-                mv.moe_round(handle, wl, x.data_ptr(), rows, out.data_ptr(), stats_q.data_ptr(), ws.data_ptr(),
-                             ws.numel(), True, st)
+                sr.replay(rows, x, out, stats_q)
                 a1.record(stream)
         torch.cuda.synchronize(dev)
         t = sorted(1e3 * a0.elapsed_time(a1) for a0, a1 in evs)
         return {"p10": t[n // 10], "p50": t[n // 2], "p90": t[(9 * n) // 10], "replays": n}
 
-    def single_layers(rows, x, out, n):
+    def single_layers(sr, rows, x, out, n):
         """One moe_decode_layer launch per layer, rotating over the L distinct layers
         (eager, stream-ordered): us per layer, for the fused round's launch saving."""
+        ws = sr.ws
         with torch.cuda.stream(stream):
-            for l in range(L):
-                mv.moe_decode_layer(handle, wl[l], x[l].data_ptr(), rows, out[l].data_ptr(), ws.data_ptr(),
-                                    ws.numel(), st)
+            for l in range(sr.L):
+                mv.moe_decode_layer(sr.handle, sr.wl[l], x[l].data_ptr(), rows, out[l].data_ptr(), ws.data_ptr(),
+                                    ws.numel(), stream.cuda_stream)
         torch.cuda.synchronize(dev)
         a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
             a0.record(stream)
             for i in range(n):
-                l = i % L
-                mv.moe_decode_layer(handle, wl[l], x[l].data_ptr(), rows, out[l].data_ptr(), ws.data_ptr(),
-                                    ws.numel(), st)
+                l = i % sr.L
+                mv.moe_decode_layer(sr.handle, sr.wl[l], x[l].data_ptr(), rows, out[l].data_ptr(), ws.data_ptr(),
+                                    ws.numel(), stream.cuda_stream)
             a1.record(stream)
         torch.cuda.synchronize(dev)
-        assert mv.moe_last_device_status(handle, st) == mv.MOE_OK
+        assert mv.moe_last_device_status(sr.handle, stream.cuda_stream) == mv.MOE_OK
         return {"us_per_layer": 1e3 * a0.elapsed_time(a1) / n, "launches": n}
 
-    def profile_phases(rows, x, out, n_rounds):
+    def profile_phases(sr, rows, x, out, n_rounds):
         """Eager rounds with per-phase device timestamps (outside every timed region)."""
-        stats_p = torch.zeros(L, dtype=torch.int32, device=dev)
-        mv.moe_profile(handle, True)
+        stats_p = torch.zeros(sr.L, dtype=torch.int32, device=dev)
+        mv.moe_profile(sr.handle, True)
         with torch.cuda.stream(stream):
             for _ in range(n_rounds):
-                mv.moe_round(handle, wl, x.data_ptr(), rows, out.data_ptr(), stats_p.data_ptr(), ws.data_ptr(),
-                             ws.numel(), False, st)
-        eager_ms, eager_n = mv.moe_profile_read(handle, mv.KIND_ROUND)
-        ph = {k: {"mean_us": v[0], "max_us": v[1]} for k, v in mv.moe_profile_phases(handle).items()}
-        mv.moe_profile(handle, False)
+                sr.replay(rows, x, out, stats_p, graph=False)
+        eager_ms, eager_n = mv.moe_profile_read(sr.handle, mv.KIND_ROUND)
+        ph = {k: {"mean_us": v[0], "max_us": v[1]} for k, v in mv.moe_profile_phases(sr.handle).items()}
+        mv.moe_profile(sr.handle, False)
         return ph, eager_ms, eager_n
+
+    def leg(sr, r, rows, name, peak):
+        msr = r["ms_total"] / r["steps"]
+        gbs = r["bytes_per_round"] / (msr * 1e-3) / 1e9
+        U = float(np.mean(r["U"]))
+        return {"workload": name, "layers": sr.L, "rows": rows, "us_per_layer": 1e3 * msr / sr.L,
+                "us_per_round": 1e3 * msr, "hbm_gbs": gbs, "frac_of_peak": gbs / peak,
+                "unique_experts_per_layer": U, "picks_per_layer": rows * sr.cfg.top_k,
+                "tokens_per_round_equiv_per_s": rows / (msr * 1e-3), "rounds_per_s": 1.0 / (msr * 1e-3),
+                "kernel": "k_round (tensor cores)" if rows >= mv.MMA_ROWS else "k_split (CUDA cores)"}
 
     peak, peak_src = peak_hbm()
     sampler = ClockSampler(local)
@@ -359,7 +422,7 @@ def run_ours(args):
     time.sleep(0.3)
     SIGMA = {1: 0.0, 4: 0.5, 16: 0.1}
     R0 = args.rows
-    head = time_rounds(R0, SIGMA[R0], args.steps, max(args.warmup, 3))
+    head = time_rounds(a3b, R0, SIGMA[R0], args.steps, max(args.warmup, 3))
     sampler.stop()
     clocks = sampler.summary(*head["t_wall"])
 
@@ -377,8 +440,7 @@ def run_ours(args):
     with torch.cuda.stream(stream):
         for _ in range(3):
             x1.copy_(xh, non_blocking=True)
-            mv.moe_round(handle, wl, x1.data_ptr(), R0, out1.data_ptr(), stats1.data_ptr(), ws.data_ptr(),
-                         ws.numel(), True, st)
+            a3b.replay(R0, x1, out1, stats1)
             oh.copy_(out1, non_blocking=True)
             stream.synchronize()
     barrier()
@@ -386,8 +448,7 @@ def run_ours(args):
     with torch.cuda.stream(stream):
         for _ in range(e2e_steps):
             x1.copy_(xh, non_blocking=True)
-            mv.moe_round(handle, wl, x1.data_ptr(), R0, out1.data_ptr(), stats1.data_ptr(), ws.data_ptr(),
-                         ws.numel(), True, st)
+            a3b.replay(R0, x1, out1, stats1)
             oh.copy_(out1, non_blocking=True)
             stream.synchronize()
     t_e2e = max_over_ranks(time.perf_counter() - t0) / e2e_steps
@@ -395,65 +456,53 @@ def run_ours(args):
            "h2d_bytes_per_step": int(xh.numel() * 2), "d2h_bytes_per_step": int(oh.numel() * 4),
            "us_per_layer": 1e6 * t_e2e / L, "steps": e2e_steps}
 
-
-    # rows sweep on the same weights
+    # the other row counts on the same weights
     sweep = {}
     for rows in (r for r in (1, 4, 16) if r != R0):
-        sigma, name = SIGMA[rows], f"a3b_r{rows}"
-        r = time_rounds(rows, sigma, max(20, args.steps // 4), max(args.warmup, 3))
-        msr = r["ms_total"] / r["steps"]
-        gbs = r["bytes_per_round"] / (msr * 1e-3) / 1e9
-        sweep[f"r{rows}"] = {"workload": name, "us_per_layer": 1e3 * msr / L, "us_per_round": 1e3 * msr,
-                             "hbm_gbs": gbs, "frac_of_peak": gbs / peak,
-                             "unique_experts_per_layer": float(np.mean(r["U"])),
-                             "picks_per_layer": rows * cfg.top_k,
-                             "tokens_per_round_equiv_per_s": rows / (msr * 1e-3)}
-        sweep[f"r{rows}"]["phases_per_layer_us"] = profile_phases(rows, r["x"], r["out"], 3)[0]
+        r = time_rounds(a3b, rows, SIGMA[rows], max(20, args.steps // 4), max(args.warmup, 3))
+        sweep[f"r{rows}"] = leg(a3b, r, rows, f"a3b_r{rows}", peak)
+        sweep[f"r{rows}"]["phases_per_layer_us"] = profile_phases(a3b, rows, r["x"], r["out"], 3)[0]
     # the same 4-row round with the routing tail skip at the page's rank 7 (an
     # approximation: experts every row ranks 7th or lower are not evaluated)
-    mv.moe_set_tail_skip(handle, 7)
+    mv.moe_set_tail_skip(a3b.handle, 7)
     try:
-        r = time_rounds(4, 0.5, max(20, args.steps // 4), max(args.warmup, 3))
+        r = time_rounds(a3b, 4, 0.5, max(20, args.steps // 4), max(args.warmup, 3))
     finally:
-        mv.moe_set_tail_skip(handle, 0)
-    msr = r["ms_total"] / r["steps"]
-    gbs = r["bytes_per_round"] / (msr * 1e-3) / 1e9
-    sweep["r4_tail7"] = {"workload": "a3b_r4 with routing tail skip at rank 7", "us_per_layer": 1e3 * msr / L,
-                         "us_per_round": 1e3 * msr, "hbm_gbs": gbs, "frac_of_peak": gbs / peak,
-                         "unique_experts_per_layer": float(np.mean(r["U"])),
-                         "tokens_per_round_equiv_per_s": 4 / (msr * 1e-3)}
+        mv.moe_set_tail_skip(a3b.handle, 0)
+    sweep["r4_tail7"] = leg(a3b, r, 4, "a3b_r4 with routing tail skip at rank 7", peak)
 
     # The price of a verify column: rounds of R = 1..16 rows on the same 40-layer stack
     # (the draft rows at sigma 0.5 around the first row, as for 4 rows), a short timing
-    # each; R <= 7 runs on the CUDA cores, R >= 8 on the tensor cores.
+    # each; below MMA_ROWS rows on the CUDA cores (split kernel), from it on the tensor cores.
     by_rows = {}
     for rows in range(1, 17):
-        r = time_rounds(rows, 0.0 if rows == 1 else 0.5, max(20, args.steps // 40), max(args.warmup, 3))
-        msr = r["ms_total"] / r["steps"]
-        gbs = r["bytes_per_round"] / (msr * 1e-3) / 1e9
-        by_rows[str(rows)] = {"us_per_layer": round(1e3 * msr / L, 3), "hbm_gbs": round(gbs, 1),
-                              "unique_experts_per_layer": round(float(np.mean(r["U"])), 3)}
+        r = time_rounds(a3b, rows, 0.0 if rows == 1 else 0.5, max(20, args.steps // 40), max(args.warmup, 3))
+        lg = leg(a3b, r, rows, "", peak)
+        by_rows[str(rows)] = {"us_per_layer": round(lg["us_per_layer"], 3), "hbm_gbs": round(lg["hbm_gbs"], 1),
+                              "unique_experts_per_layer": round(lg["unique_experts_per_layer"], 3),
+                              "kernel": lg["kernel"]}
     sweep["rows_sweep"] = {"workload": "a3b layers, R = 1..16 rows, draft rows at sigma 0.5",
                            "by_rows": by_rows}
 
     # The prefill-width layer (many tokens per call: counting sort by expert, per-expert
     # GEMMs): PF_T tokens of diverse rows, layers cycling so every call streams distinct
     # weights; device time over the calls.
-    sweep["prefill"] = prefill_leg(mv, cfg, wl, handle, dev, stream, L, max(10, args.steps // 50),
+    sweep["prefill"] = prefill_leg(mv, cfg, a3b.wl, a3b.handle, dev, stream, L, max(10, args.steps // 50),
                                    max(args.warmup, 3))
 
-    # The round is one kernel launch (k_round): its average launch duration is the timed
-    # region's per-step time, from CUDA events on the launching stream.  A separate
-    # eager pass records where the time goes inside it (device timestamps per phase).
+    # The round is one kernel launch: its average launch duration is the timed region's
+    # per-step time, from CUDA events on the launching stream.  A separate eager pass
+    # records where the time goes inside it (device timestamps per phase).
     alg_per_launch = float(head["bytes_per_round"])
     avg_launch_us = 1e3 * ms_round
     achieved = alg_per_launch / (avg_launch_us * 1e-6) / 1e9
     prof_rounds = max(3, min(20, args.steps // 50))
-    phases, eager_ms, eager_n = profile_phases(R0, x1, out1, prof_rounds)
-    pct = round_percentiles(R0, x1, out1, max(20, min(200, args.steps // 10)))
-    single = single_layers(R0, x1, out1, max(L, min(4 * L, args.steps)))
-    roofline = {"bound": "hbm", "kernel": "k_round", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "traffic": read_traffic("k_round", L, R0), "peak_source": peak_src,
+    phases, eager_ms, eager_n = profile_phases(a3b, R0, x1, out1, prof_rounds)
+    pct = round_percentiles(a3b, R0, x1, out1, max(20, min(200, args.steps // 10)))
+    single = single_layers(a3b, R0, x1, out1, max(L, min(4 * L, args.steps)))
+    kname = "k_round" if R0 >= mv.MMA_ROWS else "k_split"
+    roofline = {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": read_traffic(kname, L, R0), "peak_source": peak_src,
                 "alg_bytes_per_launch": alg_per_launch, "avg_launch_us": avg_launch_us,
                 "launch": f"one cooperative launch per {L}-layer round, timed over {args.steps} graph replays",
                 "phases_per_layer_us": phases,
@@ -463,11 +512,36 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        t, b, n = oracle_sample(cfg, list(range(L)), budget_s=10.0)
-        cpu = {"value": b / t / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "us_per_layer": 1e6 * t / n,
-               "sample": f"{n} single-row layers of the same stack, oracle route + layer only, "
-                         f"one host core, ~10 s of CPU work"}
+        cpu = cpu_baseline_leg(cfg, list(range(L)), 10.0, 1, 0.0, "the 40-layer 35B-A3B-shaped stack")
+    a3b.close()
+    del x1, out1
+    torch.cuda.empty_cache()
+
+    # The 512-expert / top-10 / 48-layer stack with 3 rows (1 token + 2 drafts): its own
+    # weights (43.5 GB), timed the same way, with its own CPU baseline.
+    ecfg = syngen.CONFIGS["e512_r3"]
+    e512 = StackRun(mv, ecfg, args.e512_layers or ecfg.layers, ecfg.rows, dev, stream)
+    r = time_rounds(e512, ecfg.rows, ecfg.row_sigma, max(20, args.steps // 4), max(args.warmup, 3))
+    sweep["e512_r3"] = leg(e512, r, ecfg.rows, "e512_r3", peak)
+    sweep["e512_r3"]["phases_per_layer_us"] = profile_phases(e512, ecfg.rows, r["x"], r["out"], 3)[0]
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sweep["e512_r3"]["cpu_baseline"] = cpu_baseline_leg(ecfg, list(range(e512.L)), 10.0, ecfg.rows,
+                                                            ecfg.row_sigma, "the 48-layer 512-expert stack")
+    e512.close()
+    torch.cuda.empty_cache()
+
+    # The tiny layer (H 512, 8 experts, top-2, I 256): a 16-layer stack of such layers, so
+    # weights and rows sit in L2 (2 MB per layer): us only, no HBM fraction.
+    tcfg = syngen.CONFIGS["tiny"]
+    tiny = StackRun(mv, tcfg, 16, 4, dev, stream)
+    r = time_rounds(tiny, 1, 0.0, max(20, args.steps // 4), max(args.warmup, 3))
+    tl = leg(tiny, r, 1, "tiny, 16 layers (L2-resident)", peak)
+    tl["hbm_gbs"] = tl["frac_of_peak"] = None
+    tl["note"] = "weights L2-resident (about 2 MB per layer): us per layer only"
+    sweep["tiny"] = tl
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sweep["tiny"]["cpu_baseline"] = cpu_baseline_leg(tcfg, list(range(16)), 3.0, 1, 0.0, "the tiny layer")
+    tiny.close()
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -485,7 +559,6 @@ def run_ours(args):
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
                 "gpu_launches": int(head["launches_per_round"] * args.steps)}
         print(json.dumps(line), flush=True)
-    mv.moe_destroy(handle)
     if world > 1:
         dist.destroy_process_group()
     return 0

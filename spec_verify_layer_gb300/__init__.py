@@ -29,6 +29,7 @@ ABI_SYMBOLS = (
 )
 MOE_NOALLOC_SCRATCH_BYTES = 8 << 20
 KIND_ROUND = 0
+MMA_ROWS = 13  # rounds of at least this many rows run on the tensor cores
 # phase intervals of a profiled moe_round, by the kernel that ran it (the library returns
 # how many it wrote): the split kernel (rows below 8) and the tensor-core kernel
 PHASES_SPLIT = ("finish_router", "barrier1", "routing", "issue", "first_data", "units_before_last",

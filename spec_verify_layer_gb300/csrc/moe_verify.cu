@@ -1503,7 +1503,12 @@ __global__ void __launch_bounds__(NT, 1) k_split(const __grid_constant__ RoundAr
 // parts are added in a fixed order, so a row's result does not depend on the rows it
 // shares the round with.
 
-constexpr int kMmaRows = 8;
+// Rounds of at least this many rows use the tensor-core kernel.  Below it the split
+// kernel measured faster on the 128-expert / top-8 layer with draft rows at sigma 0.5
+// (8 rows: 54 against 64 us per layer, 12 rows: 71 against 78); from 16 rows the tensor
+// cores win (81 against 89 us; 44 against 88 with the near-duplicate copy-span rows,
+// whose experts carry 11 rows each on average).
+constexpr int kMmaRows = 13;
 constexpr int kKPartsGu = 8;  // K parts of a gate/up tile (hidden blocks)
 constexpr int kKPartsDn = 4;  // K parts of a down tile (intermediate blocks)
 static_assert(NW % kKPartsGu == 0 && NW % kKPartsDn == 0, "a tile's K parts run in one round");
