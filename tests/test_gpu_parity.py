@@ -15,9 +15,11 @@ from gpu_helpers import TOL_W, Stack, assert_close, compare, stream_of
 pytestmark = pytest.mark.gpu
 
 SHAPES = ["tiny", "a3b_r1", "e512_r3"]   # distinct layer shapes (a3b_r4 / a3b_r16 share a3b_r1's)
-# (a3b_r1 at 6 rows: more rows than fit staged as operand pairs at hidden 2048, so the
-# CUDA-core path converts the activations from global memory for every unit)
-ROWS = {"tiny": [(1, 0.0), (3, 0.5), (4, 0.5)], "a3b_r1": [(1, 0.0), (4, 0.5), (6, 0.5), (16, 0.1)],
+# Row counts on both kernels: up to 12 rows the split kernel (CUDA cores), from 13 the
+# tensor-core kernel; 5 and 7 rows are the counts just above and below the old staging
+# limit, 12 and 13 the two sides of the kernel switch.
+ROWS = {"tiny": [(1, 0.0), (3, 0.5), (4, 0.5)],
+        "a3b_r1": [(1, 0.0), (4, 0.5), (5, 0.5), (6, 0.5), (7, 0.5), (12, 0.5), (13, 0.5), (16, 0.1)],
         "e512_r3": [(1, 0.0), (1, 1.0), (3, 0.5)]}
 
 

@@ -78,9 +78,11 @@ def test_a3b_shape_matches_oracle(a3b):
     assert_close(got, ref, "a3b prefill T=48")
 
 
-def test_a3b_full_width_sampled(a3b):
-    """2048 tokens (runs of about 128 tokens per expert: full and ragged
-    tiles); sampled tokens against the oracle, and all tokens' counts."""
+def test_a3b_full_width_full_and_ragged_tiles(a3b):
+    """2048 tokens (runs of about 128 tokens per expert).  Every token routed to the
+    busiest expert (its runs fill whole 64-token gate/up and 32-token down tiles) and
+    every token routed to an expert whose run ends in a ragged tile is compared with the
+    oracle element by element; all tokens' counts are exact."""
     cfg = a3b.cfg
     T = 2048
     xb = syngen.rows(cfg, 0, T, 1.0)
@@ -88,13 +90,19 @@ def test_a3b_full_width_sampled(a3b):
     router = syngen.router(cfg, 0)
     rt = oracle.route(router, xb, cfg.top_k)
     np.testing.assert_array_equal(cnt, np.bincount(rt.ids.reshape(-1), minlength=cfg.experts))
-    assert int(cnt.max()) > 128  # several tiles for the busiest experts
     assert np.isfinite(got).all()
-    sample = np.array([0, 1, 63, 64, 1000, T - 1])
-    xs = xb[sample]
+    full = int(np.argmax(cnt))
+    assert cnt[full] >= 128  # two or more full gate/up tiles
+    ragged_cands = [e for e in range(cfg.experts) if cnt[e] % 64 not in (0,) and cnt[e] % 32 != 0 and e != full]
+    ragged = max(ragged_cands, key=lambda e: cnt[e] % 64)
+    picked = np.unique(np.concatenate([np.nonzero((rt.ids == full).any(axis=1))[0],
+                                       np.nonzero((rt.ids == ragged).any(axis=1))[0], [0, T - 1]]))
+    assert picked.size >= cnt[full]
+    xs = xb[picked]
     rs = oracle.route(router, xs, cfg.top_k)
     ref = oracle.layer(router, xs, cfg.top_k, rs.union, syngen.experts_stacked(cfg, 0, rs.union))
-    assert_close(got[sample], ref, "a3b prefill T=2048 (sampled)")
+    assert_close(got[picked], ref, f"a3b prefill T=2048: {picked.size} tokens of experts {full} "
+                                   f"({cnt[full]} picks) and {ragged} ({cnt[ragged]} picks)")
 
 
 def test_tokens_are_independent_bitwise(tiny):

@@ -271,7 +271,6 @@ def test_forced_ties_pick_lower_id():
     assert rt.ids[0, 0] == 2 and rt.ids[0, 1] == 5
     assert rt.logits[0, 2] == rt.logits[0, 5]
     assert rt.w[0, 0] == rt.w[0, 1]
-    pos1, pos6 = list(rt.ids[0]).index(1) if 1 in rt.ids[0] else None, None
     if 1 in rt.ids[0] and 6 in rt.ids[0]:
         assert list(rt.ids[0]).index(1) < list(rt.ids[0]).index(6)
     # all-zero router: every logit is 0, the picks are 0..k-1
@@ -329,9 +328,14 @@ def test_union_and_unique_bytes(tiny4):
     for r in range(xb.shape[0]):
         picked |= set(int(e) for e in rt.ids[r])
     assert rt.union.tolist() == sorted(picked)
-    per_expert = 3 * cfg.hidden * cfg.inter * 18 // 32
-    assert oracle.unique_expert_bytes(cfg.hidden, cfg.inter, len(picked)) == len(picked) * per_expert
-    assert per_expert == cfg.expert_bytes
+    # per-expert packed bytes printed for the workloads (three H x I matrices at 18 B per
+    # 32 weights): 221,184 B for the tiny layer, 2,654,208 B for the 35B-A3B-shaped one,
+    # 1,769,472 B for the 512-expert one
+    assert oracle.unique_expert_bytes(512, 256, 1) == 221_184
+    assert oracle.unique_expert_bytes(2048, 768, 1) == 2_654_208
+    assert oracle.unique_expert_bytes(2048, 512, 1) == 1_769_472
+    assert oracle.unique_expert_bytes(2048, 768, 8) == 21_233_664  # 8 unique experts, one row
+    assert oracle.unique_expert_bytes(cfg.hidden, cfg.inter, len(picked)) == len(picked) * 221_184
 
 
 def test_all_zero_codes_give_zero(tiny4):
@@ -371,8 +375,31 @@ def test_generated_full_size_layer_routes_sanely():
     rt = oracle.route(syngen.router(cfg, 0), syngen.rows(cfg, 0), cfg.top_k)
     assert rt.ids.shape == (4, 8)
     assert cfg.top_k <= rt.union.size <= 32
-    # the fp64 shadow order agrees with the fp32 decision unless the gap is tiny
-    assert (rt.gap64 > 0).all() or (rt.gap64 >= 0).all()
+    assert (rt.gap64 >= 0).all()
+
+
+def test_fp64_shadow_gap_on_known_logits():
+    """The shadow gap is the exact (fp64) difference between the k-th and (k+1)-th
+    largest logit.  A one-hot row x = e_3 makes every logit exactly Wr[e][3]; with the
+    column set to distinct powers of two (and ties) the gaps are known in closed form."""
+    E, H = 8, 128
+    router = np.zeros((E, H), np.float32)
+    router[:, 3] = [0.5, -1.0, 0.25, 2.0, 0.125, 0.25, -0.5, 1.0]   # descending: 2, 1, .5, .25, .25, .125, ...
+    xb = np.zeros((1, H), np.uint16)
+    xb[0, 3] = bf16(1.0)
+    gaps = {1: 2.0 - 1.0, 2: 1.0 - 0.5, 3: 0.5 - 0.25, 4: 0.25 - 0.25, 5: 0.25 - 0.125, 7: -0.5 - (-1.0)}
+    for k, want in gaps.items():
+        rt = oracle.route(router, xb, k)
+        assert rt.gap64[0] == want, (k, rt.gap64[0], want)
+    assert np.isinf(oracle.route(router, xb, E).gap64[0])  # k = E: nothing left out
+    # a gap below fp32 resolution stays visible in fp64: logits 1 + 2^-30 and 1
+    r2 = np.zeros((2, H), np.float32)
+    r2[0, 0], r2[0, 1] = 1.0, 2.0 ** -30
+    r2[1, 0] = 1.0
+    x2 = np.zeros((1, H), np.uint16)
+    x2[0, 0] = x2[0, 1] = bf16(1.0)
+    rt2 = oracle.route(r2, x2, 1)
+    assert rt2.gap64[0] == 2.0 ** -30
 
 
 # ---- routing tail skip (Avalon README, "Numbers": experts that every token of a
