@@ -36,6 +36,12 @@
  *     the call or on its position among them (bitwise).
  *   - Activations must be finite with |x| < 2^40 (and so must the SwiGLU output h);
  *     beyond that range results are undefined.
+ *   - Rounds of fewer than 13 rows add each (expert, 32-element slice of the
+ *     intermediate dimension) contribution to a row's output as round(y * 2^32) into
+ *     64-bit integer accumulators, so the sum is exact and independent of the order of
+ *     the adds; every such contribution and every output must stay below 2^31 in
+ *     magnitude (beyond that results are undefined).  Wider rounds add a row's k expert
+ *     outputs in fp32 in rank order.
  */
 #ifndef MOE_VERIFY_H
 #define MOE_VERIFY_H
@@ -103,11 +109,15 @@ typedef struct moe_handle moe_handle;
 int moe_create(const moe_dims* dims, int device, moe_handle** out);
 void moe_destroy(moe_handle* h);
 
-/* Device workspace (bytes) a call with `rows` rows needs: barrier words, router logits
- * and the fp32 SwiGLU outputs exchanged between CTAs.  0 for invalid dims/rows. */
+/* Device workspace (bytes) a call with `rows` rows needs: barrier words, router logits,
+ * the SwiGLU outputs exchanged between CTAs by the tensor-core path and the output
+ * accumulators of the split path (2 x 8 copies x rows x H int64).  It depends only on
+ * the dimensions and the row count, so it takes the dimensions rather than a handle and
+ * can be sized before any handle exists.  0 for invalid dims/rows. */
 size_t moe_workspace_bytes(const moe_dims* dims, int32_t rows);
 
-/* Packed size of ONE expert: part 0 = code bytes, part 1 = scale bytes.  0 if invalid. */
+/* Packed size of ONE expert: part 0 = code bytes, part 1 = scale bytes (codes and scales
+ * are separate device arrays, so each has its own size).  0 if invalid. */
 size_t moe_packed_bytes(const moe_dims* dims, int which, int part);
 
 /* Host-side packer (HOST buffers).  Packs n_experts consecutive experts:
@@ -119,11 +129,11 @@ size_t moe_packed_bytes(const moe_dims* dims, int which, int part);
  * q + 8, element 2t in the low nibble of byte t of its block):
  *   gate/up codes  [E][I][2: gate, up][H/32 blocks][16 B]   (intermediate row i of an
  *   gate/up scales [E][I][2][H/32]                           expert: gate, then up)
- *   down codes     [E][H][I/32 blocks][16 B]                 (output-row major)
- *   down scales    [E][H][I/32]
- * where, within each row, the code block and the scale of logical block b are stored at
- * position b ^ (key & 7), key = i for the gate and up rows of intermediate index i and
- * key = o for down row o. */
+ *   down codes     [E][I/32 blocks][H rows][16 B]            (block-major: block b of all
+ *   down scales    [E][I/32][H]                               H output rows is one run)
+ * where, within each gate/up row, the code block and the scale of logical block b are
+ * stored at position b ^ (i & 7) (i the row's intermediate index; gate and up alike).
+ * Down block b of output row o is at b * H + o. */
 int moe_pack_q4(const moe_dims* dims, int which, int32_t n_experts, const int8_t* q_a,
                 const uint16_t* s_a, const int8_t* q_b, const uint16_t* s_b, uint8_t* nib_out,
                 uint16_t* scale_out);
@@ -206,12 +216,16 @@ int moe_set_tail_skip(moe_handle* h, int32_t rank);
  * buffer for them); earlier records are discarded.  moe_profile(h, 0) stops.
  * moe_profile_read synchronizes the events and returns the summed device time in ms
  * and the launch count (kind must be 0: the fused round kernel).
- * moe_profile_phases returns, for the last profiled moe_round, the mean over CTAs and
+ * moe_profile_phases writes, for the last profiled moe_round, the mean over CTAs and
  * layers (mean_us) and the per-layer maximum over CTAs averaged over layers (max_us)
- * of twelve phases: router GEMV, barrier 1, routing, wait for the first staged gate/up
- * chunk, gate/up until the last chunk has landed, gate/up after it, barrier 2, wait for
- * the first exchanged h rows, down pass until the last down or h rows have landed, down
- * pass after it, output write, barrier 3.  n_phases >= 12. */
+ * of its phases and returns how many it wrote (or a negative MOE_E* code); n_phases
+ * >= 12 always suffices.  Rounds of fewer than 13 rows (10 phases): router GEMV,
+ * logits barrier (and the previous layer's output written), routing, piece issue, wait
+ * for the first gate/up bytes, units before the last, the last unit's gate/up, its
+ * SwiGLU and the wait for its down bytes, its down products, layer-end barrier.  Wider rounds (12 phases): router GEMV,
+ * barrier 1, routing, wait for the first staged gate/up chunk, gate/up until the last
+ * chunk has landed, gate/up after it, barrier 2, (zero), down pass, (zero), output
+ * write, barrier 3. */
 int moe_profile(moe_handle* h, int enable);
 int moe_profile_read(moe_handle* h, int kind, double* total_ms, int32_t* launches);
 int moe_profile_phases(moe_handle* h, double* mean_us, double* max_us, int32_t n_phases);
@@ -221,15 +235,19 @@ int moe_profile_phases(moe_handle* h, double* mean_us, double* max_us, int32_t n
  * loops, hosts that forbid cudaMalloc after start-up).  There is no counterpart on the
  * pages this layer follows; it is an integration convenience.
  *   - Needs no handle and no workspace: the scratch (barrier words, logits, exchanged
- *     SwiGLU outputs, a status word) is one static device array of MOE_NOALLOC_SCRATCH_BYTES
- *     that every device loading this library holds until the process exits.
+ *     SwiGLU outputs, output accumulators) is one static device array of
+ *     MOE_NOALLOC_SCRATCH_BYTES that every device loading this library holds until the
+ *     process exits.
  *   - Runs on the current device.  Its first call on a device sets that device up
- *     (looks up the array's device address, the SM count, the kernel's shared-memory
- *     limit); make that first call before any stream capture on the device.
- *   - Arguments as for moe_decode_layer.  dev_status, if not NULL, is a caller-owned
- *     device word that receives the timeout bit (1) if a bounded device wait gives up;
- *     the caller clears it.  Returns MOE_EWORKSPACE if the layer needs more scratch than
- *     the array holds (256 + moe_workspace_bytes(dims, rows) > MOE_NOALLOC_SCRATCH_BYTES).
+ *     (looks up the array's device address, the SM count, the kernels' shared-memory
+ *     limits); make that first call before any stream capture on the device.
+ *   - Arguments as for moe_decode_layer, plus dev_status: a caller-owned device word
+ *     (required; NULL gives MOE_EINVAL) into which the kernel ORs what it finds: bit 1
+ *     (value 1) if a bounded device wait gave up (the output is then incomplete), bit 2
+ *     (value 2) if an expert-table entry was outside [0, n_slots) (slot 0 was used
+ *     instead).  The caller clears the word and reads it after the stream has finished.
+ *     Returns MOE_EWORKSPACE if the layer needs more scratch than the array holds
+ *     (moe_workspace_bytes(dims, rows) > MOE_NOALLOC_SCRATCH_BYTES).
  *   - Calls no cudaMalloc, cudaFree or allocating routine.  Every call shares the one
  *     array: calls whose executions overlap on the GPU (different streams, or different
  *     host threads without ordering) race on it and give wrong results. */

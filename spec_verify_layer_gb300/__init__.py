@@ -32,8 +32,8 @@ KIND_ROUND = 0
 MMA_ROWS = 13  # rounds of at least this many rows run on the tensor cores
 # phase intervals of a profiled moe_round, by the kernel that ran it (the library returns
 # how many it wrote): the split kernel (rows below 8) and the tensor-core kernel
-PHASES_SPLIT = ("finish_router", "barrier1", "routing", "issue", "first_data", "units_before_last",
-                "last_gateup", "last_swiglu", "last_down_wait", "last_down", "barrier3")
+PHASES_SPLIT = ("router", "barrier1", "routing", "issue", "first_data", "units_before_last",
+                "last_gateup", "last_swiglu_down_wait", "last_down", "barrier3")
 PHASES_WIDE = ("router", "barrier1", "routing", "first_data", "gateup_stream", "gateup_tail",
                "barrier2", "h_wait", "down", "down_tail", "out_write", "barrier3")
 

@@ -96,12 +96,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 }
 
 
-__device__ __forceinline__ long long gtimer() {
-  long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
@@ -230,7 +224,7 @@ __device__ __forceinline__ bool grid_sync(const RoundArgs& a, Sync& sy) {
 
 __device__ __forceinline__ void stamp(const RoundArgs& a, int l, int ph) {
   if (a.phase_ts && threadIdx.x == 0)
-    a.phase_ts[((size_t)l * kPhases + ph) * gridDim.x + blockIdx.x] = gtimer();
+    a.phase_ts[((size_t)l * kPhases + ph) * gridDim.x + blockIdx.x] = clock64();
 }
 
 // ---------------------------------------------------------------------------------
@@ -868,16 +862,17 @@ __device__ __forceinline__ float warp_sum_multi(float (&v)[V], int lane) {
 
 // Leaving early: gives every copy still in flight a bounded chance to land (so no bulk
 // copy targets shared memory of an exited CTA) and raises the abort flag.  Copies in
-// flight are the slots of pieces [j0, j1) of a ring of `nslot` slots (slot j % nslot,
-// parity (j / nslot) & 1), the router rows, and any extra single-use barriers.  Out of
-// line: it never runs on the normal path.
-__device__ __noinline__ void drain_and_abort(const RoundArgs& a, const uint64_t* bars, int nslot, long long j0,
-                                             long long j1, bool router_pend, uint32_t bar_router,
+// flight are the pieces [k0, k1) of the current layer in a ring of `nslot` slots (piece
+// k in slot (slot0 + k) % nslot, parity par0 ^ ((slot0 + k) / nslot & 1)) and the router
+// rows.  Out of line: it never runs on the normal path.
+__device__ __noinline__ void drain_and_abort(const RoundArgs& a, const uint64_t* bars, int nslot, unsigned slot0,
+                                             unsigned par0, int k0, int k1, bool router_pend, uint32_t bar_router,
                                              unsigned ph_router) {
   if (threadIdx.x == 0) {
-    for (long long j = j0; j < j1; ++j) {
-      const int q = (int)(j % nslot);
-      mbar_wait_bounded(smem_u32(bars + q), (unsigned)((j / nslot) & 1), a.status, kDefaultWaitCycles);
+    for (int k = k0; k < k1; ++k) {
+      const unsigned pos = slot0 + (unsigned)k;
+      mbar_wait_bounded(smem_u32(bars + pos % (unsigned)nslot), par0 ^ ((pos / (unsigned)nslot) & 1u), a.status,
+                        kDefaultWaitCycles);
     }
     if (router_pend) mbar_wait_bounded(bar_router, ph_router, a.status, kDefaultWaitCycles);
     atomicExch(a.bar + 33, 1u);
@@ -916,7 +911,7 @@ constexpr int kSplitMaxSlots = 6;  // more slots measured slower (the ring crowd
 constexpr int kGuPieces = 4;  // gate/up pieces per unit (8 intermediate indices each)
 constexpr int kDnPieces = 2;  // down pieces per unit (H/2 output rows each)
 constexpr int kPieces = kGuPieces + kDnPieces;
-constexpr int kSplitPhases = 12;  // phase stamps per layer when profiling the split kernel
+constexpr int kSplitPhases = 11;  // phase stamps per layer when profiling the split kernel
 
 struct SplitPlan {
   size_t slot_bytes, ring, router, xd, xk, part, hd, uni, csr, pair, w, pos_ui, pos_row, slot, pick, nunion, misc,
@@ -1059,21 +1054,19 @@ __device__ __forceinline__ void split_gateup(const RoundArgs& a, const Tables& T
   const int b = 32 * kg + lane;
   const bool valid = b < NB;
   const int row0 = rb * RPW;
-  if (XR) {
-    // all of the warp's rows in one pass: one reduction, RPW independent block dots
+  // all of the warp's rows in one pass per activation row: one reduction, RPW
+  // independent block dots
+  if constexpr (XR) {
     float v[1][RPW];
     split_gu_rows<RPW, 1>(piece, a.H, row0 & 15, b, valid, &xr, v);
     split_store_part<RPW>(v[0], lane, s_part, row0, NG, kg, a.R, 0);
-    return;
-  }
-  for (int pr = 0; pr < Re; ++pr) {
-    Op16 xo[1];
-    if (valid) load_xop<XS>(a, x, s_xd, s_xk, T.pos_row[p0 + pr], b, xo[0]);
-#pragma unroll 1
-    for (int h = 0; h < RPW; h += 4) {
-      float v[1][4];
-      split_gu_rows<4, 1>(piece, a.H, (row0 + h) & 15, b, valid, xo, v);
-      split_store_part<4>(v[0], lane, s_part, row0 + h, NG, kg, a.R, pr);
+  } else {
+    for (int pr = 0; pr < Re; ++pr) {
+      Op16 xo[1];
+      if (valid) load_xop<XS>(a, x, s_xd, s_xk, T.pos_row[p0 + pr], b, xo[0]);
+      float v[1][RPW];
+      split_gu_rows<RPW, 1>(piece, a.H, row0 & 15, b, valid, xo, v);
+      split_store_part<RPW>(v[0], lane, s_part, row0, NG, kg, a.R, pr);
     }
   }
 }
@@ -1230,25 +1223,24 @@ __device__ __forceinline__ void split_finish(const RoundArgs& a, int layer, int 
 
 __device__ __forceinline__ void split_stamp(const RoundArgs& a, int l, int ph) {
   if (a.phase_ts && threadIdx.x == 0)
-    a.phase_ts[((size_t)l * kSplitPhases + ph) * gridDim.x + blockIdx.x] = gtimer();
+    a.phase_ts[((size_t)l * kSplitPhases + ph) * gridDim.x + blockIdx.x] = clock64();
 }
 
-// The units [u_beg, u_end) of layer l (pieces [jbase, jbase + 6 (u_end - u_beg)) of this
-// CTA's ring sequence, the first n_init already issued); false (after draining) if a wait
-// gave up.  Inlined: a call would save and restore the kernel's live registers through
+// The units [u_beg, u_end) of layer l (its pieces 0 .. 6 (u_end - u_beg) - 1, piece k in
+// ring slot (slot0 + k) % nslot with parity par0 ^ ((slot0 + k) / nslot & 1), the first
+// n_init already issued); false (after draining) if a wait gave up.  Inlined: a call would save and restore the kernel's live registers through
 // local memory, which the large shared-memory carve-out leaves little L1 for.
 template <int NG, bool XR, bool XS>
-__device__ __forceinline__ bool split_units(const RoundArgs& a, int l, unsigned char* smem, long long jbase, int u_beg,
+__device__ __forceinline__ bool split_units(const RoundArgs& a, int l, unsigned char* smem, unsigned slot0,
+                                            unsigned par0, int u_beg,
                                          int u_end, int n_init, bool router_pend, uint32_t bar_router,
                                          unsigned ph_router) {
   const int tid = threadIdx.x, warp = tid >> 5;
   const int H = a.H, NS = a.I >> 5;
   const SplitPlan& P = g_splan;
   const int nslot = P.nslot;
-  // ring position of this layer's first piece; piece jbase + j sits in slot (s0 + j) % nslot
-  const unsigned s0 = (unsigned)(jbase % nslot), par0 = (unsigned)((jbase / nslot) & 1);
-  auto slot_of = [&](long long J) { return (int)((s0 + (unsigned)(J - jbase)) % (unsigned)nslot); };
-  auto par_of = [&](long long J) { return (par0 + (s0 + (unsigned)(J - jbase)) / (unsigned)nslot) & 1u; };
+  auto slot_of = [&](int k) { return (int)((slot0 + (unsigned)k) % (unsigned)nslot); };
+  auto par_of = [&](int k) { return par0 ^ (((slot0 + (unsigned)k) / (unsigned)nslot) & 1u); };
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P.bars);
   uint8_t* ring = smem + P.ring;
   const uint4* s_xd = reinterpret_cast<const uint4*>(smem + P.xd);
@@ -1266,7 +1258,7 @@ __device__ __forceinline__ bool split_units(const RoundArgs& a, int l, unsigned 
   unsigned long long* acc_copy = a.acc + ((size_t)(l & 1) * kSplitCopies + blockIdx.x % kSplitCopies) * a.R * H;
   const int nu = u_end - u_beg, npieces = nu * kPieces;
   int issued = n_init;  // pieces of this layer issued so far (thread 0's count, uniform)
-  long long consumed = jbase;
+  int consumed = 0;
   const int rb = warp / NG, kg = warp % NG;
   const int my_piece = (rb * 4 * NG) >> 4;  // the gate/up piece holding this warp's rows
   bool stamped = false;
@@ -1276,7 +1268,7 @@ __device__ __forceinline__ bool split_units(const RoundArgs& a, int l, unsigned 
     if (t + 1 == nu && t > 0) split_stamp(a, l, 6);
     // ---- gate/up: each warp waits for its own piece ----
     {
-      const long long J = jbase + (long long)t * kPieces + my_piece;
+      const int J = t * kPieces + my_piece;
       bool ok = mbar_wait_bounded(smem_u32(bars + slot_of(J)), par_of(J), a.status, a.wait_cycles);
       if (ok) {
         if (!stamped && warp == 0) {
@@ -1291,16 +1283,16 @@ __device__ __forceinline__ bool split_units(const RoundArgs& a, int l, unsigned 
                                     s_part);
       }
       if (__syncthreads_or(!ok)) {
-        drain_and_abort(a, bars, nslot, consumed, jbase + issued, router_pend, bar_router, ph_router);
+        drain_and_abort(a, bars, nslot, slot0, par0, consumed, issued, router_pend, bar_router, ph_router);
         return false;
       }
     }
     if (t + 1 == nu) split_stamp(a, l, 7);
-    consumed = jbase + (long long)t * kPieces + kGuPieces;
+    consumed = t * kPieces + kGuPieces;
     if (tid < kGuPieces) {
       const int j = t * kPieces + tid + nslot;
       if (j < npieces) {
-        const long long J = jbase + j;
+        const int J = j;
         issue_piece(a, W, T, NS, u_beg, j, ring + (size_t)slot_of(J) * P.slot_bytes, smem_u32(bars + slot_of(J)));
       }
     }
@@ -1309,34 +1301,31 @@ __device__ __forceinline__ bool split_units(const RoundArgs& a, int l, unsigned 
     // while the SwiGLU warps work
     DnRows dr;
     {
-      const long long J0 = jbase + (long long)t * kPieces + kGuPieces, J1 = J0 + 1;
+      const int J0 = t * kPieces + kGuPieces, J1 = J0 + 1;
       split_swiglu(a, T, s_part, NG, p0, Re, s_hd);  // (warps below Re; the others go on)
       const bool ok = mbar_wait_bounded(smem_u32(bars + slot_of(J0)), par_of(J0), a.status, a.wait_cycles) &&
                       mbar_wait_bounded(smem_u32(bars + slot_of(J1)), par_of(J1), a.status, a.wait_cycles);
       if (ok) load_dn_rows(H, ring + (size_t)slot_of(J0) * P.slot_bytes, ring + (size_t)slot_of(J1) * P.slot_bytes, dr);
       if (__syncthreads_or(!ok)) {
-        drain_and_abort(a, bars, nslot, consumed, jbase + issued, router_pend, bar_router, ph_router);
+        drain_and_abort(a, bars, nslot, slot0, par0, consumed, issued, router_pend, bar_router, ph_router);
         return false;
       }
     }
-    if (t + 1 == nu) {
-      split_stamp(a, l, 8);
-      split_stamp(a, l, 9);
-    }
+    if (t + 1 == nu) split_stamp(a, l, 8);
     split_down(a, T, dr, s_hd, p0, Re, acc_copy);
     __syncthreads();
-    consumed = jbase + (long long)(t + 1) * kPieces;
+    consumed = (t + 1) * kPieces;
     if (tid < kDnPieces) {
       const int j = t * kPieces + kGuPieces + tid + nslot;
       if (j < npieces) {
-        const long long J = jbase + j;
+        const int J = j;
         issue_piece(a, W, T, NS, u_beg, j, ring + (size_t)slot_of(J) * P.slot_bytes, smem_u32(bars + slot_of(J)));
       }
     }
     issued = min(npieces, max(issued, (t + 1) * kPieces + nslot));
   }
   if (nu == 0)
-    for (int ph = 5; ph <= 9; ++ph) split_stamp(a, l, ph);
+    for (int ph = 5; ph <= 8; ++ph) split_stamp(a, l, ph);
   return true;
 }
 
@@ -1390,8 +1379,8 @@ __global__ void __launch_bounds__(NT, 1) k_split(const __grid_constant__ RoundAr
   const bool has_rows = router_rows_of_cta(a.E) > 0;
   bool router_pend = has_rows;  // layer 0's rows are in flight
   Sync sy;
-  long long jbase = 0;  // pieces issued by this CTA in earlier layers (ring position)
-  auto slot_of = [&](long long J) { return (int)(J % nslot); };
+  // ring position of the next layer's first piece: slot and the parity of that slot's use
+  unsigned slot0 = 0u, par0 = 0u;
   for (int l = 0; l < a.L; ++l) {
     const LayerPtrs& W = a.layer[l];
     const uint16_t* x = a.x + (size_t)l * a.R * H;
@@ -1403,7 +1392,7 @@ __global__ void __launch_bounds__(NT, 1) k_split(const __grid_constant__ RoundAr
     if (router_pend) {
       const bool ok = mbar_wait_bounded(bar_router, ph_router, a.status, a.wait_cycles);
       if (__syncthreads_or(!ok)) {
-        drain_and_abort(a, bars, nslot, 0, 0, true, bar_router, ph_router);
+        drain_and_abort(a, bars, nslot, 0u, 0u, 0, 0, true, bar_router, ph_router);
         return;
       }
       ph_router ^= 1u;
@@ -1434,7 +1423,7 @@ __global__ void __launch_bounds__(NT, 1) k_split(const __grid_constant__ RoundAr
     // and is in (its closing barrier is behind us)
     if (l > 0 && !a.route_only) split_finish(a, l - 1, o0, no, fin0);
     if (!grid_wait(a, sy)) {
-      drain_and_abort(a, bars, nslot, 0, 0, router_pend, bar_router, ph_router);
+      drain_and_abort(a, bars, nslot, 0u, 0u, 0, 0, router_pend, bar_router, ph_router);
       return;
     }
     split_stamp(a, l, 2);
@@ -1451,20 +1440,25 @@ __global__ void __launch_bounds__(NT, 1) k_split(const __grid_constant__ RoundAr
     const int n_init = min(nslot, npieces);
     // one issuing thread per piece
     if (tid < n_init) {
-      const long long J = jbase + tid;
-      issue_piece(a, W, T, NS, u_beg, tid, ring + (size_t)slot_of(J) * P.slot_bytes, smem_u32(bars + slot_of(J)));
+      const int q = (int)((slot0 + (unsigned)tid) % (unsigned)nslot);
+      issue_piece(a, W, T, NS, u_beg, tid, ring + (size_t)q * P.slot_bytes, smem_u32(bars + q));
     }
     if (one && warp == 1) softmax_one(a, T);
     split_stamp(a, l, 4);
     __syncthreads();
-    if (!split_units<NG, XR, XS>(a, l, smem, jbase, u_beg, u_end, n_init, router_pend, bar_router, ph_router)) return;
-    jbase += npieces;
-    split_stamp(a, l, 10);
+    if (!split_units<NG, XR, XS>(a, l, smem, slot0, par0, u_beg, u_end, n_init, router_pend, bar_router, ph_router))
+      return;
+    {
+      const unsigned end = slot0 + (unsigned)npieces;
+      par0 ^= (end / (unsigned)nslot) & 1u;
+      slot0 = end % (unsigned)nslot;
+    }
+    split_stamp(a, l, 9);
     if (!grid_sync(a, sy)) {  // B3: every add of this layer is in
-      drain_and_abort(a, bars, nslot, 0, 0, router_pend, bar_router, ph_router);
+      drain_and_abort(a, bars, nslot, 0u, 0u, 0, 0, router_pend, bar_router, ph_router);
       return;
     }
-    split_stamp(a, l, 11);
+    split_stamp(a, l, 10);
   }
   split_finish(a, a.L - 1, o0, no, fin0);
 }
@@ -1834,7 +1828,7 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
       for (int q = 0; q < kGuSlots; ++q)
         if (gu_pend & (1u << q)) mbar_wait_bounded(smem_u32(bars + q), (gu_ph >> q) & 1u, a.status, kDefaultWaitCycles);
     }
-    drain_and_abort(a, bars, 1, 0, 0, router_pend, bar_router, ph_router);
+    drain_and_abort(a, bars, 1, 0u, 0u, 0, 0, router_pend, bar_router, ph_router);
   };
   for (int l = 0; l < a.L; ++l) {
     const LayerPtrs& W = a.layer[l];
@@ -2505,6 +2499,11 @@ int moe_profile_phases(moe_handle* h, double* mean_us, double* max_us, int32_t n
   DeviceGuard g(h->device);
   if (!g.ok) return MOE_ECUDA;
   const int G = h->sm_count, L = h->phase_layers;
+  // the stamps are SM cycle counts (differences within one CTA); cycles -> us at the
+  // SM clock the device reports
+  int khz = 0;
+  if (cudaDeviceGetAttribute(&khz, cudaDevAttrClockRate, h->device) != cudaSuccess || khz <= 0) return MOE_ECUDA;
+  const double us_per_cycle = 1e3 / (double)khz;
   std::vector<long long> ts((size_t)L * stamps * G);
   if (cudaDeviceSynchronize() != cudaSuccess ||
       cudaMemcpy(ts.data(), h->phase_ts, ts.size() * sizeof(long long), cudaMemcpyDeviceToHost) !=
@@ -2516,7 +2515,7 @@ int moe_profile_phases(moe_handle* h, double* mean_us, double* max_us, int32_t n
       double lmax = 0.0;
       for (int c = 0; c < G; ++c) {
         const double d = (double)(ts[((size_t)l * stamps + p + 1) * G + c] -
-                                  ts[((size_t)l * stamps + p) * G + c]) * 1e-3;
+                                  ts[((size_t)l * stamps + p) * G + c]) * us_per_cycle;
         sum += d;
         if (d > lmax) lmax = d;
       }
