@@ -914,8 +914,8 @@ constexpr int kPieces = kGuPieces + kDnPieces;
 constexpr int kSplitPhases = 11;  // phase stamps per layer when profiling the split kernel
 
 struct SplitPlan {
-  size_t slot_bytes, ring, router, xd, xk, part, hd, uni, csr, pair, w, pos_ui, pos_row, slot, pick, nunion, misc,
-      bars, total;
+  size_t slot_bytes, ring, router, xd, xk, part, hd, uni, csr, pair, w, pos_ui, pos_row, slot, pick, order, nunion,
+      misc, bars, total;
   int nslot, ng;
   bool x_staged, ok;
 };
@@ -934,7 +934,7 @@ __host__ __device__ inline SplitPlan split_plan(int H, int I, int E, int R, int 
   const size_t part = up128((size_t)64 * p.ng * R * 4);
   const size_t hd = up128((size_t)R * 28 * 4);
   const size_t tables = up128((size_t)E * 4) + up128((size_t)(E + 1) * 4) + 5 * up128(rk * 4) +
-                        up128((size_t)E * 4) + 128;
+                        2 * up128((size_t)E * 4) + 128;
   const size_t misc = 256, bars = 256;
   const size_t limit = (size_t)225 * 1024;
   size_t fixed = router + part + hd + tables + misc + bars;
@@ -959,6 +959,7 @@ __host__ __device__ inline SplitPlan split_plan(int H, int I, int E, int R, int 
   p.pos_row = off; off += up128(rk * 4);
   p.slot = off;    off += up128((size_t)E * 4);
   p.pick = off;    off += up128(rk * 4);
+  p.order = off;   off += up128((size_t)E * 4);
   p.nunion = off;  off += 128;
   p.misc = off;    off += misc;
   p.bars = off;    off += bars;
@@ -973,11 +974,29 @@ __host__ __device__ inline SplitPlan split_plan(int H, int I, int E, int R, int 
 // The split kernel's plan, in shared memory (written once per launch by thread 0).
 __shared__ SplitPlan g_splan;
 
-// Piece j of this CTA's units (unit u0 + j / kPieces, piece j % kPieces) -> ring slot.
-__device__ __forceinline__ void issue_piece(const RoundArgs& a, const LayerPtrs& W, const Tables& T, int NS, int u0,
-                                            int j, uint8_t* dst, uint32_t bar) {
+// Unit t of this CTA.  The union's units, heaviest first (experts by row count
+// descending, then by union index, each expert's slices in order: s_order lists the
+// union indices in that order), are dealt out to the CTAs in snake order: round r gives
+// one unit to every CTA, forward for even r and backward for odd r, so each CTA's load
+// stays within about one light unit of the others' (a contiguous cut by work can put a
+// whole heavy unit more on one CTA).  A unit is u = union index * NS + slice.
+__device__ __forceinline__ int split_unit_of(int t, int NS, const int* s_order) {
+  const int G = gridDim.x, c = blockIdx.x;
+  const int p = t * G + ((t & 1) ? G - 1 - c : c);
+  const int q = p / NS;
+  return s_order[q] * NS + (p - q * NS);
+}
+
+// How many of the N units the deal gives this CTA.
+__device__ __forceinline__ int split_unit_count(int N) {
+  const int G = gridDim.x, c = blockIdx.x, full = N / G;
+  return full + (((full & 1) ? G - 1 - c : c) < N - full * G ? 1 : 0);
+}
+
+// Piece pc of unit u -> ring slot dst (its completion counted on bar).
+__device__ __forceinline__ void issue_piece(const RoundArgs& a, const LayerPtrs& W, const Tables& T, int NS, int u,
+                                            int pc, uint8_t* dst, uint32_t bar, bool fence = true) {
   const size_t H = (size_t)a.H;
-  const int u = u0 + j / kPieces, pc = j - (j / kPieces) * kPieces;
   const int ui = u / NS, s = u - ui * NS;
   const size_t sl = (size_t)T.slot[T.uni[ui]];
   const uint8_t* src_c;
@@ -991,7 +1010,7 @@ __device__ __forceinline__ void issue_piece(const RoundArgs& a, const LayerPtrs&
     src_c = W.dn_nib + row0 * 16;
     src_s = reinterpret_cast<const uint8_t*>(W.dn_sc) + row0 * 2;
   }
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  if (fence) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   mbar_expect_tx(bar, (uint32_t)(9 * H));
   bulk_g2s(smem_u32(dst), src_c, (uint32_t)(8 * H), bar);
   bulk_g2s(smem_u32(dst + 8 * H), src_s, (uint32_t)H, bar);
@@ -1226,15 +1245,15 @@ __device__ __forceinline__ void split_stamp(const RoundArgs& a, int l, int ph) {
     a.phase_ts[((size_t)l * kSplitPhases + ph) * gridDim.x + blockIdx.x] = clock64();
 }
 
-// The units [u_beg, u_end) of layer l (its pieces 0 .. 6 (u_end - u_beg) - 1, piece k in
+// This CTA's nu units of layer l (split_unit_of; their pieces 0 .. 6 nu - 1, piece k in
 // ring slot (slot0 + k) % nslot with parity par0 ^ ((slot0 + k) / nslot & 1), the first
-// n_init already issued); false (after draining) if a wait gave up.  Inlined: a call would save and restore the kernel's live registers through
-// local memory, which the large shared-memory carve-out leaves little L1 for.
+// n_init already issued); false (after draining) if a wait gave up.  Inlined: a call
+// would save and restore the kernel's live registers through local memory, which the
+// large shared-memory carve-out leaves little L1 for.
 template <int NG, bool XR, bool XS>
 __device__ __forceinline__ bool split_units(const RoundArgs& a, int l, unsigned char* smem, unsigned slot0,
-                                            unsigned par0, int u_beg,
-                                         int u_end, int n_init, bool router_pend, uint32_t bar_router,
-                                         unsigned ph_router) {
+                                            unsigned par0, int nu, int n_init, bool router_pend, uint32_t bar_router,
+                                            unsigned ph_router) {
   const int tid = threadIdx.x, warp = tid >> 5;
   const int H = a.H, NS = a.I >> 5;
   const SplitPlan& P = g_splan;
@@ -1252,18 +1271,19 @@ __device__ __forceinline__ bool split_units(const RoundArgs& a, int l, unsigned 
                  reinterpret_cast<int*>(smem + P.nunion),  reinterpret_cast<int*>(smem + P.pos_ui),
                  reinterpret_cast<int*>(smem + P.pos_row), reinterpret_cast<int*>(smem + P.slot),
                  reinterpret_cast<int*>(smem + P.pick)};
+  const int* s_order = reinterpret_cast<const int*>(smem + P.order);
   const LayerPtrs& W = a.layer[l];
   const uint16_t* x = a.x + (size_t)l * a.R * H;
   // layer l adds into accumulator buffer l & 1, copy blockIdx % kSplitCopies
   unsigned long long* acc_copy = a.acc + ((size_t)(l & 1) * kSplitCopies + blockIdx.x % kSplitCopies) * a.R * H;
-  const int nu = u_end - u_beg, npieces = nu * kPieces;
+  const int npieces = nu * kPieces;
   int issued = n_init;  // pieces of this layer issued so far (thread 0's count, uniform)
   int consumed = 0;
   const int rb = warp / NG, kg = warp % NG;
   const int my_piece = (rb * 4 * NG) >> 4;  // the gate/up piece holding this warp's rows
   bool stamped = false;
   for (int t = 0; t < nu; ++t) {
-    const int u = u_beg + t, ui = u / NS;
+    const int ui = split_unit_of(t, NS, s_order) / NS;
     const int p0 = T.csr_off[ui], Re = T.csr_off[ui + 1] - p0;
     if (t + 1 == nu && t > 0) split_stamp(a, l, 6);
     // ---- gate/up: each warp waits for its own piece ----
@@ -1289,12 +1309,11 @@ __device__ __forceinline__ bool split_units(const RoundArgs& a, int l, unsigned 
     }
     if (t + 1 == nu) split_stamp(a, l, 7);
     consumed = t * kPieces + kGuPieces;
-    if (tid < kGuPieces) {
-      const int j = t * kPieces + tid + nslot;
-      if (j < npieces) {
-        const int J = j;
-        issue_piece(a, W, T, NS, u_beg, j, ring + (size_t)slot_of(J) * P.slot_bytes, smem_u32(bars + slot_of(J)));
-      }
+    if ((tid & 31) == 0 && warp >= NW - kGuPieces) {
+      const int j = t * kPieces + (warp - (NW - kGuPieces)) + nslot, tj = j / kPieces;
+      if (j < npieces)
+        issue_piece(a, W, T, NS, split_unit_of(tj, NS, s_order), j - tj * kPieces,
+                    ring + (size_t)slot_of(j) * P.slot_bytes, smem_u32(bars + slot_of(j)), false);
     }
     issued = min(npieces, max(issued, t * kPieces + kGuPieces + nslot));
     // the down pieces (usually landed by now) are waited and this thread's rows loaded
@@ -1315,12 +1334,11 @@ __device__ __forceinline__ bool split_units(const RoundArgs& a, int l, unsigned 
     split_down(a, T, dr, s_hd, p0, Re, acc_copy);
     __syncthreads();
     consumed = (t + 1) * kPieces;
-    if (tid < kDnPieces) {
-      const int j = t * kPieces + kGuPieces + tid + nslot;
-      if (j < npieces) {
-        const int J = j;
-        issue_piece(a, W, T, NS, u_beg, j, ring + (size_t)slot_of(J) * P.slot_bytes, smem_u32(bars + slot_of(J)));
-      }
+    if ((tid & 31) == 0 && warp >= NW - kDnPieces) {
+      const int j = t * kPieces + kGuPieces + (warp - (NW - kDnPieces)) + nslot, tj = j / kPieces;
+      if (j < npieces)
+        issue_piece(a, W, T, NS, split_unit_of(tj, NS, s_order), j - tj * kPieces,
+                    ring + (size_t)slot_of(j) * P.slot_bytes, smem_u32(bars + slot_of(j)), false);
     }
     issued = min(npieces, max(issued, (t + 1) * kPieces + nslot));
   }
@@ -1433,20 +1451,35 @@ __global__ void __launch_bounds__(NT, 1) k_split(const __grid_constant__ RoundAr
       if (one && warp == 1) softmax_one(a, T);
       return;
     }
-    (void)U;
+    // the union's experts by row count descending, then union index (one row: as is)
+    int* s_order = reinterpret_cast<int*>(smem + P.order);
+    for (int ui = tid; ui < U; ui += NT) {
+      int rank = ui;
+      if (a.R > 1) {
+        const int re = T.csr_off[ui + 1] - T.csr_off[ui];
+        rank = 0;
+        for (int uj = 0; uj < U; ++uj) {
+          const int rj = T.csr_off[uj + 1] - T.csr_off[uj];
+          rank += (rj > re || (rj == re && uj < ui)) ? 1 : 0;
+        }
+      }
+      s_order[rank] = ui;
+    }
+    __syncthreads();
     split_stamp(a, l, 3);
-    const int u_beg = s_range[0], u_end = s_range[1];
-    const int nu = u_end - u_beg, npieces = nu * kPieces;
+    const int nu = split_unit_count(U * NS), npieces = nu * kPieces;
     const int n_init = min(nslot, npieces);
-    // one issuing thread per piece
-    if (tid < n_init) {
-      const int q = (int)((slot0 + (unsigned)tid) % (unsigned)nslot);
-      issue_piece(a, W, T, NS, u_beg, tid, ring + (size_t)q * P.slot_bytes, smem_u32(bars + q));
+    // lane 0 of one warp per piece (a warp's lanes would issue their copies one after
+    // another); the refills inside the unit loop likewise come from the last warps
+    if ((tid & 31) == 0 && warp < n_init) {
+      const int q = (int)((slot0 + (unsigned)warp) % (unsigned)nslot), tj = warp / kPieces;
+      issue_piece(a, W, T, NS, split_unit_of(tj, NS, s_order), warp - tj * kPieces, ring + (size_t)q * P.slot_bytes,
+                  smem_u32(bars + q));
     }
     if (one && warp == 1) softmax_one(a, T);
     split_stamp(a, l, 4);
     __syncthreads();
-    if (!split_units<NG, XR, XS>(a, l, smem, slot0, par0, u_beg, u_end, n_init, router_pend, bar_router, ph_router))
+    if (!split_units<NG, XR, XS>(a, l, smem, slot0, par0, nu, n_init, router_pend, bar_router, ph_router))
       return;
     {
       const unsigned end = slot0 + (unsigned)npieces;
