@@ -688,6 +688,14 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
 }
 
 // Codes of one block as even / odd nibble bytes.
+// round(v) for |v| < 2^22 on the FMA and integer pipes (the conversion instructions run
+// on a slower shared pipe): adding 1.5 * 2^23, whose ulp is 1, rounds v to the nearest
+// integer (ties to even, as __float2int_rn) into the low mantissa bits.  With v = x s
+// for a power of two s, the fma rounds the exact product once: round(x s).
+__device__ __forceinline__ int rint_small(float x, float s) {
+  return __float_as_int(__fmaf_rn(x, s, 12582912.f)) - 0x4B400000;
+}
+
 struct NibBytes {
   uint32_t lo[4], hi[4];
 };
@@ -774,7 +782,7 @@ __device__ __forceinline__ void x_block_to_op16(const uint4 (&u)[4], Op16& op) {
 #pragma unroll
   for (int e = 0; e < 32; ++e) {
     const float xv = (e & 1) ? bf16_hi(v[e >> 1]) : bf16_lo(v[e >> 1]);
-    const int X = __float2int_rn(xv * scale);
+    const int X = rint_small(xv, scale);
     const int d0 = X & 0xFF, d1 = X >> 8;
     s0 += d0;
     s1 += d1;
@@ -976,15 +984,16 @@ __shared__ SplitPlan g_splan;
 
 // Unit t of this CTA.  The union's units, heaviest first (experts by row count
 // descending, then by union index, each expert's slices in order: s_order lists the
-// union indices in that order), are dealt out to the CTAs in snake order: round r gives
+// union indices in that order; with one row every expert weighs the same and the order
+// is the union's), are dealt out to the CTAs in snake order: round r gives
 // one unit to every CTA, forward for even r and backward for odd r, so each CTA's load
 // stays within about one light unit of the others' (a contiguous cut by work can put a
 // whole heavy unit more on one CTA).  A unit is u = union index * NS + slice.
-__device__ __forceinline__ int split_unit_of(int t, int NS, const int* s_order) {
+__device__ __forceinline__ int split_unit_of(int t, int NS, const int* s_order, int R) {
   const int G = gridDim.x, c = blockIdx.x;
   const int p = t * G + ((t & 1) ? G - 1 - c : c);
   const int q = p / NS;
-  return s_order[q] * NS + (p - q * NS);
+  return (R > 1 ? s_order[q] : q) * NS + (p - q * NS);
 }
 
 // How many of the N units the deal gives this CTA.
@@ -1137,7 +1146,7 @@ __device__ __forceinline__ void split_swiglu(const RoundArgs& a, const Tables& T
     const unsigned mx = __reduce_max_sync(0xffffffffu, __float_as_uint(hw) & 0x7FFFFFFFu);
     const int E = max((int)(mx >> 23), 22);
     const float scale = __int_as_float((275 - E) << 23);  // 2^(148 - E)
-    const int Hq = __float2int_rn(__fmul_rn(hw, scale));
+    const int Hq = rint_small(hw, scale);
     const int d0 = Hq & 0xFF, d1 = (Hq >> 8) & 0xFF, d2 = Hq >> 16;
     uint8_t* row = reinterpret_cast<uint8_t*>(s_hd + pr * 28);
     const int j = (lane & 7) >> 1;
@@ -1283,7 +1292,7 @@ __device__ __forceinline__ bool split_units(const RoundArgs& a, int l, unsigned 
   const int my_piece = (rb * 4 * NG) >> 4;  // the gate/up piece holding this warp's rows
   bool stamped = false;
   for (int t = 0; t < nu; ++t) {
-    const int ui = split_unit_of(t, NS, s_order) / NS;
+    const int ui = split_unit_of(t, NS, s_order, a.R) / NS;
     const int p0 = T.csr_off[ui], Re = T.csr_off[ui + 1] - p0;
     if (t + 1 == nu && t > 0) split_stamp(a, l, 6);
     // ---- gate/up: each warp waits for its own piece ----
@@ -1312,7 +1321,7 @@ __device__ __forceinline__ bool split_units(const RoundArgs& a, int l, unsigned 
     if ((tid & 31) == 0 && warp >= NW - kGuPieces) {
       const int j = t * kPieces + (warp - (NW - kGuPieces)) + nslot, tj = j / kPieces;
       if (j < npieces)
-        issue_piece(a, W, T, NS, split_unit_of(tj, NS, s_order), j - tj * kPieces,
+        issue_piece(a, W, T, NS, split_unit_of(tj, NS, s_order, a.R), j - tj * kPieces,
                     ring + (size_t)slot_of(j) * P.slot_bytes, smem_u32(bars + slot_of(j)), false);
     }
     issued = min(npieces, max(issued, t * kPieces + kGuPieces + nslot));
@@ -1337,7 +1346,7 @@ __device__ __forceinline__ bool split_units(const RoundArgs& a, int l, unsigned 
     if ((tid & 31) == 0 && warp >= NW - kDnPieces) {
       const int j = t * kPieces + kGuPieces + (warp - (NW - kDnPieces)) + nslot, tj = j / kPieces;
       if (j < npieces)
-        issue_piece(a, W, T, NS, split_unit_of(tj, NS, s_order), j - tj * kPieces,
+        issue_piece(a, W, T, NS, split_unit_of(tj, NS, s_order, a.R), j - tj * kPieces,
                     ring + (size_t)slot_of(j) * P.slot_bytes, smem_u32(bars + slot_of(j)), false);
     }
     issued = min(npieces, max(issued, (t + 1) * kPieces + nslot));
@@ -1451,21 +1460,21 @@ __global__ void __launch_bounds__(NT, 1) k_split(const __grid_constant__ RoundAr
       if (one && warp == 1) softmax_one(a, T);
       return;
     }
-    // the union's experts by row count descending, then union index (one row: as is)
+    // the union's experts by row count descending, then union index (one row: all
+    // weigh the same and the union's order is used as is)
     int* s_order = reinterpret_cast<int*>(smem + P.order);
-    for (int ui = tid; ui < U; ui += NT) {
-      int rank = ui;
-      if (a.R > 1) {
+    if (a.R > 1) {
+      for (int ui = tid; ui < U; ui += NT) {
         const int re = T.csr_off[ui + 1] - T.csr_off[ui];
-        rank = 0;
+        int rank = 0;
         for (int uj = 0; uj < U; ++uj) {
           const int rj = T.csr_off[uj + 1] - T.csr_off[uj];
           rank += (rj > re || (rj == re && uj < ui)) ? 1 : 0;
         }
+        s_order[rank] = ui;
       }
-      s_order[rank] = ui;
+      __syncthreads();
     }
-    __syncthreads();
     split_stamp(a, l, 3);
     const int nu = split_unit_count(U * NS), npieces = nu * kPieces;
     const int n_init = min(nslot, npieces);
@@ -1473,7 +1482,7 @@ __global__ void __launch_bounds__(NT, 1) k_split(const __grid_constant__ RoundAr
     // another); the refills inside the unit loop likewise come from the last warps
     if ((tid & 31) == 0 && warp < n_init) {
       const int q = (int)((slot0 + (unsigned)warp) % (unsigned)nslot), tj = warp / kPieces;
-      issue_piece(a, W, T, NS, split_unit_of(tj, NS, s_order), warp - tj * kPieces, ring + (size_t)q * P.slot_bytes,
+      issue_piece(a, W, T, NS, split_unit_of(tj, NS, s_order, a.R), warp - tj * kPieces, ring + (size_t)q * P.slot_bytes,
                   smem_u32(bars + q));
     }
     if (one && warp == 1) softmax_one(a, T);
