@@ -36,12 +36,12 @@
  *     the call or on its position among them (bitwise).
  *   - Activations must be finite with |x| < 2^40 (and so must the SwiGLU output h);
  *     beyond that range results are undefined.
- *   - Rounds of fewer than 13 rows add each (expert, 32-element slice of the
- *     intermediate dimension) contribution to a row's output as round(y * 2^32) into
- *     64-bit integer accumulators, so the sum is exact and independent of the order of
- *     the adds; every such contribution and every output must stay below 2^31 in
- *     magnitude (beyond that results are undefined).  Wider rounds add a row's k expert
- *     outputs in fp32 in rank order.
+ *   - Every contribution to a row's output (rounds of fewer than 13 rows: one expert
+ *     and 32-element slice of the intermediate dimension; wider rounds: one expert and
+ *     chunk of up to 768 intermediate elements) is added as round(y * 2^32) into 64-bit
+ *     integer accumulators, so the sum is exact and independent of the order of the
+ *     adds; every such contribution and every output must stay below 2^31 in magnitude
+ *     (beyond that results are undefined).
  */
 #ifndef MOE_VERIFY_H
 #define MOE_VERIFY_H
@@ -111,7 +111,7 @@ void moe_destroy(moe_handle* h);
 
 /* Device workspace (bytes) a call with `rows` rows needs: barrier words, router logits,
  * the SwiGLU outputs exchanged between CTAs by the tensor-core path and the output
- * accumulators of the split path (2 x 8 copies x rows x H int64).  It depends only on
+ * accumulators (2 x 8 copies x rows x H int64; the tensor-core path uses one copy).  It depends only on
  * the dimensions and the row count, so it takes the dimensions rather than a handle and
  * can be sized before any handle exists.  0 for invalid dims/rows. */
 size_t moe_workspace_bytes(const moe_dims* dims, int32_t rows);
@@ -223,9 +223,9 @@ int moe_set_tail_skip(moe_handle* h, int32_t rank);
  * logits barrier (and the previous layer's output written), routing, piece issue, wait
  * for the first gate/up bytes, units before the last, the last unit's gate/up, its
  * SwiGLU and the wait for its down bytes, its down products, layer-end barrier.  Wider rounds (12 phases): router GEMV,
- * barrier 1, routing, wait for the first staged gate/up chunk, gate/up until the last
- * chunk has landed, gate/up after it, barrier 2, (zero), down pass, (zero), output
- * write, barrier 3. */
+ * barrier 1 (and the previous layer's output written), routing, wait for the first
+ * staged gate/up chunk, gate/up until the last chunk has landed, gate/up after it,
+ * barrier 2, (zero), down pass, (zero), (zero), barrier 3. */
 int moe_profile(moe_handle* h, int enable);
 int moe_profile_read(moe_handle* h, int kind, double* total_ms, int32_t* launches);
 int moe_profile_phases(moe_handle* h, double* mean_us, double* max_us, int32_t n_phases);

@@ -1232,7 +1232,8 @@ __device__ __forceinline__ void split_down(const RoundArgs& a, const Tables& T, 
 // This CTA's output slice [o0, o0 + no) of a finished layer: sum of the accumulator
 // copies -> fp32 output; the copies are cleared for the next layer.  Threads from
 // `first` on do it.
-__device__ __forceinline__ void split_finish(const RoundArgs& a, int layer, int o0, int no, int first) {
+__device__ __forceinline__ void split_finish(const RoundArgs& a, int layer, int o0, int no, int first,
+                                             int ncopies = kSplitCopies) {
   const size_t stride = (size_t)a.R * a.H;
   float* out = a.out + (size_t)layer * stride;
   unsigned long long* buf = a.acc + (size_t)(layer & 1) * kSplitCopies * stride;
@@ -1241,10 +1242,8 @@ __device__ __forceinline__ void split_finish(const RoundArgs& a, int layer, int 
     const int r = i / no, o = o0 + (i - r * no);
     unsigned long long* p = buf + (size_t)r * a.H + o;
     unsigned long long s = 0ull;
-#pragma unroll
-    for (int c = 0; c < kSplitCopies; ++c) s += __ldcg(p + c * stride);
-#pragma unroll
-    for (int c = 0; c < kSplitCopies; ++c) __stcg(p + c * stride, 0ull);
+    for (int c = 0; c < ncopies; ++c) s += __ldcg(p + c * stride);
+    for (int c = 0; c < ncopies; ++c) __stcg(p + c * stride, 0ull);
     out[(size_t)r * a.H + o] = __fmul_rn(__ll2float_rn((long long)s), 0x1p-32f);
   }
 }
@@ -1519,8 +1518,11 @@ __global__ void __launch_bounds__(NT, 1) k_split(const __grid_constant__ RoundAr
 //       1-D bulk copies; h' = w silu(g) v goes to the workspace split into bf16 hi + lo.
 //       Meanwhile this CTA's down rows of every union expert are prefetched into L2.
 //   B2  (every h' written)
-//   P4  down: this CTA's output rows x groups of up to 16 of an expert's positions on the
-//       tensor cores; each row's picks are added in rank order.
+//   P4  down: units (expert, group of up to 16 of its positions, 16 output rows) split
+//       across CTAs, on the tensor cores, the group's h' and the unit's down codes
+//       staged in shared memory (two items in flight); each y * 2^32, rounded, is added
+//       into the int64 accumulator of its row (exact, so order-free), and after B3 each
+//       CTA sums the accumulator copies of its output slice (the next layer's B1 window).
 //   B3  (layer l+1's router waits for layer l's output)
 //
 // A nibble n in the low four bits of a bf16 whose other bits are those of 128.0 is the
@@ -1546,14 +1548,36 @@ __global__ void __launch_bounds__(NT, 1) k_split(const __grid_constant__ RoundAr
 // whose experts carry 11 rows each on average).
 constexpr int kMmaRows = 13;
 constexpr int kKPartsGu = 8;  // K parts of a gate/up tile (hidden blocks)
-constexpr int kKPartsDn = 4;  // K parts of a down tile (intermediate blocks)
-static_assert(NW % kKPartsGu == 0 && NW % kKPartsDn == 0, "a tile's K parts run in one round");
+static_assert(NW % kKPartsGu == 0, "a tile's K parts run in one round");
 constexpr int kGuSlots = 3;
 // scratch of the tensor-core path
 constexpr int kMmaMaxPos = 256;          // CSR positions (rows x top-k) of a wide round
 constexpr size_t kMmaPart = 0;           // [NW][2][16][8] fp32 partial tiles
-constexpr size_t kMmaY = (size_t)NW * 256 * 4;  // [kMmaMaxPos][16] fp32: y per position and output row
-constexpr size_t kMmaScratch = kMmaY + (size_t)kMmaMaxPos * 16 * 4;
+constexpr size_t kMmaScratch = (size_t)NW * 256 * 4;
+
+// Intermediate blocks of one staged down item: the largest of 24, 16, 8 dividing I / 32.
+__host__ __device__ inline int dn_item_blocks(int NBI) { return NBI % 24 == 0 ? 24 : (NBI % 16 == 0 ? 16 : 8); }
+// The down pass's staging: one h' chunk [16 positions][KB blocks][128 B] and a ring of
+// kDnRing unit slots, each the unit's codes [KB][16 rows][16 B] and scales [KB][16 fp16].
+constexpr int kDnRing = 16;  // two rounds of NW / 2 units
+__host__ __device__ inline size_t dn_h_bytes(int KB) { return (size_t)16 * KB * 128; }
+__host__ __device__ inline size_t dn_c_bytes(int KB) { return (size_t)KB * 256; }
+__host__ __device__ inline size_t dn_slot_bytes(int NBI) {
+  const int KB = dn_item_blocks(NBI);
+  return dn_c_bytes(KB) + (size_t)KB * 32;  // (a multiple of 16 bytes)
+}
+__host__ __device__ inline size_t dn_stage_bytes(int NBI) {
+  return dn_h_bytes(dn_item_blocks(NBI)) + (size_t)kDnRing * dn_slot_bytes(NBI);
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 struct GuChunk {
   int ui, i0, n;
@@ -1563,6 +1587,7 @@ struct GuChunk {
 struct WidePlan {
   size_t gu_slot, gu, scratch, uni, csr, pair, w, pos_ui, pos_row, slot, pick, nunion, chunks, bars, total;
   size_t ring;
+  size_t dn, dn_slot;  // the down pass's staging: offset in the ring, bytes of one unit slot
   int gu_cap;     // units per gate/up chunk
   int max_orows;  // output rows per CTA (ceil(H / grid))
   bool ok;
@@ -1586,6 +1611,11 @@ __host__ __device__ inline WidePlan wide_plan(int H, int I, int E, int R, int k,
   const size_t router_need = (size_t)rows_per_cta * H * 4;
   if (p.ring < scratch_need) p.ring = up128(scratch_need);
   if (p.ring < router_need) p.ring = up128(router_need);
+  // the down pass stages through the ring past the next layer's router rows
+  p.dn = up128(router_need);
+  p.dn_slot = dn_slot_bytes(I >> 5);
+  if (p.ring < p.dn + dn_stage_bytes(I >> 5)) p.ring = up128(p.dn + dn_stage_bytes(I >> 5));
+
   size_t off = 0;
   p.gu = off;      off += p.ring;
   p.scratch = off; off += kMmaScratch;
@@ -1601,7 +1631,7 @@ __host__ __device__ inline WidePlan wide_plan(int H, int I, int E, int R, int k,
   p.chunks = off;  off += up128(kGuSlots * 12 + 64);
   p.bars = off;    off += 256;
   p.total = off;
-  p.ok = cap >= 8 && p.max_orows <= 16 && (size_t)R * k <= kMmaMaxPos && p.total <= limit;
+  p.ok = cap >= 8 && (size_t)R * k <= kMmaMaxPos && p.total <= limit;
   return p;
 }
 
@@ -1710,119 +1740,20 @@ __device__ void gateup_chunk_mma(const RoundArgs& a, const Tables& T, const uint
   }
 }
 
-// One round of the wide down pass on the tensor cores: NW tile parts.  Assignment j ->
-// position group j / kKPartsDn (group = up to 16 consecutive CSR positions of one
-// expert: `gpe` groups per expert) and K part j % kKPartsDn; a tile = this CTA's output
-// rows (at most 16) x the group's positions (two n-tiles).  A = the down codes of this
-// CTA's rows, read from global memory (block-major: block b of rows o0.. of an expert is
-// contiguous, so the eight rows of a fragment are one 128-byte line; prefetched into L2
-// once the routing was known); B = h' (hi + lo bf16, fragment order) read from the
-// workspace through L2, two MMAs per k16 step and n-tile.  y[position][output row] ->
-// s_yall.
-__device__ void down_round_mma(const RoundArgs& a, const LayerPtrs& W, const Tables& T, int o0, int no, int j0,
-                               int n_asg, int gpe, float* s_part, float* s_yall) {
-  const int NBI = a.I >> 5, H = a.H;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-  const uint8_t* hb = reinterpret_cast<const uint8_t*>(a.hbuf);
-  const int j = j0 + warp;
-  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-  if (j < n_asg) {
-    const int gi = j / kKPartsDn, kp = j - gi * kKPartsDn;
-    const int ui = gi / gpe, p0 = T.csr_off[ui] + 16 * (gi - ui * gpe);
-    const int cnt = min(16, T.csr_off[ui + 1] - p0);
-    if (cnt > 0) {
-      const size_t sl = (size_t)T.slot[T.uni[ui]];
-      // output rows past this CTA's repeat its last one; their results are dropped
-      const int ra = min(g, no - 1), rb = min(g + 8, no - 1);
-      const size_t rowa = sl * NBI * H + o0 + ra, rowb = sl * NBI * H + o0 + rb;
-      const uint32_t* wa_ = reinterpret_cast<const uint32_t*>(W.dn_nib + rowa * 16) + t;
-      const uint32_t* wb_ = reinterpret_cast<const uint32_t*>(W.dn_nib + rowb * 16) + t;
-      const uint16_t* sa_ = W.dn_sc + rowa;
-      const uint16_t* sb_ = W.dn_sc + rowb;
-      const size_t bstride_w = (size_t)H * 4;  // 32-bit words between blocks of one row
-      // columns past the group's positions repeat its last one; their results are dropped
-      const bool two = cnt > 8;
-      const uint4* h0 = reinterpret_cast<const uint4*>(hb + (size_t)(p0 + min(g, cnt - 1)) * NBI * 128) + 2 * t;
-      const uint4* h1 = reinterpret_cast<const uint4*>(hb + (size_t)(p0 + min(g + 8, cnt - 1)) * NBI * 128) + 2 * t;
-      const int b0 = (kp * NBI) / kKPartsDn, b1 = ((kp + 1) * NBI) / kKPartsDn;
-      for (int bb = b0; bb < b1; bb += 4) {
-        // the codes and scales of up to four blocks are loaded before any is used
-        uint32_t wa[4], wb[4];
-        float sa[4], sb[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int b = min(bb + q, b1 - 1);
-          wa[q] = __ldg(wa_ + (size_t)b * bstride_w);
-          wb[q] = __ldg(wb_ + (size_t)b * bstride_w);
-          sa[q] = half_bits(__ldg(sa_ + (size_t)b * H));
-          sb[q] = half_bits(__ldg(sb_ + (size_t)b * H));
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int b = bb + q;
-          if (b < b1) {
-            uint32_t fa[4], fb[4];
-            dq_word(wa[q], fa);
-            dq_word(wb[q], fb);
-            {
-              const uint4 hi = __ldcg(h0 + 8 * b), lo = __ldcg(h0 + 8 * b + 1);
-              float d[4] = {0.f, 0.f, 0.f, 0.f};
-              mma_bf16(d, fa[0], fb[0], fa[1], fb[1], hi.x, hi.y);
-              mma_bf16(d, fa[0], fb[0], fa[1], fb[1], lo.x, lo.y);
-              mma_bf16(d, fa[2], fb[2], fa[3], fb[3], hi.z, hi.w);
-              mma_bf16(d, fa[2], fb[2], fa[3], fb[3], lo.z, lo.w);
-              acc[0][0] = __fmaf_rn(sa[q], d[0], acc[0][0]);
-              acc[0][1] = __fmaf_rn(sa[q], d[1], acc[0][1]);
-              acc[0][2] = __fmaf_rn(sb[q], d[2], acc[0][2]);
-              acc[0][3] = __fmaf_rn(sb[q], d[3], acc[0][3]);
-            }
-            if (two) {
-              const uint4 hi = __ldcg(h1 + 8 * b), lo = __ldcg(h1 + 8 * b + 1);
-              float d[4] = {0.f, 0.f, 0.f, 0.f};
-              mma_bf16(d, fa[0], fb[0], fa[1], fb[1], hi.x, hi.y);
-              mma_bf16(d, fa[0], fb[0], fa[1], fb[1], lo.x, lo.y);
-              mma_bf16(d, fa[2], fb[2], fa[3], fb[3], hi.z, hi.w);
-              mma_bf16(d, fa[2], fb[2], fa[3], fb[3], lo.z, lo.w);
-              acc[1][0] = __fmaf_rn(sa[q], d[0], acc[1][0]);
-              acc[1][1] = __fmaf_rn(sa[q], d[1], acc[1][1]);
-              acc[1][2] = __fmaf_rn(sb[q], d[2], acc[1][2]);
-              acc[1][3] = __fmaf_rn(sb[q], d[3], acc[1][3]);
-            }
-          }
-        }
-      }
-    }
-  }
-  store_part(s_part + warp * 256, acc, g, t);
-  __syncthreads();
-  for (int i = threadIdx.x; i < (NW / kKPartsDn) * 256; i += NT) {
-    const int gl = i >> 8, nt = (i >> 7) & 1, r = (i >> 3) & 15, cc = i & 7;
-    const int gi = j0 / kKPartsDn + gl;
-    if (gi * kKPartsDn >= n_asg || r >= no) continue;
-    const int ui = gi / gpe, p0 = T.csr_off[ui] + 16 * (gi - ui * gpe);
-    const int pos = nt * 8 + cc;
-    if (pos >= T.csr_off[ui + 1] - p0) continue;
-    float y = 0.f;
-#pragma unroll
-    for (int kp = 0; kp < kKPartsDn; ++kp) y = __fadd_rn(y, s_part[(gl * kKPartsDn + kp) * 256 + nt * 128 + r * 8 + cc]);
-    s_yall[(p0 + pos) * 16 + r] = y;
-  }
-  __syncthreads();
-}
-
-// This CTA's down rows [o0, o0 + no) of every union expert into L2 (they depend only on
-// the routing and are read by the down pass after the h exchange): per expert and block,
-// one bulk prefetch of the codes and one of the scales (rounded out to 16 bytes).
-__device__ void prefetch_down_rows(const RoundArgs& a, const LayerPtrs& W, const Tables& T, int U, int o0, int no) {
-  const int NBI = a.I >> 5, H = a.H;
-  for (int i = threadIdx.x; i < U * NBI; i += NT) {
-    const int ui = i / NBI, b = i - ui * NBI;
-    const size_t row = ((size_t)T.slot[T.uni[ui]] * NBI + b) * H + o0;
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(W.dn_nib + row * 16), "r"((unsigned)(no * 16))
-                 : "memory");
-    const uintptr_t s0 = reinterpret_cast<uintptr_t>(W.dn_sc + row) & ~(uintptr_t)15;
-    const uintptr_t s1 = (reinterpret_cast<uintptr_t>(W.dn_sc + row + no) + 15) & ~(uintptr_t)15;
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(s0), "r"((unsigned)(s1 - s0)) : "memory");
+// The down units [du0, du1) of this CTA (unit = (expert group, block of 16 output rows),
+// as the down pass numbers them) into L2: they depend only on the routing and are read
+// after the h exchange.  Per unit and intermediate block, one bulk prefetch of the 16
+// rows' codes (256 bytes) and one of their scales (32 bytes).
+__device__ void prefetch_down_units(const RoundArgs& a, const LayerPtrs& W, const Tables& T, int gpe, int du0,
+                                    int du1) {
+  const int NBI = a.I >> 5, H = a.H, NOB = H >> 4;
+  for (int i = threadIdx.x; i < (du1 - du0) * NBI; i += NT) {
+    const int du = du0 + i / NBI, b = i - (i / NBI) * NBI;
+    const int ug = du / NOB, ob = du - ug * NOB, ui = ug / gpe;
+    if (16 * (ug - ui * gpe) >= T.csr_off[ui + 1] - T.csr_off[ui]) continue;  // an empty group
+    const size_t row = ((size_t)T.slot[T.uni[ui]] * NBI + b) * H + (size_t)ob * 16;
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(W.dn_nib + row * 16), "r"(256u) : "memory");
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(W.dn_sc + row), "r"(32u) : "memory");
   }
 }
 
@@ -1836,7 +1767,6 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
   const uint32_t bar_router = smem_u32(bars + kGuSlots);
   uint8_t* gu = smem + P.gu;
   float* s_mpart = reinterpret_cast<float*>(smem + P.scratch + kMmaPart);
-  float* s_yall = reinterpret_cast<float*>(smem + P.scratch + kMmaY);
   float* s_rw = reinterpret_cast<float*>(gu);
   GuChunk* s_chunks = reinterpret_cast<GuChunk*>(smem + P.chunks);
   Tables T{reinterpret_cast<int*>(smem + P.uni),     reinterpret_cast<int*>(smem + P.csr),
@@ -1851,7 +1781,7 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
   int* s_ui = reinterpret_cast<int*>(gu + (size_t)a.E * 8 + (size_t)a.R * a.k * 4);
   int* s_rank = s_ui + a.E;
   if (tid == 0) {
-    for (int i = 0; i < kGuSlots + 1; ++i) mbar_init(smem_u32(bars + i), 1);
+    for (int i = 0; i < kGuSlots + 2; ++i) mbar_init(smem_u32(bars + i), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     issue_router_rows(a, a.layer[0].router, s_rw, bar_router);
   }
@@ -1863,12 +1793,24 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
   const size_t RH = (size_t)a.R * a.H;
   const int o0 = (int)(((long long)blockIdx.x * a.H) / G);
   const int no = (int)(((long long)(blockIdx.x + 1) * a.H) / G) - o0;
+  // this CTA's output slice of the accumulators (one copy per layer parity: an output
+  // receives only its row's k adds here) starts at zero, ordered before any other CTA's
+  // adds by the first grid barrier
+  for (int i = tid; i < 2 * a.R * no; i += NT) {
+    const int c = i / (a.R * no), rem = i - c * (a.R * no), r = rem / no;
+    __stcg(a.acc + ((size_t)c * kAccCopies * a.R + r) * a.H + o0 + (rem - r * no), 0ull);
+  }
   // the GU slots in flight: bit q set
   unsigned gu_pend = 0u;
+  // the down pass's h' chunk (thread 0's view): parity of its next completion, in flight
+  const uint32_t bar_dn = smem_u32(bars + kGuSlots + 1);
+  unsigned dn_ph = 0u, dn_pend = 0u;
   auto bail = [&]() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
     if (tid == 0) {
       for (int q = 0; q < kGuSlots; ++q)
         if (gu_pend & (1u << q)) mbar_wait_bounded(smem_u32(bars + q), (gu_ph >> q) & 1u, a.status, kDefaultWaitCycles);
+      if (dn_pend) mbar_wait_bounded(bar_dn, dn_ph, a.status, kDefaultWaitCycles);
     }
     drain_and_abort(a, bars, 1, 0u, 0u, 0, 0, router_pend, bar_router, ph_router);
   };
@@ -1901,6 +1843,10 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
       }
       T.slot[e] = sl;
     }
+    // the previous layer's output slice while the logits barrier completes (every add of
+    // that layer went into the other accumulator buffer and is in: its closing barrier is
+    // behind us)
+    if (l > 0 && no > 0) split_finish(a, l - 1, o0, no, 0, 1);
     if (!grid_wait(a, sy)) {
       bail();
       return;
@@ -1950,8 +1896,13 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
       }
       *reinterpret_cast<int*>(smem + P.chunks + kGuSlots * 12) = nc;
     }
-    // this CTA's down rows of every union expert are needed after B2: into L2 now
-    if (no > 0) prefetch_down_rows(a, W, T, U, o0, no);
+    // this CTA's down units are needed after B2: into L2 now
+    {
+      const int gpe = (a.R + 15) >> 4;
+      const unsigned n_du = (unsigned)U * (unsigned)gpe * (unsigned)(a.H >> 4);
+      prefetch_down_units(a, W, T, gpe, (int)(((unsigned)blockIdx.x * n_du) / (unsigned)G),
+                          (int)((((unsigned)blockIdx.x + 1u) * n_du) / (unsigned)G));
+    }
     __syncthreads();
     const int n_chunks = *reinterpret_cast<const int*>(smem + P.chunks + kGuSlots * 12);
     gu_pend = (1u << min(kGuSlots, n_chunks)) - 1u;
@@ -1994,35 +1945,140 @@ __global__ void __launch_bounds__(NT, 1) k_round(const __grid_constant__ RoundAr
     }
     stamp(a, l, 7);
     stamp(a, l, 8);
-    if (no > 0) {
-      // ---- wide down: groups of up to 16 of one expert's positions on the tensor cores ----
+    {
+      // ---- wide down on the tensor cores ----
+      // Units (union expert, group of up to 16 of its positions, block of 16 output rows),
+      // in that order, split contiguously across the CTAs: a CTA's units share one or two
+      // groups, and each expert's h' is read by the few CTAs that own its rows (a pass
+      // sliced by output rows makes every CTA read every expert's h').  Per group segment
+      // of the range and K chunk of KB blocks, the group's h' chunk is staged once (bulk
+      // copy); the units' codes and scales stream through a ring of kDnRing slots by
+      // cp.async, in rounds of NW / 2 units.  Warp = (unit of the round, n-tile) over the
+      // whole chunk: two MMAs per k16 step (h' hi + lo), the block scale applied per block,
+      // and each y[position][row] * 2^32, rounded, is added into the int64 accumulator of
+      // the position's row (exact integer adds: the output depends on neither the order,
+      // the split nor the other rows).
       const int gpe = (a.R + 15) >> 4;  // position groups per expert
-      const int per_e = gpe * kKPartsDn, n_asg = U * per_e;
-      for (int j0 = 0; j0 < n_asg; j0 += NW) down_round_mma(a, W, T, o0, no, j0, n_asg, gpe, s_mpart, s_yall);
-      stamp(a, l, 9);
-      stamp(a, l, 10);
-      // each row's picks in rank order
-      float* out = a.out + (size_t)l * RH;
-      for (int i = tid; i < a.R * no; i += NT) {
-        const int r = i / no, ol = i - r * no;
-        float acc = 0.f;
-        for (int j = 0; j < a.k; ++j) {
-          const int pp = T.pick_pos[r * a.k + j];
-          if (pp >= 0) acc = __fadd_rn(acc, s_yall[pp * 16 + ol]);
+      const int H = a.H, NOB = H >> 4, NBI = a.I >> 5, KB = dn_item_blocks(NBI), NKC = NBI / KB;
+      const unsigned n_du = (unsigned)U * (unsigned)gpe * (unsigned)NOB;
+      const int du0 = (int)(((unsigned)blockIdx.x * n_du) / (unsigned)G);
+      const int du1 = (int)((((unsigned)blockIdx.x + 1u) * n_du) / (unsigned)G);
+      const uint8_t* hb = reinterpret_cast<const uint8_t*>(a.hbuf);
+      unsigned long long* acc_copy = a.acc + (size_t)(l & 1) * kAccCopies * RH;
+      uint8_t* sh = gu + P.dn;                 // the h' chunk
+      uint8_t* ring_dn = sh + dn_h_bytes(KB);  // unit slots
+      constexpr int kRound = NW / 2;
+      const int lane = tid & 31, g = lane >> 2, t = lane & 3, wq = (tid >> 5) >> 1, nt = (tid >> 5) & 1;
+      if (du0 < du1 && tid == 0)  // h' was written by generic stores before B2; bulk copies read it
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+      for (int sg = du0; sg < du1;) {
+        const int ug = sg / NOB, ob0 = sg - ug * NOB;
+        const int seg_end = min(du1, (ug + 1) * NOB), nu = seg_end - sg;
+        const int ui = ug / gpe, p0 = T.csr_off[ui] + 16 * (ug - ui * gpe);
+        const int cnt = min(16, T.csr_off[ui + 1] - p0);
+        sg = seg_end;
+        if (cnt <= 0) continue;  // an empty group (uniform)
+        const size_t blk0 = (size_t)T.slot[T.uni[ui]] * NBI;
+        const int nr = (nu + kRound - 1) / kRound;
+        for (int kc = 0; kc < NKC; ++kc) {
+          // the group's h' chunk (its previous readers are past the last barrier)
+          if (tid == 0) {
+            const uint32_t bytes = (uint32_t)(cnt * KB * 128);
+            mbar_expect_tx(bar_dn, bytes);
+            if (NKC == 1) {
+              bulk_g2s(smem_u32(sh), hb + (size_t)p0 * NBI * 128, bytes, bar_dn);
+            } else {
+              for (int q = 0; q < cnt; ++q)
+                bulk_g2s(smem_u32(sh + (size_t)q * KB * 128), hb + ((size_t)(p0 + q) * NBI + (size_t)kc * KB) * 128,
+                         (uint32_t)(KB * 128), bar_dn);
+            }
+            dn_pend = 1u;
+          }
+          // round r: units kRound r .. of the segment, unit j in ring slot j % kDnRing: codes
+          // (block b of the 16 rows is one 256-byte run) and scales (32 bytes per block)
+          auto issue_round = [&](int r) {
+            const int j0 = r * kRound, nj = min(kRound, nu - j0);
+            for (int i = tid; i < nj * KB * 18; i += NT) {
+              const int q = i / (KB * 18), e = i - q * (KB * 18), j = j0 + q;
+              uint8_t* sc = ring_dn + (size_t)(j % kDnRing) * P.dn_slot;
+              const size_t row0 = (blk0 + (size_t)kc * KB) * (size_t)H + (size_t)(ob0 + j) * 16;
+              if (e < KB * 16)
+                cp_async16(smem_u32(sc + (size_t)e * 16), W.dn_nib + (row0 + (size_t)(e >> 4) * H + (e & 15)) * 16);
+              else {
+                const int f = e - KB * 16;  // scales: block f / 2, half f & 1 of its 16 values
+                cp_async16(smem_u32(sc + dn_c_bytes(KB) + (size_t)f * 16),
+                           W.dn_sc + row0 + (size_t)(f >> 1) * H + (f & 1) * 8);
+              }
+            }
+            cp_async_commit();
+          };
+          issue_round(0);
+          if (nr > 1) issue_round(1);
+          // (every thread waits: the wait is its acquire of the copied bytes)
+          const bool ok = mbar_wait_bounded(bar_dn, dn_ph, a.status, a.wait_cycles);
+          if (ok) {
+            dn_ph ^= 1u;
+            dn_pend = 0u;
+          }
+          // positions past the group repeat its last one; their results are dropped
+          const uint4* hrow = reinterpret_cast<const uint4*>(sh + (size_t)min(nt * 8 + g, cnt - 1) * KB * 128) + 2 * t;
+          for (int r = 0; r < nr; ++r) {
+            if (r + 1 < nr)
+              cp_async_wait<1>();
+            else
+              cp_async_wait<0>();
+            if (__syncthreads_or(!ok)) {
+              bail();
+              return;
+            }
+            const int j = r * kRound + wq;
+            if (j < nu && nt * 8 < cnt) {
+              const uint8_t* sc = ring_dn + (size_t)(j % kDnRing) * P.dn_slot;
+              const uint16_t* s16 = reinterpret_cast<const uint16_t*>(sc + dn_c_bytes(KB));
+              const uint32_t* ca = reinterpret_cast<const uint32_t*>(sc) + g * 4 + t;
+              float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 2
+              for (int b = 0; b < KB; ++b) {
+                uint32_t fa[4], fb[4];
+                dq_word(ca[b * 64], fa);
+                dq_word(ca[b * 64 + 32], fb);
+                const float sa = half_bits(s16[b * 16 + g]), sbb = half_bits(s16[b * 16 + g + 8]);
+                const uint4 hi = hrow[8 * b], lo = hrow[8 * b + 1];
+                float d[4] = {0.f, 0.f, 0.f, 0.f};
+                mma_bf16(d, fa[0], fb[0], fa[1], fb[1], hi.x, hi.y);
+                mma_bf16(d, fa[0], fb[0], fa[1], fb[1], lo.x, lo.y);
+                mma_bf16(d, fa[2], fb[2], fa[3], fb[3], hi.z, hi.w);
+                mma_bf16(d, fa[2], fb[2], fa[3], fb[3], lo.z, lo.w);
+                acc[0] = __fmaf_rn(sa, d[0], acc[0]);
+                acc[1] = __fmaf_rn(sa, d[1], acc[1]);
+                acc[2] = __fmaf_rn(sbb, d[2], acc[2]);
+                acc[3] = __fmaf_rn(sbb, d[3], acc[3]);
+              }
+              const int o = (ob0 + j) * 16 + g;
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                const int pos = nt * 8 + 2 * t + (v & 1);
+                if (pos < cnt)
+                  red_add_u64(acc_copy + (size_t)T.pos_row[p0 + pos] * H + o + (v >> 1) * 8,
+                              (unsigned long long)__float2ll_rn(acc[v] * 4294967296.0f));
+              }
+            }
+            __syncthreads();  // this round's slots are free
+            if (r + 2 < nr) issue_round(r + 2);
+          }
         }
-        out[(size_t)r * a.H + o0 + ol] = acc;
       }
-    } else {
-      stamp(a, l, 9);
-      stamp(a, l, 10);
     }
+    stamp(a, l, 9);
+    stamp(a, l, 10);
     stamp(a, l, 11);
-    if (l + 1 < a.L && !grid_sync(a, sy)) {  // B3: layer output complete
+    if (!grid_sync(a, sy)) {  // B3: every add of this layer is in
       bail();
       return;
     }
-    stamp(a, l, 12);  // (the last layer has no B3: its interval is zero)
+    stamp(a, l, 12);
   }
+  if (no > 0) split_finish(a, a.L - 1, o0, no, 0, 1);
 }
 
 }  // namespace
