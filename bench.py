@@ -42,6 +42,9 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--layers", type=int, default=0, help="override the stack depth (0 = 40)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="time the headline round (--rows, --layers) only and print a short line: "
+                         "the command the profiles under profiles/ capture")
     ap.add_argument("--e512-layers", type=int, default=0, help="override the 512-expert stack depth (0 = 48)")
     ap.add_argument("--rows", type=int, default=1, choices=[1, 4, 16],
                     help="rows of the headline round (1 = the decode-width workload; 4 and 16 "
@@ -429,6 +432,12 @@ def run_ours(args):
     ms_round = head["ms_total"] / head["steps"]
     us_layer = 1e3 * ms_round / L
     value = whole_job_gbs(head["bytes_per_round"], world, ms_round)
+    if args.headline_only:
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "value": value, "unit": UNIT, "headline_only": True,
+                              "rows": R0, "layers": L, "us_per_layer": us_layer,
+                              "unique_experts_per_layer": float(np.mean(head["U"]))}), flush=True)
+        return 0
 
     # end to end through the C ABI with host buffers (pinned), copies inside the timed region;
     # right after the device-timed round, under the same conditions

@@ -307,11 +307,10 @@ struct Tables {
 // routes only at rank 7 or lower are skipped): with a.tail_rank = T > 0 an expert whose
 // best 1-based rank over the rows that picked it is >= T leaves the union; its picks
 // are not evaluated and the other weights are not renormalised.
-// It also cuts this CTA's share of the gate/up units into s_range[0..1] (first, end):
-// units are shared out by work, a unit of an expert with R_e rows weighing 2 + 2 R_e on
-// the fp32 path (a fixed share for the weight stream plus the per-row FMA work; the
-// measured chunk times at 1, 2 and 4 rows go about 1 : 1.4 : 2.7) and ceil(R_e / 16) on
-// the tensor cores (wide != 0); one row is an even split by count.
+// For the tensor-core kernel (wide != 0) it also cuts this CTA's share of the gate/up
+// units into s_range[0..1] (first, end): units are shared out by work, a unit of an
+// expert with R_e rows weighing ceil(R_e / 16); one row is an even split by count.  (The
+// split kernel deals its units to the CTAs itself: split_unit_of.)
 // One row without tail skip (E a power of two, 32 <= E <= NT): the whole routing by
 // expert-parallel counting, no sequential rounds.  The rank of expert i is the number of
 // experts that rank before it (larger logit, or equal logit and lower id), counted over
@@ -468,6 +467,7 @@ __device__ void route_small(const RoundArgs& a, const Tables& T, const int* s_id
       if (a.stats) a.stats[layer] = U;
     }
   }
+  if (!wide) return;  // (the split kernel deals its units itself)
   const int G = gridDim.x, c = blockIdx.x;
   if (a.R == 1) {
     const unsigned N = (unsigned)U * (unsigned)upe;
@@ -482,7 +482,7 @@ __device__ void route_small(const RoundArgs& a, const Tables& T, const int* s_id
   int wu = 0;
   if (lane < U) {
     const int re = T.csr_off[lane + 1] - T.csr_off[lane];
-    wu = wide ? (re + 15) >> 4 : 2 + 2 * re;
+    wu = (re + 15) >> 4;
   }
   const int lw = upe * wu;
   int incw = lw;
@@ -553,7 +553,7 @@ __device__ int route_phase(const RoundArgs& a, const Tables& T, unsigned* s_mask
   if (warp == 0) {
     const int per = (E + 31) >> 5;  // <= 16
     const int e0 = lane * per, e1 = min(e0 + per, E);
-    auto weight = [&](unsigned m) { const int re = __popc(m); return wide ? (re + 15) >> 4 : 2 + 2 * re; };
+    auto weight = [&](unsigned m) { return (__popc(m) + 15) >> 4; };
     int lf = 0, lc = 0, lw = 0;
     for (int e = e0; e < e1; ++e) {
       unsigned m = s_mask[e];
@@ -578,10 +578,11 @@ __device__ int route_phase(const RoundArgs& a, const Tables& T, unsigned* s_mask
       }
     }
     int basef = incf - lf, basec = incc - lc;
-    // this CTA's unit range: the targets t(c) ~ c W / G are computed the same way by
+    // this CTA's unit range (the tensor-core kernel's gate/up units; the split kernel
+    // deals its units itself): the targets t(c) ~ c W / G are computed the same way by
     // neighbouring CTAs (in fp32; monotone in c, t(0) = 0, t(G) = W), so the ranges
     // tile the units.
-    {
+    if (wide) {
       const int G = gridDim.x, c = blockIdx.x;
       const int U = __shfl_sync(0xffffffffu, incf, 31);
       if (R == 1) {
