@@ -36,6 +36,12 @@
  *     the call or on its position among them (bitwise).
  *   - Activations must be finite with |x| < 2^40 (and so must the SwiGLU output h);
  *     beyond that range results are undefined.
+ *   - Rounds of fewer than 13 rows evaluate each 32-element block dot of steps 4 and 5
+ *     exactly in integers, from the block's codes and its activations in block fixed
+ *     point (x: 16 bits relative to the block's largest |x|; h: 23 bits), then scale it
+ *     in fp32; the rounding of the smaller activations of a block (at most 2^-15 and
+ *     2^-22 of the block's largest) stays within the stated output tolerance.  Wider
+ *     rounds use bf16 x (exact) and h split into bf16 hi + lo on the tensor cores.
  *   - Every contribution to a row's output (rounds of fewer than 13 rows: one expert
  *     and 32-element slice of the intermediate dimension; wider rounds: one expert and
  *     chunk of up to 768 intermediate elements) is added as round(y * 2^32) into 64-bit

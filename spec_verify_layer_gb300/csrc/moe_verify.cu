@@ -6,29 +6,28 @@
 //
 // k_split (rounds of fewer than kMmaRows rows; the CUDA cores).  Per layer:
 //   P1  router GEMV: this CTA's router rows (staged into shared memory while the
-//       previous layer ran: they depend on no data), canonical fp32 order -> logits;
-//       meanwhile the previous layer's output slice of this CTA is finished.
-//   B1
+//       previous layer ran: they depend on no data), canonical fp32 order -> logits.
+//   B1  (in its window: the slot table, this layer's activation digits and the previous
+//       layer's output slice of this CTA)
 //   P2  every CTA reads the logits and builds the same routing in shared memory:
 //       per-row top-k (lower id wins ties), renormalised weights, the ascending expert
 //       union U and, per union expert, the rows that picked it (CSR).
 //   P3  the U * I/32 work units (union expert, 32-wide slice of the intermediate
-//       dimension) are split contiguously across CTAs by work; a CTA streams each unit's
-//       gate/up rows and down block column through shared memory, computes the SwiGLU
-//       outputs of the slice and their share of the down product for every output, and
-//       adds it as exact 2^32-scaled integers into the workspace accumulators.
+//       dimension) are dealt to the CTAs heaviest first in snake order; a CTA streams
+//       each unit's gate/up rows and down block column through shared memory, computes
+//       the SwiGLU outputs of the slice and their share of the down product for every
+//       output, and adds it as exact 2^32-scaled integers into the accumulators.
 //   B3  (layer l+1's router waits for layer l's output, as a real decode would)
 //
 // k_round (wider rounds; the tensor cores): gate/up split by intermediate index, the
 // SwiGLU outputs exchanged through the workspace under a second grid barrier, the down
-// product by output row (see the section "Wide verify rounds" below).
+// product by (expert, 16 output rows) units added as exact integers (see the section
+// "Wide verify rounds" below).
 //
-// Dequantisation without a convert instruction: a nibble n placed in bits [p, p+4) of
-// an otherwise-zero fp32 word is the subnormal n * 2^(p-149); an fma with
-// x * 2^(87-4m) (m = the nibble's slot) yields n * x * 2^-62 exactly.  One AND per
-// weight (plus one shift per 8), and packed f32x2 FMAs over pairs of weights.  The
-// code offset (q = n - 8) is applied once per 32-element block:
-// sum (n-8) x = 2^62 acc - 8 sum x.
+// Expert dots on the CUDA cores are integer block dots: within a 32-element block,
+// sum (n - 8) v over the nibble codes n and the activation v held in block fixed point
+// (x: 16 bits in two byte digits; the SwiGLU output: 23 bits in three) is computed
+// exactly with dp4a on the masked nibble bytes, then scaled once per block in fp32.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -1542,11 +1541,11 @@ __global__ void __launch_bounds__(NT, 1) k_split(const __grid_constant__ RoundAr
 // parts are added in a fixed order, so a row's result does not depend on the rows it
 // shares the round with.
 
-// Rounds of at least this many rows use the tensor-core kernel.  Below it the split
-// kernel measured faster on the 128-expert / top-8 layer with draft rows at sigma 0.5
-// (8 rows: 54 against 64 us per layer, 12 rows: 71 against 78); from 16 rows the tensor
-// cores win (81 against 89 us; 44 against 88 with the near-duplicate copy-span rows,
-// whose experts carry 11 rows each on average).
+// Rounds of at least this many rows use the tensor-core kernel.  Measured on the
+// 128-expert / top-8 layer (40-layer rounds, draft rows at sigma 0.5): 12 rows on the
+// split kernel 58.0 us per layer against 64.9 us for 13 rows on the tensor cores; with
+// 14 to 16 near-duplicate copy-span rows the tensor cores take 39 to 40 us against 65 to
+// 72 us on the split kernel.
 constexpr int kMmaRows = 13;
 constexpr int kKPartsGu = 8;  // K parts of a gate/up tile (hidden blocks)
 static_assert(NW % kKPartsGu == 0, "a tile's K parts run in one round");
