@@ -116,6 +116,25 @@ def _tiny_stack(**kw):
     return Stack(cfg, n_layers=1)
 
 
+@pytest.mark.parametrize("inter", [1024, 1536])
+def test_intermediate_sizes_in_several_k_chunks(inter):
+    """I / 32 not a multiple of 24: the tensor-core down pass stages each group's h' in
+    two K chunks (one copy per position, exact adds per chunk); 13 and 16 rows on that
+    kernel and 4 rows on the split kernel against the oracle, two layers."""
+    s = Stack(syngen.CONFIGS["tiny"].with_(inter=inter, top_k=4), n_layers=2)
+    try:
+        for layer in range(2):
+            router = syngen.router(s.cfg, layer)
+            for R, sigma in ((4, 0.5), (13, 0.5), (16, 0.1)):
+                xb = s.rows(layer, R, sigma)
+                got = run_layer(s, layer, xb)
+                rt = oracle.route(router, xb, s.cfg.top_k)
+                ref = oracle.layer(router, xb, s.cfg.top_k, rt.union, syngen.experts_stacked(s.cfg, layer, rt.union))
+                assert_close(got, ref, f"I={inter} layer {layer} R={R}")
+    finally:
+        s.close()
+
+
 def test_single_expert_union():
     s = _tiny_stack(top_k=1)
     try:
