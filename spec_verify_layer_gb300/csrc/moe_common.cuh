@@ -36,56 +36,36 @@ __device__ __forceinline__ bool ranks_before(unsigned ka, int ia, unsigned kb, i
   return ka > kb || (ka == kb && ia < ib);
 }
 
-// Top-k of one row of logits by one warp.  Lane l owns experts l + 32t (t < NE), kept
-// sorted best-first in registers (bitonic network); each of the k rounds takes the
-// warp-wide best head (redux.sync max on the key, then min on the id among equal
-// keys) and the owning lane pops it.  Lane j returns pick j (logit and id).
+// Top-k of one row of logits by one warp.  Lane l owns experts l + 32t (t < NE) as keys
+// in registers; each of the k rounds takes every lane's best key (the first of equal
+// keys, i.e. its lowest id), the warp-wide best (redux.sync max on the key, then min on
+// the id among equal keys), and the owning lane clears that key.  Lane j returns pick j
+// (logit and id).
 template <int NE>
 __device__ __forceinline__ void select_row(const float* row, int E, int k, int lane, float& my_l,
                                            int& my_id) {
   unsigned kk[NE];
-  int id[NE];
 #pragma unroll
   for (int t = 0; t < NE; ++t) {
     const int e = lane + 32 * t;
-    id[t] = e;
-    kk[t] = (e < E) ? order_key(__ldcg(row + e)) : 0u;
-  }
-#pragma unroll
-  for (int size = 2; size <= NE; size <<= 1) {
-#pragma unroll
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-#pragma unroll
-      for (int i = 0; i < NE; ++i) {
-        const int j = i ^ stride;
-        if (j > i) {
-          const bool up = (i & size) == 0;  // this block sorts best-first
-          const bool sw = up ? ranks_before(kk[j], id[j], kk[i], id[i])
-                             : ranks_before(kk[i], id[i], kk[j], id[j]);
-          if (sw) {
-            const unsigned tk = kk[i];
-            kk[i] = kk[j];
-            kk[j] = tk;
-            const int ti = id[i];
-            id[i] = id[j];
-            id[j] = ti;
-          }
-        }
-      }
-    }
+    kk[t] = (e < E) ? order_key(__ldcg(row + e)) : 0u;  // (finite logits: keys >= 1)
   }
   for (int j = 0; j < k; ++j) {
-    const unsigned m = __reduce_max_sync(0xffffffffu, kk[0]);
-    const unsigned cand = (kk[0] == m) ? (unsigned)id[0] : 0xffffffffu;
-    const unsigned win = __reduce_min_sync(0xffffffffu, cand);
-    if ((unsigned)id[0] == win) {
+    unsigned best = kk[0];
+    int bt = 0;
 #pragma unroll
-      for (int t = 0; t + 1 < NE; ++t) {
-        kk[t] = kk[t + 1];
-        id[t] = id[t + 1];
+    for (int t = 1; t < NE; ++t)
+      if (kk[t] > best) {
+        best = kk[t];
+        bt = t;
       }
-      kk[NE - 1] = 0u;
-      id[NE - 1] = INT_MAX;
+    const unsigned mine = (unsigned)(lane + 32 * bt);
+    const unsigned m = __reduce_max_sync(0xffffffffu, best);
+    const unsigned win = __reduce_min_sync(0xffffffffu, best == m ? mine : 0xffffffffu);
+    if (mine == win) {
+#pragma unroll
+      for (int t = 0; t < NE; ++t)
+        if (t == bt) kk[t] = 0u;
     }
     if (lane == j) {
       my_l = key_value(m);

@@ -310,8 +310,9 @@ struct Tables {
 // units into s_range[0..1] (first, end): units are shared out by work, a unit of an
 // expert with R_e rows weighing ceil(R_e / 16); one row is an even split by count.  (The
 // split kernel deals its units to the CTAs itself: split_unit_of.)
-// One row without tail skip (E a power of two, 32 <= E <= NT): the whole routing by
-// expert-parallel counting, no sequential rounds.  The rank of expert i is the number of
+// One row without tail skip (E a power of two, 32 <= E <= 128; the counting work grows
+// as E^2 and a larger E measured faster through the selection rounds): the whole
+// routing by expert-parallel counting, no sequential rounds.  The rank of expert i is the number of
 // experts that rank before it (larger logit, or equal logit and lower id), counted over
 // quarters of the row by four threads; the k experts of rank < k are the picks (the
 // same set and order as select_row), and a ballot over the experts in id order gives
@@ -319,7 +320,7 @@ struct Tables {
 // pick j's logit; softmax_one turns it into the weight.  This CTA's unit range is the
 // even split of the k I units.
 __device__ __forceinline__ bool route_one_ok(const RoundArgs& a) {
-  return a.R == 1 && a.tail_rank == 0 && a.E <= NT && a.E >= 32 && (a.E & (a.E - 1)) == 0;
+  return a.R == 1 && a.tail_rank == 0 && a.E <= 128 && a.E >= 32 && (a.E & (a.E - 1)) == 0;
 }
 
 __device__ __forceinline__ int ranks_before_u(unsigned kj, int j, unsigned ki, int i) {
