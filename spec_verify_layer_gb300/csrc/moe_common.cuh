@@ -37,9 +37,11 @@ __device__ __forceinline__ bool ranks_before(unsigned ka, int ia, unsigned kb, i
 }
 
 // Top-k of one row of logits by one warp.  Lane l owns experts l + 32t (t < NE) as keys
-// in registers; each of the k rounds takes every lane's best key (the first of equal
-// keys, i.e. its lowest id), the warp-wide best (redux.sync max on the key, then min on
-// the id among equal keys), and the owning lane clears that key.  Lane j returns pick j
+// in registers; each of the k rounds takes the warp-wide best (redux.sync max on the
+// key, then min on the id among equal keys) of the lanes' best keys and the owning lane
+// drops it.  With up to 4 keys per lane they are sorted best-first once and a lane's
+// best is its head; with more, a lane's best is found by a scan each round (keys only:
+// a sorted network of 16 keys and ids spilled registers).  Lane j returns pick j
 // (logit and id).
 template <int NE>
 __device__ __forceinline__ void select_row(const float* row, int E, int k, int lane, float& my_l,
@@ -49,6 +51,53 @@ __device__ __forceinline__ void select_row(const float* row, int E, int k, int l
   for (int t = 0; t < NE; ++t) {
     const int e = lane + 32 * t;
     kk[t] = (e < E) ? order_key(__ldcg(row + e)) : 0u;  // (finite logits: keys >= 1)
+  }
+  if constexpr (NE <= 4) {
+    // few keys per lane: sorted best-first once (ties: the lower id, i.e. the lower t,
+    // first), then each round pops the winning lane's head
+    int id[NE];
+#pragma unroll
+    for (int t = 0; t < NE; ++t) id[t] = lane + 32 * t;
+#pragma unroll
+    for (int size = 2; size <= NE; size <<= 1) {
+#pragma unroll
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+#pragma unroll
+        for (int i = 0; i < NE; ++i) {
+          const int jj = i ^ stride;
+          if (jj > i) {
+            const bool up = (i & size) == 0;
+            const bool sw = up ? ranks_before(kk[jj], id[jj], kk[i], id[i]) : ranks_before(kk[i], id[i], kk[jj], id[jj]);
+            if (sw) {
+              const unsigned tk = kk[i];
+              kk[i] = kk[jj];
+              kk[jj] = tk;
+              const int ti = id[i];
+              id[i] = id[jj];
+              id[jj] = ti;
+            }
+          }
+        }
+      }
+    }
+    for (int j = 0; j < k; ++j) {
+      const unsigned m = __reduce_max_sync(0xffffffffu, kk[0]);
+      const unsigned win = __reduce_min_sync(0xffffffffu, kk[0] == m ? (unsigned)id[0] : 0xffffffffu);
+      if ((unsigned)id[0] == win) {
+#pragma unroll
+        for (int t = 0; t + 1 < NE; ++t) {
+          kk[t] = kk[t + 1];
+          id[t] = id[t + 1];
+        }
+        kk[NE - 1] = 0u;
+        id[NE - 1] = INT_MAX;
+      }
+      if (lane == j) {
+        my_l = key_value(m);
+        my_id = (int)win;
+      }
+    }
+    return;
   }
   for (int j = 0; j < k; ++j) {
     unsigned best = kk[0];
