@@ -97,28 +97,28 @@ __device__ __forceinline__ void select_row(const float* row, int E, int k, int l
         my_id = (int)win;
       }
     }
-    return;
-  }
-  for (int j = 0; j < k; ++j) {
-    unsigned best = kk[0];
-    int bt = 0;
+  } else {
+    for (int j = 0; j < k; ++j) {
+      unsigned best = kk[0];
+      int bt = 0;
 #pragma unroll
-    for (int t = 1; t < NE; ++t)
-      if (kk[t] > best) {
-        best = kk[t];
-        bt = t;
+      for (int t = 1; t < NE; ++t)
+        if (kk[t] > best) {
+          best = kk[t];
+          bt = t;
+        }
+      const unsigned mine = (unsigned)(lane + 32 * bt);
+      const unsigned m = __reduce_max_sync(0xffffffffu, best);
+      const unsigned win = __reduce_min_sync(0xffffffffu, best == m ? mine : 0xffffffffu);
+      if (mine == win) {
+#pragma unroll
+        for (int t = 0; t < NE; ++t)
+          if (t == bt) kk[t] = 0u;
       }
-    const unsigned mine = (unsigned)(lane + 32 * bt);
-    const unsigned m = __reduce_max_sync(0xffffffffu, best);
-    const unsigned win = __reduce_min_sync(0xffffffffu, best == m ? mine : 0xffffffffu);
-    if (mine == win) {
-#pragma unroll
-      for (int t = 0; t < NE; ++t)
-        if (t == bt) kk[t] = 0u;
-    }
-    if (lane == j) {
-      my_l = key_value(m);
-      my_id = (int)win;
+      if (lane == j) {
+        my_l = key_value(m);
+        my_id = (int)win;
+      }
     }
   }
 }
