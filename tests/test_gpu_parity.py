@@ -329,8 +329,8 @@ def test_bounded_wait_reports_timeout_without_hanging():
 
 
 def test_calls_with_fewer_rows_than_the_handle_allows():
-    """A handle sized for 16 rows serves 1-row and 16-row calls (shared-memory plan is
-    fixed by the handle, not by the call)."""
+    """A handle sized for 16 rows serves 1-row and 16-row calls (each call takes the
+    kernel and the shared-memory plan of its own row count)."""
     cfg = syngen.CONFIGS["a3b_r1"]
     s = Stack(cfg, n_layers=1, max_rows=16)
     try:
@@ -409,7 +409,7 @@ def test_a_later_handle_with_a_smaller_plan_keeps_earlier_handles_working(stack)
 
 
 def test_wide_rounds_rows_are_independent_bitwise(stack):
-    """Rounds of >= 8 rows run on the tensor cores; there too a row's output is
+    """Rounds of >= 13 rows run on the tensor cores; there too a row's output is
     bit-identical at any position and whatever other rows share the round."""
     cfg = stack.cfg
     xa = stack.rows(0, 16, 0.5)
