@@ -202,6 +202,7 @@ def run_reference(args):
     cfg = syngen.CONFIGS["a3b_r1"]
     L = args.layers or cfg.layers
     times, byts = [], 0
+    core, host, prev = pin_one_core()
     for step in range(args.warmup + args.steps):
         l = (step // cfg.top_k) % L
         j = step % cfg.top_k
@@ -216,16 +217,19 @@ def run_reference(args):
         if step >= args.warmup:
             times.append(dt)
             byts += cfg.expert_bytes + cfg.router_bytes + cfg.hidden * 6
+    unpin(prev)
     t = sum(times)
     gbs = byts / t / 1e9
     sample = (f"{len(times)} steps; each = routing of one 1-row layer + the FFN of one of its "
-              f"routed experts (layers 0..{L - 1} cycling), oracle only, one host core")
+              f"routed experts (layers 0..{L - 1} cycling), oracle only, one of {host} host cores"
+              + (" (pinned)" if core is not None else ""))
     line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / len(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded counter-based generator)",
             "config": workload_config(cfg, 1, L),
-            "cpu_baseline": {"value": gbs, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": gbs, "unit": UNIT, "cores": 1, "host_cores": host, "pinned_core": core,
+                             "kind": "oracle", "sample": sample},
             "e2e": {"value": gbs, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
