@@ -317,8 +317,7 @@ struct Tables {
 // quarters of the row by four threads; the k experts of rank < k are the picks (the
 // same set and order as select_row), and a ballot over the experts in id order gives
 // each pick its union index (the union is the k picks, ascending).  T.w[j] receives
-// pick j's logit; softmax_one turns it into the weight.  This CTA's unit range is the
-// even split of the k I units.
+// pick j's logit; softmax_one turns it into the weight.
 __device__ __forceinline__ bool route_one_ok(const RoundArgs& a) {
   return a.R == 1 && a.tail_rank == 0 && a.E <= 128 && a.E >= 32 && (a.E & (a.E - 1)) == 0;
 }
@@ -327,15 +326,10 @@ __device__ __forceinline__ int ranks_before_u(unsigned kj, int j, unsigned ki, i
   return (kj > ki || (kj == ki && j < i)) ? 1 : 0;
 }
 
-__device__ void route_one(const RoundArgs& a, const Tables& T, unsigned* s_key, int* s_cnt, int* s_wc, int layer,
-                          int upe, int* s_range) {
+__device__ void route_one(const RoundArgs& a, const Tables& T, unsigned* s_key, int* s_cnt, int* s_wc,
+                          int layer) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, E = a.E, k = a.k;
   const int lgE = __ffs(E) - 1, QE = E >> 2;
-  if (tid == 0) {
-    const unsigned N = (unsigned)k * (unsigned)upe, G = gridDim.x, c = blockIdx.x;
-    s_range[0] = (int)((c * N) / G);
-    s_range[1] = (int)(((c + 1) * N) / G);
-  }
   unsigned ki = 0;
   if (tid < E) {
     ki = order_key(__ldcg(a.logits + tid));
@@ -513,8 +507,7 @@ __device__ int route_phase(const RoundArgs& a, const Tables& T, unsigned* s_mask
   // route_one's scratch: keys [E] (16-byte aligned: read as uint4), counts [4 E], warp sums
   unsigned* s_key = reinterpret_cast<unsigned*>((reinterpret_cast<uintptr_t>(s_rank + E) + 15) & ~(uintptr_t)15);
   if (route_one_ok(a)) {  // (weights: softmax_one, by the caller)
-    route_one(a, T, s_key, reinterpret_cast<int*>(s_key + NT), reinterpret_cast<int*>(s_key + 5 * NT), layer, upe,
-              s_range);
+    route_one(a, T, s_key, reinterpret_cast<int*>(s_key + NT), reinterpret_cast<int*>(s_key + 5 * NT), layer);
     return k;
   }
   // rows: top-k, renormalised weights, row bits of each picked expert
@@ -1542,11 +1535,13 @@ __global__ void __launch_bounds__(NT, 1) k_split(const __grid_constant__ RoundAr
 // parts are added in a fixed order, so a row's result does not depend on the rows it
 // shares the round with.
 
-// Rounds of at least this many rows use the tensor-core kernel.  Measured on the
-// 128-expert / top-8 layer (40-layer rounds, draft rows at sigma 0.5): 12 rows on the
-// split kernel 58.0 us per layer against 64.9 us for 13 rows on the tensor cores; with
-// 14 to 16 near-duplicate copy-span rows the tensor cores take 39 to 40 us against 65 to
-// 72 us on the split kernel.
+// Rounds of at least this many rows use the tensor-core kernel.  The choice is made
+// before the routing is known.  Measured on the 128-expert / top-8 layer (40-layer
+// rounds): with 14 to 16 near-duplicate copy-span rows (about 11 experts per layer) the
+// tensor cores take 39 to 40 us per layer against 65 to 72 us on the split kernel; with
+// draft rows at sigma 0.5 (about 27 experts) the split kernel is faster from 13 rows on
+// (56 against 65 us at 13 rows, 65 against 69 us at 16) and below 13 rows for every row
+// mix measured.  The switch favours the copy-span rounds.
 constexpr int kMmaRows = 13;
 constexpr int kKPartsGu = 8;  // K parts of a gate/up tile (hidden blocks)
 static_assert(NW % kKPartsGu == 0, "a tile's K parts run in one round");
@@ -1590,14 +1585,12 @@ struct WidePlan {
   size_t ring;
   size_t dn, dn_slot;  // the down pass's staging: offset in the ring, bytes of one unit slot
   int gu_cap;     // units per gate/up chunk
-  int max_orows;  // output rows per CTA (ceil(H / grid))
   bool ok;
 };
 
 __host__ __device__ inline WidePlan wide_plan(int H, int I, int E, int R, int k, int grid) {
   WidePlan p{};
   const size_t unit = (size_t)H + (size_t)H / 8;
-  p.max_orows = (H + grid - 1) / grid;
   const size_t tables = up128((size_t)E * 4) + up128((size_t)(E + 1) * 4) + 5 * up128((size_t)R * k * 4) +
                         up128((size_t)E * 4) + 128 + up128(kGuSlots * 12 + 64) + 256;
   const size_t fixed = tables + kMmaScratch;
