@@ -168,6 +168,34 @@ int moe_round(moe_handle* h, const moe_layer_w* layers, int32_t L, const uint16_
               int32_t rows, float* out, int32_t* stats, void* ws, size_t ws_bytes, int use_graph,
               void* stream);
 
+/* moe_round with the rows in and the outputs out in HOST memory: on `stream`, in this
+ * order, the copy of x_host into x_dev, the round (moe_round on x_dev / out_dev), and the
+ * copy of out_dev into out_host -- what a caller holding the draft rows on the host runs
+ * once per verify round (AlphaInfer docs §2: the round's rows are ingress into one
+ * captured round).
+ *   - dims: the dims the handle was created with (the copies move L * rows * hidden
+ *     elements); call with the handle's device current.
+ *   - x_host [L][rows][H] bf16 bits and out_host [L][rows][H] fp32, host memory owned
+ *     by the caller.  Page-locked memory makes both copies asynchronous; with pageable
+ *     memory the calling thread waits for each copy.
+ *   - x_dev [L][rows][H] and out_dev [L][rows][H]: the caller's device staging buffers
+ *     (16-byte aligned); they are moe_round's x_bf16 and out, so with use_graph the
+ *     round replays while they, ws and stream stay the same.
+ *   - stats, ws, ws_bytes, use_graph, stream: as for moe_round.
+ *   - sync != 0: returns after the stream has finished, with out_host written, and with
+ *     moe_last_device_status's answer (MOE_ETIMEOUT or MOE_EINVAL if the kernel raised
+ *     one, the status word cleared).  sync == 0: returns once the work is enqueued; the
+ *     caller synchronizes the stream before reading out_host and may read the status
+ *     with moe_last_device_status.
+ * Allocates nothing.  Nothing is enqueued when an argument is wrong: MOE_EINVAL for a
+ * NULL handle, dims, layers or buffer, L outside [1, 128] or rows outside [1, max_rows],
+ * moe_create's code for dims it would reject.  Otherwise moe_round's codes for the
+ * round (the rows' copy is then already enqueued) and MOE_ECUDA if a copy fails. */
+int moe_round_host(moe_handle* h, const moe_dims* dims, const moe_layer_w* layers, int32_t L,
+                   const uint16_t* x_host, int32_t rows, float* out_host, uint16_t* x_dev,
+                   float* out_dev, int32_t* stats, void* ws, size_t ws_bytes, int use_graph, int sync,
+                   void* stream);
+
 /* Prefill-width layer: steps 1-5 for many token rows at once (a prompt's tokens), the
  * infero README's MoE prefill path ("Beyond plain text decode": a counting sort of the
  * (token, expert) picks by expert, then one GEMM per expert).  Same weights, routing

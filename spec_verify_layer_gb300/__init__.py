@@ -21,7 +21,7 @@ MOE_GATEUP, MOE_DOWN = 0, 1
 # exported symbols declared in include/moe_verify.h
 ABI_SYMBOLS = (
     "moe_create", "moe_destroy", "moe_workspace_bytes", "moe_packed_bytes", "moe_pack_q4",
-    "moe_route", "moe_decode_layer", "moe_round", "moe_last_device_status",
+    "moe_route", "moe_decode_layer", "moe_round", "moe_round_host", "moe_last_device_status",
     "moe_last_launch_count", "moe_set_wait_limit_ns", "moe_set_tail_skip", "moe_profile",
     "moe_profile_read",
     "moe_profile_phases", "moe_decode_layer_noalloc", "moe_prefill_workspace_bytes",
@@ -78,6 +78,9 @@ _lib.moe_decode_layer.restype = ctypes.c_int
 _lib.moe_round.argtypes = [_vp, ctypes.POINTER(moe_layer_w), _i32, _vp, _i32, _vp, _vp, _vp, _sz,
                            ctypes.c_int, _vp]
 _lib.moe_round.restype = ctypes.c_int
+_lib.moe_round_host.argtypes = [_vp, ctypes.POINTER(moe_dims), ctypes.POINTER(moe_layer_w), _i32, _vp, _i32, _vp,
+                                _vp, _vp, _vp, _vp, _sz, ctypes.c_int, ctypes.c_int, _vp]
+_lib.moe_round_host.restype = ctypes.c_int
 _lib.moe_last_device_status.argtypes = [_vp, _vp]
 _lib.moe_last_device_status.restype = ctypes.c_int
 _lib.moe_last_launch_count.argtypes = [_vp]
@@ -181,6 +184,17 @@ def moe_round(handle: int, layers, x_bf16: int, rows: int, out: int, stats: int,
     arr = (moe_layer_w * len(layers))(*layers)
     _check(_lib.moe_round(handle, arr, len(layers), x_bf16, int(rows), out, stats, ws, int(ws_bytes),
                           1 if use_graph else 0, stream), "moe_round")
+
+
+def moe_round_host(handle: int, dims: moe_dims, layers, x_host: int, rows: int, out_host: int, x_dev: int,
+                   out_dev: int, stats: int, ws: int, ws_bytes: int, use_graph: bool, sync: bool,
+                   stream: int) -> None:
+    """moe_round with the rows read from host memory and the outputs written to host memory
+    (x_host, out_host: host addresses; x_dev, out_dev: the device staging buffers)."""
+    arr = (moe_layer_w * len(layers))(*layers)
+    _check(_lib.moe_round_host(handle, ctypes.byref(dims), arr, len(layers), x_host, int(rows), out_host, x_dev,
+                               out_dev, stats, ws, int(ws_bytes), 1 if use_graph else 0, 1 if sync else 0, stream),
+           "moe_round_host")
 
 
 def moe_last_device_status(handle: int, stream: int) -> int:

@@ -1,6 +1,9 @@
-// Host-side parts of the verify-round MoE library that need no GPU: dimension
-// checks, workspace and packed sizes, the int4 block packer, error strings.
+// Host-side parts of the verify-round MoE library: dimension checks, workspace and
+// packed sizes, the int4 block packer, error strings (none of these touch a GPU), and
+// the host-buffer round (stream-ordered copies around moe_round).
 #include <cstring>
+
+#include <cuda_runtime.h>
 
 #include "moe_internal.h"
 
@@ -135,6 +138,30 @@ int moe_pack_q4(const moe_dims* dims, int which, int32_t n_experts, const int8_t
     return MOE_OK;
   }
   return MOE_EINVAL;
+}
+
+int moe_round_host(moe_handle* h, const moe_dims* dims, const moe_layer_w* layers, int32_t L,
+                   const uint16_t* x_host, int32_t rows, float* out_host, uint16_t* x_dev,
+                   float* out_dev, int32_t* stats, void* ws, size_t ws_bytes, int use_graph, int sync,
+                   void* stream) {
+  // every argument check comes before the first copy is enqueued
+  if (!h || !dims || !layers || !x_host || !out_host || !x_dev || !out_dev) return MOE_EINVAL;
+  const int rc = check_dims(dims);
+  if (rc != MOE_OK) return rc;
+  if (L < 1 || L > kMaxLayers || rows < 1 || rows > dims->max_rows) return MOE_EINVAL;
+  const size_t n = (size_t)L * (size_t)rows * (size_t)dims->hidden;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(x_dev, x_host, n * sizeof(uint16_t), cudaMemcpyHostToDevice, st) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ECUDA;
+  }
+  const int r = moe_round(h, layers, L, x_dev, rows, out_dev, stats, ws, ws_bytes, use_graph, stream);
+  if (r != MOE_OK) return r;
+  if (cudaMemcpyAsync(out_host, out_dev, n * sizeof(float), cudaMemcpyDeviceToHost, st) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ECUDA;
+  }
+  return sync ? moe_last_device_status(h, stream) : MOE_OK;
 }
 
 const char* moe_strerror(int code) {

@@ -95,6 +95,11 @@ def test_null_handle_calls_are_rejected():
     assert lib.moe_decode_layer(None, ctypes.byref(w), 256, 1, 256, 256, 1 << 20, None) == mv.MOE_EINVAL
     assert lib.moe_route(None, ctypes.byref(w), 256, 1, None, None, None, None, 256, 1 << 20, None) == mv.MOE_EINVAL
     assert lib.moe_last_device_status(None, None) == mv.MOE_EINVAL
+    # the host-buffer round checks its handle before it reads anything else or copies
+    xh, oh = np.zeros(256, np.uint16), np.zeros(256, np.float32)
+    ws_list = (mv.moe_layer_w * 1)(w)
+    assert lib.moe_round_host(None, ctypes.byref(dims()), ws_list, 1, xh.ctypes.data, 1, oh.ctypes.data, None,
+                              None, None, None, 0, 0, 1, None) == mv.MOE_EINVAL
     assert lib.moe_last_launch_count(None) == 0
 
 

@@ -107,3 +107,53 @@ def test_a3b_round_tail_skip(a3b_stack):
     assert (skipped <= plain).all() and skipped.sum() < plain.sum()
     _, again = round_case(a3b_stack, cfg, cfg.rows, cfg.row_sigma, True, check_layers=())
     np.testing.assert_array_equal(again, plain)
+
+
+def test_host_buffer_round_equals_device_round(a3b_stack):
+    """moe_round_host (rows copied in from host memory, outputs copied back to host memory,
+    on the caller's stream around the round) gives moe_round's outputs bitwise: from
+    page-locked buffers with the graph and eagerly, and from pageable numpy buffers with
+    the work only enqueued (sync = 0).  Wrong arguments are rejected with nothing enqueued."""
+    cfg = syngen.CONFIGS["a3b_r4"]
+    R, H, L = cfg.rows, cfg.hidden, len(a3b_stack.layers)
+    want, want_stats = round_case(a3b_stack, cfg, R, cfg.row_sigma, True, check_layers=())
+    xs = np.stack([syngen.rows(cfg, l, R, cfg.row_sigma) for l in range(L)])
+    dev = a3b_stack.device
+    x_dev = torch.empty((L, R, H), dtype=torch.int16, device=dev)
+    out_dev = torch.full((L, R, H), float("nan"), device=dev)
+    stats = torch.full((L,), -1, dtype=torch.int32, device=dev)
+    ws = a3b_stack.ws(R)
+    wl = [ly.w for ly in a3b_stack.layers]
+    s = torch.cuda.Stream(dev)
+
+    def call(x_host, out_host, rows=R, layers=wl, use_graph=True, sync=True):
+        mv.moe_round_host(a3b_stack.handle, a3b_stack.dims, layers, x_host, rows, out_host, x_dev.data_ptr(),
+                          out_dev.data_ptr(), stats.data_ptr(), ws.data_ptr(), ws.numel(), use_graph, sync,
+                          s.cuda_stream)
+
+    xh = torch.from_numpy(xs.view(np.int16)).pin_memory()
+    oh = torch.empty((L, R, H), dtype=torch.float32).pin_memory()
+    for use_graph in (True, True, False):  # capture, replay, eager
+        oh.fill_(float("nan"))
+        call(xh.data_ptr(), oh.data_ptr(), use_graph=use_graph)
+        np.testing.assert_array_equal(oh.numpy(), want)
+    np.testing.assert_array_equal(stats.cpu().numpy(), want_stats)
+
+    xp = np.ascontiguousarray(xs.view(np.uint16))
+    op = np.full((L, R, H), np.nan, dtype=np.float32)
+    call(xp.ctypes.data, op.ctypes.data, sync=False)
+    s.synchronize()
+    np.testing.assert_array_equal(op, want)
+    assert mv.moe_last_device_status(a3b_stack.handle, s.cuda_stream) == mv.MOE_OK
+
+    out_dev.fill_(float("nan"))
+    torch.cuda.synchronize(dev)
+    for kw in (dict(rows=0), dict(rows=a3b_stack.dims.max_rows + 1), dict(layers=[])):
+        with pytest.raises(mv.MoeError) as ei:
+            call(xh.data_ptr(), oh.data_ptr(), **kw)
+        assert ei.value.code == mv.MOE_EINVAL
+    with pytest.raises(mv.MoeError) as ei:
+        call(None, oh.data_ptr())
+    assert ei.value.code == mv.MOE_EINVAL
+    s.synchronize()
+    assert torch.isnan(out_dev).all()  # no round ran
