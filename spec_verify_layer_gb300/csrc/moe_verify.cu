@@ -718,8 +718,11 @@ struct Op24 {
 };
 
 // sum over the block of (n - 8) v for a 16-bit operand.
+// E_0 + 256 E_1 (16 times the block's sum, |.| < 2^28) is formed exactly in int32 and
+// converted once: the same float as an fma of the two converted digit sums, which rounds
+// the same exact integer once.  The correction terms seed the first digit's sum.
 __device__ __forceinline__ float bdot16(const NibBytes& n, const Op16& x) {
-  int a0 = 0, c0 = 0, a1 = 0, c1 = 0;
+  int a0 = 0, c0 = x.k0 + 256 * x.k1, a1 = 0, c1 = 0;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     a0 = dp4a_uu(n.lo[i], x.d[i], a0);
@@ -727,13 +730,15 @@ __device__ __forceinline__ float bdot16(const NibBytes& n, const Op16& x) {
     a1 = dp4a_us(n.lo[i], x.d[8 + i], a1);
     c1 = dp4a_us(n.hi[i], x.d[12 + i], c1);
   }
-  const int e0 = 16 * a0 + c0 + x.k0, e1 = 16 * a1 + c1 + x.k1;
-  return __fmul_rn(__fmaf_rn((float)e1, 256.f, (float)e0), x.f);
+  const int e = 16 * a0 + c0 + 256 * (16 * a1 + c1);
+  return __fmul_rn(__int2float_rn(e), x.f);
 }
 
 // sum over the block of (n - 8) v for a 24-bit operand.
+// E_0 + 256 E_1 (|.| < 2^29) exactly in int32 and converted once, as in bdot16; E_2
+// joins in fp32.
 __device__ __forceinline__ float bdot24(const NibBytes& n, const Op24& h) {
-  int a0 = 0, c0 = 0, a1 = 0, c1 = 0, a2 = 0, c2 = 0;
+  int a0 = 0, c0 = h.k0 + 256 * h.k1, a1 = 0, c1 = 0, a2 = 0, c2 = h.k2;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     a0 = dp4a_uu(n.lo[i], h.d[i], a0);
@@ -743,8 +748,8 @@ __device__ __forceinline__ float bdot24(const NibBytes& n, const Op24& h) {
     a2 = dp4a_us(n.lo[i], h.d[16 + i], a2);
     c2 = dp4a_us(n.hi[i], h.d[20 + i], c2);
   }
-  const int e0 = 16 * a0 + c0 + h.k0, e1 = 16 * a1 + c1 + h.k1, e2 = 16 * a2 + c2 + h.k2;
-  return __fmul_rn(__fmaf_rn((float)e2, 65536.f, __fmaf_rn((float)e1, 256.f, (float)e0)), h.f);
+  const int e01 = 16 * a0 + c0 + 256 * (16 * a1 + c1), e2 = 16 * a2 + c2;
+  return __fmul_rn(__fmaf_rn((float)e2, 65536.f, __int2float_rn(e01)), h.f);
 }
 
 // Byte j of digit word q for element e of a block: q = (d * 2 + (e & 1)) * 4 + (e >> 3),
